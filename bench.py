@@ -1,0 +1,416 @@
+"""Throughput of the routed-expert layer (route + forward) on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the whole layer -- k3moe_route then k3moe_forward -- over one
+batch of T synthetic tokens whose weights and activations are already resident in
+HBM.  The 129 MB L2 is flushed between steps (a 512 MiB buffer is written outside
+the timed events).  value = tokens processed by all ranks / the slowest rank's summed
+step time (CUDA events on the launching stream).  e2e times the same step through the
+C ABI from pinned host memory: H2D of x, route, forward, D2H of out.
+
+With N > 1 (torchrun, one process per GPU) every rank runs an independent replica of
+the layer: the path has no exchange step on one GPU, so there is no collective in the
+data path; a barrier and a max-reduction of the timings bracket the run.
+
+--impl reference times the CPU oracle (oracle/, fp64 C) on this host's cores on a
+bounded sample of the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s at T=1 and T=4096 on 1 GB300; % of HBM/tensor roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="decode_t1")
+    p.add_argument("--impl", default="k3moe", choices=["k3moe", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-budget-s", type=float, default=15.0)
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def layer_bytes_flops(w, distinct_experts: int):
+    """Algorithmic bytes and FLOPs of one layer call: the distinct routed experts
+    touched (packed MXFP4), the shared experts (bf16), the router (bf16), x in (bf16)
+    and out (f32).  FLOPs: 2*3*f*d per (token, expert) for k routed + S shared experts,
+    plus 2*E*d per token for the router."""
+    Be = w.expert_bytes
+    shared = w.S * 3 * w.f * w.d * 2
+    router = w.E * w.d * 2
+    act = w.T * w.d * 2 + w.T * w.d * 4
+    byts = distinct_experts * Be + shared + router + act
+    flops = w.T * (2 * 3 * w.f * w.d * (w.k + w.S) + 2 * w.E * w.d)
+    return byts, flops
+
+
+def kernel_bytes(name: str, w, distinct_experts: int):
+    """Algorithmic bytes of one launch of a forward kernel (the bytes it must move):
+    gemv_gateup: W1, W3 of the distinct experts (packed) and of the shared experts
+    (bf16), x in, h out (f32); gemv_down: W2 likewise, h in, y out (f32); any other
+    kernel is charged the whole layer's bytes."""
+    rows = w.T * w.k + w.S * w.T
+    if name == "gemv_gateup":
+        return (distinct_experts * 2 * w.f * w.d * 17 // 32 + w.S * 2 * w.f * w.d * 2
+                + w.T * w.d * 2 + rows * w.f * 4)
+    if name == "gemv_down":
+        return (distinct_experts * w.d * w.f * 17 // 32 + w.S * w.d * w.f * 2
+                + rows * w.f * 4 + rows * w.d * 4)
+    return layer_bytes_flops(w, distinct_experts)[0]
+
+
+def workload_from(spec: str):
+    """NAME or NAME:key=value,key=value (integer overrides, e.g. decode_t1:E=64)."""
+    import k3moe_inputs as ki
+    name, _, over = spec.partition(":")
+    w = ki.WORKLOADS[name]
+    if over:
+        kw = {}
+        for item in over.split(","):
+            k, v = item.split("=")
+            kw[k.strip()] = int(v)
+        w = w.with_(name=spec, **kw)
+    return w
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as fh:
+            pk = json.load(fh)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "sparse_moe_expert_k3moe_gb300", "csrc", "*"))):
+        with open(p, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    """dram read+write bytes per launch from a committed ncu summary, or None when
+    absent or taken on a different kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            tr = json.load(fh)
+        ent = tr[workload][kernel]
+        if ent.get("csrc_hash") != csrc_hash():
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if not self.rows:
+            return None
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            for i, n in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(self.rows), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def time_oracle(w, budget_s: float):
+    """Route + forward of the oracle on this host's cores over a bounded sample of
+    the workload's tokens; returns (tokens/s, tokens timed, threads, seconds)."""
+    import numpy as np
+    import k3moe_inputs as ki
+    import oracle
+    c = oracle.cfg(**w.config_kwargs())
+    x = ki.make_x(w)
+    Wr = ki.make_router(w)
+    bias = ki.make_bias(w)
+    shared = ki.make_shared(w) if w.S else None
+    experts = {}
+    done, spent = 0, 0.0
+    order = list(range(w.T))
+    batch = max(1, min(w.T, oracle.num_threads()))
+    while done < w.T and spent < budget_s:
+        rows = order[done:done + batch]
+        xs = np.ascontiguousarray(x[rows])
+        idx, wt, _ = oracle.route(c, xs, Wr, bias)        # untimed draw of the needed experts
+        for e in set(idx.ravel().tolist()) - set(experts):
+            experts[e] = ki.make_expert(w, e)
+        t0 = time.perf_counter()
+        idx, wt, _ = oracle.route(c, xs, Wr, bias)
+        oracle.forward(c, xs, idx, wt, experts, shared)
+        spent += time.perf_counter() - t0
+        done += len(rows)
+        if len(experts) > 256:
+            experts.clear()
+    return done / spent, done, oracle.num_threads(), spent
+
+
+def reference_arm(args):
+    import k3moe_inputs as ki
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = workload_from(args.workload)
+    import oracle
+    oracle.build()
+    per_step = max(2.0, args.cpu_budget_s / max(1, args.steps))
+    for _ in range(args.warmup):
+        time_oracle(w.with_(T=1), 0.1)
+    tot_tok, tot_s = 0, 0.0
+    threads = oracle.num_threads()
+    for _ in range(args.steps):
+        tps, n, threads, s = time_oracle(w, per_step)
+        tot_tok += n
+        tot_s += s
+    value = tot_tok / tot_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * tot_s / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "top_k": w.k,
+                   "n_shared": w.S},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{tot_tok} tokens of {w.name} over {args.steps} steps "
+                                   f"(each step <= {per_step:.1f} s of oracle work)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def gpu_arm(args):
+    import numpy as np
+    import torch
+    import k3moe_inputs as ki
+    from k3moe_inputs.device import build_layer
+    import sparse_moe_expert_k3moe_gb300 as k3
+    from sparse_moe_expert_k3moe_gb300 import build as kbuild
+
+    rank, world, local = dist_env()
+    kbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def allmax(v: float) -> float:
+        if world == 1:
+            return v
+        import torch.distributed as dist
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    w = workload_from(args.workload)
+    layer = build_layer(w, device=dev)
+    x = torch.from_numpy(ki.make_x(w).view(np.int16)).to(dev)
+    out = torch.empty((w.T, w.d), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        layer.route(x, stream)
+        layer.forward(x, out, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    rc, code = k3.k3moe_device_status(layer.ws)
+    if rc != 0:
+        raise RuntimeError(f"device status {code:#x} after warm-up")
+    distinct = int(torch.unique(layer.idx[: w.T]).numel())
+
+    # ---- timed region: K steps, L2 flushed between steps outside the events
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    n0 = k3.k3moe_launch_count()
+    for i in range(args.steps):
+        flush.fill_(i & 255)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    launches = k3.k3moe_launch_count() - n0
+    clk = clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    ms = allmax(ms)
+    value = world * w.T * args.steps / (ms / 1000.0)
+
+    # ---- per-kernel durations (separate pass, same work, library-side CUDA events)
+    k3.k3moe_timing_reset()
+    k3.k3moe_timing_enable(True)
+    for i in range(args.steps):
+        flush.fill_(i & 255)
+        step()
+    torch.cuda.synchronize(dev)
+    k3.k3moe_timing_enable(False)
+    kt = k3.k3moe_timing_read()
+    top = max(kt.items(), key=lambda kv: kv[1][1])
+    top_name, (top_n, top_ms) = top
+    hbm, bf16, bf16_sus, src = peaks()
+    per_launch_s = top_ms / top_n / 1000.0
+    alg = kernel_bytes(top_name, w, distinct)
+    achieved = alg / per_launch_s / 1e9
+    step_bytes, step_flops = layer_bytes_flops(w, distinct)
+    step_s = ms / args.steps / 1000.0
+
+    # ---- end to end through the C ABI from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(ki.make_x(w).view(np.int16)).pin_memory()
+        oh = torch.empty((w.T, w.d), dtype=torch.float32).pin_memory()
+        xd = torch.empty_like(x)
+        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps + 2):
+            flush.fill_(i & 255)
+            if i >= 2:
+                ee[i - 2][0].record(stream)
+            xd.copy_(xh, non_blocking=True)
+            layer.route(xd, stream)
+            layer.forward(xd, out, stream)
+            oh.copy_(out, non_blocking=True)
+            if i >= 2:
+                ee[i - 2][1].record(stream)
+        torch.cuda.synchronize(dev)
+        ems = allmax(sum(a.elapsed_time(b) for a, b in ee))
+        e2e = {"value": world * w.T * args.steps / (ems / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
+               "d2h_bytes_per_step": int(oh.numel() * oh.element_size())}
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, n, threads, s = time_oracle(w, args.cpu_budget_s)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} of {w.T} tokens of {w.name}, route + forward, {s:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "top_k": w.k,
+                       "n_shared": w.S, "weights": "routed MXFP4 (E2M1 + E8M0/32), shared bf16",
+                       "l2": "512 MiB buffer written between timed steps",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "kernel": top_name, "achieved": achieved, "peak": hbm,
+                         "unit": "GB/s", "frac": achieved / hbm, "peak_source": src,
+                         "traffic": traffic_for(top_name, w.name),
+                         "alg_bytes_per_launch": alg, "launch_ms": per_launch_s * 1e3},
+            "step_roofline": {"bytes": step_bytes, "flops": step_flops,
+                              "distinct_experts": distinct,
+                              "hbm_frac": step_bytes / step_s / 1e9 / hbm,
+                              "tensor_frac": step_flops / step_s / 1e12 / bf16_sus},
+            "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kt.items()},
+            "gpu_launches": launches,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+/*
+ * k3moe.h -- C ABI of the routed-expert layer of a Kimi-K3-style latent MoE,
+ * GPU library (libk3moe.so) for GB300 / sm_103a.
+ *
+ * What the layer computes (kimi-k3-in-c README, Part II, section 9 "Picking 16
+ * experts of 896", with the MXFP4 format of section 4): for each token x (the
+ * expert latent, width d, bf16)
+ *   1. score every routed expert e: sc[e] = sigmoid(x . Wr[e]) in float;
+ *      ch[e] = sc[e] + bias[e] steers selection only;
+ *   2. take the top_k experts by ch, ties to the lower index; their weights
+ *      are the unbiased sc, renormalised to sum 1 when renorm and the sum is
+ *      positive, then multiplied by routed_scale;
+ *   3. run each chosen expert's gated FFN straight from packed MXFP4 weights:
+ *      y = W2 . SiTU(W1 x, W3 x), SiTU(g, u) = b1 tanh(g/b1) sigmoid(g) *
+ *      b2 tanh(u/b2) (the sigmoid reads the uncapped gate);
+ *   4. add the n_shared dense bf16 experts (same form) with weight one;
+ *   5. out = sum_j weight_j * y_j + sum_s y_s, float.
+ *
+ * Conventions for every call:
+ *   - Every array pointer is DEVICE memory owned by the caller.  The library
+ *     allocates and frees nothing on these calls; scratch comes from the
+ *     caller's workspace (see k3moe_workspace_bytes).
+ *   - bf16 arrays are passed as uint16_t bit patterns; all arrays are dense,
+ *     row-major, with the shapes stated at each argument.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  A host-side validation error returns before any
+ *     launch, so nothing is half-written.
+ *   - Device-side anomalies (an expert index outside [0, E), offsets or a
+ *     permutation that do not describe the routing, an MXFP4 scale byte of
+ *     255) are never skipped silently: they set bits of the device status
+ *     word in the workspace, read with k3moe_device_status.  The kernels
+ *     bounds-check every index they derive from such inputs before using it.
+ *   - The library waits on nothing it cannot bound: no kernel spins.
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *k3moe_stream;
+
+/* Layer configuration.  Every field is required; k3moe_validate_config
+ * rejects an unset (zero) or out-of-range field instead of defaulting it
+ * (kimi-k3-in-c README, Part II, section 2 "The config reader that refuses to
+ * guess").  The K3 values are d=3584, f=3072, n_experts=896, top_k=16,
+ * n_shared=2, group=32, situ_b1=4.0, situ_b2=25.0, renorm=1,
+ * routed_scale=1.0 (same section's K3Cfg struct). */
+typedef struct k3moe_config {
+    int32_t d;            /* expert latent width; multiple of 128, <= 8192 */
+    int32_t f;            /* expert FFN width; multiple of 128, <= 8192 */
+    int32_t n_experts;    /* routed experts E, 1..1024 */
+    int32_t top_k;        /* experts per token k, 1..16 and <= E */
+    int32_t n_shared;     /* dense shared experts S, 0..8 */
+    int32_t group;        /* MXFP4 block size; must be 32 */
+    float situ_b1;        /* SiTU gate cap, finite and > 0 */
+    float situ_b2;        /* SiTU linear cap, finite and > 0 */
+    int32_t renorm;       /* 0 or 1 */
+    float routed_scale;   /* finite */
+} k3moe_config;
+
+typedef enum k3moe_status {
+    K3MOE_OK = 0,
+    K3MOE_EINVAL = 1,      /* a config field or argument is invalid */
+    K3MOE_ESHAPE = 2,      /* T or a size outside what the call supports */
+    K3MOE_EALIGN = 3,      /* a pointer lacks the alignment the call needs */
+    K3MOE_EWORKSPACE = 4,  /* workspace NULL, misaligned or too small */
+    K3MOE_ECUDA = 5,       /* a CUDA runtime call failed (launch or copy) */
+    K3MOE_EDEVICE = 6,     /* the device status word reports an error */
+    K3MOE_ETIMEOUT = 7     /* a bounded device-side wait gave up */
+} k3moe_status;
+
+/* Bits of the device status word. */
+#define K3MOE_DEV_BAD_INDEX   0x1  /* routing index outside [0, E) */
+#define K3MOE_DEV_BAD_OFFSETS 0x2  /* offsets/perm inconsistent with idx */
+#define K3MOE_DEV_NAN_SCALE   0x4  /* warning: an E8M0 scale byte of 255 (read as 0) */
+#define K3MOE_DEV_TIMEOUT     0x8  /* a bounded wait gave up */
+#define K3MOE_DEV_ERROR_MASK  (K3MOE_DEV_BAD_INDEX | K3MOE_DEV_BAD_OFFSETS | K3MOE_DEV_TIMEOUT)
+
+/* Human-readable name of a status code (static string). */
+const char *k3moe_strerror(k3moe_status s);
+
+/* K3MOE_OK when every field of *cfg is in range, else K3MOE_EINVAL or
+ * K3MOE_ESHAPE.  Pure host function. */
+k3moe_status k3moe_validate_config(const k3moe_config *cfg);
+
+/* Bytes of the packed routed-expert table for cfg->n_experts experts:
+ * E * 3 * f * d * 17/32 (half a byte per weight plus one scale byte per 32),
+ * 17,547,264 bytes per expert at the K3 shape (kimi-k3-in-c README, Part II,
+ * "The problem: a model that does not fit").  0 for an invalid config. */
+size_t k3moe_packed_bytes(const k3moe_config *cfg);
+
+/* Workspace bytes that k3moe_route and k3moe_forward need for any
+ * 0 <= T <= T_max.  The workspace is one caller-owned device buffer,
+ * 256-byte aligned, shared by both calls; its first 256 bytes hold the
+ * device status word.  Zero-fill it once before first use (the status word
+ * must start at zero); the calls keep everything else consistent. */
+k3moe_status k3moe_workspace_bytes(const k3moe_config *cfg, int32_t T_max, size_t *bytes);
+
+/* Relayout experts [expert_lo, expert_lo + n_in) from the checkpoint's MXFP4
+ * layout into the library's packed table (a relayout of codes and scales,
+ * not a quantiser: kimi-k3-in-c README, Part II, section 4).  Inputs, per
+ * tensor with a leading expert axis of n_in:
+ *   w1_packed, w3_packed [n_in][f][d/2]  (low nibble = even column)
+ *   w1_scale,  w3_scale  [n_in][f][d/32] (E8M0 bytes)
+ *   w2_packed            [n_in][d][f/2]
+ *   w2_scale             [n_in][d][f/32]
+ * The *_packed pointers must be 16-byte aligned.  `table` (table_bytes >=
+ * k3moe_packed_bytes) must be 256-byte aligned.  Scale bytes of 255 raise
+ * K3MOE_DEV_NAN_SCALE in `ws` when ws is not NULL (ws as for k3moe_route). */
+k3moe_status k3moe_pack_mxfp4(const k3moe_config *cfg, int32_t expert_lo, int32_t n_in,
+                              const uint8_t *w1_packed, const uint8_t *w1_scale,
+                              const uint8_t *w3_packed, const uint8_t *w3_scale,
+                              const uint8_t *w2_packed, const uint8_t *w2_scale,
+                              void *table, size_t table_bytes, void *ws,
+                              k3moe_stream stream);
+
+/* Inverse of k3moe_pack_mxfp4: writes experts [expert_lo, expert_lo + n_out)
+ * of `table` back in checkpoint layout (same shapes and alignment rules). */
+k3moe_status k3moe_unpack_mxfp4(const k3moe_config *cfg, int32_t expert_lo, int32_t n_out,
+                                const void *table, size_t table_bytes,
+                                uint8_t *w1_packed, uint8_t *w1_scale,
+                                uint8_t *w3_packed, uint8_t *w3_scale,
+                                uint8_t *w2_packed, uint8_t *w2_scale,
+                                k3moe_stream stream);
+
+/* Router (kimi-k3-in-c README, Part II, section 9, the k3_router listing):
+ * logits x . Wr^T accumulated in fp32, sc = 1/(1+expf(-logit)) and
+ * ch = sc + bias in float, top_k by ch with ties to the lower index, weights
+ * from sc (renormalised when renorm and their float sum is > 0, summed in
+ * rank order, then times routed_scale).  Then the token -> expert map:
+ *   x        [T][d] bf16         w_router [E][d] bf16     bias [E] f32 or NULL
+ *   idx      [T][k] int32  out: chosen experts, ch descending, ties index ascending
+ *   weight   [T][k] f32    out: routing weights in the same order
+ *   offsets  [E+1] int32   out: exclusive prefix sum of per-expert slot counts
+ *   perm     [T*k] int32   out: flat slot ids t*k+j grouped by expert, ascending
+ *                               within each expert (a stable counting sort)
+ * T may be 0 (offsets all zero).  ws per k3moe_workspace_bytes(T_max >= T). */
+k3moe_status k3moe_route(const k3moe_config *cfg, int32_t T, const uint16_t *x,
+                         const uint16_t *w_router, const float *bias,
+                         int32_t *idx, float *weight, int32_t *offsets, int32_t *perm,
+                         void *ws, size_t ws_bytes, k3moe_stream stream);
+
+/* Expert part of the layer for given routing (as k3moe_route writes it, or
+ * any routing with the same conventions), kimi-k3-in-c README, Part II,
+ * section 9, the k3_moe listing's expert loop and shared-expert step:
+ *   out[t] = sum_j weight[t][j] * W2_e . SiTU(W1_e x_t, W3_e x_t),  e = idx[t][j]
+ *          + sum_s Sh2_s . SiTU(Sh1_s x_t, Sh3_s x_t)
+ *   x            [T][d] bf16
+ *   idx, weight  [T][k] int32 / f32;  offsets [E+1], perm [T*k] int32
+ *   expert_table packed routed experts (k3moe_pack_mxfp4), table_bytes of it
+ *   sh_w1, sh_w3 [S][f][d] bf16;  sh_w2 [S][d][f] bf16 (NULL when S == 0);
+ *                16-byte aligned
+ *   out          [T][d] f32, written (not accumulated)
+ * Intermediates stay in fp32 for small T (decode) and round the SiTU output
+ * to bf16 for the tensor-core path at large T (prefill).  ws per
+ * k3moe_workspace_bytes(T_max >= T). */
+k3moe_status k3moe_forward(const k3moe_config *cfg, int32_t T, const uint16_t *x,
+                           const int32_t *idx, const float *weight,
+                           const int32_t *offsets, const int32_t *perm,
+                           const void *expert_table, size_t table_bytes,
+                           const uint16_t *sh_w1, const uint16_t *sh_w3, const uint16_t *sh_w2,
+                           float *out, void *ws, size_t ws_bytes, k3moe_stream stream);
+
+/* Synchronises `stream`, returns the device status word of `ws` in *code,
+ * and clears it.  Returns K3MOE_EDEVICE when an error bit is set, K3MOE_OK
+ * otherwise (the NAN_SCALE warning alone is OK). */
+k3moe_status k3moe_device_status(void *ws, k3moe_stream stream, int32_t *code);
+
+/* Number of GPU kernels this library has launched in this process (all
+ * calls, all devices); for launch accounting in benchmarks. */
+int64_t k3moe_launch_count(void);
+
+/* Per-kernel timing: when enabled, every launch is bracketed by CUDA events
+ * on its stream.  k3moe_timing_read fills up to `cap` entries with kernel
+ * names, launch counts and summed milliseconds (it synchronises the events)
+ * and returns the number of kernel kinds; k3moe_timing_reset clears them.
+ * Timing is off by default and costs nothing then. */
+void k3moe_timing_enable(int32_t on);
+int32_t k3moe_timing_read(const char **names, int64_t *launches, double *ms, int32_t cap);
+void k3moe_timing_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K3MOE_H */

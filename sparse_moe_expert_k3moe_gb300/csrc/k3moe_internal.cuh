@@ -1,0 +1,157 @@
+// k3moe_internal.cuh -- shared definitions of the GPU library (not public).
+//
+// Packed routed-expert table (the layout k3moe_pack_mxfp4 writes):
+//   expert e starts at e * expert_bytes; inside it
+//   - gate/up block: for row block rb in [0, f/128), for K tile kt in [0, d/128):
+//       [W1 tile (rb, kt)][W3 tile (rb, kt)]
+//   - down block:    for row block rb in [0, d/128), for K tile kt in [0, f/128):
+//       [W2 tile (rb, kt)]
+//   A tile is 128 rows x 128 columns of one matrix, 8704 bytes:
+//   - bytes [0, 8192): 16-byte chunks; chunk (c, r) at (c * 128 + r) * 16 holds the
+//     32 codes of row r, columns kt*128 + 32c .. +31, in checkpoint byte order
+//     (low nibble = even column).  Chunk-major order makes consecutive rows
+//     consecutive 16-byte words: conflict-free shared-memory reads when a thread
+//     owns a row.
+//   - bytes [8192, 8704): E8M0 scale of (row r, group c) at 8192 + r * 4 + c.
+//   Tiles are contiguous, so one bulk copy moves a tile, and a gate/up K step
+//   (both matrices) is one 17408-byte copy.  Bytes per expert = 3*f*d*17/32.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#ifdef __CUDACC__
+#include <cuda_fp16.h>
+#endif
+
+#include "../../include/k3moe.h"
+
+namespace k3moe {
+
+constexpr int kTileRows = 128;
+constexpr int kTileK = 128;
+constexpr int kGroup = 32;
+constexpr int kTileNibbleBytes = kTileRows * kTileK / 2;            // 8192
+constexpr int kTileScaleBytes = kTileRows * kTileK / kGroup;        // 512
+constexpr int kTileBytes = kTileNibbleBytes + kTileScaleBytes;      // 8704
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 16;
+constexpr int kMaxShared = 8;
+constexpr int kMaxWidth = 8192;
+constexpr int kChunkTokens = 64;      // tokens per top-k block; its slots form one chunk
+
+__host__ __device__ inline size_t gateup_block_bytes(int d, int f)
+{
+    return (size_t)(f / kTileRows) * (size_t)(d / kTileK) * 2 * kTileBytes;
+}
+__host__ __device__ inline size_t down_block_bytes(int d, int f)
+{
+    return (size_t)(d / kTileRows) * (size_t)(f / kTileK) * kTileBytes;
+}
+__host__ __device__ inline size_t expert_bytes(int d, int f)
+{
+    return gateup_block_bytes(d, f) + down_block_bytes(d, f);
+}
+
+// Device status word and abort flag live in the first 256 bytes of the workspace.
+struct StatusBlock {
+    int32_t status;   // K3MOE_DEV_* bits
+    int32_t abort;    // nonzero: inputs failed validation, later kernels skip work
+    int32_t pad[62];
+};
+
+// Workspace regions (byte offsets), sized for one call's T.
+struct WsLayout {
+    size_t status;
+    size_t sc, ch;               // router scores [T][E] f32
+    size_t chunk_counts;         // [n_chunks][E] int32
+    size_t chunk_base;           // [n_chunks][E] int32
+    size_t local_rank;           // [T*k] int32
+    size_t active;               // [E + 1] int32: active expert ids, then the count
+    size_t inv;                  // [T*k] int32: slot -> position in perm
+    size_t h;                    // [(T*k + S*T)][f] f32 (decode path)
+    size_t ys;                   // [(T*k + S*T)][d] f32 (decode path)
+    size_t total;
+    int n_chunks;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline WsLayout ws_layout(const k3moe_config &c, int T)
+{
+    WsLayout L{};
+    const size_t E = (size_t)c.n_experts, k = (size_t)c.top_k, S = (size_t)c.n_shared;
+    const size_t slots = (size_t)T * k;
+    L.n_chunks = (T + kChunkTokens - 1) / kChunkTokens;
+    size_t o = 0;
+    L.status = o; o += 256;
+    L.sc = o; o = align256(o + (size_t)T * E * 4);
+    L.ch = o; o = align256(o + (size_t)T * E * 4);
+    L.chunk_counts = o; o = align256(o + (size_t)L.n_chunks * E * 4);
+    L.chunk_base = o; o = align256(o + (size_t)L.n_chunks * E * 4);
+    L.local_rank = o; o = align256(o + slots * 4);
+    L.active = o; o = align256(o + (E + 1) * 4);
+    L.inv = o; o = align256(o + slots * 4);
+    const size_t rows = slots + S * (size_t)T;
+    L.h = o; o = align256(o + rows * (size_t)c.f * 4);
+    L.ys = o; o = align256(o + rows * (size_t)c.d * 4);
+    L.total = o;
+    return L;
+}
+
+// ----------------------------------------------------------------------------------- launch bookkeeping
+// Every launch goes through these so launches can be counted and, on request, timed.
+void timing_begin(const char *name, cudaStream_t s);
+void timing_end(const char *name, cudaStream_t s);
+void count_launch();
+
+// Host launchers implemented in the kernel files.
+cudaError_t launch_pack(const k3moe_config &c, int expert_lo, int n, const uint8_t *w1p,
+                        const uint8_t *w1s, const uint8_t *w3p, const uint8_t *w3s,
+                        const uint8_t *w2p, const uint8_t *w2s, uint8_t *table,
+                        int32_t *status, cudaStream_t s);
+cudaError_t launch_unpack(const k3moe_config &c, int expert_lo, int n, const uint8_t *table,
+                          uint8_t *w1p, uint8_t *w1s, uint8_t *w3p, uint8_t *w3s,
+                          uint8_t *w2p, uint8_t *w2s, cudaStream_t s);
+cudaError_t launch_route(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
+                         const float *bias, int32_t *idx, float *weight, int32_t *offsets,
+                         int32_t *perm, uint8_t *ws, const WsLayout &L, cudaStream_t s);
+cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
+                                const int32_t *idx, const float *weight, const int32_t *offsets,
+                                const int32_t *perm, const uint8_t *table, const uint16_t *sh_w1,
+                                const uint16_t *sh_w3, const uint16_t *sh_w2, float *out,
+                                uint8_t *ws, const WsLayout &L, cudaStream_t s);
+
+// ----------------------------------------------------------------------------------- device helpers
+#ifdef __CUDACC__
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// E8M0 byte -> 2^(b-127) as float; byte 0 is the subnormal 2^-127; 255 -> 0.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b)
+{
+    b &= 255u;
+    if (b == 255u) return 0.0f;
+    if (b == 0u) return __uint_as_float(0x00400000u);
+    return __uint_as_float(b << 23);
+}
+
+// Two E2M1 codes (one packed byte: low nibble = even element) -> two exact floats.
+// The conversion instruction decodes the pair to f16x2; E2M1 values are exact in f16.
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte_in_low_bits)
+{
+    uint32_t h;
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+        : "=r"(h) : "r"(byte_in_low_bits));
+    __half2 hh = *reinterpret_cast<__half2 *>(&h);
+    return __half22float2(hh);
+}
+
+__device__ __forceinline__ void set_status(int32_t *status, int32_t bits)
+{
+    atomicOr(status, bits);
+}
+
+#endif
+
+}  // namespace k3moe

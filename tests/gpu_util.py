@@ -1,0 +1,49 @@
+"""Helpers shared by the GPU parity tests: device setup, oracle comparisons, tolerances."""
+import numpy as np
+
+import k3moe_inputs as ki
+import oracle
+
+# Output tolerance: relative L2 <= 5e-3 and max |err| <= 2e-2 * max |ref| (the layer's
+# acceptance bar).  Indices, offsets and permutations are compared bit-exactly.
+REL_L2 = 5e-3
+MAX_REL = 2e-2
+NEAR_TIE = 1e-6
+
+
+def out_errors(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rel_l2 = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
+    max_rel = np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-300)
+    return rel_l2, max_rel
+
+
+def assert_out_close(got, ref, what=""):
+    rel_l2, max_rel = out_errors(got, ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    assert rel_l2 <= REL_L2 and max_rel <= MAX_REL, f"{what}: rel_l2={rel_l2:.3e} max_rel={max_rel:.3e}"
+    return rel_l2, max_rel
+
+
+def ocfg(w):
+    return oracle.cfg(**w.config_kwargs())
+
+
+def oracle_experts(w, ids):
+    return {int(e): ki.make_expert(w, int(e)) for e in sorted(set(int(v) for v in ids))}
+
+
+def oracle_forward_rows(w, x, idx, weight, rows, batch=8):
+    """Oracle output for the given token rows (routing taken as given)."""
+    shared = ki.make_shared(w) if w.S else None
+    c = ocfg(w)
+    outs = []
+    rows = list(rows)
+    for i in range(0, len(rows), batch):
+        r = rows[i:i + batch]
+        xi = np.ascontiguousarray(x[r])
+        ii = np.ascontiguousarray(idx[r])
+        wi = np.ascontiguousarray(weight[r])
+        outs.append(oracle.forward(c, xi, ii, wi, oracle_experts(w, ii.ravel()), shared))
+    return np.concatenate(outs, axis=0)

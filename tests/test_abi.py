@@ -1,0 +1,116 @@
+"""The C ABI library: it loads, exports every entry point include/k3moe.h declares,
+and its host-side validation rejects bad input before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_moe_expert_k3moe_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "k3moe.h")
+
+
+@pytest.fixture(scope="module")
+def k3():
+    kbuild.build()
+    import sparse_moe_expert_k3moe_gb300 as k3
+    k3.lib()
+    return k3
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(k3moe_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("k3moe_route", "k3moe_forward", "k3moe_pack_mxfp4", "k3moe_workspace_bytes",
+                 "k3moe_device_status", "k3moe_packed_bytes"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(k3):
+    raw = ctypes.CDLL(k3.library_path())
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def k3_cfg(k3, **over):
+    kw = dict(d=3584, f=3072, n_experts=896, top_k=16, n_shared=2)
+    kw.update(over)
+    return k3.k3moe_config(**kw)
+
+
+def test_config_validation(k3):
+    assert k3.k3moe_validate_config(k3_cfg(k3)) == 0
+    assert k3.k3moe_validate_config(k3_cfg(k3, d=256, f=128, n_experts=32, top_k=4, n_shared=1)) == 0
+    bad = [dict(d=0), dict(f=0), dict(n_experts=0), dict(top_k=0), dict(group=16),
+           dict(situ_b1=0.0), dict(situ_b2=-1.0), dict(situ_b1=float("inf")), dict(renorm=2),
+           dict(routed_scale=float("nan")), dict(top_k=900), dict(n_shared=-1)]
+    for b in bad:
+        assert k3.k3moe_validate_config(k3_cfg(k3, **b)) == 1, b
+    for b in (dict(d=3600), dict(f=100), dict(n_experts=2048), dict(top_k=17, n_experts=64),
+              dict(n_shared=9)):
+        assert k3.k3moe_validate_config(k3_cfg(k3, **b)) == 2, b
+
+
+def test_sizes(k3):
+    cfg = k3_cfg(k3)
+    assert k3.k3moe_packed_bytes(cfg) == 896 * 17547264
+    tiny = k3_cfg(k3, d=256, f=128, n_experts=32, top_k=4, n_shared=1)
+    assert k3.k3moe_packed_bytes(tiny) == 32 * 52224
+    w1 = k3.k3moe_workspace_bytes(cfg, 1)
+    w64 = k3.k3moe_workspace_bytes(cfg, 64)
+    assert 256 < w1 < w64
+    assert k3.k3moe_workspace_bytes(cfg, 0) >= 256
+    with pytest.raises(k3.K3MoEError):
+        k3.k3moe_workspace_bytes(cfg, -1)
+    assert k3.k3moe_packed_bytes(k3_cfg(k3, d=0)) == 0
+
+
+def test_host_validation_rejects_before_launch(k3):
+    L = k3.lib()
+    cfg = k3_cfg(k3)
+    vp = ctypes.c_void_p
+    A = 0x10000000  # fake, 256-aligned addresses: never dereferenced on the host
+    big = 1 << 40
+    # no workspace
+    rc = L.k3moe_route(ctypes.byref(cfg), 4, vp(A), vp(A), None, vp(A), vp(A), vp(A), vp(A),
+                       None, 0, None)
+    assert rc == 4
+    # misaligned activations
+    rc = L.k3moe_route(ctypes.byref(cfg), 4, vp(A + 2), vp(A), None, vp(A), vp(A), vp(A), vp(A),
+                       vp(A), big, None)
+    assert rc == 3
+    # workspace too small
+    rc = L.k3moe_route(ctypes.byref(cfg), 4, vp(A), vp(A), None, vp(A), vp(A), vp(A), vp(A),
+                       vp(A), 1024, None)
+    assert rc == 4
+    # T out of range, missing outputs, bad config
+    assert L.k3moe_route(ctypes.byref(cfg), -1, vp(A), vp(A), None, vp(A), vp(A), vp(A), vp(A),
+                         vp(A), big, None) == 2
+    assert L.k3moe_route(ctypes.byref(cfg), 4, vp(A), vp(A), None, None, vp(A), vp(A), vp(A),
+                         vp(A), big, None) == 1
+    bad = k3_cfg(k3, top_k=0)
+    assert L.k3moe_route(ctypes.byref(bad), 4, vp(A), vp(A), None, vp(A), vp(A), vp(A), vp(A),
+                         vp(A), big, None) == 1
+    # forward: table too small, missing shared experts, misaligned table
+    tb = k3.k3moe_packed_bytes(cfg)
+    args = lambda table, tbytes, sh: (ctypes.byref(cfg), 4, vp(A), vp(A), vp(A), vp(A), vp(A),
+                                      vp(table), tbytes, sh, sh, sh, vp(A), vp(A), big, None)
+    assert L.k3moe_forward(*args(A, tb - 1, vp(A))) == 2
+    assert L.k3moe_forward(*args(A, tb, None)) == 1
+    assert L.k3moe_forward(*args(A + 16, tb, vp(A))) == 3
+    # T = 0 is a no-op for forward
+    assert L.k3moe_forward(ctypes.byref(cfg), 0, None, None, None, None, None, None, 0, None,
+                           None, None, None, None, 0, None) == 0
+    # pack: range outside the table, misaligned source
+    assert L.k3moe_pack_mxfp4(ctypes.byref(cfg), 890, 10, *([vp(A)] * 6), vp(A), big, None,
+                              None) == 2
+    assert L.k3moe_pack_mxfp4(ctypes.byref(cfg), 0, 1, vp(A + 8), *([vp(A)] * 5), vp(A), big,
+                              None, None) == 3
+    assert k3.k3moe_strerror(4).startswith("workspace")

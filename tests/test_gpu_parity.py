@@ -1,0 +1,305 @@
+"""GPU parity: every call of the C ABI against the CPU oracle on the same seeded inputs.
+
+Router: indices, offsets and perm bit-exact (tokens whose oracle gap between the
+k-th and (k+1)-th selection score is below 1e-6 are counted and excluded);
+weights to float rounding.  Outputs: rel-L2 <= 5e-3 and max error <= 2e-2 max|ref|.
+"""
+import numpy as np
+import pytest
+
+import k3moe_inputs as ki
+import oracle
+from gpu_util import (NEAR_TIE, assert_out_close, ocfg, oracle_experts, oracle_forward_rows)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def k3():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_moe_expert_k3moe_gb300 import build as kbuild
+    kbuild.build()
+    import sparse_moe_expert_k3moe_gb300 as k3
+    return k3
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def dev16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def host(t):
+    return t.cpu().numpy()
+
+
+def run_route(k3, layer, x_dev, T):
+    layer.route(x_dev)
+    torch.cuda.synchronize()
+    k = layer.cfg.top_k
+    return (host(layer.idx[:T]), host(layer.weight[:T]), host(layer.offsets),
+            host(layer.perm[:T * k]))
+
+
+def check_route(w, x, gidx, gw, goff, gperm, bias=None):
+    c = ocfg(w)
+    oidx, ow, gap = oracle.route(c, x, ki.make_router(w), ki.make_bias(w) if bias is None else bias)
+    near = gap < NEAR_TIE
+    far = ~near
+    np.testing.assert_array_equal(gidx[far], oidx[far])
+    np.testing.assert_allclose(gw[far], ow[far], rtol=2e-6, atol=1e-7)
+    # the map is a pure function of idx: exact against the oracle's counting sort of the GPU's idx
+    ooff, operm = oracle.perm(gidx, w.E)
+    np.testing.assert_array_equal(goff, ooff)
+    np.testing.assert_array_equal(gperm, operm)
+    if not near.any():
+        ooff2, operm2 = oracle.perm(oidx, w.E)
+        np.testing.assert_array_equal(goff, ooff2)
+        np.testing.assert_array_equal(gperm, operm2)
+    # selections of near-tie tokens still valid: k distinct experts in range
+    for t in np.nonzero(near)[0]:
+        assert len(set(gidx[t].tolist())) == w.k and gidx[t].min() >= 0 and gidx[t].max() < w.E
+    print(f"[{w.name}] tokens={w.T} near_ties={int(near.sum())} exact_tie_tokens="
+          f"{int((gap == 0).sum())}")
+    return oidx, ow, gap
+
+
+# ----------------------------------------------------------------------------- pack / unpack
+
+def test_pack_roundtrip_every_code_and_scale(k3):
+    w = ki.Workload("rt", T=1, d=256, f=128, E=3, k=1, S=0, exp_lo=-8, exp_hi=-4, seed=5)
+    cfg = k3.k3moe_config(**w.config_kwargs())
+    blk = ki.make_experts_block(w, 0, w.E)
+    # every scale byte 0..255 and every code at every nibble position appears
+    for name in ("w1_scale", "w3_scale", "w2_scale"):
+        flat = blk[name].reshape(-1)
+        flat[:] = np.arange(flat.size) % 256
+    blk["w1_packed"].reshape(-1)[:256] = np.arange(256, dtype=np.uint8)
+    table = torch.empty(k3.k3moe_packed_bytes(cfg), dtype=torch.uint8, device="cuda")
+    d_in = {kname: dev(v) for kname, v in blk.items()}
+    ws = torch.zeros(k3.k3moe_workspace_bytes(cfg, 1), dtype=torch.uint8, device="cuda")
+    k3.k3moe_pack_mxfp4(cfg, 0, w.E, *(d_in[n] for n in ki.EXPERT_TENSORS), table, ws=ws)
+    d_out = {kname: torch.zeros_like(v) for kname, v in d_in.items()}
+    k3.k3moe_unpack_mxfp4(cfg, 0, w.E, table, *(d_out[n] for n in ki.EXPERT_TENSORS))
+    torch.cuda.synchronize()
+    for n in ki.EXPERT_TENSORS:
+        np.testing.assert_array_equal(host(d_out[n]), blk[n])
+    rc, code = k3.k3moe_device_status(ws)
+    assert rc == 0 and code & k3.DEV_NAN_SCALE      # byte 255 present: warning, not error
+    # the table is a pure relayout: same multiset of bytes
+    assert table.numel() == w.E * w.expert_bytes
+
+
+def test_pack_roundtrip_full_shape(k3):
+    w = ki.WORKLOADS["decode_t1"]
+    cfg = k3.k3moe_config(**w.config_kwargs())
+    cfg_small = k3.k3moe_config(**w.with_(E=3).config_kwargs())
+    blk = ki.make_experts_block(w, 10, 3)
+    table = torch.empty(k3.k3moe_packed_bytes(cfg_small), dtype=torch.uint8, device="cuda")
+    d_in = {kname: dev(v) for kname, v in blk.items()}
+    k3.k3moe_pack_mxfp4(cfg_small, 0, 3, *(d_in[n] for n in ki.EXPERT_TENSORS), table)
+    d_out = {kname: torch.zeros_like(v) for kname, v in d_in.items()}
+    k3.k3moe_unpack_mxfp4(cfg_small, 0, 3, table, *(d_out[n] for n in ki.EXPERT_TENSORS))
+    torch.cuda.synchronize()
+    for n in ki.EXPERT_TENSORS:
+        np.testing.assert_array_equal(host(d_out[n]), blk[n])
+    assert k3.k3moe_packed_bytes(cfg) == 896 * 17547264
+
+
+# ----------------------------------------------------------------------------- small layers, all outputs
+
+MICRO = ki.Workload("micro", T=37, d=384, f=256, E=16, k=4, S=2, exp_lo=-7, exp_hi=-3, seed=40)
+SMALL_CASES = [
+    ki.WORKLOADS["tiny"],
+    MICRO,
+    MICRO.with_(name="micro_bias", zipf_bias=True, seed=41, T=70),        # two chunks
+    MICRO.with_(name="micro_k_eq_E", E=8, k=8, seed=42, T=9),
+    MICRO.with_(name="micro_one_expert", E=1, k=1, seed=43, T=5),
+    MICRO.with_(name="micro_no_renorm", renorm=0, routed_scale=0.75, seed=44),
+    MICRO.with_(name="micro_no_shared", S=0, seed=45, T=130),             # ragged third chunk
+    MICRO.with_(name="micro_wide", d=1024, f=640, E=40, k=16, S=1, seed=46, T=23),
+]
+
+
+@pytest.mark.parametrize("w", SMALL_CASES, ids=lambda w: w.name)
+def test_small_layer_parity(k3, w):
+    from k3moe_inputs.device import build_layer
+    layer = build_layer(w)
+    x = ki.make_x(w)
+    xd = dev16(x)
+    gidx, gw, goff, gperm = run_route(k3, layer, xd, w.T)
+    check_route(w, x, gidx, gw, goff, gperm)
+    out = torch.empty((w.T, w.d), dtype=torch.float32, device="cuda")
+    layer.forward(xd, out)
+    rc, code = k3.k3moe_device_status(layer.ws)
+    assert rc == 0 and code == 0
+    ref = oracle.forward(ocfg(w), x, gidx, gw, oracle_experts(w, range(w.E)),
+                         ki.make_shared(w) if w.S else None)
+    rel, mx = assert_out_close(host(out), ref, w.name)
+    print(f"[{w.name}] rel_l2={rel:.2e} max_rel={mx:.2e}")
+
+
+def test_forward_with_injected_oracle_routing(k3):
+    """Routing computed by the oracle, uploaded, consumed by k3moe_forward."""
+    from k3moe_inputs.device import build_layer
+    w = MICRO.with_(name="inject", seed=47)
+    layer = build_layer(w)
+    x = ki.make_x(w)
+    oidx, ow, _ = oracle.route(ocfg(w), x, ki.make_router(w), ki.make_bias(w))
+    ooff, operm = oracle.perm(oidx, w.E)
+    routing = (dev(oidx), dev(ow), dev(ooff), dev(operm))
+    out = torch.empty((w.T, w.d), dtype=torch.float32, device="cuda")
+    layer.forward(dev16(x), out, routing=routing)
+    ref = oracle.forward(ocfg(w), x, oidx, ow, oracle_experts(w, range(w.E)), ki.make_shared(w))
+    assert_out_close(host(out), ref, "injected")
+
+
+def test_zero_tokens(k3):
+    from k3moe_inputs.device import build_layer
+    w = ki.WORKLOADS["tiny"]
+    layer = build_layer(w)
+    layer.offsets.fill_(7)
+    x0 = torch.empty((0, w.d), dtype=torch.int16, device="cuda")
+    layer.route(x0)
+    torch.cuda.synchronize()
+    assert host(layer.offsets).tolist() == [0] * (w.E + 1)
+    out = torch.empty((0, w.d), dtype=torch.float32, device="cuda")
+    layer.forward(x0, out)
+
+
+def test_bad_routing_sets_status_without_fault(k3):
+    from k3moe_inputs.device import build_layer
+    w = ki.WORKLOADS["tiny"]
+    layer = build_layer(w)
+    x = dev16(ki.make_x(w))
+    out = torch.empty((w.T, w.d), dtype=torch.float32, device="cuda")
+    layer.route(x)
+    good = (layer.idx.clone(), layer.weight.clone(), layer.offsets.clone(), layer.perm.clone())
+    # offsets that do not describe the routing
+    off = good[2].clone()
+    off[3] += 1
+    layer.forward(x, out, routing=(good[0], good[1], off, good[3]))
+    rc, code = k3.k3moe_device_status(layer.ws)
+    assert rc == 6 and code & k3.DEV_BAD_OFFSETS
+    assert torch.all(out == 0)
+    # an expert index out of range
+    bad_idx = good[0].clone()
+    bad_idx[0, 0] = w.E + 5
+    layer.forward(x, out, routing=(bad_idx, good[1], good[2], good[3]))
+    rc, code = k3.k3moe_device_status(layer.ws)
+    assert rc == 6 and code & k3.DEV_BAD_INDEX
+    # the next valid call is clean again
+    layer.forward(x, out, routing=good)
+    rc, code = k3.k3moe_device_status(layer.ws)
+    assert rc == 0 and code == 0
+    assert torch.isfinite(out).all() and out.abs().max() > 0
+
+
+def test_nan_scale_groups_read_as_zero(k3):
+    w = MICRO.with_(name="nanscale", seed=48, T=11)
+    cfg = k3.k3moe_config(**w.config_kwargs())
+    from sparse_moe_expert_k3moe_gb300 import MoELayer
+    from k3moe_inputs.device import to_device_u16
+    layer = MoELayer(cfg, w.T)
+    layer.w_router = to_device_u16(ki.make_router(w), "cuda")
+    sh = ki.make_shared(w)
+    layer.sh_w1, layer.sh_w3, layer.sh_w2 = (to_device_u16(sh[m], "cuda") for m in ("w1", "w3", "w2"))
+    experts = {e: ki.make_expert(w, e) for e in range(w.E)}
+    for e in range(w.E):
+        for name in ("w1_scale", "w3_scale", "w2_scale"):
+            experts[e][name][::7, 1] = 255
+    blk = {n: np.stack([experts[e][n] for e in range(w.E)]) for n in ki.EXPERT_TENSORS}
+    layer.pack_experts(0, w.E, *(dev(blk[n]) for n in ki.EXPERT_TENSORS))
+    x = ki.make_x(w)
+    xd = dev16(x)
+    layer.route(xd)
+    out = torch.empty((w.T, w.d), dtype=torch.float32, device="cuda")
+    layer.forward(xd, out)
+    rc, code = k3.k3moe_device_status(layer.ws)
+    assert rc == 0 and code == k3.DEV_NAN_SCALE
+    gidx, gw = host(layer.idx), host(layer.weight)
+    ref = oracle.forward(ocfg(w), x, gidx, gw, experts, sh)
+    assert_out_close(host(out), ref, "nan-scale")
+
+
+def test_launch_count_and_timing(k3):
+    from k3moe_inputs.device import build_layer
+    w = ki.WORKLOADS["tiny"]
+    layer = build_layer(w)
+    x = dev16(ki.make_x(w))
+    out = torch.empty((w.T, w.d), dtype=torch.float32, device="cuda")
+    n0 = k3.k3moe_launch_count()
+    k3.k3moe_timing_reset()
+    k3.k3moe_timing_enable(True)
+    layer(x, out)
+    torch.cuda.synchronize()
+    k3.k3moe_timing_enable(False)
+    tm = k3.k3moe_timing_read()
+    assert k3.k3moe_launch_count() > n0
+    assert sum(v[0] for v in tm.values()) == k3.k3moe_launch_count() - n0
+    assert all(v[1] >= 0 for v in tm.values())
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+
+@pytest.fixture(scope="module")
+def full_layers():
+    cache = {}
+    yield cache
+    cache.clear()
+
+
+def full_layer(cache, name):
+    from k3moe_inputs.device import build_layer
+    if name not in cache:
+        cache.clear()
+        torch.cuda.empty_cache()
+        w = ki.WORKLOADS[name]
+        cache[name] = (w, build_layer(w))
+    return cache[name]
+
+
+@pytest.mark.parametrize("name", ["decode_t1", "decode_t64", "prefill_t4096", "prefill_t16k"])
+def test_full_route_parity(k3, full_layers, name):
+    w, layer = full_layer(full_layers, name)
+    x = ki.make_x(w)
+    gidx, gw, goff, gperm = run_route(k3, layer, dev16(x), w.T)
+    check_route(w, x, gidx, gw, goff, gperm)
+    rc, code = k3.k3moe_device_status(layer.ws)
+    assert rc == 0 and code == 0
+
+
+@pytest.mark.parametrize("name,rows", [
+    ("decode_t1", None),                   # every output
+    ("decode_t64", None),                  # every output
+    ("prefill_t4096", "sample"),
+    ("prefill_t16k", "sample"),
+])
+def test_full_forward_parity(k3, full_layers, name, rows):
+    w, layer = full_layer(full_layers, name)
+    x = ki.make_x(w)
+    xd = dev16(x)
+    layer.route(xd)
+    out = torch.empty((w.T, w.d), dtype=torch.float32, device="cuda")
+    layer.forward(xd, out)
+    rc, code = k3.k3moe_device_status(layer.ws)
+    assert rc == 0 and code == 0
+    gidx, gw = host(layer.idx[:w.T]), host(layer.weight[:w.T])
+    if rows is None:
+        sel = list(range(w.T))
+    else:
+        # first, last, outlier rows, and tokens routed to the most loaded expert
+        counts = np.bincount(gidx.ravel(), minlength=w.E)
+        hot = int(np.argmax(counts))
+        hot_rows = np.nonzero((gidx == hot).any(axis=1))[0]
+        sel = sorted(set([0, w.T - 1, int(hot_rows[0]), int(hot_rows[-1])]
+                         + [int(r) for r in ki.outlier_rows(w)[:2]]))
+    ref = oracle_forward_rows(w, x, gidx, gw, sel)
+    got = host(out)[sel]
+    rel, mx = assert_out_close(got, ref, name)
+    print(f"[{name}] rows={len(sel)} rel_l2={rel:.2e} max_rel={mx:.2e}")
