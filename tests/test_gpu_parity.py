@@ -46,26 +46,45 @@ def run_route(k3, layer, x_dev, T):
             host(layer.perm[:T * k]))
 
 
-def check_route(w, x, gidx, gw, goff, gperm, bias=None):
+def check_route(w, x, gidx, gw, goff, gperm):
+    """Indices: exact where the oracle's choice is unique to float rounding.  A token is
+    a boundary near-tie when the oracle's k-th and (k+1)-th selection scores differ by
+    less than 1e-6 (its set is rounding-dependent: only validity is checked), and an
+    order near-tie when two adjacent chosen scores do (its set is compared exactly, the
+    order only for consistency).  Offsets depend only on the sets; perm is checked
+    exactly against the oracle's counting sort of the GPU's own indices."""
     c = ocfg(w)
-    oidx, ow, gap = oracle.route(c, x, ki.make_router(w), ki.make_bias(w) if bias is None else bias)
-    near = gap < NEAR_TIE
-    far = ~near
-    np.testing.assert_array_equal(gidx[far], oidx[far])
-    np.testing.assert_allclose(gw[far], ow[far], rtol=2e-6, atol=1e-7)
+    oidx, ow, gap, sc, ch = oracle.route(c, x, ki.make_router(w), ki.make_bias(w),
+                                         want_scores=True)
+    k = w.k
+    och = np.take_along_axis(ch, oidx.astype(np.int64), axis=1)
+    inner = (np.min(och[:, :-1] - och[:, 1:], axis=1) if k > 1
+             else np.full(w.T, np.inf, dtype=np.float32))
+    boundary = gap < NEAR_TIE
+    order = ~boundary & (inner < NEAR_TIE)
+    exact = ~boundary & ~order
+    np.testing.assert_array_equal(gidx[exact], oidx[exact])
+    np.testing.assert_allclose(gw[exact], ow[exact], rtol=2e-6, atol=1e-7)
+    for t in np.nonzero(order)[0]:
+        assert sorted(gidx[t].tolist()) == sorted(oidx[t].tolist())
+        gch = ch[t, gidx[t]]
+        assert np.all(np.diff(gch.astype(np.float64)) <= NEAR_TIE)
+        gmap = dict(zip(gidx[t].tolist(), gw[t].tolist()))
+        omap = dict(zip(oidx[t].tolist(), ow[t].tolist()))
+        for e in omap:
+            assert abs(gmap[e] - omap[e]) <= 2e-6 * abs(omap[e]) + 1e-7
+    for t in np.nonzero(boundary)[0]:
+        assert len(set(gidx[t].tolist())) == k and gidx[t].min() >= 0 and gidx[t].max() < w.E
     # the map is a pure function of idx: exact against the oracle's counting sort of the GPU's idx
     ooff, operm = oracle.perm(gidx, w.E)
     np.testing.assert_array_equal(goff, ooff)
     np.testing.assert_array_equal(gperm, operm)
-    if not near.any():
-        ooff2, operm2 = oracle.perm(oidx, w.E)
-        np.testing.assert_array_equal(goff, ooff2)
-        np.testing.assert_array_equal(gperm, operm2)
-    # selections of near-tie tokens still valid: k distinct experts in range
-    for t in np.nonzero(near)[0]:
-        assert len(set(gidx[t].tolist())) == w.k and gidx[t].min() >= 0 and gidx[t].max() < w.E
-    print(f"[{w.name}] tokens={w.T} near_ties={int(near.sum())} exact_tie_tokens="
-          f"{int((gap == 0).sum())}")
+    if not boundary.any():
+        np.testing.assert_array_equal(goff, oracle.perm(oidx, w.E)[0])
+        if not order.any():
+            np.testing.assert_array_equal(gperm, oracle.perm(oidx, w.E)[1])
+    print(f"[{w.name}] tokens={w.T} boundary_near_ties={int(boundary.sum())} "
+          f"order_near_ties={int(order.sum())} exact_tie_tokens={int((gap == 0).sum())}")
     return oidx, ow, gap
 
 
@@ -98,7 +117,7 @@ def test_pack_roundtrip_every_code_and_scale(k3):
 def test_pack_roundtrip_full_shape(k3):
     w = ki.WORKLOADS["decode_t1"]
     cfg = k3.k3moe_config(**w.config_kwargs())
-    cfg_small = k3.k3moe_config(**w.with_(E=3).config_kwargs())
+    cfg_small = k3.k3moe_config(**w.with_(E=3, k=1).config_kwargs())
     blk = ki.make_experts_block(w, 10, 3)
     table = torch.empty(k3.k3moe_packed_bytes(cfg_small), dtype=torch.uint8, device="cuda")
     d_in = {kname: dev(v) for kname, v in blk.items()}
