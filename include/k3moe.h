@@ -167,6 +167,33 @@ k3moe_status k3moe_forward(const k3moe_config *cfg, int32_t T, const uint16_t *x
                            const uint16_t *sh_w1, const uint16_t *sh_w3, const uint16_t *sh_w2,
                            float *out, void *ws, size_t ws_bytes, k3moe_stream stream);
 
+/* k3moe_forward without a caller workspace, for callers that cannot allocate
+ * device memory: code running inside another framework's execution callback
+ * (a plugin's enqueue, a serving hook) that receives only inputs and outputs,
+ * and real-time or embedded callers with a fixed memory plan that forbids
+ * cudaMalloc on the serving path (it can synchronise the device and can fail
+ * under memory pressure).  The pages have no counterpart: their engine owns
+ * all its buffers.
+ *   Arguments, results and errors as k3moe_forward, minus ws/ws_bytes, plus
+ *   status_out: optional device int32 that receives this call's device
+ *   status word (K3MOE_DEV_* bits); NULL to skip.
+ * Scratch comes from a 32 MiB array inside the library (a file-scope
+ * __device__ object): every GPU that loads the library holds it until the
+ * process exits.  Calls whose k3moe_workspace_bytes(cfg, T) exceeds 32 MiB
+ * return K3MOE_EWORKSPACE without launching (at the K3 shape, T <= 64 fits).
+ * The first call on each device looks up the array's device address with
+ * that device current; make it before any stream capture.  All calls share
+ * the array and it keeps the last call's contents (each call clears its
+ * status block first); calls that overlap on the GPU race on it, so order
+ * them on one stream.  Allocates nothing: no cudaMalloc or cudaFree. */
+k3moe_status k3moe_forward_noalloc(const k3moe_config *cfg, int32_t T, const uint16_t *x,
+                                   const int32_t *idx, const float *weight,
+                                   const int32_t *offsets, const int32_t *perm,
+                                   const void *expert_table, size_t table_bytes,
+                                   const uint16_t *sh_w1, const uint16_t *sh_w3,
+                                   const uint16_t *sh_w2, float *out, int32_t *status_out,
+                                   k3moe_stream stream);
+
 /* Synchronises `stream`, returns the device status word of `ws` in *code,
  * and clears it.  Returns K3MOE_EDEVICE when an error bit is set, K3MOE_OK
  * otherwise (the NAN_SCALE warning alone is OK). */

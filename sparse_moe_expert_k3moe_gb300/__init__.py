@@ -14,7 +14,8 @@ import os
 __all__ = [
     "K3MoEConfig", "K3MOE_OK", "K3MoEError", "lib", "k3moe_config", "k3moe_validate_config",
     "k3moe_packed_bytes", "k3moe_workspace_bytes", "k3moe_pack_mxfp4", "k3moe_unpack_mxfp4",
-    "k3moe_route", "k3moe_forward", "k3moe_device_status", "k3moe_strerror",
+    "k3moe_route", "k3moe_forward", "k3moe_forward_noalloc", "k3moe_device_status",
+    "k3moe_strerror",
     "k3moe_launch_count", "k3moe_timing_enable", "k3moe_timing_read", "k3moe_timing_reset",
     "library_path", "MoELayer",
 ]
@@ -69,6 +70,8 @@ def lib():
             "k3moe_forward": (ctypes.c_int, [cp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp,
                                              vp, sz, vp]),
             "k3moe_device_status": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32)]),
+            "k3moe_forward_noalloc": (ctypes.c_int, [cp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp,
+                                                     vp, vp, vp, vp]),
             "k3moe_launch_count": (i64, []),
             "k3moe_timing_enable": (None, [i32]),
             "k3moe_timing_read": (i32, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i64),
@@ -166,6 +169,17 @@ def k3moe_forward(cfg, T, x, idx, weight, offsets, perm, expert_table, sh_w1, sh
         ctypes.byref(cfg), T, _ptr(x), _ptr(idx), _ptr(weight), _ptr(offsets), _ptr(perm),
         _ptr(expert_table), tb, _ptr(sh_w1), _ptr(sh_w3), _ptr(sh_w2), _ptr(out), _ptr(ws), wb,
         _stream(stream)))
+
+
+def k3moe_forward_noalloc(cfg, T, x, idx, weight, offsets, perm, expert_table, sh_w1, sh_w3,
+                          sh_w2, out, status_out=None, table_bytes=None, stream=None):
+    """k3moe_forward with the library's built-in scratch instead of a workspace, for
+    callers that cannot allocate device memory; see include/k3moe.h."""
+    tb = table_bytes if table_bytes is not None else expert_table.numel() * expert_table.element_size()
+    _check("k3moe_forward_noalloc", lib().k3moe_forward_noalloc(
+        ctypes.byref(cfg), T, _ptr(x), _ptr(idx), _ptr(weight), _ptr(offsets), _ptr(perm),
+        _ptr(expert_table), tb, _ptr(sh_w1), _ptr(sh_w3), _ptr(sh_w2), _ptr(out),
+        _ptr(status_out), _stream(stream)))
 
 
 def k3moe_device_status(ws, stream=None):
