@@ -1,26 +1,39 @@
-// k3moe_gemv.cu -- the expert part of the layer as grouped, streamed mat-vecs:
-// the decode path (few tokens per expert).  kimi-k3-in-c README, Part II,
-// section 4 (MXFP4 mat-vec: per-32 partial sums times the E8M0 scale, nothing
-// dequantised to memory) and section 9 (the k3_moe expert loop: gate = w1,
-// up = w3, SiTU-GLU, down = w2, weighted sum; shared experts unweighted).
+// k3moe_gemv.cu -- the expert part of the layer as grouped, streamed mat-vecs: the
+// decode path (few tokens per expert).  kimi-k3-in-c README, Part II, section 4 (MXFP4
+// mat-vec: per-32 partial sums times the E8M0 scale, nothing dequantised to memory)
+// and section 9 (the k3_moe expert loop: gate = w1, up = w3, SiTU-GLU, down = w2,
+// weighted sum; shared experts unweighted).
 //
 // Kernels, in launch order:
-//   fwd_prep     validates offsets/perm against idx, lists the active experts and
-//                inverts perm (slot -> position); sets the abort flag on bad input;
-//   gemv_gateup  h = SiTU(W1 x, W3 x) for every (active expert, token) and every
-//                (shared expert, token), fp32, rows of h in perm order;
-//   gemv_down    y = W2 h, fp32, same row order;
-//   fwd_combine  out[t] = sum_j w[t][j] y[pos(t,j)] + sum_s y_shared[s][t], in j order.
+//   fwd_prep     validates offsets/perm against idx, lists the active experts, inverts
+//                perm (slot -> position), picks each token's activation scale; sets the
+//                abort flag on bad input;
+//   gemv_gateup  for every (active expert, token) and (shared expert, token): g = W1 x,
+//                u = W3 x; h = SiTU(g, u) when the K range is not split, else the g, u
+//                partial sums of each K part;
+//   gemv_down    y = W2 h (SiTU of the summed parts applied while staging h), fp32,
+//                one partial per K part;
+//   fwd_combine  out[t] = sum_j w[t][j] y[pos(t,j)] + sum_s y_shared[s][t], parts and
+//                terms added in a fixed order.
 //
-// Streaming: a persistent grid; each block owns a contiguous range of work items
-// (64 weight rows of one expert), so consecutive items share the expert and its
-// staged activations.  Weight tiles move global -> shared with bulk async copies
-// (cp.async.bulk for the packed MXFP4 tiles, tensor-map TMA loads for the bf16
-// shared experts) through a 4-stage mbarrier ring; each thread owns one weight
-// row and a K slice, so the activations it needs are the same for the whole
-// warp (shared-memory broadcast) and the packed bytes it reads are consecutive
-// across the warp.  MXFP4 pairs decode with the hardware e2m1x2 conversion.
+// Arithmetic: a streamed mat-vec is bound by HBM bandwidth, so the inner loop must stay
+// cheap.  The tensor-core warp MMA (m16n8k16) serves as the multiply-add engine: each
+// 16x16 MXFP4 sub-tile is decoded with the hardware e2m1x2 -> f16x2 conversion (exact;
+// the table layout hands every lane its fragment bytes in one 8-byte load), multiplied
+// against the activations in f16 and accumulated in fp32, one 32-column group at a time;
+// the group's E8M0 scale multiplies the fp32 group result.  Activations enter f16 with a
+// per-token power-of-two scale that puts the token's largest magnitude in [2^14, 2^15):
+// every bf16 element within 2^31 of that maximum converts exactly.  The SiTU output
+// enters the down projection as an f16 pair hi + lo (about 22 significant bits).  The
+// bf16 shared experts use bf16 MMAs on tensor-map (TMA) tiles, with h as a bf16 pair.
+//
+// Streaming: a persistent grid; each block owns a contiguous range of work items (128
+// weight rows of one expert, over one K part), so consecutive items share the expert
+// and its staged activations.  Weight tiles move global -> shared with bulk async copies
+// through a 4-stage mbarrier ring (cp.async.bulk for packed tiles, cp.async.bulk.tensor
+// for bf16 tiles); warp w of the block owns rows 16w..16w+15 of the item.
 #include <cuda.h>
+#include <cuda_bf16.h>
 
 #include "k3moe_internal.cuh"
 
@@ -28,11 +41,12 @@ namespace k3moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kItemRows = 64;
+constexpr int kItemRows = 128;
 constexpr int kStages = 4;
-constexpr int kStageBytes = 16384;
-constexpr int kNT = 4;                    // tokens per pass
-constexpr uint32_t kWaitLimit = 1u << 26; // bounded mbarrier polls
+constexpr int kNBMax = 2;                          // n-blocks of 8 tokens per pass
+constexpr int kPassTok = 8 * kNBMax;
+constexpr int kSharedK = 32;                       // K per stage for bf16 tiles
+constexpr long long kWaitCycles = 4000000000ll;      // bounded waits: ~2 s at 2 GHz
 
 enum Mode { kGateUp = 0, kDown = 1 };
 
@@ -51,11 +65,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
                  "r"(bytes)
                  : "memory");
 }
-// Returns false when the bounded wait gave up.
+// Returns false when the bounded wait gave up (a clock limit, checked every 32 polls).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
     const uint32_t a = smem_addr(bar);
-    for (uint32_t i = 0; i < kWaitLimit; i++) {
+    const long long t0 = clock64();
+    for (uint32_t i = 0;; i++) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -64,8 +79,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
             : "r"(a), "r"(parity)
             : "memory");
         if (done) return true;
+        if ((i & 31u) == 31u && clock64() - t0 > kWaitCycles) return false;
     }
-    return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
 {
@@ -89,18 +108,73 @@ __device__ __forceinline__ void fence_proxy_async()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Four packed bytes -> four f16x2 (each byte: low nibble -> low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t &h0, uint32_t &h1,
+                                                uint32_t &h2, uint32_t &h3)
+{
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(w));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1, const float (&c)[4])
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+          "f"(c[2]), "f"(c[3]));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1, const float (&c)[4])
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+          "f"(c[2]), "f"(c[3]));
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_addr(p)));
+}
+
 __device__ __forceinline__ float situ(float g, float u, float b1, float b2)
 {
     const float a = b1 * tanhf(g / b1) * (1.0f / (1.0f + expf(-g)));
     return a * (b2 * tanhf(u / b2));
 }
 
+// The four E8M0 scales of one row (one byte per group) as floats.
+__device__ __forceinline__ void row_scales(uint32_t s4, float (&f)[4])
+{
+    const bool special = (__vcmpeq4(s4, 0u) | __vcmpeq4(s4, 0xFFFFFFFFu)) != 0u;
+    if (!special) {
+        f[0] = __uint_as_float((s4 << 23) & 0x7F800000u);
+        f[1] = __uint_as_float((s4 << 15) & 0x7F800000u);
+        f[2] = __uint_as_float((s4 << 7) & 0x7F800000u);
+        f[3] = __uint_as_float((s4 >> 1) & 0x7F800000u);
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; c++) f[c] = e8m0_to_f32(s4 >> (8 * c));
+    }
+}
+
 // -------------------------------------------------------------------------------- prep
 struct PrepArgs {
-    int T, E, k;
+    int T, E, k, d;
+    const uint16_t *x;
     const int32_t *idx, *offsets, *perm;
     int32_t *active;     // [E + 1]
     int32_t *inv;        // [T * k]
+    float *tok_scale;    // [2][T]
     int32_t *status;
     int32_t *abort;
 };
@@ -123,6 +197,24 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
         const int e = a.idx[s];
         if (e < 0 || e >= E) atomicOr(&bad, K3MOE_DEV_BAD_INDEX);
         a.inv[s] = -1;
+    }
+    // per-token activation scale: 2^-u puts max|x_t| in [2^14, 2^15); u in [-113, 113]
+    for (int t = warp; t < a.T; t += 32) {
+        const uint32_t *row = reinterpret_cast<const uint32_t *>(a.x + (size_t)t * a.d);
+        uint32_t m = 0;
+        for (int q = lane; q < a.d / 2; q += 32) {
+            const uint32_t v = row[q];
+            m = max(m, max((v & 0x7FFFu), (v >> 16) & 0x7FFFu));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) {
+            int u = 0;
+            const int eb = (int)(m >> 7);                      // biased exponent of max|x_t|
+            if (m != 0 && eb < 255) u = min(max(eb - 127 - 14, -113), 113);
+            a.tok_scale[t] = __uint_as_float((uint32_t)(127 - u) << 23);
+            a.tok_scale[a.T + t] = __uint_as_float((uint32_t)(127 + u) << 23);
+        }
     }
     __syncthreads();
     const bool offsets_ok = !(bad & K3MOE_DEV_BAD_OFFSETS);
@@ -164,20 +256,25 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
     if (tid == 0) {
         if (bad) atomicOr(a.status, bad);
         *a.abort = bad ? 1 : 0;
+        a.abort[1] = 0;                      // work counters of the two mat-vec kernels
+        a.abort[2] = 0;
     }
 }
 
 // -------------------------------------------------------------------------------- streamed mat-vec
 struct GemvArgs {
     int T, d, f, k, S, E;
+    int p_gu, p_dn;                 // K splits of the gate/up and down items
     float b1, b2;
     const uint16_t *x;
     const int32_t *offsets, *perm, *active;
+    const float *tok_scale;
     const uint8_t *table;
     size_t expert_bytes, gateup_bytes;
-    float *h, *ys;
+    float *gu, *ys;
     const int32_t *abort;
     int32_t *status;
+    int32_t *work;                  // [2] work counters (gate/up, down), zeroed by fwd_prep
 };
 
 struct Unit {         // one expert (routed or shared) with its tokens
@@ -191,8 +288,7 @@ __device__ __forceinline__ Unit unit_of(const GemvArgs &a, int n_active, int u)
     Unit r;
     if (u < n_active) {
         r.shared = 0;
-        r.id = a.active[u];
-        r.id = min(max(r.id, 0), a.E - 1);
+        r.id = min(max(a.active[u], 0), a.E - 1);
         r.tok0 = a.offsets[r.id];
         r.ntok = a.offsets[r.id + 1] - r.tok0;
     } else {
@@ -204,346 +300,488 @@ __device__ __forceinline__ Unit unit_of(const GemvArgs &a, int n_active, int u)
     return r;
 }
 
-// The flat sequence of stages one block streams: items -> token groups -> K tiles.
-struct Cursor {
-    int item, grp, kt;
-};
-
 template <int MODE>
 struct Geo {
-    __host__ __device__ static constexpr int rows_of(int d, int f) { return MODE == kGateUp ? f : d; }
-    __host__ __device__ static constexpr int k_of(int d, int f) { return MODE == kGateUp ? d : f; }
+    // stage bytes: a W1+W3 tile pair (gate/up) or one tile (down); bf16 boxes fit in both
+    // (multiples of 1024 so every stage buffer meets the swizzled-TMA alignment)
+    static constexpr int kStageBytes = MODE == kGateUp ? 2 * kTileBytes : 9 * 1024;
+    // B operand staged in chunks of at most this many 128-column tiles
+    static constexpr int kChunkTilesMax = MODE == kGateUp ? 8 : 6;
+    __host__ __device__ static int rows(const GemvArgs &a) { return MODE == kGateUp ? a.f : a.d; }
+    __host__ __device__ static int K(const GemvArgs &a) { return MODE == kGateUp ? a.d : a.f; }
+    __host__ __device__ static int P(const GemvArgs &a) { return MODE == kGateUp ? a.p_gu : a.p_dn; }
+    // tiles per staged chunk: the largest divisor of the K part's tile count within the cap
+    __host__ __device__ static int chunk_tiles(const GemvArgs &a)
+    {
+        const int kt = K(a) / P(a) / kTileK;
+        for (int c = kChunkTilesMax; c > 1; c--)
+            if (kt % c == 0) return c;
+        return 1;
+    }
 };
 
-// Issue the copies of one stage (thread 0 only).
+// A work item: 128 rows of one unit over one K part, for passes [pass0, pass1).
+struct Item {
+    int u, rb, kp, pass0, pass1;
+};
+__device__ __forceinline__ int shared_passes(const GemvArgs &a) { return max(1, (a.T + kPassTok - 1) / kPassTok); }
+template <int MODE>
+__device__ __forceinline__ int n_items_of(const GemvArgs &a, int n_active)
+{
+    const int nrb = Geo<MODE>::rows(a) / kItemRows, P = Geo<MODE>::P(a);
+    return (a.S * shared_passes(a) + n_active) * P * nrb;
+}
+// Items are handed out heaviest first: the bf16 shared experts (four times the bytes per
+// weight, one item per token pass), then the routed experts (all passes in one item).
+template <int MODE>
+__device__ __forceinline__ Item item_of(const GemvArgs &a, int n_active, int i)
+{
+    const int nrb = Geo<MODE>::rows(a) / kItemRows, P = Geo<MODE>::P(a);
+    const int nsp = shared_passes(a), n_sh = a.S * nsp * P * nrb;
+    Item it;
+    if (i < n_sh) {
+        it.rb = i % nrb;
+        int j = i / nrb;
+        it.kp = j % P;
+        j /= P;
+        it.pass0 = j % nsp;
+        it.pass1 = it.pass0 + 1;
+        it.u = n_active + j / nsp;
+    } else {
+        const int j = i - n_sh;
+        it.rb = j % nrb;
+        it.kp = (j / nrb) % P;
+        it.u = j / (P * nrb);
+        it.pass0 = 0;
+        it.pass1 = -1;          // all passes of the unit
+    }
+    return it;
+}
+template <int MODE>
+__device__ __forceinline__ int n_stages(const GemvArgs &a, int shared)
+{
+    const int Kp = Geo<MODE>::K(a) / Geo<MODE>::P(a);
+    return shared ? Kp / kSharedK : Kp / kTileK;
+}
+__device__ __forceinline__ int n_passes(const Unit &un) { return max(1, (un.ntok + kPassTok - 1) / kPassTok); }
+
+// Row of the g/u/h and y buffers for token n of pass `pass` of unit `un`.
+__device__ __forceinline__ size_t out_row(const GemvArgs &a, const Unit &un, int pass, int n)
+{
+    return un.shared ? (size_t)a.T * a.k + (size_t)un.id * a.T + pass * kPassTok + n
+                     : (size_t)(un.tok0 + pass * kPassTok + n);
+}
+__device__ __forceinline__ int token_of(const GemvArgs &a, const Unit &un, int pass, int n)
+{
+    if (un.shared) return pass * kPassTok + n;
+    const int slot = a.perm[un.tok0 + pass * kPassTok + n];
+    return min(max(slot, 0), a.T * a.k - 1) / a.k;
+}
+
+// Copies of one weight stage (thread 0 only).
 template <int MODE>
 __device__ void issue_stage(const GemvArgs &a, const CUtensorMap *m1, const CUtensorMap *m3,
-                            const CUtensorMap *m2, const Unit &un, int item_row, int kt,
+                            const CUtensorMap *m2, const Unit &un, const Item &it, int st,
                             uint8_t *buf, uint64_t *bar)
 {
-    const int rb = item_row / kTileRows, half = (item_row % kTileRows) / kItemRows;
     if (!un.shared) {
         const uint8_t *ex = a.table + (size_t)un.id * a.expert_bytes;
+        const int kt = it.kp * n_stages<MODE>(a, 0) + st;
         if (MODE == kGateUp) {
             const int ktn = a.d / kTileK;
-            const uint8_t *pair = ex + ((size_t)rb * ktn + kt) * 2 * kTileBytes;
-            mbar_expect_tx(bar, 2 * (4 * 1024 + 256));
-            for (int m = 0; m < 2; m++) {
-                const uint8_t *tile = pair + (size_t)m * kTileBytes;
-                uint8_t *dst = buf + m * 4352;
-                for (int c = 0; c < 4; c++)
-                    bulk_g2s(dst + c * 1024, tile + c * 2048 + half * 1024, 1024, bar);
-                bulk_g2s(dst + 4096, tile + kTileNibbleBytes + half * 256, 256, bar);
-            }
+            mbar_expect_tx(bar, 2 * kTileBytes);
+            bulk_g2s(buf, ex + ((size_t)it.rb * ktn + kt) * 2 * kTileBytes, 2 * kTileBytes, bar);
         } else {
             const int ktn = a.f / kTileK;
-            const uint8_t *tile = ex + a.gateup_bytes + ((size_t)rb * ktn + kt) * kTileBytes;
-            mbar_expect_tx(bar, 4 * 1024 + 256);
-            for (int c = 0; c < 4; c++)
-                bulk_g2s(buf + c * 1024, tile + c * 2048 + half * 1024, 1024, bar);
-            bulk_g2s(buf + 4096, tile + kTileNibbleBytes + half * 256, 256, bar);
+            mbar_expect_tx(bar, kTileBytes);
+            bulk_g2s(buf, ex + a.gateup_bytes + ((size_t)it.rb * ktn + kt) * kTileBytes, kTileBytes, bar);
         }
     } else {
-        // bf16 shared experts: boxes of 64 K x 64 rows (8 KB), 128-byte swizzle
-        const int k0 = kt * 64;
+        const int k0 = (it.kp * n_stages<MODE>(a, 1) + st) * kSharedK;
         if (MODE == kGateUp) {
-            const int row = un.id * a.f + item_row;
+            const int row = un.id * a.f + it.rb * kItemRows;
             mbar_expect_tx(bar, 2 * 8192);
             tma_2d_g2s(buf, m1, k0, row, bar);
             tma_2d_g2s(buf + 8192, m3, k0, row, bar);
         } else {
-            const int row = un.id * a.d + item_row;
+            const int row = un.id * a.d + it.rb * kItemRows;
             mbar_expect_tx(bar, 8192);
             tma_2d_g2s(buf, m2, k0, row, bar);
         }
     }
 }
 
+// B-operand layout in shared memory: [n-block][k-step][lane][8 bytes]; lane 4n+t of a
+// k-step holds the pairs (k0+2t, k0+2t+1) and (k0+2t+8, k0+2t+9) of token n.
+__device__ __forceinline__ uint32_t b_offset(int nb, int ks, int KS, int n, int kk)
+{
+    const int t = (kk & 7) >> 1, half = kk >> 3;
+    return (uint32_t)(((nb * KS + ks) * 32 + 4 * (n & 7) + t) * 8 + 4 * half);
+}
+
+// Per-pass token facts, computed once per pass into shared memory.
+struct PassTok {
+    int tok[kPassTok];        // token index t
+    long long row[kPassTok];  // row of the g/u/h and y buffers
+    float xin[kPassTok];      // activation multiplier (routed: 2^-u_t; shared: 1)
+    float fo[kPassTok];       // output factor (routed: 2^u_t; shared: 1)
+};
+
+__device__ __forceinline__ void fill_pass(const GemvArgs &a, const Unit &un, int pass, int nvalid,
+                                          PassTok &pt)
+{
+    const int n = threadIdx.x;
+    if (n < nvalid) {
+        const int t = token_of(a, un, pass, n);
+        pt.tok[n] = t;
+        pt.row[n] = (long long)out_row(a, un, pass, n);
+        pt.xin[n] = un.shared ? 1.0f : a.tok_scale[t];
+        pt.fo[n] = un.shared ? 1.0f : a.tok_scale[a.T + t];
+    }
+}
+
+// Stage the activations (gate/up) or the SiTU outputs (down) of the pass's valid tokens
+// over one K chunk of the item into the B layout (hi and, for down, lo halves).
+// Columns of invalid tokens are left as they are: a column of the B operand only
+// reaches the same column of the result, and those results are never stored.
 template <int MODE>
-__device__ __forceinline__ int n_ktiles(const GemvArgs &a, int shared)
+__device__ void stage_b(const GemvArgs &a, const Unit &un, const Item &it, int nvalid, int chunk,
+                        const PassTok &pt, uint8_t *bhi, uint8_t *blo)
 {
-    const int K = Geo<MODE>::k_of(a.d, a.f);
-    return shared ? K / 64 : K / kTileK;
-}
-
-// Stage NT activation rows (f32) for token group `grp` of unit `un` into xs.
-template <int MODE>
-__device__ void stage_x(const GemvArgs &a, const Unit &un, int grp, float *xs, int &nvalid)
-{
-    const int K = Geo<MODE>::k_of(a.d, a.f);
-    const int first = grp * kNT;
-    nvalid = min(kNT, un.ntok - first);
-    for (int i = 0; i < kNT; i++) {
-        float *dst = xs + (size_t)i * K;
-        if (i >= nvalid) {
-            for (int q = threadIdx.x; q < K; q += kThreads) dst[q] = 0.0f;
-            continue;
-        }
-        if (MODE == kGateUp) {
-            int t;
-            if (un.shared) t = first + i;
-            else {
-                const int slot = a.perm[un.tok0 + first + i];
-                t = min(max(slot, 0), a.T * a.k - 1) / a.k;
-            }
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)t * K);
-            for (int q = threadIdx.x; q < K / 8; q += kThreads) {
-                const uint4 v = src[q];
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                float4 lo, hi;
-                lo.x = __uint_as_float(w[0] << 16); lo.y = __uint_as_float(w[0] & 0xFFFF0000u);
-                lo.z = __uint_as_float(w[1] << 16); lo.w = __uint_as_float(w[1] & 0xFFFF0000u);
-                hi.x = __uint_as_float(w[2] << 16); hi.y = __uint_as_float(w[2] & 0xFFFF0000u);
-                hi.z = __uint_as_float(w[3] << 16); hi.w = __uint_as_float(w[3] & 0xFFFF0000u);
-                reinterpret_cast<float4 *>(dst)[2 * q] = lo;
-                reinterpret_cast<float4 *>(dst)[2 * q + 1] = hi;
-            }
-        } else {
-            const size_t hrow = un.shared ? (size_t)a.T * a.k + (size_t)un.id * a.T + first + i
-                                          : (size_t)(un.tok0 + first + i);
-            const float4 *src = reinterpret_cast<const float4 *>(a.h + hrow * K);
-            for (int q = threadIdx.x; q < K / 4; q += kThreads)
-                reinterpret_cast<float4 *>(dst)[q] = src[q];
-        }
-    }
-}
-
-// One 32-column MXFP4 group of one row against NV activation rows (row stride K):
-// the group's partial sums, then times the group's power-of-two scale.
-template <int NV>
-__device__ __forceinline__ void mxfp4_group(const uint4 nib, float scale, const float *xk, int K,
-                                            float acc[kNT])
-{
-    float part[NV];
+    const int K = Geo<MODE>::K(a), Kp = K / Geo<MODE>::P(a);
+    const int KC = Geo<MODE>::chunk_tiles(a) * kTileK, KS = KC / 16;
+    const int k0 = it.kp * Kp + chunk * KC;
+    if (MODE == kGateUp) {
+        const int per_tok = KC / 8;                       // one 16-byte load = 8 columns
+        for (int q = threadIdx.x; q < nvalid * per_tok; q += 256) {
+            const int n = q / per_tok, j = q % per_tok;
+            const int kl = 8 * j, ks = kl >> 4, half = (kl >> 3) & 1;
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)pt.tok[n] * K + k0 + kl));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            const float m = pt.xin[n];
+            uint8_t *dst = bhi + ((size_t)((n >> 3) * KS + ks) * 32 + 4 * (n & 7)) * 8 + 4 * half;
 #pragma unroll
-    for (int i = 0; i < NV; i++) part[i] = 0.0f;
-    const uint32_t w[4] = {nib.x, nib.y, nib.z, nib.w};
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-#pragma unroll
-        for (int b = 0; b < 4; b += 2) {
-            const float2 w01 = e2m1x2_to_f32x2(w[q] >> (8 * b));
-            const float2 w23 = e2m1x2_to_f32x2(w[q] >> (8 * b + 8));
-            const int col = q * 8 + b * 2;
-#pragma unroll
-            for (int i = 0; i < NV; i++) {
-                const float4 xv = *reinterpret_cast<const float4 *>(xk + (size_t)i * K + col);
-                part[i] = fmaf(w01.x, xv.x, part[i]);
-                part[i] = fmaf(w01.y, xv.y, part[i]);
-                part[i] = fmaf(w23.x, xv.z, part[i]);
-                part[i] = fmaf(w23.y, xv.w, part[i]);
-            }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < NV; i++) acc[i] = fmaf(part[i], scale, acc[i]);
-}
-
-// 8 bf16 weights (one 16-byte chunk) against NV activation rows.
-template <int NV>
-__device__ __forceinline__ void bf16_chunk(const uint4 wv, const float *xk, int K, float acc[kNT])
-{
-    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-    for (int q = 0; q < 4; q += 2) {
-        const float w0 = __uint_as_float(w[q] << 16), w1 = __uint_as_float(w[q] & 0xFFFF0000u);
-        const float w2 = __uint_as_float(w[q + 1] << 16), w3 = __uint_as_float(w[q + 1] & 0xFFFF0000u);
-#pragma unroll
-        for (int i = 0; i < NV; i++) {
-            const float4 xv = *reinterpret_cast<const float4 *>(xk + (size_t)i * K + 2 * q);
-            acc[i] = fmaf(w0, xv.x, acc[i]);
-            acc[i] = fmaf(w1, xv.y, acc[i]);
-            acc[i] = fmaf(w2, xv.z, acc[i]);
-            acc[i] = fmaf(w3, xv.w, acc[i]);
-        }
-    }
-}
-
-// The per-thread work on one staged weight tile.
-template <int MODE, int NV>
-__device__ __forceinline__ void consume_tile(const uint8_t *buf, int shared, int kt, int K,
-                                             const float *xs, float acc[kNT])
-{
-    const int tid = threadIdx.x, r = tid & (kItemRows - 1);
-    if (!shared) {
-        if (MODE == kGateUp) {
-            // thread: row r of matrix tid>>7, groups 2*kh, 2*kh+1 of the 128-column tile
-            const int mat = tid >> 7, kh = (tid >> 6) & 1;
-            const uint8_t *mb = buf + mat * 4352;
-            const uint32_t sc4 = *reinterpret_cast<const uint32_t *>(mb + 4096 + r * 4);
-#pragma unroll
-            for (int cc = 0; cc < 2; cc++) {
-                const int c = 2 * kh + cc;
-                const float scale = e8m0_to_f32(sc4 >> (8 * c));
-                if (scale != 0.0f) {
-                    const uint4 nib = *reinterpret_cast<const uint4 *>(mb + c * 1024 + r * 16);
-                    mxfp4_group<NV>(nib, scale, xs + kt * kTileK + c * 32, K, acc);
+            for (int t = 0; t < 4; t++) {
+                uint32_t o = w[t];
+                if (!un.shared) {
+                    const __half2 h2 = __floats2half2_rn(__uint_as_float(w[t] << 16) * m,
+                                                         __uint_as_float(w[t] & 0xFFFF0000u) * m);
+                    o = *reinterpret_cast<const uint32_t *>(&h2);
                 }
-            }
-        } else {
-            const int c = tid >> 6;
-            const uint32_t sc4 = *reinterpret_cast<const uint32_t *>(buf + 4096 + r * 4);
-            const float scale = e8m0_to_f32(sc4 >> (8 * c));
-            if (scale != 0.0f) {
-                const uint4 nib = *reinterpret_cast<const uint4 *>(buf + c * 1024 + r * 16);
-                mxfp4_group<NV>(nib, scale, xs + kt * kTileK + c * 32, K, acc);
+                *reinterpret_cast<uint32_t *>(dst + t * 8) = o;
             }
         }
     } else {
-        // 128-byte swizzled rows of 64 bf16: chunk q of row r sits at r*128 + ((q ^ (r&7))*16)
-        if (MODE == kGateUp) {
-            const int mat = tid >> 7, kh = (tid >> 6) & 1;
-            const uint8_t *mb = buf + mat * 8192;
+        const int per_tok = KC / 4;                       // float4 = 4 columns = 2 pairs
+        const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
+        for (int q = threadIdx.x; q < nvalid * per_tok; q += 256) {
+            const int n = q / per_tok, j = q % per_tok;
+            const int kl = 4 * j, ks = kl >> 4, kk = kl & 15, t0 = (kk & 7) >> 1, half = kk >> 3;
+            const size_t row = (size_t)pt.row[n];
+            const int k = k0 + kl;
+            float h[4];
+            if (a.p_gu == 1) {
+                const float4 hv = *reinterpret_cast<const float4 *>(a.gu + row * a.f + k);
+                h[0] = hv.x; h[1] = hv.y; h[2] = hv.z; h[3] = hv.w;
+            } else {
+                float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int p = 0; p < a.p_gu; p++) {
+                    const float *base = a.gu + ((size_t)p * rows_all + row) * 2 * a.f;
+                    const float4 gv = *reinterpret_cast<const float4 *>(base + k);
+                    const float4 uv = *reinterpret_cast<const float4 *>(base + a.f + k);
+                    g[0] += gv.x; g[1] += gv.y; g[2] += gv.z; g[3] += gv.w;
+                    u[0] += uv.x; u[1] += uv.y; u[2] += uv.z; u[3] += uv.w;
+                }
+                const float fo = pt.fo[n];
 #pragma unroll
-            for (int cc = 0; cc < 4; cc++) {
-                const int q = kh * 4 + cc;
-                const uint4 wv = *reinterpret_cast<const uint4 *>(mb + r * 128 + ((q ^ (r & 7)) << 4));
-                bf16_chunk<NV>(wv, xs + kt * 64 + q * 8, K, acc);
+                for (int e = 0; e < 4; e++) h[e] = situ(g[e] * fo, u[e] * fo, a.b1, a.b2);
             }
-        } else {
-            const int kq = tid >> 6;
+            const size_t off = ((size_t)((n >> 3) * KS + ks) * 32 + 4 * (n & 7) + t0) * 8 + 4 * half;
 #pragma unroll
-            for (int cc = 0; cc < 2; cc++) {
-                const int q = kq * 2 + cc;
-                const uint4 wv = *reinterpret_cast<const uint4 *>(buf + r * 128 + ((q ^ (r & 7)) << 4));
-                bf16_chunk<NV>(wv, xs + kt * 64 + q * 8, K, acc);
+            for (int pr = 0; pr < 2; pr++) {
+                const float h0 = h[2 * pr], h1 = h[2 * pr + 1];
+                uint32_t hi, lo;
+                if (un.shared) {
+                    const __nv_bfloat162 hh = __floats2bfloat162_rn(h0, h1);
+                    const float2 hf = __bfloat1622float2(hh);
+                    const __nv_bfloat162 ll = __floats2bfloat162_rn(h0 - hf.x, h1 - hf.y);
+                    hi = *reinterpret_cast<const uint32_t *>(&hh);
+                    lo = *reinterpret_cast<const uint32_t *>(&ll);
+                } else {
+                    const __half2 hh = __floats2half2_rn(h0, h1);
+                    const float2 hf = __half22float2(hh);
+                    const __half2 ll = __floats2half2_rn(h0 - hf.x, h1 - hf.y);
+                    hi = *reinterpret_cast<const uint32_t *>(&hh);
+                    lo = *reinterpret_cast<const uint32_t *>(&ll);
+                }
+                *reinterpret_cast<uint32_t *>(bhi + off + pr * 8) = hi;
+                *reinterpret_cast<uint32_t *>(blo + off + pr * 8) = lo;
             }
         }
     }
 }
 
+// One weight stage of warp `w` (rows 16w..16w+15 of the item).
+template <int MODE, int NB>
+__device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, int st, int KS,
+                                              const uint8_t *bhi, const uint8_t *blo,
+                                              float (&acc1)[kNBMax][4], float (&acc3)[kNBMax][4])
+{
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2;
+    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+    if (!shared) {
+        const int ks0 = st * 8;                               // 8 k-steps per 128-column tile
+        float f1[4], f1b[4], f3[4], f3b[4];
+        row_scales(*reinterpret_cast<const uint32_t *>(buf + kTileNibbleBytes + (16 * w + g) * 4), f1);
+        row_scales(*reinterpret_cast<const uint32_t *>(buf + kTileNibbleBytes + (16 * w + g + 8) * 4), f1b);
+        if (MODE == kGateUp) {
+            row_scales(*reinterpret_cast<const uint32_t *>(buf + kTileBytes + kTileNibbleBytes + (16 * w + g) * 4), f3);
+            row_scales(*reinterpret_cast<const uint32_t *>(buf + kTileBytes + kTileNibbleBytes + (16 * w + g + 8) * 4), f3b);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            const uint2 wa = *reinterpret_cast<const uint2 *>(buf + (w * 4 + c) * 256 + 8 * lane);
+            uint32_t A0[4], A1[4];
+            e2m1x8_to_f16x2(wa.x, A0[0], A0[2], A1[0], A1[2]);
+            e2m1x8_to_f16x2(wa.y, A0[1], A0[3], A1[1], A1[3]);
+            uint32_t C0[4], C1[4];
+            if (MODE == kGateUp) {
+                const uint2 wc = *reinterpret_cast<const uint2 *>(buf + kTileBytes + (w * 4 + c) * 256 + 8 * lane);
+                e2m1x8_to_f16x2(wc.x, C0[0], C0[2], C1[0], C1[2]);
+                e2m1x8_to_f16x2(wc.y, C0[1], C0[3], C1[1], C1[3]);
+            }
+#pragma unroll
+            for (int nb = 0; nb < NB; nb++) {
+                const uint2 b0 = *reinterpret_cast<const uint2 *>(bhi + ((nb * KS + ks0 + 2 * c) * 32 + lane) * 8);
+                const uint2 b1 = *reinterpret_cast<const uint2 *>(bhi + ((nb * KS + ks0 + 2 * c + 1) * 32 + lane) * 8);
+                float t1[4];
+                mma_f16(t1, A0, b0.x, b0.y, zero);
+                mma_f16(t1, A1, b1.x, b1.y, t1);
+                if (MODE == kDown) {
+                    const uint2 l0 = *reinterpret_cast<const uint2 *>(blo + ((nb * KS + ks0 + 2 * c) * 32 + lane) * 8);
+                    const uint2 l1 = *reinterpret_cast<const uint2 *>(blo + ((nb * KS + ks0 + 2 * c + 1) * 32 + lane) * 8);
+                    mma_f16(t1, A0, l0.x, l0.y, t1);
+                    mma_f16(t1, A1, l1.x, l1.y, t1);
+                }
+                acc1[nb][0] = fmaf(f1[c], t1[0], acc1[nb][0]);
+                acc1[nb][1] = fmaf(f1[c], t1[1], acc1[nb][1]);
+                acc1[nb][2] = fmaf(f1b[c], t1[2], acc1[nb][2]);
+                acc1[nb][3] = fmaf(f1b[c], t1[3], acc1[nb][3]);
+                if (MODE == kGateUp) {
+                    float t3[4];
+                    mma_f16(t3, C0, b0.x, b0.y, zero);
+                    mma_f16(t3, C1, b1.x, b1.y, t3);
+                    acc3[nb][0] = fmaf(f3[c], t3[0], acc3[nb][0]);
+                    acc3[nb][1] = fmaf(f3[c], t3[1], acc3[nb][1]);
+                    acc3[nb][2] = fmaf(f3b[c], t3[2], acc3[nb][2]);
+                    acc3[nb][3] = fmaf(f3b[c], t3[3], acc3[nb][3]);
+                }
+            }
+        }
+    } else {
+        // bf16 tiles: 128 rows x 32 columns, 64-byte swizzle (chunk q of row r at r*64 + ((q ^ ((r>>1)&3))*16))
+        const int ks0 = st * 2;
+        const int r = 16 * w + (lane & 15);
+#pragma unroll
+        for (int kk = 0; kk < 2; kk++) {
+            const int q = 2 * kk + (lane >> 4);
+            const uint32_t roff = (uint32_t)(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+            uint32_t A[4], C[4];
+            ldmatrix_x4(A, buf + roff);
+            if (MODE == kGateUp) ldmatrix_x4(C, buf + 8192 + roff);
+#pragma unroll
+            for (int nb = 0; nb < NB; nb++) {
+                const uint2 b = *reinterpret_cast<const uint2 *>(bhi + ((nb * KS + ks0 + kk) * 32 + lane) * 8);
+                mma_bf16(acc1[nb], A, b.x, b.y, acc1[nb]);
+                if (MODE == kDown) {
+                    const uint2 l = *reinterpret_cast<const uint2 *>(blo + ((nb * KS + ks0 + kk) * 32 + lane) * 8);
+                    mma_bf16(acc1[nb], A, l.x, l.y, acc1[nb]);
+                } else {
+                    mma_bf16(acc3[nb], C, b.x, b.y, acc3[nb]);
+                }
+            }
+        }
+    }
+}
+
+// Warps 0-7 consume (warp w owns rows 16w..16w+15 of each item); warp 8 produces: it
+// takes work items from a global counter, heaviest first, and streams their weight stages
+// through a kStages ring, refilling a slot once all eight consumer warps released it.
+// Every stage carries a header (item, pass, stage) so the consumers follow the producer;
+// a header with item -1 ends the stream.  Every wait is bounded; a timeout sets the
+// status word and the block drops out.
 template <int MODE>
-__global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ GemvArgs a,
-                                                        const __grid_constant__ CUtensorMap m1,
-                                                        const __grid_constant__ CUtensorMap m3,
-                                                        const __grid_constant__ CUtensorMap m2)
+__global__ void __launch_bounds__(kThreads + 32) gemv_kernel(const __grid_constant__ GemvArgs a,
+                                                             const __grid_constant__ CUtensorMap m1,
+                                                             const __grid_constant__ CUtensorMap m3,
+                                                             const __grid_constant__ CUtensorMap m2)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    constexpr int kStageBytes = Geo<MODE>::kStageBytes;
     uint8_t *bufs = smem;                                          // kStages * kStageBytes
-    float *xs = reinterpret_cast<float *>(smem + kStages * kStageBytes);
-    const int K = Geo<MODE>::k_of(a.d, a.f);
-    float *red = xs + (size_t)kNT * K;                              // reduction scratch
-    __shared__ uint64_t full[kStages];
+    const int P = Geo<MODE>::P(a);
+    const int ctiles = Geo<MODE>::chunk_tiles(a), KS = ctiles * kTileK / 16;
+    uint8_t *bhi = smem + kStages * kStageBytes;                   // kNBMax * KS * 256 bytes
+    uint8_t *blo = bhi + (size_t)kNBMax * KS * 256;                // down only
+    __shared__ uint64_t full[kStages], empty[kStages], csync;
+    __shared__ int hdr_item[kStages], hdr_pass[kStages], hdr_st[kStages];
+    __shared__ int issued[kStages];
+    __shared__ PassTok pt;
     __shared__ int bail;
 
     if (*a.abort) return;
-    const int rows = Geo<MODE>::rows_of(a.d, a.f);
-    const int n_ri = rows / kItemRows;
     const int n_active = min(max(a.active[a.E], 0), a.E);
-    const int n_items = (n_active + a.S) * n_ri;
-    const int i_begin = (int)((long long)n_items * blockIdx.x / gridDim.x);
-    const int i_end = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x);
-    if (i_begin >= i_end) return;
-
-    const int tid = threadIdx.x;
+    const int n_items = n_items_of<MODE>(a, n_active);
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int s = 0; s < kStages; s++) mbar_init(&full[s], 1);
+        for (int s = 0; s < kStages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kThreads / 32);
+            issued[s] = 0;
+        }
+        mbar_init(&csync, kThreads);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         bail = 0;
     }
     __syncthreads();
 
-    // producer cursor (thread 0)
-    Cursor pc{i_begin, 0, 0};
-    int produced = 0;
-    auto groups_of = [&](const Unit &un) { return max(1, (un.ntok + kNT - 1) / kNT); };
-    auto advance = [&](Cursor &c) {
-        const Unit un = unit_of(a, n_active, c.item / n_ri);
-        if (++c.kt == n_ktiles<MODE>(a, un.shared)) {
-            c.kt = 0;
-            if (++c.grp == groups_of(un)) {
-                c.grp = 0;
-                ++c.item;
+    if (w == kThreads / 32) {
+        // ---------------- producer
+        if (lane == 0) {
+            int n = 0;
+            for (;;) {
+                const int i = atomicAdd(&a.work[MODE], 1);
+                const bool done = i >= n_items || bail;
+                Item it{};
+                Unit un{};
+                int pass1 = 0, nst = 0;
+                if (!done) {
+                    it = item_of<MODE>(a, n_active, i);
+                    un = unit_of(a, n_active, it.u);
+                    pass1 = it.pass1 < 0 ? n_passes(un) : it.pass1;
+                    nst = n_stages<MODE>(a, un.shared);
+                }
+                for (int pass = it.pass0; done ? pass == it.pass0 : pass < pass1; pass++)
+                    for (int st = 0; done ? st == 0 : st < nst; st++, n++) {
+                        const int slot = n % kStages;
+                        if (n >= kStages && !mbar_wait(&empty[slot], (uint32_t)((n / kStages) - 1) & 1u)) {
+                            set_status(a.status, K3MOE_DEV_TIMEOUT);
+                            bail = 1;
+                        }
+                        if (bail) break;
+                        hdr_item[slot] = done ? -1 : i;
+                        hdr_pass[slot] = pass;
+                        hdr_st[slot] = st;
+                        if (done) {
+                            mbar_arrive(&full[slot]);          // end of stream, no copy
+                        } else {
+                            fence_proxy_async();
+                            issue_stage<MODE>(a, &m1, &m3, &m2, un, it, st, bufs + slot * kStageBytes, &full[slot]);
+                            issued[slot]++;
+                        }
+                    }
+                if (done || bail) break;
             }
         }
-    };
-    auto produce = [&]() {
-        if (pc.item >= i_end) return;
-        const Unit un = unit_of(a, n_active, pc.item / n_ri);
-        const int slot = produced % kStages;
-        fence_proxy_async();
-        issue_stage<MODE>(a, &m1, &m3, &m2, un, (pc.item % n_ri) * kItemRows, pc.kt,
-                          bufs + slot * kStageBytes, &full[slot]);
-        ++produced;
-        advance(pc);
-    };
-    if (tid == 0)
-        for (int s = 0; s < kStages; s++) produce();
-
-    const int r = tid & (kItemRows - 1);
-    int consumed = 0;
-    int staged_unit = -1, staged_grp = -1, nvalid = 0;
-    for (int item = i_begin; item < i_end; item++) {
-        const int u = item / n_ri;
-        const Unit un = unit_of(a, n_active, u);
-        const int item_row = (item % n_ri) * kItemRows;
-        const int ngrp = groups_of(un);
-        for (int grp = 0; grp < ngrp; grp++) {
-            if (staged_unit != u || staged_grp != grp) {
-                __syncthreads();
-                stage_x<MODE>(a, un, grp, xs, nvalid);
-                staged_unit = u;
-                staged_grp = grp;
-                __syncthreads();
+    } else {
+        // ---------------- consumers
+        const int g = lane >> 2, t4 = lane & 3;
+        uint32_t sync_phase = 0;
+        auto csync_all = [&]() -> bool {       // all 256 consumer threads, bounded
+            mbar_arrive(&csync);
+            const bool ok = mbar_wait(&csync, sync_phase & 1u);
+            sync_phase++;
+            return ok;
+        };
+        float acc1[kNBMax][4], acc3[kNBMax][4];
+        int staged_u = -1, staged_kp = -1, staged_pass = -1, staged_chunk = -1;
+        for (int n = 0;; n++) {
+            const int slot = n % kStages;
+            if (!mbar_wait(&full[slot], (uint32_t)(n / kStages) & 1u)) {
+                set_status(a.status, K3MOE_DEV_TIMEOUT);
+                bail = 1;
+                break;
             }
-            float acc[kNT];
+            const int item = hdr_item[slot];
+            if (item < 0) break;
+            const int pass = hdr_pass[slot], st = hdr_st[slot];
+            const Item it = item_of<MODE>(a, n_active, item);
+            const Unit un = unit_of(a, n_active, it.u);
+            const int nst = n_stages<MODE>(a, un.shared);
+            const int spc = un.shared ? ctiles * kTileK / kSharedK : ctiles;   // stages per chunk
+            const int nvalid = min(kPassTok, un.ntok - pass * kPassTok);
+            if (st == 0) {
 #pragma unroll
-            for (int i = 0; i < kNT; i++) acc[i] = 0.0f;
-            const int nkt = n_ktiles<MODE>(a, un.shared);
-            for (int kt = 0; kt < nkt; kt++) {
-                const int slot = consumed % kStages;
-                const uint32_t parity = (uint32_t)(consumed / kStages) & 1u;
-                if (!mbar_wait(&full[slot], parity)) {
+                for (int nb = 0; nb < kNBMax; nb++)
+#pragma unroll
+                    for (int i = 0; i < 4; i++) acc1[nb][i] = acc3[nb][i] = 0.0f;
+            }
+            const int chunk = st / spc;
+            if (st % spc == 0 && (it.u != staged_u || it.kp != staged_kp || pass != staged_pass ||
+                                  chunk != staged_chunk)) {
+                bool ok = csync_all();               // all consumers done with bhi/blo and pt
+                fill_pass(a, un, pass, nvalid, pt);
+                ok = ok && csync_all();
+                stage_b<MODE>(a, un, it, nvalid, chunk, pt, bhi, blo);
+                ok = ok && csync_all();
+                if (!ok) {
                     set_status(a.status, K3MOE_DEV_TIMEOUT);
                     bail = 1;
+                    break;
                 }
-                const uint8_t *buf = bufs + slot * kStageBytes;
-                switch (nvalid) {
-                case 1: consume_tile<MODE, 1>(buf, un.shared, kt, K, xs, acc); break;
-                case 2: consume_tile<MODE, 2>(buf, un.shared, kt, K, xs, acc); break;
-                case 3: consume_tile<MODE, 3>(buf, un.shared, kt, K, xs, acc); break;
-                default: consume_tile<MODE, 4>(buf, un.shared, kt, K, xs, acc); break;
-                }
-                ++consumed;
-                __syncthreads();                 // everyone is done with this slot
-                if (tid == 0 && !bail) produce();
-                if (bail) break;
+                staged_u = it.u;
+                staged_kp = it.kp;
+                staged_pass = pass;
+                staged_chunk = chunk;
             }
-            if (bail) break;
-            // reduce the K slices of each row and write the item's outputs
+            const uint8_t *buf = bufs + slot * kStageBytes;
+            if (nvalid > 8)
+                consume_stage<MODE, 2>(buf, un.shared, st % spc, KS, bhi, blo, acc1, acc3);
+            else
+                consume_stage<MODE, 1>(buf, un.shared, st % spc, KS, bhi, blo, acc1, acc3);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (st != nst - 1) continue;
+            // epilogue: this thread holds rows 16w+g (+8) x tokens 8nb+2t4 (+1)
+            const int row0 = it.rb * kItemRows + 16 * w + g;
+            const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
 #pragma unroll
-            for (int i = 0; i < kNT; i++) red[(size_t)i * kThreads + tid] = acc[i];
-            __syncthreads();
-            if (tid < kItemRows) {
-                for (int i = 0; i < nvalid; i++) {
-                    const float *ri = red + (size_t)i * kThreads;
-                    const size_t orow = un.shared
-                                            ? (size_t)a.T * a.k + (size_t)un.id * a.T + grp * kNT + i
-                                            : (size_t)(un.tok0 + grp * kNT + i);
+            for (int nb = 0; nb < kNBMax; nb++) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int nn = nb * 8 + 2 * t4 + (i & 1);
+                    if (nn >= nvalid) continue;
+                    const int row = row0 + ((i >> 1) << 3);
+                    const size_t orow = (size_t)pt.row[nn];
                     if (MODE == kGateUp) {
-                        const float g = ri[tid] + ri[tid + 64];
-                        const float uu = ri[tid + 128] + ri[tid + 192];
-                        a.h[orow * a.f + item_row + tid] = situ(g, uu, a.b1, a.b2);
+                        if (P == 1) {
+                            const float fo = pt.fo[nn];
+                            a.gu[orow * a.f + row] = situ(acc1[nb][i] * fo, acc3[nb][i] * fo, a.b1, a.b2);
+                        } else {
+                            float *base = a.gu + ((size_t)it.kp * rows_all + orow) * 2 * a.f;
+                            base[row] = acc1[nb][i];
+                            base[a.f + row] = acc3[nb][i];
+                        }
                     } else {
-                        const float y = (ri[tid] + ri[tid + 64]) + (ri[tid + 128] + ri[tid + 192]);
-                        a.ys[orow * a.d + item_row + tid] = y;
+                        a.ys[((size_t)it.kp * rows_all + orow) * a.d + row] = acc1[nb][i];
                     }
                 }
             }
-            // red is rewritten only after the next item's K loop, which has barriers
         }
-        if (bail) break;
     }
+    __syncthreads();
     if (bail && tid == 0) {
-        // let copies still in flight land before the block's shared memory is released
-        for (int n = consumed; n < produced; n++) mbar_wait(&full[n % kStages], (uint32_t)(n / kStages) & 1u);
+        // a wait gave up: let every copy still in flight land before the block's shared
+        // memory is released (each wait bounded)
+        for (int s = 0; s < kStages; s++)
+            if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)(issued[s] - 1) & 1u);
     }
 }
 
 // -------------------------------------------------------------------------------- combine
 struct CombineArgs {
-    int T, d, k, S;
+    int T, d, k, S, P;
     const float *weight;
     const int32_t *inv;
     const float *ys;
@@ -557,6 +795,7 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(CombineArgs a)
     const size_t n = (size_t)a.T * d4;
     const bool ab = *a.abort != 0;
     const int slots = a.T * a.k;
+    const size_t rows_all = (size_t)slots + (size_t)a.S * a.T;
     for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n;
          q += (size_t)gridDim.x * blockDim.x) {
         const int t = (int)(q / d4), c4 = (int)(q % d4);
@@ -566,7 +805,11 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(CombineArgs a)
                 const int p = a.inv[(size_t)t * a.k + j];
                 if (p < 0 || p >= slots) continue;
                 const float w = a.weight[(size_t)t * a.k + j];
-                const float4 y = reinterpret_cast<const float4 *>(a.ys + (size_t)p * a.d)[c4];
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int kp = 0; kp < a.P; kp++) {
+                    const float4 v = reinterpret_cast<const float4 *>(a.ys + ((size_t)kp * rows_all + p) * a.d)[c4];
+                    y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+                }
                 acc.x = fmaf(w, y.x, acc.x);
                 acc.y = fmaf(w, y.y, acc.y);
                 acc.z = fmaf(w, y.z, acc.z);
@@ -574,11 +817,10 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(CombineArgs a)
             }
             for (int s = 0; s < a.S; s++) {
                 const size_t row = (size_t)slots + (size_t)s * a.T + t;
-                const float4 y = reinterpret_cast<const float4 *>(a.ys + row * a.d)[c4];
-                acc.x += y.x;
-                acc.y += y.y;
-                acc.z += y.z;
-                acc.w += y.w;
+                for (int kp = 0; kp < a.P; kp++) {
+                    const float4 y = reinterpret_cast<const float4 *>(a.ys + ((size_t)kp * rows_all + row) * a.d)[c4];
+                    acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
+                }
             }
         }
         reinterpret_cast<float4 *>(a.out + (size_t)t * a.d)[c4] = acc;
@@ -605,17 +847,17 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// bf16 matrix [rows][cols] row-major; boxes of 64 cols x 64 rows, 128-byte swizzle.
+// bf16 matrix [rows][cols] row-major; boxes of 32 cols x 128 rows, 64-byte swizzle.
 bool make_bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {64, kItemRows};
+    const cuuint32_t box[2] = {kSharedK, kItemRows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -636,7 +878,7 @@ template <typename Kern>
 int grid_blocks(Kern kernel, size_t smem)
 {
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem) != cudaSuccess || occ < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads + 32, smem) != cudaSuccess || occ < 1)
         occ = 1;
     return sm_count() * occ;
 }
@@ -653,10 +895,11 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     int32_t *abort = status + 1;
     int32_t *active = reinterpret_cast<int32_t *>(ws + L.active);
     int32_t *inv = reinterpret_cast<int32_t *>(ws + L.inv);
-    float *h = reinterpret_cast<float *>(ws + L.h);
+    float *tok_scale = reinterpret_cast<float *>(ws + L.tok_scale);
+    float *gu = reinterpret_cast<float *>(ws + L.gu);
     float *ys = reinterpret_cast<float *>(ws + L.ys);
 
-    PrepArgs pa{T, c.n_experts, c.top_k, idx, offsets, perm, active, inv, status, abort};
+    PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, status, abort};
     timing_begin("fwd_prep", s);
     fwd_prep_kernel<<<1, 1024, 0, s>>>(pa);
     count_launch();
@@ -669,28 +912,30 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
             !make_bf16_map(&m2, sh_w2, (uint64_t)c.n_shared * c.d, c.f))
             return cudaErrorInvalidValue;
     }
-    GemvArgs ga{T, c.d, c.f, c.top_k, c.n_shared, c.n_experts, c.situ_b1, c.situ_b2, x, offsets,
-                perm, active, table, expert_bytes(c.d, c.f), gateup_block_bytes(c.d, c.f), h, ys,
-                abort, status};
+    GemvArgs ga{T, c.d, c.f, c.top_k, c.n_shared, c.n_experts, L.p_gu, L.p_dn, c.situ_b1, c.situ_b2,
+                x, offsets, perm, active, tok_scale, table, expert_bytes(c.d, c.f),
+                gateup_block_bytes(c.d, c.f), gu, ys, abort, status, abort + 1};
     {
-        const size_t smem = 1024 + kStages * kStageBytes + (size_t)kNT * c.d * 4 + (size_t)kNT * kThreads * 4;
+        const size_t smem = 1024 + kStages * Geo<kGateUp>::kStageBytes +
+                            (size_t)kNBMax * (Geo<kGateUp>::chunk_tiles(ga) * kTileK / 16) * 256;
         cudaFuncSetAttribute(gemv_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         const int blocks = grid_blocks(gemv_kernel<kGateUp>, smem);
         timing_begin("gemv_gateup", s);
-        gemv_kernel<kGateUp><<<blocks, kThreads, smem, s>>>(ga, m1, m3, m2);
+        gemv_kernel<kGateUp><<<blocks, kThreads + 32, smem, s>>>(ga, m1, m3, m2);
         count_launch();
         timing_end("gemv_gateup", s);
     }
     {
-        const size_t smem = 1024 + kStages * kStageBytes + (size_t)kNT * c.f * 4 + (size_t)kNT * kThreads * 4;
+        const size_t smem = 1024 + kStages * Geo<kDown>::kStageBytes +
+                            2 * (size_t)kNBMax * (Geo<kDown>::chunk_tiles(ga) * kTileK / 16) * 256;
         cudaFuncSetAttribute(gemv_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         const int blocks = grid_blocks(gemv_kernel<kDown>, smem);
         timing_begin("gemv_down", s);
-        gemv_kernel<kDown><<<blocks, kThreads, smem, s>>>(ga, m1, m3, m2);
+        gemv_kernel<kDown><<<blocks, kThreads + 32, smem, s>>>(ga, m1, m3, m2);
         count_launch();
         timing_end("gemv_down", s);
     }
-    CombineArgs ca{T, c.d, c.top_k, c.n_shared, weight, inv, ys, out, abort};
+    CombineArgs ca{T, c.d, c.top_k, c.n_shared, L.p_dn, weight, inv, ys, out, abort};
     {
         const size_t n = (size_t)T * c.d / 4;
         int grid = (int)((n + 255) / 256);

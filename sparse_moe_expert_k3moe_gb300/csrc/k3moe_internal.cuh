@@ -7,11 +7,13 @@
 //   - down block:    for row block rb in [0, d/128), for K tile kt in [0, f/128):
 //       [W2 tile (rb, kt)]
 //   A tile is 128 rows x 128 columns of one matrix, 8704 bytes:
-//   - bytes [0, 8192): 16-byte chunks; chunk (c, r) at (c * 128 + r) * 16 holds the
-//     32 codes of row r, columns kt*128 + 32c .. +31, in checkpoint byte order
-//     (low nibble = even column).  Chunk-major order makes consecutive rows
-//     consecutive 16-byte words: conflict-free shared-memory reads when a thread
-//     owns a row.
+//   - bytes [0, 8192): the E2M1 codes, in 32 blocks of 256 bytes, block (s, c) at
+//     (s * 4 + c) * 256 for the 16-row strip s (rows 16s..16s+15) and the 32-column
+//     group c.  Inside a block, lane L = 4g + t (g < 8, t < 4) owns 8 bytes at 8L:
+//     bytes t, t+4, t+8, t+12 of row 16s+g's 16-byte group, then the same four bytes
+//     of row 16s+g+8 (checkpoint byte order: low nibble = even column).  These are
+//     exactly the A-operand pairs that lane holds in a 16x16 tensor-core fragment, for
+//     the group's two 16-column steps, so one 8-byte load per lane feeds them.
 //   - bytes [8192, 8704): E8M0 scale of (row r, group c) at 8192 + r * 4 + c.
 //   Tiles are contiguous, so one bulk copy moves a tile, and a gate/up K step
 //   (both matrices) is one 17408-byte copy.  Bytes per expert = 3*f*d*17/32.
@@ -60,6 +62,17 @@ struct StatusBlock {
     int32_t pad[62];
 };
 
+// K splits of the decode-path work items.  With few tokens there are few (expert,
+// row block) items, so each item's K range is split into P parts to fill the GPU; the
+// consumer adds the P partial sums in a fixed order.  P divides the K-tile count.
+inline int ksplit_for(int ktiles, int T, int k)
+{
+    if (T * k > 64) return 1;
+    for (int p = 4; p > 1; p >>= 1)
+        if (ktiles % p == 0) return p;
+    return 1;
+}
+
 // Workspace regions (byte offsets), sized for one call's T.
 struct WsLayout {
     size_t status;
@@ -69,10 +82,12 @@ struct WsLayout {
     size_t local_rank;           // [T*k] int32
     size_t active;               // [E + 1] int32: active expert ids, then the count
     size_t inv;                  // [T*k] int32: slot -> position in perm
-    size_t h;                    // [(T*k + S*T)][f] f32 (decode path)
-    size_t ys;                   // [(T*k + S*T)][d] f32 (decode path)
+    size_t tok_scale;            // [2][T] f32: activation multiplier 2^-u, output factor 2^u
+    size_t gu;                   // decode: h [rows][f] f32 (P_gu == 1) or g|u partials [P_gu][rows][2][f]
+    size_t ys;                   // decode: y partials [P_dn][rows][d] f32
     size_t total;
     int n_chunks;
+    int p_gu, p_dn;              // K splits of the gate/up and down items
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -83,6 +98,8 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     const size_t E = (size_t)c.n_experts, k = (size_t)c.top_k, S = (size_t)c.n_shared;
     const size_t slots = (size_t)T * k;
     L.n_chunks = (T + kChunkTokens - 1) / kChunkTokens;
+    L.p_gu = ksplit_for(c.d / kTileK, T, c.top_k);
+    L.p_dn = ksplit_for(c.f / kTileK, T, c.top_k);
     size_t o = 0;
     L.status = o; o += 256;
     L.sc = o; o = align256(o + (size_t)T * E * 4);
@@ -92,9 +109,10 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     L.local_rank = o; o = align256(o + slots * 4);
     L.active = o; o = align256(o + (E + 1) * 4);
     L.inv = o; o = align256(o + slots * 4);
+    L.tok_scale = o; o = align256(o + (size_t)T * 2 * 4);
     const size_t rows = slots + S * (size_t)T;
-    L.h = o; o = align256(o + rows * (size_t)c.f * 4);
-    L.ys = o; o = align256(o + rows * (size_t)c.d * 4);
+    L.gu = o; o = align256(o + rows * (size_t)c.f * 4 * (L.p_gu > 1 ? 2 * L.p_gu : 1));
+    L.ys = o; o = align256(o + rows * (size_t)c.d * 4 * L.p_dn);
     L.total = o;
     return L;
 }

@@ -13,11 +13,12 @@ struct PackArgs {
     int32_t *status;
 };
 
-// Decompose the 16-byte chunk number q (within one expert, in table order) into
-// the matrix (0 = W1, 1 = W3, 2 = W2), the source row and the source group, and
-// the destination offsets of its nibble chunk and scale byte within the expert.
+// Decompose the 16-byte source group number q (within one expert, in table order) into
+// the matrix (0 = W1, 1 = W3, 2 = W2), the source row and the source group, and the
+// destination offsets, within the expert, of the group's lane words and scale byte:
+// byte b of the group goes to lane 4*(r%8) + b%4, word r%16/8, byte position b/4.
 __device__ __forceinline__ void chunk_coords(int d, int f, size_t q, int &mat, int &row,
-                                             int &grp, size_t &dst_nib, size_t &dst_scale)
+                                             int &grp, size_t &dst_lane0, size_t &dst_scale)
 {
     const size_t chunks_per_tile = (size_t)kTileNibbleBytes / 16;     // 512
     const size_t tile = q / chunks_per_tile;
@@ -40,8 +41,18 @@ __device__ __forceinline__ void chunk_coords(int d, int f, size_t q, int &mat, i
     }
     row = rb * kTileRows + r;
     grp = kt * (kTileK / kGroup) + c;
-    dst_nib = tile * kTileBytes + (size_t)(c * kTileRows + r) * 16;
+    const int s = r / 16, g = r % 8, hi = (r % 16) / 8;
+    dst_lane0 = tile * kTileBytes + (size_t)(s * 4 + c) * 256 + (size_t)(4 * g) * 8 + hi * 4;
     dst_scale = tile * kTileBytes + kTileNibbleBytes + (size_t)r * 4 + c;
+}
+
+// The four lane words of a group: word t = bytes t, t+4, t+8, t+12.
+__device__ __forceinline__ uint32_t lane_word(const uint4 v, int t)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const int sh = 8 * t;
+    return ((w[0] >> sh) & 0xFFu) | (((w[1] >> sh) & 0xFFu) << 8) | (((w[2] >> sh) & 0xFFu) << 16) |
+           (((w[3] >> sh) & 0xFFu) << 24);
 }
 
 __global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
@@ -64,7 +75,8 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
             sp + (size_t)e * mat_nib + (size_t)row * (cols / 2) + (size_t)grp * 16);
         const uint8_t sb = ss[(size_t)e * mat_sc + (size_t)row * (cols / kGroup) + grp];
         uint8_t *dst = a.table + (size_t)(a.expert_lo + e) * eb;
-        *reinterpret_cast<uint4 *>(dst + dn) = v;
+        for (int t = 0; t < 4; t++)
+            *reinterpret_cast<uint32_t *>(dst + dn + (size_t)t * 8) = lane_word(v, t);
         dst[ds] = sb;
         if (sb == 255 && a.status) set_status(a.status, K3MOE_DEV_NAN_SCALE);
     }
@@ -93,8 +105,13 @@ __global__ void __launch_bounds__(256) unpack_kernel(UnpackArgs a)
         uint8_t *dsx = mat == 0 ? a.w1s : (mat == 1 ? a.w3s : a.w2s);
         const size_t mat_nib = (size_t)rows * cols / 2, mat_sc = (size_t)rows * cols / kGroup;
         const uint8_t *src = a.table + (size_t)(a.expert_lo + e) * eb;
+        uint32_t w[4] = {0, 0, 0, 0};
+        for (int t = 0; t < 4; t++) {
+            const uint32_t lw = *reinterpret_cast<const uint32_t *>(src + dn + (size_t)t * 8);
+            for (int q = 0; q < 4; q++) w[q] |= ((lw >> (8 * q)) & 0xFFu) << (8 * t);
+        }
         *reinterpret_cast<uint4 *>(dp + (size_t)e * mat_nib + (size_t)row * (cols / 2) +
-                                   (size_t)grp * 16) = *reinterpret_cast<const uint4 *>(src + dn);
+                                   (size_t)grp * 16) = make_uint4(w[0], w[1], w[2], w[3]);
         dsx[(size_t)e * mat_sc + (size_t)row * (cols / kGroup) + grp] = src[ds];
     }
 }
