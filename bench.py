@@ -312,10 +312,13 @@ def gpu_arm(args):
     barrier()
     torch.cuda.synchronize(dev)
     n0 = k3.k3moe_launch_count()
+    host_s = 0.0
     for i in range(args.steps):
         flush.fill_(i & 255)
         ev[i][0].record(stream)
+        h0 = time.perf_counter()
         step()
+        host_s += time.perf_counter() - h0
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -394,6 +397,7 @@ def gpu_arm(args):
                               "tensor_frac": step_flops / step_s / 1e12 / bf16_sus},
             "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kt.items()},
             "gpu_launches": launches,
+            "host_enqueue_ms_per_step": 1000.0 * host_s / args.steps,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,

@@ -35,6 +35,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "k3moe_internal.cuh"
 
 namespace k3moe {
@@ -45,7 +47,7 @@ constexpr int kItemRows = 128;
 constexpr int kStages = 4;
 constexpr int kNBMax = 2;                          // n-blocks of 8 tokens per pass
 constexpr int kPassTok = 8 * kNBMax;
-constexpr int kSharedK = 32;                       // K per stage for bf16 tiles
+constexpr int kSharedK = 64;                       // K per stage for bf16 tiles (one matrix)
 constexpr long long kWaitCycles = 4000000000ll;      // bounded waits: ~2 s at 2 GHz
 
 enum Mode { kGateUp = 0, kDown = 1 };
@@ -152,15 +154,22 @@ __device__ __forceinline__ float situ(float g, float u, float b1, float b2)
     return a * (b2 * tanhf(u / b2));
 }
 
-// The four E8M0 scales of one row (one byte per group) as floats.
+// The four E8M0 scales of one row (one byte per group) as floats: the hardware
+// ue8m0x2 -> bf16x2 conversion gives 2^(b-127) exactly; bf16 -> f32 is a shift.  Bytes
+// 0 (a subnormal) and 255 (read as zero) take the slow path.
 __device__ __forceinline__ void row_scales(uint32_t s4, float (&f)[4])
 {
     const bool special = (__vcmpeq4(s4, 0u) | __vcmpeq4(s4, 0xFFFFFFFFu)) != 0u;
     if (!special) {
-        f[0] = __uint_as_float((s4 << 23) & 0x7F800000u);
-        f[1] = __uint_as_float((s4 << 15) & 0x7F800000u);
-        f[2] = __uint_as_float((s4 << 7) & 0x7F800000u);
-        f[3] = __uint_as_float((s4 >> 1) & 0x7F800000u);
+        uint32_t lo, hi;
+        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+            "cvt.rn.bf16x2.ue8m0x2 %0, a;\n\tcvt.rn.bf16x2.ue8m0x2 %1, b;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(s4));
+        f[0] = __uint_as_float(lo << 16);
+        f[1] = __uint_as_float(lo & 0xFFFF0000u);
+        f[2] = __uint_as_float(hi << 16);
+        f[3] = __uint_as_float(hi & 0xFFFF0000u);
     } else {
 #pragma unroll
         for (int c = 0; c < 4; c++) f[c] = e8m0_to_f32(s4 >> (8 * c));
@@ -175,6 +184,8 @@ struct PrepArgs {
     int32_t *active;     // [E + 1]
     int32_t *inv;        // [T * k]
     float *tok_scale;    // [2][T]
+    int32_t *arrive;     // K-part arrival counters, zeroed here
+    int n_arrive;
     int32_t *status;
     int32_t *abort;
 };
@@ -198,13 +209,25 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
         if (e < 0 || e >= E) atomicOr(&bad, K3MOE_DEV_BAD_INDEX);
         a.inv[s] = -1;
     }
+    for (int i = tid; i < a.n_arrive; i += blockDim.x) a.arrive[i] = 0;
     // per-token activation scale: 2^-u puts max|x_t| in [2^14, 2^15); u in [-113, 113]
     for (int t = warp; t < a.T; t += 32) {
-        const uint32_t *row = reinterpret_cast<const uint32_t *>(a.x + (size_t)t * a.d);
+        const uint4 *row = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.d);
+        const int n16 = a.d / 8;
         uint32_t m = 0;
-        for (int q = lane; q < a.d / 2; q += 32) {
-            const uint32_t v = row[q];
-            m = max(m, max((v & 0x7FFFu), (v >> 16) & 0x7FFFu));
+        for (int q0 = lane; q0 < n16; q0 += 32 * 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {          // eight independent loads in flight
+                const int q = q0 + 32 * j;
+                v[j] = q < n16 ? row[q] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                for (int h = 0; h < 4; h++) m = max(m, max(w4[h] & 0x7FFFu, (w4[h] >> 16) & 0x7FFFu));
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -272,6 +295,8 @@ struct GemvArgs {
     const uint8_t *table;
     size_t expert_bytes, gateup_bytes;
     float *gu, *ys;
+    uint16_t *hp;                   // SiTU output planes: hi at [0], lo at [rows * f]
+    int32_t *arrive;                // K-part arrival counters per (unit, row block)
     const int32_t *abort;
     int32_t *status;
     int32_t *work;                  // [2] work counters (gate/up, down), zeroed by fwd_prep
@@ -304,9 +329,11 @@ template <int MODE>
 struct Geo {
     // stage bytes: a W1+W3 tile pair (gate/up) or one tile (down); bf16 boxes fit in both
     // (multiples of 1024 so every stage buffer meets the swizzled-TMA alignment)
-    static constexpr int kStageBytes = MODE == kGateUp ? 2 * kTileBytes : 9 * 1024;
+    static constexpr int kStageBytes = MODE == kGateUp ? 2 * kTileBytes : 16 * 1024;
     // B operand staged in chunks of at most this many 128-column tiles
-    static constexpr int kChunkTilesMax = MODE == kGateUp ? 8 : 6;
+    static constexpr int kChunkTilesMax = MODE == kGateUp ? 8 : 4;
+    // bf16 stages carry one matrix: gate/up alternates W1 and W3 slices
+    static constexpr int kSharedMats = MODE == kGateUp ? 2 : 1;
     __host__ __device__ static int rows(const GemvArgs &a) { return MODE == kGateUp ? a.f : a.d; }
     __host__ __device__ static int K(const GemvArgs &a) { return MODE == kGateUp ? a.d : a.f; }
     __host__ __device__ static int P(const GemvArgs &a) { return MODE == kGateUp ? a.p_gu : a.p_dn; }
@@ -361,7 +388,7 @@ template <int MODE>
 __device__ __forceinline__ int n_stages(const GemvArgs &a, int shared)
 {
     const int Kp = Geo<MODE>::K(a) / Geo<MODE>::P(a);
-    return shared ? Kp / kSharedK : Kp / kTileK;
+    return shared ? Geo<MODE>::kSharedMats * (Kp / kSharedK) : Kp / kTileK;
 }
 __device__ __forceinline__ int n_passes(const Unit &un) { return max(1, (un.ntok + kPassTok - 1) / kPassTok); }
 
@@ -397,17 +424,13 @@ __device__ void issue_stage(const GemvArgs &a, const CUtensorMap *m1, const CUte
             bulk_g2s(buf, ex + a.gateup_bytes + ((size_t)it.rb * ktn + kt) * kTileBytes, kTileBytes, bar);
         }
     } else {
-        const int k0 = (it.kp * n_stages<MODE>(a, 1) + st) * kSharedK;
-        if (MODE == kGateUp) {
-            const int row = un.id * a.f + it.rb * kItemRows;
-            mbar_expect_tx(bar, 2 * 8192);
-            tma_2d_g2s(buf, m1, k0, row, bar);
-            tma_2d_g2s(buf + 8192, m3, k0, row, bar);
-        } else {
-            const int row = un.id * a.d + it.rb * kItemRows;
-            mbar_expect_tx(bar, 8192);
-            tma_2d_g2s(buf, m2, k0, row, bar);
-        }
+        // one 64-column slice of one matrix; gate/up alternates W1 (even) and W3 (odd)
+        const int slice = st / Geo<MODE>::kSharedMats;
+        const int k0 = it.kp * (Geo<MODE>::K(a) / Geo<MODE>::P(a)) + slice * kSharedK;
+        const CUtensorMap *m = MODE == kGateUp ? ((st & 1) ? m3 : m1) : m2;
+        const int row = un.id * Geo<MODE>::rows(a) + it.rb * kItemRows;
+        mbar_expect_tx(bar, kItemRows * kSharedK * 2);
+        tma_2d_g2s(buf, m, k0, row, bar);
     }
 }
 
@@ -472,50 +495,22 @@ __device__ void stage_b(const GemvArgs &a, const Unit &un, const Item &it, int n
             }
         }
     } else {
-        const int per_tok = KC / 4;                       // float4 = 4 columns = 2 pairs
-        const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
+        // the SiTU output, already split into hi and lo 16-bit planes (f16 for routed
+        // experts, bf16 for shared ones): a copy into the B layout
+        const int per_tok = KC / 8;
+        const size_t plane = ((size_t)a.T * a.k + (size_t)a.S * a.T) * a.f;
         for (int q = threadIdx.x; q < nvalid * per_tok; q += 256) {
             const int n = q / per_tok, j = q % per_tok;
-            const int kl = 4 * j, ks = kl >> 4, kk = kl & 15, t0 = (kk & 7) >> 1, half = kk >> 3;
-            const size_t row = (size_t)pt.row[n];
-            const int k = k0 + kl;
-            float h[4];
-            if (a.p_gu == 1) {
-                const float4 hv = *reinterpret_cast<const float4 *>(a.gu + row * a.f + k);
-                h[0] = hv.x; h[1] = hv.y; h[2] = hv.z; h[3] = hv.w;
-            } else {
-                float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int p = 0; p < a.p_gu; p++) {
-                    const float *base = a.gu + ((size_t)p * rows_all + row) * 2 * a.f;
-                    const float4 gv = *reinterpret_cast<const float4 *>(base + k);
-                    const float4 uv = *reinterpret_cast<const float4 *>(base + a.f + k);
-                    g[0] += gv.x; g[1] += gv.y; g[2] += gv.z; g[3] += gv.w;
-                    u[0] += uv.x; u[1] += uv.y; u[2] += uv.z; u[3] += uv.w;
-                }
-                const float fo = pt.fo[n];
+            const int kl = 8 * j, ks = kl >> 4, half = (kl >> 3) & 1;
+            const size_t src = (size_t)pt.row[n] * a.f + k0 + kl;
+            const uint4 vh = *reinterpret_cast<const uint4 *>(a.hp + src);
+            const uint4 vl = *reinterpret_cast<const uint4 *>(a.hp + plane + src);
+            const uint32_t wh[4] = {vh.x, vh.y, vh.z, vh.w}, wl[4] = {vl.x, vl.y, vl.z, vl.w};
+            const size_t off = ((size_t)((n >> 3) * KS + ks) * 32 + 4 * (n & 7)) * 8 + 4 * half;
 #pragma unroll
-                for (int e = 0; e < 4; e++) h[e] = situ(g[e] * fo, u[e] * fo, a.b1, a.b2);
-            }
-            const size_t off = ((size_t)((n >> 3) * KS + ks) * 32 + 4 * (n & 7) + t0) * 8 + 4 * half;
-#pragma unroll
-            for (int pr = 0; pr < 2; pr++) {
-                const float h0 = h[2 * pr], h1 = h[2 * pr + 1];
-                uint32_t hi, lo;
-                if (un.shared) {
-                    const __nv_bfloat162 hh = __floats2bfloat162_rn(h0, h1);
-                    const float2 hf = __bfloat1622float2(hh);
-                    const __nv_bfloat162 ll = __floats2bfloat162_rn(h0 - hf.x, h1 - hf.y);
-                    hi = *reinterpret_cast<const uint32_t *>(&hh);
-                    lo = *reinterpret_cast<const uint32_t *>(&ll);
-                } else {
-                    const __half2 hh = __floats2half2_rn(h0, h1);
-                    const float2 hf = __half22float2(hh);
-                    const __half2 ll = __floats2half2_rn(h0 - hf.x, h1 - hf.y);
-                    hi = *reinterpret_cast<const uint32_t *>(&hh);
-                    lo = *reinterpret_cast<const uint32_t *>(&ll);
-                }
-                *reinterpret_cast<uint32_t *>(bhi + off + pr * 8) = hi;
-                *reinterpret_cast<uint32_t *>(blo + off + pr * 8) = lo;
+            for (int t = 0; t < 4; t++) {
+                *reinterpret_cast<uint32_t *>(bhi + off + t * 8) = wh[t];
+                *reinterpret_cast<uint32_t *>(blo + off + t * 8) = wl[t];
             }
         }
     }
@@ -579,39 +574,36 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, in
             }
         }
     } else {
-        // bf16 tiles: 128 rows x 32 columns, 64-byte swizzle (chunk q of row r at r*64 + ((q ^ ((r>>1)&3))*16))
-        const int ks0 = st * 2;
+        // bf16 tile: 128 rows x 64 columns, 128-byte swizzle (chunk q of row r at
+        // r*128 + ((q ^ (r&7))*16)); gate/up stages alternate W1 (even) and W3 (odd)
+        const int mats = Geo<MODE>::kSharedMats;
+        const int ks0 = (st / mats) * (kSharedK / 16);
+        const bool up = MODE == kGateUp && (st & 1);
         const int r = 16 * w + (lane & 15);
 #pragma unroll
-        for (int kk = 0; kk < 2; kk++) {
+        for (int kk = 0; kk < kSharedK / 16; kk++) {
             const int q = 2 * kk + (lane >> 4);
-            const uint32_t roff = (uint32_t)(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
-            uint32_t A[4], C[4];
-            ldmatrix_x4(A, buf + roff);
-            if (MODE == kGateUp) ldmatrix_x4(C, buf + 8192 + roff);
+            uint32_t A[4];
+            ldmatrix_x4(A, buf + r * 128 + ((q ^ (r & 7)) << 4));
 #pragma unroll
             for (int nb = 0; nb < NB; nb++) {
                 const uint2 b = *reinterpret_cast<const uint2 *>(bhi + ((nb * KS + ks0 + kk) * 32 + lane) * 8);
-                mma_bf16(acc1[nb], A, b.x, b.y, acc1[nb]);
                 if (MODE == kDown) {
                     const uint2 l = *reinterpret_cast<const uint2 *>(blo + ((nb * KS + ks0 + kk) * 32 + lane) * 8);
+                    mma_bf16(acc1[nb], A, b.x, b.y, acc1[nb]);
                     mma_bf16(acc1[nb], A, l.x, l.y, acc1[nb]);
+                } else if (up) {
+                    mma_bf16(acc3[nb], A, b.x, b.y, acc3[nb]);
                 } else {
-                    mma_bf16(acc3[nb], C, b.x, b.y, acc3[nb]);
+                    mma_bf16(acc1[nb], A, b.x, b.y, acc1[nb]);
                 }
             }
         }
     }
 }
 
-// Warps 0-7 consume (warp w owns rows 16w..16w+15 of each item); warp 8 produces: it
-// takes work items from a global counter, heaviest first, and streams their weight stages
-// through a kStages ring, refilling a slot once all eight consumer warps released it.
-// Every stage carries a header (item, pass, stage) so the consumers follow the producer;
-// a header with item -1 ends the stream.  Every wait is bounded; a timeout sets the
-// status word and the block drops out.
 template <int MODE>
-__global__ void __launch_bounds__(kThreads + 32) gemv_kernel(const __grid_constant__ GemvArgs a,
+__global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_constant__ GemvArgs a,
                                                              const __grid_constant__ CUtensorMap m1,
                                                              const __grid_constant__ CUtensorMap m3,
                                                              const __grid_constant__ CUtensorMap m2)
@@ -628,7 +620,7 @@ __global__ void __launch_bounds__(kThreads + 32) gemv_kernel(const __grid_consta
     __shared__ int hdr_item[kStages], hdr_pass[kStages], hdr_st[kStages];
     __shared__ int issued[kStages];
     __shared__ PassTok pt;
-    __shared__ int bail;
+    __shared__ int bail, last_part;
 
     if (*a.abort) return;
     const int n_active = min(max(a.active[a.E], 0), a.E);
@@ -696,6 +688,10 @@ __global__ void __launch_bounds__(kThreads + 32) gemv_kernel(const __grid_consta
         };
         float acc1[kNBMax][4], acc3[kNBMax][4];
         int staged_u = -1, staged_kp = -1, staged_pass = -1, staged_chunk = -1;
+        int cur_item = -1, cur_pass = -1;
+        Item it{};
+        Unit un{};
+        int nst = 0, spc = 1, nvalid = 0;
         for (int n = 0;; n++) {
             const int slot = n % kStages;
             if (!mbar_wait(&full[slot], (uint32_t)(n / kStages) & 1u)) {
@@ -706,11 +702,17 @@ __global__ void __launch_bounds__(kThreads + 32) gemv_kernel(const __grid_consta
             const int item = hdr_item[slot];
             if (item < 0) break;
             const int pass = hdr_pass[slot], st = hdr_st[slot];
-            const Item it = item_of<MODE>(a, n_active, item);
-            const Unit un = unit_of(a, n_active, it.u);
-            const int nst = n_stages<MODE>(a, un.shared);
-            const int spc = un.shared ? ctiles * kTileK / kSharedK : ctiles;   // stages per chunk
-            const int nvalid = min(kPassTok, un.ntok - pass * kPassTok);
+            if (item != cur_item || pass != cur_pass) {        // decode once per (item, pass)
+                if (item != cur_item) {
+                    it = item_of<MODE>(a, n_active, item);
+                    un = unit_of(a, n_active, it.u);
+                    nst = n_stages<MODE>(a, un.shared);
+                    spc = un.shared ? Geo<MODE>::kSharedMats * (ctiles * kTileK / kSharedK) : ctiles;
+                    cur_item = item;
+                }
+                nvalid = min(kPassTok, un.ntok - pass * kPassTok);
+                cur_pass = pass;
+            }
             if (st == 0) {
 #pragma unroll
                 for (int nb = 0; nb < kNBMax; nb++)
@@ -746,27 +748,95 @@ __global__ void __launch_bounds__(kThreads + 32) gemv_kernel(const __grid_consta
             // epilogue: this thread holds rows 16w+g (+8) x tokens 8nb+2t4 (+1)
             const int row0 = it.rb * kItemRows + 16 * w + g;
             const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
+            if (MODE == kDown) {
 #pragma unroll
-            for (int nb = 0; nb < kNBMax; nb++) {
+                for (int nb = 0; nb < kNBMax; nb++)
 #pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    const int nn = nb * 8 + 2 * t4 + (i & 1);
-                    if (nn >= nvalid) continue;
-                    const int row = row0 + ((i >> 1) << 3);
-                    const size_t orow = (size_t)pt.row[nn];
-                    if (MODE == kGateUp) {
-                        if (P == 1) {
-                            const float fo = pt.fo[nn];
-                            a.gu[orow * a.f + row] = situ(acc1[nb][i] * fo, acc3[nb][i] * fo, a.b1, a.b2);
-                        } else {
-                            float *base = a.gu + ((size_t)it.kp * rows_all + orow) * 2 * a.f;
-                            base[row] = acc1[nb][i];
-                            base[a.f + row] = acc3[nb][i];
-                        }
-                    } else {
-                        a.ys[((size_t)it.kp * rows_all + orow) * a.d + row] = acc1[nb][i];
+                    for (int i = 0; i < 4; i++) {
+                        const int nn = nb * 8 + 2 * t4 + (i & 1);
+                        if (nn >= nvalid) continue;
+                        const int row = row0 + ((i >> 1) << 3);
+                        a.ys[((size_t)it.kp * rows_all + (size_t)pt.row[nn]) * a.d + row] = acc1[nb][i];
                     }
+                continue;
+            }
+            bool finish = (P == 1);
+            if (!finish) {
+                // K split: publish this part's partial sums; the last part to arrive for
+                // this (unit, row block) adds all parts in order and applies SiTU
+#pragma unroll
+                for (int nb = 0; nb < kNBMax; nb++)
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int nn = nb * 8 + 2 * t4 + (i & 1);
+                        if (nn >= nvalid) continue;
+                        const int row = row0 + ((i >> 1) << 3);
+                        float *base = a.gu + ((size_t)it.kp * rows_all + (size_t)pt.row[nn]) * 2 * a.f;
+                        base[row] = acc1[nb][i];
+                        base[a.f + row] = acc3[nb][i];
+                    }
+                __threadfence();
+                bool ok = csync_all();
+                if (tid == 0) {
+                    int32_t *ctr = a.arrive + (size_t)it.u * (a.f / kItemRows) + it.rb;
+                    const int old = atomicAdd(ctr, 1);
+                    last_part = (old == P - 1);
+                    if (last_part) *ctr = 0;
                 }
+                ok = ok && csync_all();
+                if (!ok) {
+                    set_status(a.status, K3MOE_DEV_TIMEOUT);
+                    bail = 1;
+                    break;
+                }
+                finish = last_part != 0;
+                if (finish) {
+                    __threadfence();
+#pragma unroll
+                    for (int nb = 0; nb < kNBMax; nb++)
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const int nn = nb * 8 + 2 * t4 + (i & 1);
+                            if (nn >= nvalid) continue;
+                            const int row = row0 + ((i >> 1) << 3);
+                            float gs = 0.0f, us = 0.0f;
+                            for (int p = 0; p < P; p++) {
+                                const float *base = a.gu + ((size_t)p * rows_all + (size_t)pt.row[nn]) * 2 * a.f;
+                                gs += __ldcg(base + row);
+                                us += __ldcg(base + a.f + row);
+                            }
+                            acc1[nb][i] = gs;
+                            acc3[nb][i] = us;
+                        }
+                }
+            }
+            if (finish) {
+                const size_t plane = rows_all * a.f;
+#pragma unroll
+                for (int nb = 0; nb < kNBMax; nb++)
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int nn = nb * 8 + 2 * t4 + (i & 1);
+                        if (nn >= nvalid) continue;
+                        const int row = row0 + ((i >> 1) << 3);
+                        const float fo = pt.fo[nn];
+                        const float h = situ(acc1[nb][i] * fo, acc3[nb][i] * fo, a.b1, a.b2);
+                        uint16_t hi, lo;
+                        if (un.shared) {
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(h);
+                            const __nv_bfloat16 lb = __float2bfloat16_rn(h - __bfloat162float(hb));
+                            hi = *reinterpret_cast<const uint16_t *>(&hb);
+                            lo = *reinterpret_cast<const uint16_t *>(&lb);
+                        } else {
+                            const __half hh = __float2half_rn(h);
+                            const __half lh = __float2half_rn(h - __half2float(hh));
+                            hi = *reinterpret_cast<const uint16_t *>(&hh);
+                            lo = *reinterpret_cast<const uint16_t *>(&lh);
+                        }
+                        const size_t at = (size_t)pt.row[nn] * a.f + row;
+                        a.hp[at] = hi;
+                        a.hp[plane + at] = lo;
+                    }
             }
         }
     }
@@ -789,41 +859,67 @@ struct CombineArgs {
     const int32_t *abort;
 };
 
+// One thread per output element; the token's k positions and weights are read first and
+// every partial row is then loaded (unconditionally: prep has validated the positions,
+// and an aborted call writes zeros) before any is summed, so a thread's loads are all in
+// flight together.  Sum order: slot j ascending (its K parts in order), then the shared
+// experts in order.
+template <int P>
+__device__ __forceinline__ float combine_one(const CombineArgs &a, int t, int c, size_t rows_all)
+{
+    const int slots = a.T * a.k;
+    int pos[kMaxTopK];
+    float wt[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; j++) {
+        const int jj = j < a.k ? j : 0;
+        const int p = a.inv[(size_t)t * a.k + jj];
+        pos[j] = min(max(p, 0), slots - 1);
+        wt[j] = j < a.k ? a.weight[(size_t)t * a.k + jj] : 0.0f;
+    }
+    float y[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; j++) y[j] = 0.0f;
+#pragma unroll
+    for (int kp = 0; kp < P; kp++) {
+        const float *base = a.ys + (size_t)kp * rows_all * a.d + c;
+        float v[kMaxTopK];
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; j++) v[j] = j < a.k ? base[(size_t)pos[j] * a.d] : 0.0f;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; j++) y[j] += v[j];
+    }
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; j++)
+        if (j < a.k) acc = fmaf(wt[j], y[j], acc);
+    for (int s = 0; s < a.S; s++) {
+        const size_t row = (size_t)slots + (size_t)s * a.T + t;
+        float ysh = 0.0f;
+#pragma unroll
+        for (int kp = 0; kp < P; kp++) ysh += a.ys[((size_t)kp * rows_all + row) * a.d + c];
+        acc += ysh;
+    }
+    return acc;
+}
+
 __global__ void __launch_bounds__(256) fwd_combine_kernel(CombineArgs a)
 {
-    const int d4 = a.d / 4;
-    const size_t n = (size_t)a.T * d4;
+    const size_t n = (size_t)a.T * a.d;
     const bool ab = *a.abort != 0;
-    const int slots = a.T * a.k;
-    const size_t rows_all = (size_t)slots + (size_t)a.S * a.T;
+    const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
     for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n;
          q += (size_t)gridDim.x * blockDim.x) {
-        const int t = (int)(q / d4), c4 = (int)(q % d4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int t = (int)(q / a.d), c = (int)(q % a.d);
+        float acc = 0.0f;
         if (!ab) {
-            for (int j = 0; j < a.k; j++) {
-                const int p = a.inv[(size_t)t * a.k + j];
-                if (p < 0 || p >= slots) continue;
-                const float w = a.weight[(size_t)t * a.k + j];
-                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int kp = 0; kp < a.P; kp++) {
-                    const float4 v = reinterpret_cast<const float4 *>(a.ys + ((size_t)kp * rows_all + p) * a.d)[c4];
-                    y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
-                }
-                acc.x = fmaf(w, y.x, acc.x);
-                acc.y = fmaf(w, y.y, acc.y);
-                acc.z = fmaf(w, y.z, acc.z);
-                acc.w = fmaf(w, y.w, acc.w);
-            }
-            for (int s = 0; s < a.S; s++) {
-                const size_t row = (size_t)slots + (size_t)s * a.T + t;
-                for (int kp = 0; kp < a.P; kp++) {
-                    const float4 y = reinterpret_cast<const float4 *>(a.ys + ((size_t)kp * rows_all + row) * a.d)[c4];
-                    acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
-                }
+            switch (a.P) {
+            case 1: acc = combine_one<1>(a, t, c, rows_all); break;
+            case 2: acc = combine_one<2>(a, t, c, rows_all); break;
+            default: acc = combine_one<4>(a, t, c, rows_all); break;
             }
         }
-        reinterpret_cast<float4 *>(a.out + (size_t)t * a.d)[c4] = acc;
+        a.out[q] = acc;
     }
 }
 
@@ -847,7 +943,7 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// bf16 matrix [rows][cols] row-major; boxes of 32 cols x 128 rows, 64-byte swizzle.
+// bf16 matrix [rows][cols] row-major; boxes of 64 cols x 128 rows, 128-byte swizzle.
 bool make_bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols)
 {
     EncodeTiledFn fn = encode_fn();
@@ -857,7 +953,7 @@ bool make_bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t col
     const cuuint32_t box[2] = {kSharedK, kItemRows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -873,14 +969,50 @@ int sm_count()
     return n;
 }
 
-// Persistent grid: every SM filled to the occupancy the kernel's resources allow.
+// Persistent grid: every SM filled to the occupancy the kernel's resources allow
+// (shared memory carve-out at its maximum).  Attributes and occupancy are set up once
+// per (kernel, shared-memory size) and cached.
 template <typename Kern>
 int grid_blocks(Kern kernel, size_t smem)
 {
+    struct Entry { const void *k; size_t smem; int blocks; };
+    static Entry cache[16];
+    static int n_cache = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n_cache; i++)
+        if (cache[i].k == (const void *)kernel && cache[i].smem == smem) return cache[i].blocks;
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads + 32, smem) != cudaSuccess || occ < 1)
         occ = 1;
-    return sm_count() * occ;
+    const int blocks = sm_count() * occ;
+    if (n_cache < 16) cache[n_cache++] = Entry{(const void *)kernel, smem, blocks};
+    return blocks;
+}
+
+// Tensor maps of the shared-expert weights, cached by (address, shape).
+bool cached_bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols)
+{
+    struct Entry { const void *base; uint64_t rows, cols; CUtensorMap map; };
+    static Entry cache[32];
+    static int n_cache = 0, next = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n_cache; i++)
+        if (cache[i].base == base && cache[i].rows == rows && cache[i].cols == cols) {
+            *m = cache[i].map;
+            return true;
+        }
+    if (!make_bf16_map(m, base, rows, cols)) return false;
+    Entry &e = cache[n_cache < 32 ? n_cache++ : (next++ % 32)];
+    e.base = base;
+    e.rows = rows;
+    e.cols = cols;
+    e.map = *m;
+    return true;
 }
 
 }  // namespace
@@ -897,9 +1029,12 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     int32_t *inv = reinterpret_cast<int32_t *>(ws + L.inv);
     float *tok_scale = reinterpret_cast<float *>(ws + L.tok_scale);
     float *gu = reinterpret_cast<float *>(ws + L.gu);
+    uint16_t *hp = reinterpret_cast<uint16_t *>(ws + L.hp);
+    int32_t *arrive = reinterpret_cast<int32_t *>(ws + L.arrive);
     float *ys = reinterpret_cast<float *>(ws + L.ys);
 
-    PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, status, abort};
+    PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, arrive,
+                (c.n_experts + c.n_shared) * (c.f / kTileRows), status, abort};
     timing_begin("fwd_prep", s);
     fwd_prep_kernel<<<1, 1024, 0, s>>>(pa);
     count_launch();
@@ -907,18 +1042,17 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
 
     CUtensorMap m1{}, m3{}, m2{};
     if (c.n_shared > 0) {
-        if (!make_bf16_map(&m1, sh_w1, (uint64_t)c.n_shared * c.f, c.d) ||
-            !make_bf16_map(&m3, sh_w3, (uint64_t)c.n_shared * c.f, c.d) ||
-            !make_bf16_map(&m2, sh_w2, (uint64_t)c.n_shared * c.d, c.f))
+        if (!cached_bf16_map(&m1, sh_w1, (uint64_t)c.n_shared * c.f, c.d) ||
+            !cached_bf16_map(&m3, sh_w3, (uint64_t)c.n_shared * c.f, c.d) ||
+            !cached_bf16_map(&m2, sh_w2, (uint64_t)c.n_shared * c.d, c.f))
             return cudaErrorInvalidValue;
     }
     GemvArgs ga{T, c.d, c.f, c.top_k, c.n_shared, c.n_experts, L.p_gu, L.p_dn, c.situ_b1, c.situ_b2,
                 x, offsets, perm, active, tok_scale, table, expert_bytes(c.d, c.f),
-                gateup_block_bytes(c.d, c.f), gu, ys, abort, status, abort + 1};
+                gateup_block_bytes(c.d, c.f), gu, ys, hp, arrive, abort, status, abort + 1};
     {
         const size_t smem = 1024 + kStages * Geo<kGateUp>::kStageBytes +
                             (size_t)kNBMax * (Geo<kGateUp>::chunk_tiles(ga) * kTileK / 16) * 256;
-        cudaFuncSetAttribute(gemv_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         const int blocks = grid_blocks(gemv_kernel<kGateUp>, smem);
         timing_begin("gemv_gateup", s);
         gemv_kernel<kGateUp><<<blocks, kThreads + 32, smem, s>>>(ga, m1, m3, m2);
@@ -928,7 +1062,6 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     {
         const size_t smem = 1024 + kStages * Geo<kDown>::kStageBytes +
                             2 * (size_t)kNBMax * (Geo<kDown>::chunk_tiles(ga) * kTileK / 16) * 256;
-        cudaFuncSetAttribute(gemv_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         const int blocks = grid_blocks(gemv_kernel<kDown>, smem);
         timing_begin("gemv_down", s);
         gemv_kernel<kDown><<<blocks, kThreads + 32, smem, s>>>(ga, m1, m3, m2);
@@ -937,7 +1070,7 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     }
     CombineArgs ca{T, c.d, c.top_k, c.n_shared, L.p_dn, weight, inv, ys, out, abort};
     {
-        const size_t n = (size_t)T * c.d / 4;
+        const size_t n = (size_t)T * c.d;
         int grid = (int)((n + 255) / 256);
         if (grid > sm_count() * 8) grid = sm_count() * 8;
         if (grid < 1) grid = 1;

@@ -67,7 +67,7 @@ struct StatusBlock {
 // consumer adds the P partial sums in a fixed order.  P divides the K-tile count.
 inline int ksplit_for(int ktiles, int T, int k)
 {
-    if (T * k > 64) return 1;
+    if (T > 16 || T * k > 64) return 1;     // with a split, every unit has one token pass
     for (int p = 4; p > 1; p >>= 1)
         if (ktiles % p == 0) return p;
     return 1;
@@ -83,7 +83,9 @@ struct WsLayout {
     size_t active;               // [E + 1] int32: active expert ids, then the count
     size_t inv;                  // [T*k] int32: slot -> position in perm
     size_t tok_scale;            // [2][T] f32: activation multiplier 2^-u, output factor 2^u
-    size_t gu;                   // decode: h [rows][f] f32 (P_gu == 1) or g|u partials [P_gu][rows][2][f]
+    size_t gu;                   // decode: g|u partials [P_gu][rows][2][f] f32 (only when P_gu > 1)
+    size_t hp;                   // decode: SiTU output as hi and lo planes [2][rows][f] 16-bit
+    size_t arrive;               // decode: per (unit, row block) K-part arrival counters
     size_t ys;                   // decode: y partials [P_dn][rows][d] f32
     size_t total;
     int n_chunks;
@@ -111,7 +113,9 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     L.inv = o; o = align256(o + slots * 4);
     L.tok_scale = o; o = align256(o + (size_t)T * 2 * 4);
     const size_t rows = slots + S * (size_t)T;
-    L.gu = o; o = align256(o + rows * (size_t)c.f * 4 * (L.p_gu > 1 ? 2 * L.p_gu : 1));
+    L.gu = o; o = align256(o + (L.p_gu > 1 ? rows * (size_t)c.f * 4 * 2 * L.p_gu : 0));
+    L.hp = o; o = align256(o + rows * (size_t)c.f * 2 * 2);
+    L.arrive = o; o = align256(o + (E + S) * (size_t)(c.f / kTileRows) * 4);
     L.ys = o; o = align256(o + rows * (size_t)c.d * 4 * L.p_dn);
     L.total = o;
     return L;

@@ -1,67 +1,79 @@
-// k3moe_route.cu -- router and token -> expert map (kimi-k3-in-c README,
-// Part II, section 9 "Picking 16 experts of 896").
+// k3moe_route.cu -- router and token -> expert map (kimi-k3-in-c README, Part II,
+// section 9 "Picking 16 experts of 896").
 //
 // Kernels, in launch order:
-//   router_scores   logits = x . Wr^T (fp32 accumulation of exact bf16 products),
-//                   sc = 1/(1+expf(-logit)), ch = sc + bias, both float, to the workspace;
-//   router_topk     one warp per token: top_k by ch via repeated warp arg-max (strict
-//                   comparison, ties to the lower index), weights from sc renormalised in
-//                   rank order; then, per block of 64 tokens (one "chunk" of slots), the
-//                   per-expert slot counts and each slot's stable rank inside the chunk
-//                   (warp match + ballot prefix).  A single-chunk launch finishes the
-//                   map in place: scan, offsets, perm;
-//   perm_scan       (several chunks) per-expert exclusive scan over chunks, then over
-//                   experts -> offsets and every chunk's base;
-//   perm_scatter    (several chunks) perm[base + rank] = slot.
+//   router_scores  logits = x . Wr^T (fp32 accumulation of exact bf16 products),
+//                  sc = 1/(1+expf(-logit)), ch = sc + bias, both float, to the workspace.
+//                  A block owns 8 experts (one per warp, its Wr row held in registers)
+//                  and walks the tokens 8 at a time through shared memory;
+//   router_topk    one block per token: a bitonic sort of the E keys (ch, then the lower
+//                  index first) picks the top k in rank order; the weights are the chosen
+//                  sc renormalised by their float sum in rank order, times routed_scale.
+//                  With at most 64 tokens the last block to finish also builds the map;
+//   perm_count     (more tokens) per chunk of 64 tokens: per-expert slot counts and each
+//                  slot's stable rank inside the chunk (warp match + popc, warp by warp);
+//   perm_scan      per-expert exclusive scan over chunks, then over experts -> offsets;
+//   perm_scatter   perm[base + rank] = slot.
+// The map is a stable counting sort: offsets = exclusive prefix sum of the per-expert
+// counts, and inside an expert's segment the flat slot ids t*k+j ascend.
 #include "k3moe_internal.cuh"
 
 namespace k3moe {
 namespace {
 
-constexpr int kScoreWarps = 4;      // experts per router_scores block (one per warp)
-constexpr int kScoreTok = 8;        // tokens per register tile in router_scores
+constexpr int kScoreWarps = 8;       // experts per block (one per warp)
+constexpr int kScoreTok = 8;         // tokens staged per round
+constexpr int kScoreChunks = 16;     // 16-byte Wr chunks per lane held at once (4096 columns)
 
 // -------------------------------------------------------------------------------- scores
-// One warp per expert row of Wr; lanes stride along d in 16-byte chunks (8 bf16), so each
-// warp-wide load is 512 contiguous bytes.  Tokens go in register tiles of kScoreTok.
 __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
     int T, int d, int E, const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
     const float *__restrict__ bias, float *__restrict__ sc_out, float *__restrict__ ch_out)
 {
+    extern __shared__ __align__(16) uint8_t xs_raw[];        // kScoreTok x d bf16
+    uint4 *xs = reinterpret_cast<uint4 *>(xs_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kScoreWarps + warp;
-    if (e >= E) return;
-    const uint4 *wrow = reinterpret_cast<const uint4 *>(wr + (size_t)e * d);
-    const int nchunk = d / 8;
-    const float b = bias ? bias[e] : 0.0f;
+    const int nchunk = d / 8;                                  // 16-byte chunks per row
+    const uint4 *wrow = reinterpret_cast<const uint4 *>(wr + (size_t)min(e, E - 1) * d);
+    const float b = (bias && e < E) ? bias[e] : 0.0f;
     for (int t0 = 0; t0 < T; t0 += kScoreTok) {
+        const int nt = min(kScoreTok, T - t0);
+        __syncthreads();
+        for (int q = threadIdx.x; q < nt * nchunk; q += blockDim.x) {
+            const int i = q / nchunk, c = q % nchunk;
+            xs[i * nchunk + c] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + i) * d) + c);
+        }
+        __syncthreads();
         float acc[kScoreTok];
 #pragma unroll
         for (int i = 0; i < kScoreTok; i++) acc[i] = 0.0f;
-        const int nt = min(kScoreTok, T - t0);
-        for (int c = lane; c < nchunk; c += 32) {
-            const uint4 w = __ldg(wrow + c);
-            float wf[8];
-            const uint32_t wu[4] = {w.x, w.y, w.z, w.w};
+        for (int c0 = 0; c0 < nchunk; c0 += 32 * kScoreChunks) {
+            uint4 w[kScoreChunks];
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
-                wf[2 * q] = __uint_as_float(wu[q] << 16);
-                wf[2 * q + 1] = __uint_as_float(wu[q] & 0xFFFF0000u);
+            for (int j = 0; j < kScoreChunks; j++) {
+                const int c = c0 + lane + 32 * j;
+                w[j] = c < nchunk ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int i = 0; i < kScoreTok; i++) {
-                if (i < nt) {
-                    const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(
-                                               x + (size_t)(t0 + i) * d) + c);
-                    const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
-                    float a = acc[i];
+                if (i >= nt) break;
+                float a = acc[i];
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        a = fmaf(__uint_as_float(xu[q] << 16), wf[2 * q], a);
-                        a = fmaf(__uint_as_float(xu[q] & 0xFFFF0000u), wf[2 * q + 1], a);
+                for (int j = 0; j < kScoreChunks; j++) {
+                    const int c = c0 + lane + 32 * j;
+                    if (c < nchunk) {
+                        const uint4 xv = xs[i * nchunk + c];
+                        const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
+                        const uint32_t wu[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            a = fmaf(__uint_as_float(xu[q] << 16), __uint_as_float(wu[q] << 16), a);
+                            a = fmaf(__uint_as_float(xu[q] & 0xFFFF0000u), __uint_as_float(wu[q] & 0xFFFF0000u), a);
+                        }
                     }
-                    acc[i] = a;
                 }
+                acc[i] = a;
             }
         }
 #pragma unroll
@@ -71,7 +83,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
             acc[i] = v;
         }
-        if (lane < nt) {
+        if (e < E && lane < nt) {
             float logit = acc[0];
 #pragma unroll
             for (int i = 1; i < kScoreTok; i++)
@@ -83,106 +95,44 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
     }
 }
 
-// -------------------------------------------------------------------------------- top-k
-// (value, index) order: larger value first; equal values -> lower index first.
-__device__ __forceinline__ bool beats(float va, int ia, float vb, int ib)
-{
-    return va > vb || (va == vb && ia < ib);
-}
-
-struct TopkArgs {
-    int T, E, k, renorm;
-    float routed_scale;
-    const float *sc, *ch;
-    int32_t *idx;
-    float *weight;
+// -------------------------------------------------------------------------------- token -> expert map
+struct MapArgs {
+    int T, E, k;
+    const int32_t *idx;
     int32_t *offsets, *perm;
     int32_t *chunk_counts, *local_rank;
     int32_t *status;
 };
 
-// blockDim = 1024 (32 warps); block b owns tokens [64b, 64b+64): its slots are chunk b.
-__global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
+// One chunk of 64 tokens (k*64 <= 1024 slots) with 1024 threads: per-expert counts and
+// stable ranks; when `single`, also the scan to offsets and the scatter to perm.
+__device__ void map_chunk(const MapArgs &a, int chunk, bool single, int32_t *cnt, int32_t *slot_e,
+                          int32_t *scan_tmp)
 {
-    __shared__ int32_t cnt[kMaxExperts];
-    __shared__ int32_t slot_e[kChunkTokens * kMaxTopK];
-    __shared__ int32_t scan_tmp[32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t_begin = blockIdx.x * kChunkTokens;
-    const int t_end = min(a.T, t_begin + kChunkTokens);
     const int E = a.E, k = a.k;
-
+    const int t_begin = chunk * kChunkTokens, t_end = min(a.T, t_begin + kChunkTokens);
+    const int nslots = (t_end - t_begin) * k;
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
-
-    // ---- selection: warp per token
-    for (int t = t_begin + warp; t < t_end; t += 32) {
-        const float *chr = a.ch + (size_t)t * E;
-        float v[kMaxExperts / 32];
-#pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; i++) {
-            const int e = lane + 32 * i;
-            // -0.0 and +0.0 compare equal in the repeated maximum; canonicalise to +0.0.
-            v[i] = (e < E) ? (chr[e] + 0.0f) : -INFINITY;
+    if (threadIdx.x < nslots) {
+        int e = a.idx[(size_t)t_begin * k + threadIdx.x];
+        if (e < 0 || e >= E) {
+            set_status(a.status, K3MOE_DEV_BAD_INDEX);
+            e = 0;
         }
-        uint32_t taken = 0;
-        int my_idx = -1;
-        for (int j = 0; j < k; j++) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < kMaxExperts / 32; i++) {
-                const int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u) && (bi == 0x7fffffff || beats(v[i], e, bv, bi))) {
-                    bv = v[i];
-                    bi = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (oi != 0x7fffffff && (bi == 0x7fffffff || beats(ov, oi, bv, bi))) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            // bi is now the winner on every lane; its owner marks it taken.
-            if (bi >= 0 && bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-            if (lane == j) my_idx = bi;
-        }
-        // weights: unbiased sc of the chosen experts, renormalised in rank order
-        float w = 0.0f;
-        if (lane < k) {
-            if (my_idx < 0 || my_idx >= E) {      // cannot happen with k <= E; stay in bounds
-                set_status(a.status, K3MOE_DEV_BAD_INDEX);
-                my_idx = 0;
-            }
-            w = a.sc[(size_t)t * E + my_idx];
-        }
-        float s = 0.0f;
-        for (int j = 0; j < k; j++) s += __shfl_sync(0xffffffffu, w, j);
-        if (lane < k) {
-            if (a.renorm && s > 0.0f) w = w / s;
-            w = w * a.routed_scale;
-            a.idx[(size_t)t * k + lane] = my_idx;
-            a.weight[(size_t)t * k + lane] = w;
-            slot_e[(t - t_begin) * k + lane] = my_idx;
-        }
+        slot_e[threadIdx.x] = e;
     }
     __syncthreads();
-
-    // ---- chunk-local counts and stable ranks (slot order = t*k + j), warp by warp
-    const int nslots = (t_end - t_begin) * k;
     int my_rank = 0, my_e = -1;
     for (int w = 0; w < 32; w++) {
+        if (w * 32 >= nslots) break;
         if (warp == w) {
             const int s = w * 32 + lane;
             const bool valid = s < nslots;
             const int e = valid ? slot_e[s] : -1 - lane;   // invalid lanes never match
             const uint32_t m = __match_any_sync(0xffffffffu, e);
             if (valid) {
-                const uint32_t lower = m & ((1u << lane) - 1u);
-                my_rank = cnt[e] + __popc(lower);
+                my_rank = cnt[e] + __popc(m & ((1u << lane) - 1u));
                 my_e = e;
             }
             __syncwarp();
@@ -190,14 +140,11 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
         }
         __syncthreads();
     }
-
-    if (gridDim.x == 1) {
-        // single chunk: offsets = exclusive scan of cnt, then scatter
+    if (single) {
         int run = 0;
         for (int base = 0; base < E; base += blockDim.x) {
             const int e = base + threadIdx.x;
             const int v = (e < E) ? cnt[e] : 0;
-            // block-wide exclusive scan of v
             int incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -230,11 +177,101 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
     } else {
         if (my_e >= 0) a.local_rank[(size_t)t_begin * k + threadIdx.x] = my_rank;
         for (int e = threadIdx.x; e < E; e += blockDim.x)
-            a.chunk_counts[(size_t)blockIdx.x * E + e] = cnt[e];
+            a.chunk_counts[(size_t)chunk * E + e] = cnt[e];
     }
 }
 
-// -------------------------------------------------------------------------------- multi-chunk map
+// -------------------------------------------------------------------------------- top-k
+// Orderable image of a float: larger float -> larger unsigned (after -0.0 -> +0.0).
+__device__ __forceinline__ uint32_t orderable(float v)
+{
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+struct TopkArgs {
+    int T, E, k, renorm;
+    float routed_scale;
+    const float *sc, *ch;
+    int32_t *idx;
+    float *weight;
+    int32_t *done;          // last-block counter (kept at zero between calls)
+    MapArgs map;
+};
+
+// blockDim = 1024; block t owns token t.  Key = (orderable(ch) << 32) | ~index, so a
+// descending sort orders by ch and, among equal ch, by ascending index -- the order the
+// repeated maximum with a strict comparison produces.
+__global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
+{
+    __shared__ uint64_t keys[1024];
+    __shared__ int32_t cnt[kMaxExperts];
+    __shared__ int32_t slot_e[kChunkTokens * kMaxTopK];
+    __shared__ int32_t scan_tmp[32];
+    __shared__ int last;
+    const int i = threadIdx.x, lane = i & 31;
+    const int t = blockIdx.x, E = a.E, k = a.k;
+    uint64_t key = 0;
+    if (i < E) key = ((uint64_t)orderable(a.ch[(size_t)t * E + i]) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)i);
+    for (int size = 2; size <= 1024; size <<= 1) {
+        const bool desc = (i & size) == 0;
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            uint64_t other;
+            if (stride >= 32) {
+                keys[i] = key;
+                __syncthreads();
+                other = keys[i ^ stride];
+                __syncthreads();
+            } else {
+                other = __shfl_xor_sync(0xffffffffu, key, stride);
+            }
+            const bool lower = (i & stride) == 0;
+            const bool keep_max = (desc == lower);
+            key = keep_max ? (key > other ? key : other) : (key < other ? key : other);
+        }
+    }
+    // thread r < k now holds the rank-r key
+    if (i < 32) {
+        int e = -1;
+        float w = 0.0f;
+        if (i < k) {
+            e = (int)(0xFFFFFFFFu - (uint32_t)key);
+            if (e < 0 || e >= E) {                 // cannot happen with k <= E; stay in bounds
+                set_status(a.map.status, K3MOE_DEV_BAD_INDEX);
+                e = 0;
+            }
+            w = a.sc[(size_t)t * E + e];
+        }
+        float s = 0.0f;
+        for (int j = 0; j < k; j++) s += __shfl_sync(0xffffffffu, w, j);
+        if (i < k) {
+            if (a.renorm && s > 0.0f) w = w / s;
+            w = w * a.routed_scale;
+            a.idx[(size_t)t * k + i] = e;
+            a.weight[(size_t)t * k + i] = w;
+        }
+    }
+    (void)lane;
+    if (a.done == nullptr) return;                 // the map is built by perm_count
+    // the last block to finish builds the map of all (at most 64) tokens
+    __threadfence();
+    __syncthreads();
+    if (i == 0) last = (atomicAdd(a.done, 1) == (int)gridDim.x - 1);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    map_chunk(a.map, 0, true, cnt, slot_e, scan_tmp);
+    if (i == 0) *a.done = 0;
+}
+
+__global__ void __launch_bounds__(1024) perm_count_kernel(MapArgs a)
+{
+    __shared__ int32_t cnt[kMaxExperts];
+    __shared__ int32_t slot_e[kChunkTokens * kMaxTopK];
+    __shared__ int32_t scan_tmp[32];
+    map_chunk(a, blockIdx.x, gridDim.x == 1, cnt, slot_e, scan_tmp);
+}
+
 // One thread per expert runs over the chunks (exclusive scan down a column), then a
 // block-wide scan over experts turns totals into offsets, which are added back.
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int n_chunks, int E, int total_slots,
@@ -311,28 +348,41 @@ cudaError_t launch_route(const k3moe_config &c, int T, const uint16_t *x, const 
     }
     float *sc = reinterpret_cast<float *>(ws + L.sc);
     float *ch = reinterpret_cast<float *>(ws + L.ch);
-    timing_begin("router_scores", s);
-    router_scores_kernel<<<(E + kScoreWarps - 1) / kScoreWarps, kScoreWarps * 32, 0, s>>>(
-        T, c.d, E, x, wr, bias, sc, ch);
-    count_launch();
-    timing_end("router_scores", s);
-
-    TopkArgs a{T, E, k, c.renorm, c.routed_scale, sc, ch, idx, weight, offsets, perm,
-               reinterpret_cast<int32_t *>(ws + L.chunk_counts),
-               reinterpret_cast<int32_t *>(ws + L.local_rank), status};
+    {
+        static size_t smem_set = 0;
+        const size_t smem = (size_t)kScoreTok * c.d * 2;
+        if (smem > smem_set) {
+            cudaFuncSetAttribute(router_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            smem_set = smem;
+        }
+        timing_begin("router_scores", s);
+        router_scores_kernel<<<(E + kScoreWarps - 1) / kScoreWarps, kScoreWarps * 32, smem, s>>>(
+            T, c.d, E, x, wr, bias, sc, ch);
+        count_launch();
+        timing_end("router_scores", s);
+    }
+    MapArgs m{T, E, k, idx, offsets, perm, reinterpret_cast<int32_t *>(ws + L.chunk_counts),
+              reinterpret_cast<int32_t *>(ws + L.local_rank), status};
+    // status block word 4 is the last-block counter of router_topk
+    TopkArgs a{T, E, k, c.renorm, c.routed_scale, sc, ch, idx, weight,
+               L.n_chunks == 1 ? status + 4 : nullptr, m};
     timing_begin("router_topk", s);
-    router_topk_kernel<<<L.n_chunks, 1024, 0, s>>>(a);
+    router_topk_kernel<<<T, 1024, 0, s>>>(a);
     count_launch();
     timing_end("router_topk", s);
     if (L.n_chunks > 1) {
         int32_t *base = reinterpret_cast<int32_t *>(ws + L.chunk_base);
+        timing_begin("perm_count", s);
+        perm_count_kernel<<<L.n_chunks, 1024, 0, s>>>(m);
+        count_launch();
+        timing_end("perm_count", s);
         timing_begin("perm_scan", s);
-        perm_scan_kernel<<<1, 1024, 0, s>>>(L.n_chunks, E, T * k, a.chunk_counts, base, offsets);
+        perm_scan_kernel<<<1, 1024, 0, s>>>(L.n_chunks, E, T * k, m.chunk_counts, base, offsets);
         count_launch();
         timing_end("perm_scan", s);
         timing_begin("perm_scatter", s);
         perm_scatter_kernel<<<(T * k + 255) / 256, 256, 0, s>>>(T * k, k, E, idx, base,
-                                                                 a.local_rank, perm);
+                                                                 m.local_rank, perm);
         count_launch();
         timing_end("perm_scatter", s);
     }
