@@ -113,7 +113,7 @@ k3moe_status k3moe_validate_config(const k3moe_config *cfg) { return check_confi
 size_t k3moe_packed_bytes(const k3moe_config *cfg)
 {
     if (check_config(cfg) != K3MOE_OK) return 0;
-    return (size_t)cfg->n_experts * expert_bytes(cfg->d, cfg->f);
+    return packed_table_bytes(cfg->n_experts, cfg->d, cfg->f);
 }
 
 k3moe_status k3moe_workspace_bytes(const k3moe_config *cfg, int32_t T_max, size_t *bytes)
@@ -137,7 +137,7 @@ static k3moe_status pack_checks(const k3moe_config *cfg, int32_t lo, int32_t n, 
     if (!p1 || !s1 || !p3 || !s3 || !p2 || !s2 || !table) return K3MOE_EINVAL;
     if (!aligned(p1, 16) || !aligned(p3, 16) || !aligned(p2, 16) || !aligned(table, 256))
         return K3MOE_EALIGN;
-    if (table_bytes < (size_t)cfg->n_experts * expert_bytes(cfg->d, cfg->f)) return K3MOE_ESHAPE;
+    if (table_bytes < packed_table_bytes(cfg->n_experts, cfg->d, cfg->f)) return K3MOE_ESHAPE;
     return K3MOE_OK;
 }
 
@@ -209,11 +209,11 @@ k3moe_status k3moe_forward(const k3moe_config *cfg, int32_t T, const uint16_t *x
         return K3MOE_EALIGN;
     if (cfg->n_shared > 0 && (!aligned(sh_w1, 16) || !aligned(sh_w3, 16) || !aligned(sh_w2, 16)))
         return K3MOE_EALIGN;
-    if (table_bytes < (size_t)cfg->n_experts * expert_bytes(cfg->d, cfg->f)) return K3MOE_ESHAPE;
+    if (table_bytes < packed_table_bytes(cfg->n_experts, cfg->d, cfg->f)) return K3MOE_ESHAPE;
     if (!ws || !aligned(ws, 256)) return K3MOE_EWORKSPACE;
     const WsLayout L = ws_layout(*cfg, T);
     if (ws_bytes < L.total) return K3MOE_EWORKSPACE;
-    cudaError_t e = launch_forward_gemv(*cfg, T, x, idx, weight, offsets, perm,
+    cudaError_t e = launch_forward(*cfg, T, x, idx, weight, offsets, perm,
                                         static_cast<const uint8_t *>(expert_table), sh_w1, sh_w3,
                                         sh_w2, out, static_cast<uint8_t *>(ws), L, (cudaStream_t)stream);
     return e == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;

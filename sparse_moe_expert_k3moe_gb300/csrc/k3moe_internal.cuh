@@ -17,6 +17,9 @@
 //   - bytes [8192, 8704): E8M0 scale of (row r, group c) at 8192 + r * 4 + c.
 //   Tiles are contiguous, so one bulk copy moves a tile, and a gate/up K step
 //   (both matrices) is one 17408-byte copy.  Bytes per expert = 3*f*d*17/32.
+// After the E expert payloads comes a trailer of kTrailerBytes per expert: for each
+// matrix (W1, W3, W2) and each 128-row block, the largest E8M0 byte of the block other
+// than 255, as a uint32 (the tensor-core path scales the block's weights by it).
 #pragma once
 
 #include <cstddef>
@@ -41,6 +44,7 @@ constexpr int kMaxTopK = 16;
 constexpr int kMaxShared = 8;
 constexpr int kMaxWidth = 8192;
 constexpr int kChunkTokens = 64;      // tokens per top-k block; its slots form one chunk
+constexpr int kTrailerBytes = 1024;   // per-expert row-block scale summary (<= 3*64 uint32)
 
 __host__ __device__ inline size_t gateup_block_bytes(int d, int f)
 {
@@ -53,6 +57,18 @@ __host__ __device__ inline size_t down_block_bytes(int d, int f)
 __host__ __device__ inline size_t expert_bytes(int d, int f)
 {
     return gateup_block_bytes(d, f) + down_block_bytes(d, f);
+}
+// Whole table: E payloads, then E trailers.
+__host__ __device__ inline size_t packed_table_bytes(int E, int d, int f)
+{
+    return (size_t)E * (expert_bytes(d, f) + kTrailerBytes);
+}
+// Trailer word of (expert e, matrix m in {0: W1, 1: W3, 2: W2}, row block rb).
+__host__ __device__ inline size_t trailer_offset(int E, int d, int f, int e, int m, int rb)
+{
+    const int nrb_f = f / kTileRows;
+    const int idx = (m < 2) ? m * nrb_f + rb : 2 * nrb_f + rb;
+    return (size_t)E * expert_bytes(d, f) + (size_t)e * kTrailerBytes + (size_t)idx * 4;
 }
 
 // Device status word and abort flag live in the first 256 bytes of the workspace.
@@ -73,6 +89,13 @@ inline int ksplit_for(int ktiles, int T, int k)
     return 1;
 }
 
+// Forward path: the tensor-core GEMMs once an expert sees on average at least 8 tokens
+// (T*k >= 8*E) and T >= 32; the streamed mat-vecs otherwise.
+inline bool use_gemm_path(const k3moe_config &c, int T)
+{
+    return T >= 32 && (long long)T * c.top_k >= 8LL * c.n_experts;
+}
+
 // Workspace regions (byte offsets), sized for one call's T.
 struct WsLayout {
     size_t status;
@@ -87,7 +110,10 @@ struct WsLayout {
     size_t hp;                   // decode: SiTU output as hi and lo planes [2][rows][f] 16-bit
     size_t arrive;               // decode: per (unit, row block) K-part arrival counters
     size_t ys;                   // decode: y partials [P_dn][rows][d] f32
+    size_t xg;                   // prefill: routed activations in perm order [T*k][d] f16
+    size_t units;                // prefill: unit list [E+S][4], item prefixes, unit count
     size_t total;
+    bool gemm;                   // which forward path this T takes
     int n_chunks;
     int p_gu, p_dn;              // K splits of the gate/up and down items
 };
@@ -100,8 +126,9 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     const size_t E = (size_t)c.n_experts, k = (size_t)c.top_k, S = (size_t)c.n_shared;
     const size_t slots = (size_t)T * k;
     L.n_chunks = (T + kChunkTokens - 1) / kChunkTokens;
-    L.p_gu = ksplit_for(c.d / kTileK, T, c.top_k);
-    L.p_dn = ksplit_for(c.f / kTileK, T, c.top_k);
+    L.gemm = use_gemm_path(c, T);
+    L.p_gu = L.gemm ? 1 : ksplit_for(c.d / kTileK, T, c.top_k);
+    L.p_dn = L.gemm ? 1 : ksplit_for(c.f / kTileK, T, c.top_k);
     size_t o = 0;
     L.status = o; o += 256;
     L.sc = o; o = align256(o + (size_t)T * E * 4);
@@ -113,10 +140,12 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     L.inv = o; o = align256(o + slots * 4);
     L.tok_scale = o; o = align256(o + (size_t)T * 2 * 4);
     const size_t rows = slots + S * (size_t)T;
-    L.gu = o; o = align256(o + (L.p_gu > 1 ? rows * (size_t)c.f * 4 * 2 * L.p_gu : 0));
-    L.hp = o; o = align256(o + rows * (size_t)c.f * 2 * 2);
-    L.arrive = o; o = align256(o + (E + S) * (size_t)(c.f / kTileRows) * 4);
-    L.ys = o; o = align256(o + rows * (size_t)c.d * 4 * L.p_dn);
+    L.gu = o; o = align256(o + (!L.gemm && L.p_gu > 1 ? rows * (size_t)c.f * 4 * 2 * L.p_gu : 0));
+    L.hp = o; o = align256(o + rows * (size_t)c.f * 2 * (L.gemm ? 1 : 2));
+    L.arrive = o; o = align256(o + (L.gemm ? 0 : (E + S) * (size_t)(c.f / kTileRows) * 4));
+    L.ys = o; o = align256(o + (L.gemm ? 0 : rows * (size_t)c.d * 4 * L.p_dn));
+    L.xg = o; o = align256(o + (L.gemm ? slots * (size_t)c.d * 2 : 0));
+    L.units = o; o = align256(o + (L.gemm ? (4 * (E + S) + 2 * (E + S + 1) + 1) * 4 : 0));
     L.total = o;
     return L;
 }
@@ -138,11 +167,34 @@ cudaError_t launch_unpack(const k3moe_config &c, int expert_lo, int n, const uin
 cudaError_t launch_route(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
                          const float *bias, int32_t *idx, float *weight, int32_t *offsets,
                          int32_t *perm, uint8_t *ws, const WsLayout &L, cudaStream_t s);
+cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x, const int32_t *idx,
+                                const float *weight, const int32_t *offsets, const int32_t *perm,
+                                const uint8_t *table, const uint16_t *sh_w1, const uint16_t *sh_w3,
+                                const uint16_t *sh_w2, float *out, uint8_t *ws, const WsLayout &L,
+                                cudaStream_t s);
+// Either path, as the layout chose it.
+inline cudaError_t launch_forward(const k3moe_config &c, int T, const uint16_t *x, const int32_t *idx,
+                                  const float *weight, const int32_t *offsets, const int32_t *perm,
+                                  const uint8_t *table, const uint16_t *sh_w1, const uint16_t *sh_w3,
+                                  const uint16_t *sh_w2, float *out, uint8_t *ws, const WsLayout &L,
+                                  cudaStream_t s);
 cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
                                 const int32_t *idx, const float *weight, const int32_t *offsets,
                                 const int32_t *perm, const uint8_t *table, const uint16_t *sh_w1,
                                 const uint16_t *sh_w3, const uint16_t *sh_w2, float *out,
                                 uint8_t *ws, const WsLayout &L, cudaStream_t s);
+
+inline cudaError_t launch_forward(const k3moe_config &c, int T, const uint16_t *x, const int32_t *idx,
+                                  const float *weight, const int32_t *offsets, const int32_t *perm,
+                                  const uint8_t *table, const uint16_t *sh_w1, const uint16_t *sh_w3,
+                                  const uint16_t *sh_w2, float *out, uint8_t *ws, const WsLayout &L,
+                                  cudaStream_t s)
+{
+    return L.gemm ? launch_forward_gemm(c, T, x, idx, weight, offsets, perm, table, sh_w1, sh_w3, sh_w2,
+                                        out, ws, L, s)
+                  : launch_forward_gemv(c, T, x, idx, weight, offsets, perm, table, sh_w1, sh_w3, sh_w2,
+                                        out, ws, L, s);
+}
 
 // ----------------------------------------------------------------------------------- device helpers
 #ifdef __CUDACC__

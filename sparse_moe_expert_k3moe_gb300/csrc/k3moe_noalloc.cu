@@ -77,7 +77,7 @@ extern "C" k3moe_status k3moe_forward_noalloc(
     if (cfg->n_shared > 0 &&
         (!is_aligned(sh_w1, 16) || !is_aligned(sh_w3, 16) || !is_aligned(sh_w2, 16)))
         return K3MOE_EALIGN;
-    if (table_bytes < (size_t)cfg->n_experts * expert_bytes(cfg->d, cfg->f)) return K3MOE_ESHAPE;
+    if (table_bytes < packed_table_bytes(cfg->n_experts, cfg->d, cfg->f)) return K3MOE_ESHAPE;
     const WsLayout L = ws_layout(*cfg, T);
     if (L.total > kNoAllocScratchBytes) return K3MOE_EWORKSPACE;   // T too large for the array
 
@@ -86,7 +86,7 @@ extern "C" k3moe_status k3moe_forward_noalloc(
     cudaStream_t s = (cudaStream_t)stream;
     uint8_t *ws = static_cast<uint8_t *>(scratch);
     if (cudaMemsetAsync(ws + L.status, 0, sizeof(StatusBlock), s) != cudaSuccess) return K3MOE_ECUDA;
-    cudaError_t e = launch_forward_gemv(*cfg, T, x, idx, weight, offsets, perm,
+    cudaError_t e = launch_forward(*cfg, T, x, idx, weight, offsets, perm,
                                         static_cast<const uint8_t *>(expert_table), sh_w1, sh_w3,
                                         sh_w2, out, ws, L, s);
     if (e != cudaSuccess) return K3MOE_ECUDA;

@@ -7,7 +7,7 @@ namespace k3moe {
 namespace {
 
 struct PackArgs {
-    int d, f, expert_lo, n;
+    int d, f, E, expert_lo, n;
     const uint8_t *w1p, *w1s, *w3p, *w3s, *w2p, *w2s;   // checkpoint side
     uint8_t *table;                                     // packed side (full table base)
     int32_t *status;
@@ -78,7 +78,13 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
         for (int t = 0; t < 4; t++)
             *reinterpret_cast<uint32_t *>(dst + dn + (size_t)t * 8) = lane_word(v, t);
         dst[ds] = sb;
-        if (sb == 255 && a.status) set_status(a.status, K3MOE_DEV_NAN_SCALE);
+        if (sb == 255) {
+            if (a.status) set_status(a.status, K3MOE_DEV_NAN_SCALE);
+        } else {
+            atomicMax(reinterpret_cast<unsigned int *>(
+                          a.table + trailer_offset(a.E, a.d, a.f, a.expert_lo + e, mat, row / kTileRows)),
+                      (unsigned int)sb);
+        }
     }
 }
 
@@ -131,8 +137,12 @@ cudaError_t launch_pack(const k3moe_config &c, int expert_lo, int n, const uint8
                         int32_t *status, cudaStream_t s)
 {
     if (n == 0) return cudaSuccess;
-    PackArgs a{c.d, c.f, expert_lo, n, w1p, w1s, w3p, w3s, w2p, w2s, table, status};
+    PackArgs a{c.d, c.f, c.n_experts, expert_lo, n, w1p, w1s, w3p, w3s, w2p, w2s, table, status};
     const size_t work = (size_t)3 * c.f * c.d / 32 * (size_t)n;
+    cudaError_t e = cudaMemsetAsync(table + (size_t)c.n_experts * expert_bytes(c.d, c.f) +
+                                        (size_t)expert_lo * kTrailerBytes,
+                                    0, (size_t)n * kTrailerBytes, s);
+    if (e != cudaSuccess) return e;
     timing_begin("pack_mxfp4", s);
     pack_kernel<<<grid_for(work), 256, 0, s>>>(a);
     count_launch();

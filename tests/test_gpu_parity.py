@@ -111,7 +111,30 @@ def test_pack_roundtrip_every_code_and_scale(k3):
     rc, code = k3.k3moe_device_status(ws)
     assert rc == 0 and code & k3.DEV_NAN_SCALE      # byte 255 present: warning, not error
     # the table is a pure relayout: same multiset of bytes
-    assert table.numel() == w.E * w.expert_bytes
+    assert table.numel() == w.E * (w.expert_bytes + 1024)
+
+
+def test_pack_records_block_scale_maxima(k3):
+    """The table's trailer: per expert, matrix and 128-row block, the largest scale byte
+    other than 255."""
+    w = ki.Workload("trail", T=1, d=256, f=256, E=2, k=1, S=0, exp_lo=-9, exp_hi=-1, seed=9)
+    cfg = k3.k3moe_config(**w.config_kwargs())
+    blk = ki.make_experts_block(w, 0, w.E)
+    blk["w1_scale"][1, 5, 3] = 255                 # a NaN byte never counts as the maximum
+    blk["w2_scale"][0, 130, 0] = 140
+    table = torch.zeros(k3.k3moe_packed_bytes(cfg), dtype=torch.uint8, device="cuda")
+    k3.k3moe_pack_mxfp4(cfg, 0, w.E, *(dev(blk[n]) for n in ki.EXPERT_TENSORS), table)
+    torch.cuda.synchronize()
+    tb = host(table)
+    trailer = tb[w.E * w.expert_bytes:].view(np.uint32).reshape(w.E, 256)
+    for e in range(w.E):
+        col = 0
+        for m in ("w1", "w3", "w2"):
+            sc = blk[f"{m}_scale"][e]
+            for rb in range(sc.shape[0] // 128):
+                blkv = sc[rb * 128:(rb + 1) * 128]
+                assert trailer[e, col] == blkv[blkv != 255].max()
+                col += 1
 
 
 def test_pack_roundtrip_full_shape(k3):
@@ -127,7 +150,7 @@ def test_pack_roundtrip_full_shape(k3):
     torch.cuda.synchronize()
     for n in ki.EXPERT_TENSORS:
         np.testing.assert_array_equal(host(d_out[n]), blk[n])
-    assert k3.k3moe_packed_bytes(cfg) == 896 * 17547264
+    assert k3.k3moe_packed_bytes(cfg) == 896 * (17547264 + 1024)
 
 
 # ----------------------------------------------------------------------------- small layers, all outputs
@@ -145,7 +168,19 @@ SMALL_CASES = [
 ]
 
 
-@pytest.mark.parametrize("w", SMALL_CASES, ids=lambda w: w.name)
+# Cases on the tensor-core path (average >= 8 tokens per expert and T >= 32): several
+# 256-token tiles per expert with ragged tails, skewed routing, several row blocks.
+GEMM_CASES = [
+    ki.Workload("gemm_multi_tile", T=1100, d=256, f=256, E=8, k=2, S=1, exp_lo=-7, exp_hi=-3, seed=70),
+    ki.Workload("gemm_bias", T=300, d=384, f=256, E=12, k=3, S=2, exp_lo=-9, exp_hi=-5, seed=71,
+                zipf_bias=True),
+    ki.Workload("gemm_wide", T=64, d=1024, f=640, E=40, k=16, S=1, exp_lo=-10, exp_hi=-6, seed=72),
+    ki.Workload("gemm_outliers", T=520, d=256, f=384, E=16, k=4, S=2, exp_lo=-8, exp_hi=-4, seed=73,
+                outlier_frac=0.05),
+]
+
+
+@pytest.mark.parametrize("w", SMALL_CASES + GEMM_CASES, ids=lambda w: w.name)
 def test_small_layer_parity(k3, w):
     from k3moe_inputs.device import build_layer
     layer = build_layer(w)
