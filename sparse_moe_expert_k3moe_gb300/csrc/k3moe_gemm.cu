@@ -16,21 +16,26 @@
 //   gemm<DN>     y = W2 h; out[t] += w_slot * y (routed) or += y (shared) with fp32
 //                atomics onto out (zeroed first).
 //
-// One work item = 128 weight rows of one unit x up to 256 of its tokens x the whole K.
-// Warp roles in a block (one block per SM):
+// One work item = 128 weight rows of one unit x up to 128 (gate/up) or 256 (down) of its
+// tokens x the whole K.  Warp roles in a block (one block per SM):
 //   warp 0       producer: TMA 2-D loads of the B tiles (64 columns x 16 rows per copy)
 //                and, for bf16 shared experts, of the A tiles;
 //   warp 1       MMA: one thread issues tcgen05.mma (kind::f16, M=128, N=tile, K=16)
-//                into fp32 accumulators in tensor memory (g at column 0, u at 256);
-//   warps 2-9    dequant: packed MXFP4 straight from global memory to f16 A tiles in
-//                shared memory (128-byte swizzle, K-major) -- the E2M1 pair decoded by
-//                the hardware conversion, times 2^(b - bmax + 13) where bmax is the
-//                largest scale of the 128-row block (the packed table's trailer), so
-//                every value is exact in f16 while the block's scales span at most 36
-//                binades; the epilogue multiplies by 2^(bmax - 140);
+//                into fp32 accumulators in tensor memory, two buffers of 256 columns
+//                (gate/up: g at +0, u at +128), so one item's MMAs overlap the previous
+//                item's epilogue;
+//   warps 2-9    dequant: packed MXFP4 tiles from shared memory to f16 A tiles
+//                (128-byte swizzle, K-major) -- the E2M1 pair decoded by the hardware
+//                conversion, times 2^(b - bmax + 13) where bmax is the largest scale of
+//                the 128-row block (the packed table's trailer), so every value is exact
+//                in f16 while the block's scales span at most 36 binades; the epilogue
+//                multiplies by 2^(bmax - 140);
 //   warps 10-13  epilogue: tcgen05.ld the accumulators (warp w reads lanes 32(w%4)..),
-//                apply the scales, SiTU or the weighted combine, store.
-// Stage ring: kStg stages of (A, B); the MMA warp releases a stage with tcgen05.commit.
+//                apply the scales, SiTU or the weighted combine, store;
+//   warp 14      packed-weight producer: one bulk copy per 128-column packed tile (pair),
+//                kStgP tiles ahead of the dequant warps.
+// Rings: packed tiles (kStgP), f16 A stages (kStgA) and B stages (kStgB); the MMA thread
+// releases an A and a B stage with one tcgen05.commit each.
 // Every wait is bounded by a clock limit; a timeout sets the status word and the
 // roles drop out.
 #include <cuda.h>
@@ -43,11 +48,12 @@
 namespace k3moe {
 namespace {
 
-constexpr int kBM = 128, kBK = 64, kBNMax = 256;
-constexpr int kStg = 3;
+constexpr int kBM = 128, kBK = 64;
+constexpr int kStgP = 3, kStgA = 2, kStgB = 3;               // packed, A and B rings
 constexpr int kNumDq = 8;
 constexpr int kWarpProd = 0, kWarpMma = 1, kWarpDq0 = 2, kWarpEpi0 = 2 + kNumDq, kNumEpi = 4;
-constexpr int kGemmThreads = (kWarpEpi0 + kNumEpi) * 32;   // 448
+constexpr int kWarpPack = kWarpEpi0 + kNumEpi;                 // 14
+constexpr int kGemmThreads = (kWarpPack + 1) * 32;             // 480
 constexpr long long kWaitCyc = 4000000000ll;
 constexpr int kTmemCols = 512;
 
@@ -56,10 +62,13 @@ enum { kGU = 0, kDN = 1 };
 template <int MODE>
 struct GG {
     static constexpr int kMats = MODE == kGU ? 2 : 1;
-    static constexpr int kABytes = kMats * kBM * kBK * 2;     // f16/bf16 A tiles of a stage
-    static constexpr int kBBytes = kBNMax * kBK * 2;          // B tile of a stage
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kSmem = kStg * kStageBytes + 1024;
+    // tokens per tile: gate/up keeps two accumulators (g, u) per buffer, so 128 tokens
+    // fit twice in the 512 TMEM columns; down keeps one
+    static constexpr int kBNMax = MODE == kGU ? 128 : 256;
+    static constexpr int kPBytes = kMats * kTileBytes;         // packed tile (pair) of 128 columns
+    static constexpr int kABytes = kMats * kBM * kBK * 2;      // f16/bf16 A tiles of a stage
+    static constexpr int kBBytes = kBNMax * kBK * 2;           // B tile of a stage
+    static constexpr int kSmem = kStgP * kPBytes + kStgA * kABytes + kStgB * kBBytes + 2048;
 };
 
 // ---------------------------------------------------------------------------------- PTX
@@ -230,9 +239,9 @@ __global__ void __launch_bounds__(1024) gemm_units_kernel(UnitsArgs a)
         for (int u = 0; u < n; u++) {
             a.prefix_gu[u] = pg;
             a.prefix_dn[u] = pd;
-            const int nt = (a.units[4 * u + 3] + kBNMax - 1) / kBNMax;
-            pg += nt * a.rb_gu;
-            pd += nt * a.rb_dn;
+            const int ntok = a.units[4 * u + 3];
+            pg += (ntok + GG<kGU>::kBNMax - 1) / GG<kGU>::kBNMax * a.rb_gu;
+            pd += (ntok + GG<kDN>::kBNMax - 1) / GG<kDN>::kBNMax * a.rb_dn;
         }
         a.prefix_gu[n] = pg;
         a.prefix_dn[n] = pd;
@@ -352,12 +361,13 @@ __device__ __forceinline__ GItem gitem(const GemmArgs &a, int n_units, int i)
     it.id = u[1];
     it.tok0 = u[2];
     it.ntok = u[3];
-    const int ntiles = max(1, (it.ntok + kBNMax - 1) / kBNMax);
+    constexpr int BN = GG<MODE>::kBNMax;
+    const int ntiles = max(1, (it.ntok + BN - 1) / BN);
     const int j = i - a.prefix[lo];
     const int nt = j % ntiles;                     // token tile fastest: the block's weights stay hot in L2
     it.rb = j / ntiles;
-    it.n0 = nt * kBNMax;
-    it.ncols = min(kBNMax, it.ntok - it.n0);
+    it.n0 = nt * BN;
+    it.ncols = min(BN, it.ntok - it.n0);
     it.bn = (it.ncols + 15) & ~15;
     return it;
 }
@@ -371,12 +381,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 {
     extern __shared__ __align__(1024) uint8_t gsm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t full_a[kStg], full_b[kStg], empty[kStg], acc_full, acc_empty;
+    constexpr int kMats = GG<MODE>::kMats;
+    constexpr int kPBytes = GG<MODE>::kPBytes, kABytes = GG<MODE>::kABytes, kBBytes = GG<MODE>::kBBytes;
+    uint8_t *smA = sm;                                   // kStgA x kABytes (1024-aligned)
+    uint8_t *smB = smA + kStgA * kABytes;                // kStgB x kBBytes
+    uint8_t *smP = smB + kStgB * kBBytes;                // kStgP x kPBytes
+    __shared__ uint64_t full_p[kStgP], empty_p[kStgP], full_a[kStgA], empty_a[kStgA], full_b[kStgB],
+        empty_b[kStgB], acc_full[2], acc_empty[2], drain;
     __shared__ uint32_t tmem_base;
     __shared__ int bail;
-    constexpr int kMats = GG<MODE>::kMats;
-    constexpr int kStageBytes = GG<MODE>::kStageBytes;
-    constexpr int kABytes = GG<MODE>::kABytes;
 
     if (*a.abort) return;
     const int n_units = *a.n_units;
@@ -386,13 +399,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const int K = k_of<MODE>(a), nks = K / kBK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStg; s++) {
-            mb_init(&full_a[s], 1 + kNumDq);
-            mb_init(&full_b[s], 1);
-            mb_init(&empty[s], 1);
-        }
-        mb_init(&acc_full, 1);
-        mb_init(&acc_empty, kNumEpi);
+        for (int s = 0; s < kStgP; s++) { mb_init(&full_p[s], 1); mb_init(&empty_p[s], kNumDq); }
+        for (int s = 0; s < kStgA; s++) { mb_init(&full_a[s], kNumDq); mb_init(&empty_a[s], 1); }
+        for (int s = 0; s < kStgB; s++) { mb_init(&full_b[s], 1); mb_init(&empty_b[s], 1); }
+        for (int b = 0; b < 2; b++) { mb_init(&acc_full[b], 1); mb_init(&acc_empty[b], kNumEpi); }
+        mb_init(&drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         bail = 0;
     }
@@ -405,14 +416,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    auto timeout = [&]() {
+        set_status(a.status, K3MOE_DEV_TIMEOUT);
+        bail = 1;
+    };
+    // a stage counter st of a ring of depth D: slot st % D, fill number st / D
+    auto wait_free = [&](uint64_t *bars, int D, uint32_t st) -> bool {
+        return st < (uint32_t)D || mb_wait(&bars[st % D], ((st / D) - 1) & 1u);
+    };
+    // after a timeout: wait (bounded) for the copies of the last D fills of a ring
+    auto drain_fills = [&](uint64_t *bars, int D, uint32_t n) {
+        for (uint32_t f = n > (uint32_t)D ? n - D : 0; f < n; f++) mb_wait(&bars[f % D], (f / D) & 1u);
+    };
 
-    if (warp == kWarpProd) {
-        // ------------------------------------------------------------ producer
+    if (warp == kWarpPack) {
+        // ------------------------------------------------------------ packed-weight producer
         if (lane == 0) {
-            uint32_t st = 0;
+            uint32_t cp = 0;
             for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
                 const GItem it = gitem<MODE>(a, n_units, i);
-                int brow0;                               // first B row
+                if (it.shared) continue;
+                const uint8_t *ex = a.table + (size_t)it.id * a.expert_bytes;
+                for (int kt = 0; kt < K / kTileK; kt++, cp++) {
+                    if (!wait_free(empty_p, kStgP, cp)) { timeout(); break; }
+                    const int sp = cp % kStgP;
+                    const uint8_t *src = MODE == kGU ? ex + ((size_t)it.rb * (a.d / kTileK) + kt) * 2 * kTileBytes
+                                                     : ex + a.gateup_bytes + ((size_t)it.rb * (a.f / kTileK) + kt) * kTileBytes;
+                    mb_expect_tx(&full_p[sp], (uint32_t)kPBytes);
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                            saddr(smP + sp * kPBytes)),
+                        "l"(src), "r"((uint32_t)kPBytes), "r"(saddr(&full_p[sp]))
+                        : "memory");
+                }
+            }
+            if (bail) drain_fills(full_p, kStgP, cp);
+        }
+    } else if (warp == kWarpProd) {
+        // ------------------------------------------------------------ B (and bf16 A) producer
+        if (lane == 0) {
+            uint32_t sa = 0, sb = 0;
+            for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
+                const GItem it = gitem<MODE>(a, n_units, i);
+                int brow0;
                 const CUtensorMap *mb = &mb_routed;
                 if (MODE == kGU) {
                     if (it.shared) { mb = &mb_shared; brow0 = it.n0; }
@@ -420,95 +466,83 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 } else {
                     brow0 = it.shared ? a.T * a.k + it.id * a.T + it.n0 : it.tok0 + it.n0;
                 }
-                for (int ks = 0; ks < nks; ks++, st++) {
-                    const int s = st % kStg;
-                    if (st >= (uint32_t)kStg && !mb_wait(&empty[s], ((st / kStg) - 1) & 1u)) {
-                        set_status(a.status, K3MOE_DEV_TIMEOUT);
-                        bail = 1;
+                for (int ks = 0; ks < nks; ks++, sa++, sb++) {
+                    if (!wait_free(empty_b, kStgB, sb) || (it.shared && !wait_free(empty_a, kStgA, sa))) {
+                        timeout();
                         break;
                     }
-                    uint8_t *A = sm + s * kStageBytes, *B = A + kABytes;
-                    mb_expect_tx(&full_b[s], (uint32_t)it.bn * kBK * 2);
-                    for (int j = 0; j < it.bn / 16; j++) tma2d(B + j * 16 * 128, mb, ks * kBK, brow0 + 16 * j, &full_b[s]);
+                    uint8_t *B = smB + (sb % kStgB) * kBBytes;
+                    uint64_t *fb = &full_b[sb % kStgB];
+                    // the bf16 A tiles of a shared expert land on the B barrier too
+                    mb_expect_tx(fb, (uint32_t)it.bn * kBK * 2 + (it.shared ? (uint32_t)kABytes : 0u));
+                    for (int j = 0; j < it.bn / 16; j++) tma2d(B + j * 16 * 128, mb, ks * kBK, brow0 + 16 * j, fb);
                     if (it.shared) {
+                        uint8_t *A = smA + (sa % kStgA) * kABytes;
                         const int arow = it.id * rows_of<MODE>(a) + it.rb * kBM;
-                        mb_expect_tx(&full_a[s], (uint32_t)kABytes);
-                        tma2d(A, &ma1, ks * kBK, arow, &full_a[s]);
-                        if (MODE == kGU) tma2d(A + kBM * kBK * 2, &ma3, ks * kBK, arow, &full_a[s]);
-                    } else {
-                        mb_arrive(&full_a[s]);
+                        tma2d(A, &ma1, ks * kBK, arow, fb);
+                        if (MODE == kGU) tma2d(A + kBM * kBK * 2, &ma3, ks * kBK, arow, fb);
                     }
                 }
             }
+            if (bail) drain_fills(full_b, kStgB, sb);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            uint32_t st = 0, n = 0;
+            uint32_t sa = 0, sb = 0, n = 0;
             for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x, n++) {
                 const GItem it = gitem<MODE>(a, n_units, i);
                 const uint32_t id = idesc(it.shared ? 1 : 0, it.bn);
-                if (n > 0 && !mb_wait(&acc_empty, (n - 1) & 1u)) {
-                    set_status(a.status, K3MOE_DEV_TIMEOUT);
-                    bail = 1;
-                    break;
-                }
+                const int buf = n & 1;
+                if (n >= 2 && !mb_wait(&acc_empty[buf], ((n >> 1) - 1) & 1u)) { timeout(); break; }
                 tc_fence_after();
-                for (int ks = 0; ks < nks; ks++, st++) {
-                    const int s = st % kStg;
-                    const uint32_t ph = (st / kStg) & 1u;
-                    if (!mb_wait(&full_a[s], ph) || !mb_wait(&full_b[s], ph)) {
-                        set_status(a.status, K3MOE_DEV_TIMEOUT);
-                        bail = 1;
-                        break;
-                    }
+                const uint32_t d0 = tmem + (uint32_t)buf * 256u;
+                for (int ks = 0; ks < nks; ks++, sa++, sb++) {
+                    if (!mb_wait(&full_a[sa % kStgA], (sa / kStgA) & 1u) ||
+                        !mb_wait(&full_b[sb % kStgB], (sb / kStgB) & 1u)) { timeout(); break; }
                     tc_fence_after();
-                    const uint32_t A = saddr(sm + s * kStageBytes), B = A + kABytes;
+                    const uint32_t A = saddr(smA + (sa % kStgA) * kABytes), B = saddr(smB + (sb % kStgB) * kBBytes);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; kk++) {
                         const uint64_t bd = sdesc(B + kk * 32);
                         const uint32_t accum = (ks | kk) != 0;
-                        umma(tmem, sdesc(A + kk * 32), bd, id, accum);
-                        if (MODE == kGU) umma(tmem + 256, sdesc(A + kBM * kBK * 2 + kk * 32), bd, id, accum);
+                        umma(d0, sdesc(A + kk * 32), bd, id, accum);
+                        if (MODE == kGU) umma(d0 + 128, sdesc(A + kBM * kBK * 2 + kk * 32), bd, id, accum);
                     }
-                    umma_commit(&empty[s]);
+                    umma_commit(&empty_a[sa % kStgA]);
+                    umma_commit(&empty_b[sb % kStgB]);
                 }
                 if (bail) break;
-                umma_commit(&acc_full);
+                umma_commit(&acc_full[buf]);
             }
+            umma_commit(&drain);                       // every issued MMA done before the dealloc
+            mb_wait(&drain, 0);
         }
     } else if (warp < kWarpEpi0) {
-        // ------------------------------------------------------------ dequant
+        // ------------------------------------------------------------ dequant (packed smem -> f16 A)
         const int t = threadIdx.x - kWarpDq0 * 32;             // 0..255
         const int m = (MODE == kGU) ? (t >> 7) : 0;
         const bool active = (MODE == kGU) || t < 128;
         const int r7 = t & 127, strip = r7 >> 4, gsel = (r7 >> 3) & 1, g = r7 & 7;
-        uint32_t st = 0;
+        uint32_t sa = 0, cp = 0;
         for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
             const GItem it = gitem<MODE>(a, n_units, i);
-            const uint8_t *ex = a.table + (size_t)it.id * a.expert_bytes;
             int bmax = 0;
             if (!it.shared && active) {
                 const int mm = MODE == kGU ? m : 2;
                 bmax = (int)*reinterpret_cast<const uint32_t *>(
                     a.table + trailer_offset(a.E, a.d, a.f, it.id, mm, it.rb));
             }
-            for (int ks = 0; ks < nks; ks++, st++) {
-                const int s = st % kStg;
-                if (st >= (uint32_t)kStg && !mb_wait(&empty[s], ((st / kStg) - 1) & 1u)) {
-                    set_status(a.status, K3MOE_DEV_TIMEOUT);
-                    bail = 1;
-                    break;
-                }
+            for (int ks = 0; ks < nks; ks++, sa++) {
+                if (!it.shared && (ks & 1) == 0 && !mb_wait(&full_p[cp % kStgP], (cp / kStgP) & 1u)) { timeout(); break; }
+                if (!wait_free(empty_a, kStgA, sa)) { timeout(); break; }
                 if (!it.shared && active) {
-                    const int kt = ks >> 1, c = 2 * (ks & 1) + gsel;
-                    const uint8_t *tile =
-                        MODE == kGU ? ex + (((size_t)it.rb * (a.d / kTileK) + kt) * 2 + m) * kTileBytes
-                                    : ex + a.gateup_bytes + ((size_t)it.rb * (a.f / kTileK) + kt) * kTileBytes;
+                    const int c = 2 * (ks & 1) + gsel;
+                    const uint8_t *tile = smP + (cp % kStgP) * kPBytes + m * kTileBytes;
                     const uint4 *src = reinterpret_cast<const uint4 *>(tile + (strip * 4 + c) * 256 + 32 * g);
-                    const uint4 p0 = __ldg(src), p1 = __ldg(src + 1);
+                    const uint4 p0 = src[0], p1 = src[1];
                     const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-                    uint8_t *A = sm + s * kStageBytes + m * (kBM * kBK * 2);
+                    uint8_t *A = smA + (sa % kStgA) * kABytes + m * (kBM * kBK * 2);
 #pragma unroll
                     for (int hr = 0; hr < 2; hr++) {            // rows g and g+8 of the strip
                         const int r = strip * 16 + g + 8 * hr;
@@ -529,16 +563,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     fence_async_smem();
                 }
                 __syncwarp();
-                if (lane == 0) mb_arrive(&full_a[s]);
+                if (lane == 0) {
+                    mb_arrive(&full_a[sa % kStgA]);
+                    if (!it.shared && (ks & 1)) mb_arrive(&empty_p[cp % kStgP]);
+                }
+                if (!it.shared && (ks & 1)) cp++;
             }
         }
-    } else {
+    } else if (warp < kWarpPack) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                                 // TMEM lane quadrant
         const int row = 32 * q + lane;
         uint32_t n = 0;
         for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x, n++) {
             const GItem it = gitem<MODE>(a, n_units, i);
+            const int buf = n & 1;
             float f1 = 1.0f, f3 = 1.0f;
             if (!it.shared) {
                 const int mm1 = MODE == kGU ? 0 : 2;
@@ -548,18 +587,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     f3 = ldexpf(1.0f, (int)*reinterpret_cast<const uint32_t *>(
                                           a.table + trailer_offset(a.E, a.d, a.f, it.id, 1, it.rb)) - 140);
             }
-            if (!mb_wait(&acc_full, n & 1u)) {
-                set_status(a.status, K3MOE_DEV_TIMEOUT);
-                bail = 1;
-                break;
-            }
+            if (!mb_wait(&acc_full[buf], (n >> 1) & 1u)) { timeout(); break; }
             tc_fence_after();
             const int grow = it.rb * kBM + row;
-            const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+            const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * 256u;
             for (int c0 = 0; c0 < it.bn; c0 += 16) {
                 float vg[16], vu[16];
                 tmem_ld16(lane_addr + c0, vg);
-                if (MODE == kGU) tmem_ld16(lane_addr + 256 + c0, vu);
+                if (MODE == kGU) tmem_ld16(lane_addr + 128 + c0, vu);
 #pragma unroll
                 for (int jj = 0; jj < 16; jj++) {
                     const int col = c0 + jj;
@@ -602,14 +637,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mb_arrive(&acc_empty);
+            if (lane == 0) mb_arrive(&acc_empty[buf]);
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == kWarpMma) {
-        if (bail && lane == 0) mb_wait(&acc_full, 0);   // best effort: let issued MMAs finish
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
     }
