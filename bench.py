@@ -75,19 +75,32 @@ def layer_bytes_flops(w, distinct_experts: int):
     return byts, flops
 
 
-def kernel_bytes(name: str, w, distinct_experts: int):
-    """Algorithmic bytes of one launch of a forward kernel (the bytes it must move):
-    gemv_gateup: W1, W3 of the distinct experts (packed) and of the shared experts
-    (bf16), x in, h out (f32); gemv_down: W2 likewise, h in, y out (f32); any other
-    kernel is charged the whole layer's bytes."""
+def kernel_work(name: str, w, distinct_experts: int):
+    """Algorithmic (bytes, FLOPs) of one launch of a forward kernel: the bytes it must
+    move and the multiply-adds (x2) it must do.
+    router_scores(_tc): Wr and x in, sc and ch out (f32); 2*T*E*d FLOPs.
+    gemv_gateup / gemm_gateup: W1, W3 of the distinct routed experts (packed MXFP4,
+    17/32 byte per weight) and of the shared experts (bf16), the activations in (x;
+    the gathered f16 copy on the GEMM path) and h out; 2 * rows * 2*f*d FLOPs with
+    rows = T*k + S*T.  gemv_down / gemm_down: W2 likewise, h in, the output out.
+    Any other kernel is charged the whole layer's bytes and no FLOPs."""
     rows = w.T * w.k + w.S * w.T
+    slots = w.T * w.k
+    if name in ("router_scores", "router_scores_tc"):
+        return w.E * w.d * 2 + w.T * w.d * 2 + 2 * w.T * w.E * 4, 2 * w.T * w.E * w.d
     if name == "gemv_gateup":
         return (distinct_experts * 2 * w.f * w.d * 17 // 32 + w.S * 2 * w.f * w.d * 2
-                + w.T * w.d * 2 + rows * w.f * 4)
+                + w.T * w.d * 2 + rows * w.f * 4), 2 * rows * 2 * w.f * w.d
     if name == "gemv_down":
         return (distinct_experts * w.d * w.f * 17 // 32 + w.S * w.d * w.f * 2
-                + rows * w.f * 4 + rows * w.d * 4)
-    return layer_bytes_flops(w, distinct_experts)[0]
+                + rows * w.f * 4 + rows * w.d * 4), 2 * rows * w.f * w.d
+    if name == "gemm_gateup":
+        return (distinct_experts * 2 * w.f * w.d * 17 // 32 + w.S * 2 * w.f * w.d * 2
+                + slots * w.d * 2 + w.T * w.d * 2 + rows * w.f * 2), 2 * rows * 2 * w.f * w.d
+    if name == "gemm_down":
+        return (distinct_experts * w.d * w.f * 17 // 32 + w.S * w.d * w.f * 2
+                + rows * w.f * 2 + w.T * w.d * 4), 2 * rows * w.f * w.d
+    return layer_bytes_flops(w, distinct_experts)[0], 0
 
 
 def workload_from(spec: str):
@@ -341,8 +354,16 @@ def gpu_arm(args):
     top_name, (top_n, top_ms) = top
     hbm, bf16, bf16_sus, src = peaks()
     per_launch_s = top_ms / top_n / 1000.0
-    alg = kernel_bytes(top_name, w, distinct)
-    achieved = alg / per_launch_s / 1e9
+    alg_b, alg_f = kernel_work(top_name, w, distinct)
+    # the kernel's bound: whichever of HBM and the tensor cores its algorithmic work
+    # needs longer on (sustained tensor peak: the kernel runs inside a long step)
+    if alg_f / (bf16_sus * 1e12) > alg_b / (hbm * 1e9):
+        roof = {"bound": "tensor", "achieved": alg_f / per_launch_s / 1e12, "peak": bf16_sus,
+                "unit": "TFLOP/s", "peak_kind": "bf16 sustained (f16 and bf16 run at one rate)"}
+    else:
+        roof = {"bound": "hbm", "achieved": alg_b / per_launch_s / 1e9, "peak": hbm, "unit": "GB/s",
+                "peak_kind": "HBM copy"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
     step_bytes, step_flops = layer_bytes_flops(w, distinct)
     step_s = ms / args.steps / 1000.0
 
@@ -387,10 +408,9 @@ def gpu_arm(args):
                        "n_shared": w.S, "weights": "routed MXFP4 (E2M1 + E8M0/32), shared bf16",
                        "l2": "512 MiB buffer written between timed steps",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "kernel": top_name, "achieved": achieved, "peak": hbm,
-                         "unit": "GB/s", "frac": achieved / hbm, "peak_source": src,
-                         "traffic": traffic_for(top_name, w.name),
-                         "alg_bytes_per_launch": alg, "launch_ms": per_launch_s * 1e3},
+            "roofline": dict(roof, kernel=top_name, peak_source=src,
+                             traffic=traffic_for(top_name, w.name), alg_bytes_per_launch=alg_b,
+                             alg_flops_per_launch=alg_f, launch_ms=per_launch_s * 1e3),
             "step_roofline": {"bytes": step_bytes, "flops": step_flops,
                               "distinct_experts": distinct,
                               "hbm_frac": step_bytes / step_s / 1e9 / hbm,

@@ -147,6 +147,19 @@ k3moe_status k3moe_route(const k3moe_config *cfg, int32_t T, const uint16_t *x,
                          int32_t *idx, float *weight, int32_t *offsets, int32_t *perm,
                          void *ws, size_t ws_bytes, k3moe_stream stream);
 
+/* The router's scores alone, as k3moe_route computes them before its top-k
+ * (kimi-k3-in-c README, Part II, section 9, the k3_router listing):
+ *   scores [T][E] f32  out: sc = 1/(1+expf(-logit)), logit = x . Wr^T in fp32
+ *   choice [T][E] f32  out: ch = sc + bias (sc when bias is NULL)
+ * The same kernels as k3moe_route for the same T (the per-token kernel for few
+ * tokens, the tensor cores for many), so k3moe_route's selection is the top-k of
+ * `choice` exactly.  x, w_router 16-byte aligned; scores, choice, bias 4-byte
+ * aligned.  T may be 0 (nothing written).  ws per k3moe_workspace_bytes(T_max >= T);
+ * only its status word is used. */
+k3moe_status k3moe_router_scores(const k3moe_config *cfg, int32_t T, const uint16_t *x,
+                                 const uint16_t *w_router, const float *bias, float *scores,
+                                 float *choice, void *ws, size_t ws_bytes, k3moe_stream stream);
+
 /* Expert part of the layer for given routing (as k3moe_route writes it, or
  * any routing with the same conventions), kimi-k3-in-c README, Part II,
  * section 9, the k3_moe listing's expert loop and shared-expert step:

@@ -14,7 +14,7 @@ import os
 __all__ = [
     "K3MoEConfig", "K3MOE_OK", "K3MoEError", "lib", "k3moe_config", "k3moe_validate_config",
     "k3moe_packed_bytes", "k3moe_workspace_bytes", "k3moe_pack_mxfp4", "k3moe_unpack_mxfp4",
-    "k3moe_route", "k3moe_forward", "k3moe_forward_noalloc", "k3moe_device_status",
+    "k3moe_route", "k3moe_router_scores", "k3moe_forward", "k3moe_forward_noalloc", "k3moe_device_status",
     "k3moe_strerror",
     "k3moe_launch_count", "k3moe_timing_enable", "k3moe_timing_read", "k3moe_timing_reset",
     "library_path", "MoELayer",
@@ -67,6 +67,7 @@ def lib():
             "k3moe_pack_mxfp4": (ctypes.c_int, [cp, i32, i32] + [vp] * 6 + [vp, sz, vp, vp]),
             "k3moe_unpack_mxfp4": (ctypes.c_int, [cp, i32, i32, vp, sz] + [vp] * 6 + [vp]),
             "k3moe_route": (ctypes.c_int, [cp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "k3moe_router_scores": (ctypes.c_int, [cp, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
             "k3moe_forward": (ctypes.c_int, [cp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp,
                                              vp, sz, vp]),
             "k3moe_device_status": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32)]),
@@ -151,6 +152,13 @@ def k3moe_unpack_mxfp4(cfg, expert_lo, n_out, table, w1_packed, w1_scale, w3_pac
     _check("k3moe_unpack_mxfp4", lib().k3moe_unpack_mxfp4(
         ctypes.byref(cfg), expert_lo, n_out, _ptr(table), tb, _ptr(w1_packed), _ptr(w1_scale),
         _ptr(w3_packed), _ptr(w3_scale), _ptr(w2_packed), _ptr(w2_scale), _stream(stream)))
+
+
+def k3moe_router_scores(cfg, T, x, w_router, bias, scores, choice, ws, ws_bytes=None, stream=None):
+    wb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check("k3moe_router_scores", lib().k3moe_router_scores(
+        ctypes.byref(cfg), T, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(scores), _ptr(choice),
+        _ptr(ws), wb, _stream(stream)))
 
 
 def k3moe_route(cfg, T, x, w_router, bias, idx, weight, offsets, perm, ws, ws_bytes=None,
@@ -244,6 +252,16 @@ class MoELayer:
         T = x.shape[0]
         k3moe_route(self.cfg, T, x, self.w_router, self.bias, self.idx, self.weight, self.offsets,
                     self.perm, self.ws, self.ws_bytes, stream)
+
+    def scores(self, x, stream=None):
+        """(sc, ch) [T][E] f32 device tensors: the router scores k3moe_route selects from."""
+        import torch
+        T = x.shape[0]
+        sc = torch.empty((T, self.cfg.n_experts), dtype=torch.float32, device=self.device)
+        ch = torch.empty_like(sc)
+        k3moe_router_scores(self.cfg, T, x, self.w_router, self.bias, sc, ch, self.ws, self.ws_bytes,
+                            stream)
+        return sc, ch
 
     def forward(self, x, out, stream=None, routing=None):
         T = x.shape[0]

@@ -192,6 +192,27 @@ k3moe_status k3moe_route(const k3moe_config *cfg, int32_t T, const uint16_t *x,
     return e == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 
+k3moe_status k3moe_router_scores(const k3moe_config *cfg, int32_t T, const uint16_t *x,
+                                 const uint16_t *w_router, const float *bias, float *scores,
+                                 float *choice, void *ws, size_t ws_bytes, k3moe_stream stream)
+{
+    k3moe_status st = check_config(cfg);
+    if (st != K3MOE_OK) return st;
+    if (T < 0 || T > kMaxT) return K3MOE_ESHAPE;
+    if (T == 0) return K3MOE_OK;
+    if (!x || !w_router || !scores || !choice) return K3MOE_EINVAL;
+    if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(scores, 4) || !aligned(choice, 4) ||
+        (bias && !aligned(bias, 4)))
+        return K3MOE_EALIGN;
+    if (!ws || !aligned(ws, 256)) return K3MOE_EWORKSPACE;
+    const WsLayout L = ws_layout(*cfg, T);
+    if (ws_bytes < L.total) return K3MOE_EWORKSPACE;
+    cudaError_t e = launch_router_scores(*cfg, T, x, w_router, bias, scores, choice,
+                                         reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) + L.status),
+                                         (cudaStream_t)stream);
+    return e == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+}
+
 k3moe_status k3moe_forward(const k3moe_config *cfg, int32_t T, const uint16_t *x,
                            const int32_t *idx, const float *weight, const int32_t *offsets,
                            const int32_t *perm, const void *expert_table, size_t table_bytes,

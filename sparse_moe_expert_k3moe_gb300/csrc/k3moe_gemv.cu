@@ -970,21 +970,33 @@ int sm_count()
 }
 
 // Persistent grid: every SM filled to the occupancy the kernel's resources allow
-// (shared memory carve-out at its maximum).  Attributes and occupancy are set up once
-// per (kernel, shared-memory size) and cached.
+// (shared memory carve-out at its maximum).  Occupancy is computed once per (kernel,
+// shared-memory size) and cached.  A kernel's dynamic shared-memory limit is a property
+// of the function, so it is only ever raised: a launch that needs less than an earlier
+// one still fits.
 template <typename Kern>
 int grid_blocks(Kern kernel, size_t smem)
 {
     struct Entry { const void *k; size_t smem; int blocks; };
+    struct Limit { const void *k; size_t smem; };
     static Entry cache[16];
-    static int n_cache = 0;
+    static Limit limit[4];
+    static int n_cache = 0, n_limit = 0;
     static std::mutex mu;
     std::lock_guard<std::mutex> lk(mu);
+    int li = 0;
+    while (li < n_limit && limit[li].k != (const void *)kernel) li++;
+    if (li == n_limit) {
+        limit[n_limit++] = Limit{(const void *)kernel, 0};
+        cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    }
+    if (smem > limit[li].smem) {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        limit[li].smem = smem;
+    }
     for (int i = 0; i < n_cache; i++)
         if (cache[i].k == (const void *)kernel && cache[i].smem == smem) return cache[i].blocks;
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         (int)cudaSharedmemCarveoutMaxShared);
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads + 32, smem) != cudaSuccess || occ < 1)
         occ = 1;

@@ -167,6 +167,14 @@ cudaError_t launch_unpack(const k3moe_config &c, int expert_lo, int n, const uin
 cudaError_t launch_route(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
                          const float *bias, int32_t *idx, float *weight, int32_t *offsets,
                          int32_t *perm, uint8_t *ws, const WsLayout &L, cudaStream_t s);
+// Router scores sc, ch [T][E] f32 (per-token kernel, or the tensor cores for many tokens).
+cudaError_t launch_router_scores(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
+                                 const float *bias, float *sc, float *ch, int32_t *status, cudaStream_t s);
+// Router scores on the tensor cores (many tokens): sc, ch [T][E] as router_scores.
+constexpr int kRouterTcMinTokens = 32;
+bool router_tc_applies(const k3moe_config &c, int T);
+cudaError_t launch_router_scores_tc(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
+                                    const float *bias, float *sc, float *ch, int32_t *status, cudaStream_t s);
 cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x, const int32_t *idx,
                                 const float *weight, const int32_t *offsets, const int32_t *perm,
                                 const uint8_t *table, const uint16_t *sh_w1, const uint16_t *sh_w3,

@@ -334,6 +334,31 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(int total_slots, int 
 
 }  // namespace
 
+cudaError_t launch_router_scores(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
+                                 const float *bias, float *sc, float *ch, int32_t *status, cudaStream_t s)
+{
+    const int E = c.n_experts;
+    if (router_tc_applies(c, T)) {
+        timing_begin("router_scores_tc", s);
+        cudaError_t err = launch_router_scores_tc(c, T, x, wr, bias, sc, ch, status, s);
+        timing_end("router_scores_tc", s);
+        if (err != cudaSuccess) return err;
+    } else {
+        static size_t smem_set = 0;
+        const size_t smem = (size_t)kScoreTok * c.d * 2;
+        if (smem > smem_set) {
+            cudaFuncSetAttribute(router_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            smem_set = smem;
+        }
+        timing_begin("router_scores", s);
+        router_scores_kernel<<<(E + kScoreWarps - 1) / kScoreWarps, kScoreWarps * 32, smem, s>>>(
+            T, c.d, E, x, wr, bias, sc, ch);
+        count_launch();
+        timing_end("router_scores", s);
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_route(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
                          const float *bias, int32_t *idx, float *weight, int32_t *offsets,
                          int32_t *perm, uint8_t *ws, const WsLayout &L, cudaStream_t s)
@@ -348,19 +373,8 @@ cudaError_t launch_route(const k3moe_config &c, int T, const uint16_t *x, const 
     }
     float *sc = reinterpret_cast<float *>(ws + L.sc);
     float *ch = reinterpret_cast<float *>(ws + L.ch);
-    {
-        static size_t smem_set = 0;
-        const size_t smem = (size_t)kScoreTok * c.d * 2;
-        if (smem > smem_set) {
-            cudaFuncSetAttribute(router_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            smem_set = smem;
-        }
-        timing_begin("router_scores", s);
-        router_scores_kernel<<<(E + kScoreWarps - 1) / kScoreWarps, kScoreWarps * 32, smem, s>>>(
-            T, c.d, E, x, wr, bias, sc, ch);
-        count_launch();
-        timing_end("router_scores", s);
-    }
+    cudaError_t err = launch_router_scores(c, T, x, wr, bias, sc, ch, status, s);
+    if (err != cudaSuccess) return err;
     MapArgs m{T, E, k, idx, offsets, perm, reinterpret_cast<int32_t *>(ws + L.chunk_counts),
               reinterpret_cast<int32_t *>(ws + L.local_rank), status};
     // status block word 4 is the last-block counter of router_topk

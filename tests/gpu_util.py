@@ -8,7 +8,30 @@ import oracle
 # acceptance bar).  Indices, offsets and permutations are compared bit-exactly.
 REL_L2 = 5e-3
 MAX_REL = 2e-2
-NEAR_TIE = 1e-6
+# Router scores: the device accumulates each logit's d exact bf16 products in fp32 in
+# its own order (the oracle: exactly, then one rounding), so its scores differ from the
+# oracle's by accumulation rounding only.  That rounding grows with the size of the
+# token's logits, |x_t| * rms(Wr) (about 1.2 at the K3 shapes with unit-variance x):
+# the per-token kernel stays within 2e-7 of the oracle; the tensor-core path (T >= 32),
+# whose accumulation is coarser, was measured at 3.7e-6 max over 14.7M scores of unit
+# scale and 1.3e-5 on tokens scaled by 8.  score_tol(t) = SCORE_TOL_REL * max(1, scale_t)
+# bounds |sc_dev - sc_oracle| (plus one rounding of the bias add for ch).  A selection can
+# only differ from the oracle's where two compared choice scores lie within twice that of
+# each other: the token's near-tie threshold.
+SCORE_TOL_REL = 6e-6
+BIAS_ADD_TOL = 2.5e-7
+
+
+def score_tol(x_bf16, wr_bf16):
+    """Per-token score tolerance [T] (see above)."""
+    x = ki.bf16_to_f32(x_bf16)
+    wr = ki.bf16_to_f32(wr_bf16).astype(np.float64)
+    scale = np.linalg.norm(x, axis=1).astype(np.float64) * np.sqrt(np.mean(wr * wr))
+    return SCORE_TOL_REL * np.maximum(1.0, scale)
+
+
+def near_tie(x_bf16, wr_bf16):
+    return 2.0 * (score_tol(x_bf16, wr_bf16) + BIAS_ADD_TOL)
 
 
 def out_errors(got, ref):
