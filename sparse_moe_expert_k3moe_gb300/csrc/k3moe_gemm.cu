@@ -24,15 +24,15 @@
 //                into fp32 accumulators in tensor memory, two buffers of 256 columns
 //                (gate/up: g at +0, u at +128), so one item's MMAs overlap the previous
 //                item's epilogue;
-//   warps 2-9    dequant: packed MXFP4 tiles from shared memory to f16 A tiles
+//   warps 2-17   dequant: packed MXFP4 tiles from shared memory to f16 A tiles
 //                (128-byte swizzle, K-major) -- the E2M1 pair decoded by the hardware
 //                conversion, times 2^(b - bmax + 13) where bmax is the largest scale of
 //                the 128-row block (the packed table's trailer), so every value is exact
 //                in f16 while the block's scales span at most 36 binades; the epilogue
 //                multiplies by 2^(bmax - 140);
-//   warps 10-13  epilogue: tcgen05.ld the accumulators (warp w reads lanes 32(w%4)..),
+//   warps 18-21  epilogue: tcgen05.ld the accumulators (warp w reads lanes 32(w%4)..),
 //                apply the scales, SiTU or the weighted combine, store;
-//   warp 14      packed-weight producer: one bulk copy per 128-column packed tile (pair),
+//   warp 22      packed-weight producer: one bulk copy per 128-column packed tile (pair),
 //                kStgP tiles ahead of the dequant warps.
 // Rings: packed tiles (kStgP), f16 A stages (kStgA) and B stages (kStgB); the MMA thread
 // releases an A and a B stage with one tcgen05.commit each.
@@ -49,27 +49,21 @@
 namespace k3moe {
 namespace {
 
-constexpr int kBM = 128, kBK = 64;
-constexpr int kStgP = 3, kStgA = 2, kStgB = 3;               // packed, A and B rings
-constexpr int kNumDq = 8;
+constexpr int kBM = 128, kBK = 64;          // token rows per tile (MMA M), K per stage
+constexpr int kWRows = 256;                 // weight rows per item (MMA N): W1|W3, or two W2 blocks
+constexpr int kStgA = 4, kStgW = 2, kStgP = 4;   // token, weight and packed-weight rings
+constexpr int kNumDq = 16;
 constexpr int kWarpProd = 0, kWarpMma = 1, kWarpDq0 = 2, kWarpEpi0 = 2 + kNumDq, kNumEpi = 4;
-constexpr int kWarpPack = kWarpEpi0 + kNumEpi;                 // 14
-constexpr int kGemmThreads = (kWarpPack + 1) * 32;             // 480
+constexpr int kWarpPack = kWarpEpi0 + kNumEpi;                 // 22
+constexpr int kGemmThreads = (kWarpPack + 1) * 32;             // 736
 constexpr int kTmemCols = 512;
+constexpr int kABytes = kBM * kBK * 2;                          // token tile of a stage
+constexpr int kWBytes = kWRows * kBK * 2;                       // weight tile of a stage
+constexpr int kPBytes = 2 * kTileBytes;                         // two packed 128 x 128 tiles
+constexpr int kGemmSmem = kStgA * kABytes + kStgW * kWBytes + kStgP * kPBytes + 2048;
+static_assert(kGemmSmem + 8 * 1024 <= 232448, "shared memory per block (dynamic + static)");
 
 enum { kGU = 0, kDN = 1 };
-
-template <int MODE>
-struct GG {
-    static constexpr int kMats = MODE == kGU ? 2 : 1;
-    // tokens per tile: gate/up keeps two accumulators (g, u) per buffer, so 128 tokens
-    // fit twice in the 512 TMEM columns; down keeps one
-    static constexpr int kBNMax = MODE == kGU ? 128 : 256;
-    static constexpr int kPBytes = kMats * kTileBytes;         // packed tile (pair) of 128 columns
-    static constexpr int kABytes = kMats * kBM * kBK * 2;      // f16/bf16 A tiles of a stage
-    static constexpr int kBBytes = kBNMax * kBK * 2;           // B tile of a stage
-    static constexpr int kSmem = kStgP * kPBytes + kStgA * kABytes + kStgB * kBBytes + 2048;
-};
 
 __device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t byte)
 {
@@ -82,10 +76,20 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
     __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
     return *reinterpret_cast<uint32_t *>(&r);
 }
+// tanh(x) = 1 - 2 / (e^(2x) + 1) with the fast exponential; |x| clamped to 15, where
+// tanh is 1 to float precision.  Absolute error a few ulp of 1.
+__device__ __forceinline__ float tanh_fast(float x)
+{
+    x = fminf(fmaxf(x, -15.0f), 15.0f);
+    return 1.0f - __fdividef(2.0f, __expf(2.0f * x) + 1.0f);
+}
+// SiTU of the GEMM epilogue: b1 tanh(g/b1) sigmoid(g) b2 tanh(u/b2) with the fast
+// exponential.  Its error (a few 1e-7 relative to the gate and linear caps) is far
+// below the f16 / bf16 rounding of h that follows.
 __device__ __forceinline__ float situ(float g, float u, float b1, float b2)
 {
-    const float a = b1 * tanhf(g / b1) * (1.0f / (1.0f + expf(-g)));
-    return a * (b2 * tanhf(u / b2));
+    const float sg = __fdividef(1.0f, 1.0f + __expf(-fminf(fmaxf(g, -80.0f), 80.0f)));
+    return b1 * tanh_fast(__fdividef(g, b1)) * sg * (b2 * tanh_fast(__fdividef(u, b2)));
 }
 // f16 of 2^e for e in [-24, 15] (subnormals below -14), 0 outside.
 __device__ __forceinline__ uint32_t f16_pow2(int e)
@@ -153,9 +157,9 @@ __global__ void __launch_bounds__(1024) gemm_units_kernel(UnitsArgs a)
         for (int u = 0; u < n; u++) {
             a.prefix_gu[u] = pg;
             a.prefix_dn[u] = pd;
-            const int ntok = a.units[4 * u + 3];
-            pg += (ntok + GG<kGU>::kBNMax - 1) / GG<kGU>::kBNMax * a.rb_gu;
-            pd += (ntok + GG<kDN>::kBNMax - 1) / GG<kDN>::kBNMax * a.rb_dn;
+            const int ntiles = (a.units[4 * u + 3] + kBM - 1) / kBM;
+            pg += ntiles * a.rb_gu;
+            pd += ntiles * a.rb_dn;
         }
         a.prefix_gu[n] = pg;
         a.prefix_dn[n] = pd;
@@ -253,57 +257,55 @@ struct GemmArgs {
 
 struct GItem {
     int shared, id, tok0, ntok;     // unit
-    int rb, n0, ncols, bn;          // row block, first column, valid columns, MMA N
+    int rb;                         // gate/up: 128-row block of f; down: pair of 128-row blocks of d
+    int n0, ncols;                  // first token of the tile within the unit, tokens in the tile
+    int nw;                         // weight rows (MMA N): 256, or 128 for a last odd block of d
 };
 
-template <int MODE>
-__device__ __forceinline__ int rows_of(const GemmArgs &a) { return MODE == kGU ? a.f : a.d; }
 template <int MODE>
 __device__ __forceinline__ int k_of(const GemmArgs &a) { return MODE == kGU ? a.d : a.f; }
 
 template <int MODE>
-__device__ __forceinline__ GItem gitem(const GemmArgs &a, int n_units, int i)
+__device__ __forceinline__ GItem gitem(const GemmArgs &a, const int32_t *prefix, int n_units, int i)
 {
     int lo = 0, hi = n_units;                      // unit u with prefix[u] <= i < prefix[u+1]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (a.prefix[mid] <= i) lo = mid; else hi = mid;
+        if (prefix[mid] <= i) lo = mid; else hi = mid;
     }
-    const int32_t *u = a.units + 4 * lo;
+    const int4 u = *reinterpret_cast<const int4 *>(a.units + 4 * lo);
     GItem it;
-    it.shared = u[0];
-    it.id = u[1];
-    it.tok0 = u[2];
-    it.ntok = u[3];
-    constexpr int BN = GG<MODE>::kBNMax;
-    const int ntiles = max(1, (it.ntok + BN - 1) / BN);
-    const int j = i - a.prefix[lo];
-    const int nt = j % ntiles;                     // token tile fastest: the block's weights stay hot in L2
+    it.shared = u.x;
+    it.id = u.y;
+    it.tok0 = u.z;
+    it.ntok = u.w;
+    const int ntiles = max(1, (it.ntok + kBM - 1) / kBM);
+    const int j = i - prefix[lo];
+    const int nt = j % ntiles;                     // token tile fastest: the weight block stays hot in L2
     it.rb = j / ntiles;
-    it.n0 = nt * BN;
-    it.ncols = min(BN, it.ntok - it.n0);
-    it.bn = (it.ncols + 15) & ~15;
+    it.n0 = nt * kBM;
+    it.ncols = min(kBM, it.ntok - it.n0);
+    it.nw = (MODE == kGU || 2 * it.rb + 1 < a.d / kTileRows) ? kWRows : kWRows / 2;
     return it;
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs a,
-                                                                const __grid_constant__ CUtensorMap mb_routed,
-                                                                const __grid_constant__ CUtensorMap mb_shared,
-                                                                const __grid_constant__ CUtensorMap ma1,
-                                                                const __grid_constant__ CUtensorMap ma3)
+                                                                const __grid_constant__ CUtensorMap mtok_routed,
+                                                                const __grid_constant__ CUtensorMap mtok_shared,
+                                                                const __grid_constant__ CUtensorMap mw1,
+                                                                const __grid_constant__ CUtensorMap mw3)
 {
     extern __shared__ __align__(1024) uint8_t gsm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~(uintptr_t)1023);
-    constexpr int kMats = GG<MODE>::kMats;
-    constexpr int kPBytes = GG<MODE>::kPBytes, kABytes = GG<MODE>::kABytes, kBBytes = GG<MODE>::kBBytes;
-    uint8_t *smA = sm;                                   // kStgA x kABytes (1024-aligned)
-    uint8_t *smB = smA + kStgA * kABytes;                // kStgB x kBBytes
-    uint8_t *smP = smB + kStgB * kBBytes;                // kStgP x kPBytes
-    __shared__ uint64_t full_p[kStgP], empty_p[kStgP], full_a[kStgA], empty_a[kStgA], full_b[kStgB],
-        empty_b[kStgB], acc_full[2], acc_empty[2], drain;
+    uint8_t *smA = sm;                                   // kStgA x kABytes: token tiles
+    uint8_t *smW = smA + kStgA * kABytes;                // kStgW x kWBytes: weight tiles
+    uint8_t *smP = smW + kStgW * kWBytes;                // kStgP x kPBytes: packed weights
+    __shared__ uint64_t full_p[kStgP], empty_p[kStgP], full_a[kStgA], empty_a[kStgA], full_w[kStgW],
+        empty_w[kStgW], acc_full[2], acc_empty[2], drain;
     __shared__ uint32_t tmem_base;
     __shared__ int bail;
+    __shared__ int32_t s_prefix[kMaxExperts + kMaxShared + 1];   // item prefix of the units
 
     if (*a.abort) return;
     const int n_units = *a.n_units;
@@ -314,13 +316,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStgP; s++) { mb_init(&full_p[s], 1); mb_init(&empty_p[s], kNumDq); }
-        for (int s = 0; s < kStgA; s++) { mb_init(&full_a[s], kNumDq); mb_init(&empty_a[s], 1); }
-        for (int s = 0; s < kStgB; s++) { mb_init(&full_b[s], 1); mb_init(&empty_b[s], 1); }
+        for (int s = 0; s < kStgA; s++) { mb_init(&full_a[s], 1); mb_init(&empty_a[s], 1); }
+        for (int s = 0; s < kStgW; s++) { mb_init(&full_w[s], kNumDq); mb_init(&empty_w[s], 1); }
         for (int b = 0; b < 2; b++) { mb_init(&acc_full[b], 1); mb_init(&acc_empty[b], kNumEpi); }
         mb_init(&drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         bail = 0;
     }
+    for (int u = threadIdx.x; u <= n_units; u += blockDim.x) s_prefix[u] = a.prefix[u];
     if (warp == kWarpMma) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tmem_base)),
                      "r"(kTmemCols));
@@ -348,83 +351,86 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (lane == 0) {
             uint32_t cp = 0;
             for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
-                const GItem it = gitem<MODE>(a, n_units, i);
+                const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
                 if (it.shared) continue;
                 const uint8_t *ex = a.table + (size_t)it.id * a.expert_bytes;
                 for (int kt = 0; kt < K / kTileK; kt++, cp++) {
                     if (!wait_free(empty_p, kStgP, cp)) { timeout(); break; }
                     const int sp = cp % kStgP;
-                    const uint8_t *src = MODE == kGU ? ex + ((size_t)it.rb * (a.d / kTileK) + kt) * 2 * kTileBytes
-                                                     : ex + a.gateup_bytes + ((size_t)it.rb * (a.f / kTileK) + kt) * kTileBytes;
-                    mb_expect_tx(&full_p[sp], (uint32_t)kPBytes);
-                    asm volatile(
-                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                            saddr(smP + sp * kPBytes)),
-                        "l"(src), "r"((uint32_t)kPBytes), "r"(saddr(&full_p[sp]))
-                        : "memory");
+                    uint8_t *dst = smP + sp * kPBytes;
+                    if (MODE == kGU) {          // the W1 and W3 tiles of a block are adjacent
+                        mb_expect_tx(&full_p[sp], (uint32_t)(2 * kTileBytes));
+                        bulk_g2s(dst, ex + ((size_t)it.rb * (a.d / kTileK) + kt) * 2 * kTileBytes,
+                                 2 * kTileBytes, &full_p[sp]);
+                    } else {                    // two row blocks of W2
+                        const int nb = it.nw / kTileRows;
+                        mb_expect_tx(&full_p[sp], (uint32_t)(nb * kTileBytes));
+                        for (int b = 0; b < nb; b++)
+                            bulk_g2s(dst + b * kTileBytes,
+                                     ex + a.gateup_bytes + ((size_t)(2 * it.rb + b) * (a.f / kTileK) + kt) * kTileBytes,
+                                     kTileBytes, &full_p[sp]);
+                    }
                 }
             }
             if (bail) drain_fills(full_p, kStgP, cp);
         }
     } else if (warp == kWarpProd) {
-        // ------------------------------------------------------------ B (and bf16 A) producer
+        // ------------------------------------------------------------ token tiles (and bf16 weights)
         if (lane == 0) {
-            uint32_t sa = 0, sb = 0;
+            uint32_t st = 0;
             for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
-                const GItem it = gitem<MODE>(a, n_units, i);
-                int brow0;
-                const CUtensorMap *mb = &mb_routed;
-                if (MODE == kGU) {
-                    if (it.shared) { mb = &mb_shared; brow0 = it.n0; }
-                    else brow0 = it.tok0 + it.n0;
-                } else {
-                    brow0 = it.shared ? a.T * a.k + it.id * a.T + it.n0 : it.tok0 + it.n0;
-                }
-                for (int ks = 0; ks < nks; ks++, sa++, sb++) {
-                    if (!wait_free(empty_b, kStgB, sb) || (it.shared && !wait_free(empty_a, kStgA, sa))) {
+                const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
+                const CUtensorMap *mt = it.shared ? &mtok_shared : &mtok_routed;
+                int row0;
+                if (MODE == kGU) row0 = it.shared ? it.n0 : it.tok0 + it.n0;
+                else row0 = it.shared ? a.T * a.k + it.id * a.T + it.n0 : it.tok0 + it.n0;
+                const int nb = it.nw / kTileRows;
+                for (int ks = 0; ks < nks; ks++, st++) {
+                    if (!wait_free(empty_a, kStgA, st) || (it.shared && !wait_free(empty_w, kStgW, st))) {
                         timeout();
                         break;
                     }
-                    uint8_t *B = smB + (sb % kStgB) * kBBytes;
-                    uint64_t *fb = &full_b[sb % kStgB];
-                    // the bf16 A tiles of a shared expert land on the B barrier too
-                    mb_expect_tx(fb, (uint32_t)it.bn * kBK * 2 + (it.shared ? (uint32_t)kABytes : 0u));
-                    for (int j = 0; j < it.bn / 16; j++) tma2d(B + j * 16 * 128, mb, ks * kBK, brow0 + 16 * j, fb);
+                    uint64_t *fa = &full_a[st % kStgA];
+                    // the bf16 weight tiles of a shared expert land on the token barrier too
+                    mb_expect_tx(fa, (uint32_t)kABytes + (it.shared ? (uint32_t)(nb * kTileRows * kBK * 2) : 0u));
+                    tma2d(smA + (st % kStgA) * kABytes, mt, ks * kBK, row0, fa);
                     if (it.shared) {
-                        uint8_t *A = smA + (sa % kStgA) * kABytes;
-                        const int arow = it.id * rows_of<MODE>(a) + it.rb * kBM;
-                        tma2d(A, &ma1, ks * kBK, arow, fb);
-                        if (MODE == kGU) tma2d(A + kBM * kBK * 2, &ma3, ks * kBK, arow, fb);
+                        uint8_t *W = smW + (st % kStgW) * kWBytes;
+                        if (MODE == kGU) {
+                            const int wrow = it.id * a.f + it.rb * kTileRows;
+                            tma2d(W, &mw1, ks * kBK, wrow, fa);
+                            tma2d(W + kTileRows * kBK * 2, &mw3, ks * kBK, wrow, fa);
+                        } else {
+                            for (int b = 0; b < nb; b++)
+                                tma2d(W + b * kTileRows * kBK * 2, &mw1, ks * kBK,
+                                      it.id * a.d + (2 * it.rb + b) * kTileRows, fa);
+                        }
                     }
                 }
             }
-            if (bail) drain_fills(full_b, kStgB, sb);
+            if (bail) drain_fills(full_a, kStgA, st);
         }
     } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------ MMA issue
+        // ------------------------------------------------------------ MMA issue: D[token][weight row]
         if (lane == 0) {
-            uint32_t sa = 0, sb = 0, n = 0;
+            uint32_t st = 0, n = 0;
             for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x, n++) {
-                const GItem it = gitem<MODE>(a, n_units, i);
-                const uint32_t id = idesc(it.shared ? 1 : 0, it.bn);
+                const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
+                const uint32_t id = idesc(it.shared ? 1 : 0, it.nw);
                 const int buf = n & 1;
                 if (n >= 2 && !mb_wait(&acc_empty[buf], ((n >> 1) - 1) & 1u)) { timeout(); break; }
                 tc_fence_after();
                 const uint32_t d0 = tmem + (uint32_t)buf * 256u;
-                for (int ks = 0; ks < nks; ks++, sa++, sb++) {
-                    if (!mb_wait(&full_a[sa % kStgA], (sa / kStgA) & 1u) ||
-                        !mb_wait(&full_b[sb % kStgB], (sb / kStgB) & 1u)) { timeout(); break; }
+                for (int ks = 0; ks < nks; ks++, st++) {
+                    if (!mb_wait(&full_a[st % kStgA], (st / kStgA) & 1u) ||
+                        !mb_wait(&full_w[st % kStgW], (st / kStgW) & 1u)) { timeout(); break; }
                     tc_fence_after();
-                    const uint32_t A = saddr(smA + (sa % kStgA) * kABytes), B = saddr(smB + (sb % kStgB) * kBBytes);
+                    const uint32_t A = saddr(smA + (st % kStgA) * kABytes), W = saddr(smW + (st % kStgW) * kWBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; kk++) {
-                        const uint64_t bd = sdesc(B + kk * 32);
-                        const uint32_t accum = (ks | kk) != 0;
-                        umma(d0, sdesc(A + kk * 32), bd, id, accum);
-                        if (MODE == kGU) umma(d0 + 128, sdesc(A + kBM * kBK * 2 + kk * 32), bd, id, accum);
-                    }
-                    umma_commit(&empty_a[sa % kStgA]);
-                    umma_commit(&empty_b[sb % kStgB]);
+                    for (int kk = 0; kk < kBK / 16; kk++)
+                        umma(d0, sdesc(A + kk * 32), sdesc(W + kk * 32), id, (ks | kk) != 0);
+                    umma_commit(&empty_a[st % kStgA]);
+                    umma_commit(&empty_w[st % kStgW]);
                 }
                 if (bail) break;
                 umma_commit(&acc_full[buf]);
@@ -433,119 +439,135 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             mb_wait(&drain, 0);
         }
     } else if (warp < kWarpEpi0) {
-        // ------------------------------------------------------------ dequant (packed smem -> f16 A)
-        const int t = threadIdx.x - kWarpDq0 * 32;             // 0..255
-        const int m = (MODE == kGU) ? (t >> 7) : 0;
-        const bool active = (MODE == kGU) || t < 128;
-        const int r7 = t & 127, strip = r7 >> 4, gsel = (r7 >> 3) & 1, g = r7 & 7;
-        uint32_t sa = 0, cp = 0;
+        // ------------------------------------------------------------ dequant (packed smem -> f16 weights)
+        // Thread t: weight block m (gate/up: W1 / W3; down: first / second W2 block), strip
+        // of 16 rows, 32-column group gsel of the stage, rows g and g + 8 of the strip, half
+        // h of their 32 columns: one 16-byte load (a warp reads 512 contiguous bytes),
+        // 2 x 4 eight-byte stores.
+        const int t = threadIdx.x - kWarpDq0 * 32;             // 0..511
+        const int m = t >> 8;
+        const int u = t & 255, strip = u >> 5, gsel = (u >> 4) & 1, g = (u >> 1) & 7, h = u & 1;
+        uint32_t st = 0, cp = 0;
         for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
-            const GItem it = gitem<MODE>(a, n_units, i);
+            const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
+            const bool active = !it.shared && m * kTileRows < it.nw;
             int bmax = 0;
-            if (!it.shared && active) {
-                const int mm = MODE == kGU ? m : 2;
+            if (active)
                 bmax = (int)*reinterpret_cast<const uint32_t *>(
-                    a.table + trailer_offset(a.E, a.d, a.f, it.id, mm, it.rb));
-            }
-            for (int ks = 0; ks < nks; ks++, sa++) {
+                    a.table + (MODE == kGU ? trailer_offset(a.E, a.d, a.f, it.id, m, it.rb)
+                                           : trailer_offset(a.E, a.d, a.f, it.id, 2, 2 * it.rb + m)));
+            for (int ks = 0; ks < nks; ks++, st++) {
                 if (!it.shared && (ks & 1) == 0 && !mb_wait(&full_p[cp % kStgP], (cp / kStgP) & 1u)) { timeout(); break; }
-                if (!wait_free(empty_a, kStgA, sa)) { timeout(); break; }
-                if (!it.shared && active) {
+                if (!wait_free(empty_w, kStgW, st)) { timeout(); break; }
+                if (active) {
                     const int c = 2 * (ks & 1) + gsel;
                     const uint8_t *tile = smP + (cp % kStgP) * kPBytes + m * kTileBytes;
-                    const uint4 *src = reinterpret_cast<const uint4 *>(tile + (strip * 4 + c) * 256 + 32 * g);
-                    const uint4 p0 = src[0], p1 = src[1];
-                    const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-                    uint8_t *A = smA + (sa % kStgA) * kABytes + m * (kBM * kBK * 2);
+                    // pieces 2h and 2h+1 of lanes 4g..4g+3: each 4 bytes of row g, then 4 of row g+8
+                    const uint4 q = *reinterpret_cast<const uint4 *>(tile + (strip * 4 + c) * 256 + 32 * g + 16 * h);
+                    uint8_t *Wt = smW + (st % kStgW) * kWBytes + m * (kTileRows * kBK * 2);
 #pragma unroll
                     for (int hr = 0; hr < 2; hr++) {            // rows g and g+8 of the strip
                         const int r = strip * 16 + g + 8 * hr;
                         const uint32_t b = tile[kTileNibbleBytes + r * 4 + c];
                         const uint32_t s1 = b == 255u ? 0u : f16_pow2((int)b - bmax + 13);
                         const uint32_t s2 = s1 | (s1 << 16);
+                        const uint32_t wa = hr ? q.y : q.x, wb = hr ? q.w : q.z;
 #pragma unroll
-                        for (int j = 0; j < 4; j++) {           // 8 columns per 16-byte store
-                            uint32_t v[4];
-#pragma unroll
-                            for (int tt = 0; tt < 4; tt++)
-                                v[tt] = hmul2(e2m1x2_f16x2(w[2 * tt + hr] >> (8 * j)), s2);
+                        for (int j = 0; j < 4; j++) {           // columns 8j + 4h .. +3 of the group
+                            const uint32_t v0 = hmul2(e2m1x2_f16x2(wa >> (8 * j)), s2);
+                            const uint32_t v1 = hmul2(e2m1x2_f16x2(wb >> (8 * j)), s2);
                             const int chunk = 4 * gsel + j;
-                            *reinterpret_cast<uint4 *>(A + r * 128 + ((chunk ^ (r & 7)) << 4)) =
-                                make_uint4(v[0], v[1], v[2], v[3]);
+                            *reinterpret_cast<uint2 *>(Wt + r * 128 + ((chunk ^ (r & 7)) << 4) + 8 * h) =
+                                make_uint2(v0, v1);
                         }
                     }
                     fence_async_smem();
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    mb_arrive(&full_a[sa % kStgA]);
+                    mb_arrive(&full_w[st % kStgW]);
                     if (!it.shared && (ks & 1)) mb_arrive(&empty_p[cp % kStgP]);
                 }
                 if (!it.shared && (ks & 1)) cp++;
             }
         }
     } else if (warp < kWarpPack) {
-        // ------------------------------------------------------------ epilogue
+        // ------------------------------------------------------------ epilogue: one token per thread
         const int q = warp & 3;                                 // TMEM lane quadrant
-        const int row = 32 * q + lane;
+        const int tr = 32 * q + lane;                           // token row of the tile
         uint32_t n = 0;
         for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x, n++) {
-            const GItem it = gitem<MODE>(a, n_units, i);
+            const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
             const int buf = n & 1;
-            float f1 = 1.0f, f3 = 1.0f;
+            const bool valid = tr < it.ncols;
+            int row = 0;                                        // gate/up: h row; down: output token
+            float fo = 1.0f;                                    // gate/up: token factor; down: routing weight
+            if (valid) {
+                if (it.shared) {
+                    row = MODE == kGU ? a.T * a.k + it.id * a.T + it.n0 + tr : it.n0 + tr;
+                } else {
+                    const int p = it.tok0 + it.n0 + tr;
+                    const int slot = min(max(a.perm[p], 0), a.T * a.k - 1);
+                    if (MODE == kGU) {
+                        row = p;
+                        fo = a.tok_scale[a.T + slot / a.k];
+                    } else {
+                        row = slot / a.k;
+                        fo = a.weight[slot];
+                    }
+                }
+            }
+            float f1 = 1.0f, f3 = 1.0f;                         // block factors 2^(bmax - 140)
             if (!it.shared) {
-                const int mm1 = MODE == kGU ? 0 : 2;
-                f1 = ldexpf(1.0f, (int)*reinterpret_cast<const uint32_t *>(
-                                      a.table + trailer_offset(a.E, a.d, a.f, it.id, mm1, it.rb)) - 140);
-                if (MODE == kGU)
-                    f3 = ldexpf(1.0f, (int)*reinterpret_cast<const uint32_t *>(
-                                          a.table + trailer_offset(a.E, a.d, a.f, it.id, 1, it.rb)) - 140);
+                const size_t o1 = MODE == kGU ? trailer_offset(a.E, a.d, a.f, it.id, 0, it.rb)
+                                              : trailer_offset(a.E, a.d, a.f, it.id, 2, 2 * it.rb);
+                f1 = ldexpf(1.0f, (int)*reinterpret_cast<const uint32_t *>(a.table + o1) - 140);
+                if (it.nw == kWRows) {
+                    const size_t o3 = MODE == kGU ? trailer_offset(a.E, a.d, a.f, it.id, 1, it.rb)
+                                                  : trailer_offset(a.E, a.d, a.f, it.id, 2, 2 * it.rb + 1);
+                    f3 = ldexpf(1.0f, (int)*reinterpret_cast<const uint32_t *>(a.table + o3) - 140);
+                }
             }
             if (!mb_wait(&acc_full[buf], (n >> 1) & 1u)) { timeout(); break; }
             tc_fence_after();
-            const int grow = it.rb * kBM + row;
             const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * 256u;
-            for (int c0 = 0; c0 < it.bn; c0 += 16) {
-                float vg[16], vu[16];
-                tmem_ld16(lane_addr + c0, vg);
-                if (MODE == kGU) tmem_ld16(lane_addr + 128 + c0, vu);
+            if (MODE == kGU) {
+                const float fg = f1 * fo, fu = f3 * fo;
+                uint16_t *hrow = a.hp + (size_t)row * a.f + it.rb * kTileRows;
+                for (int c0 = 0; c0 < kTileRows; c0 += 16) {
+                    float vg[16], vu[16];
+                    tmem_ld16(lane_addr + c0, vg);
+                    tmem_ld16(lane_addr + kTileRows + c0, vu);
+                    uint32_t pk[8];
 #pragma unroll
-                for (int jj = 0; jj < 16; jj++) {
-                    const int col = c0 + jj;
-                    if (col >= it.ncols) break;
-                    if (MODE == kGU) {
-                        size_t hrow;
-                        float fo = 1.0f;
+                    for (int jj = 0; jj < 16; jj += 2) {
+                        const float h0 = situ(vg[jj] * fg, vu[jj] * fu, a.b1, a.b2);
+                        const float h1 = situ(vg[jj + 1] * fg, vu[jj + 1] * fu, a.b1, a.b2);
                         if (it.shared) {
-                            hrow = (size_t)a.T * a.k + (size_t)it.id * a.T + it.n0 + col;
+                            const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+                            pk[jj / 2] = *reinterpret_cast<const uint32_t *>(&hb);
                         } else {
-                            const int p = it.tok0 + it.n0 + col;
-                            hrow = (size_t)p;
-                            const int slot = min(max(a.perm[p], 0), a.T * a.k - 1);
-                            fo = a.tok_scale[a.T + slot / a.k];
+                            const __half2 hh = __floats2half2_rn(h0, h1);
+                            pk[jj / 2] = *reinterpret_cast<const uint32_t *>(&hh);
                         }
-                        const float h = situ(vg[jj] * f1 * fo, vu[jj] * f3 * fo, a.b1, a.b2);
-                        uint16_t hv;
-                        if (it.shared) {
-                            const __nv_bfloat16 hb = __float2bfloat16_rn(h);
-                            hv = *reinterpret_cast<const uint16_t *>(&hb);
-                        } else {
-                            const __half hh = __float2half_rn(h);
-                            hv = *reinterpret_cast<const uint16_t *>(&hh);
-                        }
-                        a.hp[hrow * a.f + grow] = hv;
-                    } else {
-                        int t;
-                        float wt = 1.0f;
-                        if (it.shared) {
-                            t = it.n0 + col;
-                        } else {
-                            const int p = it.tok0 + it.n0 + col;
-                            const int slot = min(max(a.perm[p], 0), a.T * a.k - 1);
-                            t = slot / a.k;
-                            wt = a.weight[slot];
-                        }
-                        atomicAdd(a.out + (size_t)t * a.d + grow, wt * (vg[jj] * f1));
+                    }
+                    if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(hrow + c0);
+                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
+                }
+            } else {
+                float *orow = a.out + (size_t)row * a.d + 2 * it.rb * kTileRows;
+                for (int c0 = 0; c0 < it.nw; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(lane_addr + c0, v);
+                    const float fw = fo * (c0 < kTileRows ? f1 : f3);
+                    if (valid) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 4)
+                            atomicAdd(reinterpret_cast<float4 *>(orow + c0 + jj),
+                                      make_float4(v[jj] * fw, v[jj + 1] * fw, v[jj + 2] * fw, v[jj + 3] * fw));
                     }
                 }
             }
@@ -571,12 +593,12 @@ cudaError_t launch_gemm(const GemmArgs &ga, const CUtensorMap &mbr, const CUtens
 {
     static bool set = false;
     if (!set) {
-        cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, GG<MODE>::kSmem);
+        cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
         set = true;
     }
     const int grid = max(1, min(num_sms(), max_items));
     timing_begin(name, s);
-    gemm_kernel<MODE><<<grid, kGemmThreads, GG<MODE>::kSmem, s>>>(ga, mbr, mbs, ma1, ma3);
+    gemm_kernel<MODE><<<grid, kGemmThreads, kGemmSmem, s>>>(ga, mbr, mbs, ma1, ma3);
     count_launch();
     timing_end(name, s);
     return cudaGetLastError();
@@ -604,7 +626,9 @@ cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x,
 
     cudaError_t err = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * c.d, s);
     if (err != cudaSuccess) return err;
-    UnitsArgs ua{T, E, k, S, c.f / kBM, c.d / kBM, offsets, units, prefix_gu, prefix_dn, n_units, status, abort};
+    // items per token tile: gate/up one per 128-row block of f, down one per pair of 128-row blocks of d
+    UnitsArgs ua{T, E, k, S, c.f / kTileRows, (c.d / kTileRows + 1) / 2, offsets, units, prefix_gu,
+                 prefix_dn, n_units, status, abort};
     timing_begin("gemm_units", s);
     gemm_units_kernel<<<1, 1024, 0, s>>>(ua);
     count_launch();
@@ -624,9 +648,9 @@ cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x,
     }
 
     CUtensorMap mb_routed{}, mb_shared{}, ma1{}, ma3{}, mb_h{}, ma2{};
-    bool ok = map16(&mb_routed, xg, (uint64_t)T * k, c.d, 16) && map16(&mb_h, hp, rows_all, c.f, 16);
+    bool ok = map16(&mb_routed, xg, (uint64_t)T * k, c.d, kBM) && map16(&mb_h, hp, rows_all, c.f, kBM);
     if (S > 0)
-        ok = ok && map16(&mb_shared, x, (uint64_t)T, c.d, 16) &&
+        ok = ok && map16(&mb_shared, x, (uint64_t)T, c.d, kBM) &&
              map16(&ma1, sh_w1, (uint64_t)S * c.f, c.d, kBM) && map16(&ma3, sh_w3, (uint64_t)S * c.f, c.d, kBM) &&
              map16(&ma2, sh_w2, (uint64_t)S * c.d, c.f, kBM);
     if (!ok) return cudaErrorInvalidValue;
@@ -635,11 +659,11 @@ cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x,
                 tok_scale, table, expert_bytes(c.d, c.f), gateup_block_bytes(c.d, c.f), hp, out, abort, status};
     // an upper bound on the items: every slot its own expert
     const int max_tiles = (int)std::min<long long>((long long)T * k + (long long)(E + S), (long long)1 << 30);
-    err = launch_gemm<kGU>(ga, mb_routed, mb_shared, ma1, ma3, max_tiles * (c.f / kBM), s, "gemm_gateup");
+    err = launch_gemm<kGU>(ga, mb_routed, mb_shared, ma1, ma3, max_tiles * (c.f / kTileRows), s, "gemm_gateup");
     if (err != cudaSuccess) return err;
     GemmArgs gd = ga;
     gd.prefix = prefix_dn;
-    err = launch_gemm<kDN>(gd, mb_h, mb_h, ma2, ma2, max_tiles * (c.d / kBM), s, "gemm_down");
+    err = launch_gemm<kDN>(gd, mb_h, mb_h, ma2, ma2, max_tiles * ((c.d / kTileRows + 1) / 2), s, "gemm_down");
     return err;
 }
 

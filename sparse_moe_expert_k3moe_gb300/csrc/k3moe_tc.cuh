@@ -53,6 +53,16 @@ __device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *m, int c0, i
         "l"(m), "r"(c0), "r"(c1), "r"(saddr(bar))
         : "memory");
 }
+// Plain bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16),
+// completing on an mbarrier's transaction count.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            saddr(dst)),
+        "l"(src), "r"(bytes), "r"(saddr(bar))
+        : "memory");
+}
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
