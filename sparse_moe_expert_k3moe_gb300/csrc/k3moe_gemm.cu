@@ -16,26 +16,27 @@
 //   gemm<DN>     y = W2 h; out[t] += w_slot * y (routed) or += y (shared) with fp32
 //                atomics onto out (zeroed first).
 //
-// One work item = 128 weight rows of one unit x up to 128 (gate/up) or 256 (down) of its
-// tokens x the whole K.  Warp roles in a block (one block per SM):
-//   warp 0       producer: TMA 2-D loads of the B tiles (64 columns x 16 rows per copy)
-//                and, for bf16 shared experts, of the A tiles;
-//   warp 1       MMA: one thread issues tcgen05.mma (kind::f16, M=128, N=tile, K=16)
-//                into fp32 accumulators in tensor memory, two buffers of 256 columns
-//                (gate/up: g at +0, u at +128), so one item's MMAs overlap the previous
-//                item's epilogue;
-//   warps 2-17   dequant: packed MXFP4 tiles from shared memory to f16 A tiles
+// One work item = 128 tokens of one unit (the MMA M side) x 256 weight rows (N: gate/up
+// the 128-row blocks of W1 and W3 for one block of f, down two 128-row blocks of W2)
+// x the whole K.  Warp roles in a block (one block per SM):
+//   warp 0       producer: TMA 2-D loads of the token tiles (64 columns x 128 rows) and,
+//                for bf16 shared experts, of the weight tiles;
+//   warp 1       MMA: one thread issues tcgen05.mma (kind::f16, M=128, N=256, K=16) into
+//                fp32 accumulators in tensor memory, two buffers of 256 columns, so one
+//                item's MMAs overlap the previous item's epilogue;
+//   warps 2-17   dequant: packed MXFP4 tiles from shared memory to f16 weight tiles
 //                (128-byte swizzle, K-major) -- the E2M1 pair decoded by the hardware
 //                conversion, times 2^(b - bmax + 13) where bmax is the largest scale of
 //                the 128-row block (the packed table's trailer), so every value is exact
 //                in f16 while the block's scales span at most 36 binades; the epilogue
 //                multiplies by 2^(bmax - 140);
-//   warps 18-21  epilogue: tcgen05.ld the accumulators (warp w reads lanes 32(w%4)..),
-//                apply the scales, SiTU or the weighted combine, store;
+//   warps 18-21  epilogue, one token per thread (warp w reads TMEM lanes 32(w%4)..):
+//                gate/up SiTU to h rows, down the weighted combine as float4 atomics;
 //   warp 22      packed-weight producer: one bulk copy per 128-column packed tile (pair),
 //                kStgP tiles ahead of the dequant warps.
-// Rings: packed tiles (kStgP), f16 A stages (kStgA) and B stages (kStgB); the MMA thread
-// releases an A and a B stage with one tcgen05.commit each.
+// Rings: packed tiles (kStgP) and stages (kStg) of one token tile and one weight tile,
+// each stage with one full barrier (TMA bytes + an arrive per dequant warp) and one
+// empty barrier (the MMA thread's tcgen05.commit).
 // Every wait is bounded by a clock limit; a timeout sets the status word and the
 // roles drop out.
 #include <cuda.h>
@@ -51,7 +52,7 @@ namespace {
 
 constexpr int kBM = 128, kBK = 64;          // token rows per tile (MMA M), K per stage
 constexpr int kWRows = 256;                 // weight rows per item (MMA N): W1|W3, or two W2 blocks
-constexpr int kStgA = 4, kStgW = 2, kStgP = 4;   // token, weight and packed-weight rings
+constexpr int kStg = 3, kStgP = 4;          // stage ring (token + weight tiles), packed-weight ring
 constexpr int kNumDq = 16;
 constexpr int kWarpProd = 0, kWarpMma = 1, kWarpDq0 = 2, kWarpEpi0 = 2 + kNumDq, kNumEpi = 4;
 constexpr int kWarpPack = kWarpEpi0 + kNumEpi;                 // 22
@@ -60,7 +61,7 @@ constexpr int kTmemCols = 512;
 constexpr int kABytes = kBM * kBK * 2;                          // token tile of a stage
 constexpr int kWBytes = kWRows * kBK * 2;                       // weight tile of a stage
 constexpr int kPBytes = 2 * kTileBytes;                         // two packed 128 x 128 tiles
-constexpr int kGemmSmem = kStgA * kABytes + kStgW * kWBytes + kStgP * kPBytes + 2048;
+constexpr int kGemmSmem = kStg * (kABytes + kWBytes) + kStgP * kPBytes + 2048;
 static_assert(kGemmSmem + 8 * 1024 <= 232448, "shared memory per block (dynamic + static)");
 
 enum { kGU = 0, kDN = 1 };
@@ -298,11 +299,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 {
     extern __shared__ __align__(1024) uint8_t gsm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *smA = sm;                                   // kStgA x kABytes: token tiles
-    uint8_t *smW = smA + kStgA * kABytes;                // kStgW x kWBytes: weight tiles
-    uint8_t *smP = smW + kStgW * kWBytes;                // kStgP x kPBytes: packed weights
-    __shared__ uint64_t full_p[kStgP], empty_p[kStgP], full_a[kStgA], empty_a[kStgA], full_w[kStgW],
-        empty_w[kStgW], acc_full[2], acc_empty[2], drain;
+    uint8_t *smA = sm;                                   // kStg x kABytes: token tiles
+    uint8_t *smW = smA + kStg * kABytes;                 // kStg x kWBytes: weight tiles
+    uint8_t *smP = smW + kStg * kWBytes;                 // kStgP x kPBytes: packed weights
+    // full[s]: the token tile (TMA bytes, one arrive by the producer) and the weight tile
+    // (one arrive per dequant warp); empty[s]: one tcgen05.commit per stage
+    __shared__ uint64_t full_p[kStgP], empty_p[kStgP], full[kStg], empty[kStg], acc_full[2], acc_empty[2], drain;
     __shared__ uint32_t tmem_base;
     __shared__ int bail;
     __shared__ int32_t s_prefix[kMaxExperts + kMaxShared + 1];   // item prefix of the units
@@ -316,8 +318,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStgP; s++) { mb_init(&full_p[s], 1); mb_init(&empty_p[s], kNumDq); }
-        for (int s = 0; s < kStgA; s++) { mb_init(&full_a[s], 1); mb_init(&empty_a[s], 1); }
-        for (int s = 0; s < kStgW; s++) { mb_init(&full_w[s], kNumDq); mb_init(&empty_w[s], 1); }
+        for (int s = 0; s < kStg; s++) { mb_init(&full[s], 1 + kNumDq); mb_init(&empty[s], 1); }
         for (int b = 0; b < 2; b++) { mb_init(&acc_full[b], 1); mb_init(&acc_empty[b], kNumEpi); }
         mb_init(&drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -338,26 +339,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         bail = 1;
     };
     // a stage counter st of a ring of depth D: slot st % D, fill number st / D
-    auto wait_free = [&](uint64_t *bars, int D, uint32_t st) -> bool {
-        return st < (uint32_t)D || mb_wait(&bars[st % D], ((st / D) - 1) & 1u);
+    auto wait_free_warp = [&](uint64_t *bars, int D, uint32_t st) -> bool {
+        return st < (uint32_t)D || mb_wait_warp(&bars[st % D], ((st / D) - 1) & 1u);
     };
     // after a timeout: wait (bounded) for the copies of the last D fills of a ring
     auto drain_fills = [&](uint64_t *bars, int D, uint32_t n) {
         for (uint32_t f = n > (uint32_t)D ? n - D : 0; f < n; f++) mb_wait(&bars[f % D], (f / D) & 1u);
     };
+    // the shared stop flag as lane 0 of the warp reads it (keeps loop exits warp-uniform)
+    auto stop = [&]() -> bool { return __shfl_sync(0xffffffffu, bail, 0) != 0; };
 
     if (warp == kWarpPack) {
         // ------------------------------------------------------------ packed-weight producer
-        if (lane == 0) {
-            uint32_t cp = 0;
-            for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
-                const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
-                if (it.shared) continue;
-                const uint8_t *ex = a.table + (size_t)it.id * a.expert_bytes;
-                for (int kt = 0; kt < K / kTileK; kt++, cp++) {
-                    if (!wait_free(empty_p, kStgP, cp)) { timeout(); break; }
-                    const int sp = cp % kStgP;
-                    uint8_t *dst = smP + sp * kPBytes;
+        uint32_t cp = 0;
+        bool failed = false;
+        for (int i = blockIdx.x; i < n_items && !failed && !stop(); i += gridDim.x) {
+            const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
+            if (it.shared) continue;
+            const uint8_t *ex = a.table + (size_t)it.id * a.expert_bytes;
+            for (int kt = 0; kt < K / kTileK; kt++, cp++) {
+                if (!wait_free_warp(empty_p, kStgP, cp)) { timeout(); failed = true; break; }
+                const int sp = cp % kStgP;
+                uint8_t *dst = smP + sp * kPBytes;
+                if (lane == 0) {
                     if (MODE == kGU) {          // the W1 and W3 tiles of a block are adjacent
                         mb_expect_tx(&full_p[sp], (uint32_t)(2 * kTileBytes));
                         bulk_g2s(dst, ex + ((size_t)it.rb * (a.d / kTileK) + kt) * 2 * kTileBytes,
@@ -371,31 +375,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                                      kTileBytes, &full_p[sp]);
                     }
                 }
+                __syncwarp();
             }
-            if (bail) drain_fills(full_p, kStgP, cp);
         }
+        if (lane == 0 && bail) drain_fills(full_p, kStgP, cp);
+        __syncwarp();
     } else if (warp == kWarpProd) {
         // ------------------------------------------------------------ token tiles (and bf16 weights)
-        if (lane == 0) {
-            uint32_t st = 0;
-            for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
-                const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
-                const CUtensorMap *mt = it.shared ? &mtok_shared : &mtok_routed;
-                int row0;
-                if (MODE == kGU) row0 = it.shared ? it.n0 : it.tok0 + it.n0;
-                else row0 = it.shared ? a.T * a.k + it.id * a.T + it.n0 : it.tok0 + it.n0;
-                const int nb = it.nw / kTileRows;
-                for (int ks = 0; ks < nks; ks++, st++) {
-                    if (!wait_free(empty_a, kStgA, st) || (it.shared && !wait_free(empty_w, kStgW, st))) {
-                        timeout();
-                        break;
-                    }
-                    uint64_t *fa = &full_a[st % kStgA];
-                    // the bf16 weight tiles of a shared expert land on the token barrier too
+        uint32_t st = 0;
+        bool failed = false;
+        for (int i = blockIdx.x; i < n_items && !failed && !stop(); i += gridDim.x) {
+            const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
+            const CUtensorMap *mt = it.shared ? &mtok_shared : &mtok_routed;
+            int row0;
+            if (MODE == kGU) row0 = it.shared ? it.n0 : it.tok0 + it.n0;
+            else row0 = it.shared ? a.T * a.k + it.id * a.T + it.n0 : it.tok0 + it.n0;
+            const int nb = it.nw / kTileRows;
+            for (int ks = 0; ks < nks; ks++, st++) {
+                if (!wait_free_warp(empty, kStg, st)) {
+                    timeout();
+                    failed = true;
+                    break;
+                }
+                if (lane == 0) {
+                    uint64_t *fa = &full[st % kStg];
+                    // the bf16 weight tiles of a shared expert come by TMA too
                     mb_expect_tx(fa, (uint32_t)kABytes + (it.shared ? (uint32_t)(nb * kTileRows * kBK * 2) : 0u));
-                    tma2d(smA + (st % kStgA) * kABytes, mt, ks * kBK, row0, fa);
+                    tma2d(smA + (st % kStg) * kABytes, mt, ks * kBK, row0, fa);
                     if (it.shared) {
-                        uint8_t *W = smW + (st % kStgW) * kWBytes;
+                        uint8_t *W = smW + (st % kStg) * kWBytes;
                         if (MODE == kGU) {
                             const int wrow = it.id * a.f + it.rb * kTileRows;
                             tma2d(W, &mw1, ks * kBK, wrow, fa);
@@ -407,37 +415,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                         }
                     }
                 }
+                __syncwarp();
             }
-            if (bail) drain_fills(full_a, kStgA, st);
         }
+        if (lane == 0 && bail) drain_fills(full, kStg, st);
+        __syncwarp();
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issue: D[token][weight row]
-        if (lane == 0) {
-            uint32_t st = 0, n = 0;
-            for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x, n++) {
-                const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
-                const uint32_t id = idesc(it.shared ? 1 : 0, it.nw);
-                const int buf = n & 1;
-                if (n >= 2 && !mb_wait(&acc_empty[buf], ((n >> 1) - 1) & 1u)) { timeout(); break; }
+        uint32_t st = 0, n = 0;
+        bool failed = false;
+        for (int i = blockIdx.x; i < n_items && !failed && !stop(); i += gridDim.x, n++) {
+            const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
+            const uint32_t id = idesc(it.shared ? 1 : 0, it.nw);
+            const int buf = n & 1;
+            if (n >= 2 && !mb_wait_warp(&acc_empty[buf], ((n >> 1) - 1) & 1u)) { timeout(); break; }
+            tc_fence_after();
+            const uint32_t d0 = tmem + (uint32_t)buf * 256u;
+            for (int ks = 0; ks < nks; ks++, st++) {
+                if (!mb_wait_warp(&full[st % kStg], (st / kStg) & 1u)) {
+                    timeout();
+                    failed = true;
+                    break;
+                }
                 tc_fence_after();
-                const uint32_t d0 = tmem + (uint32_t)buf * 256u;
-                for (int ks = 0; ks < nks; ks++, st++) {
-                    if (!mb_wait(&full_a[st % kStgA], (st / kStgA) & 1u) ||
-                        !mb_wait(&full_w[st % kStgW], (st / kStgW) & 1u)) { timeout(); break; }
-                    tc_fence_after();
-                    const uint32_t A = saddr(smA + (st % kStgA) * kABytes), W = saddr(smW + (st % kStgW) * kWBytes);
+                if (lane == 0) {
+                    const uint32_t A = saddr(smA + (st % kStg) * kABytes);
+                    const uint32_t W = saddr(smW + (st % kStg) * kWBytes);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; kk++)
                         umma(d0, sdesc(A + kk * 32), sdesc(W + kk * 32), id, (ks | kk) != 0);
-                    umma_commit(&empty_a[st % kStgA]);
-                    umma_commit(&empty_w[st % kStgW]);
+                    umma_commit(&empty[st % kStg]);
                 }
-                if (bail) break;
-                umma_commit(&acc_full[buf]);
+                __syncwarp();
             }
+            if (failed) break;
+            if (lane == 0) umma_commit(&acc_full[buf]);
+            __syncwarp();
+        }
+        if (lane == 0) {
             umma_commit(&drain);                       // every issued MMA done before the dealloc
             mb_wait(&drain, 0);
         }
+        __syncwarp();
     } else if (warp < kWarpEpi0) {
         // ------------------------------------------------------------ dequant (packed smem -> f16 weights)
         // Thread t: weight block m (gate/up: W1 / W3; down: first / second W2 block), strip
@@ -448,7 +467,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         const int m = t >> 8;
         const int u = t & 255, strip = u >> 5, gsel = (u >> 4) & 1, g = (u >> 1) & 7, h = u & 1;
         uint32_t st = 0, cp = 0;
-        for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
+        for (int i = blockIdx.x; i < n_items && !stop(); i += gridDim.x) {
             const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
             const bool active = !it.shared && m * kTileRows < it.nw;
             int bmax = 0;
@@ -457,14 +476,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     a.table + (MODE == kGU ? trailer_offset(a.E, a.d, a.f, it.id, m, it.rb)
                                            : trailer_offset(a.E, a.d, a.f, it.id, 2, 2 * it.rb + m)));
             for (int ks = 0; ks < nks; ks++, st++) {
-                if (!it.shared && (ks & 1) == 0 && !mb_wait(&full_p[cp % kStgP], (cp / kStgP) & 1u)) { timeout(); break; }
-                if (!wait_free(empty_w, kStgW, st)) { timeout(); break; }
+                if (!it.shared && (ks & 1) == 0 && !mb_wait_warp(&full_p[cp % kStgP], (cp / kStgP) & 1u)) {
+                    timeout();
+                    break;
+                }
+                if (!wait_free_warp(empty, kStg, st)) { timeout(); break; }
                 if (active) {
                     const int c = 2 * (ks & 1) + gsel;
                     const uint8_t *tile = smP + (cp % kStgP) * kPBytes + m * kTileBytes;
                     // pieces 2h and 2h+1 of lanes 4g..4g+3: each 4 bytes of row g, then 4 of row g+8
                     const uint4 q = *reinterpret_cast<const uint4 *>(tile + (strip * 4 + c) * 256 + 32 * g + 16 * h);
-                    uint8_t *Wt = smW + (st % kStgW) * kWBytes + m * (kTileRows * kBK * 2);
+                    uint8_t *Wt = smW + (st % kStg) * kWBytes + m * (kTileRows * kBK * 2);
 #pragma unroll
                     for (int hr = 0; hr < 2; hr++) {            // rows g and g+8 of the strip
                         const int r = strip * 16 + g + 8 * hr;
@@ -485,7 +507,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    mb_arrive(&full_w[st % kStgW]);
+                    mb_arrive(&full[st % kStg]);
                     if (!it.shared && (ks & 1)) mb_arrive(&empty_p[cp % kStgP]);
                 }
                 if (!it.shared && (ks & 1)) cp++;
@@ -496,7 +518,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         const int q = warp & 3;                                 // TMEM lane quadrant
         const int tr = 32 * q + lane;                           // token row of the tile
         uint32_t n = 0;
-        for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x, n++) {
+        for (int i = blockIdx.x; i < n_items && !stop(); i += gridDim.x, n++) {
             const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
             const int buf = n & 1;
             const bool valid = tr < it.ncols;
@@ -528,7 +550,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     f3 = ldexpf(1.0f, (int)*reinterpret_cast<const uint32_t *>(a.table + o3) - 140);
                 }
             }
-            if (!mb_wait(&acc_full[buf], (n >> 1) & 1u)) { timeout(); break; }
+            if (!mb_wait_warp(&acc_full[buf], (n >> 1) & 1u)) { timeout(); break; }
             tc_fence_after();
             const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * 256u;
             if (MODE == kGU) {

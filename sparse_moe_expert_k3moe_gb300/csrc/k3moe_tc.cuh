@@ -45,6 +45,14 @@ __device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t parity)
         if ((i & 31u) == 31u && clock64() - t0 > kTcWaitCyc) return false;
     }
 }
+// The whole warp waits (every lane polls); the result is the same on every lane.  A
+// role whose loop runs on all 32 lanes keeps its warp converged, and issues its single
+// thread operations under lane 0.
+__device__ __forceinline__ bool mb_wait_warp(uint64_t *b, uint32_t parity)
+{
+    const bool ok = mb_wait(b, parity);
+    return __all_sync(0xffffffffu, ok);
+}
 __device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *m, int c0, int c1, uint64_t *bar)
 {
     asm volatile(
