@@ -437,13 +437,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     failed = true;
                     break;
                 }
-                tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t A = saddr(smA + (st % kStg) * kABytes);
-                    const uint32_t W = saddr(smW + (st % kStg) * kWBytes);
+                    // descriptors of the stage's first K slice; each further slice of 16 is
+                    // 32 bytes on, i.e. 2 in the descriptor's start-address field
+                    const uint64_t dA = sdesc(saddr(smA + (st % kStg) * kABytes));
+                    const uint64_t dW = sdesc(saddr(smW + (st % kStg) * kWBytes));
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; kk++)
-                        umma(d0, sdesc(A + kk * 32), sdesc(W + kk * 32), id, (ks | kk) != 0);
+                        umma(d0, dA + 2 * kk, dW + 2 * kk, id, (ks | kk) != 0);
                     umma_commit(&empty[st % kStg]);
                 }
                 __syncwarp();

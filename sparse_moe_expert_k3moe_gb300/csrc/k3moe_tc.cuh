@@ -32,6 +32,16 @@ __device__ __forceinline__ void mb_expect_tx(uint64_t *b, uint32_t bytes)
 __device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t parity)
 {
     const uint32_t a = saddr(b);
+    {   // fast path: the phase is usually complete already
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
     const long long t0 = clock64();
     for (uint32_t i = 0;; i++) {
         uint32_t done;
