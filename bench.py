@@ -59,6 +59,33 @@ def dist_env():
     return rank, world, local
 
 
+# ----------------------------------------------------------------------------- replicas (N > 1)
+# The layer does not shard: N GPUs run N independent replicas of the same step.  The
+# only collectives are the timing barrier and the max over ranks of the timed region.
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(v: float, world: int, device=None) -> float:
+    """Max of v over the ranks of the initialised process group (v itself when N = 1)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, tokens_per_step: int, steps: int, ms_max: float) -> float:
+    """Whole-job tokens/s: each replica processes tokens_per_step per step, and the job
+    takes as long as the slowest replica."""
+    return world * tokens_per_step * steps / (ms_max / 1000.0)
+
+
 # ----------------------------------------------------------------------------- algorithmic work
 
 def layer_bytes_flops(w, distinct_experts: int):
@@ -204,8 +231,10 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- CPU oracle timing
 
 def time_oracle(w, budget_s: float):
-    """Route + forward of the oracle on this host's cores over a bounded sample of
-    the workload's tokens; returns (tokens/s, tokens timed, threads, seconds)."""
+    """Route + forward of the oracle on this host's cores over a bounded sample of the
+    workload: its tokens in order, cycling back to the first when a small workload (T=1)
+    is used up, until budget_s seconds of oracle work; returns (tokens/s, tokens timed,
+    threads, seconds)."""
     import numpy as np
     import k3moe_inputs as ki
     import oracle
@@ -216,10 +245,9 @@ def time_oracle(w, budget_s: float):
     shared = ki.make_shared(w) if w.S else None
     experts = {}
     done, spent = 0, 0.0
-    order = list(range(w.T))
     batch = max(1, min(w.T, oracle.num_threads()))
-    while done < w.T and spent < budget_s:
-        rows = order[done:done + batch]
+    while spent < budget_s:
+        rows = [(done + i) % w.T for i in range(batch)]
         xs = np.ascontiguousarray(x[rows])
         idx, wt, _ = oracle.route(c, xs, Wr, bias)        # untimed draw of the needed experts
         for e in set(idx.ravel().tolist()) - set(experts):
@@ -286,17 +314,10 @@ def gpu_arm(args):
         dist.init_process_group("nccl", device_id=dev)
 
     def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+        dist_barrier(world)
 
     def allmax(v: float) -> float:
-        if world == 1:
-            return v
-        import torch.distributed as dist
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return dist_max(v, world, dev)
 
     w = workload_from(args.workload)
     layer = build_layer(w, device=dev)
@@ -339,7 +360,7 @@ def gpu_arm(args):
     clk = clocks.stop()
     ms = sum(a.elapsed_time(b) for a, b in ev)
     ms = allmax(ms)
-    value = world * w.T * args.steps / (ms / 1000.0)
+    value = job_value(world, w.T, args.steps, ms)
 
     # ---- per-kernel durations (separate pass, same work, library-side CUDA events)
     k3.k3moe_timing_reset()
@@ -387,7 +408,7 @@ def gpu_arm(args):
                 ee[i - 2][1].record(stream)
         torch.cuda.synchronize(dev)
         ems = allmax(sum(a.elapsed_time(b) for a, b in ee))
-        e2e = {"value": world * w.T * args.steps / (ems / 1000.0), "unit": "tokens/s",
+        e2e = {"value": job_value(world, w.T, args.steps, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
                "d2h_bytes_per_step": int(oh.numel() * oh.element_size())}
 
@@ -396,7 +417,8 @@ def gpu_arm(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, n, threads, s = time_oracle(w, args.cpu_budget_s)
         cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n} of {w.T} tokens of {w.name}, route + forward, {s:.1f} s"}
+               "sample": f"{n} tokens of {w.name} (its {w.T} tokens in order, cycling), "
+                         f"route + forward, {s:.1f} s of oracle work"}
 
     if rank == 0:
         line = {
