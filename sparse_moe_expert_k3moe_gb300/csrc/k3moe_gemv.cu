@@ -48,6 +48,7 @@ constexpr int kStages = 4;
 constexpr int kNBMax = 2;                          // n-blocks of 8 tokens per pass
 constexpr int kPassTok = 8 * kNBMax;
 constexpr int kSharedK = 64;                       // K per stage for bf16 tiles (one matrix)
+constexpr int kBSlots = 2;                         // staged B operands (double buffer)
 constexpr long long kWaitCycles = 4000000000ll;      // bounded waits: ~2 s at 2 GHz
 
 enum Mode { kGateUp = 0, kDown = 1 };
@@ -184,18 +185,68 @@ struct PrepArgs {
     int32_t *active;     // [E + 1]
     int32_t *inv;        // [T * k]
     float *tok_scale;    // [2][T]
+    uint16_t *xs;        // [T][d] f16: x * 2^-u per token (the routed experts' B operand)
     int32_t *arrive;     // K-part arrival counters, zeroed here
     int n_arrive;
     int32_t *status;
     int32_t *abort;
 };
 
+// Block b converts tokens [32b, 32b + 32): warp per token, its scale 2^-u (max|x_t| in
+// [2^14, 2^15), u in [-113, 113]) and the f16 row x * 2^-u.  Block 0 also validates the
+// routing and builds the active list and the inverse permutation.
 __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
 {
     __shared__ int32_t bad;
     __shared__ int32_t scan_tmp[32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = a.E, slots = a.T * a.k;
+    {
+        const int t = blockIdx.x * 32 + warp;
+        if (t < a.T) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.d);
+            const int n16 = a.d / 8;
+            uint32_t m = 0;
+            for (int q0 = lane; q0 < n16; q0 += 32 * 8) {
+                uint4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) {          // eight independent loads in flight
+                    const int q = q0 + 32 * j;
+                    v[j] = q < n16 ? row[q] : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                    for (int h = 0; h < 4; h++) m = max(m, max(w4[h] & 0x7FFFu, (w4[h] >> 16) & 0x7FFFu));
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+            int u = 0;
+            const int eb = (int)(m >> 7);                      // biased exponent of max|x_t|
+            if (m != 0 && eb < 255) u = min(max(eb - 127 - 14, -113), 113);
+            const float xin = __uint_as_float((uint32_t)(127 - u) << 23);
+            if (lane == 0) {
+                a.tok_scale[t] = xin;
+                a.tok_scale[a.T + t] = __uint_as_float((uint32_t)(127 + u) << 23);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(a.xs + (size_t)t * a.d);
+            for (int q = lane; q < n16; q += 32) {
+                const uint4 v = row[q];
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int h = 0; h < 4; h++) {
+                    const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[h] << 16) * xin,
+                                                         __uint_as_float(w4[h] & 0xFFFF0000u) * xin);
+                    o[h] = *reinterpret_cast<const uint32_t *>(&h2);
+                }
+                dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+    if (blockIdx.x != 0) return;
     if (tid == 0) bad = 0;
     __syncthreads();
     // offsets: monotone, start 0, end T*k
@@ -210,35 +261,6 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
         a.inv[s] = -1;
     }
     for (int i = tid; i < a.n_arrive; i += blockDim.x) a.arrive[i] = 0;
-    // per-token activation scale: 2^-u puts max|x_t| in [2^14, 2^15); u in [-113, 113]
-    for (int t = warp; t < a.T; t += 32) {
-        const uint4 *row = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.d);
-        const int n16 = a.d / 8;
-        uint32_t m = 0;
-        for (int q0 = lane; q0 < n16; q0 += 32 * 8) {
-            uint4 v[8];
-#pragma unroll
-            for (int j = 0; j < 8; j++) {          // eight independent loads in flight
-                const int q = q0 + 32 * j;
-                v[j] = q < n16 ? row[q] : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-                for (int h = 0; h < 4; h++) m = max(m, max(w4[h] & 0x7FFFu, (w4[h] >> 16) & 0x7FFFu));
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) {
-            int u = 0;
-            const int eb = (int)(m >> 7);                      // biased exponent of max|x_t|
-            if (m != 0 && eb < 255) u = min(max(eb - 127 - 14, -113), 113);
-            a.tok_scale[t] = __uint_as_float((uint32_t)(127 - u) << 23);
-            a.tok_scale[a.T + t] = __uint_as_float((uint32_t)(127 + u) << 23);
-        }
-    }
     __syncthreads();
     const bool offsets_ok = !(bad & K3MOE_DEV_BAD_OFFSETS);
     // active experts in ascending order (block scan over flags)
@@ -289,7 +311,7 @@ struct GemvArgs {
     int T, d, f, k, S, E;
     int p_gu, p_dn;                 // K splits of the gate/up and down items
     float b1, b2;
-    const uint16_t *x;
+    const uint16_t *x, *xs;
     const int32_t *offsets, *perm, *active;
     const float *tok_scale;
     const uint8_t *table;
@@ -330,21 +352,23 @@ struct Geo {
     // stage bytes: a W1+W3 tile pair (gate/up) or one tile (down); bf16 boxes fit in both
     // (multiples of 1024 so every stage buffer meets the swizzled-TMA alignment)
     static constexpr int kStageBytes = MODE == kGateUp ? 2 * kTileBytes : 16 * 1024;
-    // B operand staged in chunks of at most this many 128-column tiles
-    static constexpr int kChunkTilesMax = MODE == kGateUp ? 8 : 4;
+    // B operand staged in chunks of at most this many 128-column tiles (two chunk
+    // buffers per block; down stages hi and lo halves)
+    static constexpr int kChunkTilesMax = MODE == kGateUp ? 4 : 2;
     // bf16 stages carry one matrix: gate/up alternates W1 and W3 slices
     static constexpr int kSharedMats = MODE == kGateUp ? 2 : 1;
     __host__ __device__ static int rows(const GemvArgs &a) { return MODE == kGateUp ? a.f : a.d; }
     __host__ __device__ static int K(const GemvArgs &a) { return MODE == kGateUp ? a.d : a.f; }
     __host__ __device__ static int P(const GemvArgs &a) { return MODE == kGateUp ? a.p_gu : a.p_dn; }
-    // tiles per staged chunk: the largest divisor of the K part's tile count within the cap
+    // 128-column tiles per staged B chunk (the last chunk of a K part may be shorter)
     __host__ __device__ static int chunk_tiles(const GemvArgs &a)
     {
         const int kt = K(a) / P(a) / kTileK;
-        for (int c = kChunkTilesMax; c > 1; c--)
-            if (kt % c == 0) return c;
-        return 1;
+        return kt < kChunkTilesMax ? kt : kChunkTilesMax;
     }
+    // bytes between two token rows of a staged B chunk: 16 bytes of padding keep the
+    // ldmatrix row reads of eight tokens on distinct banks
+    __host__ __device__ static int b_row_bytes(const GemvArgs &a) { return chunk_tiles(a) * kTileK * 2 + 16; }
 };
 
 // A work item: 128 rows of one unit over one K part, for passes [pass0, pass1).
@@ -450,75 +474,49 @@ struct PassTok {
     float fo[kPassTok];       // output factor (routed: 2^u_t; shared: 1)
 };
 
-__device__ __forceinline__ void fill_pass(const GemvArgs &a, const Unit &un, int pass, int nvalid,
-                                          PassTok &pt)
-{
-    const int n = threadIdx.x;
-    if (n < nvalid) {
-        const int t = token_of(a, un, pass, n);
-        pt.tok[n] = t;
-        pt.row[n] = (long long)out_row(a, un, pass, n);
-        pt.xin[n] = un.shared ? 1.0f : a.tok_scale[t];
-        pt.fo[n] = un.shared ? 1.0f : a.tok_scale[a.T + t];
-    }
-}
-
-// Stage the activations (gate/up) or the SiTU outputs (down) of the pass's valid tokens
-// over one K chunk of the item into the B layout (hi and, for down, lo halves).
-// Columns of invalid tokens are left as they are: a column of the B operand only
-// reaches the same column of the result, and those results are never stored.
+// B chunks in shared memory: token n's row of the chunk at n * b_row_bytes, 16-bit
+// elements in K order (routed gate/up: f16 x * 2^-u; shared gate/up: bf16 x; down: the
+// hi plane of h, and the lo plane in a second region).  The producer warp fills a chunk
+// with one bulk copy per token row (lane n copies token n); rows of invalid tokens are
+// left as they are: a column of the B operand only reaches the same column of the
+// result, and those results are never stored.
 template <int MODE>
-__device__ void stage_b(const GemvArgs &a, const Unit &un, const Item &it, int nvalid, int chunk,
-                        const PassTok &pt, uint8_t *bhi, uint8_t *blo)
+__device__ __forceinline__ void issue_b_chunk(const GemvArgs &a, const Unit &un, const Item &it, int chunk,
+                                              int nvalid, int tok, long long row, uint8_t *bhi, uint8_t *blo,
+                                              uint64_t *bar, int lane)
 {
-    const int K = Geo<MODE>::K(a), Kp = K / Geo<MODE>::P(a);
-    const int KC = Geo<MODE>::chunk_tiles(a) * kTileK, KS = KC / 16;
-    const int k0 = it.kp * Kp + chunk * KC;
-    if (MODE == kGateUp) {
-        const int per_tok = KC / 8;                       // one 16-byte load = 8 columns
-        for (int q = threadIdx.x; q < nvalid * per_tok; q += 256) {
-            const int n = q / per_tok, j = q % per_tok;
-            const int kl = 8 * j, ks = kl >> 4, half = (kl >> 3) & 1;
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)pt.tok[n] * K + k0 + kl));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            const float m = pt.xin[n];
-            uint8_t *dst = bhi + ((size_t)((n >> 3) * KS + ks) * 32 + 4 * (n & 7)) * 8 + 4 * half;
-#pragma unroll
-            for (int t = 0; t < 4; t++) {
-                uint32_t o = w[t];
-                if (!un.shared) {
-                    const __half2 h2 = __floats2half2_rn(__uint_as_float(w[t] << 16) * m,
-                                                         __uint_as_float(w[t] & 0xFFFF0000u) * m);
-                    o = *reinterpret_cast<const uint32_t *>(&h2);
-                }
-                *reinterpret_cast<uint32_t *>(dst + t * 8) = o;
-            }
-        }
-    } else {
-        // the SiTU output, already split into hi and lo 16-bit planes (f16 for routed
-        // experts, bf16 for shared ones): a copy into the B layout
-        const int per_tok = KC / 8;
-        const size_t plane = ((size_t)a.T * a.k + (size_t)a.S * a.T) * a.f;
-        for (int q = threadIdx.x; q < nvalid * per_tok; q += 256) {
-            const int n = q / per_tok, j = q % per_tok;
-            const int kl = 8 * j, ks = kl >> 4, half = (kl >> 3) & 1;
-            const size_t src = (size_t)pt.row[n] * a.f + k0 + kl;
-            const uint4 vh = *reinterpret_cast<const uint4 *>(a.hp + src);
-            const uint4 vl = *reinterpret_cast<const uint4 *>(a.hp + plane + src);
-            const uint32_t wh[4] = {vh.x, vh.y, vh.z, vh.w}, wl[4] = {vl.x, vl.y, vl.z, vl.w};
-            const size_t off = ((size_t)((n >> 3) * KS + ks) * 32 + 4 * (n & 7)) * 8 + 4 * half;
-#pragma unroll
-            for (int t = 0; t < 4; t++) {
-                *reinterpret_cast<uint32_t *>(bhi + off + t * 8) = wh[t];
-                *reinterpret_cast<uint32_t *>(blo + off + t * 8) = wl[t];
-            }
+    const int Kp = Geo<MODE>::K(a) / Geo<MODE>::P(a), CT = Geo<MODE>::chunk_tiles(a);
+    const int RS = Geo<MODE>::b_row_bytes(a);
+    const int c0 = chunk * CT * kTileK;                         // first column within the K part
+    const int cols = min(CT * kTileK, Kp - c0);
+    const uint32_t row_bytes = (uint32_t)cols * 2;
+    const int k0 = it.kp * Kp + c0;
+    if (lane == 0) mbar_expect_tx(bar, (uint32_t)nvalid * row_bytes * (MODE == kDown ? 2u : 1u));
+    __syncwarp();
+    if (lane < nvalid) {
+        if (MODE == kGateUp) {
+            const uint16_t *src = (un.shared ? a.x : a.xs) + (size_t)tok * a.d + k0;
+            bulk_g2s(bhi + lane * RS, src, row_bytes, bar);
+        } else {
+            const size_t plane = ((size_t)a.T * a.k + (size_t)a.S * a.T) * a.f;
+            const uint16_t *src = a.hp + (size_t)row * a.f + k0;
+            bulk_g2s(bhi + lane * RS, src, row_bytes, bar);
+            bulk_g2s(blo + lane * RS, src + plane, row_bytes, bar);
         }
     }
 }
 
 // One weight stage of warp `w` (rows 16w..16w+15 of the item).
+// B fragments of k-steps ks, ks+1 for n-block nb from a row-major chunk: ldmatrix x4,
+// lanes 8j..8j+7 address matrix j (tokens 8nb..8nb+7; columns 16ks + 8j .. +7).
+__device__ __forceinline__ void ldb2(uint32_t (&r)[4], const uint8_t *b, int RS, int nb, int ks, int lane)
+{
+    const int m = lane >> 3;
+    ldmatrix_x4(r, b + (8 * nb + (lane & 7)) * RS + (16 * ks + 8 * m) * 2);
+}
+
 template <int MODE, int NB>
-__device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, int st, int KS,
+__device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, int st, int RS,
                                               const uint8_t *bhi, const uint8_t *blo,
                                               float (&acc1)[kNBMax][4], float (&acc3)[kNBMax][4])
 {
@@ -547,16 +545,16 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, in
             }
 #pragma unroll
             for (int nb = 0; nb < NB; nb++) {
-                const uint2 b0 = *reinterpret_cast<const uint2 *>(bhi + ((nb * KS + ks0 + 2 * c) * 32 + lane) * 8);
-                const uint2 b1 = *reinterpret_cast<const uint2 *>(bhi + ((nb * KS + ks0 + 2 * c + 1) * 32 + lane) * 8);
+                uint32_t bb[4];
+                ldb2(bb, bhi, RS, nb, ks0 + 2 * c, lane);
                 float t1[4];
-                mma_f16(t1, A0, b0.x, b0.y, zero);
-                mma_f16(t1, A1, b1.x, b1.y, t1);
+                mma_f16(t1, A0, bb[0], bb[1], zero);
+                mma_f16(t1, A1, bb[2], bb[3], t1);
                 if (MODE == kDown) {
-                    const uint2 l0 = *reinterpret_cast<const uint2 *>(blo + ((nb * KS + ks0 + 2 * c) * 32 + lane) * 8);
-                    const uint2 l1 = *reinterpret_cast<const uint2 *>(blo + ((nb * KS + ks0 + 2 * c + 1) * 32 + lane) * 8);
-                    mma_f16(t1, A0, l0.x, l0.y, t1);
-                    mma_f16(t1, A1, l1.x, l1.y, t1);
+                    uint32_t ll[4];
+                    ldb2(ll, blo, RS, nb, ks0 + 2 * c, lane);
+                    mma_f16(t1, A0, ll[0], ll[1], t1);
+                    mma_f16(t1, A1, ll[2], ll[3], t1);
                 }
                 acc1[nb][0] = fmaf(f1[c], t1[0], acc1[nb][0]);
                 acc1[nb][1] = fmaf(f1[c], t1[1], acc1[nb][1]);
@@ -564,8 +562,8 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, in
                 acc1[nb][3] = fmaf(f1b[c], t1[3], acc1[nb][3]);
                 if (MODE == kGateUp) {
                     float t3[4];
-                    mma_f16(t3, C0, b0.x, b0.y, zero);
-                    mma_f16(t3, C1, b1.x, b1.y, t3);
+                    mma_f16(t3, C0, bb[0], bb[1], zero);
+                    mma_f16(t3, C1, bb[2], bb[3], t3);
                     acc3[nb][0] = fmaf(f3[c], t3[0], acc3[nb][0]);
                     acc3[nb][1] = fmaf(f3[c], t3[1], acc3[nb][1]);
                     acc3[nb][2] = fmaf(f3b[c], t3[2], acc3[nb][2]);
@@ -581,26 +579,67 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, in
         const bool up = MODE == kGateUp && (st & 1);
         const int r = 16 * w + (lane & 15);
 #pragma unroll
-        for (int kk = 0; kk < kSharedK / 16; kk++) {
-            const int q = 2 * kk + (lane >> 4);
-            uint32_t A[4];
-            ldmatrix_x4(A, buf + r * 128 + ((q ^ (r & 7)) << 4));
+        for (int kk = 0; kk < kSharedK / 16; kk += 2) {
+            uint32_t A[2][4];
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int q = 2 * (kk + h) + (lane >> 4);
+                ldmatrix_x4(A[h], buf + r * 128 + ((q ^ (r & 7)) << 4));
+            }
 #pragma unroll
             for (int nb = 0; nb < NB; nb++) {
-                const uint2 b = *reinterpret_cast<const uint2 *>(bhi + ((nb * KS + ks0 + kk) * 32 + lane) * 8);
+                uint32_t bb[4];
+                ldb2(bb, bhi, RS, nb, ks0 + kk, lane);
                 if (MODE == kDown) {
-                    const uint2 l = *reinterpret_cast<const uint2 *>(blo + ((nb * KS + ks0 + kk) * 32 + lane) * 8);
-                    mma_bf16(acc1[nb], A, b.x, b.y, acc1[nb]);
-                    mma_bf16(acc1[nb], A, l.x, l.y, acc1[nb]);
+                    uint32_t ll[4];
+                    ldb2(ll, blo, RS, nb, ks0 + kk, lane);
+                    mma_bf16(acc1[nb], A[0], bb[0], bb[1], acc1[nb]);
+                    mma_bf16(acc1[nb], A[0], ll[0], ll[1], acc1[nb]);
+                    mma_bf16(acc1[nb], A[1], bb[2], bb[3], acc1[nb]);
+                    mma_bf16(acc1[nb], A[1], ll[2], ll[3], acc1[nb]);
                 } else if (up) {
-                    mma_bf16(acc3[nb], A, b.x, b.y, acc3[nb]);
+                    mma_bf16(acc3[nb], A[0], bb[0], bb[1], acc3[nb]);
+                    mma_bf16(acc3[nb], A[1], bb[2], bb[3], acc3[nb]);
                 } else {
-                    mma_bf16(acc1[nb], A, b.x, b.y, acc1[nb]);
+                    mma_bf16(acc1[nb], A[0], bb[0], bb[1], acc1[nb]);
+                    mma_bf16(acc1[nb], A[1], bb[2], bb[3], acc1[nb]);
                 }
             }
         }
     }
 }
+
+// h as a hi + lo pair of 16-bit values (f16 for routed experts, bf16 for shared ones).
+__device__ __forceinline__ void store_h(const GemvArgs &a, int shared, size_t at, size_t plane, float hv)
+{
+    uint16_t hi, lo;
+    if (shared) {
+        const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+        const __nv_bfloat16 lb = __float2bfloat16_rn(hv - __bfloat162float(hb));
+        hi = *reinterpret_cast<const uint16_t *>(&hb);
+        lo = *reinterpret_cast<const uint16_t *>(&lb);
+    } else {
+        const __half hh = __float2half_rn(hv);
+        const __half lh = __float2half_rn(hv - __half2float(hh));
+        hi = *reinterpret_cast<const uint16_t *>(&hh);
+        lo = *reinterpret_cast<const uint16_t *>(&lh);
+    }
+    a.hp[at] = hi;
+    a.hp[plane + at] = lo;
+}
+
+// Bounded wait by every lane of a warp; the same result on every lane.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity)
+{
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Facts of the unit, item and pass a staged B chunk belongs to (written by the producer).
+struct BHdr {
+    int item, pass, nvalid;
+    int shared, id, rb, kp;
+};
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_constant__ GemvArgs a,
@@ -611,187 +650,169 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     constexpr int kStageBytes = Geo<MODE>::kStageBytes;
+    constexpr int kHalves = MODE == kDown ? 2 : 1;
     uint8_t *bufs = smem;                                          // kStages * kStageBytes
     const int P = Geo<MODE>::P(a);
-    const int ctiles = Geo<MODE>::chunk_tiles(a), KS = ctiles * kTileK / 16;
-    uint8_t *bhi = smem + kStages * kStageBytes;                   // kNBMax * KS * 256 bytes
-    uint8_t *blo = bhi + (size_t)kNBMax * KS * 256;                // down only
-    __shared__ uint64_t full[kStages], empty[kStages], csync;
-    __shared__ int hdr_item[kStages], hdr_pass[kStages], hdr_st[kStages];
-    __shared__ int issued[kStages];
-    __shared__ PassTok pt;
-    __shared__ int bail, last_part;
+    const int CT = Geo<MODE>::chunk_tiles(a), RS = Geo<MODE>::b_row_bytes(a);
+    const size_t bbytes = (size_t)kPassTok * RS;                   // one half of one B slot
+    uint8_t *bbase = smem + kStages * kStageBytes;                 // slot b, half h at (kHalves*b + h)
+    __shared__ uint64_t full[kStages], empty[kStages], bfull[kBSlots], bempty[kBSlots];
+    __shared__ int hdr_item[kStages], hdr_st[kStages], hdr_bu[kStages];
+    __shared__ int issued[kStages], bissued[kBSlots];
+    __shared__ PassTok pts[kBSlots];
+    __shared__ BHdr bh[kBSlots];
+    __shared__ int bail;
 
     if (*a.abort) return;
     const int n_active = min(max(a.active[a.E], 0), a.E);
     const int n_items = n_items_of<MODE>(a, n_active);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int nwarps = kThreads / 32;
     if (tid == 0) {
         for (int s = 0; s < kStages; s++) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kThreads / 32);
+            mbar_init(&empty[s], nwarps);
             issued[s] = 0;
         }
-        mbar_init(&csync, kThreads);
+        for (int b = 0; b < kBSlots; b++) {
+            mbar_init(&bfull[b], 1);
+            mbar_init(&bempty[b], nwarps);
+            bissued[b] = 0;
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         bail = 0;
     }
     __syncthreads();
+    auto timeout = [&]() {
+        set_status(a.status, K3MOE_DEV_TIMEOUT);
+        bail = 1;
+    };
 
-    if (w == kThreads / 32) {
-        // ---------------- producer
-        if (lane == 0) {
-            int n = 0;
-            for (;;) {
-                const int i = atomicAdd(&a.work[MODE], 1);
-                const bool done = i >= n_items || bail;
-                Item it{};
-                Unit un{};
-                int pass1 = 0, nst = 0;
-                if (!done) {
-                    it = item_of<MODE>(a, n_active, i);
-                    un = unit_of(a, n_active, it.u);
-                    pass1 = it.pass1 < 0 ? n_passes(un) : it.pass1;
-                    nst = n_stages<MODE>(a, un.shared);
+    if (w == nwarps) {
+        // ---------------- producer warp: work items, B chunks and weight stages, all by
+        // bulk copies; nothing here waits for data
+        int n = 0, bu = 0;
+        bool stop = false;
+        for (;;) {
+            int i = 0;
+            if (lane == 0) i = atomicAdd(&a.work[MODE], 1);
+            i = __shfl_sync(0xffffffffu, i, 0);
+            const bool done = i >= n_items || __shfl_sync(0xffffffffu, bail, 0) != 0;
+            if (done) {
+                // end of stream: one stage with no copy
+                const int slot = n % kStages;
+                if (n >= kStages && !mbar_wait_warp(&empty[slot], (uint32_t)((n / kStages) - 1) & 1u)) timeout();
+                else if (lane == 0) {
+                    hdr_item[slot] = -1;
+                    mbar_arrive(&full[slot]);
                 }
-                for (int pass = it.pass0; done ? pass == it.pass0 : pass < pass1; pass++)
-                    for (int st = 0; done ? st == 0 : st < nst; st++, n++) {
-                        const int slot = n % kStages;
-                        if (n >= kStages && !mbar_wait(&empty[slot], (uint32_t)((n / kStages) - 1) & 1u)) {
-                            set_status(a.status, K3MOE_DEV_TIMEOUT);
-                            bail = 1;
-                        }
-                        if (bail) break;
-                        hdr_item[slot] = done ? -1 : i;
-                        hdr_pass[slot] = pass;
-                        hdr_st[slot] = st;
-                        if (done) {
-                            mbar_arrive(&full[slot]);          // end of stream, no copy
-                        } else {
-                            fence_proxy_async();
-                            issue_stage<MODE>(a, &m1, &m3, &m2, un, it, st, bufs + slot * kStageBytes, &full[slot]);
-                            issued[slot]++;
-                        }
-                    }
-                if (done || bail) break;
+                break;
             }
+            const Item it = item_of<MODE>(a, n_active, i);
+            const Unit un = unit_of(a, n_active, it.u);
+            const int pass1 = it.pass1 < 0 ? n_passes(un) : it.pass1;
+            const int nst = n_stages<MODE>(a, un.shared);
+            const int spt = un.shared ? Geo<MODE>::kSharedMats * (kTileK / kSharedK) : 1;   // stages per tile
+            for (int pass = it.pass0; pass < pass1 && !stop; pass++) {
+                const int nvalid = min(kPassTok, un.ntok - pass * kPassTok);
+                // token facts of this pass: lane n holds token n's
+                int tok = 0;
+                long long row = 0;
+                float fo = 1.0f;
+                if (lane < nvalid) {
+                    tok = token_of(a, un, pass, lane);
+                    row = (long long)out_row(a, un, pass, lane);
+                    fo = un.shared ? 1.0f : a.tok_scale[a.T + tok];
+                }
+                for (int st = 0; st < nst; st++, n++) {
+                    if (st % (spt * CT) == 0) {
+                        // the B chunk of this (item, pass) for the next CT tiles of K
+                        const int b = bu % kBSlots;
+                        if (bu >= kBSlots && !mbar_wait_warp(&bempty[b], (uint32_t)((bu / kBSlots) - 1) & 1u)) {
+                            timeout();
+                            stop = true;
+                            break;
+                        }
+                        if (lane < nvalid) {
+                            pts[b].tok[lane] = tok;
+                            pts[b].row[lane] = row;
+                            pts[b].fo[lane] = fo;
+                        }
+                        if (lane == 0) bh[b] = BHdr{i, pass, nvalid, un.shared, un.id, it.rb, it.kp};
+                        __syncwarp();
+                        issue_b_chunk<MODE>(a, un, it, st / (spt * CT), nvalid, tok, row, bbase + kHalves * b * bbytes,
+                                            bbase + (kHalves * b + kHalves - 1) * bbytes, &bfull[b], lane);
+                        if (lane == 0) bissued[b]++;
+                        bu++;
+                    }
+                    const int slot = n % kStages;
+                    if (n >= kStages && !mbar_wait_warp(&empty[slot], (uint32_t)((n / kStages) - 1) & 1u)) {
+                        timeout();
+                        stop = true;
+                        break;
+                    }
+                    if (lane == 0) {
+                        hdr_item[slot] = i;
+                        hdr_st[slot] = st;
+                        hdr_bu[slot] = bu - 1;
+                        fence_proxy_async();
+                        issue_stage<MODE>(a, &m1, &m3, &m2, un, it, st, bufs + slot * kStageBytes, &full[slot]);
+                        issued[slot]++;
+                    }
+                    __syncwarp();
+                }
+            }
+            if (stop) break;
         }
     } else {
-        // ---------------- consumers
+        // ---------------- consumers: warp w owns rows 16w..16w+15 of every item
         const int g = lane >> 2, t4 = lane & 3;
-        uint32_t sync_phase = 0;
-        auto csync_all = [&]() -> bool {       // all 256 consumer threads, bounded
-            mbar_arrive(&csync);
-            const bool ok = mbar_wait(&csync, sync_phase & 1u);
-            sync_phase++;
-            return ok;
-        };
         float acc1[kNBMax][4], acc3[kNBMax][4];
-        int staged_u = -1, staged_kp = -1, staged_pass = -1, staged_chunk = -1;
-        int cur_item = -1, cur_pass = -1;
-        Item it{};
-        Unit un{};
-        int nst = 0, spc = 1, nvalid = 0;
+        int cur_bu = -1, b = 0;
+        int nst = 0, spc = 1;
+        const int nrb = Geo<MODE>::rows(a) / kItemRows;
         for (int n = 0;; n++) {
             const int slot = n % kStages;
-            if (!mbar_wait(&full[slot], (uint32_t)(n / kStages) & 1u)) {
-                set_status(a.status, K3MOE_DEV_TIMEOUT);
-                bail = 1;
+            if (!mbar_wait_warp(&full[slot], (uint32_t)(n / kStages) & 1u)) {
+                timeout();
                 break;
             }
             const int item = hdr_item[slot];
             if (item < 0) break;
-            const int pass = hdr_pass[slot], st = hdr_st[slot];
-            if (item != cur_item || pass != cur_pass) {        // decode once per (item, pass)
-                if (item != cur_item) {
-                    it = item_of<MODE>(a, n_active, item);
-                    un = unit_of(a, n_active, it.u);
-                    nst = n_stages<MODE>(a, un.shared);
-                    spc = un.shared ? Geo<MODE>::kSharedMats * (ctiles * kTileK / kSharedK) : ctiles;
-                    cur_item = item;
+            const int st = hdr_st[slot], bun = hdr_bu[slot];
+            if (bun != cur_bu) {                                // a new B chunk
+                b = bun % kBSlots;
+                if (!mbar_wait_warp(&bfull[b], (uint32_t)(bun / kBSlots) & 1u)) {
+                    timeout();
+                    break;
                 }
-                nvalid = min(kPassTok, un.ntok - pass * kPassTok);
-                cur_pass = pass;
+                cur_bu = bun;
+                nst = n_stages<MODE>(a, bh[b].shared);
+                spc = (bh[b].shared ? Geo<MODE>::kSharedMats * (kTileK / kSharedK) : 1) * CT;
             }
+            const BHdr &h = bh[b];
+            const PassTok &pt = pts[b];
+            const uint8_t *bhi = bbase + kHalves * b * bbytes, *blo = bbase + (kHalves * b + kHalves - 1) * bbytes;
             if (st == 0) {
 #pragma unroll
                 for (int nb = 0; nb < kNBMax; nb++)
 #pragma unroll
                     for (int i = 0; i < 4; i++) acc1[nb][i] = acc3[nb][i] = 0.0f;
             }
-            const int chunk = st / spc;
-            if (st % spc == 0 && (it.u != staged_u || it.kp != staged_kp || pass != staged_pass ||
-                                  chunk != staged_chunk)) {
-                bool ok = csync_all();               // all consumers done with bhi/blo and pt
-                fill_pass(a, un, pass, nvalid, pt);
-                ok = ok && csync_all();
-                stage_b<MODE>(a, un, it, nvalid, chunk, pt, bhi, blo);
-                ok = ok && csync_all();
-                if (!ok) {
-                    set_status(a.status, K3MOE_DEV_TIMEOUT);
-                    bail = 1;
-                    break;
-                }
-                staged_u = it.u;
-                staged_kp = it.kp;
-                staged_pass = pass;
-                staged_chunk = chunk;
-            }
             const uint8_t *buf = bufs + slot * kStageBytes;
-            if (nvalid > 8)
-                consume_stage<MODE, 2>(buf, un.shared, st % spc, KS, bhi, blo, acc1, acc3);
+            if (h.nvalid > 8)
+                consume_stage<MODE, 2>(buf, h.shared, st % spc, RS, bhi, blo, acc1, acc3);
             else
-                consume_stage<MODE, 1>(buf, un.shared, st % spc, KS, bhi, blo, acc1, acc3);
+                consume_stage<MODE, 1>(buf, h.shared, st % spc, RS, bhi, blo, acc1, acc3);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
-            if (st != nst - 1) continue;
-            // epilogue: this thread holds rows 16w+g (+8) x tokens 8nb+2t4 (+1)
-            const int row0 = it.rb * kItemRows + 16 * w + g;
-            const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
-            if (MODE == kDown) {
-#pragma unroll
-                for (int nb = 0; nb < kNBMax; nb++)
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const int nn = nb * 8 + 2 * t4 + (i & 1);
-                        if (nn >= nvalid) continue;
-                        const int row = row0 + ((i >> 1) << 3);
-                        a.ys[((size_t)it.kp * rows_all + (size_t)pt.row[nn]) * a.d + row] = acc1[nb][i];
-                    }
-                continue;
-            }
-            bool finish = (P == 1);
-            if (!finish) {
-                // K split: publish this part's partial sums; the last part to arrive for
-                // this (unit, row block) adds all parts in order and applies SiTU
-#pragma unroll
-                for (int nb = 0; nb < kNBMax; nb++)
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const int nn = nb * 8 + 2 * t4 + (i & 1);
-                        if (nn >= nvalid) continue;
-                        const int row = row0 + ((i >> 1) << 3);
-                        float *base = a.gu + ((size_t)it.kp * rows_all + (size_t)pt.row[nn]) * 2 * a.f;
-                        base[row] = acc1[nb][i];
-                        base[a.f + row] = acc3[nb][i];
-                    }
-                __threadfence();
-                bool ok = csync_all();
-                if (tid == 0) {
-                    int32_t *ctr = a.arrive + (size_t)it.u * (a.f / kItemRows) + it.rb;
-                    const int old = atomicAdd(ctr, 1);
-                    last_part = (old == P - 1);
-                    if (last_part) *ctr = 0;
-                }
-                ok = ok && csync_all();
-                if (!ok) {
-                    set_status(a.status, K3MOE_DEV_TIMEOUT);
-                    bail = 1;
-                    break;
-                }
-                finish = last_part != 0;
-                if (finish) {
-                    __threadfence();
+            const bool chunk_end = (st % spc == spc - 1) || st == nst - 1;
+            if (st == nst - 1) {
+                // epilogue: this thread holds rows 16w+g (+8) x tokens 8nb+2t4 (+1)
+                const int row0 = h.rb * kItemRows + 16 * w + g;
+                const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
+                const int nvalid = h.nvalid;
+                if (MODE == kDown) {
 #pragma unroll
                     for (int nb = 0; nb < kNBMax; nb++)
 #pragma unroll
@@ -799,44 +820,69 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                             const int nn = nb * 8 + 2 * t4 + (i & 1);
                             if (nn >= nvalid) continue;
                             const int row = row0 + ((i >> 1) << 3);
-                            float gs = 0.0f, us = 0.0f;
-                            for (int p = 0; p < P; p++) {
-                                const float *base = a.gu + ((size_t)p * rows_all + (size_t)pt.row[nn]) * 2 * a.f;
-                                gs += __ldcg(base + row);
-                                us += __ldcg(base + a.f + row);
-                            }
-                            acc1[nb][i] = gs;
-                            acc3[nb][i] = us;
+                            a.ys[((size_t)h.kp * rows_all + (size_t)pt.row[nn]) * a.d + row] = acc1[nb][i];
                         }
+                } else if (P == 1) {
+                    const size_t plane = rows_all * a.f;
+#pragma unroll
+                    for (int nb = 0; nb < kNBMax; nb++)
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const int nn = nb * 8 + 2 * t4 + (i & 1);
+                            if (nn >= nvalid) continue;
+                            const int row = row0 + ((i >> 1) << 3);
+                            const float fo = pt.fo[nn];
+                            store_h(a, h.shared, (size_t)pt.row[nn] * a.f + row, plane,
+                                    situ(acc1[nb][i] * fo, acc3[nb][i] * fo, a.b1, a.b2));
+                        }
+                } else {
+                    // K split: publish this warp's partial sums; the last of the P x 8 warps
+                    // holding rows of this (unit, row block) adds all parts in order and
+                    // applies SiTU to all 128 rows
+#pragma unroll
+                    for (int nb = 0; nb < kNBMax; nb++)
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const int nn = nb * 8 + 2 * t4 + (i & 1);
+                            if (nn >= nvalid) continue;
+                            const int row = row0 + ((i >> 1) << 3);
+                            float *base = a.gu + ((size_t)h.kp * rows_all + (size_t)pt.row[nn]) * 2 * a.f;
+                            base[row] = acc1[nb][i];
+                            base[a.f + row] = acc3[nb][i];
+                        }
+                    __threadfence();
+                    __syncwarp();
+                    int last = 0;
+                    if (lane == 0) {
+                        // counter of (unit, row block): routed expert e at e, shared s at E + s
+                        int32_t *ctr = a.arrive + (size_t)(h.shared ? a.E + h.id : h.id) * nrb + h.rb;
+                        const int old = atomicAdd(ctr, 1);
+                        last = (old == P * nwarps - 1);
+                        if (last) *ctr = 0;
+                    }
+                    if (__shfl_sync(0xffffffffu, last, 0)) {
+                        __threadfence();
+                        const size_t plane = rows_all * a.f;
+                        for (int nn = 0; nn < nvalid; nn++) {
+                            const size_t prow = (size_t)pt.row[nn];
+                            const float fo = pt.fo[nn];
+                            for (int r = lane; r < kItemRows; r += 32) {
+                                const int row = h.rb * kItemRows + r;
+                                float gs = 0.0f, us = 0.0f;
+                                for (int p = 0; p < P; p++) {
+                                    const float *base = a.gu + ((size_t)p * rows_all + prow) * 2 * a.f;
+                                    gs += __ldcg(base + row);
+                                    us += __ldcg(base + a.f + row);
+                                }
+                                store_h(a, h.shared, prow * a.f + row, plane, situ(gs * fo, us * fo, a.b1, a.b2));
+                            }
+                        }
+                    }
                 }
             }
-            if (finish) {
-                const size_t plane = rows_all * a.f;
-#pragma unroll
-                for (int nb = 0; nb < kNBMax; nb++)
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const int nn = nb * 8 + 2 * t4 + (i & 1);
-                        if (nn >= nvalid) continue;
-                        const int row = row0 + ((i >> 1) << 3);
-                        const float fo = pt.fo[nn];
-                        const float h = situ(acc1[nb][i] * fo, acc3[nb][i] * fo, a.b1, a.b2);
-                        uint16_t hi, lo;
-                        if (un.shared) {
-                            const __nv_bfloat16 hb = __float2bfloat16_rn(h);
-                            const __nv_bfloat16 lb = __float2bfloat16_rn(h - __bfloat162float(hb));
-                            hi = *reinterpret_cast<const uint16_t *>(&hb);
-                            lo = *reinterpret_cast<const uint16_t *>(&lb);
-                        } else {
-                            const __half hh = __float2half_rn(h);
-                            const __half lh = __float2half_rn(h - __half2float(hh));
-                            hi = *reinterpret_cast<const uint16_t *>(&hh);
-                            lo = *reinterpret_cast<const uint16_t *>(&lh);
-                        }
-                        const size_t at = (size_t)pt.row[nn] * a.f + row;
-                        a.hp[at] = hi;
-                        a.hp[plane + at] = lo;
-                    }
+            if (chunk_end) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bempty[b]);
             }
         }
     }
@@ -846,6 +892,8 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
         // memory is released (each wait bounded)
         for (int s = 0; s < kStages; s++)
             if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)(issued[s] - 1) & 1u);
+        for (int s = 0; s < kBSlots; s++)
+            if (bissued[s] > 0) mbar_wait(&bfull[s], (uint32_t)(bissued[s] - 1) & 1u);
     }
 }
 
@@ -1045,10 +1093,11 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     int32_t *arrive = reinterpret_cast<int32_t *>(ws + L.arrive);
     float *ys = reinterpret_cast<float *>(ws + L.ys);
 
-    PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, arrive,
+    uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
+    PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, xs, arrive,
                 (c.n_experts + c.n_shared) * (c.f / kTileRows), status, abort};
     timing_begin("fwd_prep", s);
-    fwd_prep_kernel<<<1, 1024, 0, s>>>(pa);
+    fwd_prep_kernel<<<(T + 31) / 32, 1024, 0, s>>>(pa);
     count_launch();
     timing_end("fwd_prep", s);
 
@@ -1060,11 +1109,11 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
             return cudaErrorInvalidValue;
     }
     GemvArgs ga{T, c.d, c.f, c.top_k, c.n_shared, c.n_experts, L.p_gu, L.p_dn, c.situ_b1, c.situ_b2,
-                x, offsets, perm, active, tok_scale, table, expert_bytes(c.d, c.f),
+                x, xs, offsets, perm, active, tok_scale, table, expert_bytes(c.d, c.f),
                 gateup_block_bytes(c.d, c.f), gu, ys, hp, arrive, abort, status, abort + 1};
     {
         const size_t smem = 1024 + kStages * Geo<kGateUp>::kStageBytes +
-                            (size_t)kNBMax * (Geo<kGateUp>::chunk_tiles(ga) * kTileK / 16) * 256;
+                            (size_t)kBSlots * kPassTok * Geo<kGateUp>::b_row_bytes(ga);
         const int blocks = grid_blocks(gemv_kernel<kGateUp>, smem);
         timing_begin("gemv_gateup", s);
         gemv_kernel<kGateUp><<<blocks, kThreads + 32, smem, s>>>(ga, m1, m3, m2);
@@ -1073,7 +1122,7 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     }
     {
         const size_t smem = 1024 + kStages * Geo<kDown>::kStageBytes +
-                            2 * (size_t)kNBMax * (Geo<kDown>::chunk_tiles(ga) * kTileK / 16) * 256;
+                            2 * (size_t)kBSlots * kPassTok * Geo<kDown>::b_row_bytes(ga);
         const int blocks = grid_blocks(gemv_kernel<kDown>, smem);
         timing_begin("gemv_down", s);
         gemv_kernel<kDown><<<blocks, kThreads + 32, smem, s>>>(ga, m1, m3, m2);

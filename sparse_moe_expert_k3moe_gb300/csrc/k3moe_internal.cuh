@@ -109,6 +109,7 @@ struct WsLayout {
     size_t gu;                   // decode: g|u partials [P_gu][rows][2][f] f32 (only when P_gu > 1)
     size_t hp;                   // decode: SiTU output as hi and lo planes [2][rows][f] 16-bit
     size_t arrive;               // decode: per (unit, row block) K-part arrival counters
+    size_t xs;                   // decode: activations x * 2^-u per token [T][d] f16
     size_t ys;                   // decode: y partials [P_dn][rows][d] f32
     size_t xg;                   // prefill: routed activations in perm order [T*k][d] f16
     size_t units;                // prefill: unit list [E+S][4], item prefixes, unit count
@@ -143,6 +144,7 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     L.gu = o; o = align256(o + (!L.gemm && L.p_gu > 1 ? rows * (size_t)c.f * 4 * 2 * L.p_gu : 0));
     L.hp = o; o = align256(o + rows * (size_t)c.f * 2 * (L.gemm ? 1 : 2));
     L.arrive = o; o = align256(o + (L.gemm ? 0 : (E + S) * (size_t)(c.f / kTileRows) * 4));
+    L.xs = o; o = align256(o + (L.gemm ? 0 : (size_t)T * c.d * 2));
     L.ys = o; o = align256(o + (L.gemm ? 0 : rows * (size_t)c.d * 4 * L.p_dn));
     L.xg = o; o = align256(o + (L.gemm ? slots * (size_t)c.d * 2 : 0));
     L.units = o; o = align256(o + (L.gemm ? (4 * (E + S) + 2 * (E + S + 1) + 1) * 4 : 0));
