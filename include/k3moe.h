@@ -194,7 +194,7 @@ k3moe_status k3moe_forward(const k3moe_config *cfg, int32_t T, const uint16_t *x
  * Scratch comes from a 32 MiB array inside the library (a file-scope
  * __device__ object): every GPU that loads the library holds it until the
  * process exits.  Calls whose k3moe_workspace_bytes(cfg, T) exceeds 32 MiB
- * return K3MOE_EWORKSPACE without launching (at the K3 shape, T <= 64 fits).
+ * return K3MOE_EWORKSPACE without launching (at the K3 shape, T <= 67 fits).
  * The first call on each device looks up the array's device address with
  * that device current; make it before any stream capture.  All calls share
  * the array and it keeps the last call's contents (each call clears its

@@ -35,6 +35,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "k3moe_internal.cuh"
@@ -44,7 +45,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kItemRows = 128;
-constexpr int kStages = 4;
+constexpr int kStages = 4;                         // weight-stage ring depth
 constexpr int kNBMax = 2;                          // n-blocks of 8 tokens per pass
 constexpr int kPassTok = 8 * kNBMax;
 constexpr int kSharedK = 64;                       // K per stage for bf16 tiles (one matrix)
@@ -310,6 +311,7 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
 struct GemvArgs {
     int T, d, f, k, S, E;
     int p_gu, p_dn;                 // K splits of the gate/up and down items
+    int brows;                      // token rows of a staged B chunk: min(16, T)
     float b1, b2;
     const uint16_t *x, *xs;
     const int32_t *offsets, *perm, *active;
@@ -508,15 +510,19 @@ __device__ __forceinline__ void issue_b_chunk(const GemvArgs &a, const Unit &un,
 
 // One weight stage of warp `w` (rows 16w..16w+15 of the item).
 // B fragments of k-steps ks, ks+1 for n-block nb from a row-major chunk: ldmatrix x4,
-// lanes 8j..8j+7 address matrix j (tokens 8nb..8nb+7; columns 16ks + 8j .. +7).
-__device__ __forceinline__ void ldb2(uint32_t (&r)[4], const uint8_t *b, int RS, int nb, int ks, int lane)
+// lanes 8j..8j+7 address matrix j (tokens 8nb..8nb+7; columns 16ks + 8j .. +7).  A chunk
+// holds `brows` token rows; the n-block's rows past them read the last row instead
+// (their results are never stored), so every address stays inside the chunk.
+__device__ __forceinline__ void ldb2(uint32_t (&r)[4], const uint8_t *b, int RS, int brows, int nb, int ks,
+                                     int lane)
 {
     const int m = lane >> 3;
-    ldmatrix_x4(r, b + (8 * nb + (lane & 7)) * RS + (16 * ks + 8 * m) * 2);
+    const int row = min(8 * nb + (lane & 7), brows - 1);
+    ldmatrix_x4(r, b + row * RS + (16 * ks + 8 * m) * 2);
 }
 
 template <int MODE, int NB>
-__device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, int st, int RS,
+__device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, int st, int RS, int brows,
                                               const uint8_t *bhi, const uint8_t *blo,
                                               float (&acc1)[kNBMax][4], float (&acc3)[kNBMax][4])
 {
@@ -546,13 +552,13 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, in
 #pragma unroll
             for (int nb = 0; nb < NB; nb++) {
                 uint32_t bb[4];
-                ldb2(bb, bhi, RS, nb, ks0 + 2 * c, lane);
+                ldb2(bb, bhi, RS, brows, nb, ks0 + 2 * c, lane);
                 float t1[4];
                 mma_f16(t1, A0, bb[0], bb[1], zero);
                 mma_f16(t1, A1, bb[2], bb[3], t1);
                 if (MODE == kDown) {
                     uint32_t ll[4];
-                    ldb2(ll, blo, RS, nb, ks0 + 2 * c, lane);
+                    ldb2(ll, blo, RS, brows, nb, ks0 + 2 * c, lane);
                     mma_f16(t1, A0, ll[0], ll[1], t1);
                     mma_f16(t1, A1, ll[2], ll[3], t1);
                 }
@@ -589,10 +595,10 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, in
 #pragma unroll
             for (int nb = 0; nb < NB; nb++) {
                 uint32_t bb[4];
-                ldb2(bb, bhi, RS, nb, ks0 + kk, lane);
+                ldb2(bb, bhi, RS, brows, nb, ks0 + kk, lane);
                 if (MODE == kDown) {
                     uint32_t ll[4];
-                    ldb2(ll, blo, RS, nb, ks0 + kk, lane);
+                    ldb2(ll, blo, RS, brows, nb, ks0 + kk, lane);
                     mma_bf16(acc1[nb], A[0], bb[0], bb[1], acc1[nb]);
                     mma_bf16(acc1[nb], A[0], ll[0], ll[1], acc1[nb]);
                     mma_bf16(acc1[nb], A[1], bb[2], bb[3], acc1[nb]);
@@ -654,7 +660,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
     uint8_t *bufs = smem;                                          // kStages * kStageBytes
     const int P = Geo<MODE>::P(a);
     const int CT = Geo<MODE>::chunk_tiles(a), RS = Geo<MODE>::b_row_bytes(a);
-    const size_t bbytes = (size_t)kPassTok * RS;                   // one half of one B slot
+    const size_t bbytes = (size_t)a.brows * RS;                    // one half of one B slot
     uint8_t *bbase = smem + kStages * kStageBytes;                 // slot b, half h at (kHalves*b + h)
     __shared__ uint64_t full[kStages], empty[kStages], bfull[kBSlots], bempty[kBSlots];
     __shared__ int hdr_item[kStages], hdr_st[kStages], hdr_bu[kStages];
@@ -801,9 +807,9 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
             }
             const uint8_t *buf = bufs + slot * kStageBytes;
             if (h.nvalid > 8)
-                consume_stage<MODE, 2>(buf, h.shared, st % spc, RS, bhi, blo, acc1, acc3);
+                consume_stage<MODE, 2>(buf, h.shared, st % spc, RS, a.brows, bhi, blo, acc1, acc3);
             else
-                consume_stage<MODE, 1>(buf, h.shared, st % spc, RS, bhi, blo, acc1, acc3);
+                consume_stage<MODE, 1>(buf, h.shared, st % spc, RS, a.brows, bhi, blo, acc1, acc3);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
             const bool chunk_end = (st % spc == spc - 1) || st == nst - 1;
@@ -1108,12 +1114,14 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
             !cached_bf16_map(&m2, sh_w2, (uint64_t)c.n_shared * c.d, c.f))
             return cudaErrorInvalidValue;
     }
-    GemvArgs ga{T, c.d, c.f, c.top_k, c.n_shared, c.n_experts, L.p_gu, L.p_dn, c.situ_b1, c.situ_b2,
+    GemvArgs ga{T, c.d, c.f, c.top_k, c.n_shared, c.n_experts, L.p_gu, L.p_dn, 0, c.situ_b1, c.situ_b2,
                 x, xs, offsets, perm, active, tok_scale, table, expert_bytes(c.d, c.f),
                 gateup_block_bytes(c.d, c.f), gu, ys, hp, arrive, abort, status, abort + 1};
+    // B chunks hold min(16, T) token rows
+    ga.brows = T < kPassTok ? T : kPassTok;
     {
-        const size_t smem = 1024 + kStages * Geo<kGateUp>::kStageBytes +
-                            (size_t)kBSlots * kPassTok * Geo<kGateUp>::b_row_bytes(ga);
+        const size_t bsl = (size_t)kBSlots * ga.brows * Geo<kGateUp>::b_row_bytes(ga);
+        const size_t smem = 1024 + (size_t)kStages * Geo<kGateUp>::kStageBytes + bsl;
         const int blocks = grid_blocks(gemv_kernel<kGateUp>, smem);
         timing_begin("gemv_gateup", s);
         gemv_kernel<kGateUp><<<blocks, kThreads + 32, smem, s>>>(ga, m1, m3, m2);
@@ -1121,8 +1129,8 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
         timing_end("gemv_gateup", s);
     }
     {
-        const size_t smem = 1024 + kStages * Geo<kDown>::kStageBytes +
-                            2 * (size_t)kBSlots * kPassTok * Geo<kDown>::b_row_bytes(ga);
+        const size_t bsl = 2 * (size_t)kBSlots * ga.brows * Geo<kDown>::b_row_bytes(ga);
+        const size_t smem = 1024 + (size_t)kStages * Geo<kDown>::kStageBytes + bsl;
         const int blocks = grid_blocks(gemv_kernel<kDown>, smem);
         timing_begin("gemv_down", s);
         gemv_kernel<kDown><<<blocks, kThreads + 32, smem, s>>>(ga, m1, m3, m2);
