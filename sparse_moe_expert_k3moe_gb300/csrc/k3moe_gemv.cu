@@ -73,6 +73,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
     const uint32_t a = smem_addr(bar);
+    {   // fast path: the phase is often complete already
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
     const long long t0 = clock64();
     for (uint32_t i = 0;; i++) {
         uint32_t done;
@@ -663,7 +673,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
     const size_t bbytes = (size_t)a.brows * RS;                    // one half of one B slot
     uint8_t *bbase = smem + kStages * kStageBytes;                 // slot b, half h at (kHalves*b + h)
     __shared__ uint64_t full[kStages], empty[kStages], bfull[kBSlots], bempty[kBSlots];
-    __shared__ int hdr_item[kStages], hdr_st[kStages], hdr_bu[kStages];
+    __shared__ int hdr_item[kStages], hdr_st[kStages], hdr_bu[kStages], hdr_sic[kStages];
     __shared__ int issued[kStages], bissued[kBSlots];
     __shared__ PassTok pts[kBSlots];
     __shared__ BHdr bh[kBSlots];
@@ -730,8 +740,9 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                     row = (long long)out_row(a, un, pass, lane);
                     fo = un.shared ? 1.0f : a.tok_scale[a.T + tok];
                 }
-                for (int st = 0; st < nst; st++, n++) {
-                    if (st % (spt * CT) == 0) {
+                const int spc = spt * CT;                        // stages per B chunk
+                for (int st = 0, sic = 0; st < nst; st++, n++, sic = (sic + 1 == spc) ? 0 : sic + 1) {
+                    if (sic == 0) {
                         // the B chunk of this (item, pass) for the next CT tiles of K
                         const int b = bu % kBSlots;
                         if (bu >= kBSlots && !mbar_wait_warp(&bempty[b], (uint32_t)((bu / kBSlots) - 1) & 1u)) {
@@ -746,7 +757,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                         }
                         if (lane == 0) bh[b] = BHdr{i, pass, nvalid, un.shared, un.id, it.rb, it.kp};
                         __syncwarp();
-                        issue_b_chunk<MODE>(a, un, it, st / (spt * CT), nvalid, tok, row, bbase + kHalves * b * bbytes,
+                        issue_b_chunk<MODE>(a, un, it, st / spc, nvalid, tok, row, bbase + kHalves * b * bbytes,
                                             bbase + (kHalves * b + kHalves - 1) * bbytes, &bfull[b], lane);
                         if (lane == 0) bissued[b]++;
                         bu++;
@@ -761,6 +772,9 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                         hdr_item[slot] = i;
                         hdr_st[slot] = st;
                         hdr_bu[slot] = bu - 1;
+                        // stage within its B chunk; bit 16: the chunk's last stage; bit 17: the pass's last
+                        hdr_sic[slot] = sic | ((sic + 1 == spc || st == nst - 1) ? 1 << 16 : 0) |
+                                        (st == nst - 1 ? 1 << 17 : 0);
                         fence_proxy_async();
                         issue_stage<MODE>(a, &m1, &m3, &m2, un, it, st, bufs + slot * kStageBytes, &full[slot]);
                         issued[slot]++;
@@ -775,7 +789,6 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
         const int g = lane >> 2, t4 = lane & 3;
         float acc1[kNBMax][4], acc3[kNBMax][4];
         int cur_bu = -1, b = 0;
-        int nst = 0, spc = 1;
         const int nrb = Geo<MODE>::rows(a) / kItemRows;
         for (int n = 0;; n++) {
             const int slot = n % kStages;
@@ -785,7 +798,8 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
             }
             const int item = hdr_item[slot];
             if (item < 0) break;
-            const int st = hdr_st[slot], bun = hdr_bu[slot];
+            const int st = hdr_st[slot], bun = hdr_bu[slot], sicf = hdr_sic[slot];
+            const int sic = sicf & 0xFFFF;
             if (bun != cur_bu) {                                // a new B chunk
                 b = bun % kBSlots;
                 if (!mbar_wait_warp(&bfull[b], (uint32_t)(bun / kBSlots) & 1u)) {
@@ -793,8 +807,6 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                     break;
                 }
                 cur_bu = bun;
-                nst = n_stages<MODE>(a, bh[b].shared);
-                spc = (bh[b].shared ? Geo<MODE>::kSharedMats * (kTileK / kSharedK) : 1) * CT;
             }
             const BHdr &h = bh[b];
             const PassTok &pt = pts[b];
@@ -807,13 +819,13 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
             }
             const uint8_t *buf = bufs + slot * kStageBytes;
             if (h.nvalid > 8)
-                consume_stage<MODE, 2>(buf, h.shared, st % spc, RS, a.brows, bhi, blo, acc1, acc3);
+                consume_stage<MODE, 2>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
             else
-                consume_stage<MODE, 1>(buf, h.shared, st % spc, RS, a.brows, bhi, blo, acc1, acc3);
+                consume_stage<MODE, 1>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
-            const bool chunk_end = (st % spc == spc - 1) || st == nst - 1;
-            if (st == nst - 1) {
+            const bool chunk_end = (sicf >> 16) & 1;
+            if ((sicf >> 17) & 1) {
                 // epilogue: this thread holds rows 16w+g (+8) x tokens 8nb+2t4 (+1)
                 const int row0 = h.rb * kItemRows + 16 * w + g;
                 const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
