@@ -9,12 +9,14 @@
 //   gemm_units   validates offsets, lists the units (shared experts first, heaviest,
 //                then the active routed experts) and the prefix of their work items;
 //   gemm_scales  per-token activation scale 2^-u (max |x_t| in [2^14, 2^15));
-//   gemm_gather  routed-expert activations in perm order, f16, times 2^-u_t; validates
-//                perm against idx;
+//   gemm_gather  zeroes out; routed-expert activations in perm order, f16, times
+//                2^-u_t; validates perm against idx;
 //   gemm<GU>     g = W1 x, u = W3 x; h = SiTU(g, u) written as f16 (routed) / bf16
 //                (shared) rows;
 //   gemm<DN>     y = W2 h; out[t] += w_slot * y (routed) or += y (shared) with fp32
-//                atomics onto out (zeroed first).
+//                atomics onto out (zeroed by gemm_gather).
+// Every kernel starts with pdl_wait(), so each is launched with programmatic dependent
+// launch and its launch overlaps the previous kernel.
 //
 // One work item = 128 tokens of one unit (the MMA M side) x 256 weight rows (N: gate/up
 // the 128-row blocks of W1 and W3 for one block of f, down two 128-row blocks of W2)
@@ -113,6 +115,8 @@ struct UnitsArgs {
 
 __global__ void __launch_bounds__(1024) gemm_units_kernel(UnitsArgs a)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int32_t bad, scan_tmp[32], base;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = a.E, slots = a.T * a.k;
@@ -172,6 +176,8 @@ __global__ void __launch_bounds__(1024) gemm_units_kernel(UnitsArgs a)
 // per-token activation scale 2^-u with max|x_t| * 2^-u in [2^14, 2^15), u in [-113, 113]
 __global__ void __launch_bounds__(256) gemm_scales_kernel(int T, int d, const uint16_t *x, float *tok_scale)
 {
+    pdl_wait();
+    pdl_trigger();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (warp >= T) return;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)warp * d);
@@ -200,12 +206,18 @@ struct GatherArgs {
     const int32_t *idx, *offsets, *perm;
     const float *tok_scale;
     uint16_t *xg;
+    float *out;                     // zeroed here: the down GEMM adds into it
     int32_t *status, *abort;
 };
 __global__ void __launch_bounds__(256) gemm_gather_kernel(GatherArgs a)
 {
+    pdl_wait();
+    pdl_trigger();
     const int slots = a.T * a.k, d8 = a.d / 8;
     const bool ok_off = *a.abort == 0;
+    for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < (size_t)a.T * (a.d / 4);
+         q += (size_t)gridDim.x * blockDim.x)
+        reinterpret_cast<float4 *>(a.out)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < (size_t)slots * d8;
          q += (size_t)gridDim.x * blockDim.x) {
         const int p = (int)(q / d8), c = (int)(q % d8);
@@ -297,6 +309,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                                                                 const __grid_constant__ CUtensorMap mw1,
                                                                 const __grid_constant__ CUtensorMap mw3)
 {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(1024) uint8_t gsm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *smA = sm;                                   // kStg x kABytes: token tiles
@@ -621,10 +635,11 @@ cudaError_t launch_gemm(const GemmArgs &ga, const CUtensorMap &mbr, const CUtens
     }
     const int grid = max(1, min(num_sms(), max_items));
     timing_begin(name, s);
-    gemm_kernel<MODE><<<grid, kGemmThreads, kGemmSmem, s>>>(ga, mbr, mbs, ma1, ma3);
+    const cudaError_t err = launch_pdl(gemm_kernel<MODE>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, ga, mbr,
+                                       mbs, ma1, ma3);
     count_launch();
     timing_end(name, s);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace
@@ -647,27 +662,29 @@ cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x,
     uint16_t *hp = reinterpret_cast<uint16_t *>(ws + L.hp);
     const size_t rows_all = (size_t)T * k + (size_t)S * T;
 
-    cudaError_t err = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * c.d, s);
-    if (err != cudaSuccess) return err;
+    cudaError_t err = cudaSuccess;
     // items per token tile: gate/up one per 128-row block of f, down one per pair of 128-row blocks of d
     UnitsArgs ua{T, E, k, S, c.f / kTileRows, (c.d / kTileRows + 1) / 2, offsets, units, prefix_gu,
                  prefix_dn, n_units, status, abort};
     timing_begin("gemm_units", s);
-    gemm_units_kernel<<<1, 1024, 0, s>>>(ua);
+    err = launch_pdl(gemm_units_kernel, dim3(1), dim3(1024), 0, s, ua);
     count_launch();
     timing_end("gemm_units", s);
+    if (err != cudaSuccess) return err;
     timing_begin("gemm_scales", s);
-    gemm_scales_kernel<<<(T * 32 + 255) / 256, 256, 0, s>>>(T, c.d, x, tok_scale);
+    err = launch_pdl(gemm_scales_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, s, T, c.d, x, tok_scale);
     count_launch();
     timing_end("gemm_scales", s);
-    GatherArgs gta{T, c.d, k, E, x, idx, offsets, perm, tok_scale, xg, status, abort};
+    if (err != cudaSuccess) return err;
+    GatherArgs gta{T, c.d, k, E, x, idx, offsets, perm, tok_scale, xg, out, status, abort};
     {
         const size_t work = (size_t)T * k * (c.d / 8);
         int grid = (int)std::min<size_t>((work + 255) / 256, (size_t)num_sms() * 16);
         timing_begin("gemm_gather", s);
-        gemm_gather_kernel<<<std::max(grid, 1), 256, 0, s>>>(gta);
+        err = launch_pdl(gemm_gather_kernel, dim3(std::max(grid, 1)), dim3(256), 0, s, gta);
         count_launch();
         timing_end("gemm_gather", s);
+        if (err != cudaSuccess) return err;
     }
 
     CUtensorMap mb_routed{}, mb_shared{}, ma1{}, ma3{}, mb_h{}, ma2{};

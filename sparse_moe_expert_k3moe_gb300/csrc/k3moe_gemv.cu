@@ -208,6 +208,8 @@ struct PrepArgs {
 // routing and builds the active list and the inverse permutation.
 __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int32_t bad;
     __shared__ int32_t scan_tmp[32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -663,6 +665,8 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                                                              const __grid_constant__ CUtensorMap m3,
                                                              const __grid_constant__ CUtensorMap m2)
 {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     constexpr int kStageBytes = Geo<MODE>::kStageBytes;
@@ -971,6 +975,8 @@ __device__ __forceinline__ float combine_one(const CombineArgs &a, int t, int c,
 
 __global__ void __launch_bounds__(256) fwd_combine_kernel(CombineArgs a)
 {
+    pdl_wait();
+    pdl_trigger();
     const size_t n = (size_t)a.T * a.d;
     const bool ab = *a.abort != 0;
     const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
@@ -1115,9 +1121,10 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, xs, arrive,
                 (c.n_experts + c.n_shared) * (c.f / kTileRows), status, abort};
     timing_begin("fwd_prep", s);
-    fwd_prep_kernel<<<(T + 31) / 32, 1024, 0, s>>>(pa);
+    cudaError_t err = launch_pdl(fwd_prep_kernel, dim3((T + 31) / 32), dim3(1024), 0, s, pa);
     count_launch();
     timing_end("fwd_prep", s);
+    if (err != cudaSuccess) return err;
 
     CUtensorMap m1{}, m3{}, m2{};
     if (c.n_shared > 0) {
@@ -1136,18 +1143,20 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
         const size_t smem = 1024 + (size_t)kStages * Geo<kGateUp>::kStageBytes + bsl;
         const int blocks = grid_blocks(gemv_kernel<kGateUp>, smem);
         timing_begin("gemv_gateup", s);
-        gemv_kernel<kGateUp><<<blocks, kThreads + 32, smem, s>>>(ga, m1, m3, m2);
+        err = launch_pdl(gemv_kernel<kGateUp>, dim3(blocks), dim3(kThreads + 32), smem, s, ga, m1, m3, m2);
         count_launch();
         timing_end("gemv_gateup", s);
+        if (err != cudaSuccess) return err;
     }
     {
         const size_t bsl = 2 * (size_t)kBSlots * ga.brows * Geo<kDown>::b_row_bytes(ga);
         const size_t smem = 1024 + (size_t)kStages * Geo<kDown>::kStageBytes + bsl;
         const int blocks = grid_blocks(gemv_kernel<kDown>, smem);
         timing_begin("gemv_down", s);
-        gemv_kernel<kDown><<<blocks, kThreads + 32, smem, s>>>(ga, m1, m3, m2);
+        err = launch_pdl(gemv_kernel<kDown>, dim3(blocks), dim3(kThreads + 32), smem, s, ga, m1, m3, m2);
         count_launch();
         timing_end("gemv_down", s);
+        if (err != cudaSuccess) return err;
     }
     CombineArgs ca{T, c.d, c.top_k, c.n_shared, L.p_dn, weight, inv, ys, out, abort};
     {
@@ -1156,9 +1165,10 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
         if (grid > sm_count() * 8) grid = sm_count() * 8;
         if (grid < 1) grid = 1;
         timing_begin("fwd_combine", s);
-        fwd_combine_kernel<<<grid, 256, 0, s>>>(ca);
+        err = launch_pdl(fwd_combine_kernel, dim3(grid), dim3(256), 0, s, ca);
         count_launch();
         timing_end("fwd_combine", s);
+        if (err != cudaSuccess) return err;
     }
     return cudaGetLastError();
 }

@@ -152,6 +152,31 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     return L;
 }
 
+// ----------------------------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the route and forward chains starts with pdl_wait(): it waits until the
+// previous kernel in the stream has completed and its writes are visible, before touching
+// memory, so the kernel may be launched early (launch_pdl) and its launch latency overlaps
+// the previous kernel.  pdl_trigger() then lets the next kernel launch the same way.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // ----------------------------------------------------------------------------------- launch bookkeeping
 // Every launch goes through these so launches can be counted and, on request, timed.
 void timing_begin(const char *name, cudaStream_t s);

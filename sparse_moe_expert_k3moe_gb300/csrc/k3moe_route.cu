@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
     int T, int d, int E, const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
     const float *__restrict__ bias, float *__restrict__ sc_out, float *__restrict__ ch_out)
 {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) uint8_t xs_raw[];        // kScoreTok x d bf16
     uint4 *xs = reinterpret_cast<uint4 *>(xs_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -204,6 +206,8 @@ struct TopkArgs {
 // repeated maximum with a strict comparison produces.
 __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ uint64_t keys[1024];
     __shared__ int32_t cnt[kMaxExperts];
     __shared__ int32_t slot_e[kChunkTokens * kMaxTopK];
@@ -266,6 +270,8 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
 
 __global__ void __launch_bounds__(1024) perm_count_kernel(MapArgs a)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int32_t cnt[kMaxExperts];
     __shared__ int32_t slot_e[kChunkTokens * kMaxTopK];
     __shared__ int32_t scan_tmp[32];
@@ -279,6 +285,8 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int n_chunks, int E, in
                                                          int32_t *__restrict__ chunk_base,
                                                          int32_t *__restrict__ offsets)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int32_t scan_tmp[32];
     const int e = threadIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -323,6 +331,8 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(int total_slots, int 
                                                            const int32_t *__restrict__ local_rank,
                                                            int32_t *__restrict__ perm)
 {
+    pdl_wait();
+    pdl_trigger();
     const int s = blockIdx.x * blockDim.x + threadIdx.x;
     if (s >= total_slots) return;
     const int e = idx[s];
@@ -351,10 +361,11 @@ cudaError_t launch_router_scores(const k3moe_config &c, int T, const uint16_t *x
             smem_set = smem;
         }
         timing_begin("router_scores", s);
-        router_scores_kernel<<<(E + kScoreWarps - 1) / kScoreWarps, kScoreWarps * 32, smem, s>>>(
-            T, c.d, E, x, wr, bias, sc, ch);
+        cudaError_t err = launch_pdl(router_scores_kernel, dim3((E + kScoreWarps - 1) / kScoreWarps),
+                                     dim3(kScoreWarps * 32), smem, s, T, c.d, E, x, wr, bias, sc, ch);
         count_launch();
         timing_end("router_scores", s);
+        if (err != cudaSuccess) return err;
     }
     return cudaGetLastError();
 }
@@ -381,24 +392,29 @@ cudaError_t launch_route(const k3moe_config &c, int T, const uint16_t *x, const 
     TopkArgs a{T, E, k, c.renorm, c.routed_scale, sc, ch, idx, weight,
                L.n_chunks == 1 ? status + 4 : nullptr, m};
     timing_begin("router_topk", s);
-    router_topk_kernel<<<T, 1024, 0, s>>>(a);
+    err = launch_pdl(router_topk_kernel, dim3(T), dim3(1024), 0, s, a);
     count_launch();
     timing_end("router_topk", s);
+    if (err != cudaSuccess) return err;
     if (L.n_chunks > 1) {
         int32_t *base = reinterpret_cast<int32_t *>(ws + L.chunk_base);
         timing_begin("perm_count", s);
-        perm_count_kernel<<<L.n_chunks, 1024, 0, s>>>(m);
+        err = launch_pdl(perm_count_kernel, dim3(L.n_chunks), dim3(1024), 0, s, m);
         count_launch();
         timing_end("perm_count", s);
+        if (err != cudaSuccess) return err;
         timing_begin("perm_scan", s);
-        perm_scan_kernel<<<1, 1024, 0, s>>>(L.n_chunks, E, T * k, m.chunk_counts, base, offsets);
+        err = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, L.n_chunks, E, T * k,
+                         (const int32_t *)m.chunk_counts, base, offsets);
         count_launch();
         timing_end("perm_scan", s);
+        if (err != cudaSuccess) return err;
         timing_begin("perm_scatter", s);
-        perm_scatter_kernel<<<(T * k + 255) / 256, 256, 0, s>>>(T * k, k, E, idx, base,
-                                                                 m.local_rank, perm);
+        err = launch_pdl(perm_scatter_kernel, dim3((T * k + 255) / 256), dim3(256), 0, s, T * k, k, E,
+                         (const int32_t *)idx, (const int32_t *)base, (const int32_t *)m.local_rank, perm);
         count_launch();
         timing_end("perm_scatter", s);
+        if (err != cudaSuccess) return err;
     }
     return cudaGetLastError();
 }

@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_scores_tc_kernel(const R
                                                                          const __grid_constant__ CUtensorMap mwr,
                                                                          const __grid_constant__ CUtensorMap mx)
 {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(1024) uint8_t rsm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *smA = sm, *smB = sm + kRtStg * kRtABytes;
@@ -185,9 +187,9 @@ cudaError_t launch_router_scores_tc(const k3moe_config &c, int T, const uint16_t
     const int n_items = ((c.n_experts + kRtBM - 1) / kRtBM) * ((T + kRtBN - 1) / kRtBN);
     const int grid = std::max(1, std::min(num_sms(), n_items));
     RtArgs a{T, c.d, c.n_experts, bias, sc, ch, status};
-    router_scores_tc_kernel<<<grid, kRtThreads, kRtSmem, s>>>(a, mwr, mx);
+    const cudaError_t err = launch_pdl(router_scores_tc_kernel, dim3(grid), dim3(kRtThreads), kRtSmem, s, a, mwr, mx);
     count_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace k3moe
