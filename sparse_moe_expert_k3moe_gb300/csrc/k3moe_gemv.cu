@@ -363,9 +363,10 @@ __device__ __forceinline__ Unit unit_of(const GemvArgs &a, int n_active, int u)
 
 template <int MODE>
 struct Geo {
-    // stage bytes: a W1+W3 tile pair (gate/up) or one tile (down); bf16 boxes fit in both
-    // (multiples of 1024 so every stage buffer meets the swizzled-TMA alignment)
-    static constexpr int kStageBytes = MODE == kGateUp ? 2 * kTileBytes : 16 * 1024;
+    // stage bytes: a W1+W3 tile pair (gate/up) or up to two consecutive K tiles (down);
+    // bf16 boxes fit in both (multiples of 1024 so every stage buffer meets the
+    // swizzled-TMA alignment)
+    static constexpr int kStageBytes = 2 * kTileBytes;
     // B operand staged in chunks of at most this many 128-column tiles (two chunk
     // buffers per block; down stages hi and lo halves)
     static constexpr int kChunkTilesMax = MODE == kGateUp ? 4 : 2;
@@ -422,11 +423,13 @@ __device__ __forceinline__ Item item_of(const GemvArgs &a, int n_active, int i)
     }
     return it;
 }
-template <int MODE>
+// TPS: K tiles per routed stage (gate/up 1: a W1+W3 pair; down 2 when the K part has an
+// even number of tiles, else 1)
+template <int MODE, int TPS>
 __device__ __forceinline__ int n_stages(const GemvArgs &a, int shared)
 {
     const int Kp = Geo<MODE>::K(a) / Geo<MODE>::P(a);
-    return shared ? Geo<MODE>::kSharedMats * (Kp / kSharedK) : Kp / kTileK;
+    return shared ? Geo<MODE>::kSharedMats * (Kp / kSharedK) : Kp / kTileK / TPS;
 }
 __device__ __forceinline__ int n_passes(const Unit &un) { return max(1, (un.ntok + kPassTok - 1) / kPassTok); }
 
@@ -444,22 +447,22 @@ __device__ __forceinline__ int token_of(const GemvArgs &a, const Unit &un, int p
 }
 
 // Copies of one weight stage (thread 0 only).
-template <int MODE>
+template <int MODE, int TPS>
 __device__ void issue_stage(const GemvArgs &a, const CUtensorMap *m1, const CUtensorMap *m3,
                             const CUtensorMap *m2, const Unit &un, const Item &it, int st,
                             uint8_t *buf, uint64_t *bar)
 {
     if (!un.shared) {
         const uint8_t *ex = a.table + (size_t)un.id * a.expert_bytes;
-        const int kt = it.kp * n_stages<MODE>(a, 0) + st;
+        const int kt = it.kp * (Geo<MODE>::K(a) / Geo<MODE>::P(a) / kTileK) + st * TPS;
         if (MODE == kGateUp) {
             const int ktn = a.d / kTileK;
             mbar_expect_tx(bar, 2 * kTileBytes);
             bulk_g2s(buf, ex + ((size_t)it.rb * ktn + kt) * 2 * kTileBytes, 2 * kTileBytes, bar);
         } else {
-            const int ktn = a.f / kTileK;
-            mbar_expect_tx(bar, kTileBytes);
-            bulk_g2s(buf, ex + a.gateup_bytes + ((size_t)it.rb * ktn + kt) * kTileBytes, kTileBytes, bar);
+            const int ktn = a.f / kTileK;           // the stage's TPS tiles are adjacent
+            mbar_expect_tx(bar, TPS * kTileBytes);
+            bulk_g2s(buf, ex + a.gateup_bytes + ((size_t)it.rb * ktn + kt) * kTileBytes, TPS * kTileBytes, bar);
         }
     } else {
         // one 64-column slice of one matrix; gate/up alternates W1 (even) and W3 (odd)
@@ -533,15 +536,18 @@ __device__ __forceinline__ void ldb2(uint32_t (&r)[4], const uint8_t *b, int RS,
     ldmatrix_x4(r, b + row * RS + (16 * ks + 8 * m) * 2);
 }
 
-template <int MODE, int NB>
-__device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, int st, int RS, int brows,
+template <int MODE, int NB, int TPS>
+__device__ __forceinline__ void consume_stage(const uint8_t *buf0, int shared, int st, int RS, int brows,
                                               const uint8_t *bhi, const uint8_t *blo,
                                               float (&acc1)[kNBMax][4], float (&acc3)[kNBMax][4])
 {
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2;
     const float zero[4] = {0.f, 0.f, 0.f, 0.f};
     if (!shared) {
-        const int ks0 = st * 8;                               // 8 k-steps per 128-column tile
+#pragma unroll
+      for (int tt = 0; tt < TPS; tt++) {
+        const uint8_t *buf = buf0 + tt * kTileBytes;
+        const int ks0 = (st * TPS + tt) * 8;                  // 8 k-steps per 128-column tile
         float f1[4], f1b[4], f3[4], f3b[4];
         row_scales(*reinterpret_cast<const uint32_t *>(buf + kTileNibbleBytes + (16 * w + g) * 4), f1);
         row_scales(*reinterpret_cast<const uint32_t *>(buf + kTileNibbleBytes + (16 * w + g + 8) * 4), f1b);
@@ -589,6 +595,7 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, in
                 }
             }
         }
+      }
     } else {
         // bf16 tile: 128 rows x 64 columns, 128-byte swizzle (chunk q of row r at
         // r*128 + ((q ^ (r&7))*16)); gate/up stages alternate W1 (even) and W3 (odd)
@@ -602,7 +609,7 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf, int shared, in
 #pragma unroll
             for (int h = 0; h < 2; h++) {
                 const int q = 2 * (kk + h) + (lane >> 4);
-                ldmatrix_x4(A[h], buf + r * 128 + ((q ^ (r & 7)) << 4));
+                ldmatrix_x4(A[h], buf0 + r * 128 + ((q ^ (r & 7)) << 4));
             }
 #pragma unroll
             for (int nb = 0; nb < NB; nb++) {
@@ -659,7 +666,7 @@ struct BHdr {
     int shared, id, rb, kp;
 };
 
-template <int MODE>
+template <int MODE, int TPS>
 __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_constant__ GemvArgs a,
                                                              const __grid_constant__ CUtensorMap m1,
                                                              const __grid_constant__ CUtensorMap m3,
@@ -731,8 +738,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
             const Item it = item_of<MODE>(a, n_active, i);
             const Unit un = unit_of(a, n_active, it.u);
             const int pass1 = it.pass1 < 0 ? n_passes(un) : it.pass1;
-            const int nst = n_stages<MODE>(a, un.shared);
-            const int spt = un.shared ? Geo<MODE>::kSharedMats * (kTileK / kSharedK) : 1;   // stages per tile
+            const int nst = n_stages<MODE, TPS>(a, un.shared);
             for (int pass = it.pass0; pass < pass1 && !stop; pass++) {
                 const int nvalid = min(kPassTok, un.ntok - pass * kPassTok);
                 // token facts of this pass: lane n holds token n's
@@ -744,7 +750,8 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                     row = (long long)out_row(a, un, pass, lane);
                     fo = un.shared ? 1.0f : a.tok_scale[a.T + tok];
                 }
-                const int spc = spt * CT;                        // stages per B chunk
+                // stages per B chunk (of CT tiles)
+                const int spc = un.shared ? Geo<MODE>::kSharedMats * (kTileK / kSharedK) * CT : CT / TPS;
                 for (int st = 0, sic = 0; st < nst; st++, n++, sic = (sic + 1 == spc) ? 0 : sic + 1) {
                     if (sic == 0) {
                         // the B chunk of this (item, pass) for the next CT tiles of K
@@ -780,7 +787,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                         hdr_sic[slot] = sic | ((sic + 1 == spc || st == nst - 1) ? 1 << 16 : 0) |
                                         (st == nst - 1 ? 1 << 17 : 0);
                         fence_proxy_async();
-                        issue_stage<MODE>(a, &m1, &m3, &m2, un, it, st, bufs + slot * kStageBytes, &full[slot]);
+                        issue_stage<MODE, TPS>(a, &m1, &m3, &m2, un, it, st, bufs + slot * kStageBytes, &full[slot]);
                         issued[slot]++;
                     }
                     __syncwarp();
@@ -823,9 +830,9 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
             }
             const uint8_t *buf = bufs + slot * kStageBytes;
             if (h.nvalid > 8)
-                consume_stage<MODE, 2>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
+                consume_stage<MODE, 2, TPS>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
             else
-                consume_stage<MODE, 1>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
+                consume_stage<MODE, 1, TPS>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
             const bool chunk_end = (sicf >> 16) & 1;
@@ -1141,9 +1148,9 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     {
         const size_t bsl = (size_t)kBSlots * ga.brows * Geo<kGateUp>::b_row_bytes(ga);
         const size_t smem = 1024 + (size_t)kStages * Geo<kGateUp>::kStageBytes + bsl;
-        const int blocks = grid_blocks(gemv_kernel<kGateUp>, smem);
+        const int blocks = grid_blocks(gemv_kernel<kGateUp, 1>, smem);
         timing_begin("gemv_gateup", s);
-        err = launch_pdl(gemv_kernel<kGateUp>, dim3(blocks), dim3(kThreads + 32), smem, s, ga, m1, m3, m2);
+        err = launch_pdl(gemv_kernel<kGateUp, 1>, dim3(blocks), dim3(kThreads + 32), smem, s, ga, m1, m3, m2);
         count_launch();
         timing_end("gemv_gateup", s);
         if (err != cudaSuccess) return err;
@@ -1151,9 +1158,12 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     {
         const size_t bsl = 2 * (size_t)kBSlots * ga.brows * Geo<kDown>::b_row_bytes(ga);
         const size_t smem = 1024 + (size_t)kStages * Geo<kDown>::kStageBytes + bsl;
-        const int blocks = grid_blocks(gemv_kernel<kDown>, smem);
+        // two K tiles per routed stage when the K part has an even number of tiles
+        const bool two = ((c.f / ga.p_dn) / kTileK) % 2 == 0;
+        const auto kern = two ? gemv_kernel<kDown, 2> : gemv_kernel<kDown, 1>;
+        const int blocks = grid_blocks(kern, smem);
         timing_begin("gemv_down", s);
-        err = launch_pdl(gemv_kernel<kDown>, dim3(blocks), dim3(kThreads + 32), smem, s, ga, m1, m3, m2);
+        err = launch_pdl(kern, dim3(blocks), dim3(kThreads + 32), smem, s, ga, m1, m3, m2);
         count_launch();
         timing_end("gemv_down", s);
         if (err != cudaSuccess) return err;
