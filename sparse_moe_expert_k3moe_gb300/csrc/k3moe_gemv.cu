@@ -6,15 +6,13 @@
 //
 // Kernels, in launch order:
 //   fwd_prep     validates offsets/perm against idx, lists the active experts, inverts
-//                perm (slot -> position), picks each token's activation scale; sets the
-//                abort flag on bad input;
+//                perm (slot -> position), picks each token's activation scale 2^-u and
+//                writes x * 2^-u as f16; sets the abort flag on bad input;
 //   gemv_gateup  for every (active expert, token) and (shared expert, token): g = W1 x,
-//                u = W3 x; h = SiTU(g, u) when the K range is not split, else the g, u
-//                partial sums of each K part;
-//   gemv_down    y = W2 h (SiTU of the summed parts applied while staging h), fp32,
-//                one partial per K part;
-//   fwd_combine  out[t] = sum_j w[t][j] y[pos(t,j)] + sum_s y_shared[s][t], parts and
-//                terms added in a fixed order.
+//                u = W3 x, h = SiTU(g, u), stored as a hi + lo pair;
+//   gemv_down    y = W2 h, fp32, one row per (slot or shared expert, token);
+//   fwd_combine  out[t] = sum_j w[t][j] y[pos(t,j)] + sum_s y_shared[s][t], terms added
+//                in a fixed order.
 //
 // Arithmetic: a streamed mat-vec is bound by HBM bandwidth, so the inner loop must stay
 // cheap.  The tensor-core warp MMA (m16n8k16) serves as the multiply-add engine: each
@@ -27,11 +25,14 @@
 // enters the down projection as an f16 pair hi + lo (about 22 significant bits).  The
 // bf16 shared experts use bf16 MMAs on tensor-map (TMA) tiles, with h as a bf16 pair.
 //
-// Streaming: a persistent grid; each block owns a contiguous range of work items (128
-// weight rows of one expert, over one K part), so consecutive items share the expert
-// and its staged activations.  Weight tiles move global -> shared with bulk async copies
-// through a 4-stage mbarrier ring (cp.async.bulk for packed tiles, cp.async.bulk.tensor
-// for bf16 tiles); warp w of the block owns rows 16w..16w+15 of the item.
+// Streaming: a persistent grid, two blocks per SM; work items (128 weight rows of one
+// unit over the whole K) are handed out heaviest first through an atomic counter.  In
+// each block one producer warp moves everything by bulk async copies and never waits for
+// data: the weight stages (a packed W1+W3 tile pair for gate/up, two consecutive packed
+// W2 tiles for down, or a bf16 tile through a tensor map) through a 4-stage mbarrier
+// ring, and the B operand (the tokens' activations or h rows, one copy per token row) in
+// chunks through two alternating slots.  Eight consumer warps each own rows 16w..16w+15
+// of the item and never synchronise the block.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -197,8 +198,6 @@ struct PrepArgs {
     int32_t *inv;        // [T * k]
     float *tok_scale;    // [2][T]
     uint16_t *xs;        // [T][d] f16: x * 2^-u per token (the routed experts' B operand)
-    int32_t *arrive;     // K-part arrival counters, zeroed here
-    int n_arrive;
     int32_t *status;
     int32_t *abort;
 };
@@ -273,7 +272,6 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
         if (e < 0 || e >= E) atomicOr(&bad, K3MOE_DEV_BAD_INDEX);
         a.inv[s] = -1;
     }
-    for (int i = tid; i < a.n_arrive; i += blockDim.x) a.arrive[i] = 0;
     __syncthreads();
     const bool offsets_ok = !(bad & K3MOE_DEV_BAD_OFFSETS);
     // active experts in ascending order (block scan over flags)
@@ -322,7 +320,6 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
 // -------------------------------------------------------------------------------- streamed mat-vec
 struct GemvArgs {
     int T, d, f, k, S, E;
-    int p_gu, p_dn;                 // K splits of the gate/up and down items
     int brows;                      // token rows of a staged B chunk: min(16, T)
     float b1, b2;
     const uint16_t *x, *xs;
@@ -330,9 +327,8 @@ struct GemvArgs {
     const float *tok_scale;
     const uint8_t *table;
     size_t expert_bytes, gateup_bytes;
-    float *gu, *ys;
+    float *ys;
     uint16_t *hp;                   // SiTU output planes: hi at [0], lo at [rows * f]
-    int32_t *arrive;                // K-part arrival counters per (unit, row block)
     const int32_t *abort;
     int32_t *status;
     int32_t *work;                  // [2] work counters (gate/up, down), zeroed by fwd_prep
@@ -374,11 +370,10 @@ struct Geo {
     static constexpr int kSharedMats = MODE == kGateUp ? 2 : 1;
     __host__ __device__ static int rows(const GemvArgs &a) { return MODE == kGateUp ? a.f : a.d; }
     __host__ __device__ static int K(const GemvArgs &a) { return MODE == kGateUp ? a.d : a.f; }
-    __host__ __device__ static int P(const GemvArgs &a) { return MODE == kGateUp ? a.p_gu : a.p_dn; }
-    // 128-column tiles per staged B chunk (the last chunk of a K part may be shorter)
+    // 128-column tiles per staged B chunk (the last chunk of K may be shorter)
     __host__ __device__ static int chunk_tiles(const GemvArgs &a)
     {
-        const int kt = K(a) / P(a) / kTileK;
+        const int kt = K(a) / kTileK;
         return kt < kChunkTilesMax ? kt : kChunkTilesMax;
     }
     // bytes between two token rows of a staged B chunk: 16 bytes of padding keep the
@@ -386,49 +381,46 @@ struct Geo {
     __host__ __device__ static int b_row_bytes(const GemvArgs &a) { return chunk_tiles(a) * kTileK * 2 + 16; }
 };
 
-// A work item: 128 rows of one unit over one K part, for passes [pass0, pass1).
+// A work item: 128 rows of one unit over the whole K, for passes [pass0, pass1).
 struct Item {
-    int u, rb, kp, pass0, pass1;
+    int u, rb, pass0, pass1;
 };
 __device__ __forceinline__ int shared_passes(const GemvArgs &a) { return max(1, (a.T + kPassTok - 1) / kPassTok); }
 template <int MODE>
 __device__ __forceinline__ int n_items_of(const GemvArgs &a, int n_active)
 {
-    const int nrb = Geo<MODE>::rows(a) / kItemRows, P = Geo<MODE>::P(a);
-    return (a.S * shared_passes(a) + n_active) * P * nrb;
+    const int nrb = Geo<MODE>::rows(a) / kItemRows;
+    return (a.S * shared_passes(a) + n_active) * nrb;
 }
 // Items are handed out heaviest first: the bf16 shared experts (four times the bytes per
 // weight, one item per token pass), then the routed experts (all passes in one item).
 template <int MODE>
 __device__ __forceinline__ Item item_of(const GemvArgs &a, int n_active, int i)
 {
-    const int nrb = Geo<MODE>::rows(a) / kItemRows, P = Geo<MODE>::P(a);
-    const int nsp = shared_passes(a), n_sh = a.S * nsp * P * nrb;
+    const int nrb = Geo<MODE>::rows(a) / kItemRows;
+    const int nsp = shared_passes(a), n_sh = a.S * nsp * nrb;
     Item it;
     if (i < n_sh) {
         it.rb = i % nrb;
-        int j = i / nrb;
-        it.kp = j % P;
-        j /= P;
+        const int j = i / nrb;
         it.pass0 = j % nsp;
         it.pass1 = it.pass0 + 1;
         it.u = n_active + j / nsp;
     } else {
         const int j = i - n_sh;
         it.rb = j % nrb;
-        it.kp = (j / nrb) % P;
-        it.u = j / (P * nrb);
+        it.u = j / nrb;
         it.pass0 = 0;
         it.pass1 = -1;          // all passes of the unit
     }
     return it;
 }
-// TPS: K tiles per routed stage (gate/up 1: a W1+W3 pair; down 2 when the K part has an
-// even number of tiles, else 1)
+// TPS: K tiles per routed stage (gate/up 1: a W1+W3 pair; down 2 when K has an even
+// number of tiles, else 1)
 template <int MODE, int TPS>
 __device__ __forceinline__ int n_stages(const GemvArgs &a, int shared)
 {
-    const int Kp = Geo<MODE>::K(a) / Geo<MODE>::P(a);
+    const int Kp = Geo<MODE>::K(a);
     return shared ? Geo<MODE>::kSharedMats * (Kp / kSharedK) : Kp / kTileK / TPS;
 }
 __device__ __forceinline__ int n_passes(const Unit &un) { return max(1, (un.ntok + kPassTok - 1) / kPassTok); }
@@ -454,7 +446,7 @@ __device__ void issue_stage(const GemvArgs &a, const CUtensorMap *m1, const CUte
 {
     if (!un.shared) {
         const uint8_t *ex = a.table + (size_t)un.id * a.expert_bytes;
-        const int kt = it.kp * (Geo<MODE>::K(a) / Geo<MODE>::P(a) / kTileK) + st * TPS;
+        const int kt = st * TPS;
         if (MODE == kGateUp) {
             const int ktn = a.d / kTileK;
             mbar_expect_tx(bar, 2 * kTileBytes);
@@ -467,7 +459,7 @@ __device__ void issue_stage(const GemvArgs &a, const CUtensorMap *m1, const CUte
     } else {
         // one 64-column slice of one matrix; gate/up alternates W1 (even) and W3 (odd)
         const int slice = st / Geo<MODE>::kSharedMats;
-        const int k0 = it.kp * (Geo<MODE>::K(a) / Geo<MODE>::P(a)) + slice * kSharedK;
+        const int k0 = slice * kSharedK;
         const CUtensorMap *m = MODE == kGateUp ? ((st & 1) ? m3 : m1) : m2;
         const int row = un.id * Geo<MODE>::rows(a) + it.rb * kItemRows;
         mbar_expect_tx(bar, kItemRows * kSharedK * 2);
@@ -502,12 +494,12 @@ __device__ __forceinline__ void issue_b_chunk(const GemvArgs &a, const Unit &un,
                                               int nvalid, int tok, long long row, uint8_t *bhi, uint8_t *blo,
                                               uint64_t *bar, int lane)
 {
-    const int Kp = Geo<MODE>::K(a) / Geo<MODE>::P(a), CT = Geo<MODE>::chunk_tiles(a);
+    const int Kp = Geo<MODE>::K(a), CT = Geo<MODE>::chunk_tiles(a);
     const int RS = Geo<MODE>::b_row_bytes(a);
-    const int c0 = chunk * CT * kTileK;                         // first column within the K part
+    const int c0 = chunk * CT * kTileK;                         // first column of the chunk
     const int cols = min(CT * kTileK, Kp - c0);
     const uint32_t row_bytes = (uint32_t)cols * 2;
-    const int k0 = it.kp * Kp + c0;
+    const int k0 = c0;
     if (lane == 0) mbar_expect_tx(bar, (uint32_t)nvalid * row_bytes * (MODE == kDown ? 2u : 1u));
     __syncwarp();
     if (lane < nvalid) {
@@ -663,7 +655,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity)
 // Facts of the unit, item and pass a staged B chunk belongs to (written by the producer).
 struct BHdr {
     int item, pass, nvalid;
-    int shared, id, rb, kp;
+    int shared, id, rb;
 };
 
 template <int MODE, int TPS>
@@ -679,7 +671,6 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
     constexpr int kStageBytes = Geo<MODE>::kStageBytes;
     constexpr int kHalves = MODE == kDown ? 2 : 1;
     uint8_t *bufs = smem;                                          // kStages * kStageBytes
-    const int P = Geo<MODE>::P(a);
     const int CT = Geo<MODE>::chunk_tiles(a), RS = Geo<MODE>::b_row_bytes(a);
     const size_t bbytes = (size_t)a.brows * RS;                    // one half of one B slot
     uint8_t *bbase = smem + kStages * kStageBytes;                 // slot b, half h at (kHalves*b + h)
@@ -766,7 +757,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                             pts[b].row[lane] = row;
                             pts[b].fo[lane] = fo;
                         }
-                        if (lane == 0) bh[b] = BHdr{i, pass, nvalid, un.shared, un.id, it.rb, it.kp};
+                        if (lane == 0) bh[b] = BHdr{i, pass, nvalid, un.shared, un.id, it.rb};
                         __syncwarp();
                         issue_b_chunk<MODE>(a, un, it, st / spc, nvalid, tok, row, bbase + kHalves * b * bbytes,
                                             bbase + (kHalves * b + kHalves - 1) * bbytes, &bfull[b], lane);
@@ -800,7 +791,6 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
         const int g = lane >> 2, t4 = lane & 3;
         float acc1[kNBMax][4], acc3[kNBMax][4];
         int cur_bu = -1, b = 0;
-        const int nrb = Geo<MODE>::rows(a) / kItemRows;
         for (int n = 0;; n++) {
             const int slot = n % kStages;
             if (!mbar_wait_warp(&full[slot], (uint32_t)(n / kStages) & 1u)) {
@@ -849,9 +839,9 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                             const int nn = nb * 8 + 2 * t4 + (i & 1);
                             if (nn >= nvalid) continue;
                             const int row = row0 + ((i >> 1) << 3);
-                            a.ys[((size_t)h.kp * rows_all + (size_t)pt.row[nn]) * a.d + row] = acc1[nb][i];
+                            a.ys[(size_t)pt.row[nn] * a.d + row] = acc1[nb][i];
                         }
-                } else if (P == 1) {
+                } else {
                     const size_t plane = rows_all * a.f;
 #pragma unroll
                     for (int nb = 0; nb < kNBMax; nb++)
@@ -864,49 +854,6 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                             store_h(a, h.shared, (size_t)pt.row[nn] * a.f + row, plane,
                                     situ(acc1[nb][i] * fo, acc3[nb][i] * fo, a.b1, a.b2));
                         }
-                } else {
-                    // K split: publish this warp's partial sums; the last of the P x 8 warps
-                    // holding rows of this (unit, row block) adds all parts in order and
-                    // applies SiTU to all 128 rows
-#pragma unroll
-                    for (int nb = 0; nb < kNBMax; nb++)
-#pragma unroll
-                        for (int i = 0; i < 4; i++) {
-                            const int nn = nb * 8 + 2 * t4 + (i & 1);
-                            if (nn >= nvalid) continue;
-                            const int row = row0 + ((i >> 1) << 3);
-                            float *base = a.gu + ((size_t)h.kp * rows_all + (size_t)pt.row[nn]) * 2 * a.f;
-                            base[row] = acc1[nb][i];
-                            base[a.f + row] = acc3[nb][i];
-                        }
-                    __threadfence();
-                    __syncwarp();
-                    int last = 0;
-                    if (lane == 0) {
-                        // counter of (unit, row block): routed expert e at e, shared s at E + s
-                        int32_t *ctr = a.arrive + (size_t)(h.shared ? a.E + h.id : h.id) * nrb + h.rb;
-                        const int old = atomicAdd(ctr, 1);
-                        last = (old == P * nwarps - 1);
-                        if (last) *ctr = 0;
-                    }
-                    if (__shfl_sync(0xffffffffu, last, 0)) {
-                        __threadfence();
-                        const size_t plane = rows_all * a.f;
-                        for (int nn = 0; nn < nvalid; nn++) {
-                            const size_t prow = (size_t)pt.row[nn];
-                            const float fo = pt.fo[nn];
-                            for (int r = lane; r < kItemRows; r += 32) {
-                                const int row = h.rb * kItemRows + r;
-                                float gs = 0.0f, us = 0.0f;
-                                for (int p = 0; p < P; p++) {
-                                    const float *base = a.gu + ((size_t)p * rows_all + prow) * 2 * a.f;
-                                    gs += __ldcg(base + row);
-                                    us += __ldcg(base + a.f + row);
-                                }
-                                store_h(a, h.shared, prow * a.f + row, plane, situ(gs * fo, us * fo, a.b1, a.b2));
-                            }
-                        }
-                    }
                 }
             }
             if (chunk_end) {
@@ -928,7 +875,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
 
 // -------------------------------------------------------------------------------- combine
 struct CombineArgs {
-    int T, d, k, S, P;
+    int T, d, k, S;
     const float *weight;
     const int32_t *inv;
     const float *ys;
@@ -937,12 +884,10 @@ struct CombineArgs {
 };
 
 // One thread per output element; the token's k positions and weights are read first and
-// every partial row is then loaded (unconditionally: prep has validated the positions,
-// and an aborted call writes zeros) before any is summed, so a thread's loads are all in
-// flight together.  Sum order: slot j ascending (its K parts in order), then the shared
-// experts in order.
-template <int P>
-__device__ __forceinline__ float combine_one(const CombineArgs &a, int t, int c, size_t rows_all)
+// every y row is then loaded (unconditionally: prep has validated the positions, and an
+// aborted call writes zeros) before any is summed, so a thread's loads are all in flight
+// together.  Sum order: slot j ascending, then the shared experts in order.
+__device__ __forceinline__ float combine_one(const CombineArgs &a, int t, int c)
 {
     const int slots = a.T * a.k;
     int pos[kMaxTopK];
@@ -956,27 +901,12 @@ __device__ __forceinline__ float combine_one(const CombineArgs &a, int t, int c,
     }
     float y[kMaxTopK];
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; j++) y[j] = 0.0f;
-#pragma unroll
-    for (int kp = 0; kp < P; kp++) {
-        const float *base = a.ys + (size_t)kp * rows_all * a.d + c;
-        float v[kMaxTopK];
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; j++) v[j] = j < a.k ? base[(size_t)pos[j] * a.d] : 0.0f;
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; j++) y[j] += v[j];
-    }
+    for (int j = 0; j < kMaxTopK; j++) y[j] = j < a.k ? a.ys[(size_t)pos[j] * a.d + c] : 0.0f;
     float acc = 0.0f;
 #pragma unroll
     for (int j = 0; j < kMaxTopK; j++)
         if (j < a.k) acc = fmaf(wt[j], y[j], acc);
-    for (int s = 0; s < a.S; s++) {
-        const size_t row = (size_t)slots + (size_t)s * a.T + t;
-        float ysh = 0.0f;
-#pragma unroll
-        for (int kp = 0; kp < P; kp++) ysh += a.ys[((size_t)kp * rows_all + row) * a.d + c];
-        acc += ysh;
-    }
+    for (int s = 0; s < a.S; s++) acc += a.ys[((size_t)slots + (size_t)s * a.T + t) * a.d + c];
     return acc;
 }
 
@@ -986,19 +916,10 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(CombineArgs a)
     pdl_trigger();
     const size_t n = (size_t)a.T * a.d;
     const bool ab = *a.abort != 0;
-    const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
     for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n;
          q += (size_t)gridDim.x * blockDim.x) {
         const int t = (int)(q / a.d), c = (int)(q % a.d);
-        float acc = 0.0f;
-        if (!ab) {
-            switch (a.P) {
-            case 1: acc = combine_one<1>(a, t, c, rows_all); break;
-            case 2: acc = combine_one<2>(a, t, c, rows_all); break;
-            default: acc = combine_one<4>(a, t, c, rows_all); break;
-            }
-        }
-        a.out[q] = acc;
+        a.out[q] = ab ? 0.0f : combine_one(a, t, c);
     }
 }
 
@@ -1119,14 +1040,11 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     int32_t *active = reinterpret_cast<int32_t *>(ws + L.active);
     int32_t *inv = reinterpret_cast<int32_t *>(ws + L.inv);
     float *tok_scale = reinterpret_cast<float *>(ws + L.tok_scale);
-    float *gu = reinterpret_cast<float *>(ws + L.gu);
     uint16_t *hp = reinterpret_cast<uint16_t *>(ws + L.hp);
-    int32_t *arrive = reinterpret_cast<int32_t *>(ws + L.arrive);
     float *ys = reinterpret_cast<float *>(ws + L.ys);
 
     uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
-    PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, xs, arrive,
-                (c.n_experts + c.n_shared) * (c.f / kTileRows), status, abort};
+    PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, xs, status, abort};
     timing_begin("fwd_prep", s);
     cudaError_t err = launch_pdl(fwd_prep_kernel, dim3((T + 31) / 32), dim3(1024), 0, s, pa);
     count_launch();
@@ -1140,9 +1058,9 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
             !cached_bf16_map(&m2, sh_w2, (uint64_t)c.n_shared * c.d, c.f))
             return cudaErrorInvalidValue;
     }
-    GemvArgs ga{T, c.d, c.f, c.top_k, c.n_shared, c.n_experts, L.p_gu, L.p_dn, 0, c.situ_b1, c.situ_b2,
+    GemvArgs ga{T, c.d, c.f, c.top_k, c.n_shared, c.n_experts, 0, c.situ_b1, c.situ_b2,
                 x, xs, offsets, perm, active, tok_scale, table, expert_bytes(c.d, c.f),
-                gateup_block_bytes(c.d, c.f), gu, ys, hp, arrive, abort, status, abort + 1};
+                gateup_block_bytes(c.d, c.f), ys, hp, abort, status, abort + 1};
     // B chunks hold min(16, T) token rows
     ga.brows = T < kPassTok ? T : kPassTok;
     {
@@ -1158,8 +1076,8 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     {
         const size_t bsl = 2 * (size_t)kBSlots * ga.brows * Geo<kDown>::b_row_bytes(ga);
         const size_t smem = 1024 + (size_t)kStages * Geo<kDown>::kStageBytes + bsl;
-        // two K tiles per routed stage when the K part has an even number of tiles
-        const bool two = ((c.f / ga.p_dn) / kTileK) % 2 == 0;
+        // two K tiles per routed stage when K has an even number of tiles
+        const bool two = (c.f / kTileK) % 2 == 0;
         const auto kern = two ? gemv_kernel<kDown, 2> : gemv_kernel<kDown, 1>;
         const int blocks = grid_blocks(kern, smem);
         timing_begin("gemv_down", s);
@@ -1168,7 +1086,7 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
         timing_end("gemv_down", s);
         if (err != cudaSuccess) return err;
     }
-    CombineArgs ca{T, c.d, c.top_k, c.n_shared, L.p_dn, weight, inv, ys, out, abort};
+    CombineArgs ca{T, c.d, c.top_k, c.n_shared, weight, inv, ys, out, abort};
     {
         const size_t n = (size_t)T * c.d;
         int grid = (int)((n + 255) / 256);

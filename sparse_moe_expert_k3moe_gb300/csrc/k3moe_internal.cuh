@@ -78,16 +78,6 @@ struct StatusBlock {
     int32_t pad[62];
 };
 
-// K splits of the decode-path work items.  With few tokens there are few (expert,
-// row block) items, so each item's K range is split into P parts to fill the GPU; the
-// consumer adds the P partial sums in a fixed order.  P divides the K-tile count.
-inline int ksplit_for(int ktiles, int T, int k)
-{
-    if (T > 16 || T * k > 64) return 1;     // with a split, every unit has one token pass
-    for (int p = 4; p > 1; p >>= 1)
-        if (ktiles % p == 0) return p;
-    return 1;
-}
 
 // Forward path: the tensor-core GEMMs once an expert sees on average at least 8 tokens
 // (T*k >= 8*E) and T >= 32; the streamed mat-vecs otherwise.
@@ -106,17 +96,14 @@ struct WsLayout {
     size_t active;               // [E + 1] int32: active expert ids, then the count
     size_t inv;                  // [T*k] int32: slot -> position in perm
     size_t tok_scale;            // [2][T] f32: activation multiplier 2^-u, output factor 2^u
-    size_t gu;                   // decode: g|u partials [P_gu][rows][2][f] f32 (only when P_gu > 1)
     size_t hp;                   // decode: SiTU output as hi and lo planes [2][rows][f] 16-bit
-    size_t arrive;               // decode: per (unit, row block) K-part arrival counters
     size_t xs;                   // decode: activations x * 2^-u per token [T][d] f16
-    size_t ys;                   // decode: y partials [P_dn][rows][d] f32
+    size_t ys;                   // decode: y rows [rows][d] f32
     size_t xg;                   // prefill: routed activations in perm order [T*k][d] f16
     size_t units;                // prefill: unit list [E+S][4], item prefixes, unit count
     size_t total;
     bool gemm;                   // which forward path this T takes
     int n_chunks;
-    int p_gu, p_dn;              // K splits of the gate/up and down items
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -128,8 +115,6 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     const size_t slots = (size_t)T * k;
     L.n_chunks = (T + kChunkTokens - 1) / kChunkTokens;
     L.gemm = use_gemm_path(c, T);
-    L.p_gu = L.gemm ? 1 : ksplit_for(c.d / kTileK, T, c.top_k);
-    L.p_dn = L.gemm ? 1 : ksplit_for(c.f / kTileK, T, c.top_k);
     size_t o = 0;
     L.status = o; o += 256;
     L.sc = o; o = align256(o + (size_t)T * E * 4);
@@ -141,11 +126,9 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     L.inv = o; o = align256(o + slots * 4);
     L.tok_scale = o; o = align256(o + (size_t)T * 2 * 4);
     const size_t rows = slots + S * (size_t)T;
-    L.gu = o; o = align256(o + (!L.gemm && L.p_gu > 1 ? rows * (size_t)c.f * 4 * 2 * L.p_gu : 0));
     L.hp = o; o = align256(o + rows * (size_t)c.f * 2 * (L.gemm ? 1 : 2));
-    L.arrive = o; o = align256(o + (L.gemm ? 0 : (E + S) * (size_t)(c.f / kTileRows) * 4));
     L.xs = o; o = align256(o + (L.gemm ? 0 : (size_t)T * c.d * 2));
-    L.ys = o; o = align256(o + (L.gemm ? 0 : rows * (size_t)c.d * 4 * L.p_dn));
+    L.ys = o; o = align256(o + (L.gemm ? 0 : rows * (size_t)c.d * 4));
     L.xg = o; o = align256(o + (L.gemm ? slots * (size_t)c.d * 2 : 0));
     L.units = o; o = align256(o + (L.gemm ? (4 * (E + S) + 2 * (E + S + 1) + 1) * 4 : 0));
     L.total = o;
