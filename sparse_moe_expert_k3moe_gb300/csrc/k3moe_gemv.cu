@@ -198,6 +198,8 @@ struct PrepArgs {
     int32_t *inv;        // [T * k]
     float *tok_scale;    // [2][T]
     uint16_t *xs;        // [T][d] f16: x * 2^-u per token (the routed experts' B operand)
+    int32_t *shctr;      // shared gate/up arrival counters, zeroed here
+    int n_shctr;
     int32_t *status;
     int32_t *abort;
 };
@@ -272,6 +274,7 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
         if (e < 0 || e >= E) atomicOr(&bad, K3MOE_DEV_BAD_INDEX);
         a.inv[s] = -1;
     }
+    for (int i = tid; i < a.n_shctr; i += blockDim.x) a.shctr[i] = 0;
     __syncthreads();
     const bool offsets_ok = !(bad & K3MOE_DEV_BAD_OFFSETS);
     // active experts in ascending order (block scan over flags)
@@ -327,7 +330,9 @@ struct GemvArgs {
     const float *tok_scale;
     const uint8_t *table;
     size_t expert_bytes, gateup_bytes;
-    float *ys;
+    float *ys;                      // y rows: slots, then per shared expert its K parts x T
+    float *gush;                    // shared gate/up partials [parts][S][T][2][f]
+    int32_t *shctr;                 // shared gate/up arrival counters [S][f/128]
     uint16_t *hp;                   // SiTU output planes: hi at [0], lo at [rows * f]
     const int32_t *abort;
     int32_t *status;
@@ -370,6 +375,10 @@ struct Geo {
     static constexpr int kSharedMats = MODE == kGateUp ? 2 : 1;
     __host__ __device__ static int rows(const GemvArgs &a) { return MODE == kGateUp ? a.f : a.d; }
     __host__ __device__ static int K(const GemvArgs &a) { return MODE == kGateUp ? a.d : a.f; }
+    __host__ __device__ static int Psh(const GemvArgs &a)
+    {
+        return MODE == kGateUp ? shared_kparts(K(a) / kTileK, a.T) : 1;
+    }
     // 128-column tiles per staged B chunk (the last chunk of K may be shorter)
     __host__ __device__ static int chunk_tiles(const GemvArgs &a)
     {
@@ -384,13 +393,14 @@ struct Geo {
 // A work item: 128 rows of one unit over the whole K, for passes [pass0, pass1).
 struct Item {
     int u, rb, pass0, pass1;
+    int kp, nkp;                    // K part of a shared item (routed: 0 of 1)
 };
 __device__ __forceinline__ int shared_passes(const GemvArgs &a) { return max(1, (a.T + kPassTok - 1) / kPassTok); }
 template <int MODE>
 __device__ __forceinline__ int n_items_of(const GemvArgs &a, int n_active)
 {
     const int nrb = Geo<MODE>::rows(a) / kItemRows;
-    return (a.S * shared_passes(a) + n_active) * nrb;
+    return (a.S * shared_passes(a) * Geo<MODE>::Psh(a) + n_active) * nrb;
 }
 // Items are handed out heaviest first: the bf16 shared experts (four times the bytes per
 // weight, one item per token pass), then the routed experts (all passes in one item).
@@ -398,11 +408,14 @@ template <int MODE>
 __device__ __forceinline__ Item item_of(const GemvArgs &a, int n_active, int i)
 {
     const int nrb = Geo<MODE>::rows(a) / kItemRows;
-    const int nsp = shared_passes(a), n_sh = a.S * nsp * nrb;
+    const int nsp = shared_passes(a), P = Geo<MODE>::Psh(a), n_sh = a.S * nsp * P * nrb;
     Item it;
     if (i < n_sh) {
         it.rb = i % nrb;
-        const int j = i / nrb;
+        int j = i / nrb;
+        it.kp = j % P;
+        it.nkp = P;
+        j /= P;
         it.pass0 = j % nsp;
         it.pass1 = it.pass0 + 1;
         it.u = n_active + j / nsp;
@@ -410,6 +423,8 @@ __device__ __forceinline__ Item item_of(const GemvArgs &a, int n_active, int i)
         const int j = i - n_sh;
         it.rb = j % nrb;
         it.u = j / nrb;
+        it.kp = 0;
+        it.nkp = 1;
         it.pass0 = 0;
         it.pass1 = -1;          // all passes of the unit
     }
@@ -420,8 +435,8 @@ __device__ __forceinline__ Item item_of(const GemvArgs &a, int n_active, int i)
 template <int MODE, int TPS>
 __device__ __forceinline__ int n_stages(const GemvArgs &a, int shared)
 {
-    const int Kp = Geo<MODE>::K(a);
-    return shared ? Geo<MODE>::kSharedMats * (Kp / kSharedK) : Kp / kTileK / TPS;
+    const int K = Geo<MODE>::K(a);
+    return shared ? Geo<MODE>::kSharedMats * (K / Geo<MODE>::Psh(a) / kSharedK) : K / kTileK / TPS;
 }
 __device__ __forceinline__ int n_passes(const Unit &un) { return max(1, (un.ntok + kPassTok - 1) / kPassTok); }
 
@@ -459,7 +474,7 @@ __device__ void issue_stage(const GemvArgs &a, const CUtensorMap *m1, const CUte
     } else {
         // one 64-column slice of one matrix; gate/up alternates W1 (even) and W3 (odd)
         const int slice = st / Geo<MODE>::kSharedMats;
-        const int k0 = slice * kSharedK;
+        const int k0 = it.kp * (Geo<MODE>::K(a) / it.nkp) + slice * kSharedK;
         const CUtensorMap *m = MODE == kGateUp ? ((st & 1) ? m3 : m1) : m2;
         const int row = un.id * Geo<MODE>::rows(a) + it.rb * kItemRows;
         mbar_expect_tx(bar, kItemRows * kSharedK * 2);
@@ -494,12 +509,12 @@ __device__ __forceinline__ void issue_b_chunk(const GemvArgs &a, const Unit &un,
                                               int nvalid, int tok, long long row, uint8_t *bhi, uint8_t *blo,
                                               uint64_t *bar, int lane)
 {
-    const int Kp = Geo<MODE>::K(a), CT = Geo<MODE>::chunk_tiles(a);
+    const int Kp = Geo<MODE>::K(a) / it.nkp, CT = Geo<MODE>::chunk_tiles(a);   // this item's K range
     const int RS = Geo<MODE>::b_row_bytes(a);
     const int c0 = chunk * CT * kTileK;                         // first column of the chunk
     const int cols = min(CT * kTileK, Kp - c0);
     const uint32_t row_bytes = (uint32_t)cols * 2;
-    const int k0 = c0;
+    const int k0 = it.kp * Kp + c0;
     if (lane == 0) mbar_expect_tx(bar, (uint32_t)nvalid * row_bytes * (MODE == kDown ? 2u : 1u));
     __syncwarp();
     if (lane < nvalid) {
@@ -655,7 +670,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity)
 // Facts of the unit, item and pass a staged B chunk belongs to (written by the producer).
 struct BHdr {
     int item, pass, nvalid;
-    int shared, id, rb;
+    int shared, id, rb, kp, nkp;
 };
 
 template <int MODE, int TPS>
@@ -757,7 +772,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                             pts[b].row[lane] = row;
                             pts[b].fo[lane] = fo;
                         }
-                        if (lane == 0) bh[b] = BHdr{i, pass, nvalid, un.shared, un.id, it.rb};
+                        if (lane == 0) bh[b] = BHdr{i, pass, nvalid, un.shared, un.id, it.rb, it.kp, it.nkp};
                         __syncwarp();
                         issue_b_chunk<MODE>(a, un, it, st / spc, nvalid, tok, row, bbase + kHalves * b * bbytes,
                                             bbase + (kHalves * b + kHalves - 1) * bbytes, &bfull[b], lane);
@@ -831,7 +846,10 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                 const int row0 = h.rb * kItemRows + 16 * w + g;
                 const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
                 const int nvalid = h.nvalid;
+                const size_t slots = (size_t)a.T * a.k;
                 if (MODE == kDown) {
+                    // y row: the slot's, or for a shared expert its K part's (the combine
+                    // adds the parts in order)
 #pragma unroll
                     for (int nb = 0; nb < kNBMax; nb++)
 #pragma unroll
@@ -839,8 +857,53 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                             const int nn = nb * 8 + 2 * t4 + (i & 1);
                             if (nn >= nvalid) continue;
                             const int row = row0 + ((i >> 1) << 3);
-                            a.ys[(size_t)pt.row[nn] * a.d + row] = acc1[nb][i];
+                            size_t yrow = (size_t)pt.row[nn];
+                            if (h.shared) {
+                                const size_t t = yrow - slots - (size_t)h.id * a.T;
+                                yrow = slots + ((size_t)h.id * h.nkp + h.kp) * a.T + t;
+                            }
+                            a.ys[yrow * a.d + row] = acc1[nb][i];
                         }
+                } else if (h.nkp > 1) {
+                    // a K part of a shared expert (one token pass): publish the partial sums;
+                    // the last of the parts' 8 x nkp warps of this row block adds the parts
+                    // in order and applies SiTU to all 128 rows
+#pragma unroll
+                    for (int nb = 0; nb < kNBMax; nb++)
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const int nn = nb * 8 + 2 * t4 + (i & 1);
+                            if (nn >= nvalid) continue;
+                            const int row = row0 + ((i >> 1) << 3);
+                            float *base = a.gush + ((((size_t)h.kp * a.S + h.id) * a.T + nn) * 2) * a.f;
+                            base[row] = acc1[nb][i];
+                            base[a.f + row] = acc3[nb][i];
+                        }
+                    __threadfence();
+                    __syncwarp();
+                    int last = 0;
+                    if (lane == 0) {
+                        int32_t *ctr = a.shctr + (size_t)h.id * (a.f / kItemRows) + h.rb;
+                        const int old = atomicAdd(ctr, 1);
+                        last = (old == h.nkp * nwarps - 1);
+                        if (last) *ctr = 0;
+                    }
+                    if (__shfl_sync(0xffffffffu, last, 0)) {
+                        __threadfence();
+                        const size_t plane = rows_all * a.f;
+                        for (int nn = 0; nn < nvalid; nn++) {
+                            for (int r = lane; r < kItemRows; r += 32) {
+                                const int row = h.rb * kItemRows + r;
+                                float gs = 0.0f, us = 0.0f;
+                                for (int p = 0; p < h.nkp; p++) {
+                                    const float *base = a.gush + ((((size_t)p * a.S + h.id) * a.T + nn) * 2) * a.f;
+                                    gs += __ldcg(base + row);
+                                    us += __ldcg(base + a.f + row);
+                                }
+                                store_h(a, 1, (size_t)pt.row[nn] * a.f + row, plane, situ(gs, us, a.b1, a.b2));
+                            }
+                        }
+                    }
                 } else {
                     const size_t plane = rows_all * a.f;
 #pragma unroll
@@ -876,6 +939,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
 // -------------------------------------------------------------------------------- combine
 struct CombineArgs {
     int T, d, k, S;
+    int psh;                        // K parts of a shared expert's y (rows in order)
     const float *weight;
     const int32_t *inv;
     const float *ys;
@@ -886,7 +950,8 @@ struct CombineArgs {
 // One thread per output element; the token's k positions and weights are read first and
 // every y row is then loaded (unconditionally: prep has validated the positions, and an
 // aborted call writes zeros) before any is summed, so a thread's loads are all in flight
-// together.  Sum order: slot j ascending, then the shared experts in order.
+// together.  Sum order: slot j ascending, then the shared experts in order (each its K
+// parts in order).
 __device__ __forceinline__ float combine_one(const CombineArgs &a, int t, int c)
 {
     const int slots = a.T * a.k;
@@ -906,7 +971,11 @@ __device__ __forceinline__ float combine_one(const CombineArgs &a, int t, int c)
 #pragma unroll
     for (int j = 0; j < kMaxTopK; j++)
         if (j < a.k) acc = fmaf(wt[j], y[j], acc);
-    for (int s = 0; s < a.S; s++) acc += a.ys[((size_t)slots + (size_t)s * a.T + t) * a.d + c];
+    for (int s = 0; s < a.S; s++) {
+        float ysh = 0.0f;
+        for (int p = 0; p < a.psh; p++) ysh += a.ys[((size_t)slots + ((size_t)s * a.psh + p) * a.T + t) * a.d + c];
+        acc += ysh;
+    }
     return acc;
 }
 
@@ -1044,7 +1113,10 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     float *ys = reinterpret_cast<float *>(ws + L.ys);
 
     uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
-    PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, xs, status, abort};
+    int32_t *shctr = reinterpret_cast<int32_t *>(ws + L.shctr);
+    float *gush = reinterpret_cast<float *>(ws + L.gush);
+    PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, xs, shctr,
+                c.n_shared * (c.f / kTileRows), status, abort};
     timing_begin("fwd_prep", s);
     cudaError_t err = launch_pdl(fwd_prep_kernel, dim3((T + 31) / 32), dim3(1024), 0, s, pa);
     count_launch();
@@ -1060,7 +1132,7 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     }
     GemvArgs ga{T, c.d, c.f, c.top_k, c.n_shared, c.n_experts, 0, c.situ_b1, c.situ_b2,
                 x, xs, offsets, perm, active, tok_scale, table, expert_bytes(c.d, c.f),
-                gateup_block_bytes(c.d, c.f), ys, hp, abort, status, abort + 1};
+                gateup_block_bytes(c.d, c.f), ys, gush, shctr, hp, abort, status, abort + 1};
     // B chunks hold min(16, T) token rows
     ga.brows = T < kPassTok ? T : kPassTok;
     {
@@ -1086,7 +1158,7 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
         timing_end("gemv_down", s);
         if (err != cudaSuccess) return err;
     }
-    CombineArgs ca{T, c.d, c.top_k, c.n_shared, weight, inv, ys, out, abort};
+    CombineArgs ca{T, c.d, c.top_k, c.n_shared, 1, weight, inv, ys, out, abort};
     {
         const size_t n = (size_t)T * c.d;
         int grid = (int)((n + 255) / 256);

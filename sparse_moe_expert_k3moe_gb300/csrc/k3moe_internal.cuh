@@ -98,7 +98,9 @@ struct WsLayout {
     size_t tok_scale;            // [2][T] f32: activation multiplier 2^-u, output factor 2^u
     size_t hp;                   // decode: SiTU output as hi and lo planes [2][rows][f] 16-bit
     size_t xs;                   // decode: activations x * 2^-u per token [T][d] f16
-    size_t ys;                   // decode: y rows [rows][d] f32
+    size_t ys;                   // decode: y rows [rows_y][d] f32 (a shared expert's K parts: one row each)
+    size_t gush;                 // decode: shared gate/up partials [parts][S][T][2][f] f32
+    size_t shctr;                // decode: shared gate/up arrival counters [S][f/128] int32
     size_t xg;                   // prefill: routed activations in perm order [T*k][d] f16
     size_t units;                // prefill: unit list [E+S][4], item prefixes, unit count
     size_t total;
@@ -107,6 +109,17 @@ struct WsLayout {
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// K parts of a shared-expert gate/up work item on the decode path.  With one token pass
+// (T <= 16) a bf16 shared item carries four times the bytes of a packed routed one and
+// would set the kernel's length, so its K range is split into up to 4 parts (the parts'
+// sums are added in order).  ktiles: 128-column tiles of K.  The down projection is not
+// split: measured, its split items cost more than the balance gains.
+__host__ __device__ inline int shared_kparts(int ktiles, int T)
+{
+    if (T > 16) return 1;
+    return ktiles % 4 == 0 ? 4 : (ktiles % 2 == 0 ? 2 : 1);
+}
 
 inline WsLayout ws_layout(const k3moe_config &c, int T)
 {
@@ -128,7 +141,10 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     const size_t rows = slots + S * (size_t)T;
     L.hp = o; o = align256(o + rows * (size_t)c.f * 2 * (L.gemm ? 1 : 2));
     L.xs = o; o = align256(o + (L.gemm ? 0 : (size_t)T * c.d * 2));
-    L.ys = o; o = align256(o + (L.gemm ? 0 : rows * (size_t)c.d * 4));
+    const size_t pgu = (size_t)shared_kparts(c.d / kTileK, T), pdn = 1;
+    L.ys = o; o = align256(o + (L.gemm ? 0 : (slots + S * pdn * (size_t)T) * (size_t)c.d * 4));
+    L.gush = o; o = align256(o + (L.gemm || pgu == 1 ? 0 : pgu * S * (size_t)T * 2 * c.f * 4));
+    L.shctr = o; o = align256(o + (L.gemm ? 0 : S * (size_t)(c.f / kTileRows) * 4));
     L.xg = o; o = align256(o + (L.gemm ? slots * (size_t)c.d * 2 : 0));
     L.units = o; o = align256(o + (L.gemm ? (4 * (E + S) + 2 * (E + S + 1) + 1) * 4 : 0));
     L.total = o;
