@@ -204,84 +204,86 @@ struct PrepArgs {
     int32_t *abort;
 };
 
-// Block b converts tokens [32b, 32b + 32): warp per token, its scale 2^-u (max|x_t| in
-// [2^14, 2^15), u in [-113, 113]) and the f16 row x * 2^-u.  Block 0 also validates the
-// routing and builds the active list and the inverse permutation.
+// Block 0 validates the routing (offsets, idx and perm, through a copy of offsets in
+// shared memory) and builds the active list and the inverse permutation; block b >= 1
+// converts tokens [32(b-1), 32b): warp per token, its scale 2^-u (max|x_t| in [2^14, 2^15),
+// u in [-113, 113]) and the f16 row x * 2^-u.
 __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
 {
     pdl_wait();
     pdl_trigger();
     __shared__ int32_t bad;
     __shared__ int32_t scan_tmp[32];
+    __shared__ int32_t off[kMaxExperts + 1];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = a.E, slots = a.T * a.k;
-    {
-        const int t = blockIdx.x * 32 + warp;
-        if (t < a.T) {
-            const uint4 *row = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.d);
-            const int n16 = a.d / 8;
-            uint32_t m = 0;
-            for (int q0 = lane; q0 < n16; q0 += 32 * 8) {
-                uint4 v[8];
+    if (blockIdx.x > 0) {
+        const int t = (blockIdx.x - 1) * 32 + warp;
+        if (t >= a.T) return;
+        const uint4 *row = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.d);
+        const int n16 = a.d / 8;
+        uint32_t m = 0;
+        for (int q0 = lane; q0 < n16; q0 += 32 * 8) {
+            uint4 v[8];
 #pragma unroll
-                for (int j = 0; j < 8; j++) {          // eight independent loads in flight
-                    const int q = q0 + 32 * j;
-                    v[j] = q < n16 ? row[q] : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-                    for (int h = 0; h < 4; h++) m = max(m, max(w4[h] & 0x7FFFu, (w4[h] >> 16) & 0x7FFFu));
-                }
+            for (int j = 0; j < 8; j++) {          // eight independent loads in flight
+                const int q = q0 + 32 * j;
+                v[j] = q < n16 ? row[q] : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-            int u = 0;
-            const int eb = (int)(m >> 7);                      // biased exponent of max|x_t|
-            if (m != 0 && eb < 255) u = min(max(eb - 127 - 14, -113), 113);
-            const float xin = __uint_as_float((uint32_t)(127 - u) << 23);
-            if (lane == 0) {
-                a.tok_scale[t] = xin;
-                a.tok_scale[a.T + t] = __uint_as_float((uint32_t)(127 + u) << 23);
-            }
-            uint4 *dst = reinterpret_cast<uint4 *>(a.xs + (size_t)t * a.d);
-            for (int q = lane; q < n16; q += 32) {
-                const uint4 v = row[q];
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                uint32_t o[4];
+            for (int j = 0; j < 8; j++) {
+                const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-                for (int h = 0; h < 4; h++) {
-                    const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[h] << 16) * xin,
-                                                         __uint_as_float(w4[h] & 0xFFFF0000u) * xin);
-                    o[h] = *reinterpret_cast<const uint32_t *>(&h2);
-                }
-                dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+                for (int h = 0; h < 4; h++) m = max(m, max(w4[h] & 0x7FFFu, (w4[h] >> 16) & 0x7FFFu));
             }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        int u = 0;
+        const int eb = (int)(m >> 7);                      // biased exponent of max|x_t|
+        if (m != 0 && eb < 255) u = min(max(eb - 127 - 14, -113), 113);
+        const float xin = __uint_as_float((uint32_t)(127 - u) << 23);
+        if (lane == 0) {
+            a.tok_scale[t] = xin;
+            a.tok_scale[a.T + t] = __uint_as_float((uint32_t)(127 + u) << 23);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(a.xs + (size_t)t * a.d);
+        for (int q = lane; q < n16; q += 32) {
+            const uint4 v = row[q];
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 4; h++) {
+                const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[h] << 16) * xin,
+                                                     __uint_as_float(w4[h] & 0xFFFF0000u) * xin);
+                o[h] = *reinterpret_cast<const uint32_t *>(&h2);
+            }
+            dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        return;
     }
-    if (blockIdx.x != 0) return;
     if (tid == 0) bad = 0;
+    for (int e = tid; e <= E; e += blockDim.x) off[e] = a.offsets[e];
+    for (int s = tid; s < slots; s += blockDim.x) a.inv[s] = -1;
+    for (int i = tid; i < a.n_shctr; i += blockDim.x) a.shctr[i] = 0;
     __syncthreads();
-    // offsets: monotone, start 0, end T*k
+    // offsets: monotone, start 0, end T*k; idx in range
     for (int e = tid; e < E; e += blockDim.x) {
-        const int lo = a.offsets[e], hi = a.offsets[e + 1];
+        const int lo = off[e], hi = off[e + 1];
         if (lo < 0 || hi < lo || hi > slots) atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
     }
-    if (tid == 0 && (a.offsets[0] != 0 || a.offsets[E] != slots)) atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
+    if (tid == 0 && (off[0] != 0 || off[E] != slots)) atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
     for (int s = tid; s < slots; s += blockDim.x) {
         const int e = a.idx[s];
         if (e < 0 || e >= E) atomicOr(&bad, K3MOE_DEV_BAD_INDEX);
-        a.inv[s] = -1;
     }
-    for (int i = tid; i < a.n_shctr; i += blockDim.x) a.shctr[i] = 0;
     __syncthreads();
     const bool offsets_ok = !(bad & K3MOE_DEV_BAD_OFFSETS);
     // active experts in ascending order (block scan over flags)
     int run = 0;
     for (int base = 0; base < E; base += blockDim.x) {
         const int e = base + tid;
-        const int flag = (offsets_ok && e < E && a.offsets[e + 1] > a.offsets[e]) ? 1 : 0;
+        const int flag = (offsets_ok && e < E && off[e + 1] > off[e]) ? 1 : 0;
         const uint32_t bal = __ballot_sync(0xffffffffu, flag);
         if (lane == 0) scan_tmp[warp] = __popc(bal);
         __syncthreads();
@@ -302,10 +304,10 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
                 atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
                 continue;
             }
-            int lo = 0, hi = E;   // find e with offsets[e] <= p < offsets[e+1]
+            int lo = 0, hi = E;   // find e with off[e] <= p < off[e+1]
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
-                if (a.offsets[mid] <= p) lo = mid; else hi = mid;
+                if (off[mid] <= p) lo = mid; else hi = mid;
             }
             if (a.idx[s] != lo) atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
             if (atomicExch(&a.inv[s], p) != -1) atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
@@ -402,13 +404,17 @@ __device__ __forceinline__ int n_items_of(const GemvArgs &a, int n_active)
     const int nrb = Geo<MODE>::rows(a) / kItemRows;
     return (a.S * shared_passes(a) * Geo<MODE>::Psh(a) + n_active) * nrb;
 }
-// Items are handed out heaviest first: the bf16 shared experts (four times the bytes per
-// weight, one item per token pass), then the routed experts (all passes in one item).
+// Items are handed out longest first.  A routed item holds all passes of its expert; a
+// shared item one token pass (gate/up: one of P K parts).  Measured per-item times: a
+// whole shared item (bf16, four times the bytes of a packed one) outlasts a routed one, so
+// shared items go first; but gate/up shared items cut into K parts (P > 1) are outlasted
+// by the routed items (packed, the e2m1 decode on every weight), which then go first.
 template <int MODE>
 __device__ __forceinline__ Item item_of(const GemvArgs &a, int n_active, int i)
 {
     const int nrb = Geo<MODE>::rows(a) / kItemRows;
     const int nsp = shared_passes(a), P = Geo<MODE>::Psh(a), n_sh = a.S * nsp * P * nrb;
+    if (P > 1) i = i < n_active * nrb ? i + n_sh : i - n_active * nrb;
     Item it;
     if (i < n_sh) {
         it.rb = i % nrb;
@@ -1118,7 +1124,7 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, xs, shctr,
                 c.n_shared * (c.f / kTileRows), status, abort};
     timing_begin("fwd_prep", s);
-    cudaError_t err = launch_pdl(fwd_prep_kernel, dim3((T + 31) / 32), dim3(1024), 0, s, pa);
+    cudaError_t err = launch_pdl(fwd_prep_kernel, dim3(1 + (T + 31) / 32), dim3(1024), 0, s, pa);
     count_launch();
     timing_end("fwd_prep", s);
     if (err != cudaSuccess) return err;

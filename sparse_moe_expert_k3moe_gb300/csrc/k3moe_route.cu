@@ -6,10 +6,11 @@
 //                  sc = 1/(1+expf(-logit)), ch = sc + bias, both float, to the workspace.
 //                  A block owns 8 experts (one per warp, its Wr row held in registers)
 //                  and walks the tokens 8 at a time through shared memory;
-//   router_topk    one block per token: a bitonic sort of the E keys (ch, then the lower
-//                  index first) picks the top k in rank order; the weights are the chosen
-//                  sc renormalised by their float sum in rank order, times routed_scale.
-//                  With at most 64 tokens the last block to finish also builds the map;
+//   router_topk    one block per token: warp-level bitonic sorts and merges of the E keys
+//                  (ch, then the lower index first) pick the top k in rank order; the
+//                  weights are the chosen sc renormalised by their float sum in rank
+//                  order, times routed_scale.  With at most 64 tokens the last block to
+//                  finish (the only one, for one token) also builds the map;
 //   perm_count     (more tokens) per chunk of 64 tokens: per-expert slot counts and each
 //                  slot's stable rank inside the chunk (warp match + popc, warp by warp);
 //   perm_scan      per-expert exclusive scan over chunks, then over experts -> offsets;
@@ -39,6 +40,14 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
     const int nchunk = d / 8;                                  // 16-byte chunks per row
     const uint4 *wrow = reinterpret_cast<const uint4 *>(wr + (size_t)min(e, E - 1) * d);
     const float b = (bias && e < E) ? bias[e] : 0.0f;
+    // the first 4096 columns of the row stay in registers across the token rounds (the
+    // whole row for d <= 4096); their loads are in flight with the first x tile's
+    uint4 w0[kScoreChunks];
+#pragma unroll
+    for (int j = 0; j < kScoreChunks; j++) {
+        const int c = lane + 32 * j;
+        w0[j] = c < nchunk ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+    }
     for (int t0 = 0; t0 < T; t0 += kScoreTok) {
         const int nt = min(kScoreTok, T - t0);
         __syncthreads();
@@ -55,7 +64,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
 #pragma unroll
             for (int j = 0; j < kScoreChunks; j++) {
                 const int c = c0 + lane + 32 * j;
-                w[j] = c < nchunk ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+                w[j] = c0 == 0 ? w0[j] : (c < nchunk ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0));
             }
 #pragma unroll
             for (int i = 0; i < kScoreTok; i++) {
@@ -201,40 +210,76 @@ struct TopkArgs {
     MapArgs map;
 };
 
+// Keys of one warp, one per lane, sorted descending across the lanes (bitonic network
+// on shuffles).
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t key, int lane)
+{
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+        const bool desc = (lane & size) == 0;
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint64_t other = __shfl_xor_sync(0xffffffffu, key, stride);
+            const bool keep_max = desc == ((lane & stride) == 0);
+            key = keep_max ? (key > other ? key : other) : (key < other ? key : other);
+        }
+    }
+    return key;
+}
+// Lanes 0-15 hold a descending list, lanes 16-31 another one in ascending order: together
+// a bitonic sequence, merged descending, so lanes 0-15 end with the 16 largest keys.
+__device__ __forceinline__ uint64_t warp_merge_desc(uint64_t key, int lane)
+{
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, key, stride);
+        const bool keep_max = (lane & stride) == 0;
+        key = keep_max ? (key > other ? key : other) : (key < other ? key : other);
+    }
+    return key;
+}
+
 // blockDim = 1024; block t owns token t.  Key = (orderable(ch) << 32) | ~index, so a
-// descending sort orders by ch and, among equal ch, by ascending index -- the order the
-// repeated maximum with a strict comparison produces.
+// descending order sorts by ch and, among equal ch, by ascending index -- the order the
+// repeated maximum with a strict comparison produces.  Every key is distinct, so the k
+// largest keys are the selection.  Warp w sorts keys 32w..32w+31 and keeps its 16
+// largest; pairs of lists are then merged warp by warp (16 of 32 kept) until one remains.
 __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
 {
     pdl_wait();
     pdl_trigger();
-    __shared__ uint64_t keys[1024];
+    __shared__ uint64_t lists[2][32][kMaxTopK];
     __shared__ int32_t cnt[kMaxExperts];
     __shared__ int32_t slot_e[kChunkTokens * kMaxTopK];
     __shared__ int32_t scan_tmp[32];
     __shared__ int last;
-    const int i = threadIdx.x, lane = i & 31;
+    const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
     const int t = blockIdx.x, E = a.E, k = a.k;
+    const int nl0 = (E + 31) >> 5;                 // lists after the first level
     uint64_t key = 0;
-    if (i < E) key = ((uint64_t)orderable(a.ch[(size_t)t * E + i]) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)i);
-    for (int size = 2; size <= 1024; size <<= 1) {
-        const bool desc = (i & size) == 0;
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            uint64_t other;
-            if (stride >= 32) {
-                keys[i] = key;
-                __syncthreads();
-                other = keys[i ^ stride];
-                __syncthreads();
-            } else {
-                other = __shfl_xor_sync(0xffffffffu, key, stride);
-            }
-            const bool lower = (i & stride) == 0;
-            const bool keep_max = (desc == lower);
-            key = keep_max ? (key > other ? key : other) : (key < other ? key : other);
-        }
+    if (warp < nl0) {
+        if (i < E) key = ((uint64_t)orderable(a.ch[(size_t)t * E + i]) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)i);
+        key = warp_sort_desc(key, lane);
+        if (lane < kMaxTopK) lists[0][warp][lane] = key;
     }
-    // thread r < k now holds the rank-r key
+    int nl = nl0, cur = 0;
+    while (nl > 1) {
+        __syncthreads();
+        const int half = (nl + 1) >> 1;
+        if (warp < half) {
+            const int la = 2 * warp, lb = 2 * warp + 1;
+            uint64_t v;
+            if (lane < 16) v = lists[cur][la][lane];
+            else v = lb < nl ? lists[cur][lb][31 - lane] : 0;
+            v = warp_merge_desc(v, lane);
+            if (lane < kMaxTopK) lists[cur ^ 1][warp][lane] = v;
+        }
+        cur ^= 1;
+        nl = half;
+    }
+    __syncthreads();
+    if (warp == 0) key = lane < kMaxTopK ? lists[cur][0][lane] : 0;
+    // lane r < k of warp 0 now holds the rank-r key
     if (i < 32) {
         int e = -1;
         float w = 0.0f;
@@ -255,8 +300,12 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
             a.weight[(size_t)t * k + i] = w;
         }
     }
-    (void)lane;
     if (a.done == nullptr) return;                 // the map is built by perm_count
+    if (gridDim.x == 1) {                          // one token: its block builds the map
+        __syncthreads();
+        map_chunk(a.map, 0, true, cnt, slot_e, scan_tmp);
+        return;
+    }
     // the last block to finish builds the map of all (at most 64) tokens
     __threadfence();
     __syncthreads();
