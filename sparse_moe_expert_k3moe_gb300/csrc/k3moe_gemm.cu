@@ -26,18 +26,16 @@
 //   warp 1       MMA: one thread issues tcgen05.mma (kind::f16, M=128, N=256, K=16) into
 //                fp32 accumulators in tensor memory, two buffers of 256 columns, so one
 //                item's MMAs overlap the previous item's epilogue;
-//   warps 2-17   dequant: packed MXFP4 tiles from shared memory to f16 weight tiles
-//                (128-byte swizzle, K-major) -- the E2M1 pair decoded by the hardware
+//   warps 2-17   dequant: packed MXFP4 tiles, loaded from global memory into registers
+//                one tile ahead (and into L2 three tiles ahead), to f16 weight tiles in
+//                shared memory (128-byte swizzle, K-major) -- the E2M1 pair decoded by the hardware
 //                conversion, times 2^(b - bmax + 13) where bmax is the largest scale of
 //                the 128-row block (the packed table's trailer), so every value is exact
 //                in f16 while the block's scales span at most 36 binades; the epilogue
 //                multiplies by 2^(bmax - 140);
 //   warps 18-21  epilogue, one token per thread (warp w reads TMEM lanes 32(w%4)..):
-//                gate/up SiTU to h rows, down the weighted combine as float4 atomics;
-//   warp 22      packed-weight producer: one bulk copy per 128-column packed tile (pair),
-//                kStgP tiles ahead of the dequant warps.
-// Rings: packed tiles (kStgP) and stages (kStg) of one token tile and one weight tile,
-// each stage with one full barrier (TMA bytes + an arrive per dequant warp) and one
+//                gate/up SiTU to h rows, down the weighted combine as float4 atomics.
+// Ring: kStg stages of one token tile and one weight tile, each stage with one full barrier (TMA bytes + an arrive per dequant warp) and one
 // empty barrier (the MMA thread's tcgen05.commit).
 // Every wait is bounded by a clock limit; a timeout sets the status word and the
 // roles drop out.
@@ -54,16 +52,14 @@ namespace {
 
 constexpr int kBM = 128, kBK = 64;          // token rows per tile (MMA M), K per stage
 constexpr int kWRows = 256;                 // weight rows per item (MMA N): W1|W3, or two W2 blocks
-constexpr int kStg = 3, kStgP = 4;          // stage ring (token + weight tiles), packed-weight ring
+constexpr int kStg = 4;                     // stage ring (token + weight tiles)
 constexpr int kNumDq = 16;
 constexpr int kWarpProd = 0, kWarpMma = 1, kWarpDq0 = 2, kWarpEpi0 = 2 + kNumDq, kNumEpi = 4;
-constexpr int kWarpPack = kWarpEpi0 + kNumEpi;                 // 22
-constexpr int kGemmThreads = (kWarpPack + 1) * 32;             // 736
+constexpr int kGemmThreads = (kWarpEpi0 + kNumEpi) * 32;       // 704
 constexpr int kTmemCols = 512;
 constexpr int kABytes = kBM * kBK * 2;                          // token tile of a stage
 constexpr int kWBytes = kWRows * kBK * 2;                       // weight tile of a stage
-constexpr int kPBytes = 2 * kTileBytes;                         // two packed 128 x 128 tiles
-constexpr int kGemmSmem = kStg * (kABytes + kWBytes) + kStgP * kPBytes + 2048;
+constexpr int kGemmSmem = kStg * (kABytes + kWBytes) + 2048;
 static_assert(kGemmSmem + 8 * 1024 <= 232448, "shared memory per block (dynamic + static)");
 
 enum { kGU = 0, kDN = 1 };
@@ -315,10 +311,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *smA = sm;                                   // kStg x kABytes: token tiles
     uint8_t *smW = smA + kStg * kABytes;                 // kStg x kWBytes: weight tiles
-    uint8_t *smP = smW + kStg * kWBytes;                 // kStgP x kPBytes: packed weights
     // full[s]: the token tile (TMA bytes, one arrive by the producer) and the weight tile
     // (one arrive per dequant warp); empty[s]: one tcgen05.commit per stage
-    __shared__ uint64_t full_p[kStgP], empty_p[kStgP], full[kStg], empty[kStg], acc_full[2], acc_empty[2], drain;
+    __shared__ uint64_t full[kStg], empty[kStg], acc_full[2], acc_empty[2], drain;
     __shared__ uint32_t tmem_base;
     __shared__ int bail;
     __shared__ int32_t s_prefix[kMaxExperts + kMaxShared + 1];   // item prefix of the units
@@ -331,7 +326,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const int K = k_of<MODE>(a), nks = K / kBK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStgP; s++) { mb_init(&full_p[s], 1); mb_init(&empty_p[s], kNumDq); }
         for (int s = 0; s < kStg; s++) { mb_init(&full[s], 1 + kNumDq); mb_init(&empty[s], 1); }
         for (int b = 0; b < 2; b++) { mb_init(&acc_full[b], 1); mb_init(&acc_empty[b], kNumEpi); }
         mb_init(&drain, 1);
@@ -363,38 +357,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     // the shared stop flag as lane 0 of the warp reads it (keeps loop exits warp-uniform)
     auto stop = [&]() -> bool { return __shfl_sync(0xffffffffu, bail, 0) != 0; };
 
-    if (warp == kWarpPack) {
-        // ------------------------------------------------------------ packed-weight producer
-        uint32_t cp = 0;
-        bool failed = false;
-        for (int i = blockIdx.x; i < n_items && !failed && !stop(); i += gridDim.x) {
-            const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
-            if (it.shared) continue;
-            const uint8_t *ex = a.table + (size_t)it.id * a.expert_bytes;
-            for (int kt = 0; kt < K / kTileK; kt++, cp++) {
-                if (!wait_free_warp(empty_p, kStgP, cp)) { timeout(); failed = true; break; }
-                const int sp = cp % kStgP;
-                uint8_t *dst = smP + sp * kPBytes;
-                if (lane == 0) {
-                    if (MODE == kGU) {          // the W1 and W3 tiles of a block are adjacent
-                        mb_expect_tx(&full_p[sp], (uint32_t)(2 * kTileBytes));
-                        bulk_g2s(dst, ex + ((size_t)it.rb * (a.d / kTileK) + kt) * 2 * kTileBytes,
-                                 2 * kTileBytes, &full_p[sp]);
-                    } else {                    // two row blocks of W2
-                        const int nb = it.nw / kTileRows;
-                        mb_expect_tx(&full_p[sp], (uint32_t)(nb * kTileBytes));
-                        for (int b = 0; b < nb; b++)
-                            bulk_g2s(dst + b * kTileBytes,
-                                     ex + a.gateup_bytes + ((size_t)(2 * it.rb + b) * (a.f / kTileK) + kt) * kTileBytes,
-                                     kTileBytes, &full_p[sp]);
-                    }
-                }
-                __syncwarp();
-            }
-        }
-        if (lane == 0 && bail) drain_fills(full_p, kStgP, cp);
-        __syncwarp();
-    } else if (warp == kWarpProd) {
+    if (warp == kWarpProd) {
         // ------------------------------------------------------------ token tiles (and bf16 weights)
         uint32_t st = 0;
         bool failed = false;
@@ -473,40 +436,87 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
         __syncwarp();
     } else if (warp < kWarpEpi0) {
-        // ------------------------------------------------------------ dequant (packed smem -> f16 weights)
+        // ------------------------------------------------------------ dequant (packed -> f16 weights)
         // Thread t: weight block m (gate/up: W1 / W3; down: first / second W2 block), strip
         // of 16 rows, 32-column group gsel of the stage, rows g and g + 8 of the strip, half
-        // h of their 32 columns: one 16-byte load (a warp reads 512 contiguous bytes),
-        // 2 x 4 eight-byte stores.
+        // h of their 32 columns.  Its bytes of a packed 128 x 128 tile come straight from
+        // global memory (no shared-memory copy): two 16-byte pieces (the tile's even and
+        // odd stage; a warp reads 512 contiguous bytes) and the scale words of its two
+        // rows, loaded one tile ahead; lane 0 of the first dequant warp also prefetches
+        // the tiles three ahead into L2.  Per stage 2 x 4 eight-byte stores.
         const int t = threadIdx.x - kWarpDq0 * 32;             // 0..511
         const int m = t >> 8;
         const int u = t & 255, strip = u >> 5, gsel = (u >> 4) & 1, g = (u >> 1) & 7, h = u & 1;
-        uint32_t st = 0, cp = 0;
-        for (int i = blockIdx.x; i < n_items && !stop(); i += gridDim.x) {
-            const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
-            const bool active = !it.shared && m * kTileRows < it.nw;
-            int bmax = 0;
-            if (active)
-                bmax = (int)*reinterpret_cast<const uint32_t *>(
-                    a.table + (MODE == kGU ? trailer_offset(a.E, a.d, a.f, it.id, m, it.rb)
-                                           : trailer_offset(a.E, a.d, a.f, it.id, 2, 2 * it.rb + m)));
-            for (int ks = 0; ks < nks; ks++, st++) {
-                if (!it.shared && (ks & 1) == 0 && !mb_wait_warp(&full_p[cp % kStgP], (cp / kStgP) & 1u)) {
-                    timeout();
-                    break;
-                }
-                if (!wait_free_warp(empty, kStg, st)) { timeout(); break; }
-                if (active) {
-                    const int c = 2 * (ks & 1) + gsel;
-                    const uint8_t *tile = smP + (cp % kStgP) * kPBytes + m * kTileBytes;
-                    // pieces 2h and 2h+1 of lanes 4g..4g+3: each 4 bytes of row g, then 4 of row g+8
-                    const uint4 q = *reinterpret_cast<const uint4 *>(tile + (strip * 4 + c) * 256 + 32 * g + 16 * h);
+        const int offA = (strip * 4 + gsel) * 256 + 32 * g + 16 * h, offB = offA + 2 * 256;
+        const int offS = kTileNibbleBytes + (strip * 16 + g) * 4;
+        const int nkt = K / kTileK;
+        // a position in this block's sequence of packed tiles: item i, K tile kt
+        struct Cur {
+            int i, kt;
+            GItem it;
+        };
+        auto cur_item = [&](Cur &c, int i) {
+            c.i = i;
+            c.kt = 0;
+            if (i < n_items) c.it = gitem<MODE>(a, s_prefix, n_units, i);
+        };
+        auto cur_next = [&](Cur &c) {
+            if (++c.kt == nkt) cur_item(c, c.i + gridDim.x);
+        };
+        // the packed tile of weight block mb at a position (routed items only)
+        auto tile_at = [&](const Cur &c, int mb) -> const uint8_t * {
+            const uint8_t *ex = a.table + (size_t)c.it.id * a.expert_bytes;
+            if (MODE == kGU) return ex + ((size_t)c.it.rb * nkt + c.kt) * 2 * kTileBytes + (size_t)mb * kTileBytes;
+            return ex + a.gateup_bytes + ((size_t)(2 * c.it.rb + mb) * nkt + c.kt) * kTileBytes;
+        };
+        auto block_on = [&](const Cur &c, int mb) { return c.i < n_items && !c.it.shared && mb * kTileRows < c.it.nw; };
+        auto bmax_at = [&](const Cur &c) -> int {
+            const size_t o = MODE == kGU ? trailer_offset(a.E, a.d, a.f, c.it.id, m, c.it.rb)
+                                         : trailer_offset(a.E, a.d, a.f, c.it.id, 2, 2 * c.it.rb + m);
+            return (int)__ldg(reinterpret_cast<const uint32_t *>(a.table + o));
+        };
+        auto prefetch_l2 = [&](const Cur &c) {
+            if (!block_on(c, 0)) return;
+            if (MODE == kGU) {
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(tile_at(c, 0)), "r"(2 * kTileBytes) : "memory");
+            } else {
+                for (int mb = 0; mb < 2; mb++)
+                    if (block_on(c, mb))
+                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(tile_at(c, mb)), "r"(kTileBytes) : "memory");
+            }
+        };
+        // this thread's bytes of one packed tile, and the tile's block scale maximum
+        struct TileRegs {
+            uint4 qa, qb;
+            uint32_t s0, s1;
+            int bmax;
+        };
+        auto load_tile = [&](const Cur &c, TileRegs &r, int bmax_prev) {
+            r.bmax = bmax_prev;
+            if (!block_on(c, m)) return;
+            const uint8_t *p = tile_at(c, m);
+            r.qa = __ldg(reinterpret_cast<const uint4 *>(p + offA));
+            r.qb = __ldg(reinterpret_cast<const uint4 *>(p + offB));
+            r.s0 = __ldg(reinterpret_cast<const uint32_t *>(p + offS));
+            r.s1 = __ldg(reinterpret_cast<const uint32_t *>(p + offS + 32));
+            if (c.kt == 0) r.bmax = bmax_at(c);
+        };
+        uint32_t st = 0;
+        bool failed = false;
+        // the two stages of the tile at c from registers r
+        auto dequant_tile = [&](const Cur &c, const TileRegs &r) {
+            const bool on = block_on(c, m);
+            for (int ks = c.kt * (kTileK / kBK); ks < (c.kt + 1) * (kTileK / kBK); ks++, st++) {
+                if (!wait_free_warp(empty, kStg, st)) { timeout(); failed = true; return; }
+                if (on) {
+                    const int cc = 2 * (ks & 1) + gsel;
+                    const uint4 q = (ks & 1) ? r.qb : r.qa;
                     uint8_t *Wt = smW + (st % kStg) * kWBytes + m * (kTileRows * kBK * 2);
 #pragma unroll
                     for (int hr = 0; hr < 2; hr++) {            // rows g and g+8 of the strip
-                        const int r = strip * 16 + g + 8 * hr;
-                        const uint32_t b = tile[kTileNibbleBytes + r * 4 + c];
-                        const uint32_t s1 = b == 255u ? 0u : f16_pow2((int)b - bmax + 13);
+                        const int row = strip * 16 + g + 8 * hr;
+                        const uint32_t b = ((hr ? r.s1 : r.s0) >> (8 * cc)) & 0xFFu;
+                        const uint32_t s1 = b == 255u ? 0u : f16_pow2((int)b - r.bmax + 13);
                         const uint32_t s2 = s1 | (s1 << 16);
                         const uint32_t wa = hr ? q.y : q.x, wb = hr ? q.w : q.z;
 #pragma unroll
@@ -514,21 +524,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                             const uint32_t v0 = hmul2(e2m1x2_f16x2(wa >> (8 * j)), s2);
                             const uint32_t v1 = hmul2(e2m1x2_f16x2(wb >> (8 * j)), s2);
                             const int chunk = 4 * gsel + j;
-                            *reinterpret_cast<uint2 *>(Wt + r * 128 + ((chunk ^ (r & 7)) << 4) + 8 * h) =
+                            *reinterpret_cast<uint2 *>(Wt + row * 128 + ((chunk ^ (row & 7)) << 4) + 8 * h) =
                                 make_uint2(v0, v1);
                         }
                     }
                     fence_async_smem();
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    mb_arrive(&full[st % kStg]);
-                    if (!it.shared && (ks & 1)) mb_arrive(&empty_p[cp % kStgP]);
-                }
-                if (!it.shared && (ks & 1)) cp++;
+                if (lane == 0) mb_arrive(&full[st % kStg]);
             }
+        };
+        // tiles in sequence: position p from register set p % 2, loaded two tiles ahead;
+        // the L2 prefetch runs two tiles further
+        Cur c0, c1, tail, pf;
+        cur_item(c0, blockIdx.x);
+        c1 = c0;
+        cur_next(c1);
+        tail = c1;
+        pf = c0;
+        const bool pf_thread = t == 0;
+        if (pf_thread)
+            for (int j = 0; j < 4; j++) { prefetch_l2(pf); cur_next(pf); }
+        TileRegs r0{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), 0, 0, 0}, r1 = r0;
+        load_tile(c0, r0, 0);
+        load_tile(c1, r1, r0.bmax);
+        while (c0.i < n_items && !stop()) {
+            if (pf_thread) { prefetch_l2(pf); cur_next(pf); }
+            dequant_tile(c0, r0);
+            if (failed) break;
+            c0 = tail;
+            cur_next(c0);                                   // position p + 2
+            load_tile(c0, r0, r1.bmax);
+            if (c1.i >= n_items || stop()) break;
+            if (pf_thread) { prefetch_l2(pf); cur_next(pf); }
+            dequant_tile(c1, r1);
+            if (failed) break;
+            c1 = c0;
+            cur_next(c1);                                   // position p + 3
+            load_tile(c1, r1, r0.bmax);
+            tail = c1;
         }
-    } else if (warp < kWarpPack) {
+    } else {
         // ------------------------------------------------------------ epilogue: one token per thread
         const int q = warp & 3;                                 // TMEM lane quadrant
         const int tr = 32 * q + lane;                           // token row of the tile
