@@ -897,15 +897,32 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                     if (__shfl_sync(0xffffffffu, last, 0)) {
                         __threadfence();
                         const size_t plane = rows_all * a.f;
+                        // every part of this lane's four rows is loaded before any is added,
+                        // so the loads are in flight together
                         for (int nn = 0; nn < nvalid; nn++) {
-                            for (int r = lane; r < kItemRows; r += 32) {
-                                const int row = h.rb * kItemRows + r;
-                                float gs = 0.0f, us = 0.0f;
-                                for (int p = 0; p < h.nkp; p++) {
-                                    const float *base = a.gush + ((((size_t)p * a.S + h.id) * a.T + nn) * 2) * a.f;
-                                    gs += __ldcg(base + row);
-                                    us += __ldcg(base + a.f + row);
+                            float gv[kItemRows / 32][kMaxSharedParts], uv[kItemRows / 32][kMaxSharedParts];
+#pragma unroll
+                            for (int q = 0; q < kItemRows / 32; q++)
+#pragma unroll
+                                for (int p = 0; p < kMaxSharedParts; p++) {
+                                    gv[q][p] = uv[q][p] = 0.0f;
+                                    if (p < h.nkp) {
+                                        const float *base = a.gush + ((((size_t)p * a.S + h.id) * a.T + nn) * 2) * a.f;
+                                        const int row = h.rb * kItemRows + 32 * q + lane;
+                                        gv[q][p] = __ldcg(base + row);
+                                        uv[q][p] = __ldcg(base + a.f + row);
+                                    }
                                 }
+#pragma unroll
+                            for (int q = 0; q < kItemRows / 32; q++) {
+                                float gs = 0.0f, us = 0.0f;
+#pragma unroll
+                                for (int p = 0; p < kMaxSharedParts; p++)
+                                    if (p < h.nkp) {
+                                        gs += gv[q][p];
+                                        us += uv[q][p];
+                                    }
+                                const int row = h.rb * kItemRows + 32 * q + lane;
                                 store_h(a, 1, (size_t)pt.row[nn] * a.f + row, plane, situ(gs, us, a.b1, a.b2));
                             }
                         }

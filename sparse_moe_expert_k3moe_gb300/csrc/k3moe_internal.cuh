@@ -115,6 +115,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // would set the kernel's length, so its K range is split into up to 4 parts (the parts'
 // sums are added in order).  ktiles: 128-column tiles of K.  The down projection is not
 // split: measured, its split items cost more than the balance gains.
+constexpr int kMaxSharedParts = 4;
 __host__ __device__ inline int shared_kparts(int ktiles, int T)
 {
     if (T > 16) return 1;
