@@ -22,13 +22,14 @@
 // the 128-row blocks of W1 and W3 for one block of f, down two 128-row blocks of W2)
 // x the whole K.  Warp roles in a block (one block per SM):
 //   warp 0       producer: TMA 2-D loads of the token tiles (64 columns x 128 rows) and,
-//                for bf16 shared experts, of the weight tiles;
+//                for bf16 shared experts, of the weight tiles; also the L2 prefetch of the
+//                packed weight tiles, kL2Ahead tiles ahead;
 //   warp 1       MMA: one thread issues tcgen05.mma (kind::f16, M=128, N=256, K=16) into
 //                fp32 accumulators in tensor memory, two buffers of 256 columns, so one
 //                item's MMAs overlap the previous item's epilogue;
 //   warps 2-17   dequant: packed MXFP4 tiles, loaded from global memory into registers
-//                one tile ahead (and into L2 three tiles ahead), to f16 weight tiles in
-//                shared memory (128-byte swizzle, K-major) -- the E2M1 pair decoded by the hardware
+//                two tiles ahead, to f16 weight tiles in shared memory (128-byte
+//                swizzle, K-major) -- the E2M1 pair decoded by the hardware
 //                conversion, times 2^(b - bmax + 13) where bmax is the largest scale of
 //                the 128-row block (the packed table's trailer), so every value is exact
 //                in f16 while the block's scales span at most 36 binades; the epilogue
@@ -53,6 +54,7 @@ namespace {
 constexpr int kBM = 128, kBK = 64;          // token rows per tile (MMA M), K per stage
 constexpr int kWRows = 256;                 // weight rows per item (MMA N): W1|W3, or two W2 blocks
 constexpr int kStg = 4;                     // stage ring (token + weight tiles)
+constexpr int kL2Ahead = 6;                 // packed tiles prefetched into L2 ahead of the token producer
 constexpr int kNumDq = 16;
 constexpr int kWarpProd = 0, kWarpMma = 1, kWarpDq0 = 2, kWarpEpi0 = 2 + kNumDq, kNumEpi = 4;
 constexpr int kGemmThreads = (kWarpEpi0 + kNumEpi) * 32;       // 704
@@ -357,10 +359,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     // the shared stop flag as lane 0 of the warp reads it (keeps loop exits warp-uniform)
     auto stop = [&]() -> bool { return __shfl_sync(0xffffffffu, bail, 0) != 0; };
 
+    const int nkt = K / kTileK;
+    // a position in this block's sequence of packed tiles: item i, K tile kt
+    struct Cur {
+        int i, kt;
+        GItem it;
+    };
+    auto cur_item = [&](Cur &c, int i) {
+        c.i = i;
+        c.kt = 0;
+        if (i < n_items) c.it = gitem<MODE>(a, s_prefix, n_units, i);
+    };
+    auto cur_next = [&](Cur &c) {
+        if (++c.kt == nkt) cur_item(c, c.i + gridDim.x);
+    };
+    // the packed tile of weight block mb at a position (routed items only)
+    auto tile_at = [&](const Cur &c, int mb) -> const uint8_t * {
+        const uint8_t *ex = a.table + (size_t)c.it.id * a.expert_bytes;
+        if (MODE == kGU) return ex + ((size_t)c.it.rb * nkt + c.kt) * 2 * kTileBytes + (size_t)mb * kTileBytes;
+        return ex + a.gateup_bytes + ((size_t)(2 * c.it.rb + mb) * nkt + c.kt) * kTileBytes;
+    };
+    auto block_on = [&](const Cur &c, int mb) { return c.i < n_items && !c.it.shared && mb * kTileRows < c.it.nw; };
+    auto prefetch_l2 = [&](const Cur &c) {
+        if (!block_on(c, 0)) return;
+        if (MODE == kGU) {
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(tile_at(c, 0)), "r"(2 * kTileBytes) : "memory");
+        } else {
+            for (int mb = 0; mb < 2; mb++)
+                if (block_on(c, mb))
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(tile_at(c, mb)), "r"(kTileBytes) : "memory");
+        }
+    };
     if (warp == kWarpProd) {
         // ------------------------------------------------------------ token tiles (and bf16 weights)
         uint32_t st = 0;
         bool failed = false;
+        // lane 0 also prefetches the packed tiles into L2, kL2Ahead tiles before the
+        // stage it issues (the dequant warps load them into registers two tiles ahead)
+        Cur pf;
+        if (lane == 0) {
+            cur_item(pf, blockIdx.x);
+            for (int j = 0; j < kL2Ahead; j++) { prefetch_l2(pf); cur_next(pf); }
+        }
         for (int i = blockIdx.x; i < n_items && !failed && !stop(); i += gridDim.x) {
             const GItem it = gitem<MODE>(a, s_prefix, n_units, i);
             const CUtensorMap *mt = it.shared ? &mtok_shared : &mtok_routed;
@@ -375,6 +415,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     break;
                 }
                 if (lane == 0) {
+                    if ((ks & 1) == 0) { prefetch_l2(pf); cur_next(pf); }
                     uint64_t *fa = &full[st % kStg];
                     // the bf16 weight tiles of a shared expert come by TMA too
                     mb_expect_tx(fa, (uint32_t)kABytes + (it.shared ? (uint32_t)(nb * kTileRows * kBK * 2) : 0u));
@@ -442,48 +483,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         // h of their 32 columns.  Its bytes of a packed 128 x 128 tile come straight from
         // global memory (no shared-memory copy): two 16-byte pieces (the tile's even and
         // odd stage; a warp reads 512 contiguous bytes) and the scale words of its two
-        // rows, loaded one tile ahead; lane 0 of the first dequant warp also prefetches
-        // the tiles three ahead into L2.  Per stage 2 x 4 eight-byte stores.
+        // rows, loaded two tiles ahead.  Per stage 2 x 4 eight-byte stores.
         const int t = threadIdx.x - kWarpDq0 * 32;             // 0..511
         const int m = t >> 8;
         const int u = t & 255, strip = u >> 5, gsel = (u >> 4) & 1, g = (u >> 1) & 7, h = u & 1;
         const int offA = (strip * 4 + gsel) * 256 + 32 * g + 16 * h, offB = offA + 2 * 256;
         const int offS = kTileNibbleBytes + (strip * 16 + g) * 4;
-        const int nkt = K / kTileK;
-        // a position in this block's sequence of packed tiles: item i, K tile kt
-        struct Cur {
-            int i, kt;
-            GItem it;
-        };
-        auto cur_item = [&](Cur &c, int i) {
-            c.i = i;
-            c.kt = 0;
-            if (i < n_items) c.it = gitem<MODE>(a, s_prefix, n_units, i);
-        };
-        auto cur_next = [&](Cur &c) {
-            if (++c.kt == nkt) cur_item(c, c.i + gridDim.x);
-        };
-        // the packed tile of weight block mb at a position (routed items only)
-        auto tile_at = [&](const Cur &c, int mb) -> const uint8_t * {
-            const uint8_t *ex = a.table + (size_t)c.it.id * a.expert_bytes;
-            if (MODE == kGU) return ex + ((size_t)c.it.rb * nkt + c.kt) * 2 * kTileBytes + (size_t)mb * kTileBytes;
-            return ex + a.gateup_bytes + ((size_t)(2 * c.it.rb + mb) * nkt + c.kt) * kTileBytes;
-        };
-        auto block_on = [&](const Cur &c, int mb) { return c.i < n_items && !c.it.shared && mb * kTileRows < c.it.nw; };
         auto bmax_at = [&](const Cur &c) -> int {
             const size_t o = MODE == kGU ? trailer_offset(a.E, a.d, a.f, c.it.id, m, c.it.rb)
                                          : trailer_offset(a.E, a.d, a.f, c.it.id, 2, 2 * c.it.rb + m);
             return (int)__ldg(reinterpret_cast<const uint32_t *>(a.table + o));
-        };
-        auto prefetch_l2 = [&](const Cur &c) {
-            if (!block_on(c, 0)) return;
-            if (MODE == kGU) {
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(tile_at(c, 0)), "r"(2 * kTileBytes) : "memory");
-            } else {
-                for (int mb = 0; mb < 2; mb++)
-                    if (block_on(c, mb))
-                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(tile_at(c, mb)), "r"(kTileBytes) : "memory");
-            }
         };
         // this thread's bytes of one packed tile, and the tile's block scale maximum
         struct TileRegs {
@@ -534,29 +543,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 if (lane == 0) mb_arrive(&full[st % kStg]);
             }
         };
-        // tiles in sequence: position p from register set p % 2, loaded two tiles ahead;
-        // the L2 prefetch runs two tiles further
-        Cur c0, c1, tail, pf;
+        // tiles in sequence: position p from register set p % 2, loaded two tiles ahead
+        Cur c0, c1, tail;
         cur_item(c0, blockIdx.x);
         c1 = c0;
         cur_next(c1);
         tail = c1;
-        pf = c0;
-        const bool pf_thread = t == 0;
-        if (pf_thread)
-            for (int j = 0; j < 4; j++) { prefetch_l2(pf); cur_next(pf); }
         TileRegs r0{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), 0, 0, 0}, r1 = r0;
         load_tile(c0, r0, 0);
         load_tile(c1, r1, r0.bmax);
         while (c0.i < n_items && !stop()) {
-            if (pf_thread) { prefetch_l2(pf); cur_next(pf); }
             dequant_tile(c0, r0);
             if (failed) break;
             c0 = tail;
             cur_next(c0);                                   // position p + 2
             load_tile(c0, r0, r1.bmax);
             if (c1.i >= n_items || stop()) break;
-            if (pf_thread) { prefetch_l2(pf); cur_next(pf); }
             dequant_tile(c1, r1);
             if (failed) break;
             c1 = c0;
