@@ -513,35 +513,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         uint32_t st = 0;
         bool failed = false;
         // the two stages of the tile at c from registers r
+        // both stages of the tile at c from registers r: the two slots are claimed, both
+        // stages written, then one proxy fence and both arrivals
         auto dequant_tile = [&](const Cur &c, const TileRegs &r) {
             const bool on = block_on(c, m);
-            for (int ks = c.kt * (kTileK / kBK); ks < (c.kt + 1) * (kTileK / kBK); ks++, st++) {
-                if (!wait_free_warp(empty, kStg, st)) { timeout(); failed = true; return; }
-                if (on) {
-                    const int cc = 2 * (ks & 1) + gsel;
-                    const uint4 q = (ks & 1) ? r.qb : r.qa;
-                    uint8_t *Wt = smW + (st % kStg) * kWBytes + m * (kTileRows * kBK * 2);
+            constexpr int kSpt = kTileK / kBK;                  // stages per tile
+#pragma unroll
+            for (int s2 = 0; s2 < kSpt; s2++)
+                if (!wait_free_warp(empty, kStg, st + s2)) { timeout(); failed = true; return; }
+            if (on) {
+#pragma unroll
+                for (int s2 = 0; s2 < kSpt; s2++) {
+                    const int cc = 2 * s2 + gsel;
+                    const uint4 q = s2 ? r.qb : r.qa;
+                    uint8_t *Wt = smW + ((st + s2) % kStg) * kWBytes + m * (kTileRows * kBK * 2);
 #pragma unroll
                     for (int hr = 0; hr < 2; hr++) {            // rows g and g+8 of the strip
                         const int row = strip * 16 + g + 8 * hr;
                         const uint32_t b = ((hr ? r.s1 : r.s0) >> (8 * cc)) & 0xFFu;
                         const uint32_t s1 = b == 255u ? 0u : f16_pow2((int)b - r.bmax + 13);
-                        const uint32_t s2 = s1 | (s1 << 16);
+                        const uint32_t sc2 = s1 | (s1 << 16);
                         const uint32_t wa = hr ? q.y : q.x, wb = hr ? q.w : q.z;
 #pragma unroll
                         for (int j = 0; j < 4; j++) {           // columns 8j + 4h .. +3 of the group
-                            const uint32_t v0 = hmul2(e2m1x2_f16x2(wa >> (8 * j)), s2);
-                            const uint32_t v1 = hmul2(e2m1x2_f16x2(wb >> (8 * j)), s2);
+                            const uint32_t v0 = hmul2(e2m1x2_f16x2(wa >> (8 * j)), sc2);
+                            const uint32_t v1 = hmul2(e2m1x2_f16x2(wb >> (8 * j)), sc2);
                             const int chunk = 4 * gsel + j;
                             *reinterpret_cast<uint2 *>(Wt + row * 128 + ((chunk ^ (row & 7)) << 4) + 8 * h) =
                                 make_uint2(v0, v1);
                         }
                     }
-                    fence_async_smem();
                 }
-                __syncwarp();
-                if (lane == 0) mb_arrive(&full[st % kStg]);
+                fence_async_smem();
             }
+            __syncwarp();
+            if (lane == 0)
+#pragma unroll
+                for (int s2 = 0; s2 < kSpt; s2++) mb_arrive(&full[(st + s2) % kStg]);
+            st += kSpt;
         };
         // tiles in sequence: position p from register set p % 2, loaded two tiles ahead
         Cur c0, c1, tail;
