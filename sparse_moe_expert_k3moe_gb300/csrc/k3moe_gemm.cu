@@ -514,13 +514,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         bool failed = false;
         // the two stages of the tile at c from registers r
         // both stages of the tile at c from registers r: the two slots are claimed, both
-        // stages written, then one proxy fence and both arrivals
+        // stages written, then one proxy fence and both arrivals.  A slot is free once the
+        // MMAs that read it have completed, and they complete in issue order, so the
+        // later slot's release covers the earlier one: one wait per tile.
         auto dequant_tile = [&](const Cur &c, const TileRegs &r) {
             const bool on = block_on(c, m);
             constexpr int kSpt = kTileK / kBK;                  // stages per tile
-#pragma unroll
-            for (int s2 = 0; s2 < kSpt; s2++)
-                if (!wait_free_warp(empty, kStg, st + s2)) { timeout(); failed = true; return; }
+            if (!wait_free_warp(empty, kStg, st + kSpt - 1)) { timeout(); failed = true; return; }
             if (on) {
 #pragma unroll
                 for (int s2 = 0; s2 < kSpt; s2++) {
