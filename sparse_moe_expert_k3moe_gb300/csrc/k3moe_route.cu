@@ -4,7 +4,7 @@
 // Kernels, in launch order:
 //   router_scores  logits = x . Wr^T (fp32 accumulation of exact bf16 products),
 //                  sc = 1/(1+expf(-logit)), ch = sc + bias, both float, to the workspace.
-//                  A block owns 8 experts (one per warp, its Wr row held in registers)
+//                  A block owns 4 experts (one per warp, its Wr row held in registers)
 //                  and walks the tokens 8 at a time through shared memory;
 //   router_topk    one block per token: warp-level bitonic sorts and merges of the E keys
 //                  (ch, then the lower index first) pick the top k in rank order; the
@@ -22,7 +22,7 @@
 namespace k3moe {
 namespace {
 
-constexpr int kScoreWarps = 8;       // experts per block (one per warp)
+constexpr int kScoreWarps = 4;       // experts per block (one per warp)
 constexpr int kScoreTok = 8;         // tokens staged per round
 constexpr int kScoreChunks = 16;     // 16-byte Wr chunks per lane held at once (4096 columns)
 
