@@ -9,7 +9,8 @@
 //                perm (slot -> position), picks each token's activation scale 2^-u and
 //                writes x * 2^-u as f16; sets the abort flag on bad input;
 //   gemv_gateup  for every (active expert, token) and (shared expert, token): g = W1 x,
-//                u = W3 x, h = SiTU(g, u), stored as a hi + lo pair;
+//                u = W3 x, h = SiTU(g, u), stored as f16 (routed) or a bf16 hi + lo
+//                pair (shared);
 //   gemv_down    y = W2 h, fp32, one row per (slot or shared expert, token);
 //   fwd_combine  out[t] = sum_j w[t][j] y[pos(t,j)] + sum_s y_shared[s][t], terms added
 //                in a fixed order.
@@ -22,8 +23,8 @@
 // the group's E8M0 scale multiplies the fp32 group result.  Activations enter f16 with a
 // per-token power-of-two scale that puts the token's largest magnitude in [2^14, 2^15):
 // every bf16 element within 2^31 of that maximum converts exactly.  The SiTU output
-// enters the down projection as an f16 pair hi + lo (about 22 significant bits).  The
-// bf16 shared experts use bf16 MMAs on tensor-map (TMA) tiles, with h as a bf16 pair.
+// enters the routed down projection as f16 (as on the tensor-core path).  The bf16
+// shared experts use bf16 MMAs on tensor-map (TMA) tiles, with h as a bf16 hi + lo pair.
 //
 // Streaming: a persistent grid, two blocks per SM; work items (128 weight rows of one
 // unit over the whole K) are handed out heaviest first through an atomic counter.  In
@@ -521,7 +522,9 @@ __device__ __forceinline__ void issue_b_chunk(const GemvArgs &a, const Unit &un,
     const int cols = min(CT * kTileK, Kp - c0);
     const uint32_t row_bytes = (uint32_t)cols * 2;
     const int k0 = it.kp * Kp + c0;
-    if (lane == 0) mbar_expect_tx(bar, (uint32_t)nvalid * row_bytes * (MODE == kDown ? 2u : 1u));
+    // down: a shared expert's h is a bf16 hi + lo pair; a routed expert's is one f16 plane
+    const bool two = MODE == kDown && un.shared;
+    if (lane == 0) mbar_expect_tx(bar, (uint32_t)nvalid * row_bytes * (two ? 2u : 1u));
     __syncwarp();
     if (lane < nvalid) {
         if (MODE == kGateUp) {
@@ -531,7 +534,7 @@ __device__ __forceinline__ void issue_b_chunk(const GemvArgs &a, const Unit &un,
             const size_t plane = ((size_t)a.T * a.k + (size_t)a.S * a.T) * a.f;
             const uint16_t *src = a.hp + (size_t)row * a.f + k0;
             bulk_g2s(bhi + lane * RS, src, row_bytes, bar);
-            bulk_g2s(blo + lane * RS, src + plane, row_bytes, bar);
+            if (two) bulk_g2s(blo + lane * RS, src + plane, row_bytes, bar);
         }
     }
 }
@@ -587,12 +590,6 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf0, int shared, i
                 float t1[4];
                 mma_f16(t1, A0, bb[0], bb[1], zero);
                 mma_f16(t1, A1, bb[2], bb[3], t1);
-                if (MODE == kDown) {
-                    uint32_t ll[4];
-                    ldb2(ll, blo, RS, brows, nb, ks0 + 2 * c, lane);
-                    mma_f16(t1, A0, ll[0], ll[1], t1);
-                    mma_f16(t1, A1, ll[2], ll[3], t1);
-                }
                 acc1[nb][0] = fmaf(f1[c], t1[0], acc1[nb][0]);
                 acc1[nb][1] = fmaf(f1[c], t1[1], acc1[nb][1]);
                 acc1[nb][2] = fmaf(f1b[c], t1[2], acc1[nb][2]);
@@ -647,23 +644,20 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf0, int shared, i
     }
 }
 
-// h as a hi + lo pair of 16-bit values (f16 for routed experts, bf16 for shared ones).
+// h of a routed expert as f16 (11 significant bits: the down projection's relative
+// error from it is about 1e-4); of a shared expert as a bf16 hi + lo pair, since its
+// down projection runs on bf16 MMAs.
 __device__ __forceinline__ void store_h(const GemvArgs &a, int shared, size_t at, size_t plane, float hv)
 {
-    uint16_t hi, lo;
     if (shared) {
         const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
         const __nv_bfloat16 lb = __float2bfloat16_rn(hv - __bfloat162float(hb));
-        hi = *reinterpret_cast<const uint16_t *>(&hb);
-        lo = *reinterpret_cast<const uint16_t *>(&lb);
+        a.hp[at] = *reinterpret_cast<const uint16_t *>(&hb);
+        a.hp[plane + at] = *reinterpret_cast<const uint16_t *>(&lb);
     } else {
         const __half hh = __float2half_rn(hv);
-        const __half lh = __float2half_rn(hv - __half2float(hh));
-        hi = *reinterpret_cast<const uint16_t *>(&hh);
-        lo = *reinterpret_cast<const uint16_t *>(&lh);
+        a.hp[at] = *reinterpret_cast<const uint16_t *>(&hh);
     }
-    a.hp[at] = hi;
-    a.hp[plane + at] = lo;
 }
 
 // Bounded wait by every lane of a warp; the same result on every lane.
