@@ -449,21 +449,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             if (n >= 2 && !mb_wait_warp(&acc_empty[buf], ((n >> 1) - 1) & 1u)) { timeout(); break; }
             tc_fence_after();
             const uint32_t d0 = tmem + (uint32_t)buf * 256u;
-            for (int ks = 0; ks < nks; ks++, st++) {
-                if (!mb_wait_warp(&full[st % kStg], (st / kStg) & 1u)) {
+            // the two stages of a packed tile at a time (their weight halves are written
+            // together): both waits first, so the second stage's MMAs queue right behind
+            // the first's
+            for (int ks = 0; ks < nks; ks += 2, st += 2) {
+                if (!mb_wait_warp(&full[st % kStg], (st / kStg) & 1u) ||
+                    !mb_wait_warp(&full[(st + 1) % kStg], ((st + 1) / kStg) & 1u)) {
                     timeout();
                     failed = true;
                     break;
                 }
                 if (lane == 0) {
-                    // descriptors of the stage's first K slice; each further slice of 16 is
-                    // 32 bytes on, i.e. 2 in the descriptor's start-address field
-                    const uint64_t dA = sdesc(saddr(smA + (st % kStg) * kABytes));
-                    const uint64_t dW = sdesc(saddr(smW + (st % kStg) * kWBytes));
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; kk++)
-                        umma(d0, dA + 2 * kk, dW + 2 * kk, id, (ks | kk) != 0);
-                    umma_commit(&empty[st % kStg]);
+                    for (int s2 = 0; s2 < 2; s2++) {
+                        const uint32_t ss = st + s2;
+                        // descriptors of the stage's first K slice; each further slice of
+                        // 16 is 32 bytes on, i.e. 2 in the descriptor's start-address field
+                        const uint64_t dA = sdesc(saddr(smA + (ss % kStg) * kABytes));
+                        const uint64_t dW = sdesc(saddr(smW + (ss % kStg) * kWBytes));
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; kk++)
+                            umma(d0, dA + 2 * kk, dW + 2 * kk, id, ((ks + s2) | kk) != 0);
+                        umma_commit(&empty[ss % kStg]);
+                    }
                 }
                 __syncwarp();
             }
