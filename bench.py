@@ -108,19 +108,21 @@ def kernel_work(name: str, w, distinct_experts: int):
     router_scores(_tc): Wr and x in, sc and ch out (f32); 2*T*E*d FLOPs.
     gemv_gateup / gemm_gateup: W1, W3 of the distinct routed experts (packed MXFP4,
     17/32 byte per weight) and of the shared experts (bf16), the activations in (x;
-    the gathered f16 copy on the GEMM path) and h out; 2 * rows * 2*f*d FLOPs with
+    the gathered f16 copy on the GEMM path) and h out (f16 for routed rows; on the
+    mat-vec path a bf16 hi + lo pair for shared rows); 2 * rows * 2*f*d FLOPs with
     rows = T*k + S*T.  gemv_down / gemm_down: W2 likewise, h in, the output out.
     Any other kernel is charged the whole layer's bytes and no FLOPs."""
     rows = w.T * w.k + w.S * w.T
     slots = w.T * w.k
+    h_gemv = slots * w.f * 2 + w.S * w.T * w.f * 4
     if name in ("router_scores", "router_scores_tc"):
         return w.E * w.d * 2 + w.T * w.d * 2 + 2 * w.T * w.E * 4, 2 * w.T * w.E * w.d
     if name == "gemv_gateup":
         return (distinct_experts * 2 * w.f * w.d * 17 // 32 + w.S * 2 * w.f * w.d * 2
-                + w.T * w.d * 2 + rows * w.f * 4), 2 * rows * 2 * w.f * w.d
+                + w.T * w.d * 2 + h_gemv), 2 * rows * 2 * w.f * w.d
     if name == "gemv_down":
         return (distinct_experts * w.d * w.f * 17 // 32 + w.S * w.d * w.f * 2
-                + rows * w.f * 4 + rows * w.d * 4), 2 * rows * w.f * w.d
+                + h_gemv + rows * w.d * 4), 2 * rows * w.f * w.d
     if name == "gemm_gateup":
         return (distinct_experts * 2 * w.f * w.d * 17 // 32 + w.S * 2 * w.f * w.d * 2
                 + slots * w.d * 2 + w.T * w.d * 2 + rows * w.f * 2), 2 * rows * 2 * w.f * w.d
