@@ -263,11 +263,26 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
         }
         return;
     }
+    // with up to kPrepSlots slots, idx and perm are read into shared memory together with
+    // offsets (one round of loads) and the inverse permutation is built there
+    constexpr int kPrepSlots = 2048;
+    __shared__ int32_t sidx[kPrepSlots], sperm[kPrepSlots], sinv[kPrepSlots];
+    const bool small = slots <= kPrepSlots;
     if (tid == 0) bad = 0;
     for (int e = tid; e <= E; e += blockDim.x) off[e] = a.offsets[e];
-    for (int s = tid; s < slots; s += blockDim.x) a.inv[s] = -1;
+    if (small) {
+        for (int s = tid; s < slots; s += blockDim.x) {
+            sidx[s] = a.idx[s];
+            sperm[s] = a.perm[s];
+            sinv[s] = -1;
+        }
+    } else {
+        for (int s = tid; s < slots; s += blockDim.x) a.inv[s] = -1;
+    }
     for (int i = tid; i < a.n_shctr; i += blockDim.x) a.shctr[i] = 0;
     __syncthreads();
+    const int32_t *pidx = small ? sidx : a.idx, *pperm = small ? sperm : a.perm;
+    int32_t *pinv = small ? sinv : a.inv;
     // offsets: monotone, start 0, end T*k; idx in range
     for (int e = tid; e < E; e += blockDim.x) {
         const int lo = off[e], hi = off[e + 1];
@@ -275,7 +290,7 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
     }
     if (tid == 0 && (off[0] != 0 || off[E] != slots)) atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
     for (int s = tid; s < slots; s += blockDim.x) {
-        const int e = a.idx[s];
+        const int e = pidx[s];
         if (e < 0 || e >= E) atomicOr(&bad, K3MOE_DEV_BAD_INDEX);
     }
     __syncthreads();
@@ -300,7 +315,7 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
     // perm: a permutation of the slots, each in the segment of its expert
     if (offsets_ok) {
         for (int p = tid; p < slots; p += blockDim.x) {
-            const int s = a.perm[p];
+            const int s = pperm[p];
             if (s < 0 || s >= slots) {
                 atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
                 continue;
@@ -310,11 +325,13 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
                 const int mid = (lo + hi) >> 1;
                 if (off[mid] <= p) lo = mid; else hi = mid;
             }
-            if (a.idx[s] != lo) atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
-            if (atomicExch(&a.inv[s], p) != -1) atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
+            if (pidx[s] != lo) atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
+            if (atomicExch(&pinv[s], p) != -1) atomicOr(&bad, K3MOE_DEV_BAD_OFFSETS);
         }
     }
     __syncthreads();
+    if (small)
+        for (int s = tid; s < slots; s += blockDim.x) a.inv[s] = sinv[s];
     if (tid == 0) {
         if (bad) atomicOr(a.status, bad);
         *a.abort = bad ? 1 : 0;

@@ -298,11 +298,27 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
             w = w * a.routed_scale;
             a.idx[(size_t)t * k + i] = e;
             a.weight[(size_t)t * k + i] = w;
+            slot_e[i] = e;
         }
     }
     if (a.done == nullptr) return;                 // the map is built by perm_count
     if (gridDim.x == 1) {                          // one token: its block builds the map
         __syncthreads();
+        if (a.T == 1) {
+            // its k experts are distinct, one slot each: offsets[e] counts the chosen
+            // experts below e, and a slot's position in perm is the rank of its expert
+            for (int ee = i; ee <= E; ee += blockDim.x) {
+                int below = 0;
+                for (int j = 0; j < k; j++) below += slot_e[j] < ee ? 1 : 0;
+                a.map.offsets[ee] = below;
+            }
+            if (i < k) {
+                int rank = 0;
+                for (int j = 0; j < k; j++) rank += slot_e[j] < slot_e[i] ? 1 : 0;
+                a.map.perm[rank] = i;
+            }
+            return;
+        }
         map_chunk(a.map, 0, true, cnt, slot_e, scan_tmp);
         return;
     }
