@@ -110,15 +110,17 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// K parts of a shared-expert gate/up work item on the decode path.  With one token pass
-// (T <= 16) a bf16 shared item carries four times the bytes of a packed routed one and
-// would set the kernel's length, so its K range is split into up to 4 parts (the parts'
-// sums are added in order).  ktiles: 128-column tiles of K.  The down projection is not
-// split: measured, its split items cost more than the balance gains.
+// K parts of a shared-expert gate/up work item on the decode path.  A bf16 shared item
+// carries four times the bytes of a packed routed one; with a single token (16 routed
+// experts) it would set the kernel's length, so its K range is split into up to 4 parts
+// (the parts' sums are added in order).  From two tokens on the routed items outnumber
+// the blocks enough to absorb whole shared items, and the split costs more than it
+// balances (measured at T = 2..16).  ktiles: 128-column tiles of K.  The down
+// projection is not split: measured, its split items cost more than the balance gains.
 constexpr int kMaxSharedParts = 4;
 __host__ __device__ inline int shared_kparts(int ktiles, int T)
 {
-    if (T > 16) return 1;
+    if (T > 1) return 1;
     return ktiles % 4 == 0 ? 4 : (ktiles % 2 == 0 ? 2 : 1);
 }
 

@@ -181,6 +181,8 @@ SMALL_CASES = [
     MICRO.with_(name="micro_no_renorm", renorm=0, routed_scale=0.75, seed=44),
     MICRO.with_(name="micro_no_shared", S=0, seed=45, T=130),             # ragged third chunk
     MICRO.with_(name="micro_wide", d=1024, f=640, E=40, k=16, S=1, seed=46, T=23),
+    # one token: the shared gate/up items are cut into K parts (d = 512: 4 tiles of K)
+    MICRO.with_(name="micro_t1_split", d=512, f=256, E=32, k=4, S=2, seed=47, T=1),
 ]
 
 
