@@ -27,7 +27,7 @@
 // shared experts use bf16 MMAs on tensor-map (TMA) tiles, with h as a bf16 hi + lo pair.
 //
 // Streaming: a persistent grid, two blocks per SM; work items (128 weight rows of one
-// unit over the whole K) are handed out heaviest first through an atomic counter.  In
+// unit over the whole K) are handed out longest first through an atomic counter.  In
 // each block one producer warp moves everything by bulk async copies and never waits for
 // data: the weight stages (a packed W1+W3 tile pair for gate/up, two consecutive packed
 // W2 tiles for down, or a bf16 tile through a tensor map) through a 4-stage mbarrier
