@@ -93,7 +93,8 @@ k3moe_status k3moe_validate_config(const k3moe_config *cfg);
  * 3 * f * d * 17/32 bytes of codes and scales (half a byte per weight plus one
  * scale byte per 32: 17,547,264 bytes at the K3 shape, kimi-k3-in-c README,
  * Part II, "The problem: a model that does not fit"), plus a 1024-byte summary
- * of the largest scale of every 128-row block.  0 for an invalid config. */
+ * of the largest scale of every 128-row block and a flag for scale bytes 0 and
+ * 255 in the expert.  0 for an invalid config. */
 size_t k3moe_packed_bytes(const k3moe_config *cfg);
 
 /* Workspace bytes that k3moe_route and k3moe_forward need for any

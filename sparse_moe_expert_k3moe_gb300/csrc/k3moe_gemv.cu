@@ -20,7 +20,9 @@
 // 16x16 MXFP4 sub-tile is decoded with the hardware e2m1x2 -> f16x2 conversion (exact;
 // the table layout hands every lane its fragment bytes in one 8-byte load), multiplied
 // against the activations in f16 and accumulated in fp32, one 32-column group at a time;
-// the group's E8M0 scale multiplies the fp32 group result.  Activations enter f16 with a
+// the group's E8M0 scale multiplies the fp32 group result (converted by the hardware
+// ue8m0 conversion, or exactly for the rare expert whose table flags a scale byte 0 or
+// 255).  Activations enter f16 with a
 // per-token power-of-two scale that puts the token's largest magnitude in [2^14, 2^15):
 // every bf16 element within 2^31 of that maximum converts exactly.  The SiTU output
 // enters the routed down projection as f16 (as on the tensor-core path).  The bf16
@@ -169,11 +171,13 @@ __device__ __forceinline__ float situ(float g, float u, float b1, float b2)
 }
 
 // The four E8M0 scales of one row (one byte per group) as floats: the hardware
-// ue8m0x2 -> bf16x2 conversion gives 2^(b-127) exactly; bf16 -> f32 is a shift.  Bytes
-// 0 (a subnormal) and 255 (read as zero) take the slow path.
+// ue8m0x2 -> bf16x2 conversion gives 2^(b-127) exactly for bytes 1..254; bf16 -> f32 is
+// a shift.  Bytes 0 (a subnormal) and 255 (read as zero) need the exact path, which
+// EXACT selects for experts whose table flags such a byte.
+template <bool EXACT>
 __device__ __forceinline__ void row_scales(uint32_t s4, float (&f)[4])
 {
-    const bool special = (__vcmpeq4(s4, 0u) | __vcmpeq4(s4, 0xFFFFFFFFu)) != 0u;
+    const bool special = EXACT && (__vcmpeq4(s4, 0u) | __vcmpeq4(s4, 0xFFFFFFFFu)) != 0u;
     if (!special) {
         uint32_t lo, hi;
         asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
@@ -531,7 +535,7 @@ struct PassTok {
 template <int MODE>
 __device__ __forceinline__ void issue_b_chunk(const GemvArgs &a, const Unit &un, const Item &it, int chunk,
                                               int nvalid, int tok, long long row, uint8_t *bhi, uint8_t *blo,
-                                              uint64_t *bar, int lane)
+                                              int32_t *flag, uint64_t *bar, int lane)
 {
     const int Kp = Geo<MODE>::K(a) / it.nkp, CT = Geo<MODE>::chunk_tiles(a);   // this item's K range
     const int RS = Geo<MODE>::b_row_bytes(a);
@@ -541,8 +545,13 @@ __device__ __forceinline__ void issue_b_chunk(const GemvArgs &a, const Unit &un,
     const int k0 = it.kp * Kp + c0;
     // down: a shared expert's h is a bf16 hi + lo pair; a routed expert's is one f16 plane
     const bool two = MODE == kDown && un.shared;
-    if (lane == 0) mbar_expect_tx(bar, (uint32_t)nvalid * row_bytes * (two ? 2u : 1u));
+    // a routed expert's chunk also brings the last 16 trailer bytes, whose last word flags
+    // scale bytes 0 and 255 in the expert (flag[3])
+    const uint32_t fbytes = un.shared ? 0u : 16u;
+    if (lane == 0) mbar_expect_tx(bar, (uint32_t)nvalid * row_bytes * (two ? 2u : 1u) + fbytes);
     __syncwarp();
+    if (lane == 31 && fbytes)
+        bulk_g2s(flag, a.table + special_flag_offset(a.E, a.d, a.f, un.id) - 12, fbytes, bar);
     if (lane < nvalid) {
         if (MODE == kGateUp) {
             const uint16_t *src = (un.shared ? a.x : a.xs) + (size_t)tok * a.d + k0;
@@ -569,7 +578,7 @@ __device__ __forceinline__ void ldb2(uint32_t (&r)[4], const uint8_t *b, int RS,
     ldmatrix_x4(r, b + row * RS + (16 * ks + 8 * m) * 2);
 }
 
-template <int MODE, int NB, int TPS>
+template <int MODE, int NB, int TPS, bool EXACT>
 __device__ __forceinline__ void consume_stage(const uint8_t *buf0, int shared, int st, int RS, int brows,
                                               const uint8_t *bhi, const uint8_t *blo,
                                               float (&acc1)[kNBMax][4], float (&acc3)[kNBMax][4])
@@ -582,11 +591,11 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf0, int shared, i
         const uint8_t *buf = buf0 + tt * kTileBytes;
         const int ks0 = (st * TPS + tt) * 8;                  // 8 k-steps per 128-column tile
         float f1[4], f1b[4], f3[4], f3b[4];
-        row_scales(*reinterpret_cast<const uint32_t *>(buf + kTileNibbleBytes + (16 * w + g) * 4), f1);
-        row_scales(*reinterpret_cast<const uint32_t *>(buf + kTileNibbleBytes + (16 * w + g + 8) * 4), f1b);
+        row_scales<EXACT>(*reinterpret_cast<const uint32_t *>(buf + kTileNibbleBytes + (16 * w + g) * 4), f1);
+        row_scales<EXACT>(*reinterpret_cast<const uint32_t *>(buf + kTileNibbleBytes + (16 * w + g + 8) * 4), f1b);
         if (MODE == kGateUp) {
-            row_scales(*reinterpret_cast<const uint32_t *>(buf + kTileBytes + kTileNibbleBytes + (16 * w + g) * 4), f3);
-            row_scales(*reinterpret_cast<const uint32_t *>(buf + kTileBytes + kTileNibbleBytes + (16 * w + g + 8) * 4), f3b);
+            row_scales<EXACT>(*reinterpret_cast<const uint32_t *>(buf + kTileBytes + kTileNibbleBytes + (16 * w + g) * 4), f3);
+            row_scales<EXACT>(*reinterpret_cast<const uint32_t *>(buf + kTileBytes + kTileNibbleBytes + (16 * w + g + 8) * 4), f3b);
         }
 #pragma unroll
         for (int c = 0; c < 4; c++) {
@@ -623,7 +632,7 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf0, int shared, i
             }
         }
       }
-    } else {
+    } else if (!EXACT) {                                      // (shared units never take EXACT)
         // bf16 tile: 128 rows x 64 columns, 128-byte swizzle (chunk q of row r at
         // r*128 + ((q ^ (r&7))*16)); gate/up stages alternate W1 (even) and W3 (odd)
         const int mats = Geo<MODE>::kSharedMats;
@@ -711,6 +720,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
     __shared__ int issued[kStages], bissued[kBSlots];
     __shared__ PassTok pts[kBSlots];
     __shared__ BHdr bh[kBSlots];
+    __shared__ __align__(16) int32_t bflag[kBSlots][4];
     __shared__ int bail;
 
     if (*a.abort) return;
@@ -792,7 +802,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                         if (lane == 0) bh[b] = BHdr{i, pass, nvalid, un.shared, un.id, it.rb, it.kp, it.nkp};
                         __syncwarp();
                         issue_b_chunk<MODE>(a, un, it, st / spc, nvalid, tok, row, bbase + kHalves * b * bbytes,
-                                            bbase + (kHalves * b + kHalves - 1) * bbytes, &bfull[b], lane);
+                                            bbase + (kHalves * b + kHalves - 1) * bbytes, bflag[b], &bfull[b], lane);
                         if (lane == 0) bissued[b]++;
                         bu++;
                     }
@@ -851,10 +861,16 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                     for (int i = 0; i < 4; i++) acc1[nb][i] = acc3[nb][i] = 0.0f;
             }
             const uint8_t *buf = bufs + slot * kStageBytes;
-            if (h.nvalid > 8)
-                consume_stage<MODE, 2, TPS>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
-            else
-                consume_stage<MODE, 1, TPS>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
+            if (!h.shared && bflag[b][3] != 0) {
+                if (h.nvalid > 8)
+                    consume_stage<MODE, 2, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, acc1, acc3);
+                else
+                    consume_stage<MODE, 1, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, acc1, acc3);
+            } else if (h.nvalid > 8) {
+                consume_stage<MODE, 2, TPS, false>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
+            } else {
+                consume_stage<MODE, 1, TPS, false>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
             const bool chunk_end = (sicf >> 16) & 1;

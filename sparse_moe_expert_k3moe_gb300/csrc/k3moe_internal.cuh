@@ -19,7 +19,10 @@
 //   (both matrices) is one 17408-byte copy.  Bytes per expert = 3*f*d*17/32.
 // After the E expert payloads comes a trailer of kTrailerBytes per expert: for each
 // matrix (W1, W3, W2) and each 128-row block, the largest E8M0 byte of the block other
-// than 255, as a uint32 (the tensor-core path scales the block's weights by it).
+// than 255, as a uint32 (the tensor-core path scales the block's weights by it); and in
+// the trailer's last word a flag, nonzero when any scale byte of the expert is 0 (the
+// subnormal 2^-127) or 255 (read as zero), the two bytes the fast conversion of the
+// decode path does not give exactly.
 #pragma once
 
 #include <cstddef>
@@ -70,6 +73,14 @@ __host__ __device__ inline size_t trailer_offset(int E, int d, int f, int e, int
     const int idx = (m < 2) ? m * nrb_f + rb : 2 * nrb_f + rb;
     return (size_t)E * expert_bytes(d, f) + (size_t)e * kTrailerBytes + (size_t)idx * 4;
 }
+
+// Trailer word of expert e that flags scale bytes 0 and 255 anywhere in the expert.
+__host__ __device__ inline size_t special_flag_offset(int E, int d, int f, int e)
+{
+    return (size_t)E * expert_bytes(d, f) + (size_t)e * kTrailerBytes + kTrailerBytes - 4;
+}
+static_assert(3 * (kMaxWidth / kTileRows) * 4 <= kTrailerBytes - 4,
+              "the block maxima and the flag word share the trailer");
 
 // Device status word and abort flag live in the first 256 bytes of the workspace.
 struct StatusBlock {

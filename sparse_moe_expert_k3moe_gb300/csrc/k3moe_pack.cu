@@ -78,6 +78,9 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
         for (int t = 0; t < 4; t++)
             *reinterpret_cast<uint32_t *>(dst + dn + (size_t)t * 8) = lane_word(v, t);
         dst[ds] = sb;
+        if (sb == 0 || sb == 255)
+            atomicOr(reinterpret_cast<unsigned int *>(
+                         a.table + special_flag_offset(a.E, a.d, a.f, a.expert_lo + e)), 1u);
         if (sb == 255) {
             if (a.status) set_status(a.status, K3MOE_DEV_NAN_SCALE);
         } else {

@@ -132,12 +132,13 @@ def test_pack_roundtrip_every_code_and_scale(k3):
 
 def test_pack_records_block_scale_maxima(k3):
     """The table's trailer: per expert, matrix and 128-row block, the largest scale byte
-    other than 255."""
-    w = ki.Workload("trail", T=1, d=256, f=256, E=2, k=1, S=0, exp_lo=-9, exp_hi=-1, seed=9)
+    other than 255; and in its last word a flag for a scale byte 0 or 255 in the expert."""
+    w = ki.Workload("trail", T=1, d=256, f=256, E=4, k=1, S=0, exp_lo=-9, exp_hi=-1, seed=9)
     cfg = k3.k3moe_config(**w.config_kwargs())
     blk = ki.make_experts_block(w, 0, w.E)
     blk["w1_scale"][1, 5, 3] = 255                 # a NaN byte never counts as the maximum
     blk["w2_scale"][0, 130, 0] = 140
+    blk["w3_scale"][2, 200, 7] = 0                 # the subnormal byte also sets the flag
     table = torch.zeros(k3.k3moe_packed_bytes(cfg), dtype=torch.uint8, device="cuda")
     k3.k3moe_pack_mxfp4(cfg, 0, w.E, *(dev(blk[n]) for n in ki.EXPERT_TENSORS), table)
     torch.cuda.synchronize()
@@ -151,6 +152,11 @@ def test_pack_records_block_scale_maxima(k3):
                 blkv = sc[rb * 128:(rb + 1) * 128]
                 assert trailer[e, col] == blkv[blkv != 255].max()
                 col += 1
+        special = any(((blk[f"{m}_scale"][e] == 0) | (blk[f"{m}_scale"][e] == 255)).any()
+                      for m in ("w1", "w3", "w2"))
+        assert (trailer[e, 255] != 0) == special
+        assert not trailer[e, col:255].any()
+    assert [trailer[e, 255] != 0 for e in range(w.E)] == [False, True, True, False]
 
 
 def test_pack_roundtrip_full_shape(k3):
@@ -299,8 +305,12 @@ def test_bad_routing_sets_status_without_fault(k3):
     assert torch.isfinite(out).all() and out.abs().max() > 0
 
 
-def test_nan_scale_groups_read_as_zero(k3):
-    w = MICRO.with_(name="nanscale", seed=48, T=11)
+@pytest.mark.parametrize("T", [1, 11, 40])
+def test_nan_scale_groups_read_as_zero(k3, T):
+    """Scale byte 255 reads as zero and byte 0 as 2^-127; experts holding either take
+    the exact scale path of the streamed mat-vecs, the others the fast one, in the same
+    launch; T = 40 takes the tensor-core path."""
+    w = MICRO.with_(name="nanscale", seed=48, T=T)
     cfg = k3.k3moe_config(**w.config_kwargs())
     from sparse_moe_expert_k3moe_gb300 import MoELayer
     from k3moe_inputs.device import to_device_u16
@@ -311,7 +321,10 @@ def test_nan_scale_groups_read_as_zero(k3):
     experts = {e: ki.make_expert(w, e) for e in range(w.E)}
     for e in range(w.E):
         for name in ("w1_scale", "w3_scale", "w2_scale"):
-            experts[e][name][::7, 1] = 255
+            if e % 3 == 0:
+                experts[e][name][::7, 1] = 255
+            elif e % 3 == 1:
+                experts[e][name][::11, 2] = 0
     blk = {n: np.stack([experts[e][n] for e in range(w.E)]) for n in ki.EXPERT_TENSORS}
     layer.pack_experts(0, w.E, *(dev(blk[n]) for n in ki.EXPERT_TENSORS))
     x = ki.make_x(w)
