@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=15.0)
+    p.add_argument("--graph", action="store_true",
+                   help="replay route + forward as one captured CUDA graph per step")
     return p.parse_args()
 
 
@@ -328,9 +330,17 @@ def gpu_arm(args):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def eager_step():
         layer.route(x, stream)
         layer.forward(x, out, stream)
+
+    step = eager_step
+    graph_launches = None
+    if args.graph:
+        n0 = k3.k3moe_launch_count()
+        graph = layer.capture(x, out)
+        graph_launches = (k3.k3moe_launch_count() - n0) // 2      # the eager call + the capture
+        step = graph.replay
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -359,6 +369,8 @@ def gpu_arm(args):
     torch.cuda.synchronize(dev)
     barrier()
     launches = k3.k3moe_launch_count() - n0
+    if graph_launches is not None:
+        launches = graph_launches * args.steps
     clk = clocks.stop()
     ms = sum(a.elapsed_time(b) for a, b in ev)
     ms = allmax(ms)
@@ -369,7 +381,7 @@ def gpu_arm(args):
     k3.k3moe_timing_enable(True)
     for i in range(args.steps):
         flush.fill_(i & 255)
-        step()
+        eager_step()
     torch.cuda.synchronize(dev)
     k3.k3moe_timing_enable(False)
     kt = k3.k3moe_timing_read()
@@ -395,7 +407,7 @@ def gpu_arm(args):
     if not args.no_e2e:
         xh = torch.from_numpy(ki.make_x(w).view(np.int16)).pin_memory()
         oh = torch.empty((w.T, w.d), dtype=torch.float32).pin_memory()
-        xd = torch.empty_like(x)
+        xd = x if args.graph else torch.empty_like(x)
         ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         for i in range(args.steps + 2):
@@ -403,8 +415,11 @@ def gpu_arm(args):
             if i >= 2:
                 ee[i - 2][0].record(stream)
             xd.copy_(xh, non_blocking=True)
-            layer.route(xd, stream)
-            layer.forward(xd, out, stream)
+            if args.graph:
+                step()
+            else:
+                layer.route(xd, stream)
+                layer.forward(xd, out, stream)
             oh.copy_(out, non_blocking=True)
             if i >= 2:
                 ee[i - 2][1].record(stream)
@@ -431,6 +446,7 @@ def gpu_arm(args):
             "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "top_k": w.k,
                        "n_shared": w.S, "weights": "routed MXFP4 (E2M1 + E8M0/32), shared bf16",
                        "l2": "512 MiB buffer written between timed steps",
+                       "launch": "one CUDA graph replay per step" if args.graph else "eager",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": dict(roof, kernel=top_name, peak_source=src,
                              traffic=traffic_for(top_name, w.name), alg_bytes_per_launch=alg_b,

@@ -273,3 +273,22 @@ class MoELayer:
         self.route(x, stream)
         self.forward(x, out, stream)
         return out
+
+    def capture(self, x, out):
+        """Record route + forward on the fixed buffers x [T][d] bf16 and out [T][d] f32 as
+        a CUDA graph and return the torch.cuda.CUDAGraph.  One eager call on a side stream
+        first settles the library's cached launch attributes, so that capture itself only
+        enqueues kernels.  The graph reads x and writes out, idx, weight, offsets, perm
+        and the workspace where they are now: copy the next tokens into x, then replay().
+        The launches keep their programmatic dependencies as graph edges."""
+        import torch
+        cur = torch.cuda.current_stream(self.device)
+        side = torch.cuda.Stream(device=self.device)
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            self(x, out)
+        cur.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self(x, out)
+        return g

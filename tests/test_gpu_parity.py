@@ -249,6 +249,44 @@ def test_alternating_shapes(k3):
         assert_out_close(host(out), ref, w.name)
 
 
+@pytest.mark.parametrize("T,bitwise", [(1, True), (4, True), (40, False)])
+def test_graph_replay(k3, T, bitwise):
+    """route + forward captured as one CUDA graph: a replay gives the eager call's routing
+    and output, and a replay on new tokens copied into the same input buffer matches the
+    oracle.  T = 1 and 4 take the streamed mat-vecs, whose combine is a fixed-order
+    gather, so the output repeats bit for bit; T = 40 takes the tensor-core path, whose
+    down epilogue adds into the output with fp32 atomics (order varies run to run)."""
+    from k3moe_inputs.device import build_layer
+    w = MICRO.with_(name=f"graph_t{T}", T=T, seed=60 + T)
+    layer = build_layer(w)
+    xd = dev16(ki.make_x(w))
+    out_eager = torch.empty((T, w.d), dtype=torch.float32, device="cuda")
+    layer(xd, out_eager)
+    idx_eager = host(layer.idx).copy()
+    out = torch.zeros_like(out_eager)
+    graph = layer.capture(xd, out)
+    out.zero_()
+    layer.idx.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(layer.idx), idx_eager)
+    if bitwise:
+        np.testing.assert_array_equal(host(out), host(out_eager))
+    else:
+        ref_scale = float(np.abs(host(out_eager)).max())
+        np.testing.assert_allclose(host(out), host(out_eager), rtol=1e-5, atol=1e-6 * ref_scale)
+    x2 = ki.make_x(w.with_(seed=w.seed + 1000))
+    xd.copy_(dev16(x2))
+    graph.replay()
+    torch.cuda.synchronize()
+    rc, code = k3.k3moe_device_status(layer.ws)
+    assert rc == 0 and code == 0
+    assert not np.array_equal(host(layer.idx), idx_eager)
+    ref = oracle.forward(ocfg(w), x2, host(layer.idx), host(layer.weight),
+                         oracle_experts(w, range(w.E)), ki.make_shared(w))
+    assert_out_close(host(out), ref, w.name + " replayed on new tokens")
+
+
 def test_forward_with_injected_oracle_routing(k3):
     """Routing computed by the oracle, uploaded, consumed by k3moe_forward."""
     from k3moe_inputs.device import build_layer
