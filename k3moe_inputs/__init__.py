@@ -20,7 +20,15 @@ decode_t1      1      3584  3072  896  16  2  scale exponents U[-10,-6]
 decode_t64     64     3584  3072  896  16  2  as decode_t1
 prefill_t4096  4096   3584  3072  896  16  2  1% of activation rows scaled by 8
 prefill_t16k   16384  3584  3072  896  16  2  Zipf(s=1.1) routing bias, seeded ranks
+full_tiny      4      128   128   8    2   1  full-width block, hidden 256
+full_t1        1      3584  3072  896  16  2  full-width block, hidden 7168
+full_t4096     4096   3584  3072  896  16  2  full-width block, hidden 7168, 1% rows x8
 =============  =====  ====  ====  ===  ==  =  ===========================================
+
+The full-width block (the Stable LatentMoE step around the layer) adds tokens of
+width H ~ N(0,1), a full-width router ~ N(0, 0.02), down [d,H] ~ N(0, 1/H) and up
+[H,d] ~ N(0, 1/d) projections, an RMSNorm gain 1 + N(0, 0.01), and the shared
+experts fused to width S*f on the full width, ~ N(0, sigma_s).
 
 Activations bf16 ~ N(0,1); router weights bf16 ~ N(0, 0.02); E2M1 codes
 uniform over all 16 codes (so packed bytes are uniform over 0..255); shared
@@ -52,6 +60,14 @@ STREAM_OUTLIER_ROWS = 4
 STREAM_SHARED_W1 = 10
 STREAM_SHARED_W3 = 11
 STREAM_SHARED_W2 = 12
+STREAM_FULL_H = 20
+STREAM_FULL_ROUTER = 21
+STREAM_FULL_DOWN = 22
+STREAM_FULL_UP = 23
+STREAM_FULL_GAIN = 24
+STREAM_FULL_SH1 = 25
+STREAM_FULL_SH3 = 26
+STREAM_FULL_SH2 = 27
 EXPERT_TENSORS = ("w1_packed", "w1_scale", "w3_packed", "w3_scale", "w2_packed", "w2_scale")
 
 
@@ -181,6 +197,9 @@ class Workload:
     situ_b2: float = 25.0
     renorm: int = 1
     routed_scale: float = 1.0
+    hidden: int = 0             # full-width block: width H of its tokens (0: latent layer only)
+    latent_norm: int = 1        # full-width block: RMSNorm the aggregate
+    rms_eps: float = 1e-5
 
     @property
     def shared_sigma(self) -> float:
@@ -217,6 +236,11 @@ WORKLOADS = {
     "decode_t64": Workload("decode_t64", T=64, seed=2, **_K3),
     "prefill_t4096": Workload("prefill_t4096", T=4096, seed=3, outlier_frac=0.01, **_K3),
     "prefill_t16k": Workload("prefill_t16k", T=16384, seed=4, zipf_bias=True, **_K3),
+    # the full-width Stable LatentMoE block around the layer (hidden 7168)
+    "full_tiny": Workload("full_tiny", T=4, d=128, f=128, E=8, k=2, S=1, exp_lo=-8, exp_hi=-4,
+                          seed=5, hidden=256),
+    "full_t1": Workload("full_t1", T=1, seed=6, hidden=7168, **_K3),
+    "full_t4096": Workload("full_t4096", T=4096, seed=7, hidden=7168, outlier_frac=0.01, **_K3),
 }
 
 
@@ -286,9 +310,43 @@ def make_shared(w: Workload) -> dict:
     }
 
 
+# ----------------------------------------------------------------------------- full-width block
+
+def make_h(w: Workload) -> np.ndarray:
+    """Full-width tokens [T, H] as bf16 bits; a seeded 1% of rows scaled by 8 when asked."""
+    h = bf16_normal(w.T * w.hidden, w.seed, STREAM_FULL_H, w.x_sigma).reshape(w.T, w.hidden)
+    n_out = int(round(w.outlier_frac * w.T))
+    if n_out:
+        rows = outlier_rows(w)
+        h[rows] = f32_to_bf16(bf16_to_f32(h[rows]) * np.float32(w.outlier_scale))
+    return h
+
+
+def make_full_router(w: Workload) -> np.ndarray:
+    """Full-width router weights [E, H] as bf16 bits, N(0, router_sigma)."""
+    return bf16_normal(w.E * w.hidden, w.seed, STREAM_FULL_ROUTER, w.router_sigma).reshape(w.E, w.hidden)
+
+
+def make_full(w: Workload) -> dict:
+    """The block's dense tensors: down [d, H] bf16 ~ N(0, 1/H) (a unit-variance token
+    gives unit-variance latents), up [H, d] bf16 ~ N(0, 1/d) (likewise from the normed
+    aggregate), gain [d] float32 = 1 + N(0, 0.1^2) in bf16 steps, and the fused shared
+    experts sh1, sh3 [S*f, H], sh2 [H, S*f] bf16 ~ N(0, sigma_s^2)."""
+    H, d, SI = w.hidden, w.d, w.S * w.f
+    sig = w.shared_sigma
+    return {
+        "down": bf16_normal(d * H, w.seed, STREAM_FULL_DOWN, 1.0 / math.sqrt(H)).reshape(d, H),
+        "up": bf16_normal(H * d, w.seed, STREAM_FULL_UP, 1.0 / math.sqrt(d)).reshape(H, d),
+        "gain": (1.0 + bf16_to_f32(bf16_normal(d, w.seed, STREAM_FULL_GAIN, 0.1))).astype(np.float32),
+        "sh1": bf16_normal(SI * H, w.seed, STREAM_FULL_SH1, sig).reshape(SI, H),
+        "sh3": bf16_normal(SI * H, w.seed, STREAM_FULL_SH3, sig).reshape(SI, H),
+        "sh2": bf16_normal(H * SI, w.seed, STREAM_FULL_SH2, sig).reshape(H, SI),
+    }
+
+
 __all__ = [
     "Workload", "WORKLOADS", "EXPERT_TENSORS", "build", "make_x", "make_router", "make_bias",
     "make_expert", "make_experts_block", "make_shared", "outlier_rows", "bf16_to_f32",
     "f32_to_bf16", "bf16_normal", "random_bytes", "uniform_bytes", "permutation",
-    "routed_weight_rms", "expert_stream",
+    "routed_weight_rms", "expert_stream", "make_h", "make_full_router", "make_full",
 ]

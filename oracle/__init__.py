@@ -71,6 +71,7 @@ def lib():
             "k3o_perm": (i, [i, i, i, p, p, p]),
             "k3o_forward": (i, [cp, i, p, p, p, p, p, p, p, p, p]),
             "k3o_moe": (i, [cp, i, p, p, p, p, p, p, p, p, p, p]),
+            "k3o_forward_full": (i, [cp, i, i, d, i] + [p] * 11),
             "k3o_num_threads": (i, []),
         }
         for name, (res, args) in sig.items():
@@ -201,3 +202,24 @@ def forward(c: Cfg, x: np.ndarray, idx: np.ndarray, w: np.ndarray, experts: dict
                              _p(np.ascontiguousarray(w, np.float32)), ctypes.cast(table.arr, ctypes.c_void_p),
                              _p(w1), _p(w3), _p(w2), _p(out), _p(outs)), "forward")
     return (out, outs) if want_shared else out
+
+
+def forward_full(c: Cfg, H: int, latent_norm: int, eps: float, h: np.ndarray, idx: np.ndarray,
+                 w: np.ndarray, Wd: np.ndarray, experts: dict, gain, Wu: np.ndarray,
+                 shared: dict | None) -> np.ndarray:
+    """The full-width block for given routing (route first with ``route`` on a config
+    whose d is H): h [T,H] bf16 bits, Wd [d,H], Wu [H,d] bf16 bits, gain [d] float32,
+    shared {"w1","w3": [S*f,H], "w2": [H,S*f]} bf16 bits.  Returns out [T,H] float32."""
+    T = h.shape[0]
+    table = ExpertTable(c.n_experts, experts)
+    out = np.empty((T, H), dtype=np.float32)
+    sh = shared or {}
+    w1, w3, w2 = (np.ascontiguousarray(sh[n]) if n in sh else None for n in ("w1", "w3", "w2"))
+    g = None if gain is None else np.ascontiguousarray(gain, dtype=np.float32)
+    _check(lib().k3o_forward_full(ctypes.byref(c), H, latent_norm, eps, T,
+                                  _p(np.ascontiguousarray(h)), _p(np.ascontiguousarray(idx, np.int32)),
+                                  _p(np.ascontiguousarray(w, np.float32)), _p(np.ascontiguousarray(Wd)),
+                                  ctypes.cast(table.arr, ctypes.c_void_p), _p(g),
+                                  _p(np.ascontiguousarray(Wu)), _p(w1), _p(w3), _p(w2), _p(out)),
+           "forward_full")
+    return out

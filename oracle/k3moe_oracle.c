@@ -24,8 +24,10 @@
  *
  * The layer built here is the latent-space part of that loop: its input x is
  * already the expert latent (width d), the router scores x directly, and the
- * d -> f -> d shared experts read the same x.  Full-width down/up projections
- * and the aggregate RMSNorm sit outside it.
+ * d -> f -> d shared experts read the same x.  k3o_forward_full adds what sits
+ * around it in the write-up's k3_moe (same section): the full-width router
+ * input, the down and up projections, the RMSNorm of the aggregate and the
+ * full-width shared experts.
  *
  * Precision: the router follows the write-up's float steps exactly, because
  * float rounding decides which experts win; everything else is computed in
@@ -39,7 +41,10 @@
  * invariants; SiTU's closed-form bound and its small-input limit; the whole
  * layer against an independent dense fp64 brute force on tiny layers; the
  * special cases k = E and E = k = 1; and the shared-expert output's
- * independence from routing.  No function here is "parity unpinned".
+ * independence from routing.  The full-width block: against an independent
+ * dense fp64 brute force on tiny blocks, its reduction to the latent layer
+ * (identity projections, no norm), and the norm's scale invariance.  No
+ * function here is "parity unpinned".
  *
  * Build: cc -O2 -std=c99 -fPIC -shared -fopenmp -ffp-contract=off -lm
  */
@@ -317,6 +322,34 @@ int k3o_perm(int T, int E, int k, const int32_t *idx, int32_t *offsets, int32_t 
 
 /* --------------------------------------------------------- expert layer (s9) */
 
+/* y [d] = W2 . situ(W1 x, W3 x) for one routed MXFP4 expert on x [d];
+ * g, u, h are scratch of f doubles. */
+static void expert_ffn(const k3o_cfg *c, const k3o_expert *q, const double *x,
+                       double *g, double *u, double *h, double *y)
+{
+    const int d = c->d, f = c->f, G = c->group;
+    k3o_mxfp4_matvec(g, x, q->w1_packed, q->w1_scale, d, f, G);
+    k3o_mxfp4_matvec(u, x, q->w3_packed, q->w3_scale, d, f, G);
+    for (int i = 0; i < f; i++)
+        h[i] = k3o_situ(g[i], u[i], c->situ_b1, c->situ_b2);
+    k3o_mxfp4_matvec(y, h, q->w2_packed, q->w2_scale, f, d, G);
+}
+
+/* Every selected expert of routing idx [T][k] must be present (non-NULL). */
+static int check_routing(const k3o_cfg *c, int T, const int32_t *idx, const k3o_expert *experts)
+{
+    for (size_t s = 0; s < (size_t)T * (size_t)c->top_k; s++) {
+        const int e = idx[s];
+        if (e < 0 || e >= c->n_experts)
+            return K3O_EINVAL;
+        const k3o_expert *q = experts + e;
+        if (!q->w1_packed || !q->w1_scale || !q->w3_packed || !q->w3_scale ||
+            !q->w2_packed || !q->w2_scale)
+            return K3O_EMISSING;
+    }
+    return K3O_OK;
+}
+
 /* out[t] = sum_j w[t][j] * FFN_{idx[t][j]}(x_t) + sum_s SharedFFN_s(x_t), where
  * FFN(x) = W2 . situ(W1 x, W3 x) on MXFP4 weights and the shared experts are
  * the same form on bf16 weights, added with weight one.  Everything in double;
@@ -331,17 +364,10 @@ int k3o_forward(const k3o_cfg *c, int T, const uint16_t *x, const int32_t *idx,
     if (k3o_check_cfg(c) || T < 0 || (T > 0 && (!x || !out)) ||
         (c->n_shared > 0 && T > 0 && (!sh_w1 || !sh_w3 || !sh_w2)))
         return K3O_EINVAL;
-    const int d = c->d, f = c->f, k = c->top_k, G = c->group;
-    for (size_t s = 0; s < (size_t)T * (size_t)k; s++) {
-        const int e = idx[s];
-        if (e < 0 || e >= c->n_experts)
-            return K3O_EINVAL;
-        const k3o_expert *q = experts + e;
-        if (!q->w1_packed || !q->w1_scale || !q->w3_packed || !q->w3_scale ||
-            !q->w2_packed || !q->w2_scale)
-            return K3O_EMISSING;
-    }
-    int err = K3O_OK;
+    const int d = c->d, f = c->f, k = c->top_k;
+    int err = check_routing(c, T, idx, experts);
+    if (err)
+        return err;
 #pragma omp parallel if (T > 1)
     {
         double *xd = malloc(sizeof(double) * (size_t)d);
@@ -365,11 +391,7 @@ int k3o_forward(const k3o_cfg *c, int T, const uint16_t *x, const int32_t *idx,
                 for (int j = 0; j < k; j++) {
                     const k3o_expert *q = experts + idx[(size_t)t * k + j];
                     const double wt = (double)w[(size_t)t * k + j];
-                    k3o_mxfp4_matvec(g, xd, q->w1_packed, q->w1_scale, d, f, G);
-                    k3o_mxfp4_matvec(u, xd, q->w3_packed, q->w3_scale, d, f, G);
-                    for (int i = 0; i < f; i++)
-                        h[i] = k3o_situ(g[i], u[i], c->situ_b1, c->situ_b2);
-                    k3o_mxfp4_matvec(y, h, q->w2_packed, q->w2_scale, f, d, G);
+                    expert_ffn(c, q, xd, g, u, h, y);
                     for (int i = 0; i < d; i++)
                         acc[i] += wt * y[i];
                 }
@@ -391,6 +413,99 @@ int k3o_forward(const k3o_cfg *c, int T, const uint16_t *x, const int32_t *idx,
             }
         }
         free(xd); free(g); free(u); free(h); free(y); free(acc); free(accs);
+    }
+    return err;
+}
+
+/* ------------------------------------------- full-width block (s9, k3_moe) */
+
+/* The whole Stable LatentMoE block for T full-width tokens h [T][H] and given
+ * routing (the router reads the full-width token: k3o_route on a config whose
+ * d is H), in the order of the write-up's six steps:
+ *   z = Wd h                          Wd [d][H] bf16, into the expert latent
+ *   a = sum_j w_j FFN_{idx_j}(z)      the routed experts, as in k3o_forward
+ *   a_i = a_i gain_i / sqrt(sum_i a_i^2 / d + eps)   when latent_norm: the norm
+ *                                     of the AGGREGATE, never of one expert
+ *   out = Wu a                        Wu [H][d] bf16, back to full width
+ *   out += Sh2 situ(Sh1 h, Sh3 h)     the shared experts on the ORIGINAL h,
+ *                                     fused to one FFN of width SI = S f:
+ *                                     Sh1, Sh3 [SI][H], Sh2 [H][SI] bf16;
+ *                                     added unweighted
+ * c describes the expert latent (d, f, E, k) and S = c->n_shared.  Everything
+ * in double, out [T][H] rounded to float once. */
+int k3o_forward_full(const k3o_cfg *c, int H, int latent_norm, double eps, int T,
+                     const uint16_t *h, const int32_t *idx, const float *w,
+                     const uint16_t *Wd, const k3o_expert *experts, const float *gain,
+                     const uint16_t *Wu, const uint16_t *sh1, const uint16_t *sh3,
+                     const uint16_t *sh2, float *out)
+{
+    if (k3o_check_cfg(c) || H <= 0 || T < 0 || !(eps > 0.0) ||
+        (latent_norm != 0 && latent_norm != 1) ||
+        (T > 0 && (!h || !idx || !w || !Wd || !Wu || !out || (latent_norm && !gain))) ||
+        (c->n_shared > 0 && T > 0 && (!sh1 || !sh3 || !sh2)))
+        return K3O_EINVAL;
+    const int d = c->d, f = c->f, k = c->top_k, SI = c->n_shared * c->f;
+    int err = check_routing(c, T, idx, experts);
+    if (err)
+        return err;
+    const int wide = f > SI ? f : SI;
+    const int dh = d > H ? d : H;
+#pragma omp parallel if (T > 1)
+    {
+        double *hd = malloc(sizeof(double) * (size_t)H);
+        double *z = malloc(sizeof(double) * (size_t)d);
+        double *a = malloc(sizeof(double) * (size_t)d);
+        double *o = malloc(sizeof(double) * (size_t)H);
+        double *y = malloc(sizeof(double) * (size_t)dh);
+        double *g = malloc(sizeof(double) * (size_t)wide);
+        double *u = malloc(sizeof(double) * (size_t)wide);
+        double *act = malloc(sizeof(double) * (size_t)wide);
+        if (!hd || !z || !a || !o || !y || !g || !u || !act) {
+#pragma omp atomic write
+            err = K3O_ENOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int t = 0; t < T; t++) {
+                for (int i = 0; i < H; i++)
+                    hd[i] = (double)k3o_bf16(h[(size_t)t * H + i]);
+                /* 2. down into the expert latent */
+                k3o_bf16_matvec(z, hd, Wd, H, d);
+                /* 3. the chosen experts, accumulated in the latent */
+                for (int i = 0; i < d; i++)
+                    a[i] = 0.0;
+                for (int j = 0; j < k; j++) {
+                    const k3o_expert *q = experts + idx[(size_t)t * k + j];
+                    const double wt = (double)w[(size_t)t * k + j];
+                    expert_ffn(c, q, z, g, u, act, y);
+                    for (int i = 0; i < d; i++)
+                        a[i] += wt * y[i];
+                }
+                /* 4. RMSNorm of the aggregate */
+                if (latent_norm) {
+                    double ss = 0.0;
+                    for (int i = 0; i < d; i++)
+                        ss += a[i] * a[i];
+                    const double r = 1.0 / sqrt(ss / d + eps);
+                    for (int i = 0; i < d; i++)
+                        a[i] = a[i] * r * (double)gain[i];
+                }
+                /* 5. back up to full width */
+                k3o_bf16_matvec(o, a, Wu, d, H);
+                /* 6. shared experts on the original h, unweighted */
+                if (SI > 0) {
+                    k3o_bf16_matvec(g, hd, sh1, H, SI);
+                    k3o_bf16_matvec(u, hd, sh3, H, SI);
+                    for (int i = 0; i < SI; i++)
+                        act[i] = k3o_situ(g[i], u[i], c->situ_b1, c->situ_b2);
+                    k3o_bf16_matvec(y, act, sh2, SI, H);
+                    for (int i = 0; i < H; i++)
+                        o[i] += y[i];
+                }
+                for (int i = 0; i < H; i++)
+                    out[(size_t)t * H + i] = (float)o[i];
+            }
+        }
+        free(hd); free(z); free(a); free(o); free(y); free(g); free(u); free(act);
     }
     return err;
 }

@@ -424,3 +424,128 @@ def test_invalid_configs_rejected():
     import ctypes
     for kw in bad:
         assert lib.k3o_check_cfg(ctypes.byref(oracle.cfg(**kw))) != 0
+
+
+# ----------------------------------------------------------------------------- full-width block
+
+def _full_case(wl):
+    h, Wr, bias = ki.make_h(wl), ki.make_full_router(wl), ki.make_bias(wl)
+    experts = {e: ki.make_expert(wl, e) for e in range(wl.E)}
+    full = ki.make_full(wl)
+    shared = {"w1": full["sh1"], "w3": full["sh3"], "w2": full["sh2"]} if wl.S else None
+    return h, Wr, bias, experts, full, shared
+
+
+def _full_oracle(wl, h, Wr, bias, experts, full, shared, route=None):
+    c_route = oracle.cfg(**dict(wl.config_kwargs(), d=wl.hidden))
+    idx, w, gap = route if route is not None else oracle.route(c_route, h, Wr, bias)
+    out = oracle.forward_full(oracle.cfg(**wl.config_kwargs()), wl.hidden, wl.latent_norm,
+                              wl.rms_eps, h, idx, w, full["down"], experts, full["gain"],
+                              full["up"], shared)
+    return out, idx, w, gap
+
+
+def brute_force_full(wl, h, Wr, bias, experts, full, shared):
+    """Independent dense fp64 restatement of the block's six steps: float32 router
+    scores on the full-width token, full-sort top-k, dense decoded weights, numpy
+    tanh/exp, the RMSNorm of the weighted sum written out, fp64 throughout."""
+    T, k = wl.T, wl.k
+    hd = dense_bf16(h)
+    logit = (hd @ dense_bf16(Wr).T).astype(np.float32)
+    sc = (np.float32(1) / (np.float32(1) + np.exp(-logit))).astype(np.float32)
+    ch = sc + (bias if bias is not None else np.float32(0))
+    b1, b2 = wl.situ_b1, wl.situ_b2
+
+    def situ(g, u):
+        return b1 * np.tanh(g / b1) / (1.0 + np.exp(-g)) * (b2 * np.tanh(u / b2))
+
+    Wd, Wu = dense_bf16(full["down"]), dense_bf16(full["up"])
+    dense = {e: tuple(dense_mxfp4(q[f"{m}_packed"], q[f"{m}_scale"]) for m in ("w1", "w3", "w2"))
+             for e, q in experts.items()}
+    out = np.zeros((T, wl.hidden))
+    idx_all = np.zeros((T, k), dtype=np.int64)
+    for t in range(T):
+        sel, _ = lexsort_topk(ch[t], k)
+        idx_all[t] = sel
+        wsel = sc[t, sel].astype(np.float32)
+        if wl.renorm:
+            s = np.float32(0)
+            for v in wsel:
+                s = np.float32(s + v)
+            if s > 0:
+                wsel = (wsel / s).astype(np.float32)
+        wsel = (wsel * np.float32(wl.routed_scale)).astype(np.float32)
+        z = Wd @ hd[t]
+        a = np.zeros(wl.d)
+        for e, wt in zip(sel, wsel):
+            W1, W3, W2 = dense[e]
+            a += float(wt) * (W2 @ situ(W1 @ z, W3 @ z))
+        if wl.latent_norm:
+            a = a / np.sqrt(np.mean(a * a) + wl.rms_eps) * full["gain"].astype(np.float64)
+        out[t] = Wu @ a
+        if shared is not None:
+            S1, S3, S2 = (dense_bf16(shared[m]) for m in ("w1", "w3", "w2"))
+            out[t] += S2 @ situ(S1 @ hd[t], S3 @ hd[t])
+    return out, idx_all
+
+
+FULL = ki.WORKLOADS["full_tiny"]
+
+
+@pytest.mark.parametrize("wl", [
+    FULL,
+    FULL.with_(name="full_no_norm", latent_norm=0, seed=31),
+    FULL.with_(name="full_no_shared", S=0, seed=32),
+    FULL.with_(name="full_two_shared", S=2, seed=33, T=3),
+    FULL.with_(name="full_bias", zipf_bias=True, E=12, k=3, seed=34),
+    FULL.with_(name="full_wide_latent", d=256, hidden=128, seed=35, T=2),
+], ids=lambda w: w.name)
+def test_full_block_matches_brute_force(wl):
+    case = _full_case(wl)
+    out, idx, w, gap = _full_oracle(wl, *case)
+    ref, ref_idx = brute_force_full(wl, *case)
+    for t in range(wl.T):
+        if gap[t] >= 1e-6:
+            assert list(idx[t]) == list(ref_idx[t])
+    assert np.max(np.abs(out - ref)) <= 1e-6 * np.max(np.abs(ref))
+
+
+def test_full_block_reduces_to_latent_layer():
+    """Identity down and up projections, no norm, and the shared experts' fused
+    weights stacked from the latent layer's: the block is the latent layer."""
+    wl = FULL.with_(name="full_identity", hidden=128, d=128, S=2, latent_norm=0, seed=36)
+    h, Wr, bias, experts, full, _ = _full_case(wl)
+    eye = np.where(np.eye(wl.d, dtype=bool), np.uint16(0x3F80), np.uint16(0))   # bf16 1.0
+    full = dict(full, down=eye, up=eye.copy())
+    sh = ki.make_shared(wl)                                  # [S,f,d], [S,d,f]
+    fused = {"w1": sh["w1"].reshape(wl.S * wl.f, wl.d), "w3": sh["w3"].reshape(wl.S * wl.f, wl.d),
+             "w2": np.ascontiguousarray(np.concatenate(list(sh["w2"]), axis=1))}
+    out, idx, w, _ = _full_oracle(wl, h, Wr, bias, experts, full, fused)
+    lat = oracle.forward(oracle.cfg(**wl.config_kwargs()), h, idx, w, experts, sh)
+    assert np.max(np.abs(out - lat)) <= 1e-6 * np.max(np.abs(lat))
+    # the identity case still routes on the full-width token: same scores as the layer's router
+    idx_l, w_l, _ = oracle.route(oracle.cfg(**wl.config_kwargs()), h, Wr, bias)
+    np.testing.assert_array_equal(idx, idx_l)
+
+
+def test_full_block_norms_the_aggregate_not_each_expert():
+    """Doubling every expert's down weights (scale bytes + 1) leaves the normed block
+    unchanged; doubling ONE chosen expert's changes it, which a per-expert norm would
+    not; without the norm, doubling all changes the routed part."""
+    wl = FULL.with_(name="full_norm", S=0, seed=37, T=3, rms_eps=1e-12)   # eps out of the way
+    h, Wr, bias, experts, full, shared = _full_case(wl)
+    base, idx, w, gap = _full_oracle(wl, h, Wr, bias, experts, full, shared)
+    route = (idx, w, gap)
+
+    def doubled(which):
+        return {e: (dict(q, w2_scale=q["w2_scale"] + 1) if e in which else q) for e, q in experts.items()}
+
+    scale = np.max(np.abs(base))
+    all2 = _full_oracle(wl, h, Wr, bias, doubled(set(experts)), full, shared, route)[0]
+    assert np.max(np.abs(all2 - base)) <= 1e-6 * scale
+    one2 = _full_oracle(wl, h, Wr, bias, doubled({int(idx[0, 0])}), full, shared, route)[0]
+    assert np.max(np.abs(one2[0] - base[0])) > 1e-2 * scale
+    raw = wl.with_(latent_norm=0)
+    r1 = _full_oracle(raw, h, Wr, bias, experts, full, shared, route)[0]
+    r2 = _full_oracle(raw, h, Wr, bias, doubled(set(experts)), full, shared, route)[0]
+    np.testing.assert_allclose(r2, 2.0 * r1, rtol=1e-9, atol=1e-9 * np.max(np.abs(r1)))
