@@ -95,6 +95,8 @@ def layer_bytes_flops(w, distinct_experts: int):
     touched (packed MXFP4), the shared experts (bf16), the router (bf16), x in (bf16)
     and out (f32).  FLOPs: 2*3*f*d per (token, expert) for k routed + S shared experts,
     plus 2*E*d per token for the router."""
+    if w.hidden:
+        return block_bytes_flops(w, distinct_experts)
     Be = w.expert_bytes
     shared = w.S * 3 * w.f * w.d * 2
     router = w.E * w.d * 2
@@ -102,6 +104,38 @@ def layer_bytes_flops(w, distinct_experts: int):
     byts = distinct_experts * Be + shared + router + act
     flops = w.T * (2 * 3 * w.f * w.d * (w.k + w.S) + 2 * w.E * w.d)
     return byts, flops
+
+
+def block_bytes_flops(w, distinct_experts: int):
+    """Algorithmic bytes and FLOPs of one full-width block call: the distinct routed
+    experts, the full-width router [E,H], the down [d,H] and up [H,d] projections, the
+    fused shared experts (3*H*S*f bf16), h in (bf16) and out (f32).  FLOPs per token:
+    2*E*H (router) + 2*2*d*H (projections) + 2*3*f*d*k (routed) + 2*3*H*S*f (shared)."""
+    H, SI = w.hidden, w.S * w.f
+    byts = (distinct_experts * w.expert_bytes + w.E * H * 2 + 2 * w.d * H * 2 + 3 * H * SI * 2
+            + w.T * H * 2 + w.T * H * 4)
+    flops = w.T * (2 * w.E * H + 4 * w.d * H + 2 * 3 * w.f * w.d * w.k + 2 * 3 * H * SI)
+    return byts, flops
+
+
+def full_kernel_work(name: str, w, distinct_experts: int):
+    """kernel_work for a full-width block: its dense GEMMs (weights, activations in and
+    out; 2*m*n*k FLOPs), else the layer's kernels as the block runs them (router on width
+    H, experts on the latent without shared experts)."""
+    T, H, d, SI = w.T, w.hidden, w.d, w.S * w.f
+    if name == "full_down_gemm":
+        return d * H * 2 + T * H * 2 + T * d * 2, 2 * T * d * H
+    if name == "full_up_gemm":
+        return H * d * 2 + T * d * 2 + T * H * 4, 2 * T * H * d
+    if name in ("full_shared_gate_gemm", "full_shared_up_gemm"):
+        return SI * H * 2 + T * H * 2 + T * SI * 4, 2 * T * SI * H
+    if name == "full_shared_down_gemm":
+        return H * SI * 2 + T * SI * 2 + 2 * T * H * 4, 2 * T * H * SI
+    if name in ("router_scores", "router_scores_tc"):
+        return kernel_work(name, w.with_(d=H, hidden=0), distinct_experts)
+    if name in ("gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down"):
+        return kernel_work(name, w.with_(S=0, hidden=0), distinct_experts)
+    return block_bytes_flops(w, distinct_experts)[0], 0
 
 
 def kernel_work(name: str, w, distinct_experts: int):
@@ -114,6 +148,8 @@ def kernel_work(name: str, w, distinct_experts: int):
     mat-vec path a bf16 hi + lo pair for shared rows); 2 * rows * 2*f*d FLOPs with
     rows = T*k + S*T.  gemv_down / gemm_down: W2 likewise, h in, the output out.
     Any other kernel is charged the whole layer's bytes and no FLOPs."""
+    if w.hidden:
+        return full_kernel_work(name, w, distinct_experts)
     rows = w.T * w.k + w.S * w.T
     slots = w.T * w.k
     h_gemv = slots * w.f * 2 + w.S * w.T * w.f * 4
@@ -243,22 +279,35 @@ def time_oracle(w, budget_s: float):
     import k3moe_inputs as ki
     import oracle
     c = oracle.cfg(**w.config_kwargs())
-    x = ki.make_x(w)
-    Wr = ki.make_router(w)
     bias = ki.make_bias(w)
-    shared = ki.make_shared(w) if w.S else None
+    if w.hidden:
+        # the full-width block: route on h, then the block's six steps
+        c_route = oracle.cfg(**dict(w.config_kwargs(), d=w.hidden))
+        x, Wr, full = ki.make_h(w), ki.make_full_router(w), ki.make_full(w)
+        shared = {"w1": full["sh1"], "w3": full["sh3"], "w2": full["sh2"]} if w.S else None
+
+        def run(xs, idx, wt):
+            oracle.forward_full(c, w.hidden, w.latent_norm, w.rms_eps, xs, idx, wt, full["down"],
+                                experts, full["gain"], full["up"], shared)
+    else:
+        c_route = c
+        x, Wr = ki.make_x(w), ki.make_router(w)
+        shared = ki.make_shared(w) if w.S else None
+
+        def run(xs, idx, wt):
+            oracle.forward(c, xs, idx, wt, experts, shared)
     experts = {}
     done, spent = 0, 0.0
     batch = max(1, min(w.T, oracle.num_threads()))
     while spent < budget_s:
         rows = [(done + i) % w.T for i in range(batch)]
         xs = np.ascontiguousarray(x[rows])
-        idx, wt, _ = oracle.route(c, xs, Wr, bias)        # untimed draw of the needed experts
+        idx, wt, _ = oracle.route(c_route, xs, Wr, bias)  # untimed draw of the needed experts
         for e in set(idx.ravel().tolist()) - set(experts):
             experts[e] = ki.make_expert(w, e)
         t0 = time.perf_counter()
-        idx, wt, _ = oracle.route(c, xs, Wr, bias)
-        oracle.forward(c, xs, idx, wt, experts, shared)
+        idx, wt, _ = oracle.route(c_route, xs, Wr, bias)
+        run(xs, idx, wt)
         spent += time.perf_counter() - t0
         done += len(rows)
         if len(experts) > 256:
@@ -324,15 +373,27 @@ def gpu_arm(args):
         return dist_max(v, world, dev)
 
     w = workload_from(args.workload)
-    layer = build_layer(w, device=dev)
-    x = torch.from_numpy(ki.make_x(w).view(np.int16)).to(dev)
-    out = torch.empty((w.T, w.d), dtype=torch.float32, device=dev)
+    width = w.hidden or w.d                                   # token width in and out
+    if w.hidden:
+        from k3moe_inputs.device import build_block
+        layer = build_block(w, device=dev)
+        x = torch.from_numpy(ki.make_h(w).view(np.int16)).to(dev)
+    else:
+        layer = build_layer(w, device=dev)
+        x = torch.from_numpy(ki.make_x(w).view(np.int16)).to(dev)
+    out = torch.empty((w.T, width), dtype=torch.float32, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    def layer_call(xin, stream):
+        if w.hidden:
+            layer.forward(xin, out, stream)
+        else:
+            layer.route(xin, stream)
+            layer.forward(xin, out, stream)
+
     def eager_step():
-        layer.route(x, stream)
-        layer.forward(x, out, stream)
+        layer_call(x, stream)
 
     step = eager_step
     graph_launches = None
@@ -405,8 +466,8 @@ def gpu_arm(args):
     # ---- end to end through the C ABI from pinned host memory
     e2e = None
     if not args.no_e2e:
-        xh = torch.from_numpy(ki.make_x(w).view(np.int16)).pin_memory()
-        oh = torch.empty((w.T, w.d), dtype=torch.float32).pin_memory()
+        xh = x.cpu().pin_memory()
+        oh = torch.empty((w.T, width), dtype=torch.float32).pin_memory()
         xd = x if args.graph else torch.empty_like(x)
         ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
@@ -418,8 +479,7 @@ def gpu_arm(args):
             if args.graph:
                 step()
             else:
-                layer.route(xd, stream)
-                layer.forward(xd, out, stream)
+                layer_call(xd, stream)
             oh.copy_(out, non_blocking=True)
             if i >= 2:
                 ee[i - 2][1].record(stream)
@@ -444,7 +504,10 @@ def gpu_arm(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "top_k": w.k,
-                       "n_shared": w.S, "weights": "routed MXFP4 (E2M1 + E8M0/32), shared bf16",
+                       "n_shared": w.S, **({"hidden": w.hidden, "latent_norm": w.latent_norm}
+                                           if w.hidden else {}),
+                       "weights": "routed MXFP4 (E2M1 + E8M0/32), shared bf16"
+                                  + (", dense projections bf16 (cuBLASLt)" if w.hidden else ""),
                        "l2": "512 MiB buffer written between timed steps",
                        "launch": "one CUDA graph replay per step" if args.graph else "eager",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

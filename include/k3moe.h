@@ -209,6 +209,57 @@ k3moe_status k3moe_forward_noalloc(const k3moe_config *cfg, int32_t T, const uin
                                    const uint16_t *sh_w2, float *out, int32_t *status_out,
                                    k3moe_stream stream);
 
+/* ---- The full-width block around the layer: the six steps of the k3_moe
+ * listing (kimi-k3-in-c README, Part II, section 9 "Picking 16 experts of 896"),
+ * for T full-width tokens h of width H:
+ *   1. route on h (not on the latent): the rules of k3moe_route with a router
+ *      [E][H] (cfg's d replaced by H);
+ *   2. z = Wd . h, into the expert latent (width cfg->d);
+ *   3. a = sum_j weight_j * W2_e . SiTU(W1_e z, W3_e z), the routed experts
+ *      of k3moe_forward on z, WITHOUT its shared experts;
+ *   4. when latent_norm: a_i = a_i * gain_i / sqrt(sum_i a_i^2 / d + rms_eps),
+ *      the RMSNorm of the weighted sum (never of one expert);
+ *   5. out = Wu . a, back to width H;
+ *   6. out += Sh2 . SiTU(Sh1 h, Sh3 h): the cfg->n_shared shared experts on
+ *      the ORIGINAL h, fused into one FFN of width SI = n_shared * f, added
+ *      with weight one.
+ * The K3 block has H = 7168, latent_norm = 1, rms_eps = 1e-5 (the K3Cfg
+ * struct of section 2). */
+typedef struct k3moe_full_dims {
+    int32_t hidden;       /* H; multiple of 128, <= 8192 */
+    int32_t latent_norm;  /* 1: RMSNorm the aggregate (step 4); 0: skip it */
+    float rms_eps;        /* > 0 and finite */
+} k3moe_full_dims;
+
+/* Workspace bytes k3moe_full_forward needs for T tokens (the layer's regions
+ * plus the block's z, a and shared intermediates and a 32 MiB GEMM scratch). */
+k3moe_status k3moe_full_workspace_bytes(const k3moe_config *cfg, const k3moe_full_dims *fd,
+                                        int32_t T_max, size_t *bytes);
+
+/* The full-width block, steps 1-6 above, asynchronous on `stream`:
+ *   h          [T][H] bf16
+ *   w_router   [E][H] bf16;  bias [E] f32 or NULL (selection only)
+ *   w_down     [d][H] bf16 (Wd);  w_up [H][d] bf16 (Wu)
+ *   expert_table, table_bytes: as k3moe_forward (packed at width d)
+ *   norm_gain  [d] f32 (NULL allowed when latent_norm == 0)
+ *   sh_w1, sh_w3 [SI][H] bf16;  sh_w2 [H][SI] bf16 (NULL when n_shared == 0)
+ *   idx, weight, offsets, perm: out, the routing, as k3moe_route writes it
+ *   out        [T][H] f32, written
+ * Matrices and h 16-byte aligned; expert_table 256-byte aligned.  The three
+ * dense projections run as bf16 GEMMs with fp32 accumulation (cuBLASLt, loaded
+ * at first use; K3MOE_ECUDA when it cannot be loaded or fails), so z, the
+ * normed a and the shared SiTU output are rounded to bf16 as their inputs.
+ * T may be 0 (offsets zeroed, nothing else written).  ws per
+ * k3moe_full_workspace_bytes(T_max >= T); its status word as k3moe_route's. */
+k3moe_status k3moe_full_forward(const k3moe_config *cfg, const k3moe_full_dims *fd, int32_t T,
+                                const uint16_t *h, const uint16_t *w_router, const float *bias,
+                                const uint16_t *w_down, const void *expert_table,
+                                size_t table_bytes, const float *norm_gain,
+                                const uint16_t *w_up, const uint16_t *sh_w1,
+                                const uint16_t *sh_w3, const uint16_t *sh_w2, int32_t *idx,
+                                float *weight, int32_t *offsets, int32_t *perm, float *out,
+                                void *ws, size_t ws_bytes, k3moe_stream stream);
+
 /* Synchronises `stream`, returns the device status word of `ws` in *code,
  * and clears it.  Returns K3MOE_EDEVICE when an error bit is set, K3MOE_OK
  * otherwise (the NAN_SCALE warning alone is OK). */

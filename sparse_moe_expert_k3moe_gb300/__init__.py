@@ -17,7 +17,8 @@ __all__ = [
     "k3moe_route", "k3moe_router_scores", "k3moe_forward", "k3moe_forward_noalloc", "k3moe_device_status",
     "k3moe_strerror",
     "k3moe_launch_count", "k3moe_timing_enable", "k3moe_timing_read", "k3moe_timing_reset",
-    "library_path", "MoELayer",
+    "library_path", "MoELayer", "K3MoEFullDims", "k3moe_full_dims", "k3moe_full_workspace_bytes",
+    "k3moe_full_forward", "MoEBlock",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,6 +35,10 @@ class K3MoEConfig(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("situ_b1", ctypes.c_float), ("situ_b2", ctypes.c_float),
                 ("renorm", ctypes.c_int32), ("routed_scale", ctypes.c_float)]
+
+
+class K3MoEFullDims(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("latent_norm", ctypes.c_int32), ("rms_eps", ctypes.c_float)]
 
 
 class K3MoEError(RuntimeError):
@@ -73,6 +78,11 @@ def lib():
             "k3moe_device_status": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32)]),
             "k3moe_forward_noalloc": (ctypes.c_int, [cp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp,
                                                      vp, vp, vp, vp]),
+            "k3moe_full_workspace_bytes": (ctypes.c_int, [cp, ctypes.POINTER(K3MoEFullDims), i32,
+                                                          ctypes.POINTER(sz)]),
+            "k3moe_full_forward": (ctypes.c_int, [cp, ctypes.POINTER(K3MoEFullDims), i32, vp, vp, vp, vp,
+                                                  vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                  sz, vp]),
             "k3moe_launch_count": (i64, []),
             "k3moe_timing_enable": (None, [i32]),
             "k3moe_timing_read": (i32, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i64),
@@ -190,6 +200,29 @@ def k3moe_forward_noalloc(cfg, T, x, idx, weight, offsets, perm, expert_table, s
         _ptr(status_out), _stream(stream)))
 
 
+def k3moe_full_dims(hidden, latent_norm=1, rms_eps=1e-5) -> K3MoEFullDims:
+    return K3MoEFullDims(hidden, latent_norm, rms_eps)
+
+
+def k3moe_full_workspace_bytes(cfg: K3MoEConfig, fd: K3MoEFullDims, T_max: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("k3moe_full_workspace_bytes", lib().k3moe_full_workspace_bytes(
+        ctypes.byref(cfg), ctypes.byref(fd), T_max, ctypes.byref(out)))
+    return out.value
+
+
+def k3moe_full_forward(cfg, fd, T, h, w_router, bias, w_down, expert_table, norm_gain, w_up, sh_w1,
+                       sh_w3, sh_w2, idx, weight, offsets, perm, out, ws, ws_bytes=None,
+                       table_bytes=None, stream=None):
+    wb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    tb = table_bytes if table_bytes is not None else expert_table.numel() * expert_table.element_size()
+    _check("k3moe_full_forward", lib().k3moe_full_forward(
+        ctypes.byref(cfg), ctypes.byref(fd), T, _ptr(h), _ptr(w_router), _ptr(bias), _ptr(w_down),
+        _ptr(expert_table), tb, _ptr(norm_gain), _ptr(w_up), _ptr(sh_w1), _ptr(sh_w3), _ptr(sh_w2),
+        _ptr(idx), _ptr(weight), _ptr(offsets), _ptr(perm), _ptr(out), _ptr(ws), wb,
+        _stream(stream)))
+
+
 def k3moe_device_status(ws, stream=None):
     """(status, code): synchronises the stream, reads and clears the device status word."""
     code = ctypes.c_int32(0)
@@ -219,7 +252,26 @@ def k3moe_timing_reset():
     lib().k3moe_timing_reset()
 
 
-# ----------------------------------------------------------------------------- convenience holder
+# ----------------------------------------------------------------------------- convenience holders
+
+def _capture(call, x, out):
+    """call(x, out) recorded as a CUDA graph on x's device.  One eager call on a side
+    stream first settles the library's cached launch attributes and GEMM plans, so that
+    capture itself only enqueues work.  The graph reads x and writes out, the routing
+    buffers and the workspace where they are now: copy the next tokens into x, then
+    replay().  The library's launches keep their programmatic dependencies as graph edges."""
+    import torch
+    cur = torch.cuda.current_stream(x.device)
+    side = torch.cuda.Stream(device=x.device)
+    side.wait_stream(cur)
+    with torch.cuda.stream(side):
+        call(x, out)
+    cur.wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(x, out)
+    return g
+
 
 class MoELayer:
     """Holds one layer's device tensors (packed expert table, router, bias,
@@ -276,19 +328,49 @@ class MoELayer:
 
     def capture(self, x, out):
         """Record route + forward on the fixed buffers x [T][d] bf16 and out [T][d] f32 as
-        a CUDA graph and return the torch.cuda.CUDAGraph.  One eager call on a side stream
-        first settles the library's cached launch attributes, so that capture itself only
-        enqueues kernels.  The graph reads x and writes out, idx, weight, offsets, perm
-        and the workspace where they are now: copy the next tokens into x, then replay().
-        The launches keep their programmatic dependencies as graph edges."""
+        a CUDA graph and return the torch.cuda.CUDAGraph (see _capture)."""
+        return _capture(self, x, out)
+
+
+class MoEBlock:
+    """Holds one full-width block's device tensors (the routed experts' packed table,
+    the full-width router, the down and up projections, the norm gain and the fused
+    shared experts) and a workspace, and calls k3moe_full_forward.  Allocation is
+    torch's; every computation is the library's (and cuBLASLt's, for the three dense
+    projections)."""
+
+    def __init__(self, cfg: K3MoEConfig, fd: K3MoEFullDims, T_max: int, device="cuda"):
         import torch
-        cur = torch.cuda.current_stream(self.device)
-        side = torch.cuda.Stream(device=self.device)
-        side.wait_stream(cur)
-        with torch.cuda.stream(side):
-            self(x, out)
-        cur.wait_stream(side)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            self(x, out)
-        return g
+        self.cfg, self.fd = cfg, fd
+        self.device = torch.device(device)
+        self.T_max = T_max
+        self.table = torch.empty(k3moe_packed_bytes(cfg), dtype=torch.uint8, device=self.device)
+        self.ws_bytes = k3moe_full_workspace_bytes(cfg, fd, T_max)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        self.w_router = self.bias = self.w_down = self.w_up = self.gain = None
+        self.sh_w1 = self.sh_w3 = self.sh_w2 = None
+        E, k = cfg.n_experts, cfg.top_k
+        self.idx = torch.empty((T_max, k), dtype=torch.int32, device=self.device)
+        self.weight = torch.empty((T_max, k), dtype=torch.float32, device=self.device)
+        self.offsets = torch.empty(E + 1, dtype=torch.int32, device=self.device)
+        self.perm = torch.empty(T_max * k, dtype=torch.int32, device=self.device)
+
+    def pack_experts(self, expert_lo, n, w1_packed, w1_scale, w3_packed, w3_scale, w2_packed,
+                     w2_scale, stream=None):
+        k3moe_pack_mxfp4(self.cfg, expert_lo, n, w1_packed, w1_scale, w3_packed, w3_scale,
+                         w2_packed, w2_scale, self.table, ws=self.ws, stream=stream)
+
+    def forward(self, h, out, stream=None):
+        T = h.shape[0]
+        k3moe_full_forward(self.cfg, self.fd, T, h, self.w_router, self.bias, self.w_down,
+                           self.table, self.gain, self.w_up, self.sh_w1, self.sh_w3, self.sh_w2,
+                           self.idx, self.weight, self.offsets, self.perm, out, self.ws,
+                           self.ws_bytes, stream=stream)
+        return out
+
+    __call__ = forward
+
+    def capture(self, h, out):
+        """k3moe_full_forward on the fixed buffers h [T][H] and out [T][H] as a CUDA graph
+        (see _capture)."""
+        return _capture(self, h, out)

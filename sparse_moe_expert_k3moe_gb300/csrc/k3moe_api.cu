@@ -240,6 +240,69 @@ k3moe_status k3moe_forward(const k3moe_config *cfg, int32_t T, const uint16_t *x
     return e == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 
+static k3moe_status check_full(const k3moe_config *cfg, const k3moe_full_dims *fd)
+{
+    k3moe_status st = check_config(cfg);
+    if (st != K3MOE_OK) return st;
+    if (!fd || fd->hidden <= 0 || (fd->latent_norm != 0 && fd->latent_norm != 1) ||
+        !finite_pos(fd->rms_eps))
+        return K3MOE_EINVAL;
+    if (fd->hidden % kTileK || fd->hidden > kMaxWidth) return K3MOE_ESHAPE;
+    return K3MOE_OK;
+}
+
+k3moe_status k3moe_full_workspace_bytes(const k3moe_config *cfg, const k3moe_full_dims *fd,
+                                        int32_t T_max, size_t *bytes)
+{
+    k3moe_status st = check_full(cfg, fd);
+    if (st != K3MOE_OK) return st;
+    if (!bytes) return K3MOE_EINVAL;
+    if (T_max < 0 || T_max > kMaxT) return K3MOE_ESHAPE;
+    *bytes = full_layout(*cfg, fd->hidden, T_max).total;
+    return K3MOE_OK;
+}
+
+k3moe_status k3moe_full_forward(const k3moe_config *cfg, const k3moe_full_dims *fd, int32_t T,
+                                const uint16_t *h, const uint16_t *w_router, const float *bias,
+                                const uint16_t *w_down, const void *expert_table,
+                                size_t table_bytes, const float *norm_gain,
+                                const uint16_t *w_up, const uint16_t *sh_w1,
+                                const uint16_t *sh_w3, const uint16_t *sh_w2, int32_t *idx,
+                                float *weight, int32_t *offsets, int32_t *perm, float *out,
+                                void *ws, size_t ws_bytes, k3moe_stream stream)
+{
+    k3moe_status st = check_full(cfg, fd);
+    if (st != K3MOE_OK) return st;
+    if (T < 0 || T > kMaxT) return K3MOE_ESHAPE;
+    if (!offsets) return K3MOE_EINVAL;
+    if (!ws || !aligned(ws, 256)) return K3MOE_EWORKSPACE;
+    const FullLayout F = full_layout(*cfg, fd->hidden, T);
+    if (ws_bytes < F.total) return K3MOE_EWORKSPACE;
+    if (T == 0) {
+        // no tokens: the routing is empty, exactly as k3moe_route leaves it
+        cudaError_t e = launch_route(F.cr, 0, h, w_router, bias, idx, weight, offsets, perm,
+                                     static_cast<uint8_t *>(ws), F.route, (cudaStream_t)stream);
+        return e == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+    }
+    if (!h || !w_router || !w_down || !expert_table || !w_up || !idx || !weight || !perm || !out ||
+        (fd->latent_norm && !norm_gain))
+        return K3MOE_EINVAL;
+    if (cfg->n_shared > 0 && (!sh_w1 || !sh_w3 || !sh_w2)) return K3MOE_EINVAL;
+    if (!aligned(h, 16) || !aligned(w_router, 16) || !aligned(w_down, 16) || !aligned(w_up, 16) ||
+        !aligned(out, 16) || !aligned(expert_table, 256) || !aligned(idx, 4) || !aligned(weight, 4) ||
+        !aligned(offsets, 4) || !aligned(perm, 4) || (bias && !aligned(bias, 4)) ||
+        (norm_gain && !aligned(norm_gain, 4)))
+        return K3MOE_EALIGN;
+    if (cfg->n_shared > 0 && (!aligned(sh_w1, 16) || !aligned(sh_w3, 16) || !aligned(sh_w2, 16)))
+        return K3MOE_EALIGN;
+    if (table_bytes < packed_table_bytes(cfg->n_experts, cfg->d, cfg->f)) return K3MOE_ESHAPE;
+    cudaError_t e = launch_full(*cfg, fd->hidden, fd->latent_norm, fd->rms_eps, T, h, w_router, bias,
+                                w_down, static_cast<const uint8_t *>(expert_table), norm_gain, w_up,
+                                sh_w1, sh_w3, sh_w2, idx, weight, offsets, perm, out,
+                                static_cast<uint8_t *>(ws), F, (cudaStream_t)stream);
+    return e == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+}
+
 k3moe_status k3moe_device_status(void *ws, k3moe_stream stream, int32_t *code)
 {
     if (!ws || !aligned(ws, 256) || !code) return K3MOE_EINVAL;

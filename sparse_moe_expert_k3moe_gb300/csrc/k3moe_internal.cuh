@@ -165,6 +165,45 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     return L;
 }
 
+// Full-width block (k3moe_full_forward).  Its router call reads the full-width token (a
+// config whose d is the hidden width H), its expert call runs the layer on the latent
+// with no shared experts (they run on the full width here).  The two calls run one after
+// the other and share the layer's regions; the block's own buffers follow them.
+constexpr size_t kLtWorkspace = 32u << 20;       // cuBLASLt scratch
+struct FullLayout {
+    k3moe_config cr, cl;         // router config (d = H), latent config (n_shared = 0)
+    WsLayout route, latent;
+    size_t z;                    // [T][d] bf16: the token projected into the latent
+    size_t acc;                  // [T][d] f32: the experts' weighted sum
+    size_t y;                    // [T][d] bf16: the normed sum, the up projection's input
+    size_t gate, up;             // [T][S*f] f32: shared gate and up projections
+    size_t act;                  // [T][S*f] bf16: their SiTU
+    size_t lt;                   // cuBLASLt scratch
+    size_t total;
+};
+
+inline FullLayout full_layout(const k3moe_config &c, int hidden, int T)
+{
+    FullLayout F{};
+    F.cr = c;
+    F.cr.d = hidden;
+    F.cl = c;
+    F.cl.n_shared = 0;
+    F.route = ws_layout(F.cr, T);
+    F.latent = ws_layout(F.cl, T);
+    const size_t td = (size_t)T * c.d, ts = (size_t)T * c.n_shared * c.f;
+    size_t o = align256(F.route.total > F.latent.total ? F.route.total : F.latent.total);
+    F.z = o; o = align256(o + td * 2);
+    F.acc = o; o = align256(o + td * 4);
+    F.y = o; o = align256(o + td * 2);
+    F.gate = o; o = align256(o + ts * 4);
+    F.up = o; o = align256(o + ts * 4);
+    F.act = o; o = align256(o + ts * 2);
+    F.lt = o; o = align256(o + kLtWorkspace);
+    F.total = o;
+    return F;
+}
+
 // ----------------------------------------------------------------------------------- programmatic dependent launch
 // Every kernel of the route and forward chains starts with pdl_wait(): it waits until the
 // previous kernel in the stream has completed and its writes are visible, before touching
@@ -220,6 +259,13 @@ cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x,
                                 const uint8_t *table, const uint16_t *sh_w1, const uint16_t *sh_w3,
                                 const uint16_t *sh_w2, float *out, uint8_t *ws, const WsLayout &L,
                                 cudaStream_t s);
+// The full-width block (k3moe_full_forward), all six steps on stream s.
+cudaError_t launch_full(const k3moe_config &c, int hidden, int latent_norm, float rms_eps, int T,
+                        const uint16_t *h, const uint16_t *wr, const float *bias, const uint16_t *wd,
+                        const uint8_t *table, const float *gain, const uint16_t *wu,
+                        const uint16_t *sh1, const uint16_t *sh3, const uint16_t *sh2, int32_t *idx,
+                        float *weight, int32_t *offsets, int32_t *perm, float *out, uint8_t *ws,
+                        const FullLayout &F, cudaStream_t s);
 // Either path, as the layout chose it.
 inline cudaError_t launch_forward(const k3moe_config &c, int T, const uint16_t *x, const int32_t *idx,
                                   const float *weight, const int32_t *offsets, const int32_t *perm,

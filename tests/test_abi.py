@@ -114,3 +114,35 @@ def test_host_validation_rejects_before_launch(k3):
     assert L.k3moe_pack_mxfp4(ctypes.byref(cfg), 0, 1, vp(A + 8), *([vp(A)] * 5), vp(A), big,
                               None, None) == 3
     assert k3.k3moe_strerror(4).startswith("workspace")
+
+
+def test_full_block_validation_and_sizes(k3):
+    cfg = k3_cfg(k3)
+    fd = k3.k3moe_full_dims(7168)
+    w1 = k3.k3moe_full_workspace_bytes(cfg, fd, 1)
+    w4096 = k3.k3moe_full_workspace_bytes(cfg, fd, 4096)
+    assert k3.k3moe_workspace_bytes(cfg, 1) + (32 << 20) < w1 < w4096
+    # the block's own buffers at T = 4096: z, a, y at width d; gate, up, act at S*f
+    assert w4096 >= 4096 * (3584 * (2 + 4 + 2) + 2 * 3072 * (4 + 4 + 2)) + (32 << 20)
+    for bad, code in ((dict(hidden=0), 1), (dict(latent_norm=2), 1), (dict(rms_eps=0.0), 1),
+                      (dict(rms_eps=float("nan")), 1), (dict(hidden=7000), 2), (dict(hidden=16384), 2)):
+        kw = dict(hidden=7168, latent_norm=1, rms_eps=1e-5)
+        kw.update(bad)
+        with pytest.raises(k3.K3MoEError) as ei:
+            k3.k3moe_full_workspace_bytes(cfg, k3.k3moe_full_dims(**kw), 4)
+        assert ei.value.status == code, bad
+    L = k3.lib()
+    vp = ctypes.c_void_p
+    A = 0x10000000  # fake, 256-aligned addresses: never dereferenced on the host
+    big = 1 << 40
+
+    def call(h=A, gain=A, ws=A, ws_bytes=big, fdim=fd):
+        return L.k3moe_full_forward(ctypes.byref(cfg), ctypes.byref(fdim), 4, vp(h), vp(A), None, vp(A),
+                                    vp(A), big, vp(gain) if gain else None, vp(A), vp(A), vp(A), vp(A),
+                                    vp(A), vp(A), vp(A), vp(A), vp(A), vp(ws) if ws else None,
+                                    ws_bytes, None)
+    assert call(h=A + 2) == 3                         # misaligned tokens
+    assert call(gain=0) == 1                          # the norm needs its gain
+    assert call(ws=0) == 4                            # no workspace
+    assert call(ws_bytes=1024) == 4                   # workspace too small
+    assert call(fdim=k3.k3moe_full_dims(7168, rms_eps=-1.0)) == 1
