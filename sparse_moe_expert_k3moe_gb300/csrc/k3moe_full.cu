@@ -140,12 +140,13 @@ Lt &lt()
     return L;
 }
 
-// One GEMM shape's descriptors and chosen algorithm, made once and kept.
+// One GEMM shape's descriptors and chosen algorithm, made once and kept (one plan per
+// distinct token count T, a few hundred bytes each).
 struct Plan {
     cublasLtMatmulDesc_t op = nullptr;
     cublasLtMatrixLayout_t a = nullptr, b = nullptr, d = nullptr;
     cublasLtMatmulAlgo_t algo{};
-    bool ok = false;
+    bool made = false, ok = false;
 };
 
 // D [n][m] (row-major) = B [n][k] . A^T (+ D when accumulate): each of the n token rows
@@ -162,7 +163,8 @@ cudaError_t lt_gemm(int m, int n, int k, const uint16_t *A, const uint16_t *B, v
     {
         std::lock_guard<std::mutex> lk(mu);
         p = &plans[std::make_tuple(m, n, k, d_f32, accumulate)];
-        if (!p->ok) {
+        if (!p->made) {
+            p->made = true;
             const cudaDataType_t dt = d_f32 ? CUDA_R_32F : CUDA_R_16BF;
             const cublasOperation_t opT = CUBLAS_OP_T, opN = CUBLAS_OP_N;
             bool ok = L.desc_create(&p->op, CUBLAS_COMPUTE_32F, CUDA_R_32F) == CUBLAS_STATUS_SUCCESS &&
@@ -181,11 +183,11 @@ cudaError_t lt_gemm(int m, int n, int k, const uint16_t *A, const uint16_t *B, v
             ok = ok && L.heuristic(L.handle, p->op, p->a, p->b, p->d, p->d, pref, 1, &res, &nres) ==
                            CUBLAS_STATUS_SUCCESS && nres > 0;
             if (pref) L.pref_destroy(pref);
-            if (!ok) return cudaErrorNotSupported;
             p->algo = res.algo;
-            p->ok = true;
+            p->ok = ok;
         }
     }
+    if (!p->ok) return cudaErrorNotSupported;
     const float alpha = 1.0f, beta = accumulate ? 1.0f : 0.0f;
     timing_begin(name, s);
     const cublasStatus_t st = L.matmul(L.handle, p->op, &alpha, A, p->a, B, p->b, &beta, D, p->d, D, p->d,
