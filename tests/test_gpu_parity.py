@@ -508,3 +508,34 @@ def test_full_block_parity(k3, w):
     blk.forward(dev16(h[:0]), out[:0])
     torch.cuda.synchronize()
     assert not host(blk.offsets).any()
+
+
+def test_block_graph_replay(k3):
+    """The full-width block (its cuBLASLt projections included) captured as one CUDA
+    graph: a replay repeats the eager call, and a replay on new tokens copied into the
+    same input buffer matches the oracle's block."""
+    from k3moe_inputs.device import build_block
+    w = ki.WORKLOADS["full_tiny"].with_(name="full_graph", T=3, seed=85)
+    blk = build_block(w)
+    hd = dev16(ki.make_h(w))
+    out_eager = torch.empty((w.T, w.hidden), dtype=torch.float32, device="cuda")
+    blk(hd, out_eager)
+    out = torch.zeros_like(out_eager)
+    graph = blk.capture(hd, out)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(host(out), host(out_eager), rtol=1e-6,
+                               atol=1e-6 * float(np.abs(host(out_eager)).max()))
+    h2 = ki.make_h(w.with_(seed=w.seed + 1000))
+    hd.copy_(dev16(h2))
+    graph.replay()
+    torch.cuda.synchronize()
+    rc, code = k3.k3moe_device_status(blk.ws)
+    assert rc == 0 and code == 0
+    gidx, gw = host(blk.idx)[:w.T], host(blk.weight)[:w.T]
+    full = ki.make_full(w)
+    shared = {"w1": full["sh1"], "w3": full["sh3"], "w2": full["sh2"]}
+    ref = oracle.forward_full(ocfg(w), w.hidden, w.latent_norm, w.rms_eps, h2, gidx, gw, full["down"],
+                              oracle_experts(w, gidx.ravel()), full["gain"], full["up"], shared)
+    assert_out_close(host(out), ref, w.name + " replayed on new tokens")
