@@ -231,8 +231,9 @@ typedef struct k3moe_full_dims {
     float rms_eps;        /* > 0 and finite */
 } k3moe_full_dims;
 
-/* Workspace bytes k3moe_full_forward needs for T tokens (the layer's regions
- * plus the block's z, a and shared intermediates and a 32 MiB GEMM scratch). */
+/* Workspace bytes k3moe_full_forward needs for any 0 <= T <= T_max (the
+ * layer's regions plus the block's z, a and shared intermediates and a 32 MiB
+ * GEMM scratch). */
 k3moe_status k3moe_full_workspace_bytes(const k3moe_config *cfg, const k3moe_full_dims *fd,
                                         int32_t T_max, size_t *bytes);
 

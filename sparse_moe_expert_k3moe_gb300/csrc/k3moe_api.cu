@@ -1,6 +1,7 @@
 // k3moe_api.cu -- the C ABI entry points: argument validation, workspace
 // layout, path choice, launch accounting and timing.  Kernels live in the other
 // files; nothing here computes on the host beyond bookkeeping.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -85,6 +86,22 @@ static k3moe_status check_config(const k3moe_config *c)
 
 static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+// The largest workspace any 0 <= T <= T_max needs.  Sizes grow with T within each
+// forward path, with two exceptions: a single token on the mat-vec path also holds the
+// split shared-expert partials, and the first T of the tensor-core path can need less
+// than the last T of the mat-vec path.  So the maximum is at T = 1, at the last mat-vec
+// T, or at T_max.  total(T) is the layout size of one call with T tokens.
+template <typename Total>
+static size_t max_total(const k3moe_config &c, int32_t T_max, Total total)
+{
+    size_t m = total(T_max);
+    if (T_max >= 1) m = std::max(m, total(1));
+    const int64_t first_gemm = std::max<int64_t>(32, (8LL * c.n_experts + c.top_k - 1) / c.top_k);
+    const int64_t last_gemv = std::min<int64_t>(T_max, first_gemm - 1);
+    if (last_gemv >= 1) m = std::max(m, total((int32_t)last_gemv));
+    return m;
+}
+
 static const int32_t kMaxT = 1 << 20;
 
 }  // namespace k3moe
@@ -122,7 +139,7 @@ k3moe_status k3moe_workspace_bytes(const k3moe_config *cfg, int32_t T_max, size_
     if (st != K3MOE_OK) return st;
     if (!bytes) return K3MOE_EINVAL;
     if (T_max < 0 || T_max > kMaxT) return K3MOE_ESHAPE;
-    *bytes = ws_layout(*cfg, T_max).total;
+    *bytes = max_total(*cfg, T_max, [&](int32_t T) { return ws_layout(*cfg, T).total; });
     return K3MOE_OK;
 }
 
@@ -258,7 +275,7 @@ k3moe_status k3moe_full_workspace_bytes(const k3moe_config *cfg, const k3moe_ful
     if (st != K3MOE_OK) return st;
     if (!bytes) return K3MOE_EINVAL;
     if (T_max < 0 || T_max > kMaxT) return K3MOE_ESHAPE;
-    *bytes = full_layout(*cfg, fd->hidden, T_max).total;
+    *bytes = max_total(*cfg, T_max, [&](int32_t T) { return full_layout(*cfg, fd->hidden, T).total; });
     return K3MOE_OK;
 }
 

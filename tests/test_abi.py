@@ -146,3 +146,20 @@ def test_full_block_validation_and_sizes(k3):
     assert call(ws=0) == 4                            # no workspace
     assert call(ws_bytes=1024) == 4                   # workspace too small
     assert call(fdim=k3.k3moe_full_dims(7168, rms_eps=-1.0)) == 1
+
+
+@pytest.mark.parametrize("kw", [
+    dict(),                                                          # K3: mat-vec path below T = 448
+    dict(d=256, f=128, n_experts=32, top_k=4, n_shared=1),
+    dict(d=256, f=8192, n_experts=8, top_k=1, n_shared=8),          # big split partials at T = 1
+])
+def test_workspace_covers_every_smaller_t(k3, kw):
+    """k3moe_workspace_bytes(T_max) serves every call with T <= T_max, so it never
+    shrinks as T_max grows, across the switch from the mat-vec to the tensor-core path
+    (where one call's own layout does shrink)."""
+    cfg = k3_cfg(k3, **kw)
+    fd = k3.k3moe_full_dims(512)
+    for size in (lambda T: k3.k3moe_workspace_bytes(cfg, T),
+                 lambda T: k3.k3moe_full_workspace_bytes(cfg, fd, T)):
+        sizes = [size(T) for T in range(0, 600)]
+        assert all(b >= a for a, b in zip(sizes, sizes[1:]))
