@@ -1,4 +1,5 @@
-"""Routed-expert layer of a Kimi-K3-style latent MoE on GB300 (sm_103a).
+"""Routed-expert layer of a Kimi-K3-style latent MoE on GB300 (sm_103a), and the
+full-width Stable LatentMoE block around it (``k3moe_full_forward``, ``MoEBlock``).
 
 A thin ctypes binding over ``libk3moe.so``; every function has the name of the C
 entry point it calls (``include/k3moe.h``) and only marshals arguments: torch
