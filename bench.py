@@ -1,20 +1,26 @@
 """Throughput of the routed-expert layer (route + forward) on GB300.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAMES] [--impl reference]
 
 A step is one pass of the whole layer -- k3moe_route then k3moe_forward -- over one
 batch of T synthetic tokens whose weights and activations are already resident in
 HBM.  The 129 MB L2 is flushed between steps (a 512 MiB buffer is written outside
 the timed events).  value = tokens processed by all ranks / the slowest rank's summed
-step time (CUDA events on the launching stream).  e2e times the same step through the
-C ABI from pinned host memory: H2D of x, route, forward, D2H of out.
+step time (CUDA events on the launching stream).  e2e times the same step end to end:
+torch copies x from pinned host memory to the device, the two C-ABI calls run, and out
+is copied back to pinned host memory, all inside the timed events.
+
+--workload takes a comma-separated list; the default, decode_t1,prefill_t4096, is the
+headline pair (T = 1 and T = 4096 at the K3 shape).  The first workload's record is the
+JSON line's top level; every other workload's complete record sits under a key named
+after it.
 
 With N > 1 (torchrun, one process per GPU) every rank runs an independent replica of
 the layer: the path has no exchange step on one GPU, so there is no collective in the
 data path; a barrier and a max-reduction of the timings bracket the run.
 
 --impl reference times the CPU oracle (oracle/, fp64 C) on this host's cores on a
-bounded sample of the same workload, as the reference arm.
+bounded sample of the same workloads, as the reference arm.
 """
 from __future__ import annotations
 
@@ -35,6 +41,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s at T=1 and T=4096 on 1 GB300; % of HBM/tensor roofline"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+DEFAULT_WORKLOADS = "decode_t1,prefill_t4096"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -44,7 +51,8 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default="decode_t1")
+    p.add_argument("--workload", default=DEFAULT_WORKLOADS,
+                   help="comma-separated workloads; the first is the line's top-level record")
     p.add_argument("--impl", default="k3moe", choices=["k3moe", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -131,7 +139,7 @@ def full_kernel_work(name: str, w, distinct_experts: int):
         return SI * H * 2 + T * H * 2 + T * SI * 4, 2 * T * SI * H
     if name == "full_shared_down_gemm":
         return H * SI * 2 + T * SI * 2 + 2 * T * H * 4, 2 * T * H * SI
-    if name in ("router_scores", "router_scores_tc"):
+    if name in ("router_scores", "router_logits_tc", "router_wnorm"):
         return kernel_work(name, w.with_(d=H, hidden=0), distinct_experts)
     if name in ("gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down"):
         return kernel_work(name, w.with_(S=0, hidden=0), distinct_experts)
@@ -141,7 +149,8 @@ def full_kernel_work(name: str, w, distinct_experts: int):
 def kernel_work(name: str, w, distinct_experts: int):
     """Algorithmic (bytes, FLOPs) of one launch of a forward kernel: the bytes it must
     move and the multiply-adds (x2) it must do.
-    router_scores(_tc): Wr and x in, sc and ch out (f32); 2*T*E*d FLOPs.
+    router_scores: Wr and x in, sc and ch out (f32); router_logits_tc: Wr and x in, the
+    logits out (f32); 2*T*E*d FLOPs each.  router_wnorm: Wr in.
     gemv_gateup / gemm_gateup: W1, W3 of the distinct routed experts (packed MXFP4,
     17/32 byte per weight) and of the shared experts (bf16), the activations in (x;
     the gathered f16 copy on the GEMM path) and h out (f16 for routed rows; on the
@@ -153,8 +162,12 @@ def kernel_work(name: str, w, distinct_experts: int):
     rows = w.T * w.k + w.S * w.T
     slots = w.T * w.k
     h_gemv = slots * w.f * 2 + w.S * w.T * w.f * 4
-    if name in ("router_scores", "router_scores_tc"):
+    if name == "router_scores":
         return w.E * w.d * 2 + w.T * w.d * 2 + 2 * w.T * w.E * 4, 2 * w.T * w.E * w.d
+    if name == "router_logits_tc":
+        return w.E * w.d * 2 + w.T * w.d * 2 + w.T * w.E * 4, 2 * w.T * w.E * w.d
+    if name == "router_wnorm":
+        return w.E * w.d * 2, 2 * w.E * w.d
     if name == "gemv_gateup":
         return (distinct_experts * 2 * w.f * w.d * 17 // 32 + w.S * 2 * w.f * w.d * 2
                 + w.T * w.d * 2 + h_gemv), 2 * rows * 2 * w.f * w.d
@@ -193,15 +206,22 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def csrc_hash():
-    """Hash of the kernel sources: every file of csrc/ but k3moe_api.cu, which holds only
-    host-side validation, workspace sizing and accounting.  A recorded DRAM traffic
-    figure is reported only while this matches the hash taken with it."""
+# Sources each timed kernel is compiled from (besides the shared k3moe_internal.cuh).
+KERNEL_SOURCES = {
+    "gemv_gateup": ["k3moe_gemv.cu"], "gemv_down": ["k3moe_gemv.cu"],
+    "gemm_gateup": ["k3moe_gemm.cu", "k3moe_tc.cuh"], "gemm_down": ["k3moe_gemm.cu", "k3moe_tc.cuh"],
+    "router_logits_tc": ["k3moe_route_tc.cu", "k3moe_tc.cuh"],
+}
+
+
+def csrc_hash(kernel: str):
+    """Hash of the sources a kernel is built from (its file and the headers it includes).
+    A recorded DRAM traffic figure is reported only while this matches the hash taken
+    with it."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "sparse_moe_expert_k3moe_gb300", "csrc", "*"))):
-        if os.path.basename(p) == "k3moe_api.cu":
-            continue
-        with open(p, "rb") as fh:
+    csrc = os.path.join(ROOT, "sparse_moe_expert_k3moe_gb300", "csrc")
+    for name in sorted(KERNEL_SOURCES.get(kernel, [])) + ["k3moe_internal.cuh"]:
+        with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -213,7 +233,7 @@ def traffic_for(kernel: str, workload: str):
         with open(TRAFFIC_FILE) as fh:
             tr = json.load(fh)
         ent = tr[workload][kernel]
-        if ent.get("csrc_hash") != csrc_hash():
+        if ent.get("csrc_hash") != csrc_hash(kernel):
             return None
         return float(ent["dram_bytes_per_launch"])
     except Exception:
@@ -277,9 +297,9 @@ class ClockSampler:
 
 def time_oracle(w, budget_s: float):
     """Route + forward of the oracle on this host's cores over a bounded sample of the
-    workload: its tokens in order, cycling back to the first when a small workload (T=1)
-    is used up, until budget_s seconds of oracle work; returns (tokens/s, tokens timed,
-    threads, seconds)."""
+    workload: its first tokens (one batch of as many tokens as the oracle has threads, at
+    most 16), cycled until budget_s seconds of oracle work, so that the routed experts
+    they use are drawn once; returns (tokens/s, tokens timed, threads, seconds)."""
     import numpy as np
     import k3moe_inputs as ki
     import oracle
@@ -301,83 +321,90 @@ def time_oracle(w, budget_s: float):
 
         def run(xs, idx, wt):
             oracle.forward(c, xs, idx, wt, experts, shared)
-    experts = {}
+    batch = max(1, min(w.T, oracle.num_threads(), 16))
+    xs = np.ascontiguousarray(x[:batch])
+    idx, wt, _ = oracle.route(c_route, xs, Wr, bias)        # untimed draw of the needed experts
+    experts = {e: ki.make_expert(w, e) for e in sorted(set(idx.ravel().tolist()))}
     done, spent = 0, 0.0
-    batch = max(1, min(w.T, oracle.num_threads()))
     while spent < budget_s:
-        rows = [(done + i) % w.T for i in range(batch)]
-        xs = np.ascontiguousarray(x[rows])
-        idx, wt, _ = oracle.route(c_route, xs, Wr, bias)  # untimed draw of the needed experts
-        for e in set(idx.ravel().tolist()) - set(experts):
-            experts[e] = ki.make_expert(w, e)
         t0 = time.perf_counter()
         idx, wt, _ = oracle.route(c_route, xs, Wr, bias)
         run(xs, idx, wt)
         spent += time.perf_counter() - t0
-        done += len(rows)
-        if len(experts) > 256:
-            experts.clear()
+        done += batch
     return done / spent, done, oracle.num_threads(), spent
 
 
 def reference_arm(args):
-    import k3moe_inputs as ki
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = workload_from(args.workload)
     import oracle
     oracle.build()
+    specs = [sp for sp in args.workload.split(",") if sp]
     per_step = max(2.0, args.cpu_budget_s / max(1, args.steps))
-    for _ in range(args.warmup):
-        time_oracle(w.with_(T=1), 0.1)
-    tot_tok, tot_s = 0, 0.0
-    threads = oracle.num_threads()
-    for _ in range(args.steps):
-        tps, n, threads, s = time_oracle(w, per_step)
-        tot_tok += n
-        tot_s += s
-    value = tot_tok / tot_s
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000.0 * tot_s / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "top_k": w.k,
-                   "n_shared": w.S},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{tot_tok} tokens of {w.name} over {args.steps} steps "
-                                   f"(each step <= {per_step:.1f} s of oracle work)"},
-        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
+    records = []
+    for spec in specs:
+        w = workload_from(spec)
+        for _ in range(args.warmup):
+            time_oracle(w.with_(T=1), 0.1)
+        tot_tok, tot_s = 0, 0.0
+        threads = oracle.num_threads()
+        for _ in range(args.steps):
+            tps, n, threads, s = time_oracle(w, per_step)
+            tot_tok += n
+            tot_s += s
+        value = tot_tok / tot_s
+        records.append({
+            "value": value, "unit": "tokens/s", "ms_per_step": 1000.0 * tot_s / args.steps,
+            "dtype": "f64",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "top_k": w.k,
+                       "n_shared": w.S},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{tot_tok} tokens of {w.name} (its first tokens, cycled) over "
+                                       f"{args.steps} steps (each step <= {per_step:.1f} s of oracle work)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        })
+    line = {"impl": "reference", "metric": METRIC, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "data": "synthetic", **records[0]}
+    for spec, rec in zip(specs[1:], records[1:]):
+        line[rec["config"]["workload"]] = rec
     print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def gpu_arm(args):
+ARITHMETIC = ("router: exact logits (bf16 products exact in fp32, two-sum compensated "
+              "accumulation, one rounding), sigmoid from a double exp rounded to float; experts: "
+              "MMA operands f16 (tokens x*2^-u, routed h; MXFP4 weights decoded exactly to f16) "
+              "and bf16 (shared-expert weights, shared h), fp32 accumulation; output f32")
+
+
+def near_tie_counts(layer, x, w):
+    """From the device's exact router scores (k3moe_router_scores, every expert of every
+    token): tokens whose k-th and (k+1)-th choice scores differ by less than 1e-6 without
+    being equal, and tokens where they are exactly equal (decided by the lower index)."""
+    import numpy as np
+    if w.E <= w.k:
+        return {"tokens": w.T, "gap_below_1e-6": 0, "exact_ties": 0}
+    _, ch = layer.scores(x)
+    top = -np.sort(-np.partition(ch.cpu().numpy(), w.E - w.k - 1, axis=1)[:, w.E - w.k - 1:], axis=1)
+    gap = top[:, w.k - 1].astype(np.float64) - top[:, w.k].astype(np.float64)
+    return {"tokens": w.T, "gap_below_1e-6": int(((gap > 0) & (gap < 1e-6)).sum()),
+            "exact_ties": int((gap == 0).sum()),
+            "from": "the device's exact scores (k3moe_router_scores)"}
+
+
+def measure(w, args, rank, world, local, dev):
+    """One workload: the timed steps, the per-kernel pass, e2e, the near-tie count and
+    (rank 0, N = 1) the CPU baseline; returns the record (rank 0) or None."""
     import numpy as np
     import torch
     import k3moe_inputs as ki
     from k3moe_inputs.device import build_layer
     import sparse_moe_expert_k3moe_gb300 as k3
-    from sparse_moe_expert_k3moe_gb300 import build as kbuild
 
-    rank, world, local = dist_env()
-    kbuild.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    def barrier():
-        dist_barrier(world)
-
-    def allmax(v: float) -> float:
-        return dist_max(v, world, dev)
-
-    w = workload_from(args.workload)
     width = w.hidden or w.d                                   # token width in and out
     if w.hidden:
         from k3moe_inputs.device import build_block
@@ -421,7 +448,7 @@ def gpu_arm(args):
           for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
-    barrier()
+    dist_barrier(world)
     torch.cuda.synchronize(dev)
     n0 = k3.k3moe_launch_count()
     host_s = 0.0
@@ -433,13 +460,13 @@ def gpu_arm(args):
         host_s += time.perf_counter() - h0
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    barrier()
+    dist_barrier(world)
     launches = k3.k3moe_launch_count() - n0
     if graph_launches is not None:
         launches = graph_launches * args.steps
     clk = clocks.stop()
     ms = sum(a.elapsed_time(b) for a, b in ev)
-    ms = allmax(ms)
+    ms = dist_max(ms, world, dev)
     value = job_value(world, w.T, args.steps, ms)
 
     # ---- per-kernel durations (separate pass, same work, library-side CUDA events)
@@ -451,24 +478,26 @@ def gpu_arm(args):
     torch.cuda.synchronize(dev)
     k3.k3moe_timing_enable(False)
     kt = k3.k3moe_timing_read()
-    top = max(kt.items(), key=lambda kv: kv[1][1])
-    top_name, (top_n, top_ms) = top
+    top_name, (top_n, top_ms) = max(kt.items(), key=lambda kv: kv[1][1])
     hbm, bf16, bf16_sus, src = peaks()
     per_launch_s = top_ms / top_n / 1000.0
     alg_b, alg_f = kernel_work(top_name, w, distinct)
-    # the kernel's bound: whichever of HBM and the tensor cores its algorithmic work
-    # needs longer on (sustained tensor peak: the kernel runs inside a long step)
-    if alg_f / (bf16_sus * 1e12) > alg_b / (hbm * 1e9):
-        roof = {"bound": "tensor", "achieved": alg_f / per_launch_s / 1e12, "peak": bf16_sus,
-                "unit": "TFLOP/s", "peak_kind": "bf16 sustained (f16 and bf16 run at one rate)"}
+    # the kernel's bound: whichever of HBM and the tensor cores its algorithmic work needs
+    # longer on.  The per-kernel pass times launches of at most milliseconds, so the tensor
+    # peak is the burst figure (the sustained one is for seconds-long loops).
+    if alg_f / (bf16 * 1e12) > alg_b / (hbm * 1e9):
+        roof = {"bound": "tensor", "achieved": alg_f / per_launch_s / 1e12, "peak": bf16,
+                "unit": "TFLOP/s", "peak_kind": "bf16 dense, burst (f16 runs at the same rate)"}
+        roof["frac_of_sustained"] = roof["achieved"] / bf16_sus
     else:
         roof = {"bound": "hbm", "achieved": alg_b / per_launch_s / 1e9, "peak": hbm, "unit": "GB/s",
                 "peak_kind": "HBM copy"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     step_bytes, step_flops = layer_bytes_flops(w, distinct)
     step_s = ms / args.steps / 1000.0
+    t_roof = max(step_bytes / (hbm * 1e9), step_flops / (bf16 * 1e12))
 
-    # ---- end to end through the C ABI from pinned host memory
+    # ---- end to end: pinned host x -> device, the C-ABI calls, device out -> pinned host
     e2e = None
     if not args.no_e2e:
         xh = x.cpu().pin_memory()
@@ -489,47 +518,78 @@ def gpu_arm(args):
             if i >= 2:
                 ee[i - 2][1].record(stream)
         torch.cuda.synchronize(dev)
-        ems = allmax(sum(a.elapsed_time(b) for a, b in ee))
+        ems = dist_max(sum(a.elapsed_time(b) for a, b in ee), world, dev)
         e2e = {"value": job_value(world, w.T, args.steps, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
-               "d2h_bytes_per_step": int(oh.numel() * oh.element_size())}
+               "d2h_bytes_per_step": int(oh.numel() * oh.element_size()),
+               "how": "torch copies between pinned host buffers and the device around the "
+                      "C-ABI calls, inside the timed events"}
+
+    ties = None
+    if rank == 0 and not w.hidden:
+        ties = near_tie_counts(layer, x, w)
+    del layer, flush
+    torch.cuda.empty_cache()
 
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, n, threads, s = time_oracle(w, args.cpu_budget_s)
         cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n} tokens of {w.name} (its {w.T} tokens in order, cycling), "
+               "sample": f"{n} tokens of {w.name} (its first {min(w.T, threads, 16)} tokens, cycled), "
                          f"route + forward, {s:.1f} s of oracle work"}
+    if rank != 0:
+        return None
+    return {
+        "value": value, "unit": "tokens/s", "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": ms / args.steps, "dtype": "f16",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "top_k": w.k,
+                   "n_shared": w.S, **({"hidden": w.hidden, "latent_norm": w.latent_norm}
+                                       if w.hidden else {}),
+                   "weights": "routed MXFP4 (E2M1 + E8M0/32), shared bf16"
+                              + (", dense projections bf16 (cuBLASLt)" if w.hidden else ""),
+                   "arithmetic": ARITHMETIC,
+                   "l2": "512 MiB buffer written between timed steps",
+                   "launch": "one CUDA graph replay per step" if args.graph else "eager",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": dict(roof, kernel=top_name, peak_source=src,
+                         traffic=traffic_for(top_name, w.name), alg_bytes_per_launch=alg_b,
+                         alg_flops_per_launch=alg_f, launch_ms=per_launch_s * 1e3),
+        "step_roofline": {"bytes": step_bytes, "flops": step_flops, "distinct_experts": distinct,
+                          "hbm_frac": step_bytes / step_s / 1e9 / hbm,
+                          "tensor_frac": step_flops / step_s / 1e12 / bf16,
+                          "bound": "hbm" if step_bytes / (hbm * 1e9) >= step_flops / (bf16 * 1e12)
+                                   else "tensor",
+                          "frac": t_roof / step_s,
+                          "peaks": f"HBM {hbm:.0f} GB/s, bf16 {bf16:.0f} TFLOP/s burst ({src})"},
+        "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kt.items()},
+        "gpu_launches": launches,
+        "host_enqueue_ms_per_step": 1000.0 * host_s / args.steps,
+        "router_near_ties": ties,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+    }
 
+
+def gpu_arm(args):
+    import torch
+    from sparse_moe_expert_k3moe_gb300 import build as kbuild
+
+    rank, world, local = dist_env()
+    kbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    specs = [sp for sp in args.workload.split(",") if sp]
+    records = [measure(workload_from(sp), args, rank, world, local, dev) for sp in specs]
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic",
-            "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "top_k": w.k,
-                       "n_shared": w.S, **({"hidden": w.hidden, "latent_norm": w.latent_norm}
-                                           if w.hidden else {}),
-                       "weights": "routed MXFP4 (E2M1 + E8M0/32), shared bf16"
-                                  + (", dense projections bf16 (cuBLASLt)" if w.hidden else ""),
-                       "l2": "512 MiB buffer written between timed steps",
-                       "launch": "one CUDA graph replay per step" if args.graph else "eager",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "roofline": dict(roof, kernel=top_name, peak_source=src,
-                             traffic=traffic_for(top_name, w.name), alg_bytes_per_launch=alg_b,
-                             alg_flops_per_launch=alg_f, launch_ms=per_launch_s * 1e3),
-            "step_roofline": {"bytes": step_bytes, "flops": step_flops,
-                              "distinct_experts": distinct,
-                              "hbm_frac": step_bytes / step_s / 1e9 / hbm,
-                              "tensor_frac": step_flops / step_s / 1e12 / bf16_sus},
-            "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kt.items()},
-            "gpu_launches": launches,
-            "host_enqueue_ms_per_step": 1000.0 * host_s / args.steps,
-            "e2e": e2e,
-            "cpu_baseline": cpu,
-            "clocks": clk,
-        }
+        line = {"metric": METRIC, "n_gpus": world, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "data": "synthetic", **records[0]}
+        for rec in records[1:]:
+            line[rec["config"]["workload"]] = rec
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

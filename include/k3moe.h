@@ -132,10 +132,14 @@ k3moe_status k3moe_unpack_mxfp4(const k3moe_config *cfg, int32_t expert_lo, int3
                                 k3moe_stream stream);
 
 /* Router (kimi-k3-in-c README, Part II, section 9, the k3_router listing):
- * logits x . Wr^T accumulated in fp32, sc = 1/(1+expf(-logit)) and
+ * logit = x . Wr^T, the exact sum of the bf16 products rounded once to float
+ * (what the listing's double accumulation gives), sc = 1/(1+expf(-logit)) and
  * ch = sc + bias in float, top_k by ch with ties to the lower index, weights
  * from sc (renormalised when renorm and their float sum is > 0, summed in
- * rank order, then times routed_scale).  Then the token -> expert map:
+ * rank order, then times routed_scale).  For many tokens the logits are first
+ * approximated on the tensor cores and only the experts that can still be
+ * chosen are scored exactly; the result is the same selection.  Then the
+ * token -> expert map:
  *   x        [T][d] bf16         w_router [E][d] bf16     bias [E] f32 or NULL
  *   idx      [T][k] int32  out: chosen experts, ch descending, ties index ascending
  *   weight   [T][k] f32    out: routing weights in the same order
@@ -148,15 +152,17 @@ k3moe_status k3moe_route(const k3moe_config *cfg, int32_t T, const uint16_t *x,
                          int32_t *idx, float *weight, int32_t *offsets, int32_t *perm,
                          void *ws, size_t ws_bytes, k3moe_stream stream);
 
-/* The router's scores alone, as k3moe_route computes them before its top-k
- * (kimi-k3-in-c README, Part II, section 9, the k3_router listing):
- *   scores [T][E] f32  out: sc = 1/(1+expf(-logit)), logit = x . Wr^T in fp32
+/* The router's exact scores for every (token, expert), as k3moe_route's
+ * selection uses them (kimi-k3-in-c README, Part II, section 9, the k3_router
+ * listing):
+ *   scores [T][E] f32  out: sc = 1/(1+expf(-logit)), logit = x . Wr^T rounded once
  *   choice [T][E] f32  out: ch = sc + bias (sc when bias is NULL)
- * The same kernels as k3moe_route for the same T (the per-token kernel for few
- * tokens, the tensor cores for many), so k3moe_route's selection is the top-k of
- * `choice` exactly.  x, w_router 16-byte aligned; scores, choice, bias 4-byte
- * aligned.  T may be 0 (nothing written).  ws per k3moe_workspace_bytes(T_max >= T);
- * only its status word is used. */
+ * k3moe_route's idx and weight are exactly the top-k of `choice` and the
+ * renormalised `scores` of the chosen experts, for any T.  Every pair is
+ * scored exactly here (no tensor-core shortcut), so at large T this call
+ * costs far more than k3moe_route.  x, w_router 16-byte aligned; scores, choice, bias 4-byte
+ * aligned.  T may be 0 (nothing written).  ws per k3moe_workspace_bytes(T_max
+ * >= T); only its status word is used. */
 k3moe_status k3moe_router_scores(const k3moe_config *cfg, int32_t T, const uint16_t *x,
                                  const uint16_t *w_router, const float *bias, float *scores,
                                  float *choice, void *ws, size_t ws_bytes, k3moe_stream stream);
@@ -191,16 +197,18 @@ k3moe_status k3moe_forward(const k3moe_config *cfg, int32_t T, const uint16_t *x
  * all its buffers.
  *   Arguments, results and errors as k3moe_forward, minus ws/ws_bytes, plus
  *   status_out: optional device int32 that receives this call's device
- *   status word (K3MOE_DEV_* bits); NULL to skip.
+ *   status word (K3MOE_DEV_* bits; 0 for T == 0); NULL to skip.
  * Scratch comes from a 32 MiB array inside the library (a file-scope
  * __device__ object): every GPU that loads the library holds it until the
  * process exits.  Calls whose k3moe_workspace_bytes(cfg, T) exceeds 32 MiB
  * return K3MOE_EWORKSPACE without launching (at the K3 shape, T <= 67 fits).
  * The first call on each device looks up the array's device address with
- * that device current; make it before any stream capture.  All calls share
- * the array and it keeps the last call's contents (each call clears its
- * status block first); calls that overlap on the GPU race on it, so order
- * them on one stream.  Allocates nothing: no cudaMalloc or cudaFree. */
+ * that device current; make it before any stream capture.  The address is
+ * kept with the device's context and looked up again if that context is
+ * replaced (a device reset).  All calls share the array and it keeps the
+ * last call's contents (each call clears its status block first); calls
+ * that overlap on the GPU race on it, so order them on one stream.
+ * Allocates nothing: no cudaMalloc or cudaFree. */
 k3moe_status k3moe_forward_noalloc(const k3moe_config *cfg, int32_t T, const uint16_t *x,
                                    const int32_t *idx, const float *weight,
                                    const int32_t *offsets, const int32_t *perm,
@@ -262,9 +270,24 @@ k3moe_status k3moe_full_forward(const k3moe_config *cfg, const k3moe_full_dims *
                                 void *ws, size_t ws_bytes, k3moe_stream stream);
 
 /* Synchronises `stream`, returns the device status word of `ws` in *code,
- * and clears it.  Returns K3MOE_EDEVICE when an error bit is set, K3MOE_OK
- * otherwise (the NAN_SCALE warning alone is OK). */
+ * and clears it: the report of the README's rule that corruption is counted,
+ * never silent (kimi-k3-in-c README, Part II, section 9, the k3_moe listing's
+ * count of dropped experts).  Returns K3MOE_ETIMEOUT when the timeout bit is
+ * set, else K3MOE_EDEVICE when another error bit is set, K3MOE_OK otherwise
+ * (the NAN_SCALE warning alone is OK). */
 k3moe_status k3moe_device_status(void *ws, k3moe_stream stream, int32_t *code);
+
+/* Exercises the failure report of a bounded wait (kimi-k3-in-c README, Part II,
+ * section 9: a fault is counted, never silent).  Every device-side wait of the
+ * library is bounded; when one runs out, its kernel sets K3MOE_DEV_TIMEOUT in
+ * the status word, drops its remaining work and returns, and the context stays
+ * usable.  This call runs both of the library's wait routines (the streamed
+ * mat-vecs' and the tensor-core kernels') on an mbarrier that nothing ever
+ * arrives on, each giving up after `limit_cycles` SM clock cycles (1 .. 4e9),
+ * so the timeout bit is set in `ws`'s status word; k3moe_device_status then
+ * returns K3MOE_ETIMEOUT.  For tests of the failure path; asynchronous on
+ * `stream`.  ws: a workspace as for k3moe_route (only its status word is used). */
+k3moe_status k3moe_check_wait_timeout(void *ws, int64_t limit_cycles, k3moe_stream stream);
 
 /* Number of GPU kernels this library has launched in this process (all
  * calls, all devices); for launch accounting in benchmarks. */

@@ -16,7 +16,7 @@ __all__ = [
     "K3MoEConfig", "K3MOE_OK", "K3MoEError", "lib", "k3moe_config", "k3moe_validate_config",
     "k3moe_packed_bytes", "k3moe_workspace_bytes", "k3moe_pack_mxfp4", "k3moe_unpack_mxfp4",
     "k3moe_route", "k3moe_router_scores", "k3moe_forward", "k3moe_forward_noalloc", "k3moe_device_status",
-    "k3moe_strerror",
+    "k3moe_check_wait_timeout", "k3moe_strerror",
     "k3moe_launch_count", "k3moe_timing_enable", "k3moe_timing_read", "k3moe_timing_reset",
     "library_path", "MoELayer", "K3MoEFullDims", "k3moe_full_dims", "k3moe_full_workspace_bytes",
     "k3moe_full_forward", "MoEBlock",
@@ -77,6 +77,7 @@ def lib():
             "k3moe_forward": (ctypes.c_int, [cp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp,
                                              vp, sz, vp]),
             "k3moe_device_status": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32)]),
+            "k3moe_check_wait_timeout": (ctypes.c_int, [vp, i64, vp]),
             "k3moe_forward_noalloc": (ctypes.c_int, [cp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp,
                                                      vp, vp, vp, vp]),
             "k3moe_full_workspace_bytes": (ctypes.c_int, [cp, ctypes.POINTER(K3MoEFullDims), i32,
@@ -188,6 +189,13 @@ def k3moe_forward(cfg, T, x, idx, weight, offsets, perm, expert_table, sh_w1, sh
         ctypes.byref(cfg), T, _ptr(x), _ptr(idx), _ptr(weight), _ptr(offsets), _ptr(perm),
         _ptr(expert_table), tb, _ptr(sh_w1), _ptr(sh_w3), _ptr(sh_w2), _ptr(out), _ptr(ws), wb,
         _stream(stream)))
+
+
+def k3moe_check_wait_timeout(ws, limit_cycles, stream=None):
+    """Runs the library's bounded waits on an mbarrier nothing arrives on, each giving up
+    after limit_cycles cycles: sets the timeout bit of ws's status word."""
+    _check("k3moe_check_wait_timeout", lib().k3moe_check_wait_timeout(_ptr(ws), int(limit_cycles),
+                                                                      _stream(stream)))
 
 
 def k3moe_forward_noalloc(cfg, T, x, idx, weight, offsets, perm, expert_table, sh_w1, sh_w3,

@@ -102,8 +102,6 @@ static size_t max_total(const k3moe_config &c, int32_t T_max, Total total)
     return m;
 }
 
-static const int32_t kMaxT = 1 << 20;
-
 }  // namespace k3moe
 
 using namespace k3moe;
@@ -333,6 +331,17 @@ k3moe_status k3moe_device_status(void *ws, k3moe_stream stream, int32_t *code)
     *code = v;
     if (v & K3MOE_DEV_TIMEOUT) return K3MOE_ETIMEOUT;
     return (v & K3MOE_DEV_ERROR_MASK) ? K3MOE_EDEVICE : K3MOE_OK;
+}
+
+k3moe_status k3moe_check_wait_timeout(void *ws, int64_t limit_cycles, k3moe_stream stream)
+{
+    if (!ws || !aligned(ws, 256)) return K3MOE_EWORKSPACE;
+    if (limit_cycles < 1 || limit_cycles > 4000000000ll) return K3MOE_ESHAPE;
+    int32_t *status = static_cast<int32_t *>(ws);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (launch_wait_check_gemv(status, limit_cycles, s) != cudaSuccess) return K3MOE_ECUDA;
+    if (launch_wait_check_tc(status, limit_cycles, s) != cudaSuccess) return K3MOE_ECUDA;
+    return K3MOE_OK;
 }
 
 int64_t k3moe_launch_count(void) { return g_launches.load(); }

@@ -74,7 +74,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
                  : "memory");
 }
 // Returns false when the bounded wait gave up (a clock limit, checked every 32 polls).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit = kWaitCycles)
 {
     const uint32_t a = smem_addr(bar);
     {   // fast path: the phase is often complete already
@@ -97,7 +97,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
             : "r"(a), "r"(parity)
             : "memory");
         if (done) return true;
-        if ((i & 31u) == 31u && clock64() - t0 > kWaitCycles) return false;
+        if ((i & 31u) == 31u && clock64() - t0 > limit) return false;
     }
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
@@ -1146,7 +1146,27 @@ bool cached_bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t c
     return true;
 }
 
+// One mbarrier that nothing arrives on, waited on by this file's bounded wait with the
+// given limit: the wait gives up and the kernel reports it the way the mat-vec kernels
+// do, by the status word's timeout bit.  For tests of that path.
+__global__ void __launch_bounds__(32) wait_check_gemv_kernel(int32_t *status, long long limit)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!mbar_wait(&bar, 0, limit)) atomicOr(status, K3MOE_DEV_TIMEOUT);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_check_gemv(int32_t *status, long long limit, cudaStream_t s)
+{
+    wait_check_gemv_kernel<<<1, 32, 0, s>>>(status, limit);
+    count_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
                                 const int32_t *idx, const float *weight, const int32_t *offsets,

@@ -100,7 +100,8 @@ inline bool use_gemm_path(const k3moe_config &c, int T)
 // Workspace regions (byte offsets), sized for one call's T.
 struct WsLayout {
     size_t status;
-    size_t sc, ch;               // router scores [T][E] f32
+    size_t sc, ch;               // router scores [T][E] f32 (tensor-core router: sc holds its logits)
+    size_t wnorm;                // router row norms |Wr[e]| [E] f32 (tensor-core router)
     size_t chunk_counts;         // [n_chunks][E] int32
     size_t chunk_base;           // [n_chunks][E] int32
     size_t local_rank;           // [T*k] int32
@@ -146,6 +147,7 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     L.status = o; o += 256;
     L.sc = o; o = align256(o + (size_t)T * E * 4);
     L.ch = o; o = align256(o + (size_t)T * E * 4);
+    L.wnorm = o; o = align256(o + E * 4);
     L.chunk_counts = o; o = align256(o + (size_t)L.n_chunks * E * 4);
     L.chunk_base = o; o = align256(o + (size_t)L.n_chunks * E * 4);
     L.local_rank = o; o = align256(o + slots * 4);
@@ -246,14 +248,16 @@ cudaError_t launch_unpack(const k3moe_config &c, int expert_lo, int n, const uin
 cudaError_t launch_route(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
                          const float *bias, int32_t *idx, float *weight, int32_t *offsets,
                          int32_t *perm, uint8_t *ws, const WsLayout &L, cudaStream_t s);
-// Router scores sc, ch [T][E] f32 (per-token kernel, or the tensor cores for many tokens).
+// Exact router scores sc, ch [T][E] f32 for every expert (the per-token kernel, any T).
 cudaError_t launch_router_scores(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
                                  const float *bias, float *sc, float *ch, int32_t *status, cudaStream_t s);
-// Router scores on the tensor cores (many tokens): sc, ch [T][E] as router_scores.
+// Approximate router logits on the tensor cores (many tokens): logit [T][E] f32, within a
+// small multiple of 2^-22 |x_t| |Wr[e]| of the exact logit; the top-k re-scores exactly
+// every expert the approximation cannot rule out.
 constexpr int kRouterTcMinTokens = 32;
 bool router_tc_applies(const k3moe_config &c, int T);
-cudaError_t launch_router_scores_tc(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
-                                    const float *bias, float *sc, float *ch, int32_t *status, cudaStream_t s);
+cudaError_t launch_router_logits_tc(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
+                                    float *logit, int32_t *status, cudaStream_t s);
 cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x, const int32_t *idx,
                                 const float *weight, const int32_t *offsets, const int32_t *perm,
                                 const uint8_t *table, const uint16_t *sh_w1, const uint16_t *sh_w3,
@@ -266,6 +270,12 @@ cudaError_t launch_full(const k3moe_config &c, int hidden, int latent_norm, floa
                         const uint16_t *sh1, const uint16_t *sh3, const uint16_t *sh2, int32_t *idx,
                         float *weight, int32_t *offsets, int32_t *perm, float *out, uint8_t *ws,
                         const FullLayout &F, cudaStream_t s);
+// One bounded wait of each kind (the mat-vec kernels', the tensor-core kernels') on an
+// mbarrier nothing arrives on, giving up after `limit` cycles: sets K3MOE_DEV_TIMEOUT.
+cudaError_t launch_wait_check_gemv(int32_t *status, long long limit, cudaStream_t s);
+cudaError_t launch_wait_check_tc(int32_t *status, long long limit, cudaStream_t s);
+// Largest T any call accepts.
+constexpr int32_t kMaxT = 1 << 20;
 // Either path, as the layout chose it.
 inline cudaError_t launch_forward(const k3moe_config &c, int T, const uint16_t *x, const int32_t *idx,
                                   const float *weight, const int32_t *offsets, const int32_t *perm,

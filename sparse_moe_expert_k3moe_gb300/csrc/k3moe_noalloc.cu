@@ -13,10 +13,14 @@
 // loads the library holds it until the process exits.  Host code cannot use the
 // array's name as a device address (in host code it is a host-side stand-in), so the
 // first call on each device, with that device current, looks up its device address
-// with cudaGetSymbolAddress and caches it; make that first call before any stream
-// capture.  All calls share the one array and it keeps the last call's contents: each
+// with cudaGetSymbolAddress and caches it together with the device's current context;
+// make that first call before any stream capture.  Should the context be destroyed and
+// created again (a device reset), the array gets a new address in the new context: the
+// next call sees the changed context and looks the address up again.  All calls share the one array and it keeps the last call's contents: each
 // call clears the status block that must start at zero, and calls that overlap on the
 // GPU (different streams, no ordering between them) race on the array.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "k3moe_internal.cuh"
@@ -31,21 +35,47 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 
 std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[kMaxDevices] = {};
+CUcontext g_noalloc_ctx[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once per device).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+// The calling thread's current context (NULL before the runtime has set one up), through
+// the driver entry point the runtime exposes.
+cudaError_t current_context(CUcontext *ctx)
+{
+    static CtxGetCurrentFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p)
+            return cudaErrorNotSupported;
+        fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    }
+    return fn(ctx) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of the scratch array on the current device, looked up once per device
+// and context.
 cudaError_t noalloc_scratch(void **out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    CUcontext ctx = nullptr;                // NULL until the runtime has set up the device
+    e = current_context(&ctx);
+    if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    if (!g_noalloc_ptr[dev] || !ctx || g_noalloc_ctx[dev] != ctx) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);   // sets up the context if needed
         if (e != cudaSuccess) return e;
         if (!p) return cudaErrorInvalidSymbol;
+        e = current_context(&ctx);
+        if (e != cudaSuccess) return e;
         g_noalloc_ptr[dev] = p;
+        g_noalloc_ctx[dev] = ctx;
     }
     *out = g_noalloc_ptr[dev];
     return cudaSuccess;
@@ -66,8 +96,14 @@ extern "C" k3moe_status k3moe_forward_noalloc(
 {
     k3moe_status st = k3moe_validate_config(cfg);
     if (st != K3MOE_OK) return st;
-    if (T < 0) return K3MOE_ESHAPE;
-    if (T == 0) return K3MOE_OK;
+    if (T < 0 || T > kMaxT) return K3MOE_ESHAPE;
+    if (status_out && !is_aligned(status_out, 4)) return K3MOE_EALIGN;
+    if (T == 0) {
+        // nothing to compute; the status word still reports this call: clean
+        if (status_out && cudaMemsetAsync(status_out, 0, sizeof(int32_t), (cudaStream_t)stream) != cudaSuccess)
+            return K3MOE_ECUDA;
+        return K3MOE_OK;
+    }
     if (!x || !idx || !weight || !offsets || !perm || !expert_table || !out) return K3MOE_EINVAL;
     if (cfg->n_shared > 0 && (!sh_w1 || !sh_w3 || !sh_w2)) return K3MOE_EINVAL;
     if (!is_aligned(x, 16) || !is_aligned(out, 16) || !is_aligned(expert_table, 256) ||

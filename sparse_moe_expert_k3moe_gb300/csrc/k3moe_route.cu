@@ -1,16 +1,27 @@
 // k3moe_route.cu -- router and token -> expert map (kimi-k3-in-c README, Part II,
 // section 9 "Picking 16 experts of 896").
 //
+// The router listing accumulates each logit in double and rounds it to float once, then
+// takes sc = 1/(1+expf(-logit)) and ch = sc + bias in float.  Those float values decide
+// which experts win, so the kernels here reproduce them: a logit is computed exactly
+// (up to the final rounding) and the sigmoid from a double exponential rounded to float.
+//
 // Kernels, in launch order:
-//   router_scores  logits = x . Wr^T (fp32 accumulation of exact bf16 products),
-//                  sc = 1/(1+expf(-logit)), ch = sc + bias, both float, to the workspace.
-//                  A block owns 4 experts (one per warp, its Wr row held in registers)
-//                  and walks the tokens 8 at a time through shared memory;
-//   router_topk    one block per token: warp-level bitonic sorts and merges of the E keys
-//                  (ch, then the lower index first) pick the top k in rank order; the
-//                  weights are the chosen sc renormalised by their float sum in rank
-//                  order, times routed_scale.  With at most 64 tokens the last block to
-//                  finish (the only one, for one token) also builds the map;
+//   router_scores  (few tokens) exact logits, sc and ch for every (token, expert), to the
+//                  workspace.  A block owns 4 experts (one per warp, its Wr row held in
+//                  registers) and walks its tokens 8 at a time through shared memory;
+//   router_wnorm   (many tokens) |Wr[e]| for every expert, for the bound below;
+//   router_logits_tc (many tokens, k3moe_route_tc.cu) approximate logits on the tensor
+//                  cores;
+//   router_topk    one block per token: warp-level bitonic sorts and merges of 64-bit keys
+//                  (ch, then the lower index first) pick the top k in rank order.  With
+//                  approximate logits it first brackets every expert's exact ch between
+//                  a lower and an upper bound, keeps the experts whose upper bound reaches
+//                  the k-th largest lower bound (the only ones that can be chosen),
+//                  re-scores those exactly and selects among them.  The weights are the
+//                  chosen sc renormalised by their float sum in rank order, times
+//                  routed_scale.  With at most 64 tokens the last block to finish (the
+//                  only one, for one token) also builds the map;
 //   perm_count     (more tokens) per chunk of 64 tokens: per-expert slot counts and each
 //                  slot's stable rank inside the chunk (warp match + popc, warp by warp);
 //   perm_scan      per-expert exclusive scan over chunks, then over experts -> offsets;
@@ -24,9 +35,108 @@ namespace {
 
 constexpr int kScoreWarps = 4;       // experts per block (one per warp)
 constexpr int kScoreTok = 8;         // tokens staged per round
+constexpr int kScoreTokBlock = 32;   // tokens per block (grid.y walks the rest)
 constexpr int kScoreChunks = 16;     // 16-byte Wr chunks per lane held at once (4096 columns)
 
-// -------------------------------------------------------------------------------- scores
+// Bound on the tensor-core logits' error, relative to |x_t| |Wr[e]|.  Their fp32
+// accumulation was measured within 2^-22 of that scale (3.7e-6 on unit-scale scores,
+// 1.3e-5 on tokens scaled by 8, over 14.7M scores); the bound keeps a factor of 1024
+// above it.  It only widens the set of experts re-scored exactly, never the result.
+constexpr float kTcLogitRel = 0x1p-12f;
+
+// -------------------------------------------------------------------------------- exact logits
+// A logit is a sum of d products of two bf16 values, each exact in fp32.  It is carried
+// as an unevaluated pair (s, c): s the fp32 running sum, c the running sum of the exact
+// rounding errors of s's additions (Knuth's two-sum), and rounded once, to s + c.  A lane
+// keeps two such pairs (its 16-byte chunks alternate between them); the pairs, then the
+// lanes, are merged by the same rule.  The result is the float nearest the exact sum
+// unless that sum lies within about 2^-40 (relative) of a rounding boundary -- what the
+// listing's double accumulation rounded to float gives.  Every kernel that computes a
+// logit exactly goes through these functions with the same chunk-to-lane assignment
+// (chunk lane + 32 m, pair m & 1, m ascending), so their results are bitwise equal.
+struct Acc2 {
+    float s, c;
+};
+
+__device__ __forceinline__ void acc_add(Acc2 &a, float p)
+{
+    const float t = __fadd_rn(a.s, p);
+    const float z = __fsub_rn(t, a.s);
+    const float e = __fadd_rn(__fsub_rn(a.s, __fsub_rn(t, z)), __fsub_rn(p, z));
+    a.s = t;
+    a.c = __fadd_rn(a.c, e);
+}
+
+// Merging is symmetric in its arguments (the two-sum error of s_a + s_b is unique), so
+// both lanes of a butterfly step hold the same pair afterwards.
+__device__ __forceinline__ Acc2 acc_merge(Acc2 a, const Acc2 b)
+{
+    a.c = __fadd_rn(a.c, b.c);
+    acc_add(a, b.s);
+    return a;
+}
+
+// One 16-byte chunk: 8 products in element order (low half of each word first).
+__device__ __forceinline__ void acc_chunk(Acc2 &a, const uint4 xv, const uint4 wv)
+{
+    const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
+    const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        acc_add(a, __fmul_rn(__uint_as_float(xu[q] << 16), __uint_as_float(wu[q] << 16)));
+        acc_add(a, __fmul_rn(__uint_as_float(xu[q] & 0xFFFF0000u), __uint_as_float(wu[q] & 0xFFFF0000u)));
+    }
+}
+
+// Both pairs of every lane -> the rounded logit, on every lane.
+__device__ __forceinline__ float acc_finish(const Acc2 a0, const Acc2 a1)
+{
+    Acc2 a = acc_merge(a0, a1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        Acc2 b;
+        b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+        b.c = __shfl_xor_sync(0xffffffffu, a.c, o);
+        a = acc_merge(a, b);
+    }
+    return __fadd_rn(a.s, a.c);
+}
+
+// sc = 1/(1+expf(-logit)) and ch = sc + bias, each step rounded to float as the listing
+// writes them; the exponential is the double one rounded to float (the correctly rounded
+// float exponential, but in cases within 2^-29 ulp of a tie).
+__device__ __forceinline__ void exact_scores(float logit, float bias, float &sc, float &ch)
+{
+    const float ef = __double2float_rn(exp(-(double)logit));
+    sc = __fdiv_rn(1.0f, __fadd_rn(1.0f, ef));
+    ch = __fadd_rn(sc, bias);
+}
+
+// Exact logit of one (token, expert) pair by one warp: the token row in shared memory, the
+// router row in global memory, nchunk 16-byte chunks each.
+__device__ __forceinline__ float exact_logit_warp(const uint4 *xs, const uint4 *__restrict__ wrow, int nchunk,
+                                                  int lane)
+{
+    Acc2 a0{0.0f, 0.0f}, a1{0.0f, 0.0f};
+    int m = 0;
+    for (; lane + 32 * (m + 3) < nchunk; m += 4) {
+        const uint4 w0 = __ldg(wrow + lane + 32 * m), w1 = __ldg(wrow + lane + 32 * (m + 1));
+        const uint4 w2 = __ldg(wrow + lane + 32 * (m + 2)), w3 = __ldg(wrow + lane + 32 * (m + 3));
+        acc_chunk(a0, xs[lane + 32 * m], w0);
+        acc_chunk(a1, xs[lane + 32 * (m + 1)], w1);
+        acc_chunk(a0, xs[lane + 32 * (m + 2)], w2);
+        acc_chunk(a1, xs[lane + 32 * (m + 3)], w3);
+    }
+    for (; lane + 32 * m < nchunk; m++) {
+        const uint4 w = __ldg(wrow + lane + 32 * m);
+        if (m & 1) acc_chunk(a1, xs[lane + 32 * m], w);
+        else acc_chunk(a0, xs[lane + 32 * m], w);
+    }
+    return acc_finish(a0, a1);
+}
+
+// -------------------------------------------------------------------------------- exact scores
+// grid (ceil(E / 4), ceil(T / 32)); block y owns tokens [32 y, 32 y + 32).
 __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
     int T, int d, int E, const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
     const float *__restrict__ bias, float *__restrict__ sc_out, float *__restrict__ ch_out)
@@ -38,6 +148,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kScoreWarps + warp;
     const int nchunk = d / 8;                                  // 16-byte chunks per row
+    const int tb0 = blockIdx.y * kScoreTokBlock, tb1 = min(T, tb0 + kScoreTokBlock);
     const uint4 *wrow = reinterpret_cast<const uint4 *>(wr + (size_t)min(e, E - 1) * d);
     const float b = (bias && e < E) ? bias[e] : 0.0f;
     // the first 4096 columns of the row stay in registers across the token rounds (the
@@ -48,17 +159,17 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
         const int c = lane + 32 * j;
         w0[j] = c < nchunk ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
     }
-    for (int t0 = 0; t0 < T; t0 += kScoreTok) {
-        const int nt = min(kScoreTok, T - t0);
+    for (int t0 = tb0; t0 < tb1; t0 += kScoreTok) {
+        const int nt = min(kScoreTok, tb1 - t0);
         __syncthreads();
         for (int q = threadIdx.x; q < nt * nchunk; q += blockDim.x) {
             const int i = q / nchunk, c = q % nchunk;
             xs[i * nchunk + c] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + i) * d) + c);
         }
         __syncthreads();
-        float acc[kScoreTok];
+        Acc2 acc[kScoreTok][2];
 #pragma unroll
-        for (int i = 0; i < kScoreTok; i++) acc[i] = 0.0f;
+        for (int i = 0; i < kScoreTok; i++) acc[i][0] = acc[i][1] = Acc2{0.0f, 0.0f};
         for (int c0 = 0; c0 < nchunk; c0 += 32 * kScoreChunks) {
             uint4 w[kScoreChunks];
 #pragma unroll
@@ -69,41 +180,52 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
 #pragma unroll
             for (int i = 0; i < kScoreTok; i++) {
                 if (i >= nt) break;
-                float a = acc[i];
 #pragma unroll
                 for (int j = 0; j < kScoreChunks; j++) {
-                    const int c = c0 + lane + 32 * j;
-                    if (c < nchunk) {
-                        const uint4 xv = xs[i * nchunk + c];
-                        const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
-                        const uint32_t wu[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            a = fmaf(__uint_as_float(xu[q] << 16), __uint_as_float(wu[q] << 16), a);
-                            a = fmaf(__uint_as_float(xu[q] & 0xFFFF0000u), __uint_as_float(wu[q] & 0xFFFF0000u), a);
-                        }
-                    }
+                    const int c = c0 + lane + 32 * j;   // this lane's chunk number (c0 / 32 + j) is even iff j is
+                    if (c < nchunk) acc_chunk(acc[i][j & 1], xs[i * nchunk + c], w[j]);
                 }
-                acc[i] = a;
             }
         }
+        float logit = 0.0f;
 #pragma unroll
         for (int i = 0; i < kScoreTok; i++) {
-            float v = acc[i];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            acc[i] = v;
+            if (i >= nt) break;
+            const float v = acc_finish(acc[i][0], acc[i][1]);
+            if (lane == i) logit = v;
         }
         if (e < E && lane < nt) {
-            float logit = acc[0];
-#pragma unroll
-            for (int i = 1; i < kScoreTok; i++)
-                if (lane == i) logit = acc[i];
-            const float s = 1.0f / (1.0f + expf(-logit));
+            float s, ch;
+            exact_scores(logit, b, s, ch);
             sc_out[(size_t)(t0 + lane) * E + e] = s;
-            ch_out[(size_t)(t0 + lane) * E + e] = s + b;
+            ch_out[(size_t)(t0 + lane) * E + e] = ch;
         }
     }
+}
+
+// |Wr[e]| (times 1.001, above the fp32 rounding of the sum of squares), one warp per row.
+__global__ void __launch_bounds__(256) router_wnorm_kernel(int d, int E, const uint16_t *__restrict__ wr,
+                                                           float *__restrict__ wnorm)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (e >= E) return;
+    const uint4 *row = reinterpret_cast<const uint4 *>(wr + (size_t)e * d);
+    float ss = 0.0f;
+    for (int c = lane; c < d / 8; c += 32) {
+        const uint4 v = __ldg(row + c);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const float lo = __uint_as_float(u[q] << 16), hi = __uint_as_float(u[q] & 0xFFFF0000u);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) wnorm[e] = sqrtf(ss) * 1.001f;
 }
 
 // -------------------------------------------------------------------------------- token -> expert map
@@ -200,10 +322,20 @@ __device__ __forceinline__ uint32_t orderable(float v)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+__device__ __forceinline__ uint64_t choice_key(float ch, int e)
+{
+    return ((uint64_t)orderable(ch) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
+}
+
 struct TopkArgs {
     int T, E, k, renorm;
     float routed_scale;
-    const float *sc, *ch;
+    const float *sc, *ch;   // exact scores [T][E] (per-token kernel), or:
+    const float *logit;     // approximate logits [T][E] (tensor cores), re-scored here
+    const float *bias;      // [E] or NULL (re-scoring only)
+    const float *wnorm;     // |Wr[e]| [E] (re-scoring only)
+    const uint16_t *x, *wr; // token rows and router rows (re-scoring only)
+    int d;
     int32_t *idx;
     float *weight;
     int32_t *done;          // last-block counter (kept at zero between calls)
@@ -239,27 +371,17 @@ __device__ __forceinline__ uint64_t warp_merge_desc(uint64_t key, int lane)
     return key;
 }
 
-// blockDim = 1024; block t owns token t.  Key = (orderable(ch) << 32) | ~index, so a
-// descending order sorts by ch and, among equal ch, by ascending index -- the order the
-// repeated maximum with a strict comparison produces.  Every key is distinct, so the k
-// largest keys are the selection.  Warp w sorts keys 32w..32w+31 and keeps its 16
-// largest; pairs of lists are then merged warp by warp (16 of 32 kept) until one remains.
-__global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
+// The 16 largest of the keys that threads 0..n-1 offer (n <= 1024; a missing key counts
+// as 0, below every real key).  Warp w sorts keys 32w..32w+31 and keeps its 16 largest;
+// pairs of lists are then merged warp by warp (16 of 32 kept) until one remains.  Returns
+// the rank-r key in lane r < 16 of warp 0 (0 elsewhere).  Called by the whole block.
+__device__ uint64_t block_top16(uint64_t key, int n, uint64_t (*lists)[32][kMaxTopK])
 {
-    pdl_wait();
-    pdl_trigger();
-    __shared__ uint64_t lists[2][32][kMaxTopK];
-    __shared__ int32_t cnt[kMaxExperts];
-    __shared__ int32_t slot_e[kChunkTokens * kMaxTopK];
-    __shared__ int32_t scan_tmp[32];
-    __shared__ int last;
     const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
-    const int t = blockIdx.x, E = a.E, k = a.k;
-    const int nl0 = (E + 31) >> 5;                 // lists after the first level
-    uint64_t key = 0;
+    const int nl0 = max(1, (n + 31) >> 5);         // lists after the first level
+    __syncthreads();                               // the lists may be in use from a previous call
     if (warp < nl0) {
-        if (i < E) key = ((uint64_t)orderable(a.ch[(size_t)t * E + i]) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)i);
-        key = warp_sort_desc(key, lane);
+        key = warp_sort_desc(i < n ? key : 0, lane);
         if (lane < kMaxTopK) lists[0][warp][lane] = key;
     }
     int nl = nl0, cur = 0;
@@ -278,18 +400,119 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
         nl = half;
     }
     __syncthreads();
-    if (warp == 0) key = lane < kMaxTopK ? lists[cur][0][lane] : 0;
+    return (warp == 0 && lane < kMaxTopK) ? lists[cur][0][lane] : 0;
+}
+
+// Float sigmoid for the bounds of the re-scoring step (any accuracy within a few ulp).
+__device__ __forceinline__ float sigmoid_bound(float v) { return 1.0f / (1.0f + expf(-v)); }
+
+// blockDim = 1024; block t owns token t.  Key = (orderable(ch) << 32) | ~index, so a
+// descending order sorts by ch and, among equal ch, by ascending index -- the order the
+// repeated maximum with a strict comparison produces.  Every key is distinct, so the k
+// largest keys are the selection.
+//
+// With approximate logits la (|la - logit| <= L = 2^-12 |x_t| |Wr[e]|), the exact ch of
+// expert e lies in [lo_e, hi_e], lo/hi = sigmoid(la -/+ L) + bias -/+ slack (slack covers
+// the float rounding of both sides).  The k-th largest exact ch is at least the k-th
+// largest lo, so an expert whose hi stays below that can never be chosen, and an expert
+// below it cannot tie with the k-th either.  The others (the candidates) are re-scored
+// exactly and the selection is the top k of their exact keys.
+__global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
+{
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ __align__(16) uint8_t tk_dyn[];   // re-scoring: the token row, d bf16
+    __shared__ uint64_t lists[2][32][kMaxTopK];
+    __shared__ int32_t cnt[kMaxExperts];                 // map counts; re-scoring: the candidates
+    __shared__ int32_t slot_e[kChunkTokens * kMaxTopK];
+    __shared__ int32_t scan_tmp[32];
+    __shared__ float scx[kMaxExperts];                   // re-scoring: exact sc by expert
+    __shared__ uint64_t ckey[kMaxExperts];               // re-scoring: exact keys of the candidates
+    __shared__ float red[32];
+    __shared__ uint32_t thr_o;
+    __shared__ int n_cand, last;
+    const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
+    const int t = blockIdx.x, E = a.E, k = a.k;
+    uint64_t top;                                        // lane r < k of warp 0: the rank-r key
+    if (a.logit == nullptr) {
+        const uint64_t key = i < E ? choice_key(a.ch[(size_t)t * E + i], i) : 0;
+        top = block_top16(key, E, lists);
+    } else {
+        // the token row into shared memory, and |x_t|
+        const int nchunk = a.d / 8;
+        uint4 *xs = reinterpret_cast<uint4 *>(tk_dyn);
+        const uint4 *xg = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.d);
+        float ss = 0.0f;
+        for (int q = i; q < nchunk; q += blockDim.x) {
+            const uint4 v = __ldg(xg + q);
+            xs[q] = v;
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int r = 0; r < 4; r++) {
+                const float lo = __uint_as_float(u[r] << 16), hi = __uint_as_float(u[r] & 0xFFFF0000u);
+                ss = fmaf(lo, lo, ss);
+                ss = fmaf(hi, hi, ss);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float xn2 = 0.0f;
+        for (int w = 0; w < 32; w++) xn2 += red[w];
+        const float xn = sqrtf(xn2) * 1.001f;
+        // bounds, and the k-th largest lower bound
+        float hi = 0.0f;
+        uint64_t key = 0;
+        if (i < E) {
+            const float la = a.logit[(size_t)t * E + i];
+            const float L = kTcLogitRel * xn * a.wnorm[i];
+            const float b = a.bias ? a.bias[i] : 0.0f;
+            const float slack = 1e-6f + fabsf(b) * 0x1p-20f;
+            const float lo = sigmoid_bound(la - L) + b - slack;
+            hi = sigmoid_bound(la + L) + b + slack;
+            key = choice_key(lo, i);
+        }
+        const uint64_t lk = block_top16(key, E, lists);
+        if (warp == 0 && lane == k - 1) thr_o = (uint32_t)(lk >> 32);
+        __syncthreads();
+        // candidates: upper bound at or above the threshold (no NaN passes)
+        const bool is_c = i < E && hi == hi && orderable(hi) >= thr_o;
+        const uint32_t m = __ballot_sync(0xffffffffu, is_c);
+        if (lane == 0) scan_tmp[warp] = __popc(m);
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; w++) base += scan_tmp[w];
+        if (is_c) cnt[base + __popc(m & ((1u << lane) - 1u))] = i;
+        if (i == 1023) n_cand = base + __popc(m);
+        __syncthreads();
+        const int C = n_cand;
+        // exact scores of the candidates, one warp per candidate
+        const uint4 *wr = reinterpret_cast<const uint4 *>(a.wr);
+        for (int c = warp; c < C; c += 32) {
+            const int e = cnt[c];
+            const float logit = exact_logit_warp(xs, wr + (size_t)e * nchunk, nchunk, lane);
+            if (lane == 0) {
+                float sv, cv;
+                exact_scores(logit, a.bias ? a.bias[e] : 0.0f, sv, cv);
+                scx[e] = sv;
+                ckey[c] = choice_key(cv, e);
+            }
+        }
+        __syncthreads();
+        top = block_top16(i < C ? ckey[i] : 0, C, lists);
+    }
     // lane r < k of warp 0 now holds the rank-r key
     if (i < 32) {
         int e = -1;
         float w = 0.0f;
         if (i < k) {
-            e = (int)(0xFFFFFFFFu - (uint32_t)key);
-            if (e < 0 || e >= E) {                 // cannot happen with k <= E; stay in bounds
+            e = (int)(0xFFFFFFFFu - (uint32_t)top);
+            if (e < 0 || e >= E) {                 // no valid key (non-finite scores); stay in bounds
                 set_status(a.map.status, K3MOE_DEV_BAD_INDEX);
                 e = 0;
             }
-            w = a.sc[(size_t)t * E + e];
+            w = a.logit == nullptr ? a.sc[(size_t)t * E + e] : scx[e];
         }
         float s = 0.0f;
         for (int j = 0; j < k; j++) s += __shfl_sync(0xffffffffu, w, j);
@@ -412,26 +635,21 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(int total_slots, int 
 cudaError_t launch_router_scores(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
                                  const float *bias, float *sc, float *ch, int32_t *status, cudaStream_t s)
 {
+    (void)status;
     const int E = c.n_experts;
-    if (router_tc_applies(c, T)) {
-        timing_begin("router_scores_tc", s);
-        cudaError_t err = launch_router_scores_tc(c, T, x, wr, bias, sc, ch, status, s);
-        timing_end("router_scores_tc", s);
-        if (err != cudaSuccess) return err;
-    } else {
-        static size_t smem_set = 0;
-        const size_t smem = (size_t)kScoreTok * c.d * 2;
-        if (smem > smem_set) {
-            cudaFuncSetAttribute(router_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            smem_set = smem;
-        }
-        timing_begin("router_scores", s);
-        cudaError_t err = launch_pdl(router_scores_kernel, dim3((E + kScoreWarps - 1) / kScoreWarps),
-                                     dim3(kScoreWarps * 32), smem, s, T, c.d, E, x, wr, bias, sc, ch);
-        count_launch();
-        timing_end("router_scores", s);
-        if (err != cudaSuccess) return err;
+    static size_t smem_set = 0;
+    const size_t smem = (size_t)kScoreTok * c.d * 2;
+    if (smem > smem_set) {
+        cudaFuncSetAttribute(router_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        smem_set = smem;
     }
+    timing_begin("router_scores", s);
+    cudaError_t err = launch_pdl(router_scores_kernel,
+                                 dim3((E + kScoreWarps - 1) / kScoreWarps, (T + kScoreTokBlock - 1) / kScoreTokBlock),
+                                 dim3(kScoreWarps * 32), smem, s, T, c.d, E, x, wr, bias, sc, ch);
+    count_launch();
+    timing_end("router_scores", s);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
@@ -449,15 +667,30 @@ cudaError_t launch_route(const k3moe_config &c, int T, const uint16_t *x, const 
     }
     float *sc = reinterpret_cast<float *>(ws + L.sc);
     float *ch = reinterpret_cast<float *>(ws + L.ch);
-    cudaError_t err = launch_router_scores(c, T, x, wr, bias, sc, ch, status, s);
+    float *wnorm = reinterpret_cast<float *>(ws + L.wnorm);
+    const bool tc = router_tc_applies(c, T);
+    cudaError_t err;
+    if (tc) {
+        // approximate logits into the sc region, re-scored by the top-k
+        timing_begin("router_wnorm", s);
+        err = launch_pdl(router_wnorm_kernel, dim3((E + 7) / 8), dim3(256), 0, s, c.d, E, wr, wnorm);
+        count_launch();
+        timing_end("router_wnorm", s);
+        if (err != cudaSuccess) return err;
+        timing_begin("router_logits_tc", s);
+        err = launch_router_logits_tc(c, T, x, wr, sc, status, s);
+        timing_end("router_logits_tc", s);
+    } else {
+        err = launch_router_scores(c, T, x, wr, bias, sc, ch, status, s);
+    }
     if (err != cudaSuccess) return err;
     MapArgs m{T, E, k, idx, offsets, perm, reinterpret_cast<int32_t *>(ws + L.chunk_counts),
               reinterpret_cast<int32_t *>(ws + L.local_rank), status};
     // status block word 4 is the last-block counter of router_topk
-    TopkArgs a{T, E, k, c.renorm, c.routed_scale, sc, ch, idx, weight,
-               L.n_chunks == 1 ? status + 4 : nullptr, m};
+    TopkArgs a{T, E, k, c.renorm, c.routed_scale, sc, ch, tc ? sc : nullptr, bias, wnorm, x, wr, c.d,
+               idx, weight, L.n_chunks == 1 ? status + 4 : nullptr, m};
     timing_begin("router_topk", s);
-    err = launch_pdl(router_topk_kernel, dim3(T), dim3(1024), 0, s, a);
+    err = launch_pdl(router_topk_kernel, dim3(T), dim3(1024), tc ? (size_t)c.d * 2 : 0, s, a);
     count_launch();
     timing_end("router_topk", s);
     if (err != cudaSuccess) return err;

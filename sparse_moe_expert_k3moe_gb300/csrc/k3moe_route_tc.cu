@@ -1,17 +1,17 @@
-// k3moe_route_tc.cu -- the router's scores on the tensor cores, for many tokens
+// k3moe_route_tc.cu -- approximate router logits on the tensor cores, for many tokens
 // (kimi-k3-in-c README, Part II, section 9 "Picking 16 experts of 896": the router
-// logits are the dot products of the token with each expert's bf16 router row, in fp32,
-// and the score is their sigmoid).
+// logits are the dot products of the token with each expert's bf16 router row).
 //
-// logits[t][e] = x[t] . Wr[e] is a plain bf16 GEMM with fp32 accumulation: the products
-// of two bf16 values are exact in fp32, as in the per-token kernel, only the order of
-// the additions differs.  Swap AB again: M = 128 router rows (experts), N = up to 256
+// logits[t][e] = x[t] . Wr[e] is a plain bf16 GEMM with fp32 accumulation.  The tensor
+// cores' accumulation is coarser than fp32 addition (measured within 2^-22 |x_t| |Wr[e]|),
+// so these logits only bracket the exact ones: the top-k kernel re-scores exactly every
+// expert they cannot rule out.  Swap AB again: M = 128 router rows (experts), N = up to 256
 // tokens, K = d.  One work item = one (128-expert block, 256-token tile); items are
 // walked token tile by token tile so the blocks reading one x tile run together.
 // Warp roles: warp 0 TMA producer (A box 64 x 128 rows, B boxes 64 x 16), warp 1
 // tcgen05.mma issue (bf16, fp32 accumulators, two 256-column buffers), warps 2-5
-// epilogue: sc = 1/(1+expf(-logit)), ch = sc + bias, stored [T][E] like the per-token
-// kernel.  Every wait is bounded; a timeout sets the status word and the roles drop out.
+// epilogue: the logits, stored [T][E].  Every wait is bounded; a timeout sets the status
+// word and the roles drop out.
 #include <cuda.h>
 
 #include <algorithm>
@@ -31,12 +31,11 @@ constexpr int kRtTmemCols = 512;
 
 struct RtArgs {
     int T, d, E;
-    const float *bias;
-    float *sc, *ch;
+    float *logit;
     int32_t *status;
 };
 
-__global__ void __launch_bounds__(kRtThreads, 1) router_scores_tc_kernel(const RtArgs a,
+__global__ void __launch_bounds__(kRtThreads, 1) router_logits_tc_kernel(const RtArgs a,
                                                                          const __grid_constant__ CUtensorMap mwr,
                                                                          const __grid_constant__ CUtensorMap mx)
 {
@@ -131,7 +130,6 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_scores_tc_kernel(const R
             const int ncols = min(kRtBN, a.T - t0);
             const int bn = (ncols + 15) & ~15;
             const int e = eb * kRtBM + row;
-            const float b = (a.bias && e < a.E) ? a.bias[e] : 0.0f;
             const int buf = n & 1;
             if (!mb_wait(&acc_full[buf], (n >> 1) & 1u)) { timeout(); break; }
             tc_fence_after();
@@ -143,10 +141,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_scores_tc_kernel(const R
 #pragma unroll
                     for (int jj = 0; jj < 16; jj++) {
                         if (c0 + jj >= ncols) break;
-                        const size_t o = (size_t)(t0 + c0 + jj) * a.E + e;
-                        const float s = 1.0f / (1.0f + expf(-v[jj]));
-                        a.sc[o] = s;
-                        a.ch[o] = s + b;
+                        a.logit[(size_t)(t0 + c0 + jj) * a.E + e] = v[jj];
                     }
                 }
             }
@@ -164,7 +159,27 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_scores_tc_kernel(const R
     }
 }
 
+// The tensor-core kernels' bounded wait (mb_wait) on an mbarrier nothing arrives on,
+// with the given limit: it gives up, and the kernel sets the status word's timeout bit
+// as those kernels do.  For tests of that path.
+__global__ void __launch_bounds__(32) wait_check_tc_kernel(int32_t *status, long long limit)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mb_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!mb_wait(&bar, 0, limit)) set_status(status, K3MOE_DEV_TIMEOUT);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_check_tc(int32_t *status, long long limit, cudaStream_t s)
+{
+    wait_check_tc_kernel<<<1, 32, 0, s>>>(status, limit);
+    count_launch();
+    return cudaGetLastError();
+}
 
 // the A box is 128 router rows: at least that many experts
 bool router_tc_applies(const k3moe_config &c, int T)
@@ -172,12 +187,12 @@ bool router_tc_applies(const k3moe_config &c, int T)
     return T >= kRouterTcMinTokens && c.n_experts >= kRtBM && c.d % kRtBK == 0;
 }
 
-cudaError_t launch_router_scores_tc(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
-                                    const float *bias, float *sc, float *ch, int32_t *status, cudaStream_t s)
+cudaError_t launch_router_logits_tc(const k3moe_config &c, int T, const uint16_t *x, const uint16_t *wr,
+                                    float *logit, int32_t *status, cudaStream_t s)
 {
     static bool set = false;
     if (!set) {
-        cudaFuncSetAttribute(router_scores_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+        cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
         set = true;
     }
     CUtensorMap mwr{}, mx{};
@@ -186,8 +201,8 @@ cudaError_t launch_router_scores_tc(const k3moe_config &c, int T, const uint16_t
         return cudaErrorInvalidValue;
     const int n_items = ((c.n_experts + kRtBM - 1) / kRtBM) * ((T + kRtBN - 1) / kRtBN);
     const int grid = std::max(1, std::min(num_sms(), n_items));
-    RtArgs a{T, c.d, c.n_experts, bias, sc, ch, status};
-    const cudaError_t err = launch_pdl(router_scores_tc_kernel, dim3(grid), dim3(kRtThreads), kRtSmem, s, a, mwr, mx);
+    RtArgs a{T, c.d, c.n_experts, logit, status};
+    const cudaError_t err = launch_pdl(router_logits_tc_kernel, dim3(grid), dim3(kRtThreads), kRtSmem, s, a, mwr, mx);
     count_launch();
     return err;
 }

@@ -29,7 +29,7 @@ __device__ __forceinline__ void mb_expect_tx(uint64_t *b, uint32_t bytes)
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t parity)
+__device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t parity, long long limit = kTcWaitCyc)
 {
     const uint32_t a = saddr(b);
     {   // fast path: the phase is usually complete already
@@ -52,7 +52,7 @@ __device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t parity)
             : "r"(a), "r"(parity)
             : "memory");
         if (done) return true;
-        if ((i & 31u) == 31u && clock64() - t0 > kTcWaitCyc) return false;
+        if ((i & 31u) == 31u && clock64() - t0 > limit) return false;
     }
 }
 // The whole warp waits (every lane polls); the result is the same on every lane.  A

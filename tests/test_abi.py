@@ -70,6 +70,13 @@ def test_sizes(k3):
     with pytest.raises(k3.K3MoEError):
         k3.k3moe_workspace_bytes(cfg, -1)
     assert k3.k3moe_packed_bytes(k3_cfg(k3, d=0)) == 0
+    # the K3 shape's workspace, pinned so that it cannot grow unnoticed: under 1 MiB for one
+    # token; the last mat-vec T (447) is the peak below the tensor-core path; T = 4096
+    MiB = 1 << 20
+    assert w1 < 1 * MiB
+    assert k3.k3moe_workspace_bytes(cfg, 447) <= 211 * MiB
+    assert k3.k3moe_workspace_bytes(cfg, 448) == k3.k3moe_workspace_bytes(cfg, 447)
+    assert k3.k3moe_workspace_bytes(cfg, 4096) <= 910 * MiB
 
 
 def test_host_validation_rejects_before_launch(k3):
@@ -114,6 +121,16 @@ def test_host_validation_rejects_before_launch(k3):
     assert L.k3moe_pack_mxfp4(ctypes.byref(cfg), 0, 1, vp(A + 8), *([vp(A)] * 5), vp(A), big,
                               None, None) == 3
     assert k3.k3moe_strerror(4).startswith("workspace")
+    # the bounded-wait check: no workspace, a limit outside 1 .. 4e9 cycles
+    assert L.k3moe_check_wait_timeout(None, 1000, None) == 4
+    assert L.k3moe_check_wait_timeout(vp(A + 8), 1000, None) == 4
+    assert L.k3moe_check_wait_timeout(vp(A), 0, None) == 2
+    assert L.k3moe_check_wait_timeout(vp(A), 4000000001, None) == 2
+    # no-allocation forward: T beyond the largest any call accepts, a misaligned status word
+    nargs = lambda T, st: (ctypes.byref(cfg), T, vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), tb,
+                           vp(A), vp(A), vp(A), vp(A), st, None)
+    assert L.k3moe_forward_noalloc(*nargs((1 << 20) + 1, None)) == 2
+    assert L.k3moe_forward_noalloc(*nargs(0, vp(A + 2))) == 3
 
 
 def test_full_block_validation_and_sizes(k3):

@@ -90,3 +90,26 @@ def test_reference_arm_line(workload):
     assert line["config"]["workload"] == workload
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_two_workloads():
+    """A list of workloads gives one line: the first workload's record at the top level and
+    each other one's complete record under its own name (the default is the headline pair
+    decode_t1,prefill_t4096)."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny,full_tiny", "--steps", "1", "--warmup", "0",
+                        "--cpu-budget-s", "0.2"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["config"]["workload"] == "tiny" and line["value"] > 0
+    sub = line["full_tiny"]
+    assert sub["config"]["workload"] == "full_tiny" and sub["value"] > 0
+    for key in ("value", "unit", "ms_per_step", "cpu_baseline", "e2e", "config"):
+        assert key in sub, key
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.DEFAULT_WORKLOADS.split(",") == ["decode_t1", "prefill_t4096"]

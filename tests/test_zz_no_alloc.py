@@ -63,6 +63,23 @@ def test_noalloc_matches_forward_twice(k3, name):
 
 
 @pytest.mark.gpu
+def test_noalloc_zero_tokens_reports_clean_status(k3):
+    """No tokens: nothing is computed, and the optional status word still reports this
+    call (clean), not what an earlier call left there."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cfg = k3.k3moe_config(**ki.WORKLOADS["tiny"].config_kwargs())
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    L = k3.lib()
+    rc = L.k3moe_forward_noalloc(ctypes.byref(cfg), 0, None, None, None, None, None, None, 0,
+                                 None, None, None, None, status.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
+@pytest.mark.gpu
 def test_noalloc_refuses_oversized_t(k3):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
