@@ -218,7 +218,7 @@ cudaError_t launch_full(const k3moe_config &c, int hidden, int latent_norm, floa
     if (e != cudaSuccess) return e;
     // 3. the chosen experts, summed with their weights
     e = launch_forward(F.cl, T, z, idx, weight, offsets, perm, table, nullptr, nullptr, nullptr, acc, ws,
-                       F.latent, s);
+                       F.latent, s, /*x_is_input=*/false);    // z is written just before
     if (e != cudaSuccess) return e;
     // 4. RMSNorm of the aggregate
     timing_begin("latent_norm", s);

@@ -203,20 +203,21 @@ struct PrepArgs {
     int32_t *inv;        // [T * k]
     float *tok_scale;    // [2][T]
     uint16_t *xs;        // [T][d] f16: x * 2^-u per token (the routed experts' B operand)
-    int32_t *shctr;      // shared gate/up arrival counters, zeroed here
-    int n_shctr;
     int32_t *status;
     int32_t *abort;
+    int early;           // 1: x is complete at launch (its conversion need not wait)
 };
 
 // Block 0 validates the routing (offsets, idx and perm, through a copy of offsets in
 // shared memory) and builds the active list and the inverse permutation; block b >= 1
 // converts tokens [32(b-1), 32b): warp per token, its scale 2^-u (max|x_t| in [2^14, 2^15),
-// u in [-113, 113]) and the f16 row x * 2^-u.
+// u in [-113, 113]) and the f16 row x * 2^-u.  The kernel lets the gate/up kernel launch
+// at once (its shared items need nothing from here); the token conversion reads only x,
+// so when x is complete at launch it runs before the wait for the routing.
 __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
 {
-    pdl_wait();
     pdl_trigger();
+    if (blockIdx.x == 0 || !a.early) pdl_wait();
     __shared__ int32_t bad;
     __shared__ int32_t scan_tmp[32];
     __shared__ int32_t off[kMaxExperts + 1];
@@ -224,7 +225,10 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
     const int E = a.E, slots = a.T * a.k;
     if (blockIdx.x > 0) {
         const int t = (blockIdx.x - 1) * 32 + warp;
-        if (t >= a.T) return;
+        if (t >= a.T) {
+            if (lane == 0) pdl_wait();      // the grid completes after the routing did
+            return;
+        }
         const uint4 *row = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.d);
         const int n16 = a.d / 8;
         uint32_t m = 0;
@@ -265,6 +269,7 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
             }
             dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
         }
+        if (lane == 0) pdl_wait();          // the grid completes after the routing did
         return;
     }
     // with up to kPrepSlots slots, idx and perm are read into shared memory together with
@@ -283,7 +288,6 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
     } else {
         for (int s = tid; s < slots; s += blockDim.x) a.inv[s] = -1;
     }
-    for (int i = tid; i < a.n_shctr; i += blockDim.x) a.shctr[i] = 0;
     __syncthreads();
     const int32_t *pidx = small ? sidx : a.idx, *pperm = small ? sperm : a.perm;
     int32_t *pinv = small ? sinv : a.inv;
@@ -339,8 +343,7 @@ __global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
     if (tid == 0) {
         if (bad) atomicOr(a.status, bad);
         *a.abort = bad ? 1 : 0;
-        a.abort[1] = 0;                      // work counters of the two mat-vec kernels
-        a.abort[2] = 0;
+        a.abort[2] = 0;                      // the down kernel's work counter (it starts after this)
     }
 }
 
@@ -360,7 +363,9 @@ struct GemvArgs {
     uint16_t *hp;                   // SiTU output planes: hi at [0], lo at [rows * f]
     const int32_t *abort;
     int32_t *status;
-    int32_t *work;                  // [2] work counters (gate/up, down), zeroed by fwd_prep
+    int32_t *work;                  // [2] work counters: gate/up (reset by its last block), down (zeroed by fwd_prep)
+    int32_t *exits;                 // gate/up blocks that have finished (reset by the last)
+    int early;                      // 1: x is complete at launch (the gate/up shared items start at once)
 };
 
 struct Unit {         // one expert (routed or shared) with its tokens
@@ -369,17 +374,18 @@ struct Unit {         // one expert (routed or shared) with its tokens
     int tok0, ntok;   // routed: positions [tok0, tok0+ntok) of perm; shared: tokens [0, T)
 };
 
-__device__ __forceinline__ Unit unit_of(const GemvArgs &a, int n_active, int u)
+// u >= 0: the u-th active routed expert; u < 0: shared expert -1 - u.
+__device__ __forceinline__ Unit unit_of(const GemvArgs &a, int u)
 {
     Unit r;
-    if (u < n_active) {
+    if (u >= 0) {
         r.shared = 0;
         r.id = min(max(a.active[u], 0), a.E - 1);
         r.tok0 = a.offsets[r.id];
         r.ntok = a.offsets[r.id + 1] - r.tok0;
     } else {
         r.shared = 1;
-        r.id = u - n_active;
+        r.id = -1 - u;
         r.tok0 = 0;
         r.ntok = a.T;
     }
@@ -420,23 +426,21 @@ struct Item {
     int kp, nkp;                    // K part of a shared item (routed: 0 of 1)
 };
 __device__ __forceinline__ int shared_passes(const GemvArgs &a) { return max(1, (a.T + kPassTok - 1) / kPassTok); }
+// Shared items first: they depend on nothing the routing produces, so the gate/up kernel
+// streams them while the router and the forward's prep are still running (it waits for
+// them only before its first routed item), and a whole shared item (bf16, four times the
+// bytes of a packed one) outlasts a routed one anyway.  A routed item holds all passes of
+// its expert; a shared item one token pass (gate/up: one of P K parts).
 template <int MODE>
-__device__ __forceinline__ int n_items_of(const GemvArgs &a, int n_active)
+__device__ __forceinline__ int n_shared_items(const GemvArgs &a)
 {
-    const int nrb = Geo<MODE>::rows(a) / kItemRows;
-    return (a.S * shared_passes(a) * Geo<MODE>::Psh(a) + n_active) * nrb;
+    return a.S * shared_passes(a) * Geo<MODE>::Psh(a) * (Geo<MODE>::rows(a) / kItemRows);
 }
-// Items are handed out longest first.  A routed item holds all passes of its expert; a
-// shared item one token pass (gate/up: one of P K parts).  Measured per-item times: a
-// whole shared item (bf16, four times the bytes of a packed one) outlasts a routed one, so
-// shared items go first; but gate/up shared items cut into K parts (P > 1) are outlasted
-// by the routed items (packed, the e2m1 decode on every weight), which then go first.
 template <int MODE>
-__device__ __forceinline__ Item item_of(const GemvArgs &a, int n_active, int i)
+__device__ __forceinline__ Item item_of(const GemvArgs &a, int i)
 {
     const int nrb = Geo<MODE>::rows(a) / kItemRows;
     const int nsp = shared_passes(a), P = Geo<MODE>::Psh(a), n_sh = a.S * nsp * P * nrb;
-    if (P > 1) i = i < n_active * nrb ? i + n_sh : i - n_active * nrb;
     Item it;
     if (i < n_sh) {
         it.rb = i % nrb;
@@ -446,7 +450,7 @@ __device__ __forceinline__ Item item_of(const GemvArgs &a, int n_active, int i)
         j /= P;
         it.pass0 = j % nsp;
         it.pass1 = it.pass0 + 1;
-        it.u = n_active + j / nsp;
+        it.u = -1 - j / nsp;
     } else {
         const int j = i - n_sh;
         it.rb = j % nrb;
@@ -705,7 +709,9 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                                                              const __grid_constant__ CUtensorMap m3,
                                                              const __grid_constant__ CUtensorMap m2)
 {
-    pdl_wait();
+    // gate/up: launched early (programmatic dependent launch) and waits for the routing only
+    // before its first routed item; down: waits for gate/up first
+    if (MODE == kDown || !a.early) pdl_wait();
     pdl_trigger();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -723,9 +729,8 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
     __shared__ __align__(16) int32_t bflag[kBSlots][4];
     __shared__ int bail;
 
-    if (*a.abort) return;
-    const int n_active = min(max(a.active[a.E], 0), a.E);
-    const int n_items = n_items_of<MODE>(a, n_active);
+    if (MODE == kDown && *a.abort) return;
+    const int n_sh = n_shared_items<MODE>(a);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int nwarps = kThreads / 32;
     if (tid == 0) {
@@ -753,11 +758,18 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
         // bulk copies; nothing here waits for data
         int n = 0, bu = 0;
         bool stop = false;
+        int n_items = -1;                       // known once the routing is
         for (;;) {
             int i = 0;
             if (lane == 0) i = atomicAdd(&a.work[MODE], 1);
             i = __shfl_sync(0xffffffffu, i, 0);
-            const bool done = i >= n_items || __shfl_sync(0xffffffffu, bail, 0) != 0;
+            if (i >= n_sh && n_items < 0) {
+                // the first routed item: the routing (and the forward's prep) must be complete
+                if (MODE == kGateUp) pdl_wait();
+                const int n_active = *a.abort ? 0 : min(max(a.active[a.E], 0), a.E);
+                n_items = n_sh + n_active * (Geo<MODE>::rows(a) / kItemRows);
+            }
+            const bool done = (i >= n_sh && i >= n_items) || __shfl_sync(0xffffffffu, bail, 0) != 0;
             if (done) {
                 // end of stream: one stage with no copy
                 const int slot = n % kStages;
@@ -768,8 +780,8 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                 }
                 break;
             }
-            const Item it = item_of<MODE>(a, n_active, i);
-            const Unit un = unit_of(a, n_active, it.u);
+            const Item it = item_of<MODE>(a, i);
+            const Unit un = unit_of(a, it.u);
             const int pass1 = it.pass1 < 0 ? n_passes(un) : it.pass1;
             const int nst = n_stages<MODE, TPS>(a, un.shared);
             for (int pass = it.pass0; pass < pass1 && !stop; pass++) {
@@ -984,6 +996,19 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
         for (int s = 0; s < kBSlots; s++)
             if (bissued[s] > 0) mbar_wait(&bfull[s], (uint32_t)(bissued[s] - 1) & 1u);
     }
+    if (MODE == kGateUp && tid == 0) {
+        // the grid completes only after the routing did (the next kernel's wait covers both)
+        pdl_wait();
+        // the last block to leave resets the work counter and the K-part arrival counters
+        // for the next call (prep cannot: this kernel may run before it)
+        __threadfence();
+        if (atomicAdd(a.exits, 1) == (int)gridDim.x - 1) {
+            a.work[MODE] = 0;
+            for (int q = 0; q < a.S * (a.f / kItemRows); q++) a.shctr[q] = 0;
+            __threadfence();
+            *a.exits = 0;
+        }
+    }
 }
 
 // -------------------------------------------------------------------------------- combine
@@ -1172,7 +1197,7 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
                                 const int32_t *idx, const float *weight, const int32_t *offsets,
                                 const int32_t *perm, const uint8_t *table, const uint16_t *sh_w1,
                                 const uint16_t *sh_w3, const uint16_t *sh_w2, float *out,
-                                uint8_t *ws, const WsLayout &L, cudaStream_t s)
+                                uint8_t *ws, const WsLayout &L, cudaStream_t s, bool x_is_input)
 {
     int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
     int32_t *abort = status + 1;
@@ -1185,8 +1210,8 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
     int32_t *shctr = reinterpret_cast<int32_t *>(ws + L.shctr);
     float *gush = reinterpret_cast<float *>(ws + L.gush);
-    PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, xs, shctr,
-                c.n_shared * (c.f / kTileRows), status, abort};
+    PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, xs, status, abort,
+                x_is_input ? 1 : 0};
     timing_begin("fwd_prep", s);
     cudaError_t err = launch_pdl(fwd_prep_kernel, dim3(1 + (T + 31) / 32), dim3(1024), 0, s, pa);
     count_launch();
@@ -1202,7 +1227,8 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     }
     GemvArgs ga{T, c.d, c.f, c.top_k, c.n_shared, c.n_experts, 0, c.situ_b1, c.situ_b2,
                 x, xs, offsets, perm, active, tok_scale, table, expert_bytes(c.d, c.f),
-                gateup_block_bytes(c.d, c.f), ys, gush, shctr, hp, abort, status, abort + 1};
+                gateup_block_bytes(c.d, c.f), ys, gush, shctr, hp, abort, status, abort + 1, status + 5,
+                x_is_input ? 1 : 0};
     // B chunks hold min(16, T) token rows
     ga.brows = T < kPassTok ? T : kPassTok;
     {

@@ -83,9 +83,13 @@ static_assert(3 * (kMaxWidth / kTileRows) * 4 <= kTrailerBytes - 4,
               "the block maxima and the flag word share the trailer");
 
 // Device status word and abort flag live in the first 256 bytes of the workspace.
+// Words: 0 status (K3MOE_DEV_* bits); 1 abort (nonzero: the routing failed validation,
+// later kernels skip work); 2, 3 the work counters of the two mat-vec kernels; 4 the
+// top-k kernel's last-block counter; 5 the gate/up mat-vec's exit counter.  Counters are
+// back at zero after every call.
 struct StatusBlock {
-    int32_t status;   // K3MOE_DEV_* bits
-    int32_t abort;    // nonzero: inputs failed validation, later kernels skip work
+    int32_t status;
+    int32_t abort;
     int32_t pad[62];
 };
 
@@ -281,23 +285,26 @@ inline cudaError_t launch_forward(const k3moe_config &c, int T, const uint16_t *
                                   const float *weight, const int32_t *offsets, const int32_t *perm,
                                   const uint8_t *table, const uint16_t *sh_w1, const uint16_t *sh_w3,
                                   const uint16_t *sh_w2, float *out, uint8_t *ws, const WsLayout &L,
-                                  cudaStream_t s);
+                                  cudaStream_t s, bool x_is_input = true);
+// x_is_input: x is complete when the call is made (not written by the kernel launched just
+// before with programmatic dependent launch), so the mat-vec path may read it before its
+// wait for the routing.
 cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
                                 const int32_t *idx, const float *weight, const int32_t *offsets,
                                 const int32_t *perm, const uint8_t *table, const uint16_t *sh_w1,
                                 const uint16_t *sh_w3, const uint16_t *sh_w2, float *out,
-                                uint8_t *ws, const WsLayout &L, cudaStream_t s);
+                                uint8_t *ws, const WsLayout &L, cudaStream_t s, bool x_is_input = true);
 
 inline cudaError_t launch_forward(const k3moe_config &c, int T, const uint16_t *x, const int32_t *idx,
                                   const float *weight, const int32_t *offsets, const int32_t *perm,
                                   const uint8_t *table, const uint16_t *sh_w1, const uint16_t *sh_w3,
                                   const uint16_t *sh_w2, float *out, uint8_t *ws, const WsLayout &L,
-                                  cudaStream_t s)
+                                  cudaStream_t s, bool x_is_input)
 {
     return L.gemm ? launch_forward_gemm(c, T, x, idx, weight, offsets, perm, table, sh_w1, sh_w3, sh_w2,
                                         out, ws, L, s)
                   : launch_forward_gemv(c, T, x, idx, weight, offsets, perm, table, sh_w1, sh_w3, sh_w2,
-                                        out, ws, L, s);
+                                        out, ws, L, s, x_is_input);
 }
 
 // ----------------------------------------------------------------------------------- device helpers

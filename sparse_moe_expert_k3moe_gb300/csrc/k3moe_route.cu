@@ -118,19 +118,19 @@ __device__ __forceinline__ float exact_logit_warp(const uint4 *xs, const uint4 *
                                                   int lane)
 {
     Acc2 a0{0.0f, 0.0f}, a1{0.0f, 0.0f};
-    int m = 0;
-    for (; lane + 32 * (m + 3) < nchunk; m += 4) {
-        const uint4 w0 = __ldg(wrow + lane + 32 * m), w1 = __ldg(wrow + lane + 32 * (m + 1));
-        const uint4 w2 = __ldg(wrow + lane + 32 * (m + 2)), w3 = __ldg(wrow + lane + 32 * (m + 3));
-        acc_chunk(a0, xs[lane + 32 * m], w0);
-        acc_chunk(a1, xs[lane + 32 * (m + 1)], w1);
-        acc_chunk(a0, xs[lane + 32 * (m + 2)], w2);
-        acc_chunk(a1, xs[lane + 32 * (m + 3)], w3);
-    }
-    for (; lane + 32 * m < nchunk; m++) {
-        const uint4 w = __ldg(wrow + lane + 32 * m);
-        if (m & 1) acc_chunk(a1, xs[lane + 32 * m], w);
-        else acc_chunk(a0, xs[lane + 32 * m], w);
+    // eight router chunks in flight per lane, then added in order (pair m & 1)
+    for (int m0 = 0; lane + 32 * m0 < nchunk; m0 += 8) {
+        uint4 w[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const int c = lane + 32 * (m0 + j);
+            w[j] = c < nchunk ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const int c = lane + 32 * (m0 + j);
+            if (c < nchunk) acc_chunk((j & 1) ? a1 : a0, xs[c], w[j]);
+        }
     }
     return acc_finish(a0, a1);
 }
@@ -144,13 +144,13 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
     pdl_wait();
     pdl_trigger();
     extern __shared__ __align__(16) uint8_t xs_raw[];        // kScoreTok x d bf16
+    __shared__ float lg[kScoreWarps][kScoreTok];               // a round's logits
     uint4 *xs = reinterpret_cast<uint4 *>(xs_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kScoreWarps + warp;
     const int nchunk = d / 8;                                  // 16-byte chunks per row
     const int tb0 = blockIdx.y * kScoreTokBlock, tb1 = min(T, tb0 + kScoreTokBlock);
     const uint4 *wrow = reinterpret_cast<const uint4 *>(wr + (size_t)min(e, E - 1) * d);
-    const float b = (bias && e < E) ? bias[e] : 0.0f;
     // the first 4096 columns of the row stay in registers across the token rounds (the
     // whole row for d <= 4096); their loads are in flight with the first x tile's
     uint4 w0[kScoreChunks];
@@ -187,18 +187,23 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
                 }
             }
         }
-        float logit = 0.0f;
 #pragma unroll
         for (int i = 0; i < kScoreTok; i++) {
             if (i >= nt) break;
             const float v = acc_finish(acc[i][0], acc[i][1]);
-            if (lane == i) logit = v;
+            if (lane == i) lg[warp][i] = v;
         }
-        if (e < E && lane < nt) {
-            float s, ch;
-            exact_scores(logit, b, s, ch);
-            sc_out[(size_t)(t0 + lane) * E + e] = s;
-            ch_out[(size_t)(t0 + lane) * E + e] = ch;
+        __syncthreads();
+        // the round's sigmoids by warp 0, lane = 8 * (expert of the block) + token: the
+        // double exponential runs on the slow fp64 pipe, once per round instead of per warp
+        if (warp == 0) {
+            const int we = lane / kScoreTok, i = lane % kScoreTok, ee = blockIdx.x * kScoreWarps + we;
+            if (i < nt && ee < E) {
+                float s, ch;
+                exact_scores(lg[we][i], bias ? bias[ee] : 0.0f, s, ch);
+                sc_out[(size_t)(t0 + i) * E + ee] = s;
+                ch_out[(size_t)(t0 + i) * E + ee] = ch;
+            }
         }
     }
 }
@@ -419,8 +424,8 @@ __device__ __forceinline__ float sigmoid_bound(float v) { return 1.0f / (1.0f + 
 // exactly and the selection is the top k of their exact keys.
 __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
 {
+    pdl_trigger();      // the next kernel may launch now: it waits for this one
     pdl_wait();
-    pdl_trigger();
     extern __shared__ __align__(16) uint8_t tk_dyn[];   // re-scoring: the token row, d bf16
     __shared__ uint64_t lists[2][32][kMaxTopK];
     __shared__ int32_t cnt[kMaxExperts];                 // map counts; re-scoring: the candidates
@@ -487,17 +492,23 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
         if (i == 1023) n_cand = base + __popc(m);
         __syncthreads();
         const int C = n_cand;
-        // exact scores of the candidates, one warp per candidate
+        // exact logits of the candidates, one warp per candidate; then their scores, one
+        // thread per candidate (the double exponential runs on the slow fp64 pipe, so it
+        // is issued once per 32 candidates instead of once per candidate)
         const uint4 *wr = reinterpret_cast<const uint4 *>(a.wr);
+        float *lgx = reinterpret_cast<float *>(ckey) + kMaxExperts;   // upper half of ckey
         for (int c = warp; c < C; c += 32) {
-            const int e = cnt[c];
-            const float logit = exact_logit_warp(xs, wr + (size_t)e * nchunk, nchunk, lane);
-            if (lane == 0) {
-                float sv, cv;
-                exact_scores(logit, a.bias ? a.bias[e] : 0.0f, sv, cv);
-                scx[e] = sv;
-                ckey[c] = choice_key(cv, e);
-            }
+            const float logit = exact_logit_warp(xs, wr + (size_t)cnt[c] * nchunk, nchunk, lane);
+            if (lane == 0) lgx[c] = logit;
+        }
+        __syncthreads();
+        float sv = 0.0f, cv = 0.0f;
+        const int e_c = i < C ? cnt[i] : 0;
+        if (i < C) exact_scores(lgx[i], a.bias ? a.bias[e_c] : 0.0f, sv, cv);
+        __syncthreads();
+        if (i < C) {
+            scx[e_c] = sv;
+            ckey[i] = choice_key(cv, e_c);
         }
         __syncthreads();
         top = block_top16(i < C ? ckey[i] : 0, C, lists);
@@ -558,8 +569,8 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
 
 __global__ void __launch_bounds__(1024) perm_count_kernel(MapArgs a)
 {
+    pdl_trigger();      // the next kernel may launch now: it waits for this one
     pdl_wait();
-    pdl_trigger();
     __shared__ int32_t cnt[kMaxExperts];
     __shared__ int32_t slot_e[kChunkTokens * kMaxTopK];
     __shared__ int32_t scan_tmp[32];
@@ -573,8 +584,8 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int n_chunks, int E, in
                                                          int32_t *__restrict__ chunk_base,
                                                          int32_t *__restrict__ offsets)
 {
+    pdl_trigger();      // the next kernel may launch now: it waits for this one
     pdl_wait();
-    pdl_trigger();
     __shared__ int32_t scan_tmp[32];
     const int e = threadIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -619,8 +630,8 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(int total_slots, int 
                                                            const int32_t *__restrict__ local_rank,
                                                            int32_t *__restrict__ perm)
 {
+    pdl_trigger();      // the next kernel may launch now: it waits for this one
     pdl_wait();
-    pdl_trigger();
     const int s = blockIdx.x * blockDim.x + threadIdx.x;
     if (s >= total_slots) return;
     const int e = idx[s];

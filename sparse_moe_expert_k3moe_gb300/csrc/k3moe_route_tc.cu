@@ -39,7 +39,9 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_logits_tc_kernel(const R
                                                                          const __grid_constant__ CUtensorMap mwr,
                                                                          const __grid_constant__ CUtensorMap mx)
 {
-    pdl_wait();
+    // the logits need nothing from the kernel before (the row-norm kernel, launched first,
+    // which waited for the previous call): start at once, and wait for it only before
+    // leaving, so that the top-k's wait on this grid covers both
     pdl_trigger();
     extern __shared__ __align__(1024) uint8_t rsm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) & ~(uintptr_t)1023);
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_logits_tc_kernel(const R
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kRtTmemCols));
     }
+    if (threadIdx.x == 0) pdl_wait();
 }
 
 // The tensor-core kernels' bounded wait (mb_wait) on an mbarrier nothing arrives on,
