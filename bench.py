@@ -127,17 +127,17 @@ def block_bytes_flops(w, distinct_experts: int):
 
 
 def full_kernel_work(name: str, w, distinct_experts: int):
-    """kernel_work for a full-width block: its dense GEMMs (weights, activations in and
-    out; 2*m*n*k FLOPs), else the layer's kernels as the block runs them (router on width
-    H, experts on the latent without shared experts)."""
+    """kernel_work for a full-width block: its dense projections (weights, activations in
+    and out; 2*m*n*k FLOPs), else the layer's kernels as the block runs them (router on
+    width H, experts on the latent without shared experts)."""
     T, H, d, SI = w.T, w.hidden, w.d, w.S * w.f
-    if name == "full_down_gemm":
+    if name == "full_down_proj":
         return d * H * 2 + T * H * 2 + T * d * 2, 2 * T * d * H
-    if name == "full_up_gemm":
+    if name == "full_up_proj":
         return H * d * 2 + T * d * 2 + T * H * 4, 2 * T * H * d
-    if name in ("full_shared_gate_gemm", "full_shared_up_gemm"):
-        return SI * H * 2 + T * H * 2 + T * SI * 4, 2 * T * SI * H
-    if name == "full_shared_down_gemm":
+    if name == "full_shared_gateup":
+        return 2 * SI * H * 2 + T * H * 2 + T * SI * 2, 2 * 2 * T * SI * H
+    if name == "full_shared_down":
         return H * SI * 2 + T * SI * 2 + 2 * T * H * 4, 2 * T * H * SI
     if name in ("router_scores", "router_logits_tc", "router_wnorm"):
         return kernel_work(name, w.with_(d=H, hidden=0), distinct_experts)
@@ -210,6 +210,8 @@ def peaks():
 KERNEL_SOURCES = {
     "gemv_gateup": ["k3moe_gemv.cu"], "gemv_down": ["k3moe_gemv.cu"],
     "gemm_gateup": ["k3moe_gemm.cu", "k3moe_tc.cuh"], "gemm_down": ["k3moe_gemm.cu", "k3moe_tc.cuh"],
+    "full_down_proj": ["k3moe_dense.cu", "k3moe_tc.cuh"], "full_up_proj": ["k3moe_dense.cu", "k3moe_tc.cuh"],
+    "full_shared_gateup": ["k3moe_dense.cu", "k3moe_tc.cuh"], "full_shared_down": ["k3moe_dense.cu", "k3moe_tc.cuh"],
     "router_logits_tc": ["k3moe_route_tc.cu", "k3moe_tc.cuh"],
 }
 
@@ -547,7 +549,7 @@ def measure(w, args, rank, world, local, dev):
                    "n_shared": w.S, **({"hidden": w.hidden, "latent_norm": w.latent_norm}
                                        if w.hidden else {}),
                    "weights": "routed MXFP4 (E2M1 + E8M0/32), shared bf16"
-                              + (", dense projections bf16 (cuBLASLt)" if w.hidden else ""),
+                              + (", dense projections bf16" if w.hidden else ""),
                    "arithmetic": ARITHMETIC,
                    "l2": "512 MiB buffer written between timed steps",
                    "launch": "one CUDA graph replay per step" if args.graph else "eager",

@@ -240,8 +240,9 @@ typedef struct k3moe_full_dims {
 } k3moe_full_dims;
 
 /* Workspace bytes k3moe_full_forward needs for any 0 <= T <= T_max (the
- * layer's regions plus the block's z, a and shared intermediates and a 32 MiB
- * GEMM scratch). */
+ * layer's regions plus the block's z, a and shared intermediates, and the
+ * projections' split-K partial sums: up to 1024 rows of the widest
+ * projection). */
 k3moe_status k3moe_full_workspace_bytes(const k3moe_config *cfg, const k3moe_full_dims *fd,
                                         int32_t T_max, size_t *bytes);
 
@@ -254,9 +255,9 @@ k3moe_status k3moe_full_workspace_bytes(const k3moe_config *cfg, const k3moe_ful
  *   sh_w1, sh_w3 [SI][H] bf16;  sh_w2 [H][SI] bf16 (NULL when n_shared == 0)
  *   idx, weight, offsets, perm: out, the routing, as k3moe_route writes it
  *   out        [T][H] f32, written
- * Matrices and h 16-byte aligned; expert_table 256-byte aligned.  The three
- * dense projections run as bf16 GEMMs with fp32 accumulation (cuBLASLt, loaded
- * at first use; K3MOE_ECUDA when it cannot be loaded or fails), so z, the
+ * Matrices and h 16-byte aligned; expert_table 256-byte aligned.  The dense
+ * projections (Wd, Wu, the fused Sh1/Sh3 with SiTU, Sh2) run on the library's
+ * tensor-core kernel with bf16 operands and fp32 accumulation, so z, the
  * normed a and the shared SiTU output are rounded to bf16 as their inputs.
  * T may be 0 (offsets zeroed, nothing else written).  ws per
  * k3moe_full_workspace_bytes(T_max >= T); its status word as k3moe_route's. */

@@ -345,8 +345,7 @@ class MoEBlock:
     """Holds one full-width block's device tensors (the routed experts' packed table,
     the full-width router, the down and up projections, the norm gain and the fused
     shared experts) and a workspace, and calls k3moe_full_forward.  Allocation is
-    torch's; every computation is the library's (and cuBLASLt's, for the three dense
-    projections)."""
+    torch's; every computation is the library's."""
 
     def __init__(self, cfg: K3MoEConfig, fd: K3MoEFullDims, T_max: int, device="cuda"):
         import torch

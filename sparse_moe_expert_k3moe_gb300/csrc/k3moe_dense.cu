@@ -1,0 +1,297 @@
+// k3moe_dense.cu -- the dense projections of the full-width block (kimi-k3-in-c README,
+// Part II, section 9 "Picking 16 experts of 896", the k3_moe listing: step 2 z = Wd h,
+// step 5 out = Wu a, step 6 the fused shared experts Sh1, Sh3 and Sh2):
+//   y[t][n] = epilogue(sum_k x[t][k] W[n][k]),  x [T][K] and W [N][K] bf16 (rows = outputs),
+// fp32 accumulation on the tensor cores (tcgen05, operands staged by TMA).
+//
+// Swap AB: M = 128 weight rows (a row block), N = a tile of up to 256 tokens (a multiple
+// of 16; 128 for the gated form, which keeps two accumulators), K in 64-column stages.  A
+// work item is (row block, token tile, K part).  Few tokens leave few items (28 row blocks
+// of Wd at T = 1), so K is cut into P parts until the items fill the GPU: each part
+// stores its fp32 partial sums, and for each 32-row quadrant of the row block the last
+// part to finish adds the P partials in order p = 0..P-1 and applies the epilogue -- a
+// fixed order, so results do not vary from run to run.  With one part the epilogue
+// reads the accumulators directly.
+//
+// Epilogues: bf16 store (z), f32 store (out), f32 add (out += Sh2 act: every element
+// belongs to one item, so a plain read-modify-write), and the gated form: two matrices W1
+// and W3 with one accumulator each, y = bf16(SiTU(g, u)) with g = W1 x, u = W3 x.
+//
+// Warp roles, one persistent block per SM: warp 0 TMA producer, warp 1 MMA issue, warps
+// 2-5 epilogue (one weight row per thread, 32x32b tensor-memory loads).  Every wait is
+// bounded; a timeout sets the status word, the roles drop out, copies in flight land and
+// the tensor memory is freed before the block leaves.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "k3moe_internal.cuh"
+#include "k3moe_tc.cuh"
+
+namespace k3moe {
+namespace {
+
+constexpr int kDnBM = 128, kDnBK = 64;
+constexpr int kDnABytes = kDnBM * kDnBK * 2;                  // one weight tile: 16 KB
+constexpr int kDnSmemBudget = 200 * 1024;                      // the stage ring
+constexpr int kDnMaxStg = 8;
+constexpr int kDnWarpProd = 0, kDnWarpMma = 1, kDnWarpEpi0 = 2, kDnNumEpi = 4;
+constexpr int kDnThreads = (kDnWarpEpi0 + kDnNumEpi) * 32;     // 192
+constexpr int kDnTmemCols = 512;
+
+struct DenseArgs {
+    int T, N, K, epi;
+    int bn, P, n_rb, n_tt, nkp, nstg, stage_bytes;
+    float b1, b2;
+    void *y;
+    float *part;                   // [P][mats][T][N] partial sums (P > 1)
+    int32_t *ctr;                  // [n_rb][n_tt][4] arrival counters (P > 1), back at zero after
+    int32_t *status;
+};
+
+__device__ __forceinline__ float situ_f(float g, float u, float b1, float b2)
+{
+    const float a = b1 * tanhf(g / b1) * (1.0f / (1.0f + expf(-g)));
+    return a * (b2 * tanhf(u / b2));
+}
+
+// Output element (t, n) from its sum (and the up sum for the gated form).
+__device__ __forceinline__ void dense_store(const DenseArgs &a, int t, int n, float v, float u)
+{
+    const size_t o = (size_t)t * a.N + n;
+    if (a.epi == kDenseBf16 || a.epi == kDenseSitu) {
+        const float r = a.epi == kDenseSitu ? situ_f(v, u, a.b1, a.b2) : v;
+        const __nv_bfloat16 b = __float2bfloat16_rn(r);
+        reinterpret_cast<uint16_t *>(a.y)[o] = *reinterpret_cast<const uint16_t *>(&b);
+    } else if (a.epi == kDenseF32) {
+        reinterpret_cast<float *>(a.y)[o] = v;
+    } else {
+        reinterpret_cast<float *>(a.y)[o] += v;
+    }
+}
+
+__global__ void __launch_bounds__(kDnThreads, 1) dense_tc_kernel(const DenseArgs a,
+                                                                 const __grid_constant__ CUtensorMap mw,
+                                                                 const __grid_constant__ CUtensorMap mw3,
+                                                                 const __grid_constant__ CUtensorMap mx)
+{
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ __align__(1024) uint8_t dsm_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t full[kDnMaxStg], empty[kDnMaxStg], acc_full[2], acc_empty[2], drain;
+    __shared__ uint32_t tmem_base;
+    __shared__ int bail;
+
+    const bool gated = a.epi == kDenseSitu;
+    const int mats = gated ? 2 : 1;
+    const int n_items = a.n_rb * a.n_tt * a.P, nstg = a.nstg;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nstg; s++) { mb_init(&full[s], 1); mb_init(&empty[s], 1); }
+        for (int b = 0; b < 2; b++) { mb_init(&acc_full[b], 1); mb_init(&acc_empty[b], kDnNumEpi); }
+        mb_init(&drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        bail = 0;
+    }
+    if (warp == kDnWarpMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tmem_base)),
+                     "r"(kDnTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    auto timeout = [&]() {
+        set_status(a.status, K3MOE_DEV_TIMEOUT);
+        bail = 1;
+    };
+    // item i -> K part, row block, token tile
+    auto part_of = [&](int i) { return i % a.P; };
+    auto rb_of = [&](int i) { return (i / a.P) % a.n_rb; };
+    auto tt_of = [&](int i) { return i / (a.P * a.n_rb); };
+
+    if (warp == kDnWarpProd) {
+        if (lane == 0) {
+            uint32_t st = 0;
+            for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
+                const int p = part_of(i), rb = rb_of(i), t0 = tt_of(i) * a.bn;
+                const int bn = (min(a.bn, a.T - t0) + 15) & ~15;
+                for (int ks = p * a.nkp; ks < (p + 1) * a.nkp; ks++, st++) {
+                    const int s = st % nstg;
+                    if (st >= (uint32_t)nstg && !mb_wait(&empty[s], ((st / nstg) - 1) & 1u)) {
+                        timeout();
+                        break;
+                    }
+                    uint8_t *stage = sm + (size_t)s * a.stage_bytes;
+                    mb_expect_tx(&full[s], (uint32_t)(mats * kDnABytes + bn * kDnBK * 2));
+                    tma2d(stage, &mw, ks * kDnBK, rb * kDnBM, &full[s]);
+                    if (gated) tma2d(stage + kDnABytes, &mw3, ks * kDnBK, rb * kDnBM, &full[s]);
+                    uint8_t *bs = stage + mats * kDnABytes;
+                    for (int j = 0; j < bn / 16; j++) tma2d(bs + j * 16 * 128, &mx, ks * kDnBK, t0 + 16 * j, &full[s]);
+                }
+            }
+            if (bail)   // wait (bounded) for the copies already issued
+                for (uint32_t f = st > (uint32_t)nstg ? st - nstg : 0; f < st; f++)
+                    mb_wait(&full[f % nstg], (f / nstg) & 1u);
+        }
+    } else if (warp == kDnWarpMma) {
+        if (lane == 0) {
+            uint32_t st = 0, n = 0;
+            for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x, n++) {
+                const int p = part_of(i), t0 = tt_of(i) * a.bn;
+                const int bn = (min(a.bn, a.T - t0) + 15) & ~15;
+                const uint32_t id = idesc(1, bn);
+                const int buf = n & 1;
+                if (n >= 2 && !mb_wait(&acc_empty[buf], ((n >> 1) - 1) & 1u)) { timeout(); break; }
+                tc_fence_after();
+                const uint32_t d0 = tmem + (uint32_t)buf * 256u;        // gated: g at d0, u at d0 + 128
+                for (int ks = p * a.nkp; ks < (p + 1) * a.nkp; ks++, st++) {
+                    const int s = st % nstg;
+                    if (!mb_wait(&full[s], (st / nstg) & 1u)) { timeout(); break; }
+                    tc_fence_after();
+                    const uint8_t *stage = sm + (size_t)s * a.stage_bytes;
+                    const uint32_t A = saddr(stage), B = saddr(stage + mats * kDnABytes);
+                    const bool first = ks == p * a.nkp;
+#pragma unroll
+                    for (int kk = 0; kk < kDnBK / 16; kk++) {
+                        umma(d0, sdesc(A + kk * 32), sdesc(B + kk * 32), id, (!first || kk) ? 1u : 0u);
+                        if (gated)
+                            umma(d0 + 128u, sdesc(A + kDnABytes + kk * 32), sdesc(B + kk * 32), id,
+                                 (!first || kk) ? 1u : 0u);
+                    }
+                    umma_commit(&empty[s]);
+                }
+                if (bail) break;
+                umma_commit(&acc_full[buf]);
+            }
+            umma_commit(&drain);                       // every issued MMA done before the dealloc
+            mb_wait(&drain, 0);
+        }
+    } else {
+        // ---------------- epilogue: weight row 32q + lane of the row block per thread
+        const int q = warp & 3;                         // tensor-memory lane quadrant of this warp
+        const int row = 32 * q + lane;
+        uint32_t n = 0;
+        for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x, n++) {
+            const int p = part_of(i), rb = rb_of(i), tt = tt_of(i), t0 = tt * a.bn;
+            const int ncols = min(a.bn, a.T - t0);
+            const int bn = (ncols + 15) & ~15;
+            const int nr = rb * kDnBM + row;             // output column n of this thread
+            const int buf = n & 1;
+            if (!mb_wait_warp(&acc_full[buf], (n >> 1) & 1u)) { timeout(); break; }
+            tc_fence_after();
+            const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * 256u;
+            for (int c0 = 0; c0 < bn; c0 += 16) {
+                float v[16], u[16];
+                tmem_ld16(lane_addr + c0, v);
+                if (gated) tmem_ld16(lane_addr + 128u + c0, u);
+#pragma unroll
+                for (int jj = 0; jj < 16; jj++) {
+                    const int t = t0 + c0 + jj;
+                    if (c0 + jj >= ncols) break;
+                    if (a.P == 1) {
+                        dense_store(a, t, nr, v[jj], gated ? u[jj] : 0.0f);
+                    } else {
+                        float *pp = a.part + (((size_t)p * mats) * a.T + t) * a.N + nr;
+                        pp[0] = v[jj];
+                        if (gated) pp[(size_t)a.T * a.N] = u[jj];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mb_arrive(&acc_empty[buf]);
+            if (a.P > 1) {
+                // the last of the P parts of this quadrant adds the partials in order
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) {
+                    int32_t *c = a.ctr + ((size_t)rb * a.n_tt + tt) * 4 + q;
+                    last = atomicAdd(c, 1) == a.P - 1;
+                    if (last) *c = 0;
+                }
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    __threadfence();
+                    for (int c = 0; c < ncols; c++) {
+                        const int t = t0 + c;
+                        float sv = 0.0f, su = 0.0f;
+                        for (int pp = 0; pp < a.P; pp++) {
+                            const float *src = a.part + (((size_t)pp * mats) * a.T + t) * a.N + nr;
+                            sv += __ldcg(src);
+                            if (gated) su += __ldcg(src + (size_t)a.T * a.N);
+                        }
+                        dense_store(a, t, nr, sv, su);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kDnWarpMma) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kDnTmemCols));
+    }
+}
+
+}  // namespace
+
+DensePlan dense_plan(int T, int N, int K, int epi)
+{
+    DensePlan pl{};
+    const bool gated = epi == kDenseSitu;
+    const int bn_max = gated ? 128 : 256;
+    pl.bn = T >= bn_max ? bn_max : std::max(16, (T + 15) & ~15);
+    pl.n_tt = (T + pl.bn - 1) / pl.bn;
+    pl.n_rb = N / kDnBM;
+    const int nks = K / kDnBK;
+    pl.P = 1;
+    // few items: cut K until they fill the GPU (kDenseTargetItems), at least 4 stages a
+    // part, and at most kDensePartRows partial rows (P * T)
+    while ((long long)pl.n_rb * pl.n_tt * pl.P * 2 <= kDenseTargetItems && nks % (2 * pl.P) == 0 &&
+           nks / (2 * pl.P) >= 4 && (long long)2 * pl.P * T <= kDensePartRows)
+        pl.P *= 2;
+    pl.nkp = nks / pl.P;
+    pl.mats = gated ? 2 : 1;
+    pl.stage_bytes = pl.mats * kDnABytes + pl.bn * kDnBK * 2;
+    pl.nstg = std::min(kDnMaxStg, kDnSmemBudget / pl.stage_bytes);
+    return pl;
+}
+
+bool dense_applies(int N, int K) { return N % kDnBM == 0 && K % kDnBK == 0; }
+
+cudaError_t launch_dense(int epi, int T, int N, int K, const uint16_t *x, const uint16_t *w,
+                         const uint16_t *w3, void *y, float b1, float b2, float *part, int32_t *ctr,
+                         int32_t *status, cudaStream_t s, const char *name)
+{
+    if (T <= 0) return cudaSuccess;
+    if (!dense_applies(N, K)) return cudaErrorInvalidValue;
+    const DensePlan pl = dense_plan(T, N, K, epi);
+    CUtensorMap mw{}, mw3{}, mx{};
+    if (!map16(&mw, w, (uint64_t)N, (uint64_t)K, kDnBM) ||
+        !map16(&mw3, epi == kDenseSitu ? w3 : w, (uint64_t)N, (uint64_t)K, kDnBM) ||
+        !map16(&mx, x, (uint64_t)T, (uint64_t)K, 16))
+        return cudaErrorInvalidValue;
+    const size_t smem = 1024 + (size_t)pl.nstg * pl.stage_bytes;
+    static size_t smem_set = 0;
+    if (smem > smem_set) {
+        cudaFuncSetAttribute(dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        smem_set = smem;
+    }
+    DenseArgs a{T, N, K, epi, pl.bn, pl.P, pl.n_rb, pl.n_tt, pl.nkp, pl.nstg, pl.stage_bytes, b1, b2,
+                y, part, ctr, status};
+    const int n_items = pl.n_rb * pl.n_tt * pl.P;
+    const int grid = std::max(1, std::min(num_sms(), n_items));
+    timing_begin(name, s);
+    const cudaError_t err = launch_pdl(dense_tc_kernel, dim3(grid), dim3(kDnThreads), smem, s, a, mw, mw3, mx);
+    count_launch();
+    timing_end(name, s);
+    return err;
+}
+
+}  // namespace k3moe

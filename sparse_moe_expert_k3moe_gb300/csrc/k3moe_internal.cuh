@@ -25,6 +25,7 @@
 // decode path does not give exactly.
 #pragma once
 
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -171,20 +172,34 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     return L;
 }
 
+// Dense projections (k3moe_dense.cu): y[t][n] = epilogue(sum_k x[t][k] W[n][k]).
+enum DenseEpi { kDenseBf16 = 0, kDenseF32 = 1, kDenseAddF32 = 2, kDenseSitu = 3 };
+constexpr int kDenseTargetItems = 456;   // work items that fill the GPU (3 per SM of 152)
+constexpr int kDensePartRows = 1024;     // at most this many partial rows (K parts x tokens)
+struct DensePlan {
+    int bn, n_tt, n_rb, P, nkp, mats, stage_bytes, nstg;
+};
+DensePlan dense_plan(int T, int N, int K, int epi);
+bool dense_applies(int N, int K);
+// part: kDensePartRows x N x mats floats when the plan splits K; ctr: n_rb * n_tt * 4 int32
+// counters at zero (left at zero).
+cudaError_t launch_dense(int epi, int T, int N, int K, const uint16_t *x, const uint16_t *w,
+                         const uint16_t *w3, void *y, float b1, float b2, float *part, int32_t *ctr,
+                         int32_t *status, cudaStream_t s, const char *name);
+
 // Full-width block (k3moe_full_forward).  Its router call reads the full-width token (a
 // config whose d is the hidden width H), its expert call runs the layer on the latent
 // with no shared experts (they run on the full width here).  The two calls run one after
 // the other and share the layer's regions; the block's own buffers follow them.
-constexpr size_t kLtWorkspace = 32u << 20;       // cuBLASLt scratch
 struct FullLayout {
     k3moe_config cr, cl;         // router config (d = H), latent config (n_shared = 0)
     WsLayout route, latent;
     size_t z;                    // [T][d] bf16: the token projected into the latent
     size_t acc;                  // [T][d] f32: the experts' weighted sum
     size_t y;                    // [T][d] bf16: the normed sum, the up projection's input
-    size_t gate, up;             // [T][S*f] f32: shared gate and up projections
-    size_t act;                  // [T][S*f] bf16: their SiTU
-    size_t lt;                   // cuBLASLt scratch
+    size_t act;                  // [T][S*f] bf16: the shared experts' SiTU
+    size_t part;                 // dense projections' K-part partial sums
+    size_t ctr;                  // their arrival counters (kept at zero between calls)
     size_t total;
 };
 
@@ -198,14 +213,19 @@ inline FullLayout full_layout(const k3moe_config &c, int hidden, int T)
     F.route = ws_layout(F.cr, T);
     F.latent = ws_layout(F.cl, T);
     const size_t td = (size_t)T * c.d, ts = (size_t)T * c.n_shared * c.f;
+    const size_t SI = (size_t)c.n_shared * c.f;
+    // widest partial row over the four projections: Wd (d), Wu and Sh2 (H), Sh1 + Sh3 (2 SI)
+    const size_t wmax = std::max(std::max((size_t)c.d, (size_t)hidden), 2 * SI);
+    // counters: row blocks x token tiles x 4 quadrants; K is split only while P * T <=
+    // kDensePartRows, so at most 512 tokens there: 4 token tiles of 128
+    const size_t nrb_max = std::max(std::max((size_t)c.d, (size_t)hidden), SI) / 128;
     size_t o = align256(F.route.total > F.latent.total ? F.route.total : F.latent.total);
     F.z = o; o = align256(o + td * 2);
     F.acc = o; o = align256(o + td * 4);
     F.y = o; o = align256(o + td * 2);
-    F.gate = o; o = align256(o + ts * 4);
-    F.up = o; o = align256(o + ts * 4);
     F.act = o; o = align256(o + ts * 2);
-    F.lt = o; o = align256(o + kLtWorkspace);
+    F.part = o; o = align256(o + (T > 0 ? (size_t)kDensePartRows * wmax * 4 : 0));
+    F.ctr = o; o = align256(o + nrb_max * 4 * 4 * 4);
     F.total = o;
     return F;
 }

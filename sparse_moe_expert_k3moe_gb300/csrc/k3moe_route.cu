@@ -28,6 +28,7 @@
 //   perm_scatter   perm[base + rank] = slot.
 // The map is a stable counting sort: offsets = exclusive prefix sum of the per-expert
 // counts, and inside an expert's segment the flat slot ids t*k+j ascend.
+#include "k3moe_exp.cuh"
 #include "k3moe_internal.cuh"
 
 namespace k3moe {
@@ -103,11 +104,11 @@ __device__ __forceinline__ float acc_finish(const Acc2 a0, const Acc2 a1)
 }
 
 // sc = 1/(1+expf(-logit)) and ch = sc + bias, each step rounded to float as the listing
-// writes them; the exponential is the double one rounded to float (the correctly rounded
-// float exponential, but in cases within 2^-29 ulp of a tie).
+// writes them, with the correctly rounded float exponential (exp_rn: wrong only within
+// ~2^-40 of a rounding tie).
 __device__ __forceinline__ void exact_scores(float logit, float bias, float &sc, float &ch)
 {
-    const float ef = __double2float_rn(exp(-(double)logit));
+    const float ef = exp_rn(-logit);
     sc = __fdiv_rn(1.0f, __fadd_rn(1.0f, ef));
     ch = __fadd_rn(sc, bias);
 }
@@ -144,13 +145,13 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
     pdl_wait();
     pdl_trigger();
     extern __shared__ __align__(16) uint8_t xs_raw[];        // kScoreTok x d bf16
-    __shared__ float lg[kScoreWarps][kScoreTok];               // a round's logits
     uint4 *xs = reinterpret_cast<uint4 *>(xs_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kScoreWarps + warp;
     const int nchunk = d / 8;                                  // 16-byte chunks per row
     const int tb0 = blockIdx.y * kScoreTokBlock, tb1 = min(T, tb0 + kScoreTokBlock);
     const uint4 *wrow = reinterpret_cast<const uint4 *>(wr + (size_t)min(e, E - 1) * d);
+    const float b = (bias && e < E) ? bias[e] : 0.0f;
     // the first 4096 columns of the row stay in registers across the token rounds (the
     // whole row for d <= 4096); their loads are in flight with the first x tile's
     uint4 w0[kScoreChunks];
@@ -177,9 +178,10 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
                 const int c = c0 + lane + 32 * j;
                 w[j] = c0 == 0 ? w0[j] : (c < nchunk ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0));
             }
+            // all kScoreTok token rows (rows past nt hold stale values, never stored): the
+            // 2 x kScoreTok accumulation chains are independent and interleave
 #pragma unroll
             for (int i = 0; i < kScoreTok; i++) {
-                if (i >= nt) break;
 #pragma unroll
                 for (int j = 0; j < kScoreChunks; j++) {
                     const int c = c0 + lane + 32 * j;   // this lane's chunk number (c0 / 32 + j) is even iff j is
@@ -187,23 +189,17 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
                 }
             }
         }
+        float logit = 0.0f;
 #pragma unroll
         for (int i = 0; i < kScoreTok; i++) {
-            if (i >= nt) break;
             const float v = acc_finish(acc[i][0], acc[i][1]);
-            if (lane == i) lg[warp][i] = v;
+            if (lane == i) logit = v;
         }
-        __syncthreads();
-        // the round's sigmoids by warp 0, lane = 8 * (expert of the block) + token: the
-        // double exponential runs on the slow fp64 pipe, once per round instead of per warp
-        if (warp == 0) {
-            const int we = lane / kScoreTok, i = lane % kScoreTok, ee = blockIdx.x * kScoreWarps + we;
-            if (i < nt && ee < E) {
-                float s, ch;
-                exact_scores(lg[we][i], bias ? bias[ee] : 0.0f, s, ch);
-                sc_out[(size_t)(t0 + i) * E + ee] = s;
-                ch_out[(size_t)(t0 + i) * E + ee] = ch;
-            }
+        if (e < E && lane < nt) {
+            float s, ch;
+            exact_scores(logit, b, s, ch);
+            sc_out[(size_t)(t0 + lane) * E + e] = s;
+            ch_out[(size_t)(t0 + lane) * E + e] = ch;
         }
     }
 }
@@ -492,23 +488,17 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
         if (i == 1023) n_cand = base + __popc(m);
         __syncthreads();
         const int C = n_cand;
-        // exact logits of the candidates, one warp per candidate; then their scores, one
-        // thread per candidate (the double exponential runs on the slow fp64 pipe, so it
-        // is issued once per 32 candidates instead of once per candidate)
+        // exact scores of the candidates, one warp per candidate
         const uint4 *wr = reinterpret_cast<const uint4 *>(a.wr);
-        float *lgx = reinterpret_cast<float *>(ckey) + kMaxExperts;   // upper half of ckey
         for (int c = warp; c < C; c += 32) {
-            const float logit = exact_logit_warp(xs, wr + (size_t)cnt[c] * nchunk, nchunk, lane);
-            if (lane == 0) lgx[c] = logit;
-        }
-        __syncthreads();
-        float sv = 0.0f, cv = 0.0f;
-        const int e_c = i < C ? cnt[i] : 0;
-        if (i < C) exact_scores(lgx[i], a.bias ? a.bias[e_c] : 0.0f, sv, cv);
-        __syncthreads();
-        if (i < C) {
-            scx[e_c] = sv;
-            ckey[i] = choice_key(cv, e_c);
+            const int e = cnt[c];
+            const float logit = exact_logit_warp(xs, wr + (size_t)e * nchunk, nchunk, lane);
+            if (lane == 0) {
+                float sv, cv;
+                exact_scores(logit, a.bias ? a.bias[e] : 0.0f, sv, cv);
+                scx[e] = sv;
+                ckey[c] = choice_key(cv, e);
+            }
         }
         __syncthreads();
         top = block_top16(i < C ? ckey[i] : 0, C, lists);

@@ -494,6 +494,10 @@ FULL_CASES = [
     ki.WORKLOADS["full_tiny"].with_(name="full_tiny_no_shared", T=5, S=0, seed=83),
     ki.Workload("full_mid", T=3, d=512, f=256, E=32, k=4, S=2, exp_lo=-9, exp_hi=-5, seed=84,
                 hidden=1024, zipf_bias=True),
+    # the dense projections over several token tiles with a ragged last one (256 + 44;
+    # the gated shared projection in tiles of 128), K not split
+    ki.Workload("full_tiles", T=300, d=256, f=256, E=16, k=4, S=2, exp_lo=-8, exp_hi=-4, seed=86,
+                hidden=512),
 ]
 
 
@@ -539,9 +543,9 @@ def test_full_block_parity(k3, w):
 
 
 def test_block_graph_replay(k3):
-    """The full-width block (its cuBLASLt projections included) captured as one CUDA
-    graph: a replay repeats the eager call, and a replay on new tokens copied into the
-    same input buffer matches the oracle's block."""
+    """The full-width block (its dense projections included) captured as one CUDA graph:
+    a replay repeats the eager call, and a replay on new tokens copied into the same
+    input buffer matches the oracle's block."""
     from k3moe_inputs.device import build_block
     w = ki.WORKLOADS["full_tiny"].with_(name="full_graph", T=3, seed=85)
     blk = build_block(w)
