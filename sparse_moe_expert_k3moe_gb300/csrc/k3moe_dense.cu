@@ -42,7 +42,7 @@ constexpr int kDnTmemCols = 512;
 
 struct DenseArgs {
     int T, N, K, epi;
-    int bn, P, n_rb, n_tt, nkp, nstg, stage_bytes;
+    int bn, P, n_rb, n_tt, nkp, kb, nstg, stage_bytes;
     float b1, b2;
     void *y;
     float *part;                   // [P][mats][T][N] partial sums (P > 1)
@@ -125,12 +125,18 @@ __global__ void __launch_bounds__(kDnThreads, 1) dense_tc_kernel(const DenseArgs
                         timeout();
                         break;
                     }
+                    // a stage is kb boxes of 64 columns: weight box (m, b) at (m kb + b) 16 KB,
+                    // token box b after the weights at b bn 128 bytes
                     uint8_t *stage = sm + (size_t)s * a.stage_bytes;
-                    mb_expect_tx(&full[s], (uint32_t)(mats * kDnABytes + bn * kDnBK * 2));
-                    tma2d(stage, &mw, ks * kDnBK, rb * kDnBM, &full[s]);
-                    if (gated) tma2d(stage + kDnABytes, &mw3, ks * kDnBK, rb * kDnBM, &full[s]);
-                    uint8_t *bs = stage + mats * kDnABytes;
-                    for (int j = 0; j < bn / 16; j++) tma2d(bs + j * 16 * 128, &mx, ks * kDnBK, t0 + 16 * j, &full[s]);
+                    mb_expect_tx(&full[s], (uint32_t)(a.kb * (mats * kDnABytes + bn * kDnBK * 2)));
+                    uint8_t *bs = stage + mats * a.kb * kDnABytes;
+                    for (int b = 0; b < a.kb; b++) {
+                        const int k0 = (ks * a.kb + b) * kDnBK;
+                        tma2d(stage + b * kDnABytes, &mw, k0, rb * kDnBM, &full[s]);
+                        if (gated) tma2d(stage + (a.kb + b) * kDnABytes, &mw3, k0, rb * kDnBM, &full[s]);
+                        for (int j = 0; j < bn / 16; j++)
+                            tma2d(bs + (size_t)b * bn * 128 + j * 16 * 128, &mx, k0, t0 + 16 * j, &full[s]);
+                    }
                 }
             }
             if (bail)   // wait (bounded) for the copies already issued
@@ -153,14 +159,16 @@ __global__ void __launch_bounds__(kDnThreads, 1) dense_tc_kernel(const DenseArgs
                     if (!mb_wait(&full[s], (st / nstg) & 1u)) { timeout(); break; }
                     tc_fence_after();
                     const uint8_t *stage = sm + (size_t)s * a.stage_bytes;
-                    const uint32_t A = saddr(stage), B = saddr(stage + mats * kDnABytes);
+                    const uint32_t A = saddr(stage), B0 = saddr(stage + mats * a.kb * kDnABytes);
                     const bool first = ks == p * a.nkp;
+                    for (int b = 0; b < a.kb; b++) {
+                        const uint32_t Ab = A + b * kDnABytes, Bb = B0 + b * bn * 128;
 #pragma unroll
-                    for (int kk = 0; kk < kDnBK / 16; kk++) {
-                        umma(d0, sdesc(A + kk * 32), sdesc(B + kk * 32), id, (!first || kk) ? 1u : 0u);
-                        if (gated)
-                            umma(d0 + 128u, sdesc(A + kDnABytes + kk * 32), sdesc(B + kk * 32), id,
-                                 (!first || kk) ? 1u : 0u);
+                        for (int kk = 0; kk < kDnBK / 16; kk++) {
+                            const uint32_t acc = (!first || b || kk) ? 1u : 0u;
+                            umma(d0, sdesc(Ab + kk * 32), sdesc(Bb + kk * 32), id, acc);
+                            if (gated) umma(d0 + 128u, sdesc(Ab + a.kb * kDnABytes + kk * 32), sdesc(Bb + kk * 32), id, acc);
+                        }
                     }
                     umma_commit(&empty[s]);
                 }
@@ -218,12 +226,24 @@ __global__ void __launch_bounds__(kDnThreads, 1) dense_tc_kernel(const DenseArgs
                     __threadfence();
                     for (int c = 0; c < ncols; c++) {
                         const int t = t0 + c;
-                        float sv = 0.0f, su = 0.0f;
-                        for (int pp = 0; pp < a.P; pp++) {
-                            const float *src = a.part + (((size_t)pp * mats) * a.T + t) * a.N + nr;
-                            sv += __ldcg(src);
-                            if (gated) su += __ldcg(src + (size_t)a.T * a.N);
+                        // every part's value is loaded before any is added (loads in flight together)
+                        float pv[kDenseMaxParts], pu[kDenseMaxParts];
+#pragma unroll
+                        for (int pp = 0; pp < kDenseMaxParts; pp++) {
+                            pv[pp] = pu[pp] = 0.0f;
+                            if (pp < a.P) {
+                                const float *src = a.part + (((size_t)pp * mats) * a.T + t) * a.N + nr;
+                                pv[pp] = __ldcg(src);
+                                if (gated) pu[pp] = __ldcg(src + (size_t)a.T * a.N);
+                            }
                         }
+                        float sv = 0.0f, su = 0.0f;
+#pragma unroll
+                        for (int pp = 0; pp < kDenseMaxParts; pp++)
+                            if (pp < a.P) {
+                                sv += pv[pp];
+                                su += pu[pp];
+                            }
                         dense_store(a, t, nr, sv, su);
                     }
                 }
@@ -249,16 +269,19 @@ DensePlan dense_plan(int T, int N, int K, int epi)
     pl.bn = T >= bn_max ? bn_max : std::max(16, (T + 15) & ~15);
     pl.n_tt = (T + pl.bn - 1) / pl.bn;
     pl.n_rb = N / kDnBM;
-    const int nks = K / kDnBK;
+    pl.mats = gated ? 2 : 1;
+    // stages of two 64-column boxes when one box would make a small stage (one weight
+    // matrix, few tokens): half the barrier round trips per byte
+    pl.kb = (!gated && pl.bn <= 64 && (K / kDnBK) % 2 == 0) ? 2 : 1;
+    const int nks = K / (kDnBK * pl.kb);
     pl.P = 1;
     // few items: cut K until they fill the GPU (kDenseTargetItems), at least 4 stages a
-    // part, and at most kDensePartRows partial rows (P * T)
+    // part, at most kDenseMaxParts parts and kDensePartRows partial rows (P * T)
     while ((long long)pl.n_rb * pl.n_tt * pl.P * 2 <= kDenseTargetItems && nks % (2 * pl.P) == 0 &&
-           nks / (2 * pl.P) >= 4 && (long long)2 * pl.P * T <= kDensePartRows)
+           nks / (2 * pl.P) >= 4 && 2 * pl.P <= kDenseMaxParts && (long long)2 * pl.P * T <= kDensePartRows)
         pl.P *= 2;
     pl.nkp = nks / pl.P;
-    pl.mats = gated ? 2 : 1;
-    pl.stage_bytes = pl.mats * kDnABytes + pl.bn * kDnBK * 2;
+    pl.stage_bytes = pl.kb * (pl.mats * kDnABytes + pl.bn * kDnBK * 2);
     pl.nstg = std::min(kDnMaxStg, kDnSmemBudget / pl.stage_bytes);
     return pl;
 }
@@ -283,7 +306,7 @@ cudaError_t launch_dense(int epi, int T, int N, int K, const uint16_t *x, const 
         cudaFuncSetAttribute(dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         smem_set = smem;
     }
-    DenseArgs a{T, N, K, epi, pl.bn, pl.P, pl.n_rb, pl.n_tt, pl.nkp, pl.nstg, pl.stage_bytes, b1, b2,
+    DenseArgs a{T, N, K, epi, pl.bn, pl.P, pl.n_rb, pl.n_tt, pl.nkp, pl.kb, pl.nstg, pl.stage_bytes, b1, b2,
                 y, part, ctr, status};
     const int n_items = pl.n_rb * pl.n_tt * pl.P;
     const int grid = std::max(1, std::min(num_sms(), n_items));

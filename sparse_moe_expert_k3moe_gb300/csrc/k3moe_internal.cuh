@@ -176,8 +176,9 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
 enum DenseEpi { kDenseBf16 = 0, kDenseF32 = 1, kDenseAddF32 = 2, kDenseSitu = 3 };
 constexpr int kDenseTargetItems = 456;   // work items that fill the GPU (3 per SM of 152)
 constexpr int kDensePartRows = 1024;     // at most this many partial rows (K parts x tokens)
+constexpr int kDenseMaxParts = 16;
 struct DensePlan {
-    int bn, n_tt, n_rb, P, nkp, mats, stage_bytes, nstg;
+    int bn, n_tt, n_rb, P, nkp, kb, mats, stage_bytes, nstg;
 };
 DensePlan dense_plan(int T, int N, int K, int epi);
 bool dense_applies(int N, int K);

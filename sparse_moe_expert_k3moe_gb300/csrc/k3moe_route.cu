@@ -168,31 +168,27 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
             xs[i * nchunk + c] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + i) * d) + c);
         }
         __syncthreads();
-        Acc2 acc[kScoreTok][2];
+        // one token at a time (a loop, not unrolled: the unrolled body of all tokens would
+        // not fit the instruction cache); its two chains over the lane's chunks, the row
+        // chunks held in registers across the tokens
+        float logit = 0.0f;
+#pragma unroll 1
+        for (int i = 0; i < nt; i++) {
+            Acc2 a0{0.0f, 0.0f}, a1{0.0f, 0.0f};
+            for (int c0 = 0; c0 < nchunk; c0 += 32 * kScoreChunks) {
+                uint4 w[kScoreChunks];
 #pragma unroll
-        for (int i = 0; i < kScoreTok; i++) acc[i][0] = acc[i][1] = Acc2{0.0f, 0.0f};
-        for (int c0 = 0; c0 < nchunk; c0 += 32 * kScoreChunks) {
-            uint4 w[kScoreChunks];
-#pragma unroll
-            for (int j = 0; j < kScoreChunks; j++) {
-                const int c = c0 + lane + 32 * j;
-                w[j] = c0 == 0 ? w0[j] : (c < nchunk ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0));
-            }
-            // all kScoreTok token rows (rows past nt hold stale values, never stored): the
-            // 2 x kScoreTok accumulation chains are independent and interleave
-#pragma unroll
-            for (int i = 0; i < kScoreTok; i++) {
+                for (int j = 0; j < kScoreChunks; j++) {
+                    const int c = c0 + lane + 32 * j;
+                    w[j] = c0 == 0 ? w0[j] : (c < nchunk ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0));
+                }
 #pragma unroll
                 for (int j = 0; j < kScoreChunks; j++) {
                     const int c = c0 + lane + 32 * j;   // this lane's chunk number (c0 / 32 + j) is even iff j is
-                    if (c < nchunk) acc_chunk(acc[i][j & 1], xs[i * nchunk + c], w[j]);
+                    if (c < nchunk) acc_chunk((j & 1) ? a1 : a0, xs[i * nchunk + c], w[j]);
                 }
             }
-        }
-        float logit = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kScoreTok; i++) {
-            const float v = acc_finish(acc[i][0], acc[i][1]);
+            const float v = acc_finish(a0, a1);
             if (lane == i) logit = v;
         }
         if (e < E && lane < nt) {
@@ -407,102 +403,23 @@ __device__ uint64_t block_top16(uint64_t key, int n, uint64_t (*lists)[32][kMaxT
 // Float sigmoid for the bounds of the re-scoring step (any accuracy within a few ulp).
 __device__ __forceinline__ float sigmoid_bound(float v) { return 1.0f / (1.0f + expf(-v)); }
 
-// blockDim = 1024; block t owns token t.  Key = (orderable(ch) << 32) | ~index, so a
-// descending order sorts by ch and, among equal ch, by ascending index -- the order the
-// repeated maximum with a strict comparison produces.  Every key is distinct, so the k
-// largest keys are the selection.
-//
-// With approximate logits la (|la - logit| <= L = 2^-12 |x_t| |Wr[e]|), the exact ch of
-// expert e lies in [lo_e, hi_e], lo/hi = sigmoid(la -/+ L) + bias -/+ slack (slack covers
-// the float rounding of both sides).  The k-th largest exact ch is at least the k-th
-// largest lo, so an expert whose hi stays below that can never be chosen, and an expert
-// below it cannot tie with the k-th either.  The others (the candidates) are re-scored
-// exactly and the selection is the top k of their exact keys.
+// blockDim = 1024; block t owns token t; the scores are the exact ones of the per-token
+// kernel.  Key = (orderable(ch) << 32) | ~index, so a descending order sorts by ch and,
+// among equal ch, by ascending index -- the order the repeated maximum with a strict
+// comparison produces.  Every key is distinct, so the k largest keys are the selection.
 __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
 {
     pdl_trigger();      // the next kernel may launch now: it waits for this one
     pdl_wait();
-    extern __shared__ __align__(16) uint8_t tk_dyn[];   // re-scoring: the token row, d bf16
     __shared__ uint64_t lists[2][32][kMaxTopK];
-    __shared__ int32_t cnt[kMaxExperts];                 // map counts; re-scoring: the candidates
+    __shared__ int32_t cnt[kMaxExperts];
     __shared__ int32_t slot_e[kChunkTokens * kMaxTopK];
     __shared__ int32_t scan_tmp[32];
-    __shared__ float scx[kMaxExperts];                   // re-scoring: exact sc by expert
-    __shared__ uint64_t ckey[kMaxExperts];               // re-scoring: exact keys of the candidates
-    __shared__ float red[32];
-    __shared__ uint32_t thr_o;
-    __shared__ int n_cand, last;
-    const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
+    __shared__ int last;
+    const int i = threadIdx.x;
     const int t = blockIdx.x, E = a.E, k = a.k;
-    uint64_t top;                                        // lane r < k of warp 0: the rank-r key
-    if (a.logit == nullptr) {
-        const uint64_t key = i < E ? choice_key(a.ch[(size_t)t * E + i], i) : 0;
-        top = block_top16(key, E, lists);
-    } else {
-        // the token row into shared memory, and |x_t|
-        const int nchunk = a.d / 8;
-        uint4 *xs = reinterpret_cast<uint4 *>(tk_dyn);
-        const uint4 *xg = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.d);
-        float ss = 0.0f;
-        for (int q = i; q < nchunk; q += blockDim.x) {
-            const uint4 v = __ldg(xg + q);
-            xs[q] = v;
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int r = 0; r < 4; r++) {
-                const float lo = __uint_as_float(u[r] << 16), hi = __uint_as_float(u[r] & 0xFFFF0000u);
-                ss = fmaf(lo, lo, ss);
-                ss = fmaf(hi, hi, ss);
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) red[warp] = ss;
-        __syncthreads();
-        float xn2 = 0.0f;
-        for (int w = 0; w < 32; w++) xn2 += red[w];
-        const float xn = sqrtf(xn2) * 1.001f;
-        // bounds, and the k-th largest lower bound
-        float hi = 0.0f;
-        uint64_t key = 0;
-        if (i < E) {
-            const float la = a.logit[(size_t)t * E + i];
-            const float L = kTcLogitRel * xn * a.wnorm[i];
-            const float b = a.bias ? a.bias[i] : 0.0f;
-            const float slack = 1e-6f + fabsf(b) * 0x1p-20f;
-            const float lo = sigmoid_bound(la - L) + b - slack;
-            hi = sigmoid_bound(la + L) + b + slack;
-            key = choice_key(lo, i);
-        }
-        const uint64_t lk = block_top16(key, E, lists);
-        if (warp == 0 && lane == k - 1) thr_o = (uint32_t)(lk >> 32);
-        __syncthreads();
-        // candidates: upper bound at or above the threshold (no NaN passes)
-        const bool is_c = i < E && hi == hi && orderable(hi) >= thr_o;
-        const uint32_t m = __ballot_sync(0xffffffffu, is_c);
-        if (lane == 0) scan_tmp[warp] = __popc(m);
-        __syncthreads();
-        int base = 0;
-        for (int w = 0; w < warp; w++) base += scan_tmp[w];
-        if (is_c) cnt[base + __popc(m & ((1u << lane) - 1u))] = i;
-        if (i == 1023) n_cand = base + __popc(m);
-        __syncthreads();
-        const int C = n_cand;
-        // exact scores of the candidates, one warp per candidate
-        const uint4 *wr = reinterpret_cast<const uint4 *>(a.wr);
-        for (int c = warp; c < C; c += 32) {
-            const int e = cnt[c];
-            const float logit = exact_logit_warp(xs, wr + (size_t)e * nchunk, nchunk, lane);
-            if (lane == 0) {
-                float sv, cv;
-                exact_scores(logit, a.bias ? a.bias[e] : 0.0f, sv, cv);
-                scx[e] = sv;
-                ckey[c] = choice_key(cv, e);
-            }
-        }
-        __syncthreads();
-        top = block_top16(i < C ? ckey[i] : 0, C, lists);
-    }
+    const uint64_t key = i < E ? choice_key(a.ch[(size_t)t * E + i], i) : 0;
+    const uint64_t top = block_top16(key, E, lists);
     // lane r < k of warp 0 now holds the rank-r key
     if (i < 32) {
         int e = -1;
@@ -513,7 +430,7 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
                 set_status(a.map.status, K3MOE_DEV_BAD_INDEX);
                 e = 0;
             }
-            w = a.logit == nullptr ? a.sc[(size_t)t * E + e] : scx[e];
+            w = a.sc[(size_t)t * E + e];
         }
         float s = 0.0f;
         for (int j = 0; j < k; j++) s += __shfl_sync(0xffffffffu, w, j);
@@ -555,6 +472,145 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(TopkArgs a)
     __threadfence();
     map_chunk(a.map, 0, true, cnt, slot_e, scan_tmp);
     if (i == 0) *a.done = 0;
+}
+
+// ---------------------------------------------------------------- top-k from tensor-core logits
+constexpr int kSelThreads = 128;    // one token per block of 4 warps
+
+// Warp w merges a list of keys (lanes 0-15 of `run`, descending) with the 32 keys of a
+// chunk (one per lane): the chunk is sorted, its 16 largest reversed into lanes 16-31,
+// and the bitonic merge leaves the 16 largest of both in lanes 0-15.
+__device__ __forceinline__ uint64_t merge_chunk(uint64_t run, uint64_t key, int lane)
+{
+    key = warp_sort_desc(key, lane);
+    const uint64_t rev = __shfl_sync(0xffffffffu, key, 31 - lane);   // lane 16+j gets rank 15-j
+    const uint64_t v = lane < 16 ? run : rev;
+    return warp_merge_desc(v, lane);
+}
+
+// The 16 largest of n keys in `keys` (shared memory; n <= 1024), by the 4 warps of the
+// block: each warp merges its chunks of 32 into a list, then warp 0 merges the 4 lists.
+// Returns the rank-r key in lane r < 16 of warp 0.  Called by the whole block.
+__device__ uint64_t sel_top16(const uint64_t *keys, int n, uint64_t (*lists)[kMaxTopK])
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint64_t run = 0;
+    for (int c0 = 32 * warp; c0 < n; c0 += 32 * (kSelThreads / 32)) {
+        const int i = c0 + lane;
+        run = merge_chunk(run, i < n ? keys[i] : 0, lane);
+    }
+    if (lane < kMaxTopK) lists[warp][lane] = run;
+    __syncthreads();
+    uint64_t top = 0;
+    if (warp == 0) {
+        top = lane < kMaxTopK ? lists[0][lane] : 0;
+        for (int w = 1; w < kSelThreads / 32; w++) {
+            const uint64_t other = lane < kMaxTopK ? lists[w][lane] : 0;    // descending in 0-15
+            const uint64_t rev = __shfl_sync(0xffffffffu, other, 31 - lane);
+            top = warp_merge_desc(lane < 16 ? top : rev, lane);
+        }
+    }
+    __syncthreads();
+    return top;
+}
+
+// blockDim = 128; block t owns token t.  The tensor-core logits la bound every expert's
+// exact choice score (|la - logit| <= L = 2^-12 |x_t| |Wr[e]|): lo/hi = sigmoid(la -/+ L)
+// + bias -/+ slack.  The k-th largest exact ch is at least the k-th largest lo, so only the
+// experts whose hi reaches it can be chosen (and none below it can tie with the k-th);
+// those are re-scored exactly and the selection is the top k of their exact keys.
+__global__ void __launch_bounds__(kSelThreads) router_select_kernel(TopkArgs a)
+{
+    pdl_trigger();      // the next kernel may launch now: it waits for this one
+    pdl_wait();
+    extern __shared__ __align__(16) uint8_t sel_dyn[];   // the token row (d bf16)
+    __shared__ uint64_t keys[kMaxExperts];
+    __shared__ uint32_t hio[kMaxExperts];
+    __shared__ int32_t cand[kMaxExperts];
+    __shared__ float scx[kMaxExperts];
+    __shared__ uint64_t lists[kSelThreads / 32][kMaxTopK];
+    __shared__ float red[kSelThreads / 32];
+    __shared__ uint32_t thr_o;
+    __shared__ int n_cand;
+    const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
+    const int t = blockIdx.x, E = a.E, k = a.k;
+    const int nchunk = a.d / 8;
+    uint4 *xs = reinterpret_cast<uint4 *>(sel_dyn);
+    const uint4 *xg = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.d);
+    float ss = 0.0f;
+    for (int q = i; q < nchunk; q += kSelThreads) {
+        const uint4 v = __ldg(xg + q);
+        xs[q] = v;
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const float lo = __uint_as_float(u[r] << 16), hi = __uint_as_float(u[r] & 0xFFFF0000u);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    if (i == 0) n_cand = 0;
+    __syncthreads();
+    float xn2 = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kSelThreads / 32; w++) xn2 += red[w];
+    const float xn = sqrtf(xn2) * 1.001f;
+    for (int e = i; e < E; e += kSelThreads) {
+        const float la = a.logit[(size_t)t * E + e];
+        const float L = kTcLogitRel * xn * a.wnorm[e];
+        const float b = a.bias ? a.bias[e] : 0.0f;
+        const float slack = 1e-6f + fabsf(b) * 0x1p-20f;
+        const float lo = sigmoid_bound(la - L) + b - slack;
+        const float hi = sigmoid_bound(la + L) + b + slack;
+        keys[e] = choice_key(lo, e);
+        hio[e] = hi == hi ? orderable(hi) : 0u;          // NaN never passes
+    }
+    __syncthreads();
+    const uint64_t lk = sel_top16(keys, E, lists);
+    if (warp == 0 && lane == k - 1) thr_o = (uint32_t)(lk >> 32);
+    __syncthreads();
+    // candidates (their order does not matter: the selection sorts their keys)
+    for (int e = i; e < E; e += kSelThreads)
+        if (hio[e] >= thr_o) cand[atomicAdd(&n_cand, 1)] = e;
+    __syncthreads();
+    const int C = min(n_cand, E);
+    // exact scores of the candidates, one warp per candidate
+    const uint4 *wr = reinterpret_cast<const uint4 *>(a.wr);
+    for (int c = warp; c < C; c += kSelThreads / 32) {
+        const int e = cand[c];
+        const float logit = exact_logit_warp(xs, wr + (size_t)e * nchunk, nchunk, lane);
+        if (lane == 0) {
+            float sv, cv;
+            exact_scores(logit, a.bias ? a.bias[e] : 0.0f, sv, cv);
+            scx[e] = sv;
+            keys[c] = choice_key(cv, e);
+        }
+    }
+    __syncthreads();
+    const uint64_t top = sel_top16(keys, C, lists);
+    if (warp == 0) {
+        int e = -1;
+        float w = 0.0f;
+        if (lane < k) {
+            e = (int)(0xFFFFFFFFu - (uint32_t)top);
+            if (e < 0 || e >= E) {                 // no valid key (non-finite scores); stay in bounds
+                set_status(a.map.status, K3MOE_DEV_BAD_INDEX);
+                e = 0;
+            }
+            w = scx[e];
+        }
+        float s = 0.0f;
+        for (int j = 0; j < k; j++) s += __shfl_sync(0xffffffffu, w, j);
+        if (lane < k) {
+            if (a.renorm && s > 0.0f) w = w / s;
+            w = w * a.routed_scale;
+            a.idx[(size_t)t * k + lane] = e;
+            a.weight[(size_t)t * k + lane] = w;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(1024) perm_count_kernel(MapArgs a)
@@ -688,13 +744,33 @@ cudaError_t launch_route(const k3moe_config &c, int T, const uint16_t *x, const 
     MapArgs m{T, E, k, idx, offsets, perm, reinterpret_cast<int32_t *>(ws + L.chunk_counts),
               reinterpret_cast<int32_t *>(ws + L.local_rank), status};
     // status block word 4 is the last-block counter of router_topk
+    // the per-token kernel's exact scores: the 1024-thread top-k, which for at most 64
+    // tokens also builds the map; the tensor-core logits: the 128-thread select kernel
+    // (re-scoring its candidates), the map by the perm kernels
     TopkArgs a{T, E, k, c.renorm, c.routed_scale, sc, ch, tc ? sc : nullptr, bias, wnorm, x, wr, c.d,
-               idx, weight, L.n_chunks == 1 ? status + 4 : nullptr, m};
+               idx, weight, (!tc && L.n_chunks == 1) ? status + 4 : nullptr, m};
     timing_begin("router_topk", s);
-    err = launch_pdl(router_topk_kernel, dim3(T), dim3(1024), tc ? (size_t)c.d * 2 : 0, s, a);
+    if (tc) {
+        static size_t sel_smem = 0;
+        const size_t smem = (size_t)c.d * 2;
+        if (smem > sel_smem) {
+            cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            sel_smem = smem;
+        }
+        err = launch_pdl(router_select_kernel, dim3(T), dim3(kSelThreads), smem, s, a);
+    } else {
+        err = launch_pdl(router_topk_kernel, dim3(T), dim3(1024), 0, s, a);
+    }
     count_launch();
     timing_end("router_topk", s);
     if (err != cudaSuccess) return err;
+    if (tc && L.n_chunks == 1) {          // one chunk: perm_count builds the whole map
+        timing_begin("perm_count", s);
+        err = launch_pdl(perm_count_kernel, dim3(1), dim3(1024), 0, s, m);
+        count_launch();
+        timing_end("perm_count", s);
+        if (err != cudaSuccess) return err;
+    }
     if (L.n_chunks > 1) {
         int32_t *base = reinterpret_cast<int32_t *>(ws + L.chunk_base);
         timing_begin("perm_count", s);
