@@ -118,7 +118,6 @@ __global__ void __launch_bounds__(kDnThreads, 1) dense_tc_kernel(const DenseArgs
             uint32_t st = 0;
             for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
                 const int p = part_of(i), rb = rb_of(i), t0 = tt_of(i) * a.bn;
-                const int bn = (min(a.bn, a.T - t0) + 15) & ~15;
                 for (int ks = p * a.nkp; ks < (p + 1) * a.nkp; ks++, st++) {
                     const int s = st % nstg;
                     if (st >= (uint32_t)nstg && !mb_wait(&empty[s], ((st / nstg) - 1) & 1u)) {
@@ -127,15 +126,15 @@ __global__ void __launch_bounds__(kDnThreads, 1) dense_tc_kernel(const DenseArgs
                     }
                     // a stage is kb boxes of 64 columns: weight box (m, b) at (m kb + b) 16 KB,
                     // token box b after the weights at b bn 128 bytes
+                    // one copy per box: the token box is a.bn rows (rows past T read as zero)
                     uint8_t *stage = sm + (size_t)s * a.stage_bytes;
-                    mb_expect_tx(&full[s], (uint32_t)(a.kb * (mats * kDnABytes + bn * kDnBK * 2)));
+                    mb_expect_tx(&full[s], (uint32_t)(a.kb * (mats * kDnABytes + a.bn * kDnBK * 2)));
                     uint8_t *bs = stage + mats * a.kb * kDnABytes;
                     for (int b = 0; b < a.kb; b++) {
                         const int k0 = (ks * a.kb + b) * kDnBK;
                         tma2d(stage + b * kDnABytes, &mw, k0, rb * kDnBM, &full[s]);
                         if (gated) tma2d(stage + (a.kb + b) * kDnABytes, &mw3, k0, rb * kDnBM, &full[s]);
-                        for (int j = 0; j < bn / 16; j++)
-                            tma2d(bs + (size_t)b * bn * 128 + j * 16 * 128, &mx, k0, t0 + 16 * j, &full[s]);
+                        tma2d(bs + (size_t)b * a.bn * 128, &mx, k0, t0, &full[s]);
                     }
                 }
             }
@@ -162,7 +161,7 @@ __global__ void __launch_bounds__(kDnThreads, 1) dense_tc_kernel(const DenseArgs
                     const uint32_t A = saddr(stage), B0 = saddr(stage + mats * a.kb * kDnABytes);
                     const bool first = ks == p * a.nkp;
                     for (int b = 0; b < a.kb; b++) {
-                        const uint32_t Ab = A + b * kDnABytes, Bb = B0 + b * bn * 128;
+                        const uint32_t Ab = A + b * kDnABytes, Bb = B0 + b * a.bn * 128;
 #pragma unroll
                         for (int kk = 0; kk < kDnBK / 16; kk++) {
                             const uint32_t acc = (!first || b || kk) ? 1u : 0u;
@@ -298,7 +297,7 @@ cudaError_t launch_dense(int epi, int T, int N, int K, const uint16_t *x, const 
     CUtensorMap mw{}, mw3{}, mx{};
     if (!map16(&mw, w, (uint64_t)N, (uint64_t)K, kDnBM) ||
         !map16(&mw3, epi == kDenseSitu ? w3 : w, (uint64_t)N, (uint64_t)K, kDnBM) ||
-        !map16(&mx, x, (uint64_t)T, (uint64_t)K, 16))
+        !map16(&mx, x, (uint64_t)T, (uint64_t)K, (uint32_t)pl.bn))
         return cudaErrorInvalidValue;
     const size_t smem = 1024 + (size_t)pl.nstg * pl.stage_bytes;
     static size_t smem_set = 0;

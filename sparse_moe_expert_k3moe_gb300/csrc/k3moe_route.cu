@@ -36,7 +36,7 @@ namespace {
 
 constexpr int kScoreWarps = 4;       // experts per block (one per warp)
 constexpr int kScoreTok = 8;         // tokens staged per round
-constexpr int kScoreTokBlock = 32;   // tokens per block (grid.y walks the rest)
+constexpr int kScoreTokBlock = 8;    // tokens per block (grid.y walks the rest)
 constexpr int kScoreChunks = 16;     // 16-byte Wr chunks per lane held at once (4096 columns)
 
 // Bound on the tensor-core logits' error, relative to |x_t| |Wr[e]|.  Their fp32
@@ -49,12 +49,12 @@ constexpr float kTcLogitRel = 0x1p-12f;
 // A logit is a sum of d products of two bf16 values, each exact in fp32.  It is carried
 // as an unevaluated pair (s, c): s the fp32 running sum, c the running sum of the exact
 // rounding errors of s's additions (Knuth's two-sum), and rounded once, to s + c.  A lane
-// keeps two such pairs (its 16-byte chunks alternate between them); the pairs, then the
-// lanes, are merged by the same rule.  The result is the float nearest the exact sum
+// keeps four such pairs (its 16-byte chunks take them in turn, for four independent
+// dependency chains); the pairs, then the lanes, are merged by the same rule.  The result is the float nearest the exact sum
 // unless that sum lies within about 2^-40 (relative) of a rounding boundary -- what the
 // listing's double accumulation rounded to float gives.  Every kernel that computes a
 // logit exactly goes through these functions with the same chunk-to-lane assignment
-// (chunk lane + 32 m, pair m & 1, m ascending), so their results are bitwise equal.
+// (chunk lane + 32 m, pair m & 3, m ascending), so their results are bitwise equal.
 struct Acc2 {
     float s, c;
 };
@@ -89,10 +89,10 @@ __device__ __forceinline__ void acc_chunk(Acc2 &a, const uint4 xv, const uint4 w
     }
 }
 
-// Both pairs of every lane -> the rounded logit, on every lane.
-__device__ __forceinline__ float acc_finish(const Acc2 a0, const Acc2 a1)
+// The four pairs of every lane -> the rounded logit, on every lane.
+__device__ __forceinline__ float acc_finish(const Acc2 a0, const Acc2 a1, const Acc2 a2, const Acc2 a3)
 {
-    Acc2 a = acc_merge(a0, a1);
+    Acc2 a = acc_merge(acc_merge(a0, a1), acc_merge(a2, a3));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         Acc2 b;
@@ -118,8 +118,8 @@ __device__ __forceinline__ void exact_scores(float logit, float bias, float &sc,
 __device__ __forceinline__ float exact_logit_warp(const uint4 *xs, const uint4 *__restrict__ wrow, int nchunk,
                                                   int lane)
 {
-    Acc2 a0{0.0f, 0.0f}, a1{0.0f, 0.0f};
-    // eight router chunks in flight per lane, then added in order (pair m & 1)
+    Acc2 a[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
+    // eight router chunks in flight per lane, then added in order (pair m & 3)
     for (int m0 = 0; lane + 32 * m0 < nchunk; m0 += 8) {
         uint4 w[8];
 #pragma unroll
@@ -130,14 +130,14 @@ __device__ __forceinline__ float exact_logit_warp(const uint4 *xs, const uint4 *
 #pragma unroll
         for (int j = 0; j < 8; j++) {
             const int c = lane + 32 * (m0 + j);
-            if (c < nchunk) acc_chunk((j & 1) ? a1 : a0, xs[c], w[j]);
+            if (c < nchunk) acc_chunk(a[j & 3], xs[c], w[j]);
         }
     }
-    return acc_finish(a0, a1);
+    return acc_finish(a[0], a[1], a[2], a[3]);
 }
 
 // -------------------------------------------------------------------------------- exact scores
-// grid (ceil(E / 4), ceil(T / 32)); block y owns tokens [32 y, 32 y + 32).
+// grid (ceil(E / 4), ceil(T / 8)); block y owns tokens [8 y, 8 y + 8).
 __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
     int T, int d, int E, const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
     const float *__restrict__ bias, float *__restrict__ sc_out, float *__restrict__ ch_out)
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
         float logit = 0.0f;
 #pragma unroll 1
         for (int i = 0; i < nt; i++) {
-            Acc2 a0{0.0f, 0.0f}, a1{0.0f, 0.0f};
+            Acc2 a[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
             for (int c0 = 0; c0 < nchunk; c0 += 32 * kScoreChunks) {
                 uint4 w[kScoreChunks];
 #pragma unroll
@@ -184,11 +184,11 @@ __global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
                 }
 #pragma unroll
                 for (int j = 0; j < kScoreChunks; j++) {
-                    const int c = c0 + lane + 32 * j;   // this lane's chunk number (c0 / 32 + j) is even iff j is
-                    if (c < nchunk) acc_chunk((j & 1) ? a1 : a0, xs[i * nchunk + c], w[j]);
+                    const int c = c0 + lane + 32 * j;   // this lane's chunk number c0 / 32 + j = j mod 4
+                    if (c < nchunk) acc_chunk(a[j & 3], xs[i * nchunk + c], w[j]);
                 }
             }
-            const float v = acc_finish(a0, a1);
+            const float v = acc_finish(a[0], a[1], a[2], a[3]);
             if (lane == i) logit = v;
         }
         if (e < E && lane < nt) {

@@ -31,6 +31,7 @@ constexpr int kRtTmemCols = 512;
 
 struct RtArgs {
     int T, d, E;
+    int bnx;                // rows of the token box: min(256, T rounded up to 16)
     float *logit;
     int32_t *status;
 };
@@ -79,17 +80,16 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_logits_tc_kernel(const R
             uint32_t st = 0;
             for (int i = blockIdx.x; i < n_items && !bail; i += gridDim.x) {
                 const int eb = i % n_eb, t0 = (i / n_eb) * kRtBN;
-                const int bn = (min(kRtBN, a.T - t0) + 15) & ~15;
                 for (int ks = 0; ks < nks; ks++, st++) {
                     const int s = st % kRtStg;
                     if (st >= (uint32_t)kRtStg && !mb_wait(&empty[s], ((st / kRtStg) - 1) & 1u)) {
                         timeout();
                         break;
                     }
-                    mb_expect_tx(&full[s], (uint32_t)(kRtABytes + bn * kRtBK * 2));
+                    // one copy of the token box (a.bnx rows; rows past T read as zero)
+                    mb_expect_tx(&full[s], (uint32_t)(kRtABytes + a.bnx * kRtBK * 2));
                     tma2d(smA + s * kRtABytes, &mwr, ks * kRtBK, eb * kRtBM, &full[s]);
-                    for (int j = 0; j < bn / 16; j++)
-                        tma2d(smB + s * kRtBBytes + j * 16 * 128, &mx, ks * kRtBK, t0 + 16 * j, &full[s]);
+                    tma2d(smB + s * kRtBBytes, &mx, ks * kRtBK, t0, &full[s]);
                 }
             }
             if (bail)   // wait (bounded) for the copies already issued
@@ -200,11 +200,11 @@ cudaError_t launch_router_logits_tc(const k3moe_config &c, int T, const uint16_t
     }
     CUtensorMap mwr{}, mx{};
     if (!map16(&mwr, wr, (uint64_t)c.n_experts, (uint64_t)c.d, kRtBM) ||
-        !map16(&mx, x, (uint64_t)T, (uint64_t)c.d, 16))
+        !map16(&mx, x, (uint64_t)T, (uint64_t)c.d, (uint32_t)std::min(kRtBN, (T + 15) & ~15)))
         return cudaErrorInvalidValue;
     const int n_items = ((c.n_experts + kRtBM - 1) / kRtBM) * ((T + kRtBN - 1) / kRtBN);
     const int grid = std::max(1, std::min(num_sms(), n_items));
-    RtArgs a{T, c.d, c.n_experts, logit, status};
+    RtArgs a{T, c.d, c.n_experts, std::min(kRtBN, (T + 15) & ~15), logit, status};
     const cudaError_t err = launch_pdl(router_logits_tc_kernel, dim3(grid), dim3(kRtThreads), kRtSmem, s, a, mwr, mx);
     count_launch();
     return err;
