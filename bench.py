@@ -183,6 +183,20 @@ def kernel_work(name: str, w, distinct_experts: int):
     return layer_bytes_flops(w, distinct_experts)[0], 0
 
 
+def workload_specs(arg: str):
+    """The comma-separated workload list; a `key=value` item without a name continues the
+    overrides of the workload before it (decode_t1:E=64,T=4 is one workload)."""
+    specs = []
+    for part in (p.strip() for p in arg.split(",")):
+        if not part:
+            continue
+        if "=" in part and ":" not in part and specs:
+            specs[-1] += "," + part
+        else:
+            specs.append(part)
+    return specs
+
+
 def workload_from(spec: str):
     """NAME or NAME:key=value,key=value (integer overrides, e.g. decode_t1:E=64)."""
     import k3moe_inputs as ki
@@ -343,7 +357,7 @@ def reference_arm(args):
         return
     import oracle
     oracle.build()
-    specs = [sp for sp in args.workload.split(",") if sp]
+    specs = workload_specs(args.workload)
     per_step = max(2.0, args.cpu_budget_s / max(1, args.steps))
     records = []
     for spec in specs:
@@ -585,7 +599,7 @@ def gpu_arm(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    specs = [sp for sp in args.workload.split(",") if sp]
+    specs = workload_specs(args.workload)
     records = [measure(workload_from(sp), args, rank, world, local, dev) for sp in specs]
     if rank == 0:
         line = {"metric": METRIC, "n_gpus": world, "higher_is_better": True, "scaling": "weak",

@@ -195,6 +195,17 @@ __global__ void __launch_bounds__(kDnThreads, 1) dense_tc_kernel(const DenseArgs
                 float v[16], u[16];
                 tmem_ld16(lane_addr + c0, v);
                 if (gated) tmem_ld16(lane_addr + 128u + c0, u);
+                if (a.P == 1 && a.epi == kDenseAddF32) {
+                    // every old value is loaded before any is stored (loads in flight together)
+                    float *yb = reinterpret_cast<float *>(a.y) + (size_t)(t0 + c0) * a.N + nr;
+                    float old[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj++) old[jj] = c0 + jj < ncols ? yb[(size_t)jj * a.N] : 0.0f;
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj++)
+                        if (c0 + jj < ncols) yb[(size_t)jj * a.N] = old[jj] + v[jj];
+                    continue;
+                }
 #pragma unroll
                 for (int jj = 0; jj < 16; jj++) {
                     const int t = t0 + c0 + jj;
@@ -258,6 +269,81 @@ __global__ void __launch_bounds__(kDnThreads, 1) dense_tc_kernel(const DenseArgs
     }
 }
 
+// ---------------------------------------------------------------- few tokens: row streaming
+// With at most kDenseRowsMaxT tokens the projection is a mat-vec bound by the weight
+// stream.  One warp per output row at a time: the row (and for the gated form the same
+// row of W3) read with 16-byte loads, eight in flight per lane -- whole contiguous rows,
+// which the DRAM serves better than the tensor-core kernel's 128-row boxes -- against the
+// tokens held in shared memory; fp32 products summed per lane in chunk order, then over
+// the warp by a fixed butterfly, so results repeat bit for bit.
+constexpr int kRowsThreads = 256;
+
+template <int NT>
+__global__ void __launch_bounds__(kRowsThreads) dense_rows_kernel(const DenseArgs a, const uint16_t *__restrict__ x,
+                                                                 const uint16_t *__restrict__ w,
+                                                                 const uint16_t *__restrict__ w3)
+{
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ __align__(16) uint4 xsm[];         // NT x K bf16
+    const int nchunk = a.K / 8;
+    const bool gated = a.epi == kDenseSitu;
+    for (int q = threadIdx.x; q < NT * nchunk; q += kRowsThreads) {
+        const int t = q / nchunk, c = q % nchunk;
+        xsm[q] = t < a.T ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * a.K) + c) : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nw = gridDim.x * (kRowsThreads / 32);
+    for (int n = blockIdx.x * (kRowsThreads / 32) + warp; n < a.N; n += nw) {
+        const uint4 *wr = reinterpret_cast<const uint4 *>(w + (size_t)n * a.K);
+        const uint4 *wr3 = reinterpret_cast<const uint4 *>((gated ? w3 : w) + (size_t)n * a.K);
+        float acc[NT], accu[NT];
+#pragma unroll
+        for (int t = 0; t < NT; t++) acc[t] = accu[t] = 0.0f;
+        for (int c0 = lane; c0 < nchunk; c0 += 32 * 8) {
+            uint4 wv[8], uv[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const int c = c0 + 32 * j;
+                wv[j] = c < nchunk ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
+                uv[j] = gated && c < nchunk ? __ldg(wr3 + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const int c = c0 + 32 * j;
+                if (c >= nchunk) break;
+                const uint32_t wu[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+                const uint32_t uu[4] = {uv[j].x, uv[j].y, uv[j].z, uv[j].w};
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                    const uint4 xv = xsm[t * nchunk + c];
+                    const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                    for (int r = 0; r < 4; r++) {
+                        const float x0 = __uint_as_float(xu[r] << 16), x1 = __uint_as_float(xu[r] & 0xFFFF0000u);
+                        acc[t] = fmaf(x0, __uint_as_float(wu[r] << 16), acc[t]);
+                        acc[t] = fmaf(x1, __uint_as_float(wu[r] & 0xFFFF0000u), acc[t]);
+                        if (gated) {
+                            accu[t] = fmaf(x0, __uint_as_float(uu[r] << 16), accu[t]);
+                            accu[t] = fmaf(x1, __uint_as_float(uu[r] & 0xFFFF0000u), accu[t]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < NT; t++) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+                accu[t] += __shfl_xor_sync(0xffffffffu, accu[t], o);
+            }
+            if (lane == 0 && t < a.T) dense_store(a, t, n, acc[t], accu[t]);
+        }
+    }
+}
+
 }  // namespace
 
 DensePlan dense_plan(int T, int N, int K, int epi)
@@ -293,6 +379,28 @@ cudaError_t launch_dense(int epi, int T, int N, int K, const uint16_t *x, const 
 {
     if (T <= 0) return cudaSuccess;
     if (!dense_applies(N, K)) return cudaErrorInvalidValue;
+    if (T <= kDenseRowsMaxT) {
+        DenseArgs a{T, N, K, epi, 0, 1, 0, 0, 0, 1, 0, 0, b1, b2, y, part, ctr, status};
+        const int nt = T <= 1 ? 1 : (T <= 2 ? 2 : 4);
+        const size_t smem = (size_t)nt * K * 2;
+        static size_t smem_set[3] = {0, 0, 0};
+        auto kern = nt == 1 ? dense_rows_kernel<1> : (nt == 2 ? dense_rows_kernel<2> : dense_rows_kernel<4>);
+        const int ki = nt == 1 ? 0 : (nt == 2 ? 1 : 2);
+        if (smem > smem_set[ki]) {
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            smem_set[ki] = smem;
+        }
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRowsThreads, smem) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        const int grid = std::max(1, std::min(num_sms() * per_sm, (N + kRowsThreads / 32 - 1) / (kRowsThreads / 32)));
+        timing_begin(name, s);
+        const cudaError_t err = launch_pdl(kern, dim3(grid), dim3(kRowsThreads), smem, s, a, x, w, w3);
+        count_launch();
+        timing_end(name, s);
+        return err;
+    }
     const DensePlan pl = dense_plan(T, N, K, epi);
     CUtensorMap mw{}, mw3{}, mx{};
     if (!map16(&mw, w, (uint64_t)N, (uint64_t)K, kDnBM) ||

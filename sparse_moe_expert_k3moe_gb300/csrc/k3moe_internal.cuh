@@ -177,6 +177,7 @@ enum DenseEpi { kDenseBf16 = 0, kDenseF32 = 1, kDenseAddF32 = 2, kDenseSitu = 3 
 constexpr int kDenseTargetItems = 456;   // work items that fill the GPU (3 per SM of 152)
 constexpr int kDensePartRows = 1024;     // at most this many partial rows (K parts x tokens)
 constexpr int kDenseMaxParts = 16;
+constexpr int kDenseRowsMaxT = 4;        // up to this many tokens: the row-streaming kernel
 struct DensePlan {
     int bn, n_tt, n_rb, P, nkp, kb, mats, stage_bytes, nstg;
 };

@@ -113,3 +113,11 @@ def test_reference_arm_two_workloads():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.DEFAULT_WORKLOADS.split(",") == ["decode_t1", "prefill_t4096"]
+
+
+def test_workload_list_keeps_overrides_together():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.workload_specs("decode_t1,prefill_t4096") == ["decode_t1", "prefill_t4096"]
+    assert bench.workload_specs("prefill_t4096:E=128,T=600") == ["prefill_t4096:E=128,T=600"]
+    assert bench.workload_specs("full_t1:E=64,decode_t1:T=4") == ["full_t1:E=64", "decode_t1:T=4"]
