@@ -220,23 +220,23 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-# Sources each timed kernel is compiled from (besides the shared k3moe_internal.cuh).
+# The source files that hold each timed kernel's device code (its own file, and the
+# tensor-core helpers for the tcgen05 kernels).
 KERNEL_SOURCES = {
     "gemv_gateup": ["k3moe_gemv.cu"], "gemv_down": ["k3moe_gemv.cu"],
     "gemm_gateup": ["k3moe_gemm.cu", "k3moe_tc.cuh"], "gemm_down": ["k3moe_gemm.cu", "k3moe_tc.cuh"],
+    "router_logits_tc": ["k3moe_route_tc.cu", "k3moe_tc.cuh"],
     "full_down_proj": ["k3moe_dense.cu", "k3moe_tc.cuh"], "full_up_proj": ["k3moe_dense.cu", "k3moe_tc.cuh"],
     "full_shared_gateup": ["k3moe_dense.cu", "k3moe_tc.cuh"], "full_shared_down": ["k3moe_dense.cu", "k3moe_tc.cuh"],
-    "router_logits_tc": ["k3moe_route_tc.cu", "k3moe_tc.cuh"],
 }
 
 
 def csrc_hash(kernel: str):
-    """Hash of the sources a kernel is built from (its file and the headers it includes).
-    A recorded DRAM traffic figure is reported only while this matches the hash taken
-    with it."""
+    """Hash of the files that hold a kernel's device code.  A recorded DRAM traffic figure
+    is reported only while this matches the hash taken with it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_moe_expert_k3moe_gb300", "csrc")
-    for name in sorted(KERNEL_SOURCES.get(kernel, [])) + ["k3moe_internal.cuh"]:
+    for name in sorted(KERNEL_SOURCES.get(kernel, [])):
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
