@@ -108,10 +108,12 @@ __global__ void __launch_bounds__(kDnThreads, 1) dense_tc_kernel(const DenseArgs
         set_status(a.status, K3MOE_DEV_TIMEOUT);
         bail = 1;
     };
-    // item i -> K part, row block, token tile
+    // item i -> K part, token tile, row block: the token tiles of one row block are
+    // consecutive, so the blocks working at once share a few row blocks' weights (read
+    // from DRAM once, then from L2) and the tokens (which fit L2) are re-read from L2
     auto part_of = [&](int i) { return i % a.P; };
-    auto rb_of = [&](int i) { return (i / a.P) % a.n_rb; };
-    auto tt_of = [&](int i) { return i / (a.P * a.n_rb); };
+    auto tt_of = [&](int i) { return (i / a.P) % a.n_tt; };
+    auto rb_of = [&](int i) { return i / (a.P * a.n_tt); };
 
     if (warp == kDnWarpProd) {
         if (lane == 0) {
