@@ -210,24 +210,21 @@ struct PrepArgs {
 
 // Block 0 validates the routing (offsets, idx and perm, through a copy of offsets in
 // shared memory) and builds the active list and the inverse permutation; block b >= 1
-// converts tokens [8(b-1), 8b): warp per token, its scale 2^-u (max|x_t| in [2^14, 2^15),
+// converts tokens [32(b-1), 32b): warp per token, its scale 2^-u (max|x_t| in [2^14, 2^15),
 // u in [-113, 113]) and the f16 row x * 2^-u.  The kernel lets the gate/up kernel launch
 // at once (its shared items need nothing from here); the token conversion reads only x,
 // so when x is complete at launch it runs before the wait for the routing.
-// 256 threads a block: small enough that the gate/up kernel launched early can share the
-// SMs with it.
-constexpr int kPrepThreads = 256;
-__global__ void __launch_bounds__(kPrepThreads) fwd_prep_kernel(PrepArgs a)
+__global__ void __launch_bounds__(1024) fwd_prep_kernel(PrepArgs a)
 {
     pdl_trigger();
     if (blockIdx.x == 0 || !a.early) pdl_wait();
     __shared__ int32_t bad;
-    __shared__ int32_t scan_tmp[kPrepThreads / 32];
+    __shared__ int32_t scan_tmp[32];
     __shared__ int32_t off[kMaxExperts + 1];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = a.E, slots = a.T * a.k;
     if (blockIdx.x > 0) {
-        const int t = (blockIdx.x - 1) * (kPrepThreads / 32) + warp;
+        const int t = (blockIdx.x - 1) * 32 + warp;
         if (t >= a.T) {
             if (lane == 0) pdl_wait();      // the grid completes after the routing did
             return;
@@ -1216,8 +1213,7 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     PrepArgs pa{T, c.n_experts, c.top_k, c.d, x, idx, offsets, perm, active, inv, tok_scale, xs, status, abort,
                 x_is_input ? 1 : 0};
     timing_begin("fwd_prep", s);
-    cudaError_t err = launch_pdl(fwd_prep_kernel, dim3(1 + (T + kPrepThreads / 32 - 1) / (kPrepThreads / 32)),
-                                 dim3(kPrepThreads), 0, s, pa);
+    cudaError_t err = launch_pdl(fwd_prep_kernel, dim3(1 + (T + 31) / 32), dim3(1024), 0, s, pa);
     count_launch();
     timing_end("fwd_prep", s);
     if (err != cudaSuccess) return err;

@@ -28,8 +28,6 @@
 //   perm_scatter   perm[base + rank] = slot.
 // The map is a stable counting sort: offsets = exclusive prefix sum of the per-expert
 // counts, and inside an expert's segment the flat slot ids t*k+j ascend.
-#include <algorithm>
-
 #include "k3moe_exp.cuh"
 #include "k3moe_internal.cuh"
 
@@ -39,7 +37,7 @@ namespace {
 constexpr int kScoreWarps = 4;       // experts per block (one per warp)
 constexpr int kScoreTok = 8;         // tokens staged per round
 constexpr int kScoreTokBlock = 8;    // tokens per block (grid.y walks the rest)
-constexpr int kScoreChunks = 12;     // 16-byte Wr chunks per lane held at once (3072 columns; a multiple of 4)
+constexpr int kScoreChunks = 16;     // 16-byte Wr chunks per lane held at once (4096 columns)
 
 // Bound on the tensor-core logits' error, relative to |x_t| |Wr[e]|.  Their fp32
 // accumulation was measured within 2^-22 of that scale (3.7e-6 on unit-scale scores,
@@ -140,9 +138,7 @@ __device__ __forceinline__ float exact_logit_warp(const uint4 *xs, const uint4 *
 
 // -------------------------------------------------------------------------------- exact scores
 // grid (ceil(E / 4), ceil(T / 8)); block y owns tokens [8 y, 8 y + 8).
-// At most 128 registers a thread (four blocks an SM by registers): at one token the
-// mat-vec kernels launched after the router can then share the SMs with it.
-__global__ void __launch_bounds__(kScoreWarps * 32, 4) router_scores_kernel(
+__global__ void __launch_bounds__(kScoreWarps * 32) router_scores_kernel(
     int T, int d, int E, const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
     const float *__restrict__ bias, float *__restrict__ sc_out, float *__restrict__ ch_out)
 {
@@ -156,8 +152,8 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 4) router_scores_kernel(
     const int tb0 = blockIdx.y * kScoreTokBlock, tb1 = min(T, tb0 + kScoreTokBlock);
     const uint4 *wrow = reinterpret_cast<const uint4 *>(wr + (size_t)min(e, E - 1) * d);
     const float b = (bias && e < E) ? bias[e] : 0.0f;
-    // the first 3072 columns of the row stay in registers across the tokens (the whole
-    // row for d <= 3072); their loads are in flight with the first x tile's
+    // the first 4096 columns of the row stay in registers across the token rounds (the
+    // whole row for d <= 4096); their loads are in flight with the first x tile's
     uint4 w0[kScoreChunks];
 #pragma unroll
     for (int j = 0; j < kScoreChunks; j++) {
@@ -188,7 +184,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 4) router_scores_kernel(
                 }
 #pragma unroll
                 for (int j = 0; j < kScoreChunks; j++) {
-                    const int c = c0 + lane + 32 * j;   // lane's chunk number c0 / 32 + j = j mod 4 (c0 / 32 = 12 w)
+                    const int c = c0 + lane + 32 * j;   // this lane's chunk number c0 / 32 + j = j mod 4
                     if (c < nchunk) acc_chunk(a[j & 3], xs[i * nchunk + c], w[j]);
                 }
             }
@@ -699,7 +695,7 @@ cudaError_t launch_router_scores(const k3moe_config &c, int T, const uint16_t *x
     (void)status;
     const int E = c.n_experts;
     static size_t smem_set = 0;
-    const size_t smem = (size_t)std::min(T, kScoreTok) * c.d * 2;   // the staged token rows
+    const size_t smem = (size_t)kScoreTok * c.d * 2;
     if (smem > smem_set) {
         cudaFuncSetAttribute(router_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         smem_set = smem;
