@@ -392,7 +392,7 @@ def reference_arm(args):
 # ----------------------------------------------------------------------------- GPU arm
 
 ARITHMETIC = ("router: exact logits (bf16 products exact in fp32, two-sum compensated "
-              "accumulation, one rounding), sigmoid from a double exp rounded to float; experts: "
+              "accumulation, one rounding), sigmoid from a correctly rounded float exp (fp32 double-float arithmetic); experts: "
               "MMA operands f16 (tokens x*2^-u, routed h; MXFP4 weights decoded exactly to f16) "
               "and bf16 (shared-expert weights, shared h), fp32 accumulation; output f32")
 
