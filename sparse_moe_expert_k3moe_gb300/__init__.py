@@ -23,7 +23,12 @@ __all__ = [
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "libk3moe.so")
+
+
+def _lib_file() -> str:
+    """The library of the variant K3MOE_BUILD_VARIANT names (libk3moe.so by default)."""
+    from .build import lib_path
+    return lib_path()
 
 K3MOE_OK = 0
 STATUS_NAMES = {0: "OK", 1: "EINVAL", 2: "ESHAPE", 3: "EALIGN", 4: "EWORKSPACE", 5: "ECUDA",
@@ -49,7 +54,7 @@ class K3MoEError(RuntimeError):
 
 
 def library_path() -> str:
-    return _LIB_PATH
+    return _lib_file()
 
 
 _lib = None
@@ -59,10 +64,11 @@ def lib():
     """The loaded libk3moe.so.  Raises if it has not been built (no fallback exists)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(_LIB_PATH):
-            raise ImportError(f"libk3moe.so is not built ({_LIB_PATH}); run "
+        path = _lib_file()
+        if not os.path.exists(path):
+            raise ImportError(f"{os.path.basename(path)} is not built ({path}); run "
                               "`python -m sparse_moe_expert_k3moe_gb300.build`")
-        L = ctypes.CDLL(_LIB_PATH)
+        L = ctypes.CDLL(path)
         vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         cp = ctypes.POINTER(K3MoEConfig)
         sig = {

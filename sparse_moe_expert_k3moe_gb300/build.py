@@ -1,6 +1,13 @@
 """Builds libk3moe.so in-tree: every csrc/*.cu compiled for sm_103a in parallel, then linked.
 
-Usage: python -m sparse_moe_expert_k3moe_gb300.build [--force]
+Variants (the environment variable K3MOE_BUILD_VARIANT picks the one the package loads):
+  release   libk3moe.so: the product;
+  debug     libk3moe_debug.so: -DK3MOE_DEBUG, device-side index checks that set the
+            K3MOE_DEV_BOUNDS status bit and skip the access;
+  sanitize  libk3moe_asan.so: host code under AddressSanitizer and UndefinedBehaviorSanitizer
+            (load it with the ASan runtime preloaded).
+
+Usage: python -m sparse_moe_expert_k3moe_gb300.build [--force] [--variant debug|sanitize]
 """
 from __future__ import annotations
 
@@ -12,11 +19,30 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
-LIB = os.path.join(HERE, "libk3moe.so")
-BUILD_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-Wall",
                      "--diag-suppress", "177", "-I", os.path.join(HERE, "..", "include")]
+_SAN = "-fsanitize=address,-fsanitize=undefined,-fno-sanitize-recover=all,-fno-omit-frame-pointer"
+# variant: (library, build folder, extra compile flags, extra link flags)
+VARIANTS = {
+    "release": ("libk3moe.so", "_build", [], []),
+    "debug": ("libk3moe_debug.so", "_build_debug", ["-DK3MOE_DEBUG"], []),
+    "sanitize": ("libk3moe_asan.so", "_build_asan", ["-Xcompiler", _SAN], ["-Xcompiler", _SAN]),
+}
+
+
+def variant() -> str:
+    v = os.environ.get("K3MOE_BUILD_VARIANT", "release") or "release"
+    if v not in VARIANTS:
+        raise ValueError(f"K3MOE_BUILD_VARIANT={v!r}: one of {sorted(VARIANTS)}")
+    return v
+
+
+def lib_path(v: str | None = None) -> str:
+    return os.path.join(HERE, VARIANTS[v or variant()][0])
+
+
+LIB = lib_path("release")
 
 
 def _nvcc() -> str:
@@ -33,22 +59,28 @@ def _deps():
         [os.path.join(HERE, "..", "include", "k3moe.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(v: str | None = None) -> bool:
+    lib = lib_path(v)
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, v: str | None = None) -> str:
+    """Builds one variant (default: the one K3MOE_BUILD_VARIANT names) and returns its path."""
+    v = v or variant()
+    lib_name, build_dir, cflags, lflags = VARIANTS[v]
+    lib = lib_path(v)
+    if not force and up_to_date(v):
+        return lib
+    build_dir = os.path.join(HERE, build_dir)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-        cmd = [nvcc] + NVCC_FLAGS + ["-c", src, "-o", obj]
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
+        cmd = [nvcc] + NVCC_FLAGS + cflags + ["-c", src, "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -60,14 +92,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lpthread", "-ldl", "-lrt"]
+    tmp = lib + f".tmp{os.getpid()}"
+    cmd = [nvcc] + ARCH + lflags + ["-shared", "-cudart", "static", "-o", tmp] + objs + \
+        ["-lpthread", "-ldl", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    var = sys.argv[sys.argv.index("--variant") + 1] if "--variant" in sys.argv else None
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, v=var))
