@@ -80,7 +80,12 @@ typedef enum k3moe_status {
 #define K3MOE_DEV_BAD_OFFSETS 0x2  /* offsets/perm inconsistent with idx */
 #define K3MOE_DEV_NAN_SCALE   0x4  /* warning: an E8M0 scale byte of 255 (read as 0) */
 #define K3MOE_DEV_TIMEOUT     0x8  /* a bounded wait gave up */
-#define K3MOE_DEV_ERROR_MASK  (K3MOE_DEV_BAD_INDEX | K3MOE_DEV_BAD_OFFSETS | K3MOE_DEV_TIMEOUT)
+/* Debug builds only (the library compiled with -DK3MOE_DEBUG, libk3moe_debug.so): an
+ * index was outside its buffer where a kernel was about to use it; the access was
+ * skipped or clamped.  Release builds keep the same guards but do not record them. */
+#define K3MOE_DEV_BOUNDS      0x10
+#define K3MOE_DEV_ERROR_MASK  (K3MOE_DEV_BAD_INDEX | K3MOE_DEV_BAD_OFFSETS | K3MOE_DEV_TIMEOUT | \
+                               K3MOE_DEV_BOUNDS)
 
 /* Human-readable name of a status code (static string). */
 const char *k3moe_strerror(k3moe_status s);
@@ -289,6 +294,22 @@ k3moe_status k3moe_device_status(void *ws, k3moe_stream stream, int32_t *code);
  * returns K3MOE_ETIMEOUT.  For tests of the failure path; asynchronous on
  * `stream`.  ws: a workspace as for k3moe_route (only its status word is used). */
 k3moe_status k3moe_check_wait_timeout(void *ws, int64_t limit_cycles, k3moe_stream stream);
+
+/* Exercises the index checks of a debug build (kimi-k3-in-c README, Part II,
+ * section 9: a fault is counted, never silent).  Launches one thread that checks
+ * `index` against [0, limit) the way the library's kernels check an index before
+ * they use it; nothing is read or written through the index.  In a debug build
+ * (k3moe_build_flags() & K3MOE_BUILD_DEBUG) an index outside the range sets
+ * K3MOE_DEV_BOUNDS in `ws`'s status word, and k3moe_device_status then returns
+ * K3MOE_EDEVICE; a release build records nothing.  Asynchronous on `stream`.
+ * ws: a workspace as for k3moe_route (only its status word is used); K3MOE_ESHAPE
+ * when limit < 1. */
+k3moe_status k3moe_check_bounds(void *ws, int32_t index, int32_t limit, k3moe_stream stream);
+
+/* How the library was built: K3MOE_BUILD_DEBUG when compiled with -DK3MOE_DEBUG
+ * (the device-side index checks record K3MOE_DEV_BOUNDS). */
+#define K3MOE_BUILD_DEBUG 0x1
+int32_t k3moe_build_flags(void);
 
 /* Number of GPU kernels this library has launched in this process (all
  * calls, all devices); for launch accounting in benchmarks. */

@@ -16,7 +16,7 @@ __all__ = [
     "K3MoEConfig", "K3MOE_OK", "K3MoEError", "lib", "k3moe_config", "k3moe_validate_config",
     "k3moe_packed_bytes", "k3moe_workspace_bytes", "k3moe_pack_mxfp4", "k3moe_unpack_mxfp4",
     "k3moe_route", "k3moe_router_scores", "k3moe_forward", "k3moe_forward_noalloc", "k3moe_device_status",
-    "k3moe_check_wait_timeout", "k3moe_strerror",
+    "k3moe_check_wait_timeout", "k3moe_check_bounds", "k3moe_build_flags", "k3moe_strerror",
     "k3moe_launch_count", "k3moe_timing_enable", "k3moe_timing_read", "k3moe_timing_reset",
     "library_path", "MoELayer", "K3MoEFullDims", "k3moe_full_dims", "k3moe_full_workspace_bytes",
     "k3moe_full_forward", "MoEBlock",
@@ -33,7 +33,7 @@ def _lib_file() -> str:
 K3MOE_OK = 0
 STATUS_NAMES = {0: "OK", 1: "EINVAL", 2: "ESHAPE", 3: "EALIGN", 4: "EWORKSPACE", 5: "ECUDA",
                 6: "EDEVICE", 7: "ETIMEOUT"}
-DEV_BAD_INDEX, DEV_BAD_OFFSETS, DEV_NAN_SCALE, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEV_BAD_INDEX, DEV_BAD_OFFSETS, DEV_NAN_SCALE, DEV_TIMEOUT, DEV_BOUNDS = 0x1, 0x2, 0x4, 0x8, 0x10
 
 
 class K3MoEConfig(ctypes.Structure):
@@ -84,6 +84,8 @@ def lib():
                                              vp, sz, vp]),
             "k3moe_device_status": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32)]),
             "k3moe_check_wait_timeout": (ctypes.c_int, [vp, i64, vp]),
+            "k3moe_check_bounds": (ctypes.c_int, [vp, i32, i32, vp]),
+            "k3moe_build_flags": (i32, []),
             "k3moe_forward_noalloc": (ctypes.c_int, [cp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp,
                                                      vp, vp, vp, vp]),
             "k3moe_full_workspace_bytes": (ctypes.c_int, [cp, ctypes.POINTER(K3MoEFullDims), i32,
@@ -202,6 +204,20 @@ def k3moe_check_wait_timeout(ws, limit_cycles, stream=None):
     after limit_cycles cycles: sets the timeout bit of ws's status word."""
     _check("k3moe_check_wait_timeout", lib().k3moe_check_wait_timeout(_ptr(ws), int(limit_cycles),
                                                                       _stream(stream)))
+
+
+def k3moe_check_bounds(ws, index, limit, stream=None):
+    """Runs one index check of the kernels' kind on index against [0, limit): a debug
+    build records K3MOE_DEV_BOUNDS in ws's status word when it fails."""
+    _check("k3moe_check_bounds", lib().k3moe_check_bounds(_ptr(ws), int(index), int(limit), _stream(stream)))
+
+
+def k3moe_build_flags():
+    """BUILD_DEBUG (0x1) when the loaded library was compiled with -DK3MOE_DEBUG."""
+    return int(lib().k3moe_build_flags())
+
+
+BUILD_DEBUG = 0x1
 
 
 def k3moe_forward_noalloc(cfg, T, x, idx, weight, offsets, perm, expert_table, sh_w1, sh_w3,

@@ -102,6 +102,12 @@ static size_t max_total(const k3moe_config &c, int32_t T_max, Total total)
     return m;
 }
 
+// The index check of k3moe_check_bounds: the guard the kernels use, with no access.
+__global__ void check_bounds_kernel(int32_t *status, int32_t index, int32_t limit)
+{
+    (void)dguard(status, index >= 0 && index < limit);
+}
+
 }  // namespace k3moe
 
 using namespace k3moe;
@@ -342,6 +348,25 @@ k3moe_status k3moe_check_wait_timeout(void *ws, int64_t limit_cycles, k3moe_stre
     if (launch_wait_check_gemv(status, limit_cycles, s) != cudaSuccess) return K3MOE_ECUDA;
     if (launch_wait_check_tc(status, limit_cycles, s) != cudaSuccess) return K3MOE_ECUDA;
     return K3MOE_OK;
+}
+
+k3moe_status k3moe_check_bounds(void *ws, int32_t index, int32_t limit, k3moe_stream stream)
+{
+    if (!ws || !aligned(ws, 256)) return K3MOE_EWORKSPACE;
+    if (limit < 1) return K3MOE_ESHAPE;
+    cudaStream_t s = (cudaStream_t)stream;
+    check_bounds_kernel<<<1, 1, 0, s>>>(static_cast<int32_t *>(ws), index, limit);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+}
+
+int32_t k3moe_build_flags(void)
+{
+#ifdef K3MOE_DEBUG
+    return K3MOE_BUILD_DEBUG;
+#else
+    return 0;
+#endif
 }
 
 int64_t k3moe_launch_count(void) { return g_launches.load(); }

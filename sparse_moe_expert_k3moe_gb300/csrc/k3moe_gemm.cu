@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(256) gemm_gather_kernel(GatherArgs a)
                 atomicOr(a.abort, 1);
             }
         }
-        s = min(max(s, 0), slots - 1);
+        s = dclamp(a.status, s, 0, slots - 1);
         const int t = s / a.k;
         const float m = a.tok_scale[t];
         const uint4 v = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.d)[c];
@@ -287,7 +287,10 @@ __device__ __forceinline__ GItem gitem(const GemmArgs &a, const int32_t *prefix,
     const int4 u = *reinterpret_cast<const int4 *>(a.units + 4 * lo);
     GItem it;
     it.shared = u.x;
-    it.id = u.y;
+    // the unit list comes from gemm_units (validated offsets); debug builds record a unit
+    // outside the table or the slots, every build keeps the expert index in range
+    it.id = dclamp(a.status, u.y, 0, (u.x ? a.S : a.E) - 1);
+    dcheck(a.status, u.z >= 0 && u.w >= 0 && (size_t)u.z + u.w <= (u.x ? (size_t)a.T : (size_t)a.T * a.k));
     it.tok0 = u.z;
     it.ntok = u.w;
     const int ntiles = max(1, (it.ntok + kBM - 1) / kBM);
@@ -599,7 +602,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     row = MODE == kGU ? a.T * a.k + it.id * a.T + it.n0 + tr : it.n0 + tr;
                 } else {
                     const int p = it.tok0 + it.n0 + tr;
-                    const int slot = min(max(a.perm[p], 0), a.T * a.k - 1);
+                    const int slot = dclamp(a.status, a.perm[p], 0, a.T * a.k - 1);
                     if (MODE == kGU) {
                         row = p;
                         fo = a.tok_scale[a.T + slot / a.k];

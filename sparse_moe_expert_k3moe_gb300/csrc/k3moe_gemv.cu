@@ -380,12 +380,14 @@ __device__ __forceinline__ Unit unit_of(const GemvArgs &a, int u)
     Unit r;
     if (u >= 0) {
         r.shared = 0;
-        r.id = min(max(a.active[u], 0), a.E - 1);
+        r.id = dclamp(a.status, a.active[u], 0, a.E - 1);
         r.tok0 = a.offsets[r.id];
         r.ntok = a.offsets[r.id + 1] - r.tok0;
+        dcheck(a.status, r.tok0 >= 0 && r.ntok >= 0 && r.tok0 + r.ntok <= a.T * a.k);
     } else {
         r.shared = 1;
         r.id = -1 - u;
+        dcheck(a.status, r.id < a.S);
         r.tok0 = 0;
         r.ntok = a.T;
     }
@@ -482,7 +484,7 @@ __device__ __forceinline__ int token_of(const GemvArgs &a, const Unit &un, int p
 {
     if (un.shared) return pass * kPassTok + n;
     const int slot = a.perm[un.tok0 + pass * kPassTok + n];
-    return min(max(slot, 0), a.T * a.k - 1) / a.k;
+    return dclamp(a.status, slot, 0, a.T * a.k - 1) / a.k;
 }
 
 // Copies of one weight stage (thread 0 only).
@@ -766,7 +768,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
             if (i >= n_sh && n_items < 0) {
                 // the first routed item: the routing (and the forward's prep) must be complete
                 if (MODE == kGateUp) pdl_wait();
-                const int n_active = *a.abort ? 0 : min(max(a.active[a.E], 0), a.E);
+                const int n_active = *a.abort ? 0 : dclamp(a.status, a.active[a.E], 0, a.E);
                 n_items = n_sh + n_active * (Geo<MODE>::rows(a) / kItemRows);
             }
             const bool done = (i >= n_sh && i >= n_items) || __shfl_sync(0xffffffffu, bail, 0) != 0;
@@ -1020,6 +1022,7 @@ struct CombineArgs {
     const float *ys;
     float *out;
     const int32_t *abort;
+    int32_t *status;
 };
 
 // One thread per output element; the token's k positions and weights are read first and
@@ -1036,7 +1039,7 @@ __device__ __forceinline__ float combine_one(const CombineArgs &a, int t, int c)
     for (int j = 0; j < kMaxTopK; j++) {
         const int jj = j < a.k ? j : 0;
         const int p = a.inv[(size_t)t * a.k + jj];
-        pos[j] = min(max(p, 0), slots - 1);
+        pos[j] = dclamp(a.status, p, 0, slots - 1);
         wt[j] = j < a.k ? a.weight[(size_t)t * a.k + jj] : 0.0f;
     }
     float y[kMaxTopK];
@@ -1254,7 +1257,7 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
         timing_end("gemv_down", s);
         if (err != cudaSuccess) return err;
     }
-    CombineArgs ca{T, c.d, c.top_k, c.n_shared, 1, weight, inv, ys, out, abort};
+    CombineArgs ca{T, c.d, c.top_k, c.n_shared, 1, weight, inv, ys, out, abort, status};
     {
         const size_t n = (size_t)T * c.d;
         int grid = (int)((n + 255) / 256);

@@ -133,7 +133,8 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // (the parts' sums are added in order).  From two tokens on the routed items outnumber
 // the blocks enough to absorb whole shared items, and the split costs more than it
 // balances (measured at T = 2..16).  ktiles: 128-column tiles of K.  The down
-// projection is not split: measured, its split items cost more than the balance gains.
+// projection is not split: measured at T = 1, its split items cost more than the
+// balance gains (gemv_down 43.8 us whole, 43.9 in two parts, 47.4 in four).
 constexpr int kMaxSharedParts = 4;
 __host__ __device__ inline int shared_kparts(int ktiles, int T)
 {
@@ -357,6 +358,39 @@ __device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte_in_low_bits)
 __device__ __forceinline__ void set_status(int32_t *status, int32_t bits)
 {
     atomicOr(status, bits);
+}
+
+// Index checks at the point of use.
+//   dguard(status, ok): a guard every build keeps (the caller skips or clamps the
+//     access when ok is false); debug builds also record K3MOE_DEV_BOUNDS.
+//   dcheck(status, ok): a check only debug builds make (the caller skips the access
+//     when it fails); release builds compile it to true.
+__device__ __forceinline__ bool dguard(int32_t *status, bool ok)
+{
+#ifdef K3MOE_DEBUG
+    if (!ok) set_status(status, K3MOE_DEV_BOUNDS);
+#else
+    (void)status;
+#endif
+    return ok;
+}
+__device__ __forceinline__ bool dcheck(int32_t *status, bool ok)
+{
+#ifdef K3MOE_DEBUG
+    if (!ok) set_status(status, K3MOE_DEV_BOUNDS);
+    return ok;
+#else
+    (void)status;
+    (void)ok;
+    return true;
+#endif
+}
+// A clamp of an index into [lo, hi] that debug builds record when it changes the value.
+__device__ __forceinline__ int dclamp(int32_t *status, int v, int lo, int hi)
+{
+    const int c = min(max(v, lo), hi);
+    dguard(status, c == v);
+    return c;
 }
 
 #endif

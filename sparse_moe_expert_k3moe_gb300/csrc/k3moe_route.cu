@@ -303,7 +303,10 @@ __device__ void map_chunk(const MapArgs &a, int chunk, bool single, int32_t *cnt
         }
         if (threadIdx.x == 0) a.offsets[E] = a.T * k;
         __syncthreads();
-        if (my_e >= 0) a.perm[cnt[my_e] + my_rank] = t_begin * k + threadIdx.x;
+        if (my_e >= 0) {
+            const int p = cnt[my_e] + my_rank;
+            if (dcheck(a.status, p >= 0 && p < a.T * k)) a.perm[p] = t_begin * k + threadIdx.x;
+        }
     } else {
         if (my_e >= 0) a.local_rank[(size_t)t_begin * k + threadIdx.x] = my_rank;
         for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -574,7 +577,10 @@ __global__ void __launch_bounds__(kSelThreads) router_select_kernel(TopkArgs a)
     __syncthreads();
     // candidates (their order does not matter: the selection sorts their keys)
     for (int e = i; e < E; e += kSelThreads)
-        if (hio[e] >= thr_o) cand[atomicAdd(&n_cand, 1)] = e;
+        if (hio[e] >= thr_o) {
+            const int c = atomicAdd(&n_cand, 1);
+            if (dcheck(a.map.status, c < E)) cand[c] = e;
+        }
     __syncthreads();
     const int C = min(n_cand, E);
     // exact scores of the candidates, one warp per candidate
@@ -674,17 +680,17 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(int total_slots, int 
                                                            const int32_t *__restrict__ idx,
                                                            const int32_t *__restrict__ chunk_base,
                                                            const int32_t *__restrict__ local_rank,
-                                                           int32_t *__restrict__ perm)
+                                                           int32_t *__restrict__ perm, int32_t *status)
 {
     pdl_trigger();      // the next kernel may launch now: it waits for this one
     pdl_wait();
     const int s = blockIdx.x * blockDim.x + threadIdx.x;
     if (s >= total_slots) return;
     const int e = idx[s];
-    if (e < 0 || e >= E) return;
+    if (!dguard(status, e >= 0 && e < E)) return;
     const int chunk = s / (kChunkTokens * k);
     const int p = chunk_base[(size_t)chunk * E + e] + local_rank[s];
-    if (p >= 0 && p < total_slots) perm[p] = s;
+    if (dguard(status, p >= 0 && p < total_slots)) perm[p] = s;
 }
 
 }  // namespace
@@ -786,7 +792,8 @@ cudaError_t launch_route(const k3moe_config &c, int T, const uint16_t *x, const 
         if (err != cudaSuccess) return err;
         timing_begin("perm_scatter", s);
         err = launch_pdl(perm_scatter_kernel, dim3((T * k + 255) / 256), dim3(256), 0, s, T * k, k, E,
-                         (const int32_t *)idx, (const int32_t *)base, (const int32_t *)m.local_rank, perm);
+                         (const int32_t *)idx, (const int32_t *)base, (const int32_t *)m.local_rank, perm,
+                         status);
         count_launch();
         timing_end("perm_scatter", s);
         if (err != cudaSuccess) return err;

@@ -126,6 +126,12 @@ def test_host_validation_rejects_before_launch(k3):
     assert L.k3moe_check_wait_timeout(vp(A + 8), 1000, None) == 4
     assert L.k3moe_check_wait_timeout(vp(A), 0, None) == 2
     assert L.k3moe_check_wait_timeout(vp(A), 4000000001, None) == 2
+    # the index-check hook: no workspace, an empty range; the build flags
+    assert L.k3moe_check_bounds(None, 0, 4, None) == 4
+    assert L.k3moe_check_bounds(vp(A + 8), 0, 4, None) == 4
+    assert L.k3moe_check_bounds(vp(A), 0, 0, None) == 2
+    want = k3.BUILD_DEBUG if k3.library_path().endswith("libk3moe_debug.so") else 0
+    assert k3.k3moe_build_flags() == want
     # no-allocation forward: T beyond the largest any call accepts, a misaligned status word
     nargs = lambda T, st: (ctypes.byref(cfg), T, vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), tb,
                            vp(A), vp(A), vp(A), vp(A), st, None)
