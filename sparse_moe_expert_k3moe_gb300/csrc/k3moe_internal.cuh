@@ -103,8 +103,22 @@ inline bool use_gemm_path(const k3moe_config &c, int T)
 }
 
 // Workspace regions (byte offsets), sized for one call's T.
+// Counters that kernels keep at zero between calls live in one block at a fixed offset
+// (right after the status block) in every layout, whatever T and the path: buffers of a
+// call with another T must never overlap them.  Sized for the largest configuration.
+constexpr size_t kCtrShared = (size_t)kMaxShared * (kMaxWidth / kTileRows);  // shared gate/up K-part arrivals
+constexpr size_t kCtrReady = (size_t)kMaxExperts + kMaxShared;                // h rows ready, per unit
+// dense split-K arrivals: 128-row blocks of the widest projection (N <= S f) x 4 token
+// tiles (K is split only while T <= 512) x 4 quadrants
+constexpr size_t kCtrDense = (size_t)kMaxShared * (kMaxWidth / 128) * 4 * 4;
+constexpr size_t kCtrOffset = 256;
+constexpr size_t kCtrBytes = ((kCtrShared + kCtrReady + kCtrDense) * 4 + 255) & ~(size_t)255;
+
 struct WsLayout {
     size_t status;
+    size_t shctr;                // fixed counter block: shared gate/up arrival counters [S][f/128] int32
+    size_t ready;                // fixed counter block: h-ready counters per unit [E + S] int32
+    size_t dctr;                 // fixed counter block: dense split-K arrival counters
     size_t sc, ch;               // router scores [T][E] f32 (tensor-core router: sc holds its logits)
     size_t wnorm;                // router row norms |Wr[e]| [E] f32 (tensor-core router)
     size_t chunk_counts;         // [n_chunks][E] int32
@@ -117,7 +131,6 @@ struct WsLayout {
     size_t xs;                   // decode: activations x * 2^-u per token [T][d] f16
     size_t ys;                   // decode: y rows [rows_y][d] f32 (a shared expert's K parts: one row each)
     size_t gush;                 // decode: shared gate/up partials [parts][S][T][2][f] f32
-    size_t shctr;                // decode: shared gate/up arrival counters [S][f/128] int32
     size_t xg;                   // prefill: routed activations in perm order [T*k][d] f16
     size_t units;                // prefill: unit list [E+S][4], item prefixes, unit count
     size_t total;
@@ -151,6 +164,10 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     L.gemm = use_gemm_path(c, T);
     size_t o = 0;
     L.status = o; o += 256;
+    L.shctr = kCtrOffset;
+    L.ready = L.shctr + kCtrShared * 4;
+    L.dctr = L.ready + kCtrReady * 4;
+    o = kCtrOffset + kCtrBytes;
     L.sc = o; o = align256(o + (size_t)T * E * 4);
     L.ch = o; o = align256(o + (size_t)T * E * 4);
     L.wnorm = o; o = align256(o + E * 4);
@@ -166,7 +183,6 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     const size_t pgu = (size_t)shared_kparts(c.d / kTileK, T), pdn = 1;
     L.ys = o; o = align256(o + (L.gemm ? 0 : (slots + S * pdn * (size_t)T) * (size_t)c.d * 4));
     L.gush = o; o = align256(o + (L.gemm || pgu == 1 ? 0 : pgu * S * (size_t)T * 2 * c.f * 4));
-    L.shctr = o; o = align256(o + (L.gemm ? 0 : S * (size_t)(c.f / kTileRows) * 4));
     L.xg = o; o = align256(o + (L.gemm ? slots * (size_t)c.d * 2 : 0));
     L.units = o; o = align256(o + (L.gemm ? (4 * (E + S) + 2 * (E + S + 1) + 1) * 4 : 0));
     L.total = o;
@@ -202,7 +218,7 @@ struct FullLayout {
     size_t y;                    // [T][d] bf16: the normed sum, the up projection's input
     size_t act;                  // [T][S*f] bf16: the shared experts' SiTU
     size_t part;                 // dense projections' K-part partial sums
-    size_t ctr;                  // their arrival counters (kept at zero between calls)
+    size_t ctr;                  // their arrival counters: the fixed counter block's
     size_t total;
 };
 
@@ -219,16 +235,13 @@ inline FullLayout full_layout(const k3moe_config &c, int hidden, int T)
     const size_t SI = (size_t)c.n_shared * c.f;
     // widest partial row over the four projections: Wd (d), Wu and Sh2 (H), Sh1 + Sh3 (2 SI)
     const size_t wmax = std::max(std::max((size_t)c.d, (size_t)hidden), 2 * SI);
-    // counters: row blocks x token tiles x 4 quadrants; K is split only while P * T <=
-    // kDensePartRows, so at most 512 tokens there: 4 token tiles of 128
-    const size_t nrb_max = std::max(std::max((size_t)c.d, (size_t)hidden), SI) / 128;
     size_t o = align256(F.route.total > F.latent.total ? F.route.total : F.latent.total);
     F.z = o; o = align256(o + td * 2);
     F.acc = o; o = align256(o + td * 4);
     F.y = o; o = align256(o + td * 2);
     F.act = o; o = align256(o + ts * 2);
     F.part = o; o = align256(o + (T > 0 ? (size_t)kDensePartRows * wmax * 4 : 0));
-    F.ctr = o; o = align256(o + nrb_max * 4 * 4 * 4);
+    F.ctr = F.route.dctr;        // at the same fixed offset in the route and latent layouts
     F.total = o;
     return F;
 }

@@ -255,6 +255,28 @@ def test_alternating_shapes(k3):
         assert_out_close(host(out), ref, w.name)
 
 
+def test_workspace_reuse_across_paths(k3):
+    """One workspace for calls whose T takes different paths: the tensor-core GEMMs
+    (T = 64, 40) and the streamed mat-vecs with the shared expert's gate/up split in K
+    (T = 1).  The counters the kernels keep at zero between calls sit in a block at a
+    fixed offset, so no buffer of a call with another T overwrites them."""
+    from k3moe_inputs.device import build_layer
+    big = ki.Workload("reuse", T=64, d=256, f=256, E=8, k=2, S=1, exp_lo=-8, exp_hi=-4, seed=87)
+    layer = build_layer(big)
+    for T in (64, 1, 64, 1, 40, 1):
+        w = big.with_(name=f"reuse_T{T}", T=T)
+        x = ki.make_x(w)
+        xd = dev16(x)
+        layer.route(xd)
+        out = torch.full((T, w.d), float("nan"), dtype=torch.float32, device="cuda")
+        layer.forward(xd, out)
+        rc, code = k3.k3moe_device_status(layer.ws)
+        assert rc == 0 and code == 0
+        ref = oracle.forward(ocfg(w), x, host(layer.idx)[:T], host(layer.weight)[:T],
+                             oracle_experts(w, range(w.E)), ki.make_shared(w))
+        assert_out_close(host(out), ref, w.name)
+
+
 @pytest.mark.parametrize("T,bitwise", [(1, True), (4, True), (40, False)])
 def test_graph_replay(k3, T, bitwise):
     """route + forward captured as one CUDA graph: a replay gives the eager call's routing
@@ -540,6 +562,30 @@ def test_full_block_parity(k3, w):
     blk.forward(dev16(h[:0]), out[:0])
     torch.cuda.synchronize()
     assert not host(blk.offsets).any()
+
+
+def test_block_workspace_reuse_across_paths(k3):
+    """One block workspace for T = 200 (latent experts on the GEMMs, dense projections
+    split in K over token tiles), T = 40 (mat-vecs, split dense projections) and T = 1
+    (row-streaming projections): the dense split-K counters and the layer's counters stay
+    consistent from call to call."""
+    from k3moe_inputs.device import build_block
+    big = ki.Workload("full_reuse", T=200, d=512, f=256, E=32, k=4, S=2, exp_lo=-9, exp_hi=-5, seed=89,
+                      hidden=1024)
+    blk = build_block(big)
+    for T in (200, 40, 200, 40, 1):
+        w = big.with_(name=f"full_reuse_T{T}", T=T)
+        h = ki.make_h(w)
+        out = torch.full((T, w.hidden), float("nan"), dtype=torch.float32, device="cuda")
+        blk.forward(dev16(h), out)
+        rc, code = k3.k3moe_device_status(blk.ws)
+        assert rc == 0 and code == 0
+        gidx, gw = host(blk.idx)[:T], host(blk.weight)[:T]
+        full = ki.make_full(w)
+        shared = {"w1": full["sh1"], "w3": full["sh3"], "w2": full["sh2"]}
+        ref = oracle.forward_full(ocfg(w), w.hidden, w.latent_norm, w.rms_eps, h, gidx, gw, full["down"],
+                                  oracle_experts(w, gidx.ravel()), full["gain"], full["up"], shared)
+        assert_out_close(host(out), ref, w.name)
 
 
 def test_block_graph_replay(k3):
