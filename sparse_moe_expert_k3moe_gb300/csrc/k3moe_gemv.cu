@@ -11,7 +11,10 @@
 //   gemv_gateup  for every (active expert, token) and (shared expert, token): g = W1 x,
 //                u = W3 x, h = SiTU(g, u), stored as f16 (routed) or a bf16 hi + lo
 //                pair (shared);
-//   gemv_down    y = W2 h, fp32, one row per (slot or shared expert, token);
+//   gemv_down    y = W2 h, fp32, one row per (slot or shared expert, token); for a single
+//                token it does not wait for the whole gate/up grid: each item waits for
+//                its unit's h rows, which the gate/up warps publish (per-unit counters,
+//                release / acquire), so down items stream while gate/up's last items run;
 //   fwd_combine  out[t] = sum_j w[t][j] y[pos(t,j)] + sum_s y_shared[s][t], terms added
 //                in a fixed order.
 //
@@ -124,6 +127,40 @@ __device__ __forceinline__ void tma_2d_g2s(void *dst, const CUtensorMap *map, in
 __device__ __forceinline__ void fence_proxy_async()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Orders this thread's earlier generic-proxy accesses (an acquire of data other SMs
+// wrote) before its later bulk copies, which read global memory through the async proxy.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+__device__ __forceinline__ int ld_acquire(const int32_t *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ int ld_relaxed(const int32_t *p)
+{
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// Waits (bounded, with short sleeps) until *p >= want; false when the limit ran out.
+__device__ __forceinline__ bool wait_at_least(const int32_t *p, int want, long long limit = kWaitCycles)
+{
+    if (ld_acquire(p) >= want) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(200);
+        if (ld_acquire(p) >= want) return true;
+        if (clock64() - t0 > limit) return false;
+    }
+}
+// Publishes what this warp stored: every lane's release fence, then lane 0 adds n to *p.
+__device__ __forceinline__ void publish_add(int32_t *p, int n, int lane)
+{
+    fence_acq_rel();
+    __syncwarp();
+    if (lane == 0) atomicAdd(p, n);
 }
 
 // Four packed bytes -> four f16x2 (each byte: low nibble -> low half).
@@ -366,7 +403,19 @@ struct GemvArgs {
     int32_t *work;                  // [2] work counters: gate/up (reset by its last block), down (zeroed by fwd_prep)
     int32_t *exits;                 // gate/up blocks that have finished (reset by the last)
     int early;                      // 1: x is complete at launch (the gate/up shared items start at once)
+    int32_t *ready;                 // [E + S] h rows published per unit (gate/up warps add, down reads)
+    int32_t *route_seen;            // raised by gate/up once the routing is visible to it
+    int32_t *dn_exits;              // down blocks that have finished (the last resets ready, route_seen)
+    int32_t *gu_done;               // raised by the last gate/up block to finish (all h published)
 };
+
+// gate/up, after a wait for the routing: tells the down kernel that the routing (and
+// what the forward's prep wrote) is visible; release, so an acquire of the flag carries it.
+__device__ __forceinline__ void raise_route_seen(const GemvArgs &a)
+{
+    __threadfence();
+    atomicExch(a.route_seen, 1);
+}
 
 struct Unit {         // one expert (routed or shared) with its tokens
     int shared;       // 0: routed expert e; 1: shared expert s
@@ -701,20 +750,37 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity)
 
 // Facts of the unit, item and pass a staged B chunk belongs to (written by the producer).
 struct BHdr {
-    int item, pass, nvalid;
+    int item, pass;
+    int nvalid;                     // tokens of the pass (<= 16); the single-token schedule sets bit 8 on the item's last pass
     int shared, id, rb, kp, nkp;
 };
+constexpr int kLastPass = 1 << 8;
 
-template <int MODE, int TPS>
+template <int MODE, int TPS, bool STREAM>
 __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_constant__ GemvArgs a,
                                                              const __grid_constant__ CUtensorMap m1,
                                                              const __grid_constant__ CUtensorMap m3,
                                                              const __grid_constant__ CUtensorMap m2)
 {
     // gate/up: launched early (programmatic dependent launch) and waits for the routing only
-    // before its first routed item; down: waits for gate/up first
-    if (MODE == kDown || !a.early) pdl_wait();
-    pdl_trigger();
+    // before its first routed item.  down, for several tokens: waits for gate/up first.
+    // down for a single token (STREAM), where gate/up's last items leave most blocks
+    // idle: launched early too, and it waits neither for the gate/up grid nor for all of
+    // h: first for the routing to be visible (the flag gate/up raises after its own wait
+    // for it), then, item by item, for its unit's h rows, which gate/up publishes unit by
+    // unit (a.ready).  That down never lets its dependents launch early, and each block
+    // waits for the gate/up grid before it exits, so the kernels after it still start on a
+    // completed chain.
+    if (MODE == kGateUp) {
+        if (!a.early) {
+            pdl_wait();
+            if (STREAM && threadIdx.x == 0) raise_route_seen(a);
+        }
+        pdl_trigger();
+    } else if (!STREAM) {
+        pdl_wait();
+        pdl_trigger();
+    }
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     constexpr int kStageBytes = Geo<MODE>::kStageBytes;
@@ -729,9 +795,9 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
     __shared__ PassTok pts[kBSlots];
     __shared__ BHdr bh[kBSlots];
     __shared__ __align__(16) int32_t bflag[kBSlots][4];
-    __shared__ int bail;
+    __shared__ int bail, route_ok, last_dn;
 
-    if (MODE == kDown && *a.abort) return;
+    if (MODE == kDown && !STREAM && *a.abort) return;
     const int n_sh = n_shared_items<MODE>(a);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int nwarps = kThreads / 32;
@@ -748,12 +814,26 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         bail = 0;
+        if (MODE == kDown && STREAM) {
+            route_ok = 1;
+            if (!wait_at_least(a.route_seen, 1)) {
+                set_status(a.status, K3MOE_DEV_TIMEOUT);
+                route_ok = 0;
+            }
+        }
     }
     __syncthreads();
     auto timeout = [&]() {
         set_status(a.status, K3MOE_DEV_TIMEOUT);
         bail = 1;
     };
+    // down: every thread acquires the flag itself before it reads the routing; no items
+    // when the routing failed validation or never became visible
+    bool down_skip = false;
+    if (MODE == kDown && STREAM) {
+        if (route_ok) (void)ld_acquire(a.route_seen);
+        down_skip = !route_ok || *a.abort != 0;
+    }
 
     if (w == nwarps) {
         // ---------------- producer warp: work items, B chunks and weight stages, all by
@@ -761,17 +841,21 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
         int n = 0, bu = 0;
         bool stop = false;
         int n_items = -1;                       // known once the routing is
+        bool gu_seen = false;                   // down: gate/up's last block has finished
         for (;;) {
             int i = 0;
-            if (lane == 0) i = atomicAdd(&a.work[MODE], 1);
+            if (lane == 0 && !down_skip) i = atomicAdd(&a.work[MODE], 1);
             i = __shfl_sync(0xffffffffu, i, 0);
-            if (i >= n_sh && n_items < 0) {
+            if (!down_skip && i >= n_sh && n_items < 0) {
                 // the first routed item: the routing (and the forward's prep) must be complete
-                if (MODE == kGateUp) pdl_wait();
+                if (MODE == kGateUp) {
+                    pdl_wait();
+                    if (STREAM && lane == 0) raise_route_seen(a);
+                }
                 const int n_active = *a.abort ? 0 : dclamp(a.status, a.active[a.E], 0, a.E);
                 n_items = n_sh + n_active * (Geo<MODE>::rows(a) / kItemRows);
             }
-            const bool done = (i >= n_sh && i >= n_items) || __shfl_sync(0xffffffffu, bail, 0) != 0;
+            const bool done = down_skip || (i >= n_sh && i >= n_items) || __shfl_sync(0xffffffffu, bail, 0) != 0;
             if (done) {
                 // end of stream: one stage with no copy
                 const int slot = n % kStages;
@@ -786,6 +870,29 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
             const Unit un = unit_of(a, it.u);
             const int pass1 = it.pass1 < 0 ? n_passes(un) : it.pass1;
             const int nst = n_stages<MODE, TPS>(a, un.shared);
+            if (MODE == kDown && STREAM && !gu_seen) {
+                // the unit's h rows are complete once every gate/up warp of every row block
+                // (and token pass) has published them, and all of h once gate/up's last block
+                // has finished; after that flag is seen no item checks again.  Lane 0 reads
+                // both (relaxed, one round trip), then acquires; the warp's bulk copies that
+                // read h are ordered after it.
+                const int want = nwarps * (a.f / kItemRows) * (un.shared ? shared_passes(a) : 1);
+                const int32_t *rp = a.ready + (un.shared ? a.E + un.id : un.id);
+                int ok = 1, done_all = 0;
+                if (lane == 0) {
+                    done_all = ld_relaxed(a.gu_done);
+                    const int r = ld_relaxed(rp);
+                    if (!done_all && r < want) ok = wait_at_least(rp, want) ? 1 : 0;
+                    fence_acq_rel();
+                }
+                __syncwarp();
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    timeout();
+                    break;
+                }
+                gu_seen = __shfl_sync(0xffffffffu, done_all, 0) != 0;
+                fence_proxy_async_all();
+            }
             for (int pass = it.pass0; pass < pass1 && !stop; pass++) {
                 const int nvalid = min(kPassTok, un.ntok - pass * kPassTok);
                 // token facts of this pass: lane n holds token n's
@@ -813,7 +920,9 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                             pts[b].row[lane] = row;
                             pts[b].fo[lane] = fo;
                         }
-                        if (lane == 0) bh[b] = BHdr{i, pass, nvalid, un.shared, un.id, it.rb, it.kp, it.nkp};
+                        if (lane == 0)
+                            bh[b] = BHdr{i, pass, nvalid | (STREAM && pass == pass1 - 1 ? kLastPass : 0), un.shared,
+                                         un.id, it.rb, it.kp, it.nkp};
                         __syncwarp();
                         issue_b_chunk<MODE>(a, un, it, st / spc, nvalid, tok, row, bbase + kHalves * b * bbytes,
                                             bbase + (kHalves * b + kHalves - 1) * bbytes, bflag[b], &bfull[b], lane);
@@ -876,11 +985,11 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
             }
             const uint8_t *buf = bufs + slot * kStageBytes;
             if (!h.shared && bflag[b][3] != 0) {
-                if (h.nvalid > 8)
+                if ((STREAM ? h.nvalid & 0xFF : h.nvalid) > 8)
                     consume_stage<MODE, 2, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, acc1, acc3);
                 else
                     consume_stage<MODE, 1, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, acc1, acc3);
-            } else if (h.nvalid > 8) {
+            } else if ((STREAM ? h.nvalid & 0xFF : h.nvalid) > 8) {
                 consume_stage<MODE, 2, TPS, false>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
             } else {
                 consume_stage<MODE, 1, TPS, false>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
@@ -892,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                 // epilogue: this thread holds rows 16w+g (+8) x tokens 8nb+2t4 (+1)
                 const int row0 = h.rb * kItemRows + 16 * w + g;
                 const size_t rows_all = (size_t)a.T * a.k + (size_t)a.S * a.T;
-                const int nvalid = h.nvalid;
+                const int nvalid = STREAM ? h.nvalid & 0xFF : h.nvalid;
                 const size_t slots = (size_t)a.T * a.k;
                 if (MODE == kDown) {
                     // y row: the slot's, or for a shared expert its K part's (the combine
@@ -967,6 +1076,9 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                                 store_h(a, 1, (size_t)pt.row[nn] * a.f + row, plane, situ(gs, us, a.b1, a.b2));
                             }
                         }
+                        // this warp wrote the row block's 128 rows: as much as eight warps of
+                        // an unsplit item
+                        if (STREAM) publish_add(a.ready + a.E + h.id, nwarps, lane);
                     }
                 } else {
                     const size_t plane = rows_all * a.f;
@@ -981,6 +1093,8 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                             store_h(a, h.shared, (size_t)pt.row[nn] * a.f + row, plane,
                                     situ(acc1[nb][i] * fo, acc3[nb][i] * fo, a.b1, a.b2));
                         }
+                    // after the item's last pass this warp's 16 rows of h are complete
+                    if (STREAM && (h.nvalid & kLastPass)) publish_add(a.ready + (h.shared ? a.E + h.id : h.id), 1, lane);
                 }
             }
             if (chunk_end) {
@@ -1001,6 +1115,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
     if (MODE == kGateUp && tid == 0) {
         // the grid completes only after the routing did (the next kernel's wait covers both)
         pdl_wait();
+        if (STREAM) raise_route_seen(a);
         // the last block to leave resets the work counter and the K-part arrival counters
         // for the next call (prep cannot: this kernel may run before it)
         __threadfence();
@@ -1009,6 +1124,29 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
             for (int q = 0; q < a.S * (a.f / kItemRows); q++) a.shctr[q] = 0;
             __threadfence();
             *a.exits = 0;
+            // every block has finished, after its fence: all of h is published
+            if (STREAM) atomicExch(a.gu_done, 1);
+        }
+    }
+    if (MODE == kDown && STREAM) {
+        if (tid == 0) {
+            // the grid completes only after gate/up did: the kernels after it rely on that
+            pdl_wait();
+            __threadfence();
+            last_dn = atomicAdd(a.dn_exits, 1) == (int)gridDim.x - 1;
+        }
+        __syncthreads();
+        if (last_dn) {
+            // the last block to leave (every gate/up increment is done, every down block has
+            // read its counters): reset the h-ready counters and the routing flag
+            for (int u = tid; u < a.E + a.S; u += blockDim.x) a.ready[u] = 0;
+            __syncthreads();
+            if (tid == 0) {
+                *a.route_seen = 0;
+                *a.gu_done = 0;
+                __threadfence();
+                *a.dn_exits = 0;
+            }
         }
     }
 }
@@ -1127,20 +1265,21 @@ int grid_blocks(Kern kernel, size_t smem)
     struct Entry { const void *k; size_t smem; int blocks; };
     struct Limit { const void *k; size_t smem; };
     static Entry cache[16];
-    static Limit limit[4];
+    static Limit limit[8];               // the six mat-vec kernels (mode x ring x schedule)
     static int n_cache = 0, n_limit = 0;
     static std::mutex mu;
     std::lock_guard<std::mutex> lk(mu);
     int li = 0;
     while (li < n_limit && limit[li].k != (const void *)kernel) li++;
     if (li == n_limit) {
-        limit[n_limit++] = Limit{(const void *)kernel, 0};
+        if (n_limit < 8) limit[n_limit++] = Limit{(const void *)kernel, 0};
+        else li = -1;                    // not cached: the attributes are set on every call
         cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     }
-    if (smem > limit[li].smem) {
+    if (li < 0 || smem > limit[li].smem) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        limit[li].smem = smem;
+        if (li >= 0) limit[li].smem = smem;
     }
     for (int i = 0; i < n_cache; i++)
         if (cache[i].k == (const void *)kernel && cache[i].smem == smem) return cache[i].blocks;
@@ -1231,15 +1370,19 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
     GemvArgs ga{T, c.d, c.f, c.top_k, c.n_shared, c.n_experts, 0, c.situ_b1, c.situ_b2,
                 x, xs, offsets, perm, active, tok_scale, table, expert_bytes(c.d, c.f),
                 gateup_block_bytes(c.d, c.f), ys, gush, shctr, hp, abort, status, abort + 1, status + 5,
-                x_is_input ? 1 : 0};
+                x_is_input ? 1 : 0, reinterpret_cast<int32_t *>(ws + L.ready), status + 6, status + 7,
+                status + 8};
+    // a single token: down starts unit by unit as gate/up publishes h
+    const bool stream = T == 1;
     // B chunks hold min(16, T) token rows
     ga.brows = T < kPassTok ? T : kPassTok;
     {
         const size_t bsl = (size_t)kBSlots * ga.brows * Geo<kGateUp>::b_row_bytes(ga);
         const size_t smem = 1024 + (size_t)kStages * Geo<kGateUp>::kStageBytes + bsl;
-        const int blocks = grid_blocks(gemv_kernel<kGateUp, 1>, smem);
+        const auto kern = stream ? gemv_kernel<kGateUp, 1, true> : gemv_kernel<kGateUp, 1, false>;
+        const int blocks = grid_blocks(kern, smem);
         timing_begin("gemv_gateup", s);
-        err = launch_pdl(gemv_kernel<kGateUp, 1>, dim3(blocks), dim3(kThreads + 32), smem, s, ga, m1, m3, m2);
+        err = launch_pdl(kern, dim3(blocks), dim3(kThreads + 32), smem, s, ga, m1, m3, m2);
         count_launch();
         timing_end("gemv_gateup", s);
         if (err != cudaSuccess) return err;
@@ -1249,7 +1392,8 @@ cudaError_t launch_forward_gemv(const k3moe_config &c, int T, const uint16_t *x,
         const size_t smem = 1024 + (size_t)kStages * Geo<kDown>::kStageBytes + bsl;
         // two K tiles per routed stage when K has an even number of tiles
         const bool two = (c.f / kTileK) % 2 == 0;
-        const auto kern = two ? gemv_kernel<kDown, 2> : gemv_kernel<kDown, 1>;
+        const auto kern = two ? (stream ? gemv_kernel<kDown, 2, true> : gemv_kernel<kDown, 2, false>)
+                              : (stream ? gemv_kernel<kDown, 1, true> : gemv_kernel<kDown, 1, false>);
         const int blocks = grid_blocks(kern, smem);
         timing_begin("gemv_down", s);
         err = launch_pdl(kern, dim3(blocks), dim3(kThreads + 32), smem, s, ga, m1, m3, m2);

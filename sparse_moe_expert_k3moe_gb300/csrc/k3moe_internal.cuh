@@ -86,8 +86,10 @@ static_assert(3 * (kMaxWidth / kTileRows) * 4 <= kTrailerBytes - 4,
 // Device status word and abort flag live in the first 256 bytes of the workspace.
 // Words: 0 status (K3MOE_DEV_* bits); 1 abort (nonzero: the routing failed validation,
 // later kernels skip work); 2, 3 the work counters of the two mat-vec kernels; 4 the
-// top-k kernel's last-block counter; 5 the gate/up mat-vec's exit counter.  Counters are
-// back at zero after every call.
+// top-k kernel's last-block counter; 5 the gate/up mat-vec's exit counter; 6 the flag the
+// gate/up mat-vec raises once the routing is visible to it; 7 the down mat-vec's exit
+// counter; 8 the flag the last gate/up block raises when all of h is published.  Counters
+// and flags are back at zero after every call.
 struct StatusBlock {
     int32_t status;
     int32_t abort;
