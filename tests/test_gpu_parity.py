@@ -257,13 +257,15 @@ def test_alternating_shapes(k3):
 
 def test_workspace_reuse_across_paths(k3):
     """One workspace for calls whose T takes different paths: the tensor-core GEMMs
-    (T = 64, 40) and the streamed mat-vecs with the shared expert's gate/up split in K
-    (T = 1).  The counters the kernels keep at zero between calls sit in a block at a
-    fixed offset, so no buffer of a call with another T overwrites them."""
+    (T = 64, 40), the streamed mat-vecs whose down items start per unit (T = 1, 2, 3;
+    at T = 1 with the shared expert's gate/up split in K), and those whose down waits for
+    all of gate/up (T = 4).  The counters the kernels keep at zero between calls sit in a
+    block at a fixed offset, so no buffer of a call with another T overwrites them, and
+    each schedule leaves them at zero for the next."""
     from k3moe_inputs.device import build_layer
     big = ki.Workload("reuse", T=64, d=256, f=256, E=8, k=2, S=1, exp_lo=-8, exp_hi=-4, seed=87)
     layer = build_layer(big)
-    for T in (64, 1, 64, 1, 40, 1):
+    for T in (64, 1, 64, 1, 4, 2, 40, 3, 1, 4, 1):
         w = big.with_(name=f"reuse_T{T}", T=T)
         x = ki.make_x(w)
         xd = dev16(x)
