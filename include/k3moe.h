@@ -105,8 +105,10 @@ size_t k3moe_packed_bytes(const k3moe_config *cfg);
 /* Workspace bytes that k3moe_route and k3moe_forward need for any
  * 0 <= T <= T_max.  The workspace is one caller-owned device buffer,
  * 256-byte aligned, shared by both calls; its first 256 bytes hold the
- * device status word.  Zero-fill it once before first use (the status word
- * must start at zero); the calls keep everything else consistent. */
+ * device status word, and the block after them the counters the kernels
+ * return to zero at the end of every call.  Zero-fill it once before first
+ * use; the calls keep everything else consistent, so one workspace serves
+ * calls of any T <= T_max in any order (calls on one stream). */
 k3moe_status k3moe_workspace_bytes(const k3moe_config *cfg, int32_t T_max, size_t *bytes);
 
 /* Relayout experts [expert_lo, expert_lo + n_in) from the checkpoint's MXFP4
