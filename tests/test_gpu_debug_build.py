@@ -9,8 +9,10 @@ word (kimi-k3-in-c README, Part II, section 9: a fault is counted, never silent)
   debug build reports K3MOE_DEV_BOUNDS and stays usable, the release build records
   nothing;
 - the debug build on the parity cases: the small layers (both forward paths, every
-  shape class of the suite), shape alternation and graph replay, each of which asserts a
-  clean status word after every call -- so no check fires on valid input.
+  shape class of the suite), shape alternation, graph replay, one workspace reused
+  across both forward paths and both mat-vec schedules, and the full K3 shape at T = 1
+  (the single-token schedule), each of which asserts a clean status word after every
+  call -- so no check fires on valid input.
 The debug library is built on the GPU machine and loaded by a child process
 (K3MOE_BUILD_VARIANT=debug); the release library in this process is untouched.
 """
@@ -82,7 +84,8 @@ def test_debug_build_records_a_bad_index(debug_lib):
 def test_debug_build_is_clean_on_the_parity_cases(debug_lib):
     cmd = [sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_gpu_parity.py"), "-q", "-m", "gpu",
            "-p", "no:cacheprovider", "-k",
-           "small_layer_parity or alternating_shapes or graph_replay or zero_tokens or injected_oracle_routing"]
+           "small_layer_parity or alternating_shapes or graph_replay or zero_tokens or injected_oracle_routing"
+           " or reuse or (full_forward_parity and decode_t1)"]
     r = subprocess.run(cmd, capture_output=True, text=True, env=_debug_env(), cwd=ROOT, timeout=1800)
     tail = r.stdout.strip().splitlines()
     print(tail[-1] if tail else "")
