@@ -565,14 +565,6 @@ __device__ void issue_stage(const GemvArgs &a, const CUtensorMap *m1, const CUte
     }
 }
 
-// B-operand layout in shared memory: [n-block][k-step][lane][8 bytes]; lane 4n+t of a
-// k-step holds the pairs (k0+2t, k0+2t+1) and (k0+2t+8, k0+2t+9) of token n.
-__device__ __forceinline__ uint32_t b_offset(int nb, int ks, int KS, int n, int kk)
-{
-    const int t = (kk & 7) >> 1, half = kk >> 3;
-    return (uint32_t)(((nb * KS + ks) * 32 + 4 * (n & 7) + t) * 8 + 4 * half);
-}
-
 // Per-pass token facts, computed once per pass into shared memory.
 struct PassTok {
     int tok[kPassTok];        // token index t
