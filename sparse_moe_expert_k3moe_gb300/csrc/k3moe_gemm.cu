@@ -1,9 +1,9 @@
 // k3moe_gemm.cu -- the expert part of the layer as grouped tensor-core GEMMs: the
 // prefill path (many tokens per expert).  Same mathematics as the decode path
 // (kimi-k3-in-c README, Part II, section 4 for the MXFP4 format, section 9 for the
-// expert loop and SiTU-GLU); here the weights are the 128-row M side of tcgen05 MMAs
-// ("swap AB"), an expert's tokens the N side, so an expert with few tokens still fills
-// the 128-row tile.
+// expert loop and SiTU-GLU).  An expert's tokens are the 128-row M side of the tcgen05
+// MMAs and its dequantised weight rows the 256-wide N side: an MMA instruction costs
+// about the same whatever its N, so only N = 256 runs at the tensor rate.
 //
 // Kernels, in launch order:
 //   gemm_units   validates offsets, lists the units (shared experts first, heaviest,
