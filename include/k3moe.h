@@ -185,9 +185,13 @@ k3moe_status k3moe_router_scores(const k3moe_config *cfg, int32_t T, const uint1
  *   sh_w1, sh_w3 [S][f][d] bf16;  sh_w2 [S][d][f] bf16 (NULL when S == 0);
  *                16-byte aligned
  *   out          [T][d] f32, written (not accumulated)
- * Intermediates stay in fp32 for small T (decode) and round the SiTU output
- * to bf16 for the tensor-core path at large T (prefill).  ws per
- * k3moe_workspace_bytes(T_max >= T). */
+ * Precision: x enters the MMAs as f16 times a per-token power of two (exact for
+ * every bf16 element within 2^31 of the token's largest), the MXFP4 weights
+ * are decoded exactly, and every accumulation is fp32.  The SiTU output of a
+ * routed expert is rounded to f16 before its down projection on both paths;
+ * that of a shared expert is kept as a bf16 hi + lo pair for small T (the
+ * streamed mat-vecs) and rounded to bf16 for the tensor-core path at large T.
+ * ws per k3moe_workspace_bytes(T_max >= T). */
 k3moe_status k3moe_forward(const k3moe_config *cfg, int32_t T, const uint16_t *x,
                            const int32_t *idx, const float *weight,
                            const int32_t *offsets, const int32_t *perm,
