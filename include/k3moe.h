@@ -317,6 +317,30 @@ k3moe_status k3moe_check_bounds(void *ws, int32_t index, int32_t limit, k3moe_st
 #define K3MOE_BUILD_DEBUG 0x1
 int32_t k3moe_build_flags(void);
 
+/* Which kernel runs the routed experts' gate/up projection on the prefill path
+ * (the tensor-core path k3moe_forward takes for T >= 32 and T*top_k >= 8*E).  Both
+ * compute g = W1 x, u = W3 x straight from the packed MXFP4 table (kimi-k3-in-c
+ * README, Part II, section 4 "Reduction one: the experts already ship at half a
+ * byte": an E2M1 code times the E8M0 scale of its 32-element group):
+ *   1  f16 MMAs on weights dequantised into shared memory (code x 2^(scale - block
+ *      maximum), exact in f16), the tokens as f16 x 2^-u;
+ *   2  block-scaled MMAs (tcgen05 kind::mxf8f6f4): the E2M1 codes and their E8M0
+ *      scales go to the tensor core as they are, and the tensor core applies the
+ *      scales per 32 elements; the tokens as two e4m3 planes with their own E8M0
+ *      scales per 32 elements, hi = rn(x / 2^sa) and lo = rn((x / 2^sa - hi) / 2^sl),
+ *      so each 32-wide K step is two MMAs into the same fp32 accumulator.  The two
+ *      planes hold a bf16 token exactly while its element lies within 2^12 of
+ *      its 32-block's largest magnitude (smaller ones: absolute error below 2^-21 of
+ *      that magnitude).  A scale byte of 255, which the format reads as zero, becomes
+ *      2^-127 (a contribution below 2^-120 of the group's codes);
+ *   0  the library's default, which is 1.
+ * The shared experts (bf16) and the down projection run on the f16 kernel either way.
+ * Process-wide; takes effect at the next k3moe_forward call (a captured graph keeps
+ * the kernels it recorded).  K3MOE_EINVAL for another value.  The workspace
+ * (k3moe_workspace_bytes) covers both. */
+k3moe_status k3moe_set_prefill_gemm(int32_t variant);
+int32_t k3moe_get_prefill_gemm(void);
+
 /* Number of GPU kernels this library has launched in this process (all
  * calls, all devices); for launch accounting in benchmarks. */
 int64_t k3moe_launch_count(void);

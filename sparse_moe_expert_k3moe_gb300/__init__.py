@@ -18,6 +18,7 @@ __all__ = [
     "k3moe_route", "k3moe_router_scores", "k3moe_forward", "k3moe_forward_noalloc", "k3moe_device_status",
     "k3moe_check_wait_timeout", "k3moe_check_bounds", "k3moe_build_flags", "k3moe_strerror",
     "k3moe_launch_count", "k3moe_timing_enable", "k3moe_timing_read", "k3moe_timing_reset",
+    "k3moe_set_prefill_gemm", "k3moe_get_prefill_gemm", "PREFILL_GEMM_F16", "PREFILL_GEMM_BLOCK_SCALED",
     "library_path", "MoELayer", "K3MoEFullDims", "k3moe_full_dims", "k3moe_full_workspace_bytes",
     "k3moe_full_forward", "MoEBlock",
 ]
@@ -94,6 +95,8 @@ def lib():
                                                   vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                   sz, vp]),
             "k3moe_launch_count": (i64, []),
+            "k3moe_set_prefill_gemm": (ctypes.c_int, [i32]),
+            "k3moe_get_prefill_gemm": (i32, []),
             "k3moe_timing_enable": (None, [i32]),
             "k3moe_timing_read": (i32, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i64),
                                         ctypes.POINTER(ctypes.c_double), i32]),
@@ -263,6 +266,20 @@ def k3moe_device_status(ws, stream=None):
 
 def k3moe_launch_count() -> int:
     return lib().k3moe_launch_count()
+
+
+PREFILL_GEMM_DEFAULT, PREFILL_GEMM_F16, PREFILL_GEMM_BLOCK_SCALED = 0, 1, 2
+
+
+def k3moe_set_prefill_gemm(variant: int):
+    """The kernel of the routed gate/up projection on the prefill path: PREFILL_GEMM_F16
+    (dequantised weights), PREFILL_GEMM_BLOCK_SCALED (kind::mxf8f6f4 on the packed codes
+    and scales) or PREFILL_GEMM_DEFAULT; process-wide."""
+    _check("k3moe_set_prefill_gemm", lib().k3moe_set_prefill_gemm(int(variant)))
+
+
+def k3moe_get_prefill_gemm() -> int:
+    return int(lib().k3moe_get_prefill_gemm())
 
 
 def k3moe_timing_enable(on: bool):

@@ -42,6 +42,16 @@ static cudaEvent_t take_event()
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+static std::atomic<int> g_prefill_gemm{0};
+int prefill_gemm_setting() { return g_prefill_gemm.load(std::memory_order_relaxed); }
+// The default (setting 0) is the f16 GEMM on dequantised weights.
+bool prefill_gemm_block_scaled(const k3moe_config &c, int T)
+{
+    (void)c;
+    (void)T;
+    return prefill_gemm_setting() == 2;
+}
+
 void timing_begin(const char *name, cudaStream_t s)
 {
     if (!g_timing_on.load(std::memory_order_relaxed)) return;
@@ -370,6 +380,15 @@ int32_t k3moe_build_flags(void)
 }
 
 int64_t k3moe_launch_count(void) { return g_launches.load(); }
+
+k3moe_status k3moe_set_prefill_gemm(int32_t variant)
+{
+    if (variant < 0 || variant > 2) return K3MOE_EINVAL;
+    g_prefill_gemm.store(variant, std::memory_order_relaxed);
+    return K3MOE_OK;
+}
+
+int32_t k3moe_get_prefill_gemm(void) { return prefill_gemm_setting(); }
 
 void k3moe_timing_enable(int32_t on) { g_timing_on.store(on ? 1 : 0); }
 

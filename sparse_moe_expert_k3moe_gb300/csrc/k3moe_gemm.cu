@@ -43,6 +43,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <climits>
 #include <mutex>
 
 #include "k3moe_internal.cuh"
@@ -264,6 +265,8 @@ struct GemmArgs {
     float *out;
     const int32_t *abort;
     int32_t *status;
+    int item_hi;                    // the kernel takes items [0, min(item_hi, all items))
+    const uint8_t *sfa;             // block-scaled GEMM: the token tiles' scale blocks
 };
 
 struct GItem {
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
     if (*a.abort) return;
     const int n_units = *a.n_units;
-    const int n_items = a.prefix[n_units];
+    const int n_items = min(a.prefix[n_units], a.item_hi);
     if ((int)blockIdx.x >= n_items) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int K = k_of<MODE>(a), nks = K / kBK;
@@ -680,6 +683,468 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
 }
 
+// ---------------------------------------------------------------------------------- block-scaled GEMM
+// The routed experts' gate/up projection on kind::mxf8f6f4 MMAs: the weights stay in
+// their E2M1 codes and the tensor core applies their E8M0 scales; nothing is dequantised.
+// The tokens enter as two e4m3 planes with their own per-32 scales (gemm_gather_mx): a
+// 32-wide K step is two MMAs, hi and lo, into the same fp32 accumulator.  For a bf16 token
+// the two planes hold it exactly while its element lies within 2^12 of its 32-block's
+// largest; a smaller element keeps an absolute error below 2^-21 of that largest.
+
+// Two floats -> two e4m3 bytes (round to nearest even, saturating), x0 in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_rn(float x0, float x1)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(x1), "f"(x0));
+    return r;
+}
+// Two e4m3 bytes (low byte first) -> two exact floats.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t b2)
+{
+    uint32_t h;
+    asm("{\n\t.reg .b16 b;\n\tcvt.u16.u32 b, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, b;\n\t}" : "=r"(h) : "r"(b2));
+    return __half22float2(*reinterpret_cast<__half2 *>(&h));
+}
+// The smallest s with v / 2^s <= 448 (the largest e4m3) for finite v > 0: with
+// v = m 2^e, m in [1, 2), s = e - 8, or e - 7 when m > 1.75.  Subnormal v gives a value
+// below -127, which the callers clamp.
+__device__ __forceinline__ int pow2_over448(float v)
+{
+    const uint32_t u = __float_as_uint(v);
+    const int b = (int)((u >> 23) & 255u);
+    return (b == 0 ? -127 : b - 127) - 8 + ((u & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+}
+
+struct GatherMxArgs {
+    int T, d, k, E, S, rb;          // rb: items per token tile (128-row blocks of f)
+    const uint16_t *x;
+    const int32_t *idx, *offsets, *perm;
+    const int32_t *units, *prefix, *n_units;
+    uint8_t *hi, *lo;               // [T*k][d] e4m3 planes, perm order
+    uint8_t *sfa;                   // [tiles][d/128][2][512] e8m0 scale blocks of the token tiles
+    size_t tiles;                   // tiles the scale region holds
+    float *out;                     // zeroed here: the down GEMM adds into it
+    int32_t *status, *abort;
+};
+
+// One warp per routed position p (perm order).  For each 32-element block of the token's
+// row (four lanes, eight elements each): 2^sa the smallest power of two that brings the
+// block's largest |x| to 448 or below, hi = rn(x / 2^sa); the residual r = x / 2^sa - hi
+// is exact in fp32; 2^sl likewise for max |r|, lo = rn(r / 2^sl).
+// Scale bytes sa + 127 and sa + sl + 127 go to the token tile's scale blocks (row m of the
+// tile at 16 (m % 32) + 4 (m / 32) + the block's index within its 128 columns).
+__global__ void __launch_bounds__(256) gemm_gather_mx_kernel(GatherMxArgs a)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int slots = a.T * a.k, nkc = a.d / 128;
+    const bool ok_off = *a.abort == 0;
+    const int n_units = *a.n_units;
+    for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < (size_t)a.T * (a.d / 4);
+         q += (size_t)gridDim.x * blockDim.x)
+        reinterpret_cast<float4 *>(a.out)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int lane = threadIdx.x & 31;
+    const int n_warps = (int)((gridDim.x * blockDim.x) >> 5);
+    for (int p = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); p < slots; p += n_warps) {
+        int s = a.perm[p];
+        if (lane == 0) {
+            bool bad = s < 0 || s >= slots;
+            if (!bad && ok_off) {
+                int lo = 0, hi = a.E;
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (a.offsets[mid] <= p) lo = mid; else hi = mid;
+                }
+                if (a.idx[s] != lo) bad = true;
+            }
+            if (bad) {
+                set_status(a.status, K3MOE_DEV_BAD_OFFSETS);
+                atomicOr(a.abort, 1);
+            }
+        }
+        s = dclamp(a.status, s, 0, slots - 1);
+        const int t = s / a.k;
+        // the routed unit holding p (units after the shared ones ascend in their first row)
+        int tile = -1, m = 0;
+        if (ok_off && n_units > a.S) {
+            int lo = a.S, hi = n_units;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (a.units[4 * mid + 2] <= p) lo = mid; else hi = mid;
+            }
+            const int l = p - a.units[4 * lo + 2];
+            if (l >= 0 && l < a.units[4 * lo + 3]) {
+                tile = a.prefix[lo] / a.rb + l / kBM;
+                m = l % kBM;
+            }
+            if (!dguard(a.status, tile >= 0 && (size_t)tile < a.tiles)) tile = -1;
+        }
+        const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.d);
+        uint2 *hr = reinterpret_cast<uint2 *>(a.hi + (size_t)p * a.d);
+        uint2 *lr = reinterpret_cast<uint2 *>(a.lo + (size_t)p * a.d);
+        for (int c0 = 0; c0 < a.d / 8; c0 += 32) {
+            const int c = c0 + lane;                       // 8-element chunk; block c / 4
+            const bool on = c < a.d / 8;                   // whole blocks are on or off (d % 128 == 0)
+            float v[8];
+            float mx = 0.0f;
+            {
+                const uint4 w = on ? xr[c] : make_uint4(0, 0, 0, 0);
+                const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int h = 0; h < 4; h++) {
+                    v[2 * h] = __uint_as_float(w4[h] << 16);
+                    v[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; j++) mx = fmaxf(mx, fabsf(v[j]));
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const int sa = mx > 0.0f ? max(pow2_over448(mx), -127) : 0;
+            const float inv_a = __uint_as_float((uint32_t)(127 - sa) << 23);    // 2^-sa, sa in [-127, 120]
+            uint32_t hw[4];
+            float rmx = 0.0f;
+#pragma unroll
+            for (int h = 0; h < 4; h++) {
+                const float a0 = v[2 * h] * inv_a, a1 = v[2 * h + 1] * inv_a;
+                hw[h] = e4m3x2_rn(a0, a1);
+                const float2 hf = e4m3x2_to_f32x2(hw[h]);
+                v[2 * h] = a0 - hf.x;                      // exact residuals
+                v[2 * h + 1] = a1 - hf.y;
+                rmx = fmaxf(rmx, fmaxf(fabsf(v[2 * h]), fabsf(v[2 * h + 1])));
+            }
+            rmx = fmaxf(rmx, __shfl_xor_sync(0xffffffffu, rmx, 1));
+            rmx = fmaxf(rmx, __shfl_xor_sync(0xffffffffu, rmx, 2));
+            // lo's scale 2^(sa + sl) must stay an e8m0 value, sa + sl in [-127, 127]; |r| <= 16
+            // (half the e4m3 step at 448), so sl <= -4 and 2^-sl is a normal float
+            const int sl = rmx > 0.0f ? min(max(pow2_over448(rmx), max(-127, -127 - sa)), 127 - sa) : 0;
+            const float inv_l = __uint_as_float((uint32_t)(127 - sl) << 23);
+            uint32_t lw[4];
+#pragma unroll
+            for (int h = 0; h < 4; h++) lw[h] = e4m3x2_rn(v[2 * h] * inv_l, v[2 * h + 1] * inv_l);
+            if (on) {
+                hr[c] = make_uint2(hw[0] | (hw[1] << 16), hw[2] | (hw[3] << 16));
+                lr[c] = make_uint2(lw[0] | (lw[1] << 16), lw[2] | (lw[3] << 16));
+                if ((lane & 3) == 0 && tile >= 0) {
+                    const int b = c >> 2, kc = b >> 2, kb = b & 3;
+                    uint8_t *sf = a.sfa + ((size_t)tile * nkc + kc) * 1024 + 16 * (m & 31) + 4 * (m >> 5) + kb;
+                    sf[0] = (uint8_t)(sa + 127);
+                    sf[512] = (uint8_t)(sa + sl + 127);
+                }
+            }
+        }
+    }
+}
+
+constexpr int kMxStg = 3;                              // stage ring
+constexpr int kMxBK = 128;                             // K per stage
+constexpr int kMxA = kBM * kMxBK;                      // one e4m3 token plane tile: 16 KB
+constexpr int kMxW = kWRows * kMxBK;                   // e2m1 weight tile (16 elements per 16 bytes): 32 KB
+constexpr int kMxSF = 4 * 512;                         // scale blocks: token hi, token lo, W1 rows, W3 rows
+constexpr int kMxStage = 2 * kMxA + kMxW + kMxSF;      // 67584 (a multiple of 1024)
+constexpr int kMxNumLd = 4, kMxNumEpi = 16;
+constexpr int kMxWarpProd = 0, kMxWarpMma = 1, kMxWarpLd0 = 2, kMxWarpEpi0 = 2 + kMxNumLd;
+constexpr int kMxThreads = (kMxWarpEpi0 + kMxNumEpi) * 32;     // 704
+constexpr int kMxSmem = kMxStg * kMxStage + 1024;
+constexpr uint32_t kMxSfCol = 256;                     // scale columns: 16 per stage slot after the accumulator
+static_assert(kMxStage % 1024 == 0, "stage slots keep the 1024-byte alignment of the swizzled tiles");
+static_assert(kMxSmem + 8 * 1024 <= 232448, "shared memory per block (dynamic + static)");
+static_assert(kMxSfCol + 16 * kMxStg <= 512, "tensor-memory columns");
+
+struct MxItem {
+    int id, tok0, ntok, rb, n0, ncols, tile;
+};
+// Item i of the routed gate/up items: unit, 128-row block of f, token tile; tile numbers
+// count the 128-row token tiles of all units in unit order.
+__device__ __forceinline__ MxItem mx_item(const GemmArgs &a, const int32_t *prefix, int n_units, int rbn, int i)
+{
+    int lo = 0, hi = n_units;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= i) lo = mid; else hi = mid;
+    }
+    const int4 u = *reinterpret_cast<const int4 *>(a.units + 4 * lo);
+    MxItem it;
+    it.id = dclamp(a.status, u.y, 0, a.E - 1);
+    dcheck(a.status, u.x == 0 && u.z >= 0 && u.w >= 0 && (size_t)u.z + u.w <= (size_t)a.T * a.k);
+    it.tok0 = u.z;
+    it.ntok = u.w;
+    const int ntiles = max(1, (it.ntok + kBM - 1) / kBM);
+    const int j = i - prefix[lo];
+    const int nt = j % ntiles;
+    it.rb = j / ntiles;
+    it.n0 = nt * kBM;
+    it.ncols = min(kBM, it.ntok - it.n0);
+    it.tile = prefix[lo] / rbn + nt;
+    return it;
+}
+
+// Roles (one block per SM):
+//   warp 0       producer: TMA of the two token planes' tiles (128 columns x 128 rows),
+//                a bulk copy of the tile's two scale blocks; the L2 prefetch of the
+//                packed weight tiles kL2Ahead stages ahead;
+//   warp 1       MMA: tcgen05.cp of the four scale blocks into tensor memory, then per
+//                32-wide K step the hi and the lo MMA (M=128 tokens, N=256 weight rows);
+//                one accumulator of 256 columns;
+//   warps 2-5    weight loaders: the packed W1 and W3 tiles of the stage from global
+//                memory, each row's 16-byte group re-ordered from the table's fragment
+//                order (byte permutes) into the MMA's row layout, and the rows' scale
+//                words into the scale-block layout (byte 255, read as zero, becomes 0:
+//                2^-127);
+//   warps 6-21   epilogue: four warps per lane quadrant, 32 columns of g and of u each;
+//                the accumulator is read into registers and released before SiTU.
+__global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_constant__ GemmArgs a, int item_lo,
+                                                                const __grid_constant__ CUtensorMap mhi,
+                                                                const __grid_constant__ CUtensorMap mlo)
+{
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ __align__(1024) uint8_t gsm_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t full[kMxStg], empty[kMxStg], acc_full, acc_empty, drain;
+    __shared__ uint32_t tmem_base;
+    __shared__ int bail;
+    __shared__ int32_t s_prefix[kMaxExperts + kMaxShared + 1];
+
+    if (*a.abort) return;
+    const int n_units = *a.n_units;
+    const int n_items = a.prefix[n_units];
+    if (item_lo + (int)blockIdx.x >= n_items) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nkc = a.d / kMxBK, rbn = a.f / kTileRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMxStg; s++) { mb_init(&full[s], 1 + kMxNumLd); mb_init(&empty[s], 1); }
+        mb_init(&acc_full, 1);
+        mb_init(&acc_empty, kMxNumEpi);
+        mb_init(&drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        bail = 0;
+    }
+    for (int u = threadIdx.x; u <= n_units; u += blockDim.x) s_prefix[u] = a.prefix[u];
+    if (warp == kMxWarpMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tmem_base)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    auto timeout = [&]() {
+        set_status(a.status, K3MOE_DEV_TIMEOUT);
+        bail = 1;
+    };
+    auto stop = [&]() -> bool { return __shfl_sync(0xffffffffu, bail, 0) != 0; };
+    const int i0 = item_lo + (int)blockIdx.x;
+    // packed tile pair (W1, W3) of (item, K stage)
+    auto wtile = [&](const MxItem &it, int kc) -> const uint8_t * {
+        return a.table + (size_t)it.id * a.expert_bytes + ((size_t)it.rb * nkc + kc) * 2 * kTileBytes;
+    };
+
+    if (warp == kMxWarpProd) {
+        // ------------------------------------------------------------ token planes and their scales
+        uint32_t st = 0;
+        bool failed = false;
+        int pf_i = i0, pf_kc = 0;
+        MxItem pf{};
+        auto pf_step = [&]() {
+            if (pf_i >= n_items) return;
+            if (pf_kc == 0) pf = mx_item(a, s_prefix, n_units, rbn, pf_i);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(wtile(pf, pf_kc)), "r"(2 * kTileBytes)
+                         : "memory");
+            if (++pf_kc == nkc) { pf_kc = 0; pf_i += gridDim.x; }
+        };
+        if (lane == 0)
+            for (int j = 0; j < kL2Ahead; j++) pf_step();
+        for (int i = i0; i < n_items && !failed && !stop(); i += gridDim.x) {
+            const MxItem it = mx_item(a, s_prefix, n_units, rbn, i);
+            const int row0 = it.tok0 + it.n0;
+            for (int kc = 0; kc < nkc; kc++, st++) {
+                if (st >= (uint32_t)kMxStg && !mb_wait_warp(&empty[st % kMxStg], ((st / kMxStg) - 1) & 1u)) {
+                    timeout();
+                    failed = true;
+                    break;
+                }
+                if (lane == 0) {
+                    pf_step();
+                    uint8_t *sb = sm + (st % kMxStg) * kMxStage;
+                    uint64_t *fb = &full[st % kMxStg];
+                    mb_expect_tx(fb, 2u * kMxA + 1024u);
+                    tma2d(sb, &mhi, kc * kMxBK, row0, fb);
+                    tma2d(sb + kMxA, &mlo, kc * kMxBK, row0, fb);
+                    bulk_g2s(sb + 2 * kMxA + kMxW, a.sfa + ((size_t)it.tile * nkc + kc) * 1024, 1024u, fb);
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0 && bail)
+            for (uint32_t f = st > (uint32_t)kMxStg ? st - kMxStg : 0; f < st; f++)
+                mb_wait(&full[f % kMxStg], (f / kMxStg) & 1u);
+        __syncwarp();
+    } else if (warp == kMxWarpMma) {
+        // ------------------------------------------------------------ scales to tensor memory, MMAs
+        uint32_t st = 0, n = 0;
+        bool failed = false;
+        for (int i = i0; i < n_items && !failed && !stop(); i += gridDim.x, n++) {
+            if (n >= 1 && !mb_wait_warp(&acc_empty, (n - 1) & 1u)) { timeout(); break; }
+            tc_fence_after();
+            for (int kc = 0; kc < nkc; kc++, st++) {
+                if (!mb_wait_warp(&full[st % kMxStg], (st / kMxStg) & 1u)) {
+                    timeout();
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    uint8_t *sb = sm + (st % kMxStg) * kMxStage;
+                    uint8_t *sf = sb + 2 * kMxA + kMxW;
+                    const uint32_t sft = tmem + kMxSfCol + 16u * (st % kMxStg);
+                    tc_cp_sf(sft, sdesc_sf(saddr(sf)));                // token hi
+                    tc_cp_sf(sft + 4, sdesc_sf(saddr(sf + 512)));      // token lo
+                    tc_cp_sf(sft + 8, sdesc_sf(saddr(sf + 1024)));     // W1 rows (N 0..127)
+                    tc_cp_sf(sft + 12, sdesc_sf(saddr(sf + 1536)));    // W3 rows (N 128..255)
+                    const uint64_t dh = sdesc(saddr(sb)), dl = sdesc(saddr(sb + kMxA)),
+                                   dw = sdesc(saddr(sb + 2 * kMxA));
+#pragma unroll
+                    for (int kb = 0; kb < kMxBK / 32; kb++) {
+                        const uint32_t id = idesc_mx(kWRows, kb, kb);
+                        umma_mx(tmem, dh + 2 * kb, dw + 2 * kb, id, sft, sft + 8, (kc | kb) != 0);
+                        umma_mx(tmem, dl + 2 * kb, dw + 2 * kb, id, sft + 4, sft + 8, 1u);
+                    }
+                    umma_commit(&empty[st % kMxStg]);
+                }
+                __syncwarp();
+            }
+            if (failed) break;
+            if (lane == 0) umma_commit(&acc_full);
+            __syncwarp();
+        }
+        if (lane == 0) {
+            umma_commit(&drain);
+            mb_wait(&drain, 0);
+        }
+        __syncwarp();
+    } else if (warp < kMxWarpEpi0) {
+        // ------------------------------------------------------------ weight loaders
+        // Thread l: quad tasks j = l + 128 q (q < 4): matrix j >> 8, block (strip, group)
+        // (j & 255) >> 3 of the tile, quad g = j & 7 (rows g and g + 8 of the strip: 32
+        // contiguous table bytes); scale rows l of W1 and of W3.
+        const int l = threadIdx.x - kMxWarpLd0 * 32;
+        uint32_t st = 0;
+        bool failed = false;
+        uint4 v[4][2];
+        uint32_t sw[2];
+        auto load = [&](const MxItem &it, int kc) {
+            const uint8_t *tp = wtile(it, kc);
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int j = l + 128 * q;
+                const uint8_t *src = tp + (j >> 8) * kTileBytes + (size_t)(j & 255) * 32;
+                v[q][0] = __ldg(reinterpret_cast<const uint4 *>(src));
+                v[q][1] = __ldg(reinterpret_cast<const uint4 *>(src + 16));
+            }
+#pragma unroll
+            for (int mm = 0; mm < 2; mm++)
+                sw[mm] = __ldg(reinterpret_cast<const uint32_t *>(tp + mm * kTileBytes + kTileNibbleBytes + 4 * l));
+        };
+        int ci = i0, ckc = 0;
+        MxItem cit{};
+        if (ci < n_items) { cit = mx_item(a, s_prefix, n_units, rbn, ci); load(cit, 0); }
+        while (ci < n_items && !failed && !stop()) {
+            if (st >= (uint32_t)kMxStg && !mb_wait_warp(&empty[st % kMxStg], ((st / kMxStg) - 1) & 1u)) {
+                timeout();
+                failed = true;
+                break;
+            }
+            uint8_t *sb = sm + (st % kMxStg) * kMxStage;
+            uint8_t *W = sb + 2 * kMxA;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int j = l + 128 * q;
+                const int blk = (j & 255) >> 3, g = j & 7, c = blk & 3;
+                const int ra = (j >> 8) * 128 + 16 * (blk >> 2) + g;      // B rows ra and ra + 8
+#pragma unroll
+                for (int hr = 0; hr < 2; hr++) {
+                    const int row = ra + 8 * hr;
+                    const uint32_t x0 = hr ? v[q][0].y : v[q][0].x, z0 = hr ? v[q][0].w : v[q][0].z;
+                    const uint32_t x1 = hr ? v[q][1].y : v[q][1].x, z1 = hr ? v[q][1].w : v[q][1].z;
+                    // group bytes 0..7 (chunk 2c) and 8..15 (chunk 2c + 1) of the row
+                    const uint32_t pa = __byte_perm(x0, z0, 0x5140), pb = __byte_perm(x1, z1, 0x5140);
+                    const uint32_t qa = __byte_perm(x0, z0, 0x7362), qb = __byte_perm(x1, z1, 0x7362);
+                    const int q0 = 2 * c, q1 = 2 * c + 1;
+                    *reinterpret_cast<uint2 *>(W + row * 128 + ((q0 ^ (row & 7)) << 4)) =
+                        make_uint2(__byte_perm(pa, pb, 0x5410), __byte_perm(pa, pb, 0x7632));
+                    *reinterpret_cast<uint2 *>(W + row * 128 + ((q1 ^ (row & 7)) << 4)) =
+                        make_uint2(__byte_perm(qa, qb, 0x5410), __byte_perm(qa, qb, 0x7632));
+                }
+            }
+            uint8_t *sfb = sb + 2 * kMxA + kMxW + 1024;
+#pragma unroll
+            for (int mm = 0; mm < 2; mm++) {
+                const uint32_t w = sw[mm] & ~__vcmpeq4(sw[mm], 0xFFFFFFFFu);
+                *reinterpret_cast<uint32_t *>(sfb + mm * 512 + 16 * (l & 31) + 4 * (l >> 5)) = w;
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mb_arrive(&full[st % kMxStg]);
+            st++;
+            if (++ckc == nkc) {
+                ckc = 0;
+                ci += gridDim.x;
+                if (ci < n_items) cit = mx_item(a, s_prefix, n_units, rbn, ci);
+            }
+            if (ci < n_items) load(cit, ckc);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                                 // TMEM lane quadrant
+        const int part = (warp - kMxWarpEpi0) >> 2;             // columns 32 part .. of g and of u
+        const int tr = 32 * q + lane;
+        uint32_t n = 0;
+        for (int i = i0; i < n_items && !stop(); i += gridDim.x, n++) {
+            const MxItem it = mx_item(a, s_prefix, n_units, rbn, i);
+            const bool valid = tr < it.ncols;
+            if (!mb_wait_warp(&acc_full, n & 1u)) { timeout(); break; }
+            tc_fence_after();
+            const uint32_t la = tmem + ((uint32_t)(32 * q) << 16) + 32u * part;
+            uint32_t g0[16], g1[16], u0[16], u1[16];
+            tmem_ld16_nowait(la, g0);
+            tmem_ld16_nowait(la + 16, g1);
+            tmem_ld16_nowait(la + kTileRows, u0);
+            tmem_ld16_nowait(la + kTileRows + 16, u1);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mb_arrive(&acc_empty);
+            uint32_t pk[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 2) {
+                const __half2 h0 = __floats2half2_rn(situ(__uint_as_float(g0[jj]), __uint_as_float(u0[jj]), a.b1, a.b2),
+                                                     situ(__uint_as_float(g0[jj + 1]), __uint_as_float(u0[jj + 1]), a.b1, a.b2));
+                const __half2 h1 = __floats2half2_rn(situ(__uint_as_float(g1[jj]), __uint_as_float(u1[jj]), a.b1, a.b2),
+                                                     situ(__uint_as_float(g1[jj + 1]), __uint_as_float(u1[jj + 1]), a.b1, a.b2));
+                pk[jj / 2] = *reinterpret_cast<const uint32_t *>(&h0);
+                pk[8 + jj / 2] = *reinterpret_cast<const uint32_t *>(&h1);
+            }
+            if (valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(a.hp + (size_t)(it.tok0 + it.n0 + tr) * a.f +
+                                                       it.rb * kTileRows + 32 * part);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; c4++)
+                    dst[c4] = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMxWarpMma) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
 // ---------------------------------------------------------------------------------- host
 template <int MODE>
 cudaError_t launch_gemm(const GemmArgs &ga, const CUtensorMap &mbr, const CUtensorMap &mbs,
@@ -697,6 +1162,23 @@ cudaError_t launch_gemm(const GemmArgs &ga, const CUtensorMap &mbr, const CUtens
                                        mbs, ma1, ma3);
     count_launch();
     timing_end(name, s);
+    return err;
+}
+
+cudaError_t launch_gemm_mx(const GemmArgs &ga, int item_lo, const CUtensorMap &mhi, const CUtensorMap &mlo,
+                           int max_items, cudaStream_t s)
+{
+    static bool set = false;
+    if (!set) {
+        cudaFuncSetAttribute(gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
+        set = true;
+    }
+    const int grid = max(1, min(num_sms(), max_items));
+    timing_begin("gemm_gateup_mx", s);
+    const cudaError_t err =
+        launch_pdl(gemm_mx_kernel, dim3(grid), dim3(kMxThreads), kMxSmem, s, ga, item_lo, mhi, mlo);
+    count_launch();
+    timing_end("gemm_gateup_mx", s);
     return err;
 }
 
@@ -729,13 +1211,17 @@ cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x,
     count_launch();
     timing_end("gemm_units", s);
     if (err != cudaSuccess) return err;
-    timing_begin("gemm_scales", s);
-    err = launch_pdl(gemm_scales_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, s, T, c.d, x, tok_scale);
-    count_launch();
-    timing_end("gemm_scales", s);
-    if (err != cudaSuccess) return err;
-    GatherArgs gta{T, c.d, k, E, x, idx, offsets, perm, tok_scale, xg, out, status, abort};
-    {
+    // the routed gate/up projection on the block-scaled MMAs: the tokens as two e4m3
+    // planes in xg's bytes, their scale blocks per token tile
+    const bool mx = prefill_gemm_block_scaled(c, T);
+    uint8_t *xhi = reinterpret_cast<uint8_t *>(xg), *xlo = xhi + (size_t)T * k * c.d;
+    if (!mx) {
+        timing_begin("gemm_scales", s);
+        err = launch_pdl(gemm_scales_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, s, T, c.d, x, tok_scale);
+        count_launch();
+        timing_end("gemm_scales", s);
+        if (err != cudaSuccess) return err;
+        GatherArgs gta{T, c.d, k, E, x, idx, offsets, perm, tok_scale, xg, out, status, abort};
         const size_t work = (size_t)T * k * (c.d / 8);
         int grid = (int)std::min<size_t>((work + 255) / 256, (size_t)num_sms() * 16);
         timing_begin("gemm_gather", s);
@@ -743,10 +1229,22 @@ cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x,
         count_launch();
         timing_end("gemm_gather", s);
         if (err != cudaSuccess) return err;
+    } else {
+        GatherMxArgs gmx{T, c.d, k, E, S, c.f / kTileRows, x, idx, offsets, perm, units, prefix_gu, n_units,
+                         xhi, xlo, ws + L.sfa, gemm_token_tiles(c, T), out, status, abort};
+        const size_t warps = (size_t)T * k;
+        int grid = (int)std::min<size_t>((warps * 32 + 255) / 256, (size_t)num_sms() * 16);
+        timing_begin("gemm_gather_mx", s);
+        err = launch_pdl(gemm_gather_mx_kernel, dim3(std::max(grid, 1)), dim3(256), 0, s, gmx);
+        count_launch();
+        timing_end("gemm_gather_mx", s);
+        if (err != cudaSuccess) return err;
     }
 
-    CUtensorMap mb_routed{}, mb_shared{}, ma1{}, ma3{}, mb_h{}, ma2{};
-    bool ok = map16(&mb_routed, xg, (uint64_t)T * k, c.d, kBM) && map16(&mb_h, hp, rows_all, c.f, kBM);
+    CUtensorMap mb_routed{}, mb_shared{}, ma1{}, ma3{}, mb_h{}, ma2{}, mhi{}, mlo{};
+    bool ok = map16(&mb_h, hp, rows_all, c.f, kBM);
+    if (mx) ok = ok && map8(&mhi, xhi, (uint64_t)T * k, c.d, kBM) && map8(&mlo, xlo, (uint64_t)T * k, c.d, kBM);
+    else ok = ok && map16(&mb_routed, xg, (uint64_t)T * k, c.d, kBM);
     if (S > 0)
         ok = ok && map16(&mb_shared, x, (uint64_t)T, c.d, kBM) &&
              map16(&ma1, sh_w1, (uint64_t)S * c.f, c.d, kBM) && map16(&ma3, sh_w3, (uint64_t)S * c.f, c.d, kBM) &&
@@ -754,11 +1252,26 @@ cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x,
     if (!ok) return cudaErrorInvalidValue;
 
     GemmArgs ga{T, c.d, c.f, k, S, E, c.situ_b1, c.situ_b2, units, prefix_gu, n_units, perm, weight,
-                tok_scale, table, expert_bytes(c.d, c.f), gateup_block_bytes(c.d, c.f), hp, out, abort, status};
+                tok_scale, table, expert_bytes(c.d, c.f), gateup_block_bytes(c.d, c.f), hp, out, abort, status,
+                INT_MAX, ws + L.sfa};
     // an upper bound on the items: every slot its own expert
     const int max_tiles = (int)std::min<long long>((long long)T * k + (long long)(E + S), (long long)1 << 30);
-    err = launch_gemm<kGU>(ga, mb_routed, mb_shared, ma1, ma3, max_tiles * (c.f / kTileRows), s, "gemm_gateup");
-    if (err != cudaSuccess) return err;
+    if (!mx) {
+        err = launch_gemm<kGU>(ga, mb_routed, mb_shared, ma1, ma3, max_tiles * (c.f / kTileRows), s, "gemm_gateup");
+        if (err != cudaSuccess) return err;
+    } else {
+        // the shared experts' items (the first S ceil(T/128) rb of the gate/up items) on the
+        // f16 kernel, then the routed ones on the block-scaled kernel
+        const int shared_items = S * ((T + kBM - 1) / kBM) * (c.f / kTileRows);
+        if (S > 0) {
+            GemmArgs gs = ga;
+            gs.item_hi = shared_items;
+            err = launch_gemm<kGU>(gs, mb_shared, mb_shared, ma1, ma3, shared_items, s, "gemm_gateup");
+            if (err != cudaSuccess) return err;
+        }
+        err = launch_gemm_mx(ga, shared_items, mhi, mlo, max_tiles * (c.f / kTileRows), s);
+        if (err != cudaSuccess) return err;
+    }
     GemmArgs gd = ga;
     gd.prefix = prefix_dn;
     err = launch_gemm<kDN>(gd, mb_h, mb_h, ma2, ma2, max_tiles * ((c.d / kTileRows + 1) / 2), s, "gemm_down");

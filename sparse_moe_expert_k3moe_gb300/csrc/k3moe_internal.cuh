@@ -135,6 +135,7 @@ struct WsLayout {
     size_t gush;                 // decode: shared gate/up partials [parts][S][T][2][f] f32
     size_t xg;                   // prefill: routed activations in perm order [T*k][d] f16
     size_t units;                // prefill: unit list [E+S][4], item prefixes, unit count
+    size_t sfa;                  // prefill, block-scaled GEMM: token tiles' e8m0 scales [tiles][d/128][2][512]
     size_t total;
     bool gemm;                   // which forward path this T takes
     int n_chunks;
@@ -156,6 +157,22 @@ __host__ __device__ inline int shared_kparts(int ktiles, int T)
     if (T > 1) return 1;
     return ktiles % 4 == 0 ? 4 : (ktiles % 2 == 0 ? 2 : 1);
 }
+
+// Token tiles of 128 rows over the prefill units (shared experts' first, as the GEMMs
+// number them): each unit needs ceil(rows / 128), so at most S ceil(T / 128) for the
+// shared units plus T k / 128 + (one partial tile per active expert) for the routed ones.
+inline size_t gemm_token_tiles(const k3moe_config &c, int T)
+{
+    const size_t slots = (size_t)T * c.top_k;
+    return (size_t)c.n_shared * (((size_t)T + 127) / 128) + (slots + 127) / 128 +
+           std::min(slots, (size_t)c.n_experts);
+}
+
+// Which kernel the prefill gate/up projection of the routed experts uses (a process-wide
+// choice, k3moe_set_prefill_gemm): 1 the f16 GEMM on dequantised weights, 2 the
+// block-scaled GEMM on the packed MXFP4 weights, 0 the default (prefill_gemm_choice).
+int prefill_gemm_setting();
+bool prefill_gemm_block_scaled(const k3moe_config &c, int T);
 
 inline WsLayout ws_layout(const k3moe_config &c, int T)
 {
@@ -187,6 +204,7 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     L.gush = o; o = align256(o + (L.gemm || pgu == 1 ? 0 : pgu * S * (size_t)T * 2 * c.f * 4));
     L.xg = o; o = align256(o + (L.gemm ? slots * (size_t)c.d * 2 : 0));
     L.units = o; o = align256(o + (L.gemm ? (4 * (E + S) + 2 * (E + S + 1) + 1) * 4 : 0));
+    L.sfa = o; o = align256(o + (L.gemm ? gemm_token_tiles(c, T) * (size_t)(c.d / 128) * 1024 : 0));
     L.total = o;
     return L;
 }

@@ -110,6 +110,46 @@ __device__ __forceinline__ void umma(uint32_t dtmem, uint64_t a, uint64_t b, uin
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
         "l"(a), "l"(b), "r"(id), "r"(acc));
 }
+// ---- block-scaled MMA (kind::mxf8f6f4): A e4m3, B e2m1, one ue8m0 scale per 32 K
+// elements of every A row and B row, read by the tensor core from tensor memory.
+// Operand layouts, as measured on sm_103a: K-major, 128-byte swizzle like the f16 tiles,
+// an e4m3 row of 128 elements is 128 bytes; an e2m1 row keeps 16 elements per 16-byte
+// chunk, their 8 packed bytes (low nibble = even element) first and 8 bytes that are not
+// read.  Scales: a 512-byte shared-memory block per 128 rows and 4 K blocks, row m's 4
+// bytes at 16 (m % 32) + 4 (m / 32); tcgen05.cp 32x128b.warpx4 puts them in tensor
+// memory as 4 columns (row m in column m / 32 of lane m % 32, every lane quadrant a
+// copy); the instruction descriptor's scale ids pick the byte, i.e. the K block.
+// Instruction descriptor: fp32 D, A e4m3 (0), B e2m1 (5), both K-major, N = n, M = 128,
+// ue8m0 scales, scale ids sfa (A) and sfb (B).
+__device__ __forceinline__ uint32_t idesc_mx(int n, int sfa, int sfb)
+{
+    return ((uint32_t)sfb << 4) | (0u << 7) | (5u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(128 >> 7) << 27) | ((uint32_t)sfa << 29);
+}
+__device__ __forceinline__ void umma_mx(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t id, uint32_t sfa_tmem,
+                                        uint32_t sfb_tmem, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            dtmem),
+        "l"(a), "l"(b), "r"(id), "r"(sfa_tmem), "r"(sfb_tmem), "r"(acc));
+}
+// Shared-memory descriptor of a contiguous 512-byte scale block (no swizzle, 8-row groups
+// of 16-byte rows 128 bytes apart) for tcgen05.cp.
+__device__ __forceinline__ uint64_t sdesc_sf(uint32_t addr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(128u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    return d;
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc));
+}
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -128,6 +168,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 #pragma unroll
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
+// The same load without the wait: several loads in flight, then one tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -171,6 +221,20 @@ inline bool map16(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols
     Entry &e = cache[n_cache < 64 ? n_cache++ : (next++ % 64)];
     e.base = base; e.rows = rows; e.cols = cols; e.br = box_rows; e.map = *m;
     return true;
+}
+
+// 8-bit matrix [rows][cols]: boxes of 128 columns x box_rows rows, 128-byte swizzle.
+inline bool map8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {128u, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 inline int num_sms()

@@ -76,7 +76,24 @@ def test_sizes(k3):
     assert w1 < 1 * MiB
     assert k3.k3moe_workspace_bytes(cfg, 447) <= 211 * MiB
     assert k3.k3moe_workspace_bytes(cfg, 448) == k3.k3moe_workspace_bytes(cfg, 447)
-    assert k3.k3moe_workspace_bytes(cfg, 4096) <= 910 * MiB
+    assert k3.k3moe_workspace_bytes(cfg, 4096) <= 950 * MiB
+
+
+def test_prefill_gemm_switch(k3):
+    """The process-wide choice of the prefill gate/up kernel: 0 (default), 1 (f16 on
+    dequantised weights), 2 (block-scaled); anything else is refused and changes nothing."""
+    assert k3.k3moe_get_prefill_gemm() == 0
+    try:
+        for v in (2, 1, 0):
+            k3.k3moe_set_prefill_gemm(v)
+            assert k3.k3moe_get_prefill_gemm() == v
+        k3.k3moe_set_prefill_gemm(2)
+        for bad in (-1, 3):
+            with pytest.raises(k3.K3MoEError):
+                k3.k3moe_set_prefill_gemm(bad)
+            assert k3.k3moe_get_prefill_gemm() == 2
+    finally:
+        k3.k3moe_set_prefill_gemm(0)
 
 
 def test_host_validation_rejects_before_launch(k3):
