@@ -59,6 +59,8 @@ def parse():
     p.add_argument("--cpu-budget-s", type=float, default=15.0)
     p.add_argument("--graph", action="store_true",
                    help="replay route + forward as one captured CUDA graph per step")
+    p.add_argument("--prefill-gemm", default="default", choices=["default", "f16", "block_scaled"],
+                   help="kernel of the prefill path's routed projections (k3moe_set_prefill_gemm)")
     return p.parse_args()
 
 
@@ -141,12 +143,12 @@ def full_kernel_work(name: str, w, distinct_experts: int):
         return H * SI * 2 + T * SI * 2 + 2 * T * H * 4, 2 * T * H * SI
     if name in ("router_scores", "router_logits_tc", "router_wnorm"):
         return kernel_work(name, w.with_(d=H, hidden=0), distinct_experts)
-    if name in ("gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down"):
+    if name in ("gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "gemm_gateup_mx"):
         return kernel_work(name, w.with_(S=0, hidden=0), distinct_experts)
     return block_bytes_flops(w, distinct_experts)[0], 0
 
 
-def kernel_work(name: str, w, distinct_experts: int):
+def kernel_work(name: str, w, distinct_experts: int, block_scaled: bool = False):
     """Algorithmic (bytes, FLOPs) of one launch of a forward kernel: the bytes it must
     move and the multiply-adds (x2) it must do.
     router_scores: Wr and x in, sc and ch out (f32); router_logits_tc: Wr and x in, the
@@ -162,6 +164,14 @@ def kernel_work(name: str, w, distinct_experts: int):
     rows = w.T * w.k + w.S * w.T
     slots = w.T * w.k
     h_gemv = slots * w.f * 2 + w.S * w.T * w.f * 4
+    if name == "gemm_gateup_mx":
+        # routed rows only: the packed W1, W3 (codes and scales as they are), the two e4m3
+        # token planes and their scale bytes in, h (f16) out
+        return (distinct_experts * 2 * w.f * w.d * 17 // 32 + slots * w.d * 2 + slots * w.d // 16
+                + slots * w.f * 2), 2 * slots * 2 * w.f * w.d
+    if name == "gemm_gateup" and block_scaled:
+        # beside the block-scaled kernel, the f16 kernel runs the shared experts alone
+        return (w.S * 2 * w.f * w.d * 2 + w.T * w.d * 2 + w.S * w.T * w.f * 2), 2 * w.S * w.T * 2 * w.f * w.d
     if name == "router_scores":
         return w.E * w.d * 2 + w.T * w.d * 2 + 2 * w.T * w.E * 4, 2 * w.T * w.E * w.d
     if name == "router_logits_tc":
@@ -394,7 +404,10 @@ def reference_arm(args):
 ARITHMETIC = ("router: exact logits (bf16 products exact in fp32, two-sum compensated "
               "accumulation, one rounding), sigmoid from a correctly rounded float exp (fp32 double-float arithmetic); experts: "
               "MMA operands f16 (tokens x*2^-u, routed h; MXFP4 weights decoded exactly to f16) "
-              "and bf16 (shared-expert weights, shared h), fp32 accumulation; output f32")
+              "and bf16 (shared-expert weights, shared h), fp32 accumulation; on the prefill path "
+              "the routed gate/up projection by default on block-scaled MMAs (kind::mxf8f6f4: the "
+              "E2M1 codes with their E8M0 scales as packed, the tokens as two e4m3 planes with "
+              "E8M0 scales per 32, fp32 accumulation); output f32")
 
 
 def near_tie_counts(layer, x, w):
@@ -421,6 +434,8 @@ def measure(w, args, rank, world, local, dev):
     from k3moe_inputs.device import build_layer
     import sparse_moe_expert_k3moe_gb300 as k3
 
+    k3.k3moe_set_prefill_gemm({"default": k3.PREFILL_GEMM_DEFAULT, "f16": k3.PREFILL_GEMM_F16,
+                               "block_scaled": k3.PREFILL_GEMM_BLOCK_SCALED}[args.prefill_gemm])
     width = w.hidden or w.d                                   # token width in and out
     if w.hidden:
         from k3moe_inputs.device import build_block
@@ -497,14 +512,25 @@ def measure(w, args, rank, world, local, dev):
     top_name, (top_n, top_ms) = max(kt.items(), key=lambda kv: kv[1][1])
     hbm, bf16, bf16_sus, src = peaks()
     per_launch_s = top_ms / top_n / 1000.0
-    alg_b, alg_f = kernel_work(top_name, w, distinct)
+    block_scaled = "gemm_gateup_mx" in kt
+    alg_b, alg_f = kernel_work(top_name, w, distinct, block_scaled)
     # the kernel's bound: whichever of HBM and the tensor cores its algorithmic work needs
     # longer on.  The per-kernel pass times launches of at most milliseconds, so the tensor
-    # peak is the burst figure (the sustained one is for seconds-long loops).
-    if alg_f / (bf16 * 1e12) > alg_b / (hbm * 1e9):
-        roof = {"bound": "tensor", "achieved": alg_f / per_launch_s / 1e12, "peak": bf16,
-                "unit": "TFLOP/s", "peak_kind": "bf16 dense, burst (f16 runs at the same rate)"}
-        roof["frac_of_sustained"] = roof["achieved"] / bf16_sus
+    # peak is the burst figure (the sustained one is for seconds-long loops).  The
+    # block-scaled GEMM's MMAs (kind::mxf8f6f4: e4m3 x e2m1) take the FP8 peak: the measured
+    # bf16 burst figure times the nominal FP8/BF16 ratio (4.5 / 2.25 PFLOP/s).
+    fp8 = top_name == "gemm_gateup_mx"
+    tpeak = bf16 * (2.0 if fp8 else 1.0)
+    if alg_f / (tpeak * 1e12) > alg_b / (hbm * 1e9):
+        roof = {"bound": "tensor", "achieved": alg_f / per_launch_s / 1e12, "peak": tpeak,
+                "unit": "TFLOP/s",
+                "peak_kind": ("fp8 dense, burst: the measured bf16 burst x 2 (nominal fp8/bf16); the "
+                              "tokens are two e4m3 terms, so the MMAs execute twice the algorithmic "
+                              "FLOPs (at most 0.5 of this peak by construction)") if fp8
+                else "bf16 dense, burst (f16 runs at the same rate)"}
+        roof["frac_of_sustained"] = roof["achieved"] / (bf16_sus * (2.0 if fp8 else 1.0))
+        if fp8:
+            roof["frac_of_bf16_burst"] = roof["achieved"] / bf16
     else:
         roof = {"bound": "hbm", "achieved": alg_b / per_launch_s / 1e9, "peak": hbm, "unit": "GB/s",
                 "peak_kind": "HBM copy"}
@@ -567,6 +593,9 @@ def measure(w, args, rank, world, local, dev):
                    "arithmetic": ARITHMETIC,
                    "l2": "512 MiB buffer written between timed steps",
                    "launch": "one CUDA graph replay per step" if args.graph else "eager",
+                   "prefill_gemm": ("block_scaled (routed gate/up on kind::mxf8f6f4)" if block_scaled
+                                    else ("f16 on dequantised weights" if "gemm_gateup" in kt
+                                          else "not used (mat-vec path)")),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": dict(roof, kernel=top_name, peak_source=src,
                          traffic=traffic_for(top_name, w.name), alg_bytes_per_launch=alg_b,

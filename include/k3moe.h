@@ -333,7 +333,7 @@ int32_t k3moe_build_flags(void);
  *      its 32-block's largest magnitude (smaller ones: absolute error below 2^-21 of
  *      that magnitude).  A scale byte of 255, which the format reads as zero, becomes
  *      2^-127 (a contribution below 2^-120 of the group's codes);
- *   0  the library's default, which is 1.
+ *   0  the library's default, which is 2.
  * The shared experts (bf16) and the down projection run on the f16 kernel either way.
  * Process-wide; takes effect at the next k3moe_forward call (a captured graph keeps
  * the kernels it recorded).  K3MOE_EINVAL for another value.  The workspace
