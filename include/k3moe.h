@@ -97,9 +97,13 @@ k3moe_status k3moe_validate_config(const k3moe_config *cfg);
 /* Bytes of the packed routed-expert table for cfg->n_experts experts: per expert
  * 3 * f * d * 17/32 bytes of codes and scales (half a byte per weight plus one
  * scale byte per 32: 17,547,264 bytes at the K3 shape, kimi-k3-in-c README,
- * Part II, "The problem: a model that does not fit"), plus a 1024-byte summary
- * of the largest scale of every 128-row block and a flag for scale bytes 0 and
- * 255 in the expert.  0 for an invalid config. */
+ * Part II, "The problem: a model that does not fit") in the tiles the mat-vecs and
+ * the f16 GEMM read, a 1024-byte summary of the largest scale of every 128-row
+ * block and a flag for scale bytes 0 and 255 in the expert, and the same codes and
+ * scales a second time (another 3 * f * d * 17/32 bytes) in the layouts the
+ * block-scaled prefill GEMM's tensor-map loads take: the codes row-major as the
+ * checkpoint has them, the scales in 512-byte blocks of 128 rows x 4 groups.  At
+ * the K3 shape 896 experts take 31.4 GB.  0 for an invalid config. */
 size_t k3moe_packed_bytes(const k3moe_config *cfg);
 
 /* Workspace bytes that k3moe_route and k3moe_forward need for any

@@ -842,9 +842,10 @@ constexpr int kMxA = kBM * kMxBK;                      // one e4m3 token plane t
 constexpr int kMxW = kWRows * kMxBK;                   // e2m1 weight tile (16 elements per 16 bytes): 32 KB
 constexpr int kMxSF = 4 * 512;                         // scale blocks: token hi, token lo, W1 rows, W3 rows
 constexpr int kMxStage = 2 * kMxA + kMxW + kMxSF;      // 67584 (a multiple of 1024)
-constexpr int kMxNumLd = 4, kMxNumEpi = 16;
-constexpr int kMxWarpProd = 0, kMxWarpMma = 1, kMxWarpLd0 = 2, kMxWarpEpi0 = 2 + kMxNumLd;
-constexpr int kMxThreads = (kMxWarpEpi0 + kMxNumEpi) * 32;     // 704
+constexpr int kMxNumEpi = 16;
+constexpr int kMxWarpProd = 0, kMxWarpMma = 1, kMxWarpEpi0 = 2;
+constexpr int kMxThreads = (kMxWarpEpi0 + kMxNumEpi) * 32;     // 576
+constexpr uint32_t kMxWBox = kTileRows * kMxBK / 2;   // packed bytes of one 128 x 128 weight box (the TMA's count)
 constexpr int kMxSmem = kMxStg * kMxStage + 1024;
 constexpr uint32_t kMxSfCol = 256;                     // scale columns: 16 per stage slot after the accumulator
 static_assert(kMxStage % 1024 == 0, "stage slots keep the 1024-byte alignment of the swizzled tiles");
@@ -880,22 +881,23 @@ __device__ __forceinline__ MxItem mx_item(const GemmArgs &a, const int32_t *pref
 }
 
 // Roles (one block per SM):
-//   warp 0       producer: TMA of the two token planes' tiles (128 columns x 128 rows),
-//                a bulk copy of the tile's two scale blocks; the L2 prefetch of the
-//                packed weight tiles kL2Ahead stages ahead;
+//   warp 0       producer, everything by TMA or bulk copy into the stage ring: the two
+//                token planes' tiles (128 columns x 128 rows), the tile's two token scale
+//                blocks, the W1 and W3 boxes (128 columns x 128 rows each) from the table's
+//                row-major codes with the packed-FP4 tensor-map type (each 16 codes land as
+//                8 bytes at the start of a 16-byte chunk: the MMA's e2m1 layout), and
+//                their two scale blocks; the L2 prefetch of the weight boxes kL2Ahead
+//                stages ahead;
 //   warp 1       MMA: tcgen05.cp of the four scale blocks into tensor memory, then per
 //                32-wide K step the hi and the lo MMA (M=128 tokens, N=256 weight rows);
 //                one accumulator of 256 columns;
-//   warps 2-5    weight loaders: the packed W1 and W3 tiles of the stage from global
-//                memory, each row's 16-byte group re-ordered from the table's fragment
-//                order (byte permutes) into the MMA's row layout, and the rows' scale
-//                words into the scale-block layout (byte 255, read as zero, becomes 0:
-//                2^-127);
-//   warps 6-21   epilogue: four warps per lane quadrant, 32 columns of g and of u each;
+//   warps 2-17   epilogue: four warps per lane quadrant, 32 columns of g and of u each;
 //                the accumulator is read into registers and released before SiTU.
 __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_constant__ GemmArgs a, int item_lo,
                                                                 const __grid_constant__ CUtensorMap mhi,
-                                                                const __grid_constant__ CUtensorMap mlo)
+                                                                const __grid_constant__ CUtensorMap mlo,
+                                                                const __grid_constant__ CUtensorMap mw1,
+                                                                const __grid_constant__ CUtensorMap mw3)
 {
     pdl_wait();
     pdl_trigger();
@@ -914,7 +916,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
     const int nkc = a.d / kMxBK, rbn = a.f / kTileRows;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kMxStg; s++) { mb_init(&full[s], 1 + kMxNumLd); mb_init(&empty[s], 1); }
+        for (int s = 0; s < kMxStg; s++) { mb_init(&full[s], 1); mb_init(&empty[s], 1); }
         mb_init(&acc_full, 1);
         mb_init(&acc_empty, kMxNumEpi);
         mb_init(&drain, 1);
@@ -937,13 +939,14 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
     };
     auto stop = [&]() -> bool { return __shfl_sync(0xffffffffu, bail, 0) != 0; };
     const int i0 = item_lo + (int)blockIdx.x;
-    // packed tile pair (W1, W3) of (item, K stage)
-    auto wtile = [&](const MxItem &it, int kc) -> const uint8_t * {
-        return a.table + (size_t)it.id * a.expert_bytes + ((size_t)it.rb * nkc + kc) * 2 * kTileBytes;
+    // the scale blocks (W1, W3) of (item, K stage) in the table's block-scaled section
+    const uint8_t *sfgu = a.table + mx_sfgu_offset(a.E, a.d, a.f);
+    auto wsf = [&](const MxItem &it, int kc) -> const uint8_t * {
+        return sfgu + (((size_t)it.id * rbn + it.rb) * nkc + kc) * 1024;
     };
 
     if (warp == kMxWarpProd) {
-        // ------------------------------------------------------------ token planes and their scales
+        // ------------------------------------------------------------ everything by TMA
         uint32_t st = 0;
         bool failed = false;
         int pf_i = i0, pf_kc = 0;
@@ -951,8 +954,11 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
         auto pf_step = [&]() {
             if (pf_i >= n_items) return;
             if (pf_kc == 0) pf = mx_item(a, s_prefix, n_units, rbn, pf_i);
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(wtile(pf, pf_kc)), "r"(2 * kTileBytes)
-                         : "memory");
+            const int wrow = pf.id * a.f + pf.rb * kTileRows;
+            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(&mw1),
+                         "r"(pf_kc * kMxBK), "r"(wrow) : "memory");
+            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(&mw3),
+                         "r"(pf_kc * kMxBK), "r"(wrow) : "memory");
             if (++pf_kc == nkc) { pf_kc = 0; pf_i += gridDim.x; }
         };
         if (lane == 0)
@@ -960,6 +966,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
         for (int i = i0; i < n_items && !failed && !stop(); i += gridDim.x) {
             const MxItem it = mx_item(a, s_prefix, n_units, rbn, i);
             const int row0 = it.tok0 + it.n0;
+            const int wrow = it.id * a.f + it.rb * kTileRows;
             for (int kc = 0; kc < nkc; kc++, st++) {
                 if (st >= (uint32_t)kMxStg && !mb_wait_warp(&empty[st % kMxStg], ((st / kMxStg) - 1) & 1u)) {
                     timeout();
@@ -970,10 +977,13 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
                     pf_step();
                     uint8_t *sb = sm + (st % kMxStg) * kMxStage;
                     uint64_t *fb = &full[st % kMxStg];
-                    mb_expect_tx(fb, 2u * kMxA + 1024u);
+                    mb_expect_tx(fb, 2u * kMxA + 2u * kMxWBox + 2048u);
                     tma2d(sb, &mhi, kc * kMxBK, row0, fb);
                     tma2d(sb + kMxA, &mlo, kc * kMxBK, row0, fb);
+                    tma2d(sb + 2 * kMxA, &mw1, kc * kMxBK, wrow, fb);
+                    tma2d(sb + 2 * kMxA + kMxW / 2, &mw3, kc * kMxBK, wrow, fb);
                     bulk_g2s(sb + 2 * kMxA + kMxW, a.sfa + ((size_t)it.tile * nkc + kc) * 1024, 1024u, fb);
+                    bulk_g2s(sb + 2 * kMxA + kMxW + 1024, wsf(it, kc), 1024u, fb);
                 }
                 __syncwarp();
             }
@@ -1025,77 +1035,6 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
             mb_wait(&drain, 0);
         }
         __syncwarp();
-    } else if (warp < kMxWarpEpi0) {
-        // ------------------------------------------------------------ weight loaders
-        // Thread l: quad tasks j = l + 128 q (q < 4): matrix j >> 8, block (strip, group)
-        // (j & 255) >> 3 of the tile, quad g = j & 7 (rows g and g + 8 of the strip: 32
-        // contiguous table bytes); scale rows l of W1 and of W3.
-        const int l = threadIdx.x - kMxWarpLd0 * 32;
-        uint32_t st = 0;
-        bool failed = false;
-        uint4 v[4][2];
-        uint32_t sw[2];
-        auto load = [&](const MxItem &it, int kc) {
-            const uint8_t *tp = wtile(it, kc);
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const int j = l + 128 * q;
-                const uint8_t *src = tp + (j >> 8) * kTileBytes + (size_t)(j & 255) * 32;
-                v[q][0] = __ldg(reinterpret_cast<const uint4 *>(src));
-                v[q][1] = __ldg(reinterpret_cast<const uint4 *>(src + 16));
-            }
-#pragma unroll
-            for (int mm = 0; mm < 2; mm++)
-                sw[mm] = __ldg(reinterpret_cast<const uint32_t *>(tp + mm * kTileBytes + kTileNibbleBytes + 4 * l));
-        };
-        int ci = i0, ckc = 0;
-        MxItem cit{};
-        if (ci < n_items) { cit = mx_item(a, s_prefix, n_units, rbn, ci); load(cit, 0); }
-        while (ci < n_items && !failed && !stop()) {
-            if (st >= (uint32_t)kMxStg && !mb_wait_warp(&empty[st % kMxStg], ((st / kMxStg) - 1) & 1u)) {
-                timeout();
-                failed = true;
-                break;
-            }
-            uint8_t *sb = sm + (st % kMxStg) * kMxStage;
-            uint8_t *W = sb + 2 * kMxA;
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const int j = l + 128 * q;
-                const int blk = (j & 255) >> 3, g = j & 7, c = blk & 3;
-                const int ra = (j >> 8) * 128 + 16 * (blk >> 2) + g;      // B rows ra and ra + 8
-#pragma unroll
-                for (int hr = 0; hr < 2; hr++) {
-                    const int row = ra + 8 * hr;
-                    const uint32_t x0 = hr ? v[q][0].y : v[q][0].x, z0 = hr ? v[q][0].w : v[q][0].z;
-                    const uint32_t x1 = hr ? v[q][1].y : v[q][1].x, z1 = hr ? v[q][1].w : v[q][1].z;
-                    // group bytes 0..7 (chunk 2c) and 8..15 (chunk 2c + 1) of the row
-                    const uint32_t pa = __byte_perm(x0, z0, 0x5140), pb = __byte_perm(x1, z1, 0x5140);
-                    const uint32_t qa = __byte_perm(x0, z0, 0x7362), qb = __byte_perm(x1, z1, 0x7362);
-                    const int q0 = 2 * c, q1 = 2 * c + 1;
-                    *reinterpret_cast<uint2 *>(W + row * 128 + ((q0 ^ (row & 7)) << 4)) =
-                        make_uint2(__byte_perm(pa, pb, 0x5410), __byte_perm(pa, pb, 0x7632));
-                    *reinterpret_cast<uint2 *>(W + row * 128 + ((q1 ^ (row & 7)) << 4)) =
-                        make_uint2(__byte_perm(qa, qb, 0x5410), __byte_perm(qa, qb, 0x7632));
-                }
-            }
-            uint8_t *sfb = sb + 2 * kMxA + kMxW + 1024;
-#pragma unroll
-            for (int mm = 0; mm < 2; mm++) {
-                const uint32_t w = sw[mm] & ~__vcmpeq4(sw[mm], 0xFFFFFFFFu);
-                *reinterpret_cast<uint32_t *>(sfb + mm * 512 + 16 * (l & 31) + 4 * (l >> 5)) = w;
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mb_arrive(&full[st % kMxStg]);
-            st++;
-            if (++ckc == nkc) {
-                ckc = 0;
-                ci += gridDim.x;
-                if (ci < n_items) cit = mx_item(a, s_prefix, n_units, rbn, ci);
-            }
-            if (ci < n_items) load(cit, ckc);
-        }
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                                 // TMEM lane quadrant
@@ -1166,7 +1105,7 @@ cudaError_t launch_gemm(const GemmArgs &ga, const CUtensorMap &mbr, const CUtens
 }
 
 cudaError_t launch_gemm_mx(const GemmArgs &ga, int item_lo, const CUtensorMap &mhi, const CUtensorMap &mlo,
-                           int max_items, cudaStream_t s)
+                           const CUtensorMap &mw1, const CUtensorMap &mw3, int max_items, cudaStream_t s)
 {
     static bool set = false;
     if (!set) {
@@ -1176,7 +1115,7 @@ cudaError_t launch_gemm_mx(const GemmArgs &ga, int item_lo, const CUtensorMap &m
     const int grid = max(1, min(num_sms(), max_items));
     timing_begin("gemm_gateup_mx", s);
     const cudaError_t err =
-        launch_pdl(gemm_mx_kernel, dim3(grid), dim3(kMxThreads), kMxSmem, s, ga, item_lo, mhi, mlo);
+        launch_pdl(gemm_mx_kernel, dim3(grid), dim3(kMxThreads), kMxSmem, s, ga, item_lo, mhi, mlo, mw1, mw3);
     count_launch();
     timing_end("gemm_gateup_mx", s);
     return err;
@@ -1269,7 +1208,11 @@ cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x,
             err = launch_gemm<kGU>(gs, mb_shared, mb_shared, ma1, ma3, shared_items, s, "gemm_gateup");
             if (err != cudaSuccess) return err;
         }
-        err = launch_gemm_mx(ga, shared_items, mhi, mlo, max_tiles * (c.f / kTileRows), s);
+        CUtensorMap mw1{}, mw3{};
+        if (!map4(&mw1, table + mx_w1_offset(E, c.d, c.f), (uint64_t)E * c.f, c.d) ||
+            !map4(&mw3, table + mx_w3_offset(E, c.d, c.f), (uint64_t)E * c.f, c.d))
+            return cudaErrorInvalidValue;
+        err = launch_gemm_mx(ga, shared_items, mhi, mlo, mw1, mw3, max_tiles * (c.f / kTileRows), s);
         if (err != cudaSuccess) return err;
     }
     GemmArgs gd = ga;

@@ -62,10 +62,37 @@ __host__ __device__ inline size_t expert_bytes(int d, int f)
 {
     return gateup_block_bytes(d, f) + down_block_bytes(d, f);
 }
-// Whole table: E payloads, then E trailers.
-__host__ __device__ inline size_t packed_table_bytes(int E, int d, int f)
+// After the trailers, the block-scaled section: the codes again in the checkpoint's own
+// row-major order, for tensor-map loads, and the scales in the tensor core's scale-block
+// order (the prefill block-scaled GEMM reads only this section):
+//   W1 [E*f][d/2], W3 [E*f][d/2], W2 [E*d][f/2] packed bytes (low nibble = even column);
+//   gate/up scale blocks [E][f/128][d/128][2: W1, W3][512], down [E][d/128][f/128][512]:
+//   a block covers rows 128 rb.. of one matrix and K columns 128 kc..; row r's 4 bytes
+//   (its 4 groups of 32) at 16 (r % 32) + 4 (r / 32); byte 255 (read as zero) stored as 0.
+__host__ __device__ inline size_t mx_w1_offset(int E, int d, int f)
 {
     return (size_t)E * (expert_bytes(d, f) + kTrailerBytes);
+}
+__host__ __device__ inline size_t mx_w3_offset(int E, int d, int f)
+{
+    return mx_w1_offset(E, d, f) + (size_t)E * f * d / 2;
+}
+__host__ __device__ inline size_t mx_w2_offset(int E, int d, int f)
+{
+    return mx_w3_offset(E, d, f) + (size_t)E * f * d / 2;
+}
+__host__ __device__ inline size_t mx_sfgu_offset(int E, int d, int f)
+{
+    return mx_w2_offset(E, d, f) + (size_t)E * d * f / 2;
+}
+__host__ __device__ inline size_t mx_sfdn_offset(int E, int d, int f)
+{
+    return mx_sfgu_offset(E, d, f) + (size_t)E * (f / kTileRows) * (d / kTileK) * 1024;
+}
+// Whole table: E payloads, E trailers, the block-scaled section.
+__host__ __device__ inline size_t packed_table_bytes(int E, int d, int f)
+{
+    return mx_sfdn_offset(E, d, f) + (size_t)E * (d / kTileRows) * (f / kTileK) * 512;
 }
 // Trailer word of (expert e, matrix m in {0: W1, 1: W3, 2: W2}, row block rb).
 __host__ __device__ inline size_t trailer_offset(int E, int d, int f, int e, int m, int rb)

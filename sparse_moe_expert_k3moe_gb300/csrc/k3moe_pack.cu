@@ -78,6 +78,19 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
         for (int t = 0; t < 4; t++)
             *reinterpret_cast<uint32_t *>(dst + dn + (size_t)t * 8) = lane_word(v, t);
         dst[ds] = sb;
+        // the block-scaled section: the group in row-major order, its scale in its block
+        {
+            const int ex = a.expert_lo + e;
+            const size_t rmo = (mat == 0 ? mx_w1_offset(a.E, a.d, a.f)
+                                         : (mat == 1 ? mx_w3_offset(a.E, a.d, a.f) : mx_w2_offset(a.E, a.d, a.f))) +
+                               ((size_t)ex * rows + row) * (cols / 2) + (size_t)grp * 16;
+            *reinterpret_cast<uint4 *>(a.table + rmo) = v;
+            const int rb = row / kTileRows, r = row % kTileRows, kc = grp / 4, kb = grp % 4;
+            const size_t so = mat < 2
+                ? mx_sfgu_offset(a.E, a.d, a.f) + ((((size_t)ex * (a.f / kTileRows) + rb) * (a.d / kTileK) + kc) * 2 + mat) * 512
+                : mx_sfdn_offset(a.E, a.d, a.f) + (((size_t)ex * (a.d / kTileRows) + rb) * (a.f / kTileK) + kc) * 512;
+            a.table[so + 16 * (r % 32) + 4 * (r / 32) + kb] = sb == 255 ? 0 : sb;
+        }
         if (sb == 0 || sb == 255)
             atomicOr(reinterpret_cast<unsigned int *>(
                          a.table + special_flag_offset(a.E, a.d, a.f, a.expert_lo + e)), 1u);

@@ -237,6 +237,24 @@ inline bool map8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Packed 4-bit matrix [rows][cols / 2 bytes] (low nibble = even column): boxes of 128
+// columns x 128 rows with the packed-FP4 type, which lands each 16 codes as 8 bytes at the
+// start of a 16-byte chunk (the e2m1 operand layout of the block-scaled MMA), 128-byte
+// swizzle.  The box's transaction count is its packed size, 8192 bytes (measured).  Needs
+// cols % 128 == 0, a 32-byte aligned base and a row stride that is a multiple of 32.
+inline bool map4(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn || cols % 128 != 0 || (cols / 2) % 32 != 0 || reinterpret_cast<uintptr_t>(base) % 32 != 0) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols / 2};
+    const cuuint32_t box[2] = {128u, 128u};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline int num_sms()
 {
     static int n = 0;

@@ -60,9 +60,9 @@ def test_config_validation(k3):
 
 def test_sizes(k3):
     cfg = k3_cfg(k3)
-    assert k3.k3moe_packed_bytes(cfg) == 896 * (17547264 + 1024)
+    assert k3.k3moe_packed_bytes(cfg) == 896 * (2 * 17547264 + 1024)
     tiny = k3_cfg(k3, d=256, f=128, n_experts=32, top_k=4, n_shared=1)
-    assert k3.k3moe_packed_bytes(tiny) == 32 * (52224 + 1024)
+    assert k3.k3moe_packed_bytes(tiny) == 32 * (2 * 52224 + 1024)
     w1 = k3.k3moe_workspace_bytes(cfg, 1)
     w64 = k3.k3moe_workspace_bytes(cfg, 64)
     assert 256 < w1 < w64

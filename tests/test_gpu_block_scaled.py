@@ -72,6 +72,42 @@ def run_both(k3, layer, xd, T):
     return outs[k3.PREFILL_GEMM_F16], outs[k3.PREFILL_GEMM_BLOCK_SCALED]
 
 
+def test_pack_writes_block_scaled_section(k3):
+    """The packed table's block-scaled section, which the block-scaled GEMM loads by
+    tensor map: the codes row-major exactly as the checkpoint holds them, and every scale
+    byte in its 512-byte block (rows 128 rb.., K groups of 128 kc..: row r's 4 bytes at
+    16 (r % 32) + 4 (r / 32)), byte 255 stored as 0."""
+    w = ki.Workload("mx_pack", T=1, d=384, f=256, E=3, k=1, S=0, exp_lo=-9, exp_hi=-1, seed=97)
+    cfg = k3.k3moe_config(**w.config_kwargs())
+    blk = ki.make_experts_block(w, 0, w.E)
+    blk["w1_scale"][1, 5, 3] = 255
+    blk["w2_scale"][2, 7, 1] = 0
+    blk["w3_scale"][0, 130, 11] = 255
+    table = torch.zeros(k3.k3moe_packed_bytes(cfg), dtype=torch.uint8, device="cuda")
+    k3.k3moe_pack_mxfp4(cfg, 0, w.E, *(dev(blk[n]) for n in ki.EXPERT_TENSORS), table)
+    torch.cuda.synchronize()
+    tb = host(table)
+    E, d, f = w.E, w.d, w.f
+    o = E * (w.expert_bytes + 1024)
+    for name, rows, cols in (("w1", f, d), ("w3", f, d), ("w2", d, f)):
+        n = E * rows * cols // 2
+        np.testing.assert_array_equal(tb[o:o + n].reshape(E, rows, cols // 2), blk[name + "_packed"])
+        o += n
+
+    def blocks(sc, rows, cols):
+        s = np.where(sc == 255, 0, sc).astype(np.uint8)
+        s = s.reshape(E, rows // 128, 4, 32, cols // 128, 4)         # e, rb, j, i, kc, kb (r = i + 32 j)
+        return s.transpose(0, 1, 4, 3, 2, 5).reshape(E, rows // 128, cols // 128, 512)
+    n = E * (f // 128) * (d // 128) * 1024
+    gu = tb[o:o + n].reshape(E, f // 128, d // 128, 2, 512)
+    np.testing.assert_array_equal(gu[:, :, :, 0], blocks(blk["w1_scale"], f, d))
+    np.testing.assert_array_equal(gu[:, :, :, 1], blocks(blk["w3_scale"], f, d))
+    o += n
+    n = E * (d // 128) * (f // 128) * 512
+    np.testing.assert_array_equal(tb[o:o + n].reshape(E, d // 128, f // 128, 512), blocks(blk["w2_scale"], d, f))
+    assert o + n == tb.size
+
+
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
 def test_block_scaled_gemm_parity(k3, w):
     from k3moe_inputs.device import build_layer

@@ -132,8 +132,9 @@ def test_pack_roundtrip_every_code_and_scale(k3):
         np.testing.assert_array_equal(host(d_out[n]), blk[n])
     rc, code = k3.k3moe_device_status(ws)
     assert rc == 0 and code & k3.DEV_NAN_SCALE      # byte 255 present: warning, not error
-    # the table is a pure relayout: same multiset of bytes
-    assert table.numel() == w.E * (w.expert_bytes + 1024)
+    # per expert: the tiles, the trailer, and the block-scaled section (the same codes and
+    # scales again, row-major and in scale blocks)
+    assert table.numel() == w.E * (2 * w.expert_bytes + 1024)
 
 
 def test_pack_records_block_scale_maxima(k3):
@@ -149,7 +150,7 @@ def test_pack_records_block_scale_maxima(k3):
     k3.k3moe_pack_mxfp4(cfg, 0, w.E, *(dev(blk[n]) for n in ki.EXPERT_TENSORS), table)
     torch.cuda.synchronize()
     tb = host(table)
-    trailer = tb[w.E * w.expert_bytes:].view(np.uint32).reshape(w.E, 256)
+    trailer = tb[w.E * w.expert_bytes:w.E * (w.expert_bytes + 1024)].view(np.uint32).reshape(w.E, 256)
     for e in range(w.E):
         col = 0
         for m in ("w1", "w3", "w2"):
@@ -178,7 +179,7 @@ def test_pack_roundtrip_full_shape(k3):
     torch.cuda.synchronize()
     for n in ki.EXPERT_TENSORS:
         np.testing.assert_array_equal(host(d_out[n]), blk[n])
-    assert k3.k3moe_packed_bytes(cfg) == 896 * (17547264 + 1024)
+    assert k3.k3moe_packed_bytes(cfg) == 896 * (2 * 17547264 + 1024)
 
 
 # ----------------------------------------------------------------------------- small layers, all outputs
