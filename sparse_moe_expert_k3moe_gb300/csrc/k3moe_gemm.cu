@@ -266,7 +266,9 @@ struct GemmArgs {
     const int32_t *abort;
     int32_t *status;
     int item_hi;                    // the kernel takes items [0, min(item_hi, all items))
-    const uint8_t *sfa;             // block-scaled GEMM: the token tiles' scale blocks
+    const uint8_t *sfa;             // block-scaled GEMMs: gate/up's token tiles' scale blocks
+    uint8_t *sfa_dn;                //   down's (h) token tiles' scale blocks
+    uint8_t *hq;                    //   routed h as two e4m3 planes [2][T*k][f] (in hp's routed rows)
 };
 
 struct GItem {
@@ -853,10 +855,12 @@ static_assert(kMxSmem + 8 * 1024 <= 232448, "shared memory per block (dynamic + 
 static_assert(kMxSfCol + 16 * kMxStg <= 512, "tensor-memory columns");
 
 struct MxItem {
-    int id, tok0, ntok, rb, n0, ncols, tile;
+    int id, tok0, ntok, rb, n0, ncols, tile, nw;
 };
-// Item i of the routed gate/up items: unit, 128-row block of f, token tile; tile numbers
-// count the 128-row token tiles of all units in unit order.
+// Item i of the routed items: unit, weight block (gate/up: a 128-row block of f, W1 and W3;
+// down: a pair of 128-row blocks of d, or the last single block), token tile.  Tile numbers
+// count the 128-row token tiles of all units in unit order (the same for both projections).
+template <int MODE>
 __device__ __forceinline__ MxItem mx_item(const GemmArgs &a, const int32_t *prefix, int n_units, int rbn, int i)
 {
     int lo = 0, hi = n_units;
@@ -877,27 +881,67 @@ __device__ __forceinline__ MxItem mx_item(const GemmArgs &a, const int32_t *pref
     it.n0 = nt * kBM;
     it.ncols = min(kBM, it.ntok - it.n0);
     it.tile = prefix[lo] / rbn + nt;
+    it.nw = (MODE == kGU || 2 * it.rb + 1 < a.d / kTileRows) ? kWRows : kWRows / 2;
     return it;
+}
+
+// 32 values of one row -> the two e4m3 planes' 32 bytes each and the two scale exponents:
+// the split gemm_gather_mx makes, for a block one thread holds.
+__device__ __forceinline__ void split32(float (&v)[32], uint4 (&hq)[2], uint4 (&lq)[2], int &sa, int &sl)
+{
+    float mx = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; j++) mx = fmaxf(mx, fabsf(v[j]));
+    sa = mx > 0.0f ? max(pow2_over448(mx), -127) : 0;
+    const float ia = __uint_as_float((uint32_t)(127 - sa) << 23);
+    uint32_t hw[8], lw[8];
+    float rmx = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; j++) {
+        const float a0 = v[2 * j] * ia, a1 = v[2 * j + 1] * ia;
+        const uint32_t h2 = e4m3x2_rn(a0, a1);
+        const float2 hf = e4m3x2_to_f32x2(h2);
+        v[2 * j] = a0 - hf.x;
+        v[2 * j + 1] = a1 - hf.y;
+        rmx = fmaxf(rmx, fmaxf(fabsf(v[2 * j]), fabsf(v[2 * j + 1])));
+        if (j & 1) hw[j >> 1] |= h2 << 16; else hw[j >> 1] = h2;
+    }
+    sl = rmx > 0.0f ? min(max(pow2_over448(rmx), max(-127, -127 - sa)), 127 - sa) : 0;
+    const float il = __uint_as_float((uint32_t)(127 - sl) << 23);
+#pragma unroll
+    for (int j = 0; j < 16; j++) {
+        const uint32_t l2 = e4m3x2_rn(v[2 * j] * il, v[2 * j + 1] * il);
+        if (j & 1) lw[j >> 1] |= l2 << 16; else lw[j >> 1] = l2;
+    }
+    hq[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    hq[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    lq[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    lq[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
 }
 
 // Roles (one block per SM):
 //   warp 0       producer, everything by TMA or bulk copy into the stage ring: the two
-//                token planes' tiles (128 columns x 128 rows), the tile's two token scale
-//                blocks, the W1 and W3 boxes (128 columns x 128 rows each) from the table's
-//                row-major codes with the packed-FP4 tensor-map type (each 16 codes land as
-//                8 bytes at the start of a 16-byte chunk: the MMA's e2m1 layout), and
-//                their two scale blocks; the L2 prefetch of the weight boxes kL2Ahead
-//                stages ahead;
+//                token planes' tiles (128 columns x 128 rows; gate/up: the gathered
+//                tokens, down: h), the tile's two token scale blocks, the item's two weight
+//                boxes (128 columns x 128 rows each: W1 and W3 of a block of f, or two W2
+//                blocks of d) from the table's row-major codes with the packed-FP4
+//                tensor-map type (each 16 codes land as 8 bytes at the start of a 16-byte
+//                chunk: the MMA's e2m1 layout), and their scale blocks; the L2 prefetch of
+//                the weight boxes kL2Ahead stages ahead;
 //   warp 1       MMA: tcgen05.cp of the four scale blocks into tensor memory, then per
-//                32-wide K step the hi and the lo MMA (M=128 tokens, N=256 weight rows);
-//                one accumulator of 256 columns;
-//   warps 2-17   epilogue: four warps per lane quadrant, 32 columns of g and of u each;
-//                the accumulator is read into registers and released before SiTU.
+//                32-wide K step the hi and the lo MMA (M=128 tokens, N=256 weight rows,
+//                or 128 for a last odd block of d); one accumulator of 256 columns;
+//   warps 2-17   epilogue, four warps per lane quadrant, 64 accumulator columns each
+//                (gate/up: 32 of g and the matching 32 of u); the accumulator is read into
+//                registers and released before the arithmetic.  Gate/up: h = SiTU(g, u),
+//                split into the down projection's two e4m3 planes and scale blocks; down:
+//                out[t] += w * y, float4 atomics.
+template <int MODE>
 __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_constant__ GemmArgs a, int item_lo,
                                                                 const __grid_constant__ CUtensorMap mhi,
                                                                 const __grid_constant__ CUtensorMap mlo,
-                                                                const __grid_constant__ CUtensorMap mw1,
-                                                                const __grid_constant__ CUtensorMap mw3)
+                                                                const __grid_constant__ CUtensorMap mw0,
+                                                                const __grid_constant__ CUtensorMap mw1)
 {
     pdl_wait();
     pdl_trigger();
@@ -913,7 +957,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
     const int n_items = a.prefix[n_units];
     if (item_lo + (int)blockIdx.x >= n_items) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nkc = a.d / kMxBK, rbn = a.f / kTileRows;
+    const int K = MODE == kGU ? a.d : a.f;
+    const int nkc = K / kMxBK;
+    const int rbn = MODE == kGU ? a.f / kTileRows : (a.d / kTileRows + 1) / 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMxStg; s++) { mb_init(&full[s], 1); mb_init(&empty[s], 1); }
@@ -939,11 +985,18 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
     };
     auto stop = [&]() -> bool { return __shfl_sync(0xffffffffu, bail, 0) != 0; };
     const int i0 = item_lo + (int)blockIdx.x;
-    // the scale blocks (W1, W3) of (item, K stage) in the table's block-scaled section
-    const uint8_t *sfgu = a.table + mx_sfgu_offset(a.E, a.d, a.f);
-    auto wsf = [&](const MxItem &it, int kc) -> const uint8_t * {
-        return sfgu + (((size_t)it.id * rbn + it.rb) * nkc + kc) * 1024;
+    // weight box mm of an item: its first row in the row-major codes (the tensor map mw0
+    // or mw1), and the scale block of (item, mm, K stage)
+    auto wrow = [&](const MxItem &it, int mm) -> int {
+        return MODE == kGU ? it.id * a.f + it.rb * kTileRows : it.id * a.d + (2 * it.rb + mm) * kTileRows;
     };
+    auto wsf = [&](const MxItem &it, int mm, int kc) -> const uint8_t * {
+        if (MODE == kGU)
+            return a.table + mx_sfgu_offset(a.E, a.d, a.f) + ((((size_t)it.id * rbn + it.rb) * nkc + kc) * 2 + mm) * 512;
+        return a.table + mx_sfdn_offset(a.E, a.d, a.f) +
+               (((size_t)it.id * (a.d / kTileRows) + 2 * it.rb + mm) * nkc + kc) * 512;
+    };
+    const uint8_t *sfa_in = MODE == kGU ? a.sfa : a.sfa_dn;
 
     if (warp == kMxWarpProd) {
         // ------------------------------------------------------------ everything by TMA
@@ -953,20 +1006,20 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
         MxItem pf{};
         auto pf_step = [&]() {
             if (pf_i >= n_items) return;
-            if (pf_kc == 0) pf = mx_item(a, s_prefix, n_units, rbn, pf_i);
-            const int wrow = pf.id * a.f + pf.rb * kTileRows;
-            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(&mw1),
-                         "r"(pf_kc * kMxBK), "r"(wrow) : "memory");
-            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(&mw3),
-                         "r"(pf_kc * kMxBK), "r"(wrow) : "memory");
+            if (pf_kc == 0) pf = mx_item<MODE>(a, s_prefix, n_units, rbn, pf_i);
+            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(&mw0),
+                         "r"(pf_kc * kMxBK), "r"(wrow(pf, 0)) : "memory");
+            if (pf.nw > kTileRows)
+                asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(&mw1),
+                             "r"(pf_kc * kMxBK), "r"(wrow(pf, 1)) : "memory");
             if (++pf_kc == nkc) { pf_kc = 0; pf_i += gridDim.x; }
         };
         if (lane == 0)
             for (int j = 0; j < kL2Ahead; j++) pf_step();
         for (int i = i0; i < n_items && !failed && !stop(); i += gridDim.x) {
-            const MxItem it = mx_item(a, s_prefix, n_units, rbn, i);
+            const MxItem it = mx_item<MODE>(a, s_prefix, n_units, rbn, i);
             const int row0 = it.tok0 + it.n0;
-            const int wrow = it.id * a.f + it.rb * kTileRows;
+            const bool two = it.nw > kTileRows;
             for (int kc = 0; kc < nkc; kc++, st++) {
                 if (st >= (uint32_t)kMxStg && !mb_wait_warp(&empty[st % kMxStg], ((st / kMxStg) - 1) & 1u)) {
                     timeout();
@@ -977,13 +1030,16 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
                     pf_step();
                     uint8_t *sb = sm + (st % kMxStg) * kMxStage;
                     uint64_t *fb = &full[st % kMxStg];
-                    mb_expect_tx(fb, 2u * kMxA + 2u * kMxWBox + 2048u);
+                    mb_expect_tx(fb, 2u * kMxA + 1024u + (two ? 2u : 1u) * (kMxWBox + 512u));
                     tma2d(sb, &mhi, kc * kMxBK, row0, fb);
                     tma2d(sb + kMxA, &mlo, kc * kMxBK, row0, fb);
-                    tma2d(sb + 2 * kMxA, &mw1, kc * kMxBK, wrow, fb);
-                    tma2d(sb + 2 * kMxA + kMxW / 2, &mw3, kc * kMxBK, wrow, fb);
-                    bulk_g2s(sb + 2 * kMxA + kMxW, a.sfa + ((size_t)it.tile * nkc + kc) * 1024, 1024u, fb);
-                    bulk_g2s(sb + 2 * kMxA + kMxW + 1024, wsf(it, kc), 1024u, fb);
+                    bulk_g2s(sb + 2 * kMxA + kMxW, sfa_in + ((size_t)it.tile * nkc + kc) * 1024, 1024u, fb);
+                    tma2d(sb + 2 * kMxA, &mw0, kc * kMxBK, wrow(it, 0), fb);
+                    bulk_g2s(sb + 2 * kMxA + kMxW + 1024, wsf(it, 0, kc), 512u, fb);
+                    if (two) {
+                        tma2d(sb + 2 * kMxA + kMxW / 2, &mw1, kc * kMxBK, wrow(it, 1), fb);
+                        bulk_g2s(sb + 2 * kMxA + kMxW + 1536, wsf(it, 1, kc), 512u, fb);
+                    }
                 }
                 __syncwarp();
             }
@@ -997,6 +1053,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
         uint32_t st = 0, n = 0;
         bool failed = false;
         for (int i = i0; i < n_items && !failed && !stop(); i += gridDim.x, n++) {
+            const int nw = MODE == kGU ? kWRows : mx_item<MODE>(a, s_prefix, n_units, rbn, i).nw;
             if (n >= 1 && !mb_wait_warp(&acc_empty, (n - 1) & 1u)) { timeout(); break; }
             tc_fence_after();
             for (int kc = 0; kc < nkc; kc++, st++) {
@@ -1012,13 +1069,13 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
                     const uint32_t sft = tmem + kMxSfCol + 16u * (st % kMxStg);
                     tc_cp_sf(sft, sdesc_sf(saddr(sf)));                // token hi
                     tc_cp_sf(sft + 4, sdesc_sf(saddr(sf + 512)));      // token lo
-                    tc_cp_sf(sft + 8, sdesc_sf(saddr(sf + 1024)));     // W1 rows (N 0..127)
-                    tc_cp_sf(sft + 12, sdesc_sf(saddr(sf + 1536)));    // W3 rows (N 128..255)
+                    tc_cp_sf(sft + 8, sdesc_sf(saddr(sf + 1024)));     // weight rows N 0..127
+                    if (nw > kTileRows) tc_cp_sf(sft + 12, sdesc_sf(saddr(sf + 1536)));   // N 128..255
                     const uint64_t dh = sdesc(saddr(sb)), dl = sdesc(saddr(sb + kMxA)),
                                    dw = sdesc(saddr(sb + 2 * kMxA));
 #pragma unroll
                     for (int kb = 0; kb < kMxBK / 32; kb++) {
-                        const uint32_t id = idesc_mx(kWRows, kb, kb);
+                        const uint32_t id = idesc_mx(nw, kb, kb);
                         umma_mx(tmem, dh + 2 * kb, dw + 2 * kb, id, sft, sft + 8, (kc | kb) != 0);
                         umma_mx(tmem, dl + 2 * kb, dw + 2 * kb, id, sft + 4, sft + 8, 1u);
                     }
@@ -1038,40 +1095,70 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                                 // TMEM lane quadrant
-        const int part = (warp - kMxWarpEpi0) >> 2;             // columns 32 part .. of g and of u
+        const int part = (warp - kMxWarpEpi0) >> 2;             // 0..3
         const int tr = 32 * q + lane;
+        const int nkc_dn = a.f / kMxBK;
         uint32_t n = 0;
         for (int i = i0; i < n_items && !stop(); i += gridDim.x, n++) {
-            const MxItem it = mx_item(a, s_prefix, n_units, rbn, i);
+            const MxItem it = mx_item<MODE>(a, s_prefix, n_units, rbn, i);
             const bool valid = tr < it.ncols;
+            const int p = it.tok0 + it.n0 + tr;                  // position (perm order) of the row
             if (!mb_wait_warp(&acc_full, n & 1u)) { timeout(); break; }
             tc_fence_after();
-            const uint32_t la = tmem + ((uint32_t)(32 * q) << 16) + 32u * part;
-            uint32_t g0[16], g1[16], u0[16], u1[16];
-            tmem_ld16_nowait(la, g0);
-            tmem_ld16_nowait(la + 16, g1);
-            tmem_ld16_nowait(la + kTileRows, u0);
-            tmem_ld16_nowait(la + kTileRows + 16, u1);
-            tmem_wait_ld();
+            const uint32_t lrow = tmem + ((uint32_t)(32 * q) << 16);
+            // gate/up: g columns 32 part.., u columns 128 + 32 part..; down: columns 64 part..
+            const uint32_t c0 = MODE == kGU ? 32u * part : 64u * part;
+            const uint32_t c1 = MODE == kGU ? kTileRows + 32u * part : 64u * part + 32u;
+            const bool on = MODE == kGU || (int)c0 < it.nw;
+            uint32_t r0[16], r1[16], r2[16], r3[16];
+            if (on) {
+                tmem_ld16_nowait(lrow + c0, r0);
+                tmem_ld16_nowait(lrow + c0 + 16, r1);
+                tmem_ld16_nowait(lrow + c1, r2);
+                tmem_ld16_nowait(lrow + c1 + 16, r3);
+                tmem_wait_ld();
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mb_arrive(&acc_empty);
-            uint32_t pk[16];
+            if (!on || !valid) continue;
+            if (MODE == kGU) {
+                float hv[32];
 #pragma unroll
-            for (int jj = 0; jj < 16; jj += 2) {
-                const __half2 h0 = __floats2half2_rn(situ(__uint_as_float(g0[jj]), __uint_as_float(u0[jj]), a.b1, a.b2),
-                                                     situ(__uint_as_float(g0[jj + 1]), __uint_as_float(u0[jj + 1]), a.b1, a.b2));
-                const __half2 h1 = __floats2half2_rn(situ(__uint_as_float(g1[jj]), __uint_as_float(u1[jj]), a.b1, a.b2),
-                                                     situ(__uint_as_float(g1[jj + 1]), __uint_as_float(u1[jj + 1]), a.b1, a.b2));
-                pk[jj / 2] = *reinterpret_cast<const uint32_t *>(&h0);
-                pk[8 + jj / 2] = *reinterpret_cast<const uint32_t *>(&h1);
-            }
-            if (valid) {
-                uint4 *dst = reinterpret_cast<uint4 *>(a.hp + (size_t)(it.tok0 + it.n0 + tr) * a.f +
-                                                       it.rb * kTileRows + 32 * part);
+                for (int jj = 0; jj < 16; jj++) {
+                    hv[jj] = situ(__uint_as_float(r0[jj]), __uint_as_float(r2[jj]), a.b1, a.b2);
+                    hv[16 + jj] = situ(__uint_as_float(r1[jj]), __uint_as_float(r3[jj]), a.b1, a.b2);
+                }
+                uint4 hq[2], lq[2];
+                int sa, sl;
+                split32(hv, hq, lq, sa, sl);
+                const size_t at = (size_t)p * a.f + it.rb * kTileRows + 32 * part;
+                uint4 *dh = reinterpret_cast<uint4 *>(a.hq + at);
+                uint4 *dl = reinterpret_cast<uint4 *>(a.hq + (size_t)a.T * a.k * a.f + at);
+                dh[0] = hq[0]; dh[1] = hq[1];
+                dl[0] = lq[0]; dl[1] = lq[1];
+                uint8_t *sf = a.sfa_dn + ((size_t)it.tile * nkc_dn + it.rb) * 1024 + 16 * (tr & 31) + 4 * (tr >> 5) + part;
+                sf[0] = (uint8_t)(sa + 127);
+                sf[512] = (uint8_t)(sa + sl + 127);
+            } else {
+                const int slot = dclamp(a.status, a.perm[p], 0, a.T * a.k - 1);
+                const float fw = a.weight[slot];
+                float *orow = a.out + (size_t)(slot / a.k) * a.d + 2 * it.rb * kTileRows + 64 * part;
 #pragma unroll
-                for (int c4 = 0; c4 < 4; c4++)
-                    dst[c4] = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+                for (int jj = 0; jj < 16; jj += 4) {
+                    atomicAdd(reinterpret_cast<float4 *>(orow + jj),
+                              make_float4(__uint_as_float(r0[jj]) * fw, __uint_as_float(r0[jj + 1]) * fw,
+                                          __uint_as_float(r0[jj + 2]) * fw, __uint_as_float(r0[jj + 3]) * fw));
+                    atomicAdd(reinterpret_cast<float4 *>(orow + 16 + jj),
+                              make_float4(__uint_as_float(r1[jj]) * fw, __uint_as_float(r1[jj + 1]) * fw,
+                                          __uint_as_float(r1[jj + 2]) * fw, __uint_as_float(r1[jj + 3]) * fw));
+                    atomicAdd(reinterpret_cast<float4 *>(orow + 32 + jj),
+                              make_float4(__uint_as_float(r2[jj]) * fw, __uint_as_float(r2[jj + 1]) * fw,
+                                          __uint_as_float(r2[jj + 2]) * fw, __uint_as_float(r2[jj + 3]) * fw));
+                    atomicAdd(reinterpret_cast<float4 *>(orow + 48 + jj),
+                              make_float4(__uint_as_float(r3[jj]) * fw, __uint_as_float(r3[jj + 1]) * fw,
+                                          __uint_as_float(r3[jj + 2]) * fw, __uint_as_float(r3[jj + 3]) * fw));
+                }
             }
         }
     }
@@ -1104,20 +1191,22 @@ cudaError_t launch_gemm(const GemmArgs &ga, const CUtensorMap &mbr, const CUtens
     return err;
 }
 
+template <int MODE>
 cudaError_t launch_gemm_mx(const GemmArgs &ga, int item_lo, const CUtensorMap &mhi, const CUtensorMap &mlo,
-                           const CUtensorMap &mw1, const CUtensorMap &mw3, int max_items, cudaStream_t s)
+                           const CUtensorMap &mw0, const CUtensorMap &mw1, int max_items, cudaStream_t s,
+                           const char *name)
 {
     static bool set = false;
     if (!set) {
-        cudaFuncSetAttribute(gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
+        cudaFuncSetAttribute(gemm_mx_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
         set = true;
     }
     const int grid = max(1, min(num_sms(), max_items));
-    timing_begin("gemm_gateup_mx", s);
+    timing_begin(name, s);
     const cudaError_t err =
-        launch_pdl(gemm_mx_kernel, dim3(grid), dim3(kMxThreads), kMxSmem, s, ga, item_lo, mhi, mlo, mw1, mw3);
+        launch_pdl(gemm_mx_kernel<MODE>, dim3(grid), dim3(kMxThreads), kMxSmem, s, ga, item_lo, mhi, mlo, mw0, mw1);
     count_launch();
-    timing_end("gemm_gateup_mx", s);
+    timing_end(name, s);
     return err;
 }
 
@@ -1192,7 +1281,7 @@ cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x,
 
     GemmArgs ga{T, c.d, c.f, k, S, E, c.situ_b1, c.situ_b2, units, prefix_gu, n_units, perm, weight,
                 tok_scale, table, expert_bytes(c.d, c.f), gateup_block_bytes(c.d, c.f), hp, out, abort, status,
-                INT_MAX, ws + L.sfa};
+                INT_MAX, ws + L.sfa, ws + L.sfa_dn, reinterpret_cast<uint8_t *>(hp)};
     // an upper bound on the items: every slot its own expert
     const int max_tiles = (int)std::min<long long>((long long)T * k + (long long)(E + S), (long long)1 << 30);
     if (!mx) {
@@ -1212,13 +1301,29 @@ cudaError_t launch_forward_gemm(const k3moe_config &c, int T, const uint16_t *x,
         if (!map4(&mw1, table + mx_w1_offset(E, c.d, c.f), (uint64_t)E * c.f, c.d) ||
             !map4(&mw3, table + mx_w3_offset(E, c.d, c.f), (uint64_t)E * c.f, c.d))
             return cudaErrorInvalidValue;
-        err = launch_gemm_mx(ga, shared_items, mhi, mlo, mw1, mw3, max_tiles * (c.f / kTileRows), s);
+        err = launch_gemm_mx<kGU>(ga, shared_items, mhi, mlo, mw1, mw3, max_tiles * (c.f / kTileRows), s,
+                                  "gemm_gateup_mx");
         if (err != cudaSuccess) return err;
     }
     GemmArgs gd = ga;
     gd.prefix = prefix_dn;
-    err = launch_gemm<kDN>(gd, mb_h, mb_h, ma2, ma2, max_tiles * ((c.d / kTileRows + 1) / 2), s, "gemm_down");
-    return err;
+    const int rb_dn = (c.d / kTileRows + 1) / 2;
+    if (!mx) return launch_gemm<kDN>(gd, mb_h, mb_h, ma2, ma2, max_tiles * rb_dn, s, "gemm_down");
+    // block-scaled: the shared experts' down items on the f16 kernel, the routed ones (h as
+    // the two e4m3 planes the gate/up epilogue wrote in hp's routed rows) on the block-scaled one
+    const int shared_dn = S * ((T + kBM - 1) / kBM) * rb_dn;
+    if (S > 0) {
+        GemmArgs gs = gd;
+        gs.item_hi = shared_dn;
+        err = launch_gemm<kDN>(gs, mb_h, mb_h, ma2, ma2, shared_dn, s, "gemm_down");
+        if (err != cudaSuccess) return err;
+    }
+    CUtensorMap mhh{}, mhl{}, mw2{};
+    uint8_t *hq = reinterpret_cast<uint8_t *>(hp);
+    if (!map8(&mhh, hq, (uint64_t)T * k, c.f, kBM) || !map8(&mhl, hq + (size_t)T * k * c.f, (uint64_t)T * k, c.f, kBM) ||
+        !map4(&mw2, table + mx_w2_offset(E, c.d, c.f), (uint64_t)E * c.d, c.f))
+        return cudaErrorInvalidValue;
+    return launch_gemm_mx<kDN>(gd, shared_dn, mhh, mhl, mw2, mw2, max_tiles * rb_dn, s, "gemm_down_mx");
 }
 
 }  // namespace k3moe

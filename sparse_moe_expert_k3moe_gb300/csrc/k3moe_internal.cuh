@@ -162,7 +162,8 @@ struct WsLayout {
     size_t gush;                 // decode: shared gate/up partials [parts][S][T][2][f] f32
     size_t xg;                   // prefill: routed activations in perm order [T*k][d] f16
     size_t units;                // prefill: unit list [E+S][4], item prefixes, unit count
-    size_t sfa;                  // prefill, block-scaled GEMM: token tiles' e8m0 scales [tiles][d/128][2][512]
+    size_t sfa;                  // prefill, block-scaled GEMMs: token tiles' e8m0 scales [tiles][d/128][2][512]
+    size_t sfa_dn;               //   and h's, the down projection's tokens [tiles][f/128][2][512]
     size_t total;
     bool gemm;                   // which forward path this T takes
     int n_chunks;
@@ -232,6 +233,7 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     L.xg = o; o = align256(o + (L.gemm ? slots * (size_t)c.d * 2 : 0));
     L.units = o; o = align256(o + (L.gemm ? (4 * (E + S) + 2 * (E + S + 1) + 1) * 4 : 0));
     L.sfa = o; o = align256(o + (L.gemm ? gemm_token_tiles(c, T) * (size_t)(c.d / 128) * 1024 : 0));
+    L.sfa_dn = o; o = align256(o + (L.gemm ? gemm_token_tiles(c, T) * (size_t)(c.f / 128) * 1024 : 0));
     L.total = o;
     return L;
 }

@@ -76,7 +76,7 @@ def test_sizes(k3):
     assert w1 < 1 * MiB
     assert k3.k3moe_workspace_bytes(cfg, 447) <= 211 * MiB
     assert k3.k3moe_workspace_bytes(cfg, 448) == k3.k3moe_workspace_bytes(cfg, 447)
-    assert k3.k3moe_workspace_bytes(cfg, 4096) <= 950 * MiB
+    assert k3.k3moe_workspace_bytes(cfg, 4096) <= 985 * MiB
 
 
 def test_prefill_gemm_switch(k3):
