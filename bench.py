@@ -143,7 +143,7 @@ def full_kernel_work(name: str, w, distinct_experts: int):
         return H * SI * 2 + T * SI * 2 + 2 * T * H * 4, 2 * T * H * SI
     if name in ("router_scores", "router_logits_tc", "router_wnorm"):
         return kernel_work(name, w.with_(d=H, hidden=0), distinct_experts)
-    if name in ("gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "gemm_gateup_mx"):
+    if name in ("gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "gemm_gateup_mx", "gemm_down_mx"):
         return kernel_work(name, w.with_(S=0, hidden=0), distinct_experts)
     return block_bytes_flops(w, distinct_experts)[0], 0
 
@@ -166,12 +166,19 @@ def kernel_work(name: str, w, distinct_experts: int, block_scaled: bool = False)
     h_gemv = slots * w.f * 2 + w.S * w.T * w.f * 4
     if name == "gemm_gateup_mx":
         # routed rows only: the packed W1, W3 (codes and scales as they are), the two e4m3
-        # token planes and their scale bytes in, h (f16) out
+        # token planes and their scale bytes in, h as two e4m3 planes and scale bytes out
         return (distinct_experts * 2 * w.f * w.d * 17 // 32 + slots * w.d * 2 + slots * w.d // 16
-                + slots * w.f * 2), 2 * slots * 2 * w.f * w.d
+                + slots * w.f * 2 + slots * w.f // 16), 2 * slots * 2 * w.f * w.d
+    if name == "gemm_down_mx":
+        # routed rows only: the packed W2, h's two planes and scale bytes in, the output
+        # (f32, accumulated in place) read and written once
+        return (distinct_experts * w.d * w.f * 17 // 32 + slots * w.f * 2 + slots * w.f // 16
+                + 2 * w.T * w.d * 4), 2 * slots * w.f * w.d
     if name == "gemm_gateup" and block_scaled:
-        # beside the block-scaled kernel, the f16 kernel runs the shared experts alone
+        # beside the block-scaled kernels, the f16 kernel runs the shared experts alone
         return (w.S * 2 * w.f * w.d * 2 + w.T * w.d * 2 + w.S * w.T * w.f * 2), 2 * w.S * w.T * 2 * w.f * w.d
+    if name == "gemm_down" and block_scaled:
+        return (w.S * w.d * w.f * 2 + w.S * w.T * w.f * 2 + 2 * w.T * w.d * 4), 2 * w.S * w.T * w.f * w.d
     if name == "router_scores":
         return w.E * w.d * 2 + w.T * w.d * 2 + 2 * w.T * w.E * 4, 2 * w.T * w.E * w.d
     if name == "router_logits_tc":
@@ -235,6 +242,7 @@ def peaks():
 KERNEL_SOURCES = {
     "gemv_gateup": ["k3moe_gemv.cu"], "gemv_down": ["k3moe_gemv.cu"],
     "gemm_gateup": ["k3moe_gemm.cu", "k3moe_tc.cuh"], "gemm_down": ["k3moe_gemm.cu", "k3moe_tc.cuh"],
+    "gemm_gateup_mx": ["k3moe_gemm.cu", "k3moe_tc.cuh"], "gemm_down_mx": ["k3moe_gemm.cu", "k3moe_tc.cuh"],
     "router_logits_tc": ["k3moe_route_tc.cu", "k3moe_tc.cuh"],
     "full_down_proj": ["k3moe_dense.cu", "k3moe_tc.cuh"], "full_up_proj": ["k3moe_dense.cu", "k3moe_tc.cuh"],
     "full_shared_gateup": ["k3moe_dense.cu", "k3moe_tc.cuh"], "full_shared_down": ["k3moe_dense.cu", "k3moe_tc.cuh"],
@@ -405,9 +413,9 @@ ARITHMETIC = ("router: exact logits (bf16 products exact in fp32, two-sum compen
               "accumulation, one rounding), sigmoid from a correctly rounded float exp (fp32 double-float arithmetic); experts: "
               "MMA operands f16 (tokens x*2^-u, routed h; MXFP4 weights decoded exactly to f16) "
               "and bf16 (shared-expert weights, shared h), fp32 accumulation; on the prefill path "
-              "the routed gate/up projection by default on block-scaled MMAs (kind::mxf8f6f4: the "
-              "E2M1 codes with their E8M0 scales as packed, the tokens as two e4m3 planes with "
-              "E8M0 scales per 32, fp32 accumulation); output f32")
+              "the routed experts' projections by default on block-scaled MMAs (kind::mxf8f6f4: the "
+              "E2M1 codes with their E8M0 scales as packed, the tokens and h as two e4m3 planes "
+              "with E8M0 scales per 32, fp32 accumulation); output f32")
 
 
 def near_tie_counts(layer, x, w):
@@ -519,7 +527,7 @@ def measure(w, args, rank, world, local, dev):
     # peak is the burst figure (the sustained one is for seconds-long loops).  The
     # block-scaled GEMM's MMAs (kind::mxf8f6f4: e4m3 x e2m1) take the FP8 peak: the measured
     # bf16 burst figure times the nominal FP8/BF16 ratio (4.5 / 2.25 PFLOP/s).
-    fp8 = top_name == "gemm_gateup_mx"
+    fp8 = top_name in ("gemm_gateup_mx", "gemm_down_mx")
     tpeak = bf16 * (2.0 if fp8 else 1.0)
     if alg_f / (tpeak * 1e12) > alg_b / (hbm * 1e9):
         roof = {"bound": "tensor", "achieved": alg_f / per_launch_s / 1e12, "peak": tpeak,
@@ -593,7 +601,7 @@ def measure(w, args, rank, world, local, dev):
                    "arithmetic": ARITHMETIC,
                    "l2": "512 MiB buffer written between timed steps",
                    "launch": "one CUDA graph replay per step" if args.graph else "eager",
-                   "prefill_gemm": ("block_scaled (routed gate/up on kind::mxf8f6f4)" if block_scaled
+                   "prefill_gemm": ("block_scaled (routed gate/up and down on kind::mxf8f6f4)" if block_scaled
                                     else ("f16 on dequantised weights" if "gemm_gateup" in kt
                                           else "not used (mat-vec path)")),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

@@ -189,12 +189,15 @@ k3moe_status k3moe_router_scores(const k3moe_config *cfg, int32_t T, const uint1
  *   sh_w1, sh_w3 [S][f][d] bf16;  sh_w2 [S][d][f] bf16 (NULL when S == 0);
  *                16-byte aligned
  *   out          [T][d] f32, written (not accumulated)
- * Precision: x enters the MMAs as f16 times a per-token power of two (exact for
- * every bf16 element within 2^31 of the token's largest), the MXFP4 weights
- * are decoded exactly, and every accumulation is fp32.  The SiTU output of a
- * routed expert is rounded to f16 before its down projection on both paths;
- * that of a shared expert is kept as a bf16 hi + lo pair for small T (the
- * streamed mat-vecs) and rounded to bf16 for the tensor-core path at large T.
+ * Precision: every accumulation is fp32 and the MXFP4 weights enter exactly
+ * (decoded, or as codes with their scales on the block-scaled MMAs).  On the
+ * streamed mat-vecs (small T) x enters as f16 times a per-token power of two
+ * (exact for every bf16 element within 2^31 of the token's largest), a routed
+ * expert's SiTU output is rounded to f16 before its down projection, and a shared
+ * expert's is kept as a bf16 hi + lo pair.  On the tensor-core path (large T) the
+ * routed experts take x and their SiTU output as the two e4m3 planes of
+ * k3moe_set_prefill_gemm's variant 2 (or f16, as above, with variant 1), and the
+ * shared experts' SiTU output is rounded to bf16.
  * ws per k3moe_workspace_bytes(T_max >= T). */
 k3moe_status k3moe_forward(const k3moe_config *cfg, int32_t T, const uint16_t *x,
                            const int32_t *idx, const float *weight,
@@ -321,24 +324,26 @@ k3moe_status k3moe_check_bounds(void *ws, int32_t index, int32_t limit, k3moe_st
 #define K3MOE_BUILD_DEBUG 0x1
 int32_t k3moe_build_flags(void);
 
-/* Which kernel runs the routed experts' gate/up projection on the prefill path
- * (the tensor-core path k3moe_forward takes for T >= 32 and T*top_k >= 8*E).  Both
- * compute g = W1 x, u = W3 x straight from the packed MXFP4 table (kimi-k3-in-c
+/* Which kernels run the routed experts' projections on the prefill path (the
+ * tensor-core path k3moe_forward takes for T >= 32 and T*top_k >= 8*E).  Both compute
+ * g = W1 x, u = W3 x and y = W2 h straight from the packed MXFP4 table (kimi-k3-in-c
  * README, Part II, section 4 "Reduction one: the experts already ship at half a
  * byte": an E2M1 code times the E8M0 scale of its 32-element group):
  *   1  f16 MMAs on weights dequantised into shared memory (code x 2^(scale - block
  *      maximum), exact in f16), the tokens as f16 x 2^-u;
  *   2  block-scaled MMAs (tcgen05 kind::mxf8f6f4): the E2M1 codes and their E8M0
- *      scales go to the tensor core as they are, and the tensor core applies the
- *      scales per 32 elements; the tokens as two e4m3 planes with their own E8M0
- *      scales per 32 elements, hi = rn(x / 2^sa) and lo = rn((x / 2^sa - hi) / 2^sl),
- *      so each 32-wide K step is two MMAs into the same fp32 accumulator.  The two
- *      planes hold a bf16 token exactly while its element lies within 2^12 of
- *      its 32-block's largest magnitude (smaller ones: absolute error below 2^-21 of
- *      that magnitude).  A scale byte of 255, which the format reads as zero, becomes
- *      2^-127 (a contribution below 2^-120 of the group's codes);
+ *      scales go to the tensor core as they are (from the table's row-major section,
+ *      k3moe_packed_bytes), and the tensor core applies the scales per 32 elements;
+ *      the tokens, and h for the down projection, as two e4m3 planes with their own
+ *      E8M0 scales per 32 elements, hi = rn(v / 2^sa) and lo = rn((v / 2^sa - hi) /
+ *      2^sl), so each 32-wide K step is two MMAs into the same fp32 accumulator.  The
+ *      two planes hold a bf16 token exactly while its element lies within 2^12 of its
+ *      32-block's largest magnitude (smaller ones: absolute error below 2^-21 of that
+ *      magnitude); h (fp32) keeps about 8 significant bits, as bf16 would.  A scale
+ *      byte of 255, which the format reads as zero, becomes 2^-127 (a contribution
+ *      below 2^-120 of the group's codes);
  *   0  the library's default, which is 2.
- * The shared experts (bf16) and the down projection run on the f16 kernel either way.
+ * The shared experts (bf16) run on the f16 kernels either way.
  * Process-wide; takes effect at the next k3moe_forward call (a captured graph keeps
  * the kernels it recorded).  K3MOE_EINVAL for another value.  The workspace
  * (k3moe_workspace_bytes) covers both. */
