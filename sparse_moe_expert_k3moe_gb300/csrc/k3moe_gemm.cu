@@ -93,6 +93,21 @@ __device__ __forceinline__ float situ(float g, float u, float b1, float b2)
     const float sg = __fdividef(1.0f, 1.0f + __expf(-fminf(fmaxf(g, -80.0f), 80.0f)));
     return b1 * tanh_fast(__fdividef(g, b1)) * sg * (b2 * tanh_fast(__fdividef(u, b2)));
 }
+// SiTU of the block-scaled GEMM's epilogue, whose h is split into two e4m3 terms (about
+// 8 significant bits, 2^-9 relative): the two caps by the hardware tanh approximation
+// (tanh.approx.f32, relative error about 2^-11), the sigmoid by the fast exponential and
+// reciprocal; ib1 = 1/b1, ib2 = 1/b2.
+__device__ __forceinline__ float tanh_approx(float x)
+{
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float situ_mx(float g, float u, float b1, float b2, float ib1, float ib2)
+{
+    const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
+    return b1 * tanh_approx(g * ib1) * sg * (b2 * tanh_approx(u * ib2));
+}
 // f16 of 2^e for e in [-24, 15] (subnormals below -14), 0 outside.
 __device__ __forceinline__ uint32_t f16_pow2(int e)
 {
@@ -1123,11 +1138,12 @@ __global__ void __launch_bounds__(kMxThreads, 1) gemm_mx_kernel(const __grid_con
             if (lane == 0) mb_arrive(&acc_empty);
             if (!on || !valid) continue;
             if (MODE == kGU) {
+                const float ib1 = 1.0f / a.b1, ib2 = 1.0f / a.b2;
                 float hv[32];
 #pragma unroll
                 for (int jj = 0; jj < 16; jj++) {
-                    hv[jj] = situ(__uint_as_float(r0[jj]), __uint_as_float(r2[jj]), a.b1, a.b2);
-                    hv[16 + jj] = situ(__uint_as_float(r1[jj]), __uint_as_float(r3[jj]), a.b1, a.b2);
+                    hv[jj] = situ_mx(__uint_as_float(r0[jj]), __uint_as_float(r2[jj]), a.b1, a.b2, ib1, ib2);
+                    hv[16 + jj] = situ_mx(__uint_as_float(r1[jj]), __uint_as_float(r3[jj]), a.b1, a.b2, ib1, ib2);
                 }
                 uint4 hq[2], lq[2];
                 int sa, sl;
