@@ -124,8 +124,12 @@ k3moe_status k3moe_workspace_bytes(const k3moe_config *cfg, int32_t T_max, size_
  *   w2_packed            [n_in][d][f/2]
  *   w2_scale             [n_in][d][f/32]
  * The *_packed pointers must be 16-byte aligned.  `table` (table_bytes >=
- * k3moe_packed_bytes) must be 256-byte aligned.  Scale bytes of 255 raise
- * K3MOE_DEV_NAN_SCALE in `ws` when ws is not NULL (ws as for k3moe_route). */
+ * k3moe_packed_bytes) must be 256-byte aligned.  Each expert is written twice:
+ * into the tiles the streamed mat-vecs and the f16 GEMM read, and into the
+ * block-scaled section (row-major codes, scales in 512-byte blocks) the default
+ * prefill GEMMs read; both are complete once the call's work has run.  Scale
+ * bytes of 255 raise K3MOE_DEV_NAN_SCALE in `ws` when ws is not NULL (ws as for
+ * k3moe_route). */
 k3moe_status k3moe_pack_mxfp4(const k3moe_config *cfg, int32_t expert_lo, int32_t n_in,
                               const uint8_t *w1_packed, const uint8_t *w1_scale,
                               const uint8_t *w3_packed, const uint8_t *w3_scale,
