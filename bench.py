@@ -543,6 +543,9 @@ def measure(w, args, rank, world, local, dev):
         roof = {"bound": "hbm", "achieved": alg_b / per_launch_s / 1e9, "peak": hbm, "unit": "GB/s",
                 "peak_kind": "HBM copy"}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    if alg_f:
+        # the algorithmic FLOPs at the bf16 dense burst peak, whatever the kernel's bound
+        roof["bf16_tensor_frac"] = alg_f / per_launch_s / 1e12 / bf16
     step_bytes, step_flops = layer_bytes_flops(w, distinct)
     step_s = ms / args.steps / 1000.0
     t_roof = max(step_bytes / (hbm * 1e9), step_flops / (bf16 * 1e12))
