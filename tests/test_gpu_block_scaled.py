@@ -124,6 +124,38 @@ def test_block_scaled_gemm_parity(k3, w):
     print(f"[{w.name}] block-scaled rel_l2={rel:.2e} max_rel={mxe:.2e} (f16 GEMM rel_l2={rel16:.2e})")
 
 
+def test_block_scaled_tile_edges(k3):
+    """Injected routing that puts experts exactly on the 128-token tile edges: 0, 1, 63, 64,
+    65, 127, 128, 129, 192 and 256 tokens, both kernels against the oracle (every row)."""
+    from k3moe_inputs.device import build_layer
+    w = ki.Workload("mx_edges", T=600, d=256, f=256, E=12, k=2, S=1, exp_lo=-8, exp_hi=-4, seed=98)
+    counts = [128, 129, 1, 0, 256, 127, 64, 65, 192, 63, 175, 0]
+    assert sum(counts) == w.T * w.k and max(counts) < w.T
+    # slot list sorted by expert; token t takes entries t and t + T (distinct: no count reaches T)
+    lst = np.repeat(np.arange(w.E, dtype=np.int32), counts)
+    idx = np.stack([lst[:w.T], lst[w.T:]], axis=1).astype(np.int32)
+    assert (idx[:, 0] != idx[:, 1]).all()
+    rng = np.random.default_rng(w.seed)
+    wt = rng.uniform(0.2, 1.0, size=idx.shape).astype(np.float32)
+    wt /= wt.sum(axis=1, keepdims=True)
+    off, perm = oracle.perm(idx, w.E)
+    assert list(np.diff(off)) == counts
+    layer = build_layer(w)
+    x = ki.make_x(w)
+    xd = dev16(x)
+    routing = (dev(idx), dev(wt), dev(off), dev(perm))
+    ref = oracle.forward(ocfg(w), x, idx, wt, oracle_experts(w, range(w.E)), ki.make_shared(w))
+    for v in (k3.PREFILL_GEMM_F16, k3.PREFILL_GEMM_BLOCK_SCALED):
+        k3.k3moe_set_prefill_gemm(v)
+        out = torch.empty((w.T, w.d), dtype=torch.float32, device="cuda")
+        layer.forward(xd, out, routing=routing)
+        rc, code = k3.k3moe_device_status(layer.ws)
+        assert rc == 0 and code == 0, (v, rc, code)
+        rel, mxe = assert_out_close(host(out), ref, f"tile edges, variant {v}")
+        print(f"[mx_edges variant {v}] rel_l2={rel:.2e} max_rel={mxe:.2e}")
+    k3.k3moe_set_prefill_gemm(k3.PREFILL_GEMM_DEFAULT)
+
+
 def test_block_scaled_repeats_bit_for_bit(k3):
     """Two calls on the same routing give the same output (the gate/up GEMM has no atomics;
     the down GEMM's fp32 atomics may reorder additions, so the comparison is at 1e-6)."""
