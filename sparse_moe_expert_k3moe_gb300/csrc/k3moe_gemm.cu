@@ -5,7 +5,10 @@
 // MMAs and its dequantised weight rows the 256-wide N side: an MMA instruction costs
 // about the same whatever its N, so only N = 256 runs at the tensor rate.
 //
-// Kernels, in launch order:
+// Two variants, chosen per call by k3moe_set_prefill_gemm.  The block-scaled one (the
+// default) is at the end of this file (gemm_gather_mx, gemm_mx_kernel); it runs the
+// shared experts on the f16 kernels below, restricted to their items.  The f16 variant,
+// in launch order:
 //   gemm_units   validates offsets, lists the units (shared experts first, heaviest,
 //                then the active routed experts) and the prefix of their work items;
 //   gemm_scales  per-token activation scale 2^-u (max |x_t| in [2^14, 2^15));
@@ -700,13 +703,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
 }
 
-// ---------------------------------------------------------------------------------- block-scaled GEMM
-// The routed experts' gate/up projection on kind::mxf8f6f4 MMAs: the weights stay in
-// their E2M1 codes and the tensor core applies their E8M0 scales; nothing is dequantised.
-// The tokens enter as two e4m3 planes with their own per-32 scales (gemm_gather_mx): a
-// 32-wide K step is two MMAs, hi and lo, into the same fp32 accumulator.  For a bf16 token
-// the two planes hold it exactly while its element lies within 2^12 of its 32-block's
-// largest; a smaller element keeps an absolute error below 2^-21 of that largest.
+// ---------------------------------------------------------------------------------- block-scaled GEMMs
+// The routed experts' gate/up and down projections on kind::mxf8f6f4 MMAs: the weights
+// stay in their E2M1 codes and the tensor core applies their E8M0 scales; nothing is
+// dequantised.  The tokens (gemm_gather_mx) and h (the gate/up epilogue) enter as two
+// e4m3 planes with their own per-32 scales: a 32-wide K step is two MMAs, hi and lo, into
+// the same fp32 accumulator.  For a bf16 token the two planes hold it exactly while its
+// element lies within 2^12 of its 32-block's largest; a smaller element keeps an absolute
+// error below 2^-21 of that largest.  h (fp32) keeps about 8 significant bits.
 
 // Two floats -> two e4m3 bytes (round to nearest even, saturating), x0 in the low byte.
 __device__ __forceinline__ uint32_t e4m3x2_rn(float x0, float x1)
