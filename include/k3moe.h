@@ -264,7 +264,8 @@ typedef struct k3moe_full_dims {
 /* Workspace bytes k3moe_full_forward needs for any 0 <= T <= T_max (the
  * layer's regions plus the block's z, a and shared intermediates, and the
  * projections' split-K partial sums: up to 1024 rows of the widest
- * projection). */
+ * projection, and as many again for the shared experts' projections, which
+ * run beside the others). */
 k3moe_status k3moe_full_workspace_bytes(const k3moe_config *cfg, const k3moe_full_dims *fd,
                                         int32_t T_max, size_t *bytes);
 
@@ -281,6 +282,14 @@ k3moe_status k3moe_full_workspace_bytes(const k3moe_config *cfg, const k3moe_ful
  * projections (Wd, Wu, the fused Sh1/Sh3 with SiTU, Sh2) run on the library's
  * tensor-core kernel with bf16 operands and fp32 accumulation, so z, the
  * normed a and the shared SiTU output are rounded to bf16 as their inputs.
+ * Step 6 needs only h: it runs beside steps 1-4 on a stream the library keeps
+ * per device, forked from `stream` where the call begins and joined back into
+ * it before step 5, which adds Wu a to the shared experts' out (the same sum,
+ * one rounding).  The side stream is created by the first call on a device
+ * that is not made during a stream capture (until then step 6 runs on
+ * `stream` after step 5); calls enqueue under one lock.  A call captured into
+ * a graph takes the side stream into the capture until that capture ends, so
+ * calls on one device that overlap a capture come from the capturing thread.
  * T may be 0 (offsets zeroed, nothing else written).  ws per
  * k3moe_full_workspace_bytes(T_max >= T); its status word as k3moe_route's. */
 k3moe_status k3moe_full_forward(const k3moe_config *cfg, const k3moe_full_dims *fd, int32_t T,

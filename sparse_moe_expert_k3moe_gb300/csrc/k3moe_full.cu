@@ -14,10 +14,14 @@
 // bf16 operands, fp32 accumulation; z, the normed aggregate and the shared SiTU output
 // are rounded to bf16 as they become the next projection's operand.  The norm is a
 // kernel here.
+// Step 6 reads only h, so it runs beside steps 1-4 on a side stream: forked from the
+// caller's stream where the call begins, it stores Sh2 SiTU(...) into out, and step 5,
+// after the join, adds Wu a to it (one rounding of the same two terms either way).
 #include <cuda_bf16.h>
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "k3moe_internal.cuh"
 
@@ -61,6 +65,44 @@ __global__ void __launch_bounds__(kNormThreads) latent_norm_kernel(int d, int no
     }
 }
 
+// One side stream per device with its fork and join events, created on first use outside
+// a stream capture (a call made while its stream is capturing, before the device has one,
+// runs step 6 on the caller's stream instead).  Calls enqueue under one lock, so two host
+// threads never interleave their fork and join.
+constexpr int kMaxSideDevices = 64;
+struct Side {
+    bool tried;
+    cudaStream_t s;
+    cudaEvent_t fork, join;
+};
+Side g_side[kMaxSideDevices];
+std::mutex g_side_mu;
+
+Side *side_stream(cudaStream_t caller)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return nullptr;
+    Side &sd = g_side[dev];
+    if (sd.s) return &sd;
+    if (sd.tried) return nullptr;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
+    sd.tried = true;
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+        if (f) cudaEventDestroy(f);
+        cudaStreamDestroy(st);
+        return nullptr;
+    }
+    sd.fork = f;
+    sd.join = j;
+    sd.s = st;
+    return &sd;
+}
+
 }  // namespace
 
 cudaError_t launch_full(const k3moe_config &c, int hidden, int latent_norm, float rms_eps, int T,
@@ -77,29 +119,59 @@ cudaError_t launch_full(const k3moe_config &c, int hidden, int latent_norm, floa
     float *part = reinterpret_cast<float *>(ws + F.part);
     int32_t *ctr = reinterpret_cast<int32_t *>(ws + F.ctr);
     int32_t *status = reinterpret_cast<int32_t *>(ws + F.route.status);
+    uint16_t *act = reinterpret_cast<uint16_t *>(ws + F.act);
+    std::lock_guard<std::mutex> lk(g_side_mu);
+    Side *sd = SI > 0 ? side_stream(s) : nullptr;
+    cudaError_t es = cudaSuccess;
+    if (sd) {
+        // 6. the shared experts on the original token, from where the caller's stream is,
+        // into out (stored; step 5 adds to it): their own partials and counters
+        float *part2 = reinterpret_cast<float *>(ws + F.part2);
+        int32_t *ctr2 = reinterpret_cast<int32_t *>(ws + F.ctr2);
+        es = cudaEventRecord(sd->fork, s);
+        if (es != cudaSuccess) return es;
+        es = cudaStreamWaitEvent(sd->s, sd->fork, 0);
+        if (es != cudaSuccess) return es;
+        es = launch_dense(kDenseSitu, T, SI, H, h, sh1, sh3, act, c.situ_b1, c.situ_b2, part2, ctr2, status, sd->s,
+                          "full_shared_gateup");
+        if (es == cudaSuccess)
+            es = launch_dense(kDenseF32, T, H, SI, act, sh2, nullptr, out, 0.0f, 0.0f, part2, ctr2, status, sd->s,
+                              "full_shared_down");
+        // joined back in every case, so a capture of the caller's stream stays whole
+        const cudaError_t ej = cudaEventRecord(sd->join, sd->s);
+        if (es == cudaSuccess) es = ej;
+    }
+    auto join = [&](cudaError_t e) -> cudaError_t {
+        if (sd) {
+            const cudaError_t ew = cudaStreamWaitEvent(s, sd->join, 0);
+            if (e == cudaSuccess) e = es != cudaSuccess ? es : ew;
+        }
+        return e;
+    };
     // 1. route on the full-width token
     cudaError_t e = launch_route(F.cr, T, h, wr, bias, idx, weight, offsets, perm, ws, F.route, s);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) return join(e);
     // 2. into the expert latent
     e = launch_dense(kDenseBf16, T, d, H, h, wd, nullptr, z, 0.0f, 0.0f, part, ctr, status, s, "full_down_proj");
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) return join(e);
     // 3. the chosen experts, summed with their weights
     e = launch_forward(F.cl, T, z, idx, weight, offsets, perm, table, nullptr, nullptr, nullptr, acc, ws,
                        F.latent, s, /*x_is_input=*/false);    // z is written just before
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) return join(e);
     // 4. RMSNorm of the aggregate
     timing_begin("latent_norm", s);
     e = launch_pdl(latent_norm_kernel, dim3(T), dim3(kNormThreads), 0, s, d, latent_norm, rms_eps,
                    (const float *)acc, gain, y);
     count_launch();
     timing_end("latent_norm", s);
+    if (e != cudaSuccess) return join(e);
+    // 5. back to full width: added to the shared experts' out after the join
+    e = join(cudaSuccess);
     if (e != cudaSuccess) return e;
-    // 5. back to full width
-    e = launch_dense(kDenseF32, T, H, d, y, wu, nullptr, out, 0.0f, 0.0f, part, ctr, status, s, "full_up_proj");
-    if (e != cudaSuccess) return e;
-    if (SI == 0) return cudaGetLastError();
-    // 6. the shared experts on the original token, added with weight one
-    uint16_t *act = reinterpret_cast<uint16_t *>(ws + F.act);
+    e = launch_dense(sd ? kDenseAddF32 : kDenseF32, T, H, d, y, wu, nullptr, out, 0.0f, 0.0f, part, ctr, status, s,
+                     "full_up_proj");
+    if (e != cudaSuccess || SI == 0 || sd) return e != cudaSuccess ? e : cudaGetLastError();
+    // 6. without a side stream: the shared experts after step 5, added with weight one
     e = launch_dense(kDenseSitu, T, SI, H, h, sh1, sh3, act, c.situ_b1, c.situ_b2, part, ctr, status, s,
                      "full_shared_gateup");
     if (e != cudaSuccess) return e;

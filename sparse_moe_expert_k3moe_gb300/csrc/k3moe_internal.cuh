@@ -138,16 +138,18 @@ inline bool use_gemm_path(const k3moe_config &c, int T)
 constexpr size_t kCtrShared = (size_t)kMaxShared * (kMaxWidth / kTileRows);  // shared gate/up K-part arrivals
 constexpr size_t kCtrReady = (size_t)kMaxExperts + kMaxShared;                // h rows ready, per unit
 // dense split-K arrivals: 128-row blocks of the widest projection (N <= S f) x 4 token
-// tiles (K is split only while T <= 512) x 4 quadrants
+// tiles (K is split only while T <= 512) x 4 quadrants; a second set for the projections
+// the full-width block runs on its side stream
 constexpr size_t kCtrDense = (size_t)kMaxShared * (kMaxWidth / 128) * 4 * 4;
 constexpr size_t kCtrOffset = 256;
-constexpr size_t kCtrBytes = ((kCtrShared + kCtrReady + kCtrDense) * 4 + 255) & ~(size_t)255;
+constexpr size_t kCtrBytes = ((kCtrShared + kCtrReady + 2 * kCtrDense) * 4 + 255) & ~(size_t)255;
 
 struct WsLayout {
     size_t status;
     size_t shctr;                // fixed counter block: shared gate/up arrival counters [S][f/128] int32
     size_t ready;                // fixed counter block: h-ready counters per unit [E + S] int32
     size_t dctr;                 // fixed counter block: dense split-K arrival counters
+    size_t dctr2;                // fixed counter block: the same for the full block's side stream
     size_t sc, ch;               // router scores [T][E] f32 (tensor-core router: sc holds its logits)
     size_t wnorm;                // router row norms |Wr[e]| [E] f32 (tensor-core router)
     size_t chunk_counts;         // [n_chunks][E] int32
@@ -214,6 +216,7 @@ inline WsLayout ws_layout(const k3moe_config &c, int T)
     L.shctr = kCtrOffset;
     L.ready = L.shctr + kCtrShared * 4;
     L.dctr = L.ready + kCtrReady * 4;
+    L.dctr2 = L.dctr + kCtrDense * 4;
     o = kCtrOffset + kCtrBytes;
     L.sc = o; o = align256(o + (size_t)T * E * 4);
     L.ch = o; o = align256(o + (size_t)T * E * 4);
@@ -268,6 +271,7 @@ struct FullLayout {
     size_t act;                  // [T][S*f] bf16: the shared experts' SiTU
     size_t part;                 // dense projections' K-part partial sums
     size_t ctr;                  // their arrival counters: the fixed counter block's
+    size_t part2, ctr2;          // the same for the shared experts' projections (side stream)
     size_t total;
 };
 
@@ -290,7 +294,12 @@ inline FullLayout full_layout(const k3moe_config &c, int hidden, int T)
     F.y = o; o = align256(o + td * 2);
     F.act = o; o = align256(o + ts * 2);
     F.part = o; o = align256(o + (T > 0 ? (size_t)kDensePartRows * wmax * 4 : 0));
+    // the shared experts' projections run beside the others (side stream): partials of
+    // their own, Sh1 + Sh3 (2 SI) or Sh2 (H) wide
+    const size_t wsh = SI > 0 ? std::max((size_t)hidden, 2 * SI) : 0;
+    F.part2 = o; o = align256(o + (T > 0 ? (size_t)kDensePartRows * wsh * 4 : 0));
     F.ctr = F.route.dctr;        // at the same fixed offset in the route and latent layouts
+    F.ctr2 = F.route.dctr2;
     F.total = o;
     return F;
 }
