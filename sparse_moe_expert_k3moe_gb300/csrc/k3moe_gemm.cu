@@ -130,14 +130,20 @@ struct UnitsArgs {
     int32_t *status, *abort;
 };
 
+// One block: validates offsets, lists the units (shared experts first, then the active
+// routed experts ascending) and their item prefixes.  A unit's items start after every
+// earlier unit's token tiles times the row blocks per tile, so the prefixes come from a
+// block scan of the tile counts, done in the same pass as the scan of the active flags.
 __global__ void __launch_bounds__(1024) gemm_units_kernel(UnitsArgs a)
 {
     pdl_wait();
     pdl_trigger();
-    __shared__ int32_t bad, scan_tmp[32], base;
+    __shared__ int32_t bad, scan_n[32], scan_t[32], base, tbase;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nwarps = (int)(blockDim.x >> 5);
     const int E = a.E, slots = a.T * a.k;
-    if (tid == 0) { bad = 0; base = a.S; }
+    const int ntS = (a.T + kBM - 1) / kBM;             // token tiles of a shared unit
+    if (tid == 0) { bad = 0; base = a.S; tbase = a.S * ntS; }
     __syncthreads();
     for (int e = tid; e < E; e += blockDim.x) {
         const int lo = a.offsets[e], hi = a.offsets[e + 1];
@@ -149,42 +155,50 @@ __global__ void __launch_bounds__(1024) gemm_units_kernel(UnitsArgs a)
     if (tid < a.S) {
         int32_t *u = a.units + 4 * tid;
         u[0] = 1; u[1] = tid; u[2] = 0; u[3] = a.T;
+        a.prefix_gu[tid] = tid * ntS * a.rb_gu;
+        a.prefix_dn[tid] = tid * ntS * a.rb_dn;
     }
-    // active routed experts after the shared units, ascending (block scan of flags)
+    // active routed experts after the shared units, ascending (block scans of the flags
+    // and of the token tiles)
     for (int b0 = 0; b0 < E; b0 += blockDim.x) {
         const int e = b0 + tid;
-        const int flag = (ok && e < E && a.offsets[e + 1] > a.offsets[e]) ? 1 : 0;
+        const int lo = ok && e < E ? a.offsets[e] : 0;
+        const int cnt = ok && e < E ? a.offsets[e + 1] - lo : 0;
+        const int flag = cnt > 0 ? 1 : 0;
+        const int nt = (cnt + kBM - 1) / kBM;
         const uint32_t bal = __ballot_sync(0xffffffffu, flag);
-        if (lane == 0) scan_tmp[warp] = __popc(bal);
+        int incl = nt;                                  // inclusive warp scan of the tiles
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) { scan_n[warp] = __popc(bal); scan_t[warp] = incl; }
         __syncthreads();
-        int before = base;
-        for (int w = 0; w < warp; w++) before += scan_tmp[w];
+        int before = base, tiles = tbase;
+        for (int w = 0; w < warp; w++) { before += scan_n[w]; tiles += scan_t[w]; }
         if (flag) {
-            int32_t *u = a.units + 4 * (before + __popc(bal & ((1u << lane) - 1u)));
-            u[0] = 0; u[1] = e; u[2] = a.offsets[e]; u[3] = a.offsets[e + 1] - a.offsets[e];
+            const int ui = before + __popc(bal & ((1u << lane) - 1u));
+            int32_t *u = a.units + 4 * ui;
+            u[0] = 0; u[1] = e; u[2] = lo; u[3] = cnt;
+            const int t0 = tiles + incl - nt;           // tiles of every earlier unit
+            a.prefix_gu[ui] = t0 * a.rb_gu;
+            a.prefix_dn[ui] = t0 * a.rb_dn;
         }
         __syncthreads();
         if (tid == 0) {
-            int tot = 0;
-            for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += scan_tmp[w];
+            int tot = 0, ttot = 0;
+            for (int w = 0; w < nwarps; w++) { tot += scan_n[w]; ttot += scan_t[w]; }
             base += tot;
+            tbase += ttot;
         }
         __syncthreads();
     }
-    // item prefix (one thread: at most E + S units)
     if (tid == 0) {
         const int n = base;
         *a.n_units = n;
-        int pg = 0, pd = 0;
-        for (int u = 0; u < n; u++) {
-            a.prefix_gu[u] = pg;
-            a.prefix_dn[u] = pd;
-            const int ntiles = (a.units[4 * u + 3] + kBM - 1) / kBM;
-            pg += ntiles * a.rb_gu;
-            pd += ntiles * a.rb_dn;
-        }
-        a.prefix_gu[n] = pg;
-        a.prefix_dn[n] = pd;
+        a.prefix_gu[n] = tbase * a.rb_gu;
+        a.prefix_dn[n] = tbase * a.rb_dn;
         if (bad) atomicOr(a.status, bad);
         *a.abort = bad ? 1 : 0;
     }
