@@ -194,11 +194,25 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
           "f"(c[2]), "f"(c[3]));
 }
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void *p)
+// Shared-memory operand reads at 32-bit shared addresses (the stage buffers' addresses are
+// taken once per stage; the per-fragment offsets are immediates).
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t a)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_addr(p)));
+                 : "r"(a));
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
 }
 
 __device__ __forceinline__ float situ(float g, float u, float b1, float b2)
@@ -617,42 +631,44 @@ __device__ __forceinline__ void issue_b_chunk(const GemvArgs &a, const Unit &un,
 // lanes 8j..8j+7 address matrix j (tokens 8nb..8nb+7; columns 16ks + 8j .. +7).  A chunk
 // holds `brows` token rows; the n-block's rows past them read the last row instead
 // (their results are never stored), so every address stays inside the chunk.
-__device__ __forceinline__ void ldb2(uint32_t (&r)[4], const uint8_t *b, int RS, int brows, int nb, int ks,
+__device__ __forceinline__ void ldb2(uint32_t (&r)[4], uint32_t b, int RS, int brows, int nb, int ks,
                                      int lane)
 {
     const int m = lane >> 3;
     const int row = min(8 * nb + (lane & 7), brows - 1);
-    ldmatrix_x4(r, b + row * RS + (16 * ks + 8 * m) * 2);
+    ldmatrix_x4(r, b + (uint32_t)(row * RS + (16 * ks + 8 * m) * 2));
 }
 
 template <int MODE, int NB, int TPS, bool EXACT>
-__device__ __forceinline__ void consume_stage(const uint8_t *buf0, int shared, int st, int RS, int brows,
-                                              const uint8_t *bhi, const uint8_t *blo,
-                                              float (&acc1)[kNBMax][4], float (&acc3)[kNBMax][4])
+__device__ __forceinline__ void consume_stage(uint32_t buf0, int shared, int st, int RS, int brows, uint32_t bhi,
+                                              uint32_t blo, int w, int lane, float (&acc1)[kNBMax][4],
+                                              float (&acc3)[kNBMax][4])
 {
-    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2;
+    const int g = lane >> 2;
     const float zero[4] = {0.f, 0.f, 0.f, 0.f};
     if (!shared) {
 #pragma unroll
       for (int tt = 0; tt < TPS; tt++) {
-        const uint8_t *buf = buf0 + tt * kTileBytes;
+        const uint32_t buf = buf0 + tt * kTileBytes;
         const int ks0 = (st * TPS + tt) * 8;                  // 8 k-steps per 128-column tile
         float f1[4], f1b[4], f3[4], f3b[4];
-        row_scales<EXACT>(*reinterpret_cast<const uint32_t *>(buf + kTileNibbleBytes + (16 * w + g) * 4), f1);
-        row_scales<EXACT>(*reinterpret_cast<const uint32_t *>(buf + kTileNibbleBytes + (16 * w + g + 8) * 4), f1b);
+        const uint32_t srow = buf + kTileNibbleBytes + (16 * w + g) * 4;
+        row_scales<EXACT>(lds32(srow), f1);
+        row_scales<EXACT>(lds32(srow + 32), f1b);
         if (MODE == kGateUp) {
-            row_scales<EXACT>(*reinterpret_cast<const uint32_t *>(buf + kTileBytes + kTileNibbleBytes + (16 * w + g) * 4), f3);
-            row_scales<EXACT>(*reinterpret_cast<const uint32_t *>(buf + kTileBytes + kTileNibbleBytes + (16 * w + g + 8) * 4), f3b);
+            row_scales<EXACT>(lds32(srow + kTileBytes), f3);
+            row_scales<EXACT>(lds32(srow + kTileBytes + 32), f3b);
         }
+        const uint32_t wrow = buf + w * 1024 + 8 * lane;      // this lane's fragment bytes
 #pragma unroll
         for (int c = 0; c < 4; c++) {
-            const uint2 wa = *reinterpret_cast<const uint2 *>(buf + (w * 4 + c) * 256 + 8 * lane);
+            const uint2 wa = lds64(wrow + c * 256);
             uint32_t A0[4], A1[4];
             e2m1x8_to_f16x2(wa.x, A0[0], A0[2], A1[0], A1[2]);
             e2m1x8_to_f16x2(wa.y, A0[1], A0[3], A1[1], A1[3]);
             uint32_t C0[4], C1[4];
             if (MODE == kGateUp) {
-                const uint2 wc = *reinterpret_cast<const uint2 *>(buf + kTileBytes + (w * 4 + c) * 256 + 8 * lane);
+                const uint2 wc = lds64(wrow + kTileBytes + c * 256);
                 e2m1x8_to_f16x2(wc.x, C0[0], C0[2], C1[0], C1[2]);
                 e2m1x8_to_f16x2(wc.y, C0[1], C0[3], C1[1], C1[3]);
             }
@@ -692,7 +708,7 @@ __device__ __forceinline__ void consume_stage(const uint8_t *buf0, int shared, i
 #pragma unroll
             for (int h = 0; h < 2; h++) {
                 const int q = 2 * (kk + h) + (lane >> 4);
-                ldmatrix_x4(A[h], buf0 + r * 128 + ((q ^ (r & 7)) << 4));
+                ldmatrix_x4(A[h], buf0 + (uint32_t)(r * 128 + ((q ^ (r & 7)) << 4)));
             }
 #pragma unroll
             for (int nb = 0; nb < NB; nb++) {
@@ -968,23 +984,24 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
             }
             const BHdr &h = bh[b];
             const PassTok &pt = pts[b];
-            const uint8_t *bhi = bbase + kHalves * b * bbytes, *blo = bbase + (kHalves * b + kHalves - 1) * bbytes;
+            const uint32_t bhi = smem_addr(bbase + kHalves * b * bbytes),
+                           blo = smem_addr(bbase + (kHalves * b + kHalves - 1) * bbytes);
             if (st == 0) {
 #pragma unroll
                 for (int nb = 0; nb < kNBMax; nb++)
 #pragma unroll
                     for (int i = 0; i < 4; i++) acc1[nb][i] = acc3[nb][i] = 0.0f;
             }
-            const uint8_t *buf = bufs + slot * kStageBytes;
+            const uint32_t buf = smem_addr(bufs + slot * kStageBytes);
             if (!h.shared && bflag[b][3] != 0) {
                 if ((STREAM ? h.nvalid & 0xFF : h.nvalid) > 8)
-                    consume_stage<MODE, 2, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, acc1, acc3);
+                    consume_stage<MODE, 2, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3);
                 else
-                    consume_stage<MODE, 1, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, acc1, acc3);
+                    consume_stage<MODE, 1, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3);
             } else if ((STREAM ? h.nvalid & 0xFF : h.nvalid) > 8) {
-                consume_stage<MODE, 2, TPS, false>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
+                consume_stage<MODE, 2, TPS, false>(buf, h.shared, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3);
             } else {
-                consume_stage<MODE, 1, TPS, false>(buf, h.shared, sic, RS, a.brows, bhi, blo, acc1, acc3);
+                consume_stage<MODE, 1, TPS, false>(buf, h.shared, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
