@@ -963,7 +963,9 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
         // ---------------- consumers: warp w owns rows 16w..16w+15 of every item
         const int g = lane >> 2, t4 = lane & 3;
         float acc1[kNBMax][4], acc3[kNBMax][4];
-        int cur_bu = -1, b = 0;
+        int cur_bu = -1, b = 0, var = 0;
+        uint32_t bhi = 0, blo = 0;
+        const uint32_t sbufs = smem_addr(bufs);
         for (int n = 0;; n++) {
             const int slot = n % kStages;
             if (!mbar_wait_warp(&full[slot], (uint32_t)(n / kStages) & 1u)) {
@@ -981,27 +983,31 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gemv_kernel(const __grid_con
                     break;
                 }
                 cur_bu = bun;
+                // once per chunk: its B operand addresses and the consume variant of its
+                // stages (bit 0: more than 8 tokens, two n-blocks; bit 1: a routed expert
+                // whose trailer flags a scale byte 0 or 255, the exact scale path; bit 2:
+                // bf16 shared-expert tiles)
+                bhi = smem_addr(bbase + kHalves * b * bbytes);
+                blo = smem_addr(bbase + (kHalves * b + kHalves - 1) * bbytes);
+                const int nv = STREAM ? bh[b].nvalid & 0xFF : bh[b].nvalid;
+                var = (nv > 8 ? 1 : 0) | (bh[b].shared ? 4 : (bflag[b][3] != 0 ? 2 : 0));
             }
             const BHdr &h = bh[b];
             const PassTok &pt = pts[b];
-            const uint32_t bhi = smem_addr(bbase + kHalves * b * bbytes),
-                           blo = smem_addr(bbase + (kHalves * b + kHalves - 1) * bbytes);
             if (st == 0) {
 #pragma unroll
                 for (int nb = 0; nb < kNBMax; nb++)
 #pragma unroll
                     for (int i = 0; i < 4; i++) acc1[nb][i] = acc3[nb][i] = 0.0f;
             }
-            const uint32_t buf = smem_addr(bufs + slot * kStageBytes);
-            if (!h.shared && bflag[b][3] != 0) {
-                if ((STREAM ? h.nvalid & 0xFF : h.nvalid) > 8)
-                    consume_stage<MODE, 2, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3);
-                else
-                    consume_stage<MODE, 1, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3);
-            } else if ((STREAM ? h.nvalid & 0xFF : h.nvalid) > 8) {
-                consume_stage<MODE, 2, TPS, false>(buf, h.shared, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3);
-            } else {
-                consume_stage<MODE, 1, TPS, false>(buf, h.shared, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3);
+            const uint32_t buf = sbufs + slot * kStageBytes;
+            switch (var) {
+            case 3: consume_stage<MODE, 2, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3); break;
+            case 2: consume_stage<MODE, 1, TPS, true>(buf, 0, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3); break;
+            case 5: consume_stage<MODE, 2, TPS, false>(buf, 1, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3); break;
+            case 4: consume_stage<MODE, 1, TPS, false>(buf, 1, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3); break;
+            case 1: consume_stage<MODE, 2, TPS, false>(buf, 0, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3); break;
+            default: consume_stage<MODE, 1, TPS, false>(buf, 0, sic, RS, a.brows, bhi, blo, w, lane, acc1, acc3); break;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
